@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Throughput of the Mamba-2 SSD chunked forward at the Mamba-2 2.7B layer shape.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path -- chunk cumsum, chunk states, state
+pass, fused output -- over one batch of the workload (b=8, T=4096, H=80, P=64,
+N=128, G=1, L=256, bf16; x is 335 MB, larger than L2, so nothing is flushed
+between steps).  Inputs are seeded synthetic tensors, resident in HBM before
+the timed region.  The four stages are launched through the C ABI's stage
+entry points with CUDA events between them on the launching stream, so the
+per-kernel times and the whole-step time come from the same timed region.
+
+Printed (one JSON line, rank 0): tokens/s (value), TFLOP/s, per-kernel times,
+the roofline of the dominant kernel, the whole-path roofline under the fixed
+four-stage byte model, an end-to-end figure through ssd_fwd with host buffers
+(H2D and D2H inside the timed region), SM clocks sampled during the timed
+region, and the fp64 oracle timed on the host cores on a bounded sample.
+
+--impl reference times the oracle (the reference arm of this method: a plain
+CPU fp64 recurrence) on the same workload, metric and unit.
+
+Multi-GPU (torchrun, N > 1): each rank runs its own batch of the workload
+(independent (b, h) problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd tokens/s & TFLOP/s at Mamba-2 2.7B shape; % of roofline on 1 GB300"
+KERNELS = ("chunk_cumsum", "chunk_state", "state_pass", "chunk_out")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="mamba2-2.7b",
+                    help="mamba2-2.7b (default), long-prefill, grouped-init")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload(name):
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+    return {"mamba2-2.7b": W.MAMBA2_2P7B, "long-prefill": W.LONG_PREFILL,
+            "grouped-init": W.GROUPED_INIT}[name]
+
+
+# ----------------------------------------------------------- algorithmic model ---
+def model(w):
+    """Algorithmic bytes and tensor FLOPs per launch of each stage, and the
+    whole-path figures (fixed four-stage byte model with fp32 states)."""
+    b, T, H, P, N, G, L = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
+    E = 2 if w.dtype == "bf16" else 4
+    nc = -(-T // L)
+    th = b * T * H                        # token-heads
+    st = b * nc * H * P * N               # per-chunk state elements
+    init = 1 if w.init_std > 0 else 0
+    k = {
+        "chunk_cumsum": dict(bytes=12 * th + 4 * H, flops=0),
+        "chunk_state": dict(bytes=th * (P * E + 8) + b * T * G * N * E + 4 * st,
+                            flops=2 * th * P * N),
+        "state_pass": dict(bytes=4 * st + E * st + 4 * b * H * P * N * (1 + init) + 4 * b * H * nc,
+                           flops=0),
+        "chunk_out": dict(bytes=th * (2 * P * E + 8) + 2 * b * T * G * N * E + E * st + 4 * H,
+                          flops=b * T * (H * (2 * P * N + P * (L + 1)) + G * N * (L + 1))),
+    }
+    graded = b * T * (H * (3 * P * E + 28 + 16 * P * N / L) + 3 * G * N * E) + \
+        4 * b * H * P * N * (1 + init)
+    flops = b * T * (H * (4 * P * N + P * (L + 1)) + G * N * (L + 1))
+    return k, graded, flops
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_from_profile(kernel, w):
+    """DRAM bytes per launch recorded by the committed ncu summary of this kernel
+    and workload, or None when absent or taken on a different kernel source."""
+    tag = w.name.split()[0]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    src = fields.get("source")
+    if not src or "traffic_bytes_per_launch" not in fields:
+        return None
+    spath = os.path.join(ROOT, src)
+    if not os.path.exists(spath) or hashlib.sha256(open(spath, "rb").read()).hexdigest()[:16] \
+            != fields.get("source_sha256_16"):
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
+# --------------------------------------------------------------------- clocks ---
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            self.t0 = time.time()
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin, t_end):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for i, line in enumerate(fh):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        # -lms 100: row i was taken about 0.1*i s after start; keep the rows of the
+        # timed region (with one sample of slack either side).
+        span = [r for i, r in enumerate(rows)
+                if t_begin - 0.15 <= self.t0 + 0.1 * i <= t_end + 0.15] or rows
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in span]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in span:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": num(span[0][2]),
+                "reasons": sorted(reasons), "samples": len(span),
+                "power_w_max": max(num(r[3]) for r in span)}
+
+
+# ------------------------------------------------------------------ CPU legs ---
+def oracle_sample(inp, w, npairs, nthreads=0):
+    """Time the fp64 recurrent oracle, as it stands, on `npairs` (b=0, h) pairs."""
+    import oracle
+    sl = {k: (v[:1] if v is not None and k in ("x", "dt", "B", "C", "initial_state") else v)
+          for k, v in inp.items()}
+    pairs = [(0, h % w.nheads) for h in range(npairs)]
+    t0 = time.perf_counter()
+    oracle.ssd_recurrent(**sl, ngroups=w.ngroups, pairs=pairs, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, w, budget_s=15.0):
+    import oracle
+    cores = oracle.max_threads()
+    t1 = oracle_sample(inp, w, cores)                  # one pair per thread: calibration
+    rounds = max(1, int(budget_s / max(t1, 1e-3)))
+    npairs = min(cores * rounds, 16 * w.nheads * w.batch)
+    t = oracle_sample(inp, w, npairs)
+    tokens = npairs * w.seqlen / w.nheads               # (b, h) pairs -> layer tokens
+    return {"value": tokens / t, "unit": "tokens/s", "cores": min(cores, npairs),
+            "kind": "oracle",
+            "sample": f"fp64 recurrent oracle on {npairs} (batch, head) pairs x {w.seqlen} tokens "
+                      f"of {w.name} ({npairs / w.nheads:.2f} layer-sequences), {t:.1f} s"}
+
+
+def run_reference(args, w):
+    import oracle
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+    inp = W.make_inputs(w.scaled(batch=1))
+    cores = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle_sample(inp, w, cores)
+    times = [oracle_sample(inp, w, cores) for _ in range(args.steps)]
+    t = sum(times)
+    tokens = args.steps * cores * w.seqlen / w.nheads
+    val = tokens / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: fp64 recurrent oracle on {cores} (batch, head) "
+                                   f"pairs x {w.seqlen} tokens of {w.name}"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, n):
+    return {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen, "nheads": w.nheads,
+            "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+            "chunk_size": w.chunk_size, "io_dtype": w.dtype,
+            "l2": "inputs larger than L2 (x alone is larger), no flush",
+            "parallelism": "replicas" if n == 1 else f"dp{n}: one batch per rank, no collective"}
+
+
+# ------------------------------------------------------------------- GPU leg ---
+def main():
+    args = parse_args()
+    w = workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    import torch
+    import mamba_ssd_chunked_02_gb300 as m2
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    inp_cpu = W.make_inputs(w.scaled(seed=w.seed + rank))
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
+    b, T, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    nc = sh.nchunks
+    f32 = dict(dtype=torch.float32, device="cuda")
+    cum2 = torch.empty((b, H, T), **f32)
+    dtT = torch.empty((b, H, T), **f32)
+    dS = torch.empty((b, nc, H, P, N), **f32)
+    Sprev = torch.empty((b, nc, H, P, N), dtype=w.torch_dtype, device="cuda")
+    y = torch.empty((b, T, H, P), dtype=w.torch_dtype, device="cuda")
+    fin = torch.empty((b, H, P, N), **f32)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        m2.chunk_cumsum(sh, dev["dt"], dev["A"], cum2, dtT, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        m2.state_pass(sh, dS, cum2, dev["initial_state"], Sprev, fin, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        m2.chunk_out(sh, dev["x"], dev["B"], dev["C"], cum2, dtT, Sprev, dev["D"], y, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if m2.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop(wall0, wall1)
+    if m2.device_error() != 0:
+        raise RuntimeError("device-side error in the timed region")
+
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / K
+    per = {k: 0.0 for k in KERNELS}
+    for i in range(K):
+        e = evs[i]
+        nxt = evs[i + 1][0] if i + 1 < K else t_end
+        marks = [e[0], e[1], e[2], e[3], nxt]
+        for j, kname in enumerate(KERNELS):
+            per[kname] += marks[j].elapsed_time(marks[j + 1])
+    per = {k: v / K for k, v in per.items()}
+
+    kmodel, graded_bytes, flops = model(w)
+    pk, pk_src = peaks()
+    tokens = w.tokens * world
+    value = tokens / (ms_step * 1e-3)
+
+    dom = max(per, key=per.get)
+    dm = kmodel[dom]
+    t_dom = per[dom] * 1e-3
+    hbm_time = dm["bytes"] / (pk["hbm_gbs"] * 1e9)
+    tc_time = dm["flops"] / (pk["bf16_tflops"] * 1e12) if dm["flops"] else 0.0
+    if hbm_time >= tc_time:
+        roof = {"bound": "hbm", "achieved": dm["bytes"] / t_dom / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": dm["flops"] / t_dom / 1e12,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = traffic_from_profile(dom, w)
+    roof.update({"traffic": tr, "kernel": dom, "algorithmic_bytes": dm["bytes"],
+                 "algorithmic_flops": dm["flops"], "ms": per[dom],
+                 "peak_source": f"{pk_src} (MEASURED_PEAKS.json)" if pk_src == "measured"
+                 else "fallback"})
+
+    t_path = max(graded_bytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    path_roof = {"model": "four-stage HBM hand-off, dS and Sprev counted at fp32",
+                 "graded_bytes": graded_bytes, "flops": flops, "roofline_ms": t_path * 1e3,
+                 "frac": t_path / (ms_step * 1e-3)}
+    kernels = {}
+    for kname in KERNELS:
+        km = kmodel[kname]
+        tk = per[kname] * 1e-3
+        kernels[kname] = {"ms": per[kname], "GB/s": km["bytes"] / tk / 1e9,
+                          "TFLOP/s": km["flops"] / tk / 1e12,
+                          "hbm_frac": km["bytes"] / tk / 1e9 / pk["hbm_gbs"]}
+
+    # End to end through ssd_fwd with pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inp_cpu.items()}
+        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        f_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        d2h = y_host.numel() * y_host.element_size() + f_host.numel() * f_host.element_size()
+
+        def e2e_step():
+            for k, v in host_in.items():
+                if v is not None:
+                    dev[k].copy_(v, non_blocking=True)
+            m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                       dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
+                       y=y, final_state=fin, workspace=ws)
+            y_host.copy_(y, non_blocking=True)
+            f_host.copy_(fin, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(1, args.e2e_steps)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        z.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(z)
+        if dist:
+            tt = torch.tensor([ems], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ems = float(tt.item())
+        e2e = {"value": tokens / (ems / ke * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke,
+               "ms_per_step": ems / ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp_cpu, w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_of(w, world),
+            "tflops": flops * world / (ms_step * 1e-3) / 1e12,
+            "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
+            "path": "tcgen05" if m2.path(sh) == m2.PATH_TCGEN05 else "simt",
+            "gpu_launches": 4 * K, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * mamba2_ssd.h -- C ABI of the GB300 (sm_103a) Mamba-2 SSD chunked forward pass.
+ *
+ * Pages cited (by title and section):
+ *   [P1] "NVIDIA、cuTileでMamba-2フォワードパスを高速化" (ai.newsbites.today),
+ *        "cuTileによるMamba-2フォワードパスの3段階カーネル設計" and the
+ *        optimisation table.
+ *   [P2] "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr),
+ *        "Mamba-2 아키텍처의 핵심 연산", "세 가지 핵심 커널 구현",
+ *        "cuTile 기반 성능 최적화 기법".
+ *   [P3] "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+ *        NVIDIA CUDA Tile" (brifing.si), sections 4, 5, 7, 8, 9, 11.
+ *
+ * The operation.  Per batch b and head h, with state S in R^{P x N} and
+ * a_t = dt[b,t,h] * A[h] (A[h] < 0):
+ *     S_t = exp(a_t) S_{t-1} + dt[b,t,h] x[b,t,h,:] B[b,t,g,:]^T
+ *     y[b,t,h,:] = S_t C[b,t,g,:] + D[h] x[b,t,h,:]
+ * S_{-1} = initial_state[b,h] (or 0), final_state[b,h] = S_{T-1}; head h reads
+ * group g = h / (H/G).  [P2 "핵심 연산"] prints the read-out
+ * y_t = c_t^T h_t + D x_t; the update is the standard Mamba-2 discretisation
+ * that the pages' log-space cumulative sum of a_t presumes.  It is evaluated
+ * chunk by chunk (chunk length L) in four steps [P2 "세 가지 핵심 커널 구현",
+ * P3 sections 4-9]: a log2-scaled chunk-local cumsum, per-chunk states by the
+ * jump formula, a sequential pass over chunks, and a fused three-term output.
+ *
+ * Conventions for every entry point.
+ *   - All tensors are dense, row-major, contiguous device memory, owned by the
+ *     caller.  The library allocates nothing and keeps no per-call host state;
+ *     it may be called concurrently from several host threads on different
+ *     streams with disjoint buffers.
+ *   - Every pointer must be 16-byte aligned (tensor-memory-accelerator copies).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronise.  Argument errors are detected on the host,
+ *     before any launch, and nothing is launched when a call fails.
+ *   - Outputs must not alias inputs or each other.
+ *   - `dtype` selects the element type of x, B, C, y (and of the Sprev
+ *     intermediate): MAMBA2_F32 (float) or MAMBA2_BF16 (__nv_bfloat16).
+ *     dt, A, D, initial_state, final_state and the other intermediates are
+ *     always float.
+ *
+ * Layouts (nc = ceil(T / L)):
+ *   x, y           [b, T, H, P]     dtype
+ *   dt             [b, T, H]        float, dt > 0 (taken as given: no softplus)
+ *   A              [H]              float, A < 0
+ *   B, C           [b, T, G, N]     dtype
+ *   D              [H]              float, or NULL (= 0)
+ *   initial_state  [b, H, P, N]     float, or NULL (= 0)
+ *   final_state    [b, H, P, N]     float
+ *   cum2, dtT      [b, H, T]        float (chunk-local cumsum * log2(e); dt transposed)
+ *   dS             [b, nc, H, P, N] float (state each chunk builds from zero)
+ *   Sprev          [b, nc, H, P, N] dtype (state entering each chunk)
+ */
+#ifndef MAMBA2_SSD_H
+#define MAMBA2_SSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(MAMBA2_SSD_BUILD) && defined(__GNUC__)
+#define MAMBA2_API __attribute__((visibility("default")))
+#else
+#define MAMBA2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mamba2_status {
+    MAMBA2_OK = 0,
+    MAMBA2_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad dimension       */
+    MAMBA2_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shape set      */
+    MAMBA2_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed           */
+    MAMBA2_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required        */
+    MAMBA2_ERR_DEVICE = 5         /* a kernel recorded a device-side error (timeout) */
+} mamba2_status;
+
+typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
+
+/* Force the CUDA-core (SIMT) chunk-state and chunk-output kernels even where
+ * the tcgen05 tensor-core kernels apply (cross-checks and debugging). */
+#define MAMBA2_FLAG_FORCE_SIMT 1
+
+/* Shape of one call.  Supported set:
+ *   batch, seqlen, nheads >= 0 (a zero batch or head count is a no-op; seqlen 0
+ *   writes final_state = initial_state, or 0);
+ *   headdim P in {16, 32, 64, 128}; dstate N in {16, 32, 64, 128, 256};
+ *   ngroups G >= 1 with nheads % G == 0; chunk_size L in {64, 128, 256};
+ *   seqlen need not be a multiple of L (the last chunk is shorter).
+ * The tensor-core path is used for dtype BF16 with L in {128, 256},
+ * P in {64, 128} and N in {64, 128, 256}; every other supported shape runs on
+ * the CUDA-core kernels (mamba2_ssd_path reports which). */
+typedef struct mamba2_ssd_shape {
+    int64_t batch;
+    int64_t seqlen;
+    int64_t nheads;
+    int64_t headdim;
+    int64_t dstate;
+    int64_t ngroups;
+    int64_t chunk_size;
+    int32_t dtype;   /* mamba2_dtype */
+    int32_t flags;   /* MAMBA2_FLAG_* */
+} mamba2_ssd_shape;
+
+/* Paths reported by mamba2_ssd_path. */
+#define MAMBA2_PATH_SIMT 0
+#define MAMBA2_PATH_TCGEN05 1
+
+/* Validate a shape without touching any pointer or the GPU. */
+MAMBA2_API mamba2_status mamba2_ssd_check_shape(const mamba2_ssd_shape* shape);
+
+/* Which kernels mamba2_ssd_fwd would launch for this shape (MAMBA2_PATH_*),
+ * or -1 for an invalid / unsupported shape.  Host-only. */
+MAMBA2_API int32_t mamba2_ssd_path(const mamba2_ssd_shape* shape);
+
+/* Bytes of workspace mamba2_ssd_fwd needs: cum2, dtT, dS and Sprev, each
+ * 256-byte aligned.  0 for an invalid shape.  Host-only. */
+MAMBA2_API size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape);
+
+/* The whole forward pass: the four stages below, in order, on `stream`.
+ *   workspace: device buffer of at least mamba2_ssd_workspace_size(shape)
+ *   bytes, 256-byte aligned, owned by the caller, contents ignored on entry.
+ * Returns MAMBA2_OK once the launches are queued. */
+MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape,
+                             const void* x, const float* dt, const float* A,
+                             const void* B, const void* C, const float* D,
+                             const float* initial_state,
+                             void* y, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 1, chunk_cumsum [P3 section 7; P2 "세 가지 핵심 커널 구현"]:
+ *   cum2[b,h,t] = log2(e) * sum_{r = chunk start of t}^{t} dt[b,r,h] * A[h]
+ *   dtT[b,h,t]  = dt[b,t,h]
+ * (inclusive, restarting at every chunk start; the [b,h,t] layout is the
+ * transposed layout of the optimisation table of [P1] / [P2 "성능 최적화"]). */
+MAMBA2_API mamba2_status mamba2_ssd_chunk_cumsum(const mamba2_ssd_shape* shape,
+                                      const float* dt, const float* A,
+                                      float* cum2, float* dtT, void* stream);
+
+/* Stage 2, chunk states by the jump formula [P3 sections 4, 8]:
+ *   dS[b,c,h,p,n] = sum_{s in chunk c} exp2(cum2_last(c) - cum2[s]) dtT[s] x[s,p] B[s,n]
+ * (tcgen05 tensor cores where the shape allows). */
+MAMBA2_API mamba2_status mamba2_ssd_chunk_state(const mamba2_ssd_shape* shape,
+                                     const void* x, const void* B,
+                                     const float* cum2, const float* dtT,
+                                     float* dS, void* stream);
+
+/* Stage 3, sequential pass over chunks [P2 "세 가지 핵심 커널 구현", fwd_pass_state]:
+ *   S = initial_state (or 0); for c: Sprev[c] = S; S = exp2(cum2_last(c)) S + dS[c];
+ *   final_state = S.
+ * Sprev is rounded to `dtype` (it is the tensor-core operand of stage 4). */
+MAMBA2_API mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape,
+                                    const float* dS, const float* cum2,
+                                    const float* initial_state,
+                                    void* Sprev, float* final_state, void* stream);
+
+/* Stage 4, fused output [P3 sections 9, 11; P2 "세 가지 핵심 커널 구현", compute_out]:
+ *   y[t,p] = sum_{s<=t in chunk} (C_t . B_s) exp2(cum2_t - cum2_s) dtT_s x[s,p]
+ *          + exp2(cum2_t) (Sprev[c] C_t)[p] + D[h] x[t,p]
+ * The causal mask is generated from indices and applied before exp2; the
+ * L x L interaction matrix never leaves the chip. */
+MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
+                                   const void* x, const void* B, const void* C,
+                                   const float* cum2, const float* dtT,
+                                   const void* Sprev, const float* D,
+                                   void* y, void* stream);
+
+/* Device-side error word.  The tensor-core kernels bound every wait; a wait
+ * that runs out sets a bit here and the kernel returns early (its outputs are
+ * then invalid).  This call synchronises the current device, reads the word
+ * into *code (0 = no error) and clears it when `clear` is nonzero.  Returns
+ * MAMBA2_ERR_DEVICE when the word was nonzero, MAMBA2_ERR_CUDA on a CUDA
+ * failure, MAMBA2_OK otherwise. */
+MAMBA2_API mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear);
+
+/* Static description of a status code. */
+MAMBA2_API const char* mamba2_status_string(mamba2_status status);
+
+/* Library version, e.g. "0.1.0". */
+MAMBA2_API const char* mamba2_ssd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA2_SSD_H */

@@ -1,1 +1,262 @@
-"""Mamba-2 SSD chunked forward pass on GB300 (sm_103a)."""
+"""Mamba-2 SSD chunked forward pass on GB300 (sm_103a).
+
+Thin ctypes binding of the C ABI in include/mamba2_ssd.h (library
+``_lib/libmamba2_ssd.so``, built by ``python -m mamba_ssd_chunked_02_gb300.build``).
+The binding only marshals arguments: every step of the computation runs in
+the library's CUDA kernels.  torch supplies device memory and streams.  There
+is no CPU path: calling any entry point without the built library or without a
+CUDA device raises.
+
+Entry points (same names as the C ABI, minus the ``mamba2_ssd_`` prefix):
+  ssd_fwd, chunk_cumsum, chunk_state, state_pass, chunk_out,
+  workspace_size, path, check_shape, device_error, version.
+
+Pages: "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr),
+"Mamba-2 아키텍처의 핵심 연산" (y_t = c_t^T h_t + D x_t) and "세 가지 핵심 커널
+구현" (chunk_cumsum / fwd_pass_state / compute_out); "Accelerating Mamba-2 with
+High-Performance Forward Pass Kernels in NVIDIA CUDA Tile" (brifing.si),
+sections 4-9.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmamba2_ssd.so")
+
+F32, BF16 = 0, 1
+FLAG_FORCE_SIMT = 1
+PATH_SIMT, PATH_TCGEN05 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = range(6)
+
+# Symbols the library exports (checked by the CPU test suite).
+SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_size",
+           "mamba2_ssd_fwd", "mamba2_ssd_chunk_cumsum", "mamba2_ssd_chunk_state",
+           "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
+           "mamba2_status_string", "mamba2_ssd_version")
+
+
+class Shape(ctypes.Structure):
+    """mirror of struct mamba2_ssd_shape"""
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int64), ("headdim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+    @property
+    def nchunks(self) -> int:
+        return (self.seqlen + self.chunk_size - 1) // self.chunk_size
+
+
+class Mamba2Error(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load():
+    """Load the C-ABI library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m mamba_ssd_chunked_02_gb300.build`"
+                " (there is no CPU fallback)")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, sp, i32 = ctypes.c_void_p, ctypes.POINTER(Shape), ctypes.c_int32
+        lib.mamba2_ssd_check_shape.argtypes = [sp]
+        lib.mamba2_ssd_check_shape.restype = ctypes.c_int
+        lib.mamba2_ssd_path.argtypes = [sp]
+        lib.mamba2_ssd_path.restype = i32
+        lib.mamba2_ssd_workspace_size.argtypes = [sp]
+        lib.mamba2_ssd_workspace_size.restype = ctypes.c_size_t
+        lib.mamba2_ssd_fwd.argtypes = [sp] + [vp] * 9 + [vp, ctypes.c_size_t, vp]
+        lib.mamba2_ssd_fwd.restype = ctypes.c_int
+        lib.mamba2_ssd_chunk_cumsum.argtypes = [sp, vp, vp, vp, vp, vp]
+        lib.mamba2_ssd_chunk_cumsum.restype = ctypes.c_int
+        lib.mamba2_ssd_chunk_state.argtypes = [sp, vp, vp, vp, vp, vp, vp]
+        lib.mamba2_ssd_chunk_state.restype = ctypes.c_int
+        lib.mamba2_ssd_state_pass.argtypes = [sp, vp, vp, vp, vp, vp, vp]
+        lib.mamba2_ssd_state_pass.restype = ctypes.c_int
+        lib.mamba2_ssd_chunk_out.argtypes = [sp] + [vp] * 8 + [vp]
+        lib.mamba2_ssd_chunk_out.restype = ctypes.c_int
+        lib.mamba2_ssd_device_error.argtypes = [ctypes.POINTER(i32), i32]
+        lib.mamba2_ssd_device_error.restype = ctypes.c_int
+        lib.mamba2_status_string.argtypes = [ctypes.c_int]
+        lib.mamba2_status_string.restype = ctypes.c_char_p
+        lib.mamba2_ssd_version.argtypes = []
+        lib.mamba2_ssd_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().mamba2_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return load().mamba2_ssd_version().decode()
+
+
+def make_shape(batch, seqlen, nheads, headdim, dstate, ngroups=1, chunk_size=256,
+               dtype=BF16, flags=0) -> Shape:
+    return Shape(int(batch), int(seqlen), int(nheads), int(headdim), int(dstate),
+                 int(ngroups), int(chunk_size), int(dtype), int(flags))
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float32:
+        return F32
+    raise TypeError(f"unsupported element type {t}: x, B, C must be bfloat16 or float32")
+
+
+def shape_of(x, B, chunk_size=256, ngroups=None, flags=0) -> Shape:
+    b, T, H, P = x.shape
+    G = B.shape[2] if ngroups is None else ngroups
+    return make_shape(b, T, H, P, B.shape[3], G, chunk_size, _dtype_code(x.dtype), flags)
+
+
+def check_shape(shape: Shape) -> int:
+    return int(load().mamba2_ssd_check_shape(ctypes.byref(shape)))
+
+
+def path(shape: Shape) -> int:
+    """PATH_TCGEN05 or PATH_SIMT for a valid shape, -1 otherwise."""
+    return int(load().mamba2_ssd_path(ctypes.byref(shape)))
+
+
+def workspace_size(shape: Shape) -> int:
+    return int(load().mamba2_ssd_workspace_size(ctypes.byref(shape)))
+
+
+def _ptr(t, name, dtype=None, shape=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _io_dtype(shape):
+    return torch.bfloat16 if shape.dtype == BF16 else torch.float32
+
+
+def _check(fn, rc):
+    if rc != OK:
+        raise Mamba2Error(fn, rc)
+
+
+def ssd_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=None, *,
+            y=None, final_state=None, workspace=None, stream=None, flags=0):
+    """Forward pass (mamba2_ssd_fwd).  Returns (y, final_state).
+
+    x [b,T,H,P] bf16|f32, dt [b,T,H] f32, A [H] f32, B/C [b,T,G,N] (x's dtype),
+    D [H] f32 or None, initial_state [b,H,P,N] f32 or None.  y, final_state and
+    workspace are allocated with torch when not given.
+    """
+    lib = load()
+    sh = shape_of(x, B, chunk_size, ngroups, flags)
+    b, T, H, P, N, G = sh.batch, sh.seqlen, sh.nheads, sh.headdim, sh.dstate, sh.ngroups
+    io = _io_dtype(sh)
+    if y is None:
+        y = torch.empty((b, T, H, P), dtype=io, device=x.device)
+    if final_state is None:
+        final_state = torch.empty((b, H, P, N), dtype=torch.float32, device=x.device)
+    need = workspace_size(sh)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    args = [
+        _ptr(x, "x", io, (b, T, H, P)), _ptr(dt, "dt", torch.float32, (b, T, H)),
+        _ptr(A, "A", torch.float32, (H,)), _ptr(B, "B", io, (b, T, G, N)),
+        _ptr(C, "C", io, (b, T, G, N)), _ptr(D, "D", torch.float32, (H,), optional=True),
+        _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
+        _ptr(y, "y", io, (b, T, H, P)), _ptr(final_state, "final_state", torch.float32, (b, H, P, N)),
+        _ptr(workspace, "workspace", optional=True),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
+        _stream(stream)]
+    _check("mamba2_ssd_fwd", lib.mamba2_ssd_fwd(ctypes.byref(sh), *args))
+    return y, final_state
+
+
+def chunk_cumsum(shape, dt, A, cum2, dtT, stream=None):
+    """Stage 1 (mamba2_ssd_chunk_cumsum): cum2, dtT [b,H,T] f32 outputs."""
+    b, T, H = shape.batch, shape.seqlen, shape.nheads
+    _check("mamba2_ssd_chunk_cumsum", load().mamba2_ssd_chunk_cumsum(
+        ctypes.byref(shape), _ptr(dt, "dt", torch.float32, (b, T, H)),
+        _ptr(A, "A", torch.float32, (H,)), _ptr(cum2, "cum2", torch.float32, (b, H, T)),
+        _ptr(dtT, "dtT", torch.float32, (b, H, T)), _stream(stream)))
+
+
+def chunk_state(shape, x, B, cum2, dtT, dS, stream=None):
+    """Stage 2 (mamba2_ssd_chunk_state): dS [b,nc,H,P,N] f32 output."""
+    b, T, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                        shape.ngroups)
+    io = _io_dtype(shape)
+    _check("mamba2_ssd_chunk_state", load().mamba2_ssd_chunk_state(
+        ctypes.byref(shape), _ptr(x, "x", io, (b, T, H, P)), _ptr(B, "B", io, (b, T, G, N)),
+        _ptr(cum2, "cum2", torch.float32, (b, H, T)), _ptr(dtT, "dtT", torch.float32, (b, H, T)),
+        _ptr(dS, "dS", torch.float32, (b, shape.nchunks, H, P, N)), _stream(stream)))
+
+
+def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
+    """Stage 3 (mamba2_ssd_state_pass): Sprev [b,nc,H,P,N] (I/O dtype), final_state f32."""
+    b, T, H, P, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate
+    nc = shape.nchunks
+    _check("mamba2_ssd_state_pass", load().mamba2_ssd_state_pass(
+        ctypes.byref(shape), _ptr(dS, "dS", torch.float32, (b, nc, H, P, N)),
+        _ptr(cum2, "cum2", torch.float32, (b, H, T)),
+        _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
+        _ptr(Sprev, "Sprev", _io_dtype(shape), (b, nc, H, P, N)),
+        _ptr(final_state, "final_state", torch.float32, (b, H, P, N)), _stream(stream)))
+
+
+def chunk_out(shape, x, B, C, cum2, dtT, Sprev, D, y, stream=None):
+    """Stage 4 (mamba2_ssd_chunk_out): y [b,T,H,P] output."""
+    b, T, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                        shape.ngroups)
+    io = _io_dtype(shape)
+    _check("mamba2_ssd_chunk_out", load().mamba2_ssd_chunk_out(
+        ctypes.byref(shape), _ptr(x, "x", io, (b, T, H, P)), _ptr(B, "B", io, (b, T, G, N)),
+        _ptr(C, "C", io, (b, T, G, N)), _ptr(cum2, "cum2", torch.float32, (b, H, T)),
+        _ptr(dtT, "dtT", torch.float32, (b, H, T)),
+        _ptr(Sprev, "Sprev", io, (b, shape.nchunks, H, P, N)),
+        _ptr(D, "D", torch.float32, (H,), optional=True), _ptr(y, "y", io, (b, T, H, P)),
+        _stream(stream)))
+
+
+def device_error(clear=True) -> int:
+    """Synchronise and return the library's device-side error word (0 = none)."""
+    code = ctypes.c_int32(0)
+    rc = load().mamba2_ssd_device_error(ctypes.byref(code), int(bool(clear)))
+    if rc not in (OK, ERR_DEVICE):
+        raise Mamba2Error("mamba2_ssd_device_error", rc)
+    return int(code.value)

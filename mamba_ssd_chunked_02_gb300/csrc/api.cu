@@ -1,0 +1,247 @@
+// api.cu -- the C ABI declared in include/mamba2_ssd.h: argument validation,
+// workspace carving and the launch sequence of the four stages.
+//
+// Pages: "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr),
+// "세 가지 핵심 커널 구현" (chunk_cumsum -> fwd_pass_state -> compute_out);
+// "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA
+// CUDA Tile" (brifing.si), section 6 "The Three Custom Kernels".  The pages'
+// state kernel is split here into a parallel chunk-state contraction (stage 2)
+// and a sequential pass over chunks (stage 3).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "mamba2_ssd.h"
+
+using m2::Dims;
+
+namespace {
+
+// Device-side error word (see mamba2_ssd_device_error).  Kernels receive its
+// device address; it is read back only on request.
+__device__ int32_t g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_sym_mu;
+int32_t* g_sym_addr[kMaxDevices] = {};
+
+int32_t* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_sym_mu);
+    if (!g_sym_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        g_sym_addr[dev] = static_cast<int32_t*>(p);
+    }
+    return g_sym_addr[dev];
+}
+
+bool in_set(int64_t v, std::initializer_list<int64_t> s) {
+    for (int64_t e : s)
+        if (v == e) return true;
+    return false;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mamba2_status check(const mamba2_ssd_shape* s) {
+    if (!s) return MAMBA2_ERR_INVALID_ARG;
+    if (s->batch < 0 || s->seqlen < 0 || s->nheads < 0) return MAMBA2_ERR_INVALID_ARG;
+    if (s->headdim <= 0 || s->dstate <= 0 || s->ngroups <= 0 || s->chunk_size <= 0)
+        return MAMBA2_ERR_INVALID_ARG;
+    if (s->dtype != MAMBA2_F32 && s->dtype != MAMBA2_BF16) return MAMBA2_ERR_INVALID_ARG;
+    if (s->flags & ~MAMBA2_FLAG_FORCE_SIMT) return MAMBA2_ERR_INVALID_ARG;
+    if (s->nheads % s->ngroups != 0) return MAMBA2_ERR_INVALID_ARG;
+    if (!in_set(s->headdim, {16, 32, 64, 128})) return MAMBA2_ERR_UNSUPPORTED;
+    if (!in_set(s->dstate, {16, 32, 64, 128, 256})) return MAMBA2_ERR_UNSUPPORTED;
+    if (!in_set(s->chunk_size, {64, 128, 256})) return MAMBA2_ERR_UNSUPPORTED;
+    // Launch-grid limits (grid y/z dimensions and 32-bit grid x products).
+    if (s->batch > 65535) return MAMBA2_ERR_UNSUPPORTED;
+    if (s->seqlen > (int64_t(1) << 31) || s->nheads > 65535) return MAMBA2_ERR_UNSUPPORTED;
+    const int64_t nc = (s->seqlen + s->chunk_size - 1) / s->chunk_size;
+    if (s->batch * nc * s->nheads >= (int64_t(1) << 31)) return MAMBA2_ERR_UNSUPPORTED;
+    return MAMBA2_OK;
+}
+
+Dims dims_of(const mamba2_ssd_shape* s) {
+    Dims d;
+    d.b = s->batch; d.T = s->seqlen; d.H = s->nheads; d.P = s->headdim; d.N = s->dstate;
+    d.G = s->ngroups; d.L = s->chunk_size; d.nc = (d.T + d.L - 1) / d.L;
+    d.dtype = s->dtype == MAMBA2_BF16 ? 1 : 0;
+    return d;
+}
+
+bool use_tc(const mamba2_ssd_shape* s, const Dims& d) {
+    return !(s->flags & MAMBA2_FLAG_FORCE_SIMT) && m2::tc_supported(d);
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Carve {
+    size_t cum2, dtT, dS, Sprev, total;
+};
+
+Carve carve(const Dims& d) {
+    Carve c;
+    c.cum2 = 0;
+    c.dtT = c.cum2 + align256(sizeof(float) * (size_t)m2::n_cum(d));
+    c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
+    c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
+    c.total = c.Sprev + align256((size_t)m2::esize(d) * (size_t)m2::n_state(d));
+    return c;
+}
+
+mamba2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MAMBA2_OK : MAMBA2_ERR_CUDA; }
+
+// A required pointer: non-null and 16-byte aligned, unless the tensor is empty.
+bool req(const void* p, bool empty) { return empty || (p && aligned16(p)); }
+// An optional pointer: null, or 16-byte aligned.
+bool opt(const void* p) { return !p || aligned16(p); }
+
+}  // namespace
+
+extern "C" {
+
+mamba2_status mamba2_ssd_check_shape(const mamba2_ssd_shape* shape) { return check(shape); }
+
+int32_t mamba2_ssd_path(const mamba2_ssd_shape* shape) {
+    if (check(shape) != MAMBA2_OK) return -1;
+    return use_tc(shape, dims_of(shape)) ? MAMBA2_PATH_TCGEN05 : MAMBA2_PATH_SIMT;
+}
+
+size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape) {
+    if (check(shape) != MAMBA2_OK) return 0;
+    return carve(dims_of(shape)).total;
+}
+
+mamba2_status mamba2_ssd_chunk_cumsum(const mamba2_ssd_shape* shape, const float* dt,
+                                      const float* A, float* cum2, float* dtT, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(dt, empty) || !req(A, empty) || !req(cum2, empty) || !req(dtT, empty))
+        return MAMBA2_ERR_INVALID_ARG;
+    return from_cuda(m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, error_word(),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+mamba2_status mamba2_ssd_chunk_state(const mamba2_ssd_shape* shape, const void* x, const void* B,
+                                     const float* cum2, const float* dtT, float* dS,
+                                     void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(x, empty) || !req(B, empty) || !req(cum2, empty) || !req(dtT, empty) ||
+        !req(dS, empty))
+        return MAMBA2_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc(shape, d) ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, error_word(), s)
+                                     : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, error_word(), s);
+    return from_cuda(e);
+}
+
+mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape, const float* dS,
+                                    const float* cum2, const float* initial_state, void* Sprev,
+                                    float* final_state, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(dS, empty) || !req(cum2, empty) || !opt(initial_state) || !req(Sprev, empty) ||
+        !req(final_state, d.b * d.H == 0))
+        return MAMBA2_ERR_INVALID_ARG;
+    return from_cuda(m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state,
+                                           error_word(), static_cast<cudaStream_t>(stream)));
+}
+
+mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape, const void* x, const void* B,
+                                   const void* C, const float* cum2, const float* dtT,
+                                   const void* Sprev, const float* D, void* y, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(x, empty) || !req(B, empty) || !req(C, empty) || !req(cum2, empty) ||
+        !req(dtT, empty) || !req(Sprev, empty) || !opt(D) || !req(y, empty))
+        return MAMBA2_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = use_tc(shape, d)
+                        ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, error_word(), s)
+                        : m2::launch_chunk_out_simt(d, x, B, C, cum2, dtT, Sprev, D, y, error_word(), s);
+    return from_cuda(e);
+}
+
+mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
+                             const float* A, const void* B, const void* C, const float* D,
+                             const float* initial_state, void* y, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(x, empty) || !req(dt, empty) || !req(A, empty) || !req(B, empty) ||
+        !req(C, empty) || !opt(D) || !opt(initial_state) || !req(y, empty) ||
+        !req(final_state, d.b * d.H == 0))
+        return MAMBA2_ERR_INVALID_ARG;
+    const Carve cv = carve(d);
+    if (d.b * d.H == 0) return MAMBA2_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t* err = error_word();
+    if (d.T == 0)   // final_state = initial_state (or 0); nothing else to write
+        return from_cuda(m2::launch_state_pass(d, nullptr, nullptr, initial_state, nullptr,
+                                               final_state, err, s));
+    if (!workspace || workspace_bytes < cv.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MAMBA2_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    float* cum2 = reinterpret_cast<float*>(ws + cv.cum2);
+    float* dtT = reinterpret_cast<float*>(ws + cv.dtT);
+    float* dS = reinterpret_cast<float*>(ws + cv.dS);
+    void* Sprev = ws + cv.Sprev;
+    const bool tc = use_tc(shape, d);
+
+    cudaError_t e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+    if (e == cudaSuccess)
+        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, err, s)
+               : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
+    if (e == cudaSuccess) e = m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state, err, s);
+    if (e == cudaSuccess)
+        e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s)
+               : m2::launch_chunk_out_simt(d, x, B, C, cum2, dtT, Sprev, D, y, err, s);
+    return from_cuda(e);
+}
+
+mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear) {
+    if (!code) return MAMBA2_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MAMBA2_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return MAMBA2_ERR_CUDA;
+    if (clear && v) {
+        const int32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
+            return MAMBA2_ERR_CUDA;
+    }
+    *code = v;
+    return v ? MAMBA2_ERR_DEVICE : MAMBA2_OK;
+}
+
+const char* mamba2_status_string(mamba2_status status) {
+    switch (status) {
+        case MAMBA2_OK: return "ok";
+        case MAMBA2_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer or bad dimension)";
+        case MAMBA2_ERR_UNSUPPORTED: return "unsupported shape (see mamba2_ssd_shape)";
+        case MAMBA2_ERR_CUDA: return "CUDA runtime error or launch failure";
+        case MAMBA2_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MAMBA2_ERR_DEVICE: return "a kernel recorded a device-side error";
+    }
+    return "unknown status";
+}
+
+const char* mamba2_ssd_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// k1_cumsum.cu -- stage 1: chunk-local decay cumsum in log2 space, [b,h,t] layout.
+//
+// Pages: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+// NVIDIA CUDA Tile" (brifing.si), section 7 "Optimizing chunk_cumsum Kernel":
+// per-token, per-head cumulative sums of the decay term, scaled by log2(e) so
+// that later stages use exp2.  "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널
+// 가속화" (devin.kr), "cuTile 기반 성능 최적화 기법": dt and the decay cumsum are
+// stored in a [batch, head, token] layout so that later loads are contiguous.
+//
+// cum2[b,h,t] = log2(e) * sum_{r = chunk start}^{t} dt[b,r,h] * A[h]   (inclusive)
+// dtT[b,h,t]  = dt[b,t,h]
+//
+// One CTA per (chunk, batch, block of 32 heads).  The [L x 32] dt tile is read
+// with coalesced 128-byte rows (32 heads of one token), transposed through
+// shared memory, scanned by one warp per head (each lane owns L/32 consecutive
+// tokens; lane totals are combined with a shuffle scan), and written back as
+// coalesced [h][t] rows.  HBM-bound: 12 bytes per (token, head).
+#include "common.cuh"
+#include "internal.h"
+
+namespace m2 {
+namespace {
+
+constexpr int kHB = 32;        // heads per CTA
+constexpr int kThreads = 256;  // 8 warps
+
+template <int L>
+__global__ void __launch_bounds__(kThreads)
+chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
+                    float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H) {
+    constexpr int E = L / 32;  // tokens per lane
+    __shared__ float tile[kHB][L + 1];
+    const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
+    const int64_t t0 = c * L;
+    const int nt = (int)min((int64_t)L, T - t0);
+    const int nh = (int)min((int64_t)kHB, H - h0);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Load [nt x nh] (token-major in HBM), transpose into tile[head][token].
+    for (int idx = threadIdx.x; idx < L * kHB; idx += kThreads) {
+        const int i = idx / kHB, j = idx % kHB;
+        float v = 0.f;
+        if (i < nt && j < nh) v = __ldg(dt + (b * T + t0 + i) * H + h0 + j);
+        tile[j][i] = v;
+    }
+    __syncthreads();
+
+    for (int j = warp; j < nh; j += kThreads / 32) {
+        const int64_t row = (b * H + h0 + j) * T + t0;
+        // dtT row: coalesced.
+        for (int i = lane; i < nt; i += 32) dtT[row + i] = tile[j][i];
+        __syncwarp();
+        const float a2 = __ldg(A + h0 + j) * kLog2e;
+        float s[E];
+        float run = 0.f;
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+            run += tile[j][lane * E + k] * a2;   // tokens past T hold 0
+            s[k] = run;
+        }
+        float tot = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, tot, o);
+            if (lane >= o) tot += n;
+        }
+        const float excl = tot - run;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < E; ++k) tile[j][lane * E + k] = s[k] + excl;
+        __syncwarp();
+        for (int i = lane; i < nt; i += 32) cum2[row + i] = tile[j][i];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, float* cum2,
+                                float* dtT, int32_t* /*err*/, cudaStream_t st) {
+    if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
+    const dim3 grid((unsigned)d.nc, (unsigned)d.b, (unsigned)((d.H + kHB - 1) / kHB));
+    switch (d.L) {
+        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
+        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
+        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace m2

@@ -1,0 +1,150 @@
+"""Host-side tests of the C ABI: no GPU needed, no kernel launched.
+
+The library must load on a machine without a GPU, export every entry point
+include/mamba2_ssd.h declares, and reject bad arguments on the host before any
+CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mamba_ssd_chunked_02_gb300 as m2
+from mamba_ssd_chunked_02_gb300 import build as m2build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    m2build.build()
+    return m2.load()
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"MAMBA2_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+    assert set(m2.SYMBOLS) <= set(names)
+
+
+def test_version_and_status_strings(lib):
+    assert re.match(r"\d+\.\d+\.\d+", m2.version())
+    for code in range(6):
+        assert m2.status_string(code) and "unknown" not in m2.status_string(code)
+    assert "unknown" in m2.status_string(99)
+
+
+def shp(**kw):
+    base = dict(batch=2, seqlen=512, nheads=8, headdim=64, dstate=128, ngroups=1,
+                chunk_size=256, dtype=m2.BF16, flags=0)
+    base.update(kw)
+    return m2.make_shape(**base)
+
+
+def test_check_shape(lib):
+    assert m2.check_shape(shp()) == m2.OK
+    assert m2.check_shape(shp(seqlen=300)) == m2.OK          # ragged last chunk
+    assert m2.check_shape(shp(seqlen=0)) == m2.OK
+    assert m2.check_shape(shp(batch=0)) == m2.OK
+    assert m2.check_shape(shp(nheads=6, ngroups=4)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(batch=-1)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(headdim=0)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(dtype=7)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(flags=8)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(headdim=48)) == m2.ERR_UNSUPPORTED
+    assert m2.check_shape(shp(dstate=96)) == m2.ERR_UNSUPPORTED
+    assert m2.check_shape(shp(chunk_size=32)) == m2.ERR_UNSUPPORTED
+    assert lib.mamba2_ssd_check_shape(None) == m2.ERR_INVALID_ARG
+
+
+def test_workspace_size(lib):
+    def a256(v):
+        return (v + 255) // 256 * 256
+    for kw in (dict(), dict(seqlen=300), dict(dtype=m2.F32, headdim=16, dstate=16, chunk_size=64)):
+        s = shp(**kw)
+        b, T, H, P, N, L = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.chunk_size
+        nc = -(-T // L)
+        es = 2 if s.dtype == m2.BF16 else 4
+        want = 2 * a256(4 * b * H * T) + a256(4 * b * nc * H * P * N) + a256(es * b * nc * H * P * N)
+        assert m2.workspace_size(s) == want
+    assert m2.workspace_size(shp(headdim=48)) == 0
+    # The 2.7B-layer workload: cum2 + dtT (2 x 10.5 MB), dS (335.5 MB fp32), Sprev (167.8 MB bf16).
+    s = shp(batch=8, seqlen=4096, nheads=80)
+    assert m2.workspace_size(s) == 2 * 10_485_760 + 335_544_320 + 167_772_160
+
+
+def test_path_selection(lib):
+    assert m2.path(shp(headdim=48)) == -1
+    assert m2.path(shp(dtype=m2.F32)) == m2.PATH_SIMT
+    assert m2.path(shp(chunk_size=64)) == m2.PATH_SIMT
+    assert m2.path(shp(headdim=32)) == m2.PATH_SIMT
+    assert m2.path(shp(flags=m2.FLAG_FORCE_SIMT)) == m2.PATH_SIMT
+
+
+def test_fwd_rejects_bad_pointers_without_launching(lib):
+    s = shp()
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)       # aligned, never dereferenced: validation fails first
+    bad = vp((1 << 20) + 8)  # misaligned
+    args = [good] * 9
+    # null x
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s), None, *args[1:], good, ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_INVALID_ARG
+    # misaligned B
+    a = list(args)
+    a[3] = bad
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s), *a, good, ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_INVALID_ARG
+    # misaligned optional D
+    a = list(args)
+    a[5] = bad
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s), *a, good, ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_INVALID_ARG
+    # invalid shape
+    s2 = shp(nheads=6, ngroups=4)
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s2), *args, good, ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_INVALID_ARG
+    # unsupported shape
+    s3 = shp(dstate=96)
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s3), *args, good, ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_UNSUPPORTED
+
+
+def test_stage_entry_points_validate(lib):
+    s = shp()
+    vp = ctypes.c_void_p
+    g = vp(1 << 20)
+    assert lib.mamba2_ssd_chunk_cumsum(ctypes.byref(s), None, g, g, g, None) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_chunk_state(ctypes.byref(s), g, g, g, g, None, None) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_state_pass(ctypes.byref(s), g, g, vp((1 << 20) + 4), g, g,
+                                     None) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_chunk_out(ctypes.byref(s), g, g, g, g, g, g, None, None,
+                                    None) == m2.ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_noop(lib):
+    # batch 0: nothing to do, no pointer needed, no CUDA call.
+    s = shp(batch=0)
+    assert m2.workspace_size(s) == 0
+    rc = lib.mamba2_ssd_fwd(ctypes.byref(s), *([None] * 9), None, ctypes.c_size_t(0), None)
+    assert rc == m2.OK
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 64, 2, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        m2.ssd_fwd(x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 16),
+                   torch.zeros(1, 64, 1, 16), chunk_size=64)

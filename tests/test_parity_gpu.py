@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Element-by-element comparisons at sizes the oracle finishes in seconds (several
+tiles, ragged tails, grouped heads, an initial state), stage by stage and end
+to end; full-size workloads in the benchmark's launch configuration on sampled
+(batch, head) pairs recomputed by the recurrent oracle; edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mamba_ssd_chunked_02_gb300 as m2
+import oracle
+from mamba_ssd_chunked_02_gb300 import workloads as W
+from parity import assert_close, metrics, run_fwd, sample_pairs, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba_ssd_chunked_02_gb300 import build
+    build.build()
+    m2.load()
+    m2.device_error(clear=True)
+
+
+def wl(b, T, H, P, N, G, L, dtype="bf16", init=0.0, seed=1, dt_lo=1e-3, dt_hi=1e-1):
+    return W.Workload(f"t b{b} T{T} H{H} P{P} N{N} G{G} L{L} {dtype}", b, T, H, P, N, G, L,
+                      dtype=dtype, dt_lo=dt_lo, dt_hi=dt_hi, init_std=init, seed=seed)
+
+
+SMALL = [
+    wl(1, 256, 2, 16, 16, 1, 64, dtype="f32", seed=1001),              # the tiny fp32 workload
+    wl(2, 512, 4, 64, 128, 1, 256, seed=11),                            # 2.7B head/state shape
+    wl(1, 700, 3, 64, 128, 1, 256, seed=12),                            # ragged tail, odd heads
+    wl(2, 384, 16, 64, 128, 8, 128, init=0.1, seed=13),                 # groups + initial state
+    wl(1, 1024, 2, 64, 64, 1, 256, seed=14),                            # N = 64
+    wl(1, 512, 2, 64, 256, 1, 256, seed=15),                            # N = 256
+    wl(1, 640, 2, 64, 128, 1, 256, seed=16, dt_lo=1e-4),                # wide decay range
+    wl(1, 300, 4, 128, 64, 2, 128, init=0.1, seed=17),                  # P = 128, ragged
+    wl(1, 200, 4, 32, 32, 2, 64, seed=18),                              # small P/N, bf16 SIMT
+    wl(2, 192, 3, 16, 16, 3, 64, dtype="f32", init=0.1, seed=19),       # fp32, G = H
+    wl(1, 100, 2, 64, 128, 1, 256, seed=20),                            # T < L
+    wl(1, 1, 2, 64, 128, 1, 128, seed=21),                              # a single token
+]
+
+
+def _ids(ws):
+    return [w.name[2:] for w in ws]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=_ids(SMALL))
+def test_fwd_matches_oracle(w):
+    inp = W.make_inputs(w)
+    y, f = run_fwd(inp, w)
+    ref = oracle.ssd_chunked(**inp, ngroups=w.ngroups, chunk_size=w.chunk_size)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
+    assert np.abs(ref["y"] - yr).max() <= 1e-9 * max(1.0, np.abs(yr).max())
+    assert_close(to_np(y), yr, w.dtype, f"y {w.name}")
+    assert_close(to_np(f), fr, w.dtype, f"final_state {w.name}")
+
+
+@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+def test_stages_match_oracle(w):
+    """Each stage against the oracle's chunked intermediates."""
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    b, T, H, P, N, nc = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, sh.nchunks
+    ref = oracle.ssd_chunked(**inp, ngroups=w.ngroups, chunk_size=w.chunk_size)
+    f32 = dict(dtype=torch.float32, device="cuda")
+
+    cum2 = torch.empty((b, H, T), **f32)
+    dtT = torch.empty((b, H, T), **f32)
+    m2.chunk_cumsum(sh, dev["dt"], dev["A"], cum2, dtT)
+    torch.cuda.synchronize()
+    rel, _ = metrics(to_np(cum2), ref["cum2"])
+    assert rel <= 1e-5, f"cum2 relL2 {rel:.3e}"
+    assert torch.equal(dtT.cpu(), inp["dt"].permute(0, 2, 1).contiguous())
+
+    dS = torch.empty((b, nc, H, P, N), **f32)
+    m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS)
+    torch.cuda.synchronize()
+    assert_close(to_np(dS), ref["dS"], w.dtype, "dS")
+
+    # Stage 3 from the oracle's dS (rounded to fp32), so it is checked on its own.
+    dS_ref = torch.from_numpy(ref["dS"]).float().cuda()
+    Sprev = torch.empty((b, nc, H, P, N), dtype=w.torch_dtype, device="cuda")
+    fin = torch.empty((b, H, P, N), **f32)
+    m2.state_pass(sh, dS_ref, cum2, dev["initial_state"], Sprev, fin)
+    torch.cuda.synchronize()
+    assert_close(to_np(Sprev), ref["Sprev"], w.dtype, "Sprev")
+    assert_close(to_np(fin), ref["final_state"], w.dtype, "final_state")
+
+    # Stage 4 from the oracle's Sprev (rounded to the I/O dtype).
+    Sp_ref = torch.from_numpy(ref["Sprev"]).to(w.torch_dtype).cuda()
+    y = torch.empty((b, T, H, P), dtype=w.torch_dtype, device="cuda")
+    m2.chunk_out(sh, dev["x"], dev["B"], dev["C"], cum2, dtT, Sp_ref, dev["D"], y)
+    torch.cuda.synchronize()
+    assert_close(to_np(y), ref["y"], w.dtype, "y")
+    assert m2.device_error() == 0
+
+
+@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+def test_tensor_core_path_matches_cuda_core_path(w):
+    inp = W.make_inputs(w)
+    y0, f0 = run_fwd(inp, w, flags=m2.FLAG_FORCE_SIMT)
+    y1, f1 = run_fwd(inp, w)
+    assert_close(to_np(y1), to_np(y0), w.dtype, "y tc vs simt")
+    assert_close(to_np(f1), to_np(f0), w.dtype, "final tc vs simt")
+
+
+def test_chunk_size_independence():
+    """The chunking is an evaluation order: L in {64, 128, 256} give the same result."""
+    w = wl(1, 1024, 4, 64, 128, 1, 256, seed=31)
+    inp = W.make_inputs(w)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=1)
+    for L in (64, 128, 256):
+        y, f = run_fwd(inp, w, chunk_size=L)
+        assert_close(to_np(y), yr, "bf16", f"y L={L}")
+        assert_close(to_np(f), fr, "bf16", f"final L={L}")
+
+
+def test_linear_attention_limit_on_gpu():
+    """A -> 0 (decay 1): the GPU matches causal linear attention (oracle, A = 0)."""
+    w = wl(1, 512, 2, 64, 128, 1, 128, seed=32)
+    inp = W.make_inputs(w)
+    inp["A"] = torch.zeros_like(inp["A"])
+    y, f = run_fwd(inp, w)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=1)
+    assert_close(to_np(y), yr, "bf16", "y A=0")
+    assert_close(to_np(f), fr, "bf16", "final A=0")
+
+
+def test_split_and_resume_on_gpu():
+    """Two halves, the second started from the first's final_state, equal one run."""
+    w = wl(2, 1024, 16, 64, 128, 8, 128, init=0.1, seed=33)
+    inp = W.make_inputs(w)
+    y, f = run_fwd(inp, w)
+    h1 = dict(inp)
+    h2 = dict(inp)
+    for k in ("x", "dt", "B", "C"):
+        h1[k] = inp[k][:, :512].contiguous()
+        h2[k] = inp[k][:, 512:].contiguous()
+    w2 = w.scaled(seqlen=512)
+    y1, f1 = run_fwd(h1, w2)
+    h2["initial_state"] = f1.cpu()
+    y2, f2 = run_fwd(h2, w2)
+    assert_close(to_np(torch.cat([y1, y2], dim=1)), to_np(y), "bf16", "split y")
+    assert_close(to_np(f2), to_np(f), "bf16", "split final")
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
+    assert_close(to_np(torch.cat([y1, y2], dim=1)), yr, "bf16", "split y vs oracle")
+
+
+def test_edge_cases():
+    # seqlen 0: final_state is the initial state (or zero), nothing else written.
+    w = wl(2, 0, 4, 64, 128, 1, 256, init=0.1, seed=34)
+    inp = W.make_inputs(w)
+    y, f = run_fwd(inp, w)
+    assert y.numel() == 0 and torch.equal(f.cpu(), inp["initial_state"])
+    w0 = wl(2, 0, 4, 64, 128, 1, 256, seed=34)
+    y, f = run_fwd(W.make_inputs(w0), w0)
+    assert torch.count_nonzero(f) == 0
+    # batch 0: a no-op.
+    wb = wl(0, 64, 4, 64, 128, 1, 64, seed=35)
+    y, f = run_fwd(W.make_inputs(wb), wb)
+    assert y.numel() == 0 and f.numel() == 0
+    # dt = 0 everywhere: y = S0 C + D x exactly up to rounding.
+    wd = wl(1, 300, 2, 64, 128, 1, 128, init=0.1, seed=36)
+    inp = W.make_inputs(wd)
+    inp["dt"] = torch.zeros_like(inp["dt"])
+    y, f = run_fwd(inp, wd)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=1)
+    assert_close(to_np(y), yr, "bf16", "dt=0")
+    assert torch.allclose(f.cpu(), inp["initial_state"], rtol=0, atol=0)
+
+
+def test_outputs_do_not_depend_on_workspace_contents():
+    w = wl(1, 512, 4, 64, 128, 1, 256, seed=37)
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    outs = []
+    for fill in (0, 255):
+        ws = torch.full((m2.workspace_size(sh),), fill, dtype=torch.uint8, device="cuda")
+        y, f = m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], None,
+                          chunk_size=w.chunk_size, workspace=ws)
+        outs.append((y.clone(), f.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_workspace_too_small_is_rejected():
+    w = wl(1, 256, 2, 64, 128, 1, 256, seed=38)
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    sh = m2.shape_of(dev["x"], dev["B"], 256, 1)
+    ws = torch.empty(m2.workspace_size(sh) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m2.Mamba2Error) as e:
+        m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], workspace=ws,
+                   chunk_size=256)
+    assert e.value.status == m2.ERR_WORKSPACE
+
+
+# --------------------------------------------------------------- full size -----------
+FULL = [W.MAMBA2_2P7B, W.GROUPED_INIT, W.LONG_PREFILL] + W.sweep_workloads()
+
+
+@pytest.mark.parametrize("w", FULL, ids=[w.name.split()[0] + "-" + "-".join(w.name.split()[1:3])
+                                         + f"-N{w.dstate}" for w in FULL])
+def test_full_size_sampled(w):
+    """Full-size workload in the benchmark's launch configuration; sampled
+    (batch, head) pairs recomputed by the recurrent oracle."""
+    inp = W.make_inputs(w)
+    if w.dtype == "bf16":
+        assert m2.path(m2.shape_of(inp["x"], inp["B"], w.chunk_size, w.ngroups)) in (
+            m2.PATH_TCGEN05, m2.PATH_SIMT)
+    y, f = run_fwd(inp, w)
+    k = 4 if w.seqlen >= 65536 else 8
+    pairs = sample_pairs(w.batch, w.nheads, k, seed=w.seed)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups, pairs=pairs)
+    yg, fg = to_np(y), to_np(f)
+    for (b, h) in pairs:
+        assert_close(yg[b, :, h], yr[b, :, h], w.dtype, f"y {w.name} (b={b}, h={h})")
+        assert_close(fg[b, h], fr[b, h], w.dtype, f"final {w.name} (b={b}, h={h})")
+    assert np.isfinite(yg).all() and np.isfinite(fg).all()
