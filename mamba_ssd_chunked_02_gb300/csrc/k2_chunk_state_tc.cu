@@ -1,0 +1,315 @@
+// k2_chunk_state_tc.cu -- stage 2 on tcgen05 tensor cores: chunk states by the
+// jump formula.
+//
+// Pages: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+// NVIDIA CUDA Tile" (brifing.si), section 4 "Mathematical Jump Formula
+// Implementation" (stacking a chunk's B and X turns the state update into one
+// matrix product) and section 5 "Handling Exponential Decay Terms" (rows are
+// pre-multiplied by their decay so that tensor cores still apply);
+// "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr), "세 가지 핵심
+// 커널 구현" (fwd_pass_state uses tensor-core MMA for the chunk states).
+//
+//   dS[b,c,h,p,n] = sum_{s in chunk c} B[s,n] * w_s * x[s,p],
+//   w_s = dtT[s] * exp2(cum2[last token of c] - cum2[s])
+//
+// As a GEMM per (b, c, h): D[n, p] = A[n, s] * X~[s, p] with M = n (a 128-wide
+// tile of the state dimension), N = P = 64, K = L (the chunk).
+//   * A = B_chunk^T straight from HBM: B is [s][n] with n contiguous, i.e. an
+//     MN-major operand; it is shared by every head of the group, so one CTA
+//     loads it once (TMA, 128-byte swizzle) and reuses it for `hpc` heads.
+//   * X~ = diag(w) X: x is [s][p] with p contiguous (MN-major); TMA brings the
+//     chunk into a stage buffer and four warps scale each 128-byte row s by w_s
+//     in place (a row of the swizzled tile is one s, so the swizzle does not
+//     matter), then hand it to the tensor core.  The decay is thus folded into
+//     the operand the kernel produces itself; the pages route that operand to
+//     tensor memory instead, to avoid shared-memory contention, which does not
+//     limit this HBM-bound kernel.
+//   * D accumulates in tensor memory (fp32), double buffered across heads; four
+//     warps read it back (tcgen05.ld) and store dS rows of 32 consecutive n
+//     (128-byte coalesced stores).
+// Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2-5 = scaling,
+// 6-9 = epilogue.  Stage ring of NS x-buffers; every wait is bounded.
+#include "common.cuh"
+#include "internal.h"
+#include "tc5.cuh"
+#include "tmap.h"
+
+namespace m2 {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 320;
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
+
+template <int L>
+struct K2Cfg {
+    static constexpr int P = 64;
+    static constexpr int NS = 3;                          // x stages
+    static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
+    static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
+    static constexpr int X_BYTES = ATOM;                  // P = 64: one block
+    static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES;
+    static constexpr int TMEM_COLS = 128;                 // 2 accumulators x 64 columns
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 1, 1);
+};
+
+struct K2Bars {
+    uint64_t bt_full;
+    uint64_t full[4], scaled[4], xfree[4];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t drain;         // commit target used to drain in-flight MMAs on abort
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int L>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
+                      const __grid_constant__ CUtensorMap tm_b,
+                      const float* __restrict__ cum2, const float* __restrict__ dtT,
+                      float* __restrict__ dS, int T, int H, int N, int G, int nc, int n_tiles,
+                      int hpc, int n_hblk, int32_t* err) {
+    using C = K2Cfg<L>;
+    constexpr int NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t* sBt = smem;
+    uint8_t* sX = smem + C::BT_BYTES;
+    __shared__ K2Bars bars;
+    volatile int* abort = &bars.abort;
+
+    // Work item: (b, c, n-tile) outer, head block inner (CTAs sharing B^T run together).
+    int rest = blockIdx.x;
+    const int hblk = rest % n_hblk; rest /= n_hblk;
+    const int nt = rest % n_tiles; rest /= n_tiles;
+    const int c = rest % nc;
+    const int b = rest / nc;
+    const int hpg = H / G;
+    const int h0 = hblk * hpc;
+    const int g = h0 / hpg;
+    const int nh = hpc;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars.bt_full, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bars.full[i], 1);
+            mbar_init(&bars.scaled[i], 128);
+            mbar_init(&bars.xfree[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.acc_full[i], 1);
+            mbar_init(&bars.acc_empty[i], 128);
+        }
+        mbar_init(&bars.drain, 1);
+        bars.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars.tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+            mbar_arrive_expect_tx(&bars.bt_full, C::BT_BYTES);
+            for (int a = 0; a < 2; ++a) {
+                // N = 64: both halves of the 128-row M tile hold n in [0, 64).
+                const int n_off = (N == 64) ? 0 : nt * 128 + 64 * a;
+                tma_load_3d(sBt + a * C::ATOM, &tm_b, &bars.bt_full, g * N + n_off, c * L, b);
+            }
+            int issued = 0;
+            for (int i = 0; i < nh; ++i) {
+                const int st = i % NS, k = i / NS;
+                if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
+                mbar_arrive_expect_tx(&bars.full[st], C::X_BYTES);
+                tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], (h0 + i) * C::P, c * L, b);
+                issued = i + 1;
+            }
+            if (*abort) {
+                // Let every copy already issued land before the CTA can exit.
+                mbar_wait(&bars.bt_full, 0, kWaitNs);
+                for (int i = issued - 1; i >= 0 && i >= issued - NS; --i)
+                    mbar_wait(&bars.full[i % NS], (i / NS) & 1, kWaitNs);
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            int last = -1;
+            if (mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs)) {
+                const uint32_t bt_addr = smem_u32(sBt);
+                for (int i = 0; i < nh; ++i) {
+                    const int st = i % NS, k = i / NS, ab = i & 1, ka = i >> 1;
+                    if (!mbar_wait_or_abort(&bars.scaled[st], k & 1, abort, kWaitNs)) break;
+                    if (!mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs)) break;
+                    tc_fence_after();
+                    const uint32_t x_addr = smem_u32(sX + st * C::X_BYTES);
+                    const uint32_t d = tmem + ab * C::P;
+#pragma unroll
+                    for (int kk = 0; kk < L / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(bt_addr + kk * 2048, C::ATOM, 1024);
+                        const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::ATOM, 1024);
+                        mma_ss(d, ad, bd, C::IDESC, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars.acc_full[ab]);
+                    mma_commit(&bars.xfree[st]);
+                    last = i;
+                }
+            }
+            if (last >= 0 && *abort) {   // nothing may be in flight when TMEM is freed
+                mma_commit(&bars.drain);
+                mbar_wait(&bars.drain, 0, kWaitNs);
+            }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------- scaling
+        const int idx = threadIdx.x - 64;                // 0..127
+        const int Lc = min(L, T - c * L);
+        for (int i = 0; i < nh; ++i) {
+            const int st = i % NS, k = i / NS;
+            const int64_t bh = (int64_t)b * H + h0 + i;
+            const float* crow = cum2 + bh * T + (int64_t)c * L;
+            const float* drow = dtT + bh * T + (int64_t)c * L;
+            const float last = __ldg(crow + Lc - 1);
+            float w[L / 128];
+#pragma unroll
+            for (int r = 0; r < L / 128; ++r) {
+                const int s = idx + 128 * r;
+                w[r] = s < Lc ? __ldg(drow + s) * ex2(last - __ldg(crow + s)) : 0.f;
+            }
+            const bool ok = __all_sync(0xffffffffu,
+                                       mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
+            if (!ok) break;
+            uint8_t* xs = sX + st * C::X_BYTES;
+#pragma unroll
+            for (int r = 0; r < L / 128; ++r) {
+                const int s = idx + 128 * r;
+                uint4* row = reinterpret_cast<uint4*>(xs + s * 128);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint4 v = row[q];
+                    uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(u[e] << 16) * w[r];
+                        const float hi = __uint_as_float(u[e] & 0xffff0000u) * w[r];
+                        u[e] = pack_bf16x2(lo, hi);
+                    }
+                    row[q] = v;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars.scaled[st]);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                          // TMEM lane quadrant
+        const int n = (N == 64 ? 0 : nt * 128) + 32 * q + lane;
+        const bool valid = n < N && (N != 64 || q < 2);
+        for (int i = 0; i < nh; ++i) {
+            const int ab = i & 1, ka = i >> 1;
+            const bool ok = __all_sync(0xffffffffu,
+                                       mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
+            if (!ok) break;
+            tc_fence_after();
+            float* out = dS + ((((int64_t)b * nc + c) * H + h0 + i) * C::P) * N + n;
+#pragma unroll
+            for (int cc = 0; cc < C::P / 32; ++cc) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) out[(int64_t)(32 * cc + j) * N] = __uint_as_float(r[j]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[ab]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && bars.abort) record_error(err, kErrTimeoutK2);
+}
+
+int num_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
+    }
+    return cached[dev];
+}
+
+// Heads per CTA: the largest divisor of H/G (at most 16) that still gives every
+// SM about four CTAs; with too few work items, one head per CTA.
+int pick_hpc(const Dims& d, int64_t outer) {
+    const int hpg = (int)(d.H / d.G);
+    const int64_t want = 4LL * num_sms();
+    for (int v = 16; v >= 1; --v)
+        if (hpg % v == 0 && outer * (d.H / v) >= want) return v;
+    return 1;
+}
+
+template <int L>
+cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
+                      const float* dtT, float* dS, int32_t* err, cudaStream_t st) {
+    using C = K2Cfg<L>;
+    CUtensorMap tm_x, tm_b;
+    const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
+    const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
+    const uint32_t box[3] = {64, (uint32_t)L, 1};
+    const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
+    const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
+    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box))
+        return cudaErrorInvalidValue;
+    const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
+    const int64_t outer = d.b * d.nc * n_tiles;
+    const int hpc = pick_hpc(d, outer);
+    const int n_hblk = (int)(d.H / hpc);
+    const int64_t grid = outer * n_hblk;
+    auto k = chunk_state_tc_kernel<L>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, cum2, dtT, dS, (int)d.T, (int)d.H,
+                                                 (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
+                                                 n_hblk, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const Dims& d) {
+    return d.dtype == 1 && (d.L == 128 || d.L == 256) && d.P == 64 &&
+           (d.N == 64 || d.N == 128 || d.N == 256) && d.T < (int64_t(1) << 31) &&
+           d.b * d.nc * d.H * d.P < (int64_t(1) << 31) &&      // TMA row coordinate of Sprev
+           d.H * d.P < (int64_t(1) << 31) && d.G * d.N < (int64_t(1) << 31);
+}
+
+cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
+                                  const float* dtT, float* dS, int32_t* err, cudaStream_t st) {
+    if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
+    if (!tc_supported(d)) return cudaErrorInvalidValue;
+    return d.L == 256 ? launch_k2<256>(d, x, B, cum2, dtT, dS, err, st)
+                      : launch_k2<128>(d, x, B, cum2, dtT, dS, err, st);
+}
+
+}  // namespace m2

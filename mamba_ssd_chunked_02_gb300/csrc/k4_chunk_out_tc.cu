@@ -1,0 +1,499 @@
+// k4_chunk_out_tc.cu -- stage 4 on tcgen05 tensor cores: the fused output.
+//
+// Pages: "Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+// NVIDIA CUDA Tile" (brifing.si), section 9 "Fusing Operations in compute_out"
+// (interaction matrix, carried-state term and skip term in one tiled kernel,
+// the interaction matrix never in global memory) and section 11 "Causal
+// Masking and Stability" (mask before exponentiating: every in-mask exponent
+// is <= 0); "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr),
+// "세 가지 핵심 커널 구현" (compute_out: the lower-triangular mask is generated
+// from indices, decay by exp2) and "cuTile 기반 성능 최적화 기법" (the operand a
+// kernel produces itself goes to tensor memory as MMA operand A, using
+// (AB)^T = B^T A^T).
+//
+// For a 128-token query tile (rows t) of chunk c, keys s in [0, KS) of the same
+// chunk (KS = 128 * (tile + 1)), and each head h of a block of heads that share
+// the B/C group:
+//   y[t,:] = sum_s M[t,s] x[s,:] + exp2(cum2_t) (C_t . Sprev_c^T) + D_h x[t,:]
+//   M[t,s] = (C_t . B_s) * exp2(cum2_t - cum2_s) * dt_s  for s <= t, else 0.
+// Tensor-memory plan (512 columns, fp32 unless noted):
+//   [0, KS)         CB = C_tile . B_keys^T      (GEMM1, once per CTA: C.B^T does
+//                                               not depend on the head)
+//   [256, 256+KS/2) M as bf16 pairs, MMA operand A of GEMM2 (written by the
+//                   epilogue warps with tcgen05.st)
+//   [384, 512)      two 64-column accumulators, one per head in flight
+// Per head: GEMM3 acc = C . Sprev^T (A = C tile, B = Sprev, both K-major in
+// shared memory); the epilogue rescales each accumulator row t by
+// exp2(cum2_t) in tensor memory and builds M from CB: the causal mask comes
+// from the row/column indices and is applied before exp2; below the warp's
+// diagonal 32x32 block the decay is split as
+// exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the warp's first row, so
+// both factors are <= 1 and only the diagonal block needs one exp2 per
+// element.  GEMM2 acc += M . X (A from tensor memory, X MN-major in shared
+// memory); the epilogue adds D_h x_t, rounds to bf16 and stores the tile with a
+// TMA store (rows past the sequence end are clipped by the tensor map).
+// Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner),
+// 2 .. 2+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column group
+// (warp-2)/4).  Loads stream through a ring of NS stages: first the B blocks
+// of GEMM1 (64 state dims each), then per head x (KS rows) and Sprev.
+#include "common.cuh"
+#include "internal.h"
+#include "tc5.cuh"
+#include "tmap.h"
+
+namespace m2 {
+namespace {
+
+using namespace tc;
+
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int EG = 2;                         // epilogue warp groups (4 warps each)
+constexpr int kEpiThreads = 128 * EG;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int PC = 64 / EG;                   // y columns per epilogue group
+static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread");
+constexpr uint32_t COL_CB = 0, COL_MM = 256, COL_ACC = 384;
+
+template <int L, int NA>   // NA = N / 64
+struct K4Cfg {
+    static constexpr int P = 64;
+    static constexpr int C_BYTES = NA * 128 * 128;         // C tile: NA K-major atoms
+    static constexpr int X_BYTES = L * 128;                 // x rows [0, L) (or a B block)
+    static constexpr int S_BYTES = NA * 64 * 128;           // Sprev: NA K-major atoms, 64 rows
+    static constexpr int STAGE = X_BYTES + S_BYTES;
+    static constexpr int Y_BYTES = 128 * 128;
+    static constexpr int VEC_BYTES = (2 * 256 + 4 * 256) * 4;
+    static constexpr int budget(int ns, int yb) {
+        return 1024 + C_BYTES + ns * STAGE + yb * Y_BYTES + VEC_BYTES;
+    }
+    static constexpr int NS = budget(3, 2) <= 220 * 1024 ? 3 : 2;
+    static constexpr int YB = budget(NS, 2) <= 220 * 1024 ? 2 : 1;
+    static constexpr int SMEM = budget(NS, YB);
+};
+
+struct K4Bars {
+    uint64_t full[3], xfree[3];
+    uint64_t cb_full;
+    uint64_t s3_done[2], acc_full[2], acc_empty[2];
+    uint64_t mm_ready;
+    uint64_t epi_sync;      // group barrier of the epilogue warps (abortable, unlike bar.sync)
+    uint64_t drain;         // commit target used to drain in-flight MMAs on abort
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int L, int NA>
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
+                    const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
+                    const float* __restrict__ dtT, const float* __restrict__ Dvec, int T, int H,
+                    int G, int nc, int hpc, int n_hblk, int32_t* err) {
+    using C = K4Cfg<L, NA>;
+    constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t* sC = smem;
+    uint8_t* sStage = sC + C::C_BYTES;
+    uint8_t* sY = sStage + NS * C::STAGE;
+    float* cum_k = reinterpret_cast<float*>(sY + YB * C::Y_BYTES);   // [256]
+    float* dt_k = cum_k + 256;                                        // [256]
+    float* vdt = dt_k + 256;                                          // [4][256]
+    __shared__ K4Bars bars;
+    volatile int* abort = &bars.abort;
+
+    // Work item: (b, c, head block) outer; the query tiles of one item are
+    // adjacent (heaviest first) so that they share x and Sprev through L2.
+    int rest = blockIdx.x;
+    const int qt = NQ - 1 - rest % NQ; rest /= NQ;
+    const int hblk = rest % n_hblk; rest /= n_hblk;
+    const int c = rest % nc;
+    const int b = rest / nc;
+    const int KS = 128 * (qt + 1);
+    const int h0 = hblk * hpc;
+    const int g = h0 / (H / G);
+    const int nh = hpc;
+    const int n_items = NA + nh;
+    const int Lc = min(L, T - c * L);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (128 * qt >= Lc) return;       // tile entirely past the end of the sequence
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&bars.full[i], 1);
+            mbar_init(&bars.xfree[i], 1);
+        }
+        mbar_init(&bars.cb_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s3_done[i], 1);
+            mbar_init(&bars.acc_full[i], 1);
+            mbar_init(&bars.acc_empty[i], kEpiThreads);
+        }
+        mbar_init(&bars.mm_ready, kEpiThreads);
+        mbar_init(&bars.epi_sync, kEpiThreads);
+        mbar_init(&bars.drain, 1);
+        bars.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_x);
+            prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_c);
+            prefetch_tmap(&tm_s);
+            prefetch_tmap(&tm_y);
+            int issued = 0;
+            for (int it = 0; it < n_items; ++it) {
+                const int st = it % NS, k = it / NS;
+                if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
+                uint8_t* sx = sStage + st * C::STAGE;
+                if (it < NA) {
+                    // B block `it`: keys [0, KS) x state dims [64 it, 64 it + 64), K-major.
+                    mbar_arrive_expect_tx(&bars.full[st], KS * 128 + (it == 0 ? C::C_BYTES : 0));
+                    for (int r = 0; r < KS / 128; ++r)
+                        tma_load_3d(sx + r * 16384, &tm_b, &bars.full[st], g * N + 64 * it,
+                                    c * L + 128 * r, b);
+                    if (it == 0)
+                        for (int a = 0; a < NA; ++a)
+                            tma_load_3d(sC + a * 16384, &tm_c, &bars.full[st], g * N + 64 * a,
+                                        c * L + 128 * qt, b);
+                } else {
+                    const int h = h0 + it - NA;
+                    mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
+                    for (int r = 0; r < KS / 128; ++r)
+                        tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], h * C::P,
+                                    c * L + 128 * r, b);
+                    const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
+                    for (int a = 0; a < NA; ++a)
+                        tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
+                }
+                issued = it + 1;
+            }
+            if (*abort)
+                for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
+                    mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t c_addr = smem_u32(sC);
+            const uint32_t id_cb = idesc_bf16_f32(128, KS, 0, 0);
+            constexpr uint32_t id_s3 = idesc_bf16_f32(128, 64, 0, 0);
+            constexpr uint32_t id_s2 = idesc_bf16_f32(128, 64, 0, 1);
+            int last = -1;
+            bool ok = true;
+            for (int it = 0; it < n_items && ok; ++it) {
+                const int st = it % NS, k = it / NS;
+                const uint32_t x_addr = smem_u32(sStage + st * C::STAGE);
+                if (!(ok = mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs))) break;
+                if (it < NA) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(c_addr + it * 16384 + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(x_addr + kk * 32, 16, 1024);
+                        mma_ss(tmem + COL_CB, ad, bd, id_cb, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars.xfree[st]);
+                    if (it == NA - 1) mma_commit(&bars.cb_full);
+                    continue;
+                }
+                const int hi = it - NA, ab = hi & 1, ka = hi >> 1;
+                if (!(ok = mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs))) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + COL_ACC + 64 * ab;
+                const uint32_t s_addr = x_addr + C::X_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {   // GEMM3: acc = C . Sprev^T
+                    const uint64_t ad = smem_desc_sw128(c_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(s_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                    mma_ss(acc, ad, bd, id_s3, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars.s3_done[ab]);
+                if (!(ok = mbar_wait_or_abort(&bars.mm_ready, hi & 1, abort, kWaitNs))) break;
+                tc_fence_after();
+                for (int kk = 0; kk < KS / 16; ++kk) {   // GEMM2: acc += M . X
+                    const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::X_BYTES, 1024);
+                    mma_ts(acc, tmem + COL_MM + 8 * kk, bd, id_s2, 1u);
+                }
+                mma_commit(&bars.acc_full[ab]);
+                mma_commit(&bars.xfree[st]);
+                last = hi;
+            }
+            if (*abort) {   // nothing may be in flight when TMEM is freed
+                (void)last;
+                mma_commit(&bars.drain);
+                mbar_wait(&bars.drain, 0, kWaitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;                       // 0 .. 4*EG-1
+        const int q = warp & 3;                        // TMEM lane quadrant
+        const int grp = ew >> 2;                       // column group
+        const int etid = threadIdx.x - 64;             // 0 .. kEpiThreads-1
+        const int tl = 32 * q + lane;                  // row within the tile
+        const int tc_ = 128 * qt + tl;                 // row within the chunk
+        const int jd = 4 * qt + q;                     // this warp's diagonal key block
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        const int nblk = KS / 32;
+        uint32_t sync_phase = 0;
+        // Barrier of all epilogue threads; gives up (false) on abort or timeout.
+        auto group_sync = [&]() -> bool {
+            mbar_arrive(&bars.epi_sync);
+            const bool r = mbar_wait_or_abort(&bars.epi_sync, sync_phase, abort, kWaitNs);
+            sync_phase ^= 1u;
+            return __all_sync(0xffffffffu, r);
+        };
+
+        // Key blocks above the diagonal are zero for every head: write them once.
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+            for (int j = jd + 1; j < nblk; ++j)
+                if (j % EG == grp) tmem_st16(tmem + lane_off + COL_MM + 16 * j, z);
+            tmem_wait_st();
+        }
+        bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cb_full, 0, abort, kWaitNs));
+        tc_fence_after();
+
+        uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
+        float d_prev = 0.f, d_cur = 0.f;
+        for (int hi = 0; hi <= nh && ok; ++hi) {
+            if (hi < nh) {
+                // --------------------------------------------------- prep(hi)
+                const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1;
+                const int h = h0 + hi;
+                const int64_t bh = (int64_t)b * H + h;
+                if (!(ok = group_sync())) break;         // previous head done with the vectors
+                {
+                    const float* crow = cum2 + bh * T + (int64_t)c * L;
+                    const float* drow = dtT + bh * T + (int64_t)c * L;
+                    const float clast = __ldg(crow + Lc - 1);
+                    for (int s = etid; s < KS; s += kEpiThreads) {
+                        const bool in = s < Lc;
+                        cum_k[s] = in ? __ldg(crow + s) : clast;
+                        dt_k[s] = in ? __ldg(drow + s) : 0.f;
+                    }
+                }
+                d_cur = Dvec ? __ldg(Dvec + h) : 0.f;
+                if (!(ok = group_sync())) break;
+                const float ct = cum_k[tc_];
+                const float e_t = ex2(ct);
+                const float cr = cum_k[32 * jd];
+                const float u_t = ex2(ct - cr);
+                for (int j = grp; j < jd; j += EG)
+                    vdt[q * 256 + 32 * j + lane] =
+                        ex2(cr - cum_k[32 * j + lane]) * dt_k[32 * j + lane];
+                __syncwarp();
+
+                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
+                if (!ok) break;
+                {   // x row t (this group's columns) for the skip term
+                    const uint8_t* xrow = sStage + st * C::STAGE + tc_ * 128;
+#pragma unroll
+                    for (int cc = 0; cc < PC / 8; ++cc) {
+                        const int chunk = grp * (PC / 8) + cc;
+                        const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((chunk ^ (tc_ & 7)) << 4));
+                        xv_cur[4 * cc + 0] = v.x; xv_cur[4 * cc + 1] = v.y;
+                        xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
+                    }
+                }
+                // Rescale the carried-state accumulator row by exp2(cum2_t).
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.s3_done[ab], (hi >> 1) & 1, abort, kWaitNs));
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    const uint32_t a = tmem + lane_off + COL_ACC + 64 * ab + grp * PC;
+                    uint32_t r[32];
+                    tmem_ld32(a, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * e_t);
+                    tmem_st32(a, r);
+                }
+                // The M region is free once the previous head's GEMM2 completed.
+                if (hi > 0) {
+                    const int pb = (hi - 1) & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.acc_full[pb],
+                                                                    ((hi - 1) >> 1) & 1, abort, kWaitNs));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                for (int j = grp; j <= jd; j += EG) {
+                    uint32_t r[32], m[16];
+                    tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
+                    tmem_wait_ld();
+                    if (j < jd) {
+                        const float4* v4 = reinterpret_cast<const float4*>(vdt + q * 256 + 32 * j);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 v = v4[e4];
+                            const float m0 = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
+                            const float m1 = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
+                            const float m2 = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
+                            const float m3 = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
+                            m[2 * e4 + 0] = pack_bf16x2(m0, m1);
+                            m[2 * e4 + 1] = pack_bf16x2(m2, m3);
+                        }
+                    } else {
+                        const float4* c4 = reinterpret_cast<const float4*>(cum_k + 32 * j);
+                        const float4* d4 = reinterpret_cast<const float4*>(dt_k + 32 * j);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 cv = c4[e4], dv = d4[e4];
+                            const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+                            const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
+                            float mv[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = 4 * e4 + u;   // key s = 32 j + e, row t = 32 j + lane
+                                mv[u] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
+                            }
+                            m[2 * e4 + 0] = pack_bf16x2(mv[0], mv[1]);
+                            m[2 * e4 + 1] = pack_bf16x2(mv[2], mv[3]);
+                        }
+                    }
+                    tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars.mm_ready);
+            }
+            if (hi > 0) {
+                // ------------------------------------------------- finish(hi-1)
+                const int hp = hi - 1, pb = hp & 1;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty[pb]);
+                uint32_t yv[PC / 2];
+#pragma unroll
+                for (int e = 0; e < PC / 2; ++e) {
+                    const uint32_t xw = xv_prev[e];
+                    const float y0 = __uint_as_float(r[2 * e]) + d_prev * __uint_as_float(xw << 16);
+                    const float y1 = __uint_as_float(r[2 * e + 1]) + d_prev * __uint_as_float(xw & 0xffff0000u);
+                    yv[e] = pack_bf16x2(y0, y1);
+                }
+                const int yb = hp % YB;
+                uint8_t* ytile = sY + yb * C::Y_BYTES;
+                if (etid == 0) bulk_wait_read<YB - 1>();   // the store that last used ytile is done reading
+                if (!(ok = group_sync())) break;
+#pragma unroll
+                for (int cc = 0; cc < PC / 8; ++cc) {
+                    const int chunk = grp * (PC / 8) + cc;
+                    *reinterpret_cast<uint4*>(ytile + tl * 128 + ((chunk ^ (tl & 7)) << 4)) =
+                        make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
+                }
+                fence_proxy_async_smem();
+                if (!(ok = group_sync())) break;
+                if (etid == 0) {
+                    tma_store_3d(&tm_y, ytile, (h0 + hp) * C::P, c * L + 128 * qt, b);
+                    bulk_commit();
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
+            d_prev = d_cur;
+        }
+        if (etid == 0) bulk_wait<0>();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && bars.abort) record_error(err, kErrTimeoutK4);
+}
+
+int num_sms4() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
+    }
+    return cached[dev];
+}
+
+template <int L, int NA>
+cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
+                      const float* cum2, const float* dtT, const void* Sprev, const float* D,
+                      void* y, int32_t* err, cudaStream_t st) {
+    using C = K4Cfg<L, NA>;
+    CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
+    const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
+    const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
+    const uint32_t box[3] = {64, 128, 1};
+    const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
+    const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
+    const uint64_t sd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
+    const uint64_t ss[1] = {(uint64_t)(d.N * 2)};
+    const uint32_t sbox[2] = {64, 64};
+    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
+        !make_tmap_bf16(&tm_c, Cm, 3, bd, bs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
+        !make_tmap_bf16(&tm_y, y, 3, xd, xs, box))
+        return cudaErrorInvalidValue;
+    const int NQ = L / 128;
+    const int64_t outer = d.b * d.nc * NQ;
+    const int hpg = (int)(d.H / d.G);
+    int hpc = 1;
+    for (int v = 16; v >= 1; --v)
+        if (hpg % v == 0 && outer * (d.H / v) >= 4LL * num_sms4()) { hpc = v; break; }
+    const int n_hblk = (int)(d.H / hpc);
+    const int64_t grid = outer * n_hblk;
+    auto k = chunk_out_tc_kernel<L, NA>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_c, tm_s, tm_y, cum2, dtT, D,
+                                                 (int)d.T, (int)d.H, (int)d.G, (int)d.nc, hpc,
+                                                 n_hblk, err);
+    return cudaGetLastError();
+}
+
+template <int L>
+cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void* Cm,
+                        const float* cum2, const float* dtT, const void* Sprev, const float* D,
+                        void* y, int32_t* err, cudaStream_t st) {
+    switch (d.N) {
+        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
+        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
+        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
+                                const float* cum2, const float* dtT, const void* Sprev,
+                                const float* D, void* y, int32_t* err, cudaStream_t st) {
+    if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
+    if (!tc_supported(d)) return cudaErrorInvalidValue;
+    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st)
+                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st);
+}
+
+}  // namespace m2
