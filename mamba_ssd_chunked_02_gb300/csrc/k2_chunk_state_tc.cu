@@ -174,18 +174,27 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // ------------------------------------------------------------- scaling
         const int idx = threadIdx.x - 64;                // 0..127
         const int Lc = min(L, T - c * L);
-        for (int i = 0; i < nh; ++i) {
-            const int st = i % NS, k = i / NS;
-            const int64_t bh = (int64_t)b * H + h0 + i;
+        // Raw decay inputs of the next head, fetched one head ahead.
+        float pc[L / 128], pd[L / 128], plast = 0.f;
+        auto prefetch = [&](int hh) {
+            const int64_t bh = (int64_t)b * H + h0 + hh;
             const float* crow = cum2 + bh * T + (int64_t)c * L;
             const float* drow = dtT + bh * T + (int64_t)c * L;
-            const float last = __ldg(crow + Lc - 1);
-            float w[L / 128];
+            plast = __ldg(crow + Lc - 1);
 #pragma unroll
             for (int r = 0; r < L / 128; ++r) {
                 const int s = idx + 128 * r;
-                w[r] = s < Lc ? __ldg(drow + s) * ex2(last - __ldg(crow + s)) : 0.f;
+                pc[r] = s < Lc ? __ldg(crow + s) : 0.f;
+                pd[r] = s < Lc ? __ldg(drow + s) : 0.f;
             }
+        };
+        prefetch(0);
+        for (int i = 0; i < nh; ++i) {
+            const int st = i % NS, k = i / NS;
+            float w[L / 128];
+#pragma unroll
+            for (int r = 0; r < L / 128; ++r) w[r] = pd[r] * ex2(plast - pc[r]);   // 0 past Lc
+            if (i + 1 < nh) prefetch(i + 1);
             const bool ok = __all_sync(0xffffffffu,
                                        mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
             if (!ok) break;
@@ -225,8 +234,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 #pragma unroll
             for (int cc = 0; cc < C::P / 32; ++cc) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
-                tmem_wait_ld();
+                tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
                 if (valid) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) out[(int64_t)(32 * cc + j) * N] = __uint_as_float(r[j]);

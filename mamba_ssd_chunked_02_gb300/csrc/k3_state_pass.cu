@@ -13,7 +13,7 @@
 // Sequential over chunks, parallel over (b, h, 4-element slices of the P x N
 // state): one thread owns a float4 of the state for the whole chain.  The dS
 // loads do not depend on the chain, so each thread keeps kDepth chunks of loads
-// in flight before it walks the chain through them: a pure HBM stream of
+// in flight (a rolling prefetch) while it walks the chain: a pure HBM stream of
 // 4 + esize bytes per state element per chunk.
 #include "common.cuh"
 #include "internal.h"
@@ -53,27 +53,42 @@ state_pass_kernel(const float* __restrict__ dS, const float* __restrict__ cum2,
     const int64_t cstride = H * PN;                       // chunk stride in dS / Sprev
     const int64_t base = (b * nc * H + h) * PN + e;       // [b, c=0, h, e]
 
-    for (int64_t c0 = 0; c0 < nc; c0 += kDepth) {
-        float4 d[kDepth];
-        float dec[kDepth];
+    // Rolling prefetch: the loads of chunk c + kDepth are issued when chunk c is
+    // consumed, so kDepth chunks of dS stay in flight for the whole chain.
+    // Addresses advance by running pointers (one chunk = cstride elements).
+    const float* pd = dS + base;                 // next chunk of dS to fetch
+    const float* pl = crow + L - 1;              // its last token's cum2 (clamped below)
+    const float* const plend = crow + T - 1;
+    TS* ps = Sprev + base;
+    float4 buf[kDepth];
+    float cl[kDepth];
 #pragma unroll
-        for (int u = 0; u < kDepth; ++u) {
-            const int64_t c = c0 + u;
-            if (c < nc) {
-                d[u] = __ldcs(reinterpret_cast<const float4*>(dS + base + c * cstride));
-                const int64_t last = min((c + 1) * L, T) - 1;
-                dec[u] = ex2(__ldg(crow + last));
-            }
+    for (int u = 0; u < kDepth; ++u) {
+        if (u < nc) {
+            buf[u] = __ldcs(reinterpret_cast<const float4*>(pd));
+            cl[u] = __ldg(pl < plend ? pl : plend);
+            pd += cstride;
+            pl += L;
         }
+    }
+    for (int64_t c0 = 0; c0 < nc; c0 += kDepth) {
 #pragma unroll
         for (int u = 0; u < kDepth; ++u) {
-            const int64_t c = c0 + u;
-            if (c < nc) {
-                store4(Sprev + base + c * cstride, S);
-                S.x = fmaf(dec[u], S.x, d[u].x);
-                S.y = fmaf(dec[u], S.y, d[u].y);
-                S.z = fmaf(dec[u], S.z, d[u].z);
-                S.w = fmaf(dec[u], S.w, d[u].w);
+            if (c0 + u < nc) {
+                const float4 d = buf[u];
+                const float dec = ex2(cl[u]);
+                if (c0 + u + kDepth < nc) {
+                    buf[u] = __ldcs(reinterpret_cast<const float4*>(pd));
+                    cl[u] = __ldg(pl < plend ? pl : plend);
+                    pd += cstride;
+                    pl += L;
+                }
+                store4(ps, S);
+                ps += cstride;
+                S.x = fmaf(dec, S.x, d.x);
+                S.y = fmaf(dec, S.y, d.y);
+                S.z = fmaf(dec, S.z, d.z);
+                S.w = fmaf(dec, S.w, d.w);
             }
         }
     }

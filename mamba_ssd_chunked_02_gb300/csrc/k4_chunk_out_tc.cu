@@ -19,8 +19,8 @@
 // Tensor-memory plan (512 columns, fp32 unless noted):
 //   [0, KS)         CB = C_tile . B_keys^T      (GEMM1, once per CTA: C.B^T does
 //                                               not depend on the head)
-//   [256, 256+KS/2) M as bf16 pairs, MMA operand A of GEMM2 (written by the
-//                   epilogue warps with tcgen05.st)
+//   [256, 256+KS/2) M as 16-bit pairs, MMA operand A of GEMM2, in two K-halves
+//                   (written by the epilogue warps with tcgen05.st)
 //   [384, 512)      two 64-column accumulators, one per head in flight
 // Per head: GEMM3 acc = C . Sprev^T (A = C tile, B = Sprev, both K-major in
 // shared memory); the epilogue rescales each accumulator row t by
@@ -29,9 +29,19 @@
 // diagonal 32x32 block the decay is split as
 // exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the warp's first row, so
 // both factors are <= 1 and only the diagonal block needs one exp2 per
-// element.  GEMM2 acc += M . X (A from tensor memory, X MN-major in shared
-// memory); the epilogue adds D_h x_t, rounds to bf16 and stores the tile with a
-// TMA store (rows past the sequence end are clipped by the tensor map).
+// element.  GEMM2 acc += M . X in two K-halves (A from tensor memory, X
+// MN-major in shared memory), so that the tensor core works on one half while
+// the epilogue builds the other.  The epilogue adds D_h x_t, rounds to bf16
+// and stores its 32x32 piece of the tile with a TMA store (rows past the
+// sequence end are clipped by the tensor map).
+//
+// Precision of GEMM2.  M and X enter GEMM2 as fp16 (10-bit mantissa) rather
+// than bf16 (7-bit): the worst-case error of a large output is then set by the
+// final bf16 rounding of y alone.  Per head the epilogue checks that fp16
+// cannot overflow -- max|x| <= 2^15 over the tile and max|C.B| * max(dt) <=
+// 2^15 (|M| is at most that product, every decay being <= 1) -- and otherwise
+// keeps bf16 for that head (x stays untouched, M is packed as bf16).
+//
 // Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner),
 // 2 .. 2+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column group
 // (warp-2)/4).  Loads stream through a ring of NS stages: first the B blocks
@@ -48,11 +58,13 @@ using namespace tc;
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int EG = 2;                         // epilogue warp groups (4 warps each)
-constexpr int kEpiThreads = 128 * EG;
+constexpr int kEpiWarps = 4 * EG;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int PC = 64 / EG;                   // y columns per epilogue group
 static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread");
 constexpr uint32_t COL_CB = 0, COL_MM = 256, COL_ACC = 384;
+constexpr uint32_t kF16Limit = 0x4700u;       // bf16 bit pattern of 2^15
 
 template <int L, int NA>   // NA = N / 64
 struct K4Cfg {
@@ -61,8 +73,10 @@ struct K4Cfg {
     static constexpr int X_BYTES = L * 128;                 // x rows [0, L) (or a B block)
     static constexpr int S_BYTES = NA * 64 * 128;           // Sprev: NA K-major atoms, 64 rows
     static constexpr int STAGE = X_BYTES + S_BYTES;
-    static constexpr int Y_BYTES = 128 * 128;
-    static constexpr int VEC_BYTES = (2 * 256 + 4 * 256) * 4;
+    static constexpr int YW_BYTES = 32 * 64;                // one warp's 32x32 bf16 piece of y
+    static constexpr int Y_BYTES = kEpiWarps * YW_BYTES;    // one y buffer for all warps
+    // cum_k[2][256], dt_k[2][256], vdt[4][256], red[2][warps][2], red_cb[warps]
+    static constexpr int VEC_BYTES = (2 * 256 + 2 * 256 + 4 * 256 + 2 * kEpiWarps * 2 + kEpiWarps) * 4;
     static constexpr int budget(int ns, int yb) {
         return 1024 + C_BYTES + ns * STAGE + yb * Y_BYTES + VEC_BYTES;
     }
@@ -75,12 +89,21 @@ struct K4Bars {
     uint64_t full[3], xfree[3];
     uint64_t cb_full;
     uint64_t s3_done[2], acc_full[2], acc_empty[2];
-    uint64_t mm_ready;
+    uint64_t mm_ready[2], mm_free[2];   // per K-half of M
     uint64_t epi_sync;      // group barrier of the epilogue warps (abortable, unlike bar.sync)
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
     uint32_t tmem_base;
     int abort;
+    int use16[2];           // per head (parity): GEMM2 operands in fp16 (1) or bf16 (0)
 };
+
+__device__ __forceinline__ uint32_t bf16_abs_max2(uint32_t m, uint32_t w) {
+    return max(m, max(w & 0x7fffu, (w >> 16) & 0x7fffu));
+}
+// Two bf16 (one word) -> f16x2, exactly when |v| is in the fp16 normal range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
 
 template <int L, int NA>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,9 +119,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     uint8_t* sC = smem;
     uint8_t* sStage = sC + C::C_BYTES;
     uint8_t* sY = sStage + NS * C::STAGE;
-    float* cum_k = reinterpret_cast<float*>(sY + YB * C::Y_BYTES);   // [256]
-    float* dt_k = cum_k + 256;                                        // [256]
-    float* vdt = dt_k + 256;                                          // [4][256]
+    float* cum_k = reinterpret_cast<float*>(sY + YB * C::Y_BYTES);   // [2][256]
+    float* dt_k = cum_k + 2 * 256;                                    // [2][256]
+    float* vdt = dt_k + 2 * 256;                                      // [4][256]
+    uint32_t* red = reinterpret_cast<uint32_t*>(vdt + 4 * 256);       // [2][kEpiWarps][2]
+    uint32_t* red_cb = red + 2 * kEpiWarps * 2;                       // [kEpiWarps]
     __shared__ K4Bars bars;
     volatile int* abort = &bars.abort;
 
@@ -128,8 +153,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             mbar_init(&bars.s3_done[i], 1);
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], kEpiThreads);
+            mbar_init(&bars.mm_ready[i], kEpiThreads);
+            mbar_init(&bars.mm_free[i], 1);
         }
-        mbar_init(&bars.mm_ready, kEpiThreads);
         mbar_init(&bars.epi_sync, kEpiThreads);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
@@ -189,8 +215,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const uint32_t c_addr = smem_u32(sC);
             const uint32_t id_cb = idesc_bf16_f32(128, KS, 0, 0);
             constexpr uint32_t id_s3 = idesc_bf16_f32(128, 64, 0, 0);
-            constexpr uint32_t id_s2 = idesc_bf16_f32(128, 64, 0, 1);
-            int last = -1;
             bool ok = true;
             for (int it = 0; it < n_items && ok; ++it) {
                 const int st = it % NS, k = it / NS;
@@ -220,25 +244,30 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     mma_ss(acc, ad, bd, id_s3, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars.s3_done[ab]);
-                if (!(ok = mbar_wait_or_abort(&bars.mm_ready, hi & 1, abort, kWaitNs))) break;
-                tc_fence_after();
-                for (int kk = 0; kk < KS / 16; ++kk) {   // GEMM2: acc += M . X
-                    const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::X_BYTES, 1024);
-                    mma_ts(acc, tmem + COL_MM + 8 * kk, bd, id_s2, 1u);
+                for (int half = 0; half < 2 && ok; ++half) {   // GEMM2: acc += M . X
+                    if (!(ok = mbar_wait_or_abort(&bars.mm_ready[half], hi & 1, abort, kWaitNs))) break;
+                    tc_fence_after();
+                    const uint32_t id_s2 = bars.use16[hi & 1] ? idesc_f16_f32(128, 64, 0, 1)
+                                                              : idesc_bf16_f32(128, 64, 0, 1);
+                    const int k0 = half * (KS / 32);
+                    for (int kk = k0; kk < k0 + KS / 32; ++kk) {
+                        const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::X_BYTES, 1024);
+                        mma_ts(acc, tmem + COL_MM + 8 * kk, bd, id_s2, 1u);
+                    }
+                    mma_commit(&bars.mm_free[half]);
                 }
+                if (!ok) break;
                 mma_commit(&bars.acc_full[ab]);
                 mma_commit(&bars.xfree[st]);
-                last = hi;
             }
             if (*abort) {   // nothing may be in flight when TMEM is freed
-                (void)last;
                 mma_commit(&bars.drain);
                 mbar_wait(&bars.drain, 0, kWaitNs);
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;                       // 0 .. 4*EG-1
+        const int ew = warp - 2;                       // 0 .. kEpiWarps-1
         const int q = warp & 3;                        // TMEM lane quadrant
         const int grp = ew >> 2;                       // column group
         const int etid = threadIdx.x - 64;             // 0 .. kEpiThreads-1
@@ -246,7 +275,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         const int tc_ = 128 * qt + tl;                 // row within the chunk
         const int jd = 4 * qt + q;                     // this warp's diagonal key block
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
-        const int nblk = KS / 32;
+        const int nblk = KS / 32, hblkn = KS / 64;    // key blocks, key blocks per K-half
         uint32_t sync_phase = 0;
         // Barrier of all epilogue threads; gives up (false) on abort or timeout.
         auto group_sync = [&]() -> bool {
@@ -255,6 +284,19 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
+        // Next head's decay vectors are fetched one head ahead (register prefetch).
+        float pf_cum = 0.f, pf_dt = 0.f, pf_last = 0.f, pf_D = 0.f;
+        auto prefetch = [&](int hh) {
+            const int64_t bh = (int64_t)b * H + h0 + hh;
+            const float* crow = cum2 + bh * T + (int64_t)c * L;
+            pf_last = __ldg(crow + Lc - 1);
+            if (etid < KS && etid < Lc) {
+                pf_cum = __ldg(crow + etid);
+                pf_dt = __ldg(dtT + bh * T + (int64_t)c * L + etid);
+            }
+            pf_D = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
+        };
+        prefetch(0);
 
         // Key blocks above the diagonal are zero for every head: write them once.
         {
@@ -267,41 +309,46 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         }
         bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cb_full, 0, abort, kWaitNs));
         tc_fence_after();
+        // max |C.B| over the entries this tile uses (bounds |M| for the fp16 check).
+        float cbmax = 0.f;
+        if (ok) {
+            for (int j = grp; j <= jd; j += EG) {
+                uint32_t r[32];
+                tmem_ld32_sync(tmem + lane_off + COL_CB + 32 * j, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) cbmax = fmaxf(cbmax, fabsf(__uint_as_float(r[e])));
+            }
+            uint32_t m = __float_as_uint(cbmax);   // non-negative floats order as integers
+            m = __reduce_max_sync(0xffffffffu, m);
+            if (lane == 0) red_cb[ew] = m;
+            ok = group_sync();
+            uint32_t mm = 0;
+            for (int i = 0; i < kEpiWarps; ++i) mm = max(mm, red_cb[i]);
+            cbmax = __uint_as_float(mm);
+        }
 
         uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
         float d_prev = 0.f, d_cur = 0.f;
         for (int hi = 0; hi <= nh && ok; ++hi) {
             if (hi < nh) {
                 // --------------------------------------------------- prep(hi)
-                const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1;
-                const int h = h0 + hi;
-                const int64_t bh = (int64_t)b * H + h;
-                if (!(ok = group_sync())) break;         // previous head done with the vectors
-                {
-                    const float* crow = cum2 + bh * T + (int64_t)c * L;
-                    const float* drow = dtT + bh * T + (int64_t)c * L;
-                    const float clast = __ldg(crow + Lc - 1);
-                    for (int s = etid; s < KS; s += kEpiThreads) {
-                        const bool in = s < Lc;
-                        cum_k[s] = in ? __ldg(crow + s) : clast;
-                        dt_k[s] = in ? __ldg(drow + s) : 0.f;
-                    }
+                const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1, vb = hi & 1;
+                float* ck = cum_k + vb * 256;
+                float* dk = dt_k + vb * 256;
+                if (etid < KS) {
+                    const bool in = etid < Lc;
+                    ck[etid] = in ? pf_cum : pf_last;
+                    dk[etid] = in ? pf_dt : 0.f;
                 }
-                d_cur = Dvec ? __ldg(Dvec + h) : 0.f;
-                if (!(ok = group_sync())) break;
-                const float ct = cum_k[tc_];
-                const float e_t = ex2(ct);
-                const float cr = cum_k[32 * jd];
-                const float u_t = ex2(ct - cr);
-                for (int j = grp; j < jd; j += EG)
-                    vdt[q * 256 + 32 * j + lane] =
-                        ex2(cr - cum_k[32 * j + lane]) * dt_k[32 * j + lane];
-                __syncwarp();
+                const float dloc = (etid < KS && etid < Lc) ? pf_dt : 0.f;
+                d_cur = pf_D;
+                if (hi + 1 < nh) prefetch(hi + 1);
 
                 ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
                 if (!ok) break;
-                {   // x row t (this group's columns) for the skip term
-                    const uint8_t* xrow = sStage + st * C::STAGE + tc_ * 128;
+                uint8_t* xs = sStage + st * C::STAGE;
+                {   // x row t (this group's columns) for the skip term, still bf16
+                    const uint8_t* xrow = xs + tc_ * 128;
 #pragma unroll
                     for (int cc = 0; cc < PC / 8; ++cc) {
                         const int chunk = grp * (PC / 8) + cc;
@@ -310,6 +357,55 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
                     }
                 }
+                // This thread's share of the x tile: chunks etid + kEpiThreads * i.
+                constexpr int kMaxChunks = L * 8 / kEpiThreads;
+                const int nch = KS * 8 / kEpiThreads;
+                uint4 xc[kMaxChunks];
+                uint32_t xmax = 0;
+#pragma unroll
+                for (int i = 0; i < kMaxChunks; ++i) {
+                    if (i < nch) {
+                        xc[i] = *reinterpret_cast<const uint4*>(xs + (etid + kEpiThreads * i) * 16);
+                        xmax = bf16_abs_max2(xmax, xc[i].x); xmax = bf16_abs_max2(xmax, xc[i].y);
+                        xmax = bf16_abs_max2(xmax, xc[i].z); xmax = bf16_abs_max2(xmax, xc[i].w);
+                    }
+                }
+                xmax = __reduce_max_sync(0xffffffffu, xmax);
+                const uint32_t dmax = __reduce_max_sync(0xffffffffu, __float_as_uint(dloc));
+                if (lane == 0) {
+                    red[(vb * kEpiWarps + ew) * 2 + 0] = xmax;
+                    red[(vb * kEpiWarps + ew) * 2 + 1] = dmax;
+                }
+                if (!(ok = group_sync())) break;     // vectors and maxima visible to all
+                uint32_t gx = 0, gd = 0;
+                for (int i = 0; i < kEpiWarps; ++i) {
+                    gx = max(gx, red[(vb * kEpiWarps + i) * 2 + 0]);
+                    gd = max(gd, red[(vb * kEpiWarps + i) * 2 + 1]);
+                }
+                const bool use16 = gx <= kF16Limit && cbmax * __uint_as_float(gd) <= 32768.f;
+                if (use16) {
+#pragma unroll
+                    for (int i = 0; i < kMaxChunks; ++i) {
+                        if (i < nch) {
+                            const uint4 v = xc[i];
+                            *reinterpret_cast<uint4*>(xs + (etid + kEpiThreads * i) * 16) =
+                                make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                           bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                }
+                if (etid == 0) bars.use16[hi & 1] = use16 ? 1 : 0;
+
+                const float ct = ck[tc_];
+                const float e_t = ex2(ct);
+                const float cr = ck[32 * jd];
+                const float u_t = ex2(ct - cr);
+                float* vq = vdt + q * 256;
+                for (int j = grp; j < jd; j += EG)
+                    vq[32 * j + lane] = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
+                __syncwarp();
+
                 // Rescale the carried-state accumulator row by exp2(cum2_t).
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait_or_abort(&bars.s3_done[ab], (hi >> 1) & 1, abort, kWaitNs));
@@ -318,59 +414,70 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 {
                     const uint32_t a = tmem + lane_off + COL_ACC + 64 * ab + grp * PC;
                     uint32_t r[32];
-                    tmem_ld32(a, r);
-                    tmem_wait_ld();
+                    tmem_ld32_sync(a, r);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * e_t);
                     tmem_st32(a, r);
                 }
-                // The M region is free once the previous head's GEMM2 completed.
-                if (hi > 0) {
-                    const int pb = (hi - 1) & 1;
-                    ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.acc_full[pb],
-                                                                    ((hi - 1) >> 1) & 1, abort, kWaitNs));
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                for (int j = grp; j <= jd; j += EG) {
-                    uint32_t r[32], m[16];
-                    tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
-                    tmem_wait_ld();
-                    if (j < jd) {
-                        const float4* v4 = reinterpret_cast<const float4*>(vdt + q * 256 + 32 * j);
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 v = v4[e4];
-                            const float m0 = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
-                            const float m1 = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
-                            const float m2 = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
-                            const float m3 = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
-                            m[2 * e4 + 0] = pack_bf16x2(m0, m1);
-                            m[2 * e4 + 1] = pack_bf16x2(m2, m3);
-                        }
-                    } else {
-                        const float4* c4 = reinterpret_cast<const float4*>(cum_k + 32 * j);
-                        const float4* d4 = reinterpret_cast<const float4*>(dt_k + 32 * j);
-#pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 cv = c4[e4], dv = d4[e4];
-                            const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
-                            const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
-                            float mv[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = 4 * e4 + u;   // key s = 32 j + e, row t = 32 j + lane
-                                mv[u] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
-                            }
-                            m[2 * e4 + 0] = pack_bf16x2(mv[0], mv[1]);
-                            m[2 * e4 + 1] = pack_bf16x2(mv[2], mv[3]);
-                        }
+                for (int half = 0; half < 2 && ok; ++half) {
+                    // The half's M columns are free once the previous head's GEMM2 half completed.
+                    if (hi > 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.mm_free[half], (hi - 1) & 1,
+                                                                        abort, kWaitNs));
+                        if (!ok) break;
+                        tc_fence_after();
                     }
-                    tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
+                    const int jlo = half * hblkn, jhi = min(jd, jlo + hblkn - 1);
+                    int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own block >= jlo
+                    uint32_t r[32];
+                    if (j <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
+                    for (; j <= jhi; j += EG) {
+                        tmem_wait_ld_regs(r);
+                        float cbv[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) cbv[e] = __uint_as_float(r[e]);
+                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
+                        float mv[32];
+                        if (j < jd) {
+                            const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 v = v4[e4];
+                                mv[4 * e4 + 0] = cbv[4 * e4 + 0] * (u_t * v.x);
+                                mv[4 * e4 + 1] = cbv[4 * e4 + 1] * (u_t * v.y);
+                                mv[4 * e4 + 2] = cbv[4 * e4 + 2] * (u_t * v.z);
+                                mv[4 * e4 + 3] = cbv[4 * e4 + 3] * (u_t * v.w);
+                            }
+                        } else {
+                            const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
+                            const float4* d4 = reinterpret_cast<const float4*>(dk + 32 * j);
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 cv = c4[e4], dv = d4[e4];
+                                const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+                                const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
+                                    mv[e] = e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f;
+                                }
+                            }
+                        }
+                        uint32_t m[16];
+                        if (use16) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
+                        }
+                        tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars.mm_ready[half]);
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars.mm_ready);
+                if (!ok) break;
             }
             if (hi > 0) {
                 // ------------------------------------------------- finish(hi-1)
@@ -380,8 +487,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
-                tmem_wait_ld();
+                tmem_ld32_sync(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
                 tc_fence_before();
                 mbar_arrive(&bars.acc_empty[pb]);
                 uint32_t yv[PC / 2];
@@ -392,20 +498,19 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float y1 = __uint_as_float(r[2 * e + 1]) + d_prev * __uint_as_float(xw & 0xffff0000u);
                     yv[e] = pack_bf16x2(y0, y1);
                 }
-                const int yb = hp % YB;
-                uint8_t* ytile = sY + yb * C::Y_BYTES;
-                if (etid == 0) bulk_wait_read<YB - 1>();   // the store that last used ytile is done reading
-                if (!(ok = group_sync())) break;
+                // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
+                // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
+                uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
+                if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
+                __syncwarp();
 #pragma unroll
-                for (int cc = 0; cc < PC / 8; ++cc) {
-                    const int chunk = grp * (PC / 8) + cc;
-                    *reinterpret_cast<uint4*>(ytile + tl * 128 + ((chunk ^ (tl & 7)) << 4)) =
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(yw + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
                         make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
-                }
                 fence_proxy_async_smem();
-                if (!(ok = group_sync())) break;
-                if (etid == 0) {
-                    tma_store_3d(&tm_y, ytile, (h0 + hp) * C::P, c * L + 128 * qt, b);
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tm_y, yw, (h0 + hp) * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
                     bulk_commit();
                 }
             }
@@ -413,7 +518,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
             d_prev = d_cur;
         }
-        if (etid == 0) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();
     }
 
     tc_fence_before();
@@ -447,6 +552,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
     const uint32_t box[3] = {64, 128, 1};
+    const uint32_t ybox[3] = {32, 32, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
     const uint64_t sd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
@@ -454,7 +560,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint32_t sbox[2] = {64, 64};
     if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
         !make_tmap_bf16(&tm_c, Cm, 3, bd, bs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
-        !make_tmap_bf16(&tm_y, y, 3, xd, xs, box))
+        !make_tmap_bf16(&tm_y, y, 3, xd, xs, ybox, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     const int NQ = L / 128;
     const int64_t outer = d.b * d.nc * NQ;
