@@ -45,7 +45,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate 
 template <int L>
 struct K2Cfg {
     static constexpr int P = 64;
-    static constexpr int NS = 3;                          // x stages
+    static constexpr int NS = L == 256 ? 5 : 6;           // x stages (fill the SMEM)
     static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
     static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
     static constexpr int X_BYTES = ATOM;                  // P = 64: one block
@@ -56,7 +56,7 @@ struct K2Cfg {
 
 struct K2Bars {
     uint64_t bt_full;
-    uint64_t full[4], scaled[4], xfree[4];
+    uint64_t full[6], scaled[6], xfree[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
     uint32_t tmem_base;

@@ -216,34 +216,45 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const uint32_t id_cb = idesc_bf16_f32(128, KS, 0, 0);
             constexpr uint32_t id_s3 = idesc_bf16_f32(128, 64, 0, 0);
             bool ok = true;
-            for (int it = 0; it < n_items && ok; ++it) {
+            // GEMM1: C . B^T, one 64-state-dim block per ring item.
+            for (int it = 0; it < NA && ok; ++it) {
                 const int st = it % NS, k = it / NS;
                 const uint32_t x_addr = smem_u32(sStage + st * C::STAGE);
                 if (!(ok = mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs))) break;
-                if (it < NA) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(c_addr + it * 16384 + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(x_addr + kk * 32, 16, 1024);
-                        mma_ss(tmem + COL_CB, ad, bd, id_cb, (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&bars.xfree[st]);
-                    if (it == NA - 1) mma_commit(&bars.cb_full);
-                    continue;
-                }
-                const int hi = it - NA, ab = hi & 1, ka = hi >> 1;
-                if (!(ok = mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs))) break;
                 tc_fence_after();
-                const uint32_t acc = tmem + COL_ACC + 64 * ab;
-                const uint32_t s_addr = x_addr + C::X_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {   // GEMM3: acc = C . Sprev^T
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(c_addr + it * 16384 + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(x_addr + kk * 32, 16, 1024);
+                    mma_ss(tmem + COL_CB, ad, bd, id_cb, (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars.xfree[st]);
+                if (it == NA - 1) mma_commit(&bars.cb_full);
+            }
+            // GEMM3 of head hh: acc[hh & 1] = C . Sprev_hh^T.
+            auto gemm3 = [&](int hh) -> bool {
+                const int it = NA + hh, st = it % NS, k = it / NS, ab = hh & 1, ka = hh >> 1;
+                if (!mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs)) return false;
+                if (!mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs)) return false;
+                tc_fence_after();
+                const uint32_t s_addr = smem_u32(sStage + st * C::STAGE) + C::X_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
                     const uint64_t ad = smem_desc_sw128(c_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(s_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(acc, ad, bd, id_s3, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + COL_ACC + 64 * ab, ad, bd, id_s3, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars.s3_done[ab]);
+                return true;
+            };
+            if (ok && nh > 0) ok = gemm3(0);
+            // Per head: GEMM3 of the next head goes first, so that the epilogue's
+            // rescale of head hi+1 never waits behind this head's GEMM2.
+            for (int hi = 0; hi < nh && ok; ++hi) {
+                if (hi + 1 < nh && !(ok = gemm3(hi + 1))) break;
+                const int it = NA + hi, st = it % NS, ab = hi & 1;
+                const uint32_t x_addr = smem_u32(sStage + st * C::STAGE);
+                const uint32_t acc = tmem + COL_ACC + 64 * ab;
                 for (int half = 0; half < 2 && ok; ++half) {   // GEMM2: acc += M . X
                     if (!(ok = mbar_wait_or_abort(&bars.mm_ready[half], hi & 1, abort, kWaitNs))) break;
                     tc_fence_after();
@@ -329,195 +340,202 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 
         uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
         float d_prev = 0.f, d_cur = 0.f;
-        for (int hi = 0; hi <= nh && ok; ++hi) {
-            if (hi < nh) {
-                // --------------------------------------------------- prep(hi)
-                const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1, vb = hi & 1;
-                float* ck = cum_k + vb * 256;
-                float* dk = dt_k + vb * 256;
-                if (etid < KS) {
-                    const bool in = etid < Lc;
-                    ck[etid] = in ? pf_cum : pf_last;
-                    dk[etid] = in ? pf_dt : 0.f;
-                }
-                const float dloc = (etid < KS && etid < Lc) ? pf_dt : 0.f;
-                d_cur = pf_D;
-                if (hi + 1 < nh) prefetch(hi + 1);
-
-                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
-                if (!ok) break;
-                uint8_t* xs = sStage + st * C::STAGE;
-                {   // x row t (this group's columns) for the skip term, still bf16
-                    const uint8_t* xrow = xs + tc_ * 128;
+        // finish(hp): y rows of head hp = acc + D x, bf16, TMA-stored per warp.
+        auto finish = [&](int hp) -> bool {
+            const int pb = hp & 1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
+                return false;
+            tc_fence_after();
+            uint32_t r[32];
+            tmem_ld32_sync(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[pb]);
+            uint32_t yv[PC / 2];
 #pragma unroll
-                    for (int cc = 0; cc < PC / 8; ++cc) {
-                        const int chunk = grp * (PC / 8) + cc;
-                        const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((chunk ^ (tc_ & 7)) << 4));
-                        xv_cur[4 * cc + 0] = v.x; xv_cur[4 * cc + 1] = v.y;
-                        xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
+            for (int e = 0; e < PC / 2; ++e) {
+                const uint32_t xw = xv_prev[e];
+                const float y0 = __uint_as_float(r[2 * e]) + d_prev * __uint_as_float(xw << 16);
+                const float y1 = __uint_as_float(r[2 * e + 1]) + d_prev * __uint_as_float(xw & 0xffff0000u);
+                yv[e] = pack_bf16x2(y0, y1);
+            }
+            // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
+            // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
+            uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
+            if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
+            __syncwarp();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(yw + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&tm_y, yw, (h0 + hp) * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
+                bulk_commit();
+            }
+            return true;
+        };
+        for (int hi = 0; hi < nh && ok; ++hi) {
+            const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1, vb = hi & 1;
+            // ---- tensor-independent part of head hi: decay vectors, x tile.
+            float* ck = cum_k + vb * 256;
+            float* dk = dt_k + vb * 256;
+            if (etid < KS) {
+                const bool in = etid < Lc;
+                ck[etid] = in ? pf_cum : pf_last;
+                dk[etid] = in ? pf_dt : 0.f;
+            }
+            const float dloc = (etid < KS && etid < Lc) ? pf_dt : 0.f;
+            d_cur = pf_D;
+            if (hi + 1 < nh) prefetch(hi + 1);
+
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
+            if (!ok) break;
+            uint8_t* xs = sStage + st * C::STAGE;
+            {   // x row t (this group's columns) for the skip term, still bf16
+                const uint8_t* xrow = xs + tc_ * 128;
+#pragma unroll
+                for (int cc = 0; cc < PC / 8; ++cc) {
+                    const int chunk = grp * (PC / 8) + cc;
+                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((chunk ^ (tc_ & 7)) << 4));
+                    xv_cur[4 * cc + 0] = v.x; xv_cur[4 * cc + 1] = v.y;
+                    xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
+                }
+            }
+            // This thread's share of the x tile: chunks etid + kEpiThreads * i.
+            constexpr int kMaxChunks = L * 8 / kEpiThreads;
+            const int nch = KS * 8 / kEpiThreads;
+            uint4 xc[kMaxChunks];
+            __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kMaxChunks; ++i) {
+                if (i < nch) {
+                    xc[i] = *reinterpret_cast<const uint4*>(xs + (etid + kEpiThreads * i) * 16);
+                    const uint32_t w4[4] = {xc[i].x, xc[i].y, xc[i].z, xc[i].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t a = w4[e] & 0x7fff7fffu;   // |x|, two at a time
+                        xm2 = __hmax2(xm2, *reinterpret_cast<const __nv_bfloat162*>(&a));
                     }
                 }
-                // This thread's share of the x tile: chunks etid + kEpiThreads * i.
-                constexpr int kMaxChunks = L * 8 / kEpiThreads;
-                const int nch = KS * 8 / kEpiThreads;
-                uint4 xc[kMaxChunks];
-                uint32_t xmax = 0;
+            }
+            const uint32_t xm2u = *reinterpret_cast<const uint32_t*>(&xm2);
+            uint32_t xmax = max(xm2u & 0xffffu, xm2u >> 16);
+            xmax = __reduce_max_sync(0xffffffffu, xmax);
+            const uint32_t dmax = __reduce_max_sync(0xffffffffu, __float_as_uint(dloc));
+            if (lane == 0) {
+                red[(vb * kEpiWarps + ew) * 2 + 0] = xmax;
+                red[(vb * kEpiWarps + ew) * 2 + 1] = dmax;
+            }
+            if (!(ok = group_sync())) break;     // vectors and maxima visible to all
+            uint32_t gx = 0, gd = 0;
+            for (int i = 0; i < kEpiWarps; ++i) {
+                gx = max(gx, red[(vb * kEpiWarps + i) * 2 + 0]);
+                gd = max(gd, red[(vb * kEpiWarps + i) * 2 + 1]);
+            }
+            const bool use16 = gx <= kF16Limit && cbmax <= 32768.f &&
+                               cbmax * __uint_as_float(gd) <= 32768.f;
+            if (use16) {
 #pragma unroll
                 for (int i = 0; i < kMaxChunks; ++i) {
                     if (i < nch) {
-                        xc[i] = *reinterpret_cast<const uint4*>(xs + (etid + kEpiThreads * i) * 16);
-                        xmax = bf16_abs_max2(xmax, xc[i].x); xmax = bf16_abs_max2(xmax, xc[i].y);
-                        xmax = bf16_abs_max2(xmax, xc[i].z); xmax = bf16_abs_max2(xmax, xc[i].w);
+                        const uint4 v = xc[i];
+                        *reinterpret_cast<uint4*>(xs + (etid + kEpiThreads * i) * 16) =
+                            make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                       bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
                     }
                 }
-                xmax = __reduce_max_sync(0xffffffffu, xmax);
-                const uint32_t dmax = __reduce_max_sync(0xffffffffu, __float_as_uint(dloc));
-                if (lane == 0) {
-                    red[(vb * kEpiWarps + ew) * 2 + 0] = xmax;
-                    red[(vb * kEpiWarps + ew) * 2 + 1] = dmax;
-                }
-                if (!(ok = group_sync())) break;     // vectors and maxima visible to all
-                uint32_t gx = 0, gd = 0;
-                for (int i = 0; i < kEpiWarps; ++i) {
-                    gx = max(gx, red[(vb * kEpiWarps + i) * 2 + 0]);
-                    gd = max(gd, red[(vb * kEpiWarps + i) * 2 + 1]);
-                }
-                const bool use16 = gx <= kF16Limit && cbmax * __uint_as_float(gd) <= 32768.f;
-                if (use16) {
-#pragma unroll
-                    for (int i = 0; i < kMaxChunks; ++i) {
-                        if (i < nch) {
-                            const uint4 v = xc[i];
-                            *reinterpret_cast<uint4*>(xs + (etid + kEpiThreads * i) * 16) =
-                                make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
-                                           bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-                        }
-                    }
-                    fence_proxy_async_smem();
-                }
-                if (etid == 0) bars.use16[hi & 1] = use16 ? 1 : 0;
-
-                const float ct = ck[tc_];
-                const float e_t = ex2(ct);
-                const float cr = ck[32 * jd];
-                const float u_t = ex2(ct - cr);
-                float* vq = vdt + q * 256;
-                for (int j = grp; j < jd; j += EG)
-                    vq[32 * j + lane] = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
-                __syncwarp();
-
-                // Rescale the carried-state accumulator row by exp2(cum2_t).
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&bars.s3_done[ab], (hi >> 1) & 1, abort, kWaitNs));
-                if (!ok) break;
-                tc_fence_after();
-                {
-                    const uint32_t a = tmem + lane_off + COL_ACC + 64 * ab + grp * PC;
-                    uint32_t r[32];
-                    tmem_ld32_sync(a, r);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * e_t);
-                    tmem_st32(a, r);
-                }
-                for (int half = 0; half < 2 && ok; ++half) {
-                    // The half's M columns are free once the previous head's GEMM2 half completed.
-                    if (hi > 0) {
-                        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.mm_free[half], (hi - 1) & 1,
-                                                                        abort, kWaitNs));
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
-                    const int jlo = half * hblkn, jhi = min(jd, jlo + hblkn - 1);
-                    int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own block >= jlo
-                    uint32_t r[32];
-                    if (j <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
-                    for (; j <= jhi; j += EG) {
-                        tmem_wait_ld_regs(r);
-                        float cbv[32];
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) cbv[e] = __uint_as_float(r[e]);
-                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
-                        float mv[32];
-                        if (j < jd) {
-                            const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
-#pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 v = v4[e4];
-                                mv[4 * e4 + 0] = cbv[4 * e4 + 0] * (u_t * v.x);
-                                mv[4 * e4 + 1] = cbv[4 * e4 + 1] * (u_t * v.y);
-                                mv[4 * e4 + 2] = cbv[4 * e4 + 2] * (u_t * v.z);
-                                mv[4 * e4 + 3] = cbv[4 * e4 + 3] * (u_t * v.w);
-                            }
-                        } else {
-                            const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
-                            const float4* d4 = reinterpret_cast<const float4*>(dk + 32 * j);
-#pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 cv = c4[e4], dv = d4[e4];
-                                const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
-                                const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
-                                    mv[e] = e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f;
-                                }
-                            }
-                        }
-                        uint32_t m[16];
-                        if (use16) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
-                        }
-                        tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    mbar_arrive(&bars.mm_ready[half]);
-                }
-                if (!ok) break;
-            }
-            if (hi > 0) {
-                // ------------------------------------------------- finish(hi-1)
-                const int hp = hi - 1, pb = hp & 1;
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs));
-                if (!ok) break;
-                tc_fence_after();
-                uint32_t r[32];
-                tmem_ld32_sync(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
-                tc_fence_before();
-                mbar_arrive(&bars.acc_empty[pb]);
-                uint32_t yv[PC / 2];
-#pragma unroll
-                for (int e = 0; e < PC / 2; ++e) {
-                    const uint32_t xw = xv_prev[e];
-                    const float y0 = __uint_as_float(r[2 * e]) + d_prev * __uint_as_float(xw << 16);
-                    const float y1 = __uint_as_float(r[2 * e + 1]) + d_prev * __uint_as_float(xw & 0xffff0000u);
-                    yv[e] = pack_bf16x2(y0, y1);
-                }
-                // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
-                // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
-                uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
-                if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
-                __syncwarp();
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4*>(yw + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
-                        make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(&tm_y, yw, (h0 + hp) * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
-                    bulk_commit();
-                }
             }
+            if (etid == 0) bars.use16[hi & 1] = use16 ? 1 : 0;
+
+            const float ct = ck[tc_];
+            const float e_t = ex2(ct);
+            const float cr = ck[32 * jd];
+            const float u_t = ex2(ct - cr);
+            float* vq = vdt + q * 256;
+            for (int j = grp; j < jd; j += EG)
+                vq[32 * j + lane] = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
+            __syncwarp();
+
+            // ---- previous head's output while this head's GEMM3 completes.
+            if (hi > 0 && !(ok = finish(hi - 1))) break;
 #pragma unroll
             for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
             d_prev = d_cur;
+
+            // ---- rescale the carried-state accumulator row by exp2(cum2_t).
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bars.s3_done[ab], (hi >> 1) & 1, abort, kWaitNs));
+            if (!ok) break;
+            tc_fence_after();
+            {
+                const uint32_t a = tmem + lane_off + COL_ACC + 64 * ab + grp * PC;
+                uint32_t r[32];
+                tmem_ld32_sync(a, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * e_t);
+                tmem_st32(a, r);
+            }
+            // ---- M, in two K-halves.
+            for (int half = 0; half < 2 && ok; ++half) {
+                // The half's M columns are free once the previous head's GEMM2 half completed.
+                if (hi > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.mm_free[half], (hi - 1) & 1,
+                                                                    abort, kWaitNs));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const int jlo = half * hblkn, jhi = min(jd, jlo + hblkn - 1);
+                int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own block >= jlo
+                uint32_t r[32];
+                if (j <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
+                for (; j <= jhi; j += EG) {
+                    tmem_wait_ld_regs(r);
+                    float mv[32];
+                    if (j < jd) {
+                        const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 v = v4[e4];
+                            mv[4 * e4 + 0] = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
+                            mv[4 * e4 + 1] = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
+                            mv[4 * e4 + 2] = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
+                            mv[4 * e4 + 3] = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
+                        }
+                    } else {
+                        const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
+                        const float4* d4 = reinterpret_cast<const float4*>(dk + 32 * j);
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 cv = c4[e4], dv = d4[e4];
+                            const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+                            const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
+                                mv[e] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
+                            }
+                        }
+                    }
+                    if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
+                    uint32_t m[16];
+                    if (use16) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
+                    }
+                    tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars.mm_ready[half]);
+            }
         }
+        if (ok && nh > 0) ok = finish(nh - 1);
         if (lane == 0) bulk_wait<0>();
     }
 
