@@ -45,11 +45,12 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate 
 template <int L>
 struct K2Cfg {
     static constexpr int P = 64;
-    static constexpr int NS = L == 256 ? 5 : 6;           // x stages (fill the SMEM)
+    static constexpr int NS = L == 256 ? 3 : 6;           // x stages
     static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
     static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
     static constexpr int X_BYTES = ATOM;                  // P = 64: one block
-    static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES;
+    static constexpr int D_BYTES = 64 * 128 * 4;          // one dS tile [p][n-tile], fp32
+    static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + 2 * D_BYTES;
     static constexpr int TMEM_COLS = 128;                 // 2 accumulators x 64 columns
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 1, 1);
 };
@@ -59,6 +60,7 @@ struct K2Bars {
     uint64_t full[6], scaled[6], xfree[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
+    uint64_t epi_sync;      // group barrier of the 4 epilogue warps (abortable)
     uint32_t tmem_base;
     int abort;
 };
@@ -67,6 +69,7 @@ template <int L>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_d,
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       float* __restrict__ dS, int T, int H, int N, int G, int nc, int n_tiles,
                       int hpc, int n_hblk, int32_t* err) {
@@ -76,6 +79,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sBt = smem;
     uint8_t* sX = smem + C::BT_BYTES;
+    float* sD = reinterpret_cast<float*>(sX + NS * C::X_BYTES);   // [2][64][128]
     __shared__ K2Bars bars;
     volatile int* abort = &bars.abort;
 
@@ -103,6 +107,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&bars.acc_empty[i], 128);
         }
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.epi_sync, 128);
         bars.abort = 0;
         fence_barrier_init();
     }
@@ -120,6 +125,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         if (lane == 0) {
             prefetch_tmap(&tm_x);
             prefetch_tmap(&tm_b);
+            prefetch_tmap(&tm_d);
             mbar_arrive_expect_tx(&bars.bt_full, C::BT_BYTES);
             for (int a = 0; a < 2; ++a) {
                 // N = 64: both halves of the 128-row M tile hold n in [0, 64).
@@ -221,28 +227,49 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // D[n, p] (lane = n) goes to a shared [p][n] fp32 tile (conflict-free:
+        // a warp writes 32 consecutive n of one p), then one TMA store per head
+        // writes the tile to dS[b, c, h, :, n-tile].
         const int q = warp & 3;                          // TMEM lane quadrant
-        const int n = (N == 64 ? 0 : nt * 128) + 32 * q + lane;
-        const bool valid = n < N && (N != 64 || q < 2);
+        const int ep = threadIdx.x - 192;                // 0..127
+        const int NT = N < 128 ? N : 128;                // n-tile width = tile row pitch
+        const int nl = 32 * q + lane;                    // n within the tile
+        uint32_t sync_phase = 0;
+        auto group_sync = [&]() -> bool {
+            mbar_arrive(&bars.epi_sync);
+            const bool r = mbar_wait_or_abort(&bars.epi_sync, sync_phase, abort, kWaitNs);
+            sync_phase ^= 1u;
+            return __all_sync(0xffffffffu, r);
+        };
         for (int i = 0; i < nh; ++i) {
             const int ab = i & 1, ka = i >> 1;
             const bool ok = __all_sync(0xffffffffu,
                                        mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
             if (!ok) break;
             tc_fence_after();
-            float* out = dS + ((((int64_t)b * nc + c) * H + h0 + i) * C::P) * N + n;
+            float* tile = sD + ab * (64 * 128);
+            if (ep == 0) bulk_wait_read<1>();            // the store that used this tile is done
+            if (!group_sync()) break;                    // ... before any warp writes it
 #pragma unroll
             for (int cc = 0; cc < C::P / 32; ++cc) {
                 uint32_t r[32];
                 tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
-                if (valid) {
+                if (nl < NT) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) out[(int64_t)(32 * cc + j) * N] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) tile[(32 * cc + j) * NT + nl] = __uint_as_float(r[j]);
                 }
             }
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[ab]);
+            fence_proxy_async_smem();
+            if (!group_sync()) break;
+            if (ep == 0) {
+                const int row = (int)((((int64_t)b * nc + c) * H + h0 + i) * C::P);
+                tma_store_2d(&tm_d, tile, nt * 128, row);
+                bulk_commit();
+            }
         }
+        if (ep == 0) bulk_wait<0>();
     }
 
     tc_fence_before();
@@ -287,7 +314,13 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     const uint32_t box[3] = {64, (uint32_t)L, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
-    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box))
+    CUtensorMap tm_d;
+    const uint64_t dd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
+    const uint64_t ds[1] = {(uint64_t)(d.N * 4)};
+    const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
+    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
+        !make_tmap(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dS, 2, dd, ds, dbox,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
     const int64_t outer = d.b * d.nc * n_tiles;
@@ -297,7 +330,7 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     auto k = chunk_state_tc_kernel<L>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, cum2, dtT, dS, (int)d.T, (int)d.H,
+    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, cum2, dtT, dS, (int)d.T, (int)d.H,
                                                  (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
                                                  n_hblk, err);
     return cudaGetLastError();

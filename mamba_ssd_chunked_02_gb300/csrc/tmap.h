@@ -26,12 +26,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
     return fn;
 }
 
-// A bf16 tensor of rank 2 or 3: dims[0] is contiguous; strides are the byte
-// strides of dims 1 and 2; box the tile copied per request.  128-byte swizzle,
-// zero fill outside the tensor.  Returns false when the encoder rejects it.
-inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                           const uint64_t* strides_bytes, const uint32_t* box,
-                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+// A tensor of rank 2 or 3 and element type `dtype`: dims[0] is contiguous;
+// strides are the byte strides of dims 1 and 2; box the tile copied per
+// request; zero fill outside the tensor.  Returns false when the encoder
+// rejects it.
+inline bool make_tmap(CUtensorMap* m, CUtensorMapDataType dtype, const void* base, int rank,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle) {
     auto enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t gd[3], gs[2];
@@ -41,10 +42,18 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uin
         bx[i] = box[i];
     }
     for (int i = 0; i + 1 < rank; ++i) gs[i] = strides_bytes[i];
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
-                     gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The same for bf16, 128-byte swizzle by default.
+inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box,
+                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box,
+                     swizzle);
 }
 
 }  // namespace m2
