@@ -173,6 +173,35 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
  * failure, MAMBA2_OK otherwise. */
 MAMBA2_API mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear);
 
+/* Forward pass for callers that cannot allocate device memory.
+ *
+ * No counterpart on the pages: this is a convenience of this library.  Some
+ * callers have no way to obtain device memory of their own -- code running
+ * where cudaMalloc is forbidden or unavailable (for example inside a host
+ * framework that owns every allocation, or a plug-in whose host may not call
+ * the CUDA allocator), or code that must not allocate on its hot path.  For
+ * them this entry point runs exactly mamba2_ssd_fwd, but with the workspace
+ * taken from a fixed device array compiled into this library,
+ * MAMBA2_NOALLOC_SCRATCH_BYTES (64 MiB) large; every GPU that loads the
+ * library keeps that array until the process exits.  The caller still passes
+ * every input and output buffer.
+ *   - Shapes whose mamba2_ssd_workspace_size exceeds the array are rejected
+ *     with MAMBA2_ERR_WORKSPACE before anything is launched.
+ *   - The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ *     library routine.  The first call on each device looks up the array's
+ *     device address (cudaGetSymbolAddress, with that device current); make
+ *     that first call before any stream capture on the device.
+ *   - Every call on a device shares the one array.  Nothing in it needs to
+ *     start at zero (each stage writes what the next reads), but two calls
+ *     that overlap on the GPU (different streams, no ordering between them)
+ *     race on it and produce wrong results: order such calls. */
+#define MAMBA2_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_ssd_shape* shape,
+                             const void* x, const float* dt, const float* A,
+                             const void* B, const void* C, const float* D,
+                             const float* initial_state,
+                             void* y, float* final_state, void* stream);
+
 /* Static description of a status code. */
 MAMBA2_API const char* mamba2_status_string(mamba2_status status);
 

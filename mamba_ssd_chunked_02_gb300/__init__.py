@@ -37,7 +37,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = rang
 SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_size",
            "mamba2_ssd_fwd", "mamba2_ssd_chunk_cumsum", "mamba2_ssd_chunk_state",
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
-           "mamba2_status_string", "mamba2_ssd_version")
+           "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc")
 
 
 class Shape(ctypes.Structure):
@@ -97,6 +97,8 @@ def load():
         lib.mamba2_status_string.restype = ctypes.c_char_p
         lib.mamba2_ssd_version.argtypes = []
         lib.mamba2_ssd_version.restype = ctypes.c_char_p
+        lib.mamba2_ssd_fwd_noalloc.argtypes = [sp] + [vp] * 9 + [vp]
+        lib.mamba2_ssd_fwd_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -251,6 +253,30 @@ def chunk_out(shape, x, B, C, cum2, dtT, Sprev, D, y, stream=None):
         _ptr(Sprev, "Sprev", io, (b, shape.nchunks, H, P, N)),
         _ptr(D, "D", torch.float32, (H,), optional=True), _ptr(y, "y", io, (b, T, H, P)),
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def ssd_fwd_noalloc(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=None,
+                    *, y, final_state, stream=None, flags=0):
+    """Forward pass through mamba2_ssd_fwd_noalloc, for callers that cannot
+    allocate device memory: the workspace is the library's own fixed 64 MiB
+    device array, so the caller passes preallocated outputs `y` and
+    `final_state` and nothing is allocated here.  Calls on one device share
+    that array and must not overlap on the GPU."""
+    sh = shape_of(x, B, chunk_size, ngroups, flags)
+    b, T, H, P, N, G = sh.batch, sh.seqlen, sh.nheads, sh.headdim, sh.dstate, sh.ngroups
+    io = _io_dtype(sh)
+    args = [
+        _ptr(x, "x", io, (b, T, H, P)), _ptr(dt, "dt", torch.float32, (b, T, H)),
+        _ptr(A, "A", torch.float32, (H,)), _ptr(B, "B", io, (b, T, G, N)),
+        _ptr(C, "C", io, (b, T, G, N)), _ptr(D, "D", torch.float32, (H,), optional=True),
+        _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
+        _ptr(y, "y", io, (b, T, H, P)), _ptr(final_state, "final_state", torch.float32, (b, H, P, N)),
+        _stream(stream)]
+    _check("mamba2_ssd_fwd_noalloc", load().mamba2_ssd_fwd_noalloc(ctypes.byref(sh), *args))
+    return y, final_state
 
 
 def device_error(clear=True) -> int:
