@@ -211,7 +211,10 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 uint4* row = reinterpret_cast<uint4*>(xs + s * 128);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    uint4 v = row[q];
+                    // Lanes own consecutive rows (128 bytes apart); visiting chunk
+                    // (q + s) mod 8 spreads a warp's accesses over all 32 banks.
+                    const int qc = (q + s) & 7;
+                    uint4 v = row[qc];
                     uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -219,7 +222,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const float hi = __uint_as_float(u[e] & 0xffff0000u) * w[r];
                         u[e] = pack_bf16x2(lo, hi);
                     }
-                    row[q] = v;
+                    row[qc] = v;
                 }
             }
             fence_proxy_async_smem();
