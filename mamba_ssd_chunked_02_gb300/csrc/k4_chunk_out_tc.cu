@@ -29,7 +29,8 @@
 // diagonal 32x32 block the decay is split as
 // exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the warp's first row, so
 // both factors are <= 1 and only the diagonal block needs one exp2 per
-// element.  GEMM2 acc += M . X in two K-halves (A from tensor memory, X
+// element; on the fp16 path the two multiplies of a below-diagonal entry are
+// packed fp16 multiplies, two keys per instruction.  GEMM2 acc += M . X in two K-halves (A from tensor memory, X
 // MN-major in shared memory), so that the tensor core works on one half while
 // the epilogue builds the other.  The epilogue adds D_h x_t, rounds to bf16
 // and stores its 32x32 piece of the tile with a TMA store (rows past the
@@ -46,6 +47,8 @@
 // 2 .. 2+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column group
 // (warp-2)/4).  Loads stream through a ring of NS stages: first the B blocks
 // of GEMM1 (64 state dims each), then per head x (KS rows) and Sprev.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc5.cuh"
@@ -333,8 +336,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             m = __reduce_max_sync(0xffffffffu, m);
             if (lane == 0) red_cb[ew] = m;
             ok = group_sync();
-            uint32_t mm = 0;
-            for (int i = 0; i < kEpiWarps; ++i) mm = max(mm, red_cb[i]);
+            const uint32_t mm = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red_cb[lane] : 0u);
             cbmax = __uint_as_float(mm);
         }
 
@@ -429,11 +431,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 red[(vb * kEpiWarps + ew) * 2 + 1] = dmax;
             }
             if (!(ok = group_sync())) break;     // vectors and maxima visible to all
-            uint32_t gx = 0, gd = 0;
-            for (int i = 0; i < kEpiWarps; ++i) {
-                gx = max(gx, red[(vb * kEpiWarps + i) * 2 + 0]);
-                gd = max(gd, red[(vb * kEpiWarps + i) * 2 + 1]);
-            }
+            const uint32_t gx = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red[(vb * kEpiWarps + lane) * 2 + 0] : 0u);
+            const uint32_t gd = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red[(vb * kEpiWarps + lane) * 2 + 1] : 0u);
             const bool use16 = gx <= kF16Limit && cbmax <= 32768.f &&
                                cbmax * __uint_as_float(gd) <= 32768.f;
             if (use16) {
@@ -455,9 +454,14 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const float cr = ck[32 * jd];
             const float u_t = ex2(ct - cr);
             float* vq = vdt + q * 256;
-            for (int j = grp; j < jd; j += EG)
-                vq[32 * j + lane] = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
+            __half* vh = reinterpret_cast<__half*>(vq);
+            for (int j = grp; j < jd; j += EG) {
+                const float v = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
+                if (use16) vh[32 * j + lane] = __float2half_rn(v);
+                else vq[32 * j + lane] = v;
+            }
             __syncwarp();
+            const __half2 u2 = __float2half2_rn(u_t);
 
             // ---- previous head's output while this head's GEMM3 completes.
             if (hi > 0 && !(ok = finish(hi - 1))) break;
@@ -493,40 +497,58 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (j <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
                 for (; j <= jhi; j += EG) {
                     tmem_wait_ld_regs(r);
-                    float mv[32];
-                    if (j < jd) {
-                        const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
+                    uint32_t m[16];
+                    if (j < jd && use16) {
+                        const uint4* v4 = reinterpret_cast<const uint4*>(vh + 32 * j);
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 v = v4[e4];
-                            mv[4 * e4 + 0] = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
-                            mv[4 * e4 + 1] = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
-                            mv[4 * e4 + 2] = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
-                            mv[4 * e4 + 3] = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
-                        }
-                    } else {
-                        const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
-                        const float4* d4 = reinterpret_cast<const float4*>(dk + 32 * j);
+                        for (int e8 = 0; e8 < 4; ++e8) {
+                            const uint4 vv = v4[e8];
+                            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 cv = c4[e4], dv = d4[e4];
-                            const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
-                            const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
-                                mv[e] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
+                            for (int k2 = 0; k2 < 4; ++k2) {
+                                const int e = 8 * e8 + 2 * k2;
+                                const __half2 cb2 = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                                const __half2 uv = __hmul2(u2, *reinterpret_cast<const __half2*>(&vw[k2]));
+                                const __half2 mm2 = __hmul2(cb2, uv);
+                                m[4 * e8 + k2] = *reinterpret_cast<const uint32_t*>(&mm2);
                             }
                         }
-                    }
-                    if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
-                    uint32_t m[16];
-                    if (use16) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
+                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
                     } else {
+                        float mv[32];
+                        if (j < jd) {
+                            const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 v = v4[e4];
+                                mv[4 * e4 + 0] = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
+                                mv[4 * e4 + 1] = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
+                                mv[4 * e4 + 2] = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
+                                mv[4 * e4 + 3] = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
+                            }
+                        } else {
+                            const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
+                            const float4* d4 = reinterpret_cast<const float4*>(dk + 32 * j);
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 cv = c4[e4], dv = d4[e4];
+                                const float cs[4] = {cv.x, cv.y, cv.z, cv.w};
+                                const float ds[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
+                                    mv[e] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
+                                }
+                            }
+                        }
+                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
+                        if (use16) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
+                        }
                     }
                     tmem_st16(tmem + lane_off + COL_MM + 16 * j, m);
                 }
