@@ -38,15 +38,19 @@
 //
 // Precision of GEMM2.  M and X enter GEMM2 as fp16 (10-bit mantissa) rather
 // than bf16 (7-bit): the worst-case error of a large output is then set by the
-// final bf16 rounding of y alone.  Per head the epilogue checks that fp16
-// cannot overflow -- max|x| <= 2^15 over the tile and max|C.B| * max(dt) <=
-// 2^15 (|M| is at most that product, every decay being <= 1) -- and otherwise
-// keeps bf16 for that head (x stays untouched, M is packed as bf16).
+// final bf16 rounding of y alone.  Per head the converter warps check that
+// fp16 cannot overflow -- max|x| <= 2^15 over the tile and max|C.B| * max(dt)
+// <= 2^15 (|M| is at most that product, every decay being <= 1) -- and
+// otherwise keep bf16 for that head (x stays untouched, M is packed as bf16).
 //
 // Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner),
 // 2 .. 2+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column group
-// (warp-2)/4).  Loads stream through a ring of NS stages: first the B blocks
-// of GEMM1 (64 state dims each), then per head x (KS rows) and Sprev.
+// (warp-2)/4), the last kConvWarps = converters.  Loads stream through a ring
+// of NS stages: first the B blocks of GEMM1 (64 state dims each), then per
+// head x (KS rows) and Sprev.  As soon as a head's stage lands, the converters
+// copy its cum2 and dt rows into that stage's vector buffers, take the range
+// check and convert the x tile to fp16 in place; the epilogue warps, which
+// set the pace, only build M, rescale and write y.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -63,7 +67,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int EG = 2;                         // epilogue warp groups (4 warps each)
 constexpr int kEpiWarps = 4 * EG;
 constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kConvWarps = 2;                 // converter warps
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 constexpr int PC = 64 / EG;                   // y columns per epilogue group
 static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread");
 constexpr uint32_t COL_CB = 0, COL_MM = 256, COL_ACC = 384;
@@ -78,8 +84,8 @@ struct K4Cfg {
     static constexpr int STAGE = X_BYTES + S_BYTES;
     static constexpr int YW_BYTES = 32 * 64;                // one warp's 32x32 bf16 piece of y
     static constexpr int Y_BYTES = kEpiWarps * YW_BYTES;    // one y buffer for all warps
-    // cum_k[2][256], dt_k[2][256], vdt[4][256], red[2][warps][2], red_cb[warps]
-    static constexpr int VEC_BYTES = (2 * 256 + 2 * 256 + 4 * 256 + 2 * kEpiWarps * 2 + kEpiWarps) * 4;
+    // cumv[3][256], dtv[3][256] (per stage), vdt[4][256], red_x[3][kConvWarps][2], red_cb[warps]
+    static constexpr int VEC_BYTES = (3 * 256 + 3 * 256 + 4 * 256 + 3 * kConvWarps * 2 + kEpiWarps) * 4;
     static constexpr int budget(int ns, int yb) {
         return 1024 + C_BYTES + ns * STAGE + yb * Y_BYTES + VEC_BYTES;
     }
@@ -97,12 +103,14 @@ struct K4Bars {
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
     uint32_t tmem_base;
     int abort;
-    int use16[2];           // per head (parity): GEMM2 operands in fp16 (1) or bf16 (0)
+    uint64_t xready[3];     // per stage: x tile converted, decay vectors and flags written
+    uint64_t conv_sync;     // group barrier of the converter warps (abortable)
+    uint64_t cbinfo;        // max |C.B| published by the epilogue
+    float cbmax;
+    int use16s[3];          // per stage: GEMM2 operands of that head in fp16 (1) or bf16 (0)
+    float dvals[3];         // per stage: D of that head
 };
 
-__device__ __forceinline__ uint32_t bf16_abs_max2(uint32_t m, uint32_t w) {
-    return max(m, max(w & 0x7fffu, (w >> 16) & 0x7fffu));
-}
 // Two bf16 (one word) -> f16x2, exactly when |v| is in the fp16 normal range.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
@@ -122,11 +130,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     uint8_t* sC = smem;
     uint8_t* sStage = sC + C::C_BYTES;
     uint8_t* sY = sStage + NS * C::STAGE;
-    float* cum_k = reinterpret_cast<float*>(sY + YB * C::Y_BYTES);   // [2][256]
-    float* dt_k = cum_k + 2 * 256;                                    // [2][256]
-    float* vdt = dt_k + 2 * 256;                                      // [4][256]
-    uint32_t* red = reinterpret_cast<uint32_t*>(vdt + 4 * 256);       // [2][kEpiWarps][2]
-    uint32_t* red_cb = red + 2 * kEpiWarps * 2;                       // [kEpiWarps]
+    float* cumv = reinterpret_cast<float*>(sY + YB * C::Y_BYTES);    // [stage][256]
+    float* dtv = cumv + 3 * 256;                                      // [stage][256]
+    float* vdt = dtv + 3 * 256;                                       // [4][256]
+    uint32_t* red_x = reinterpret_cast<uint32_t*>(vdt + 4 * 256);     // [stage][kConvWarps][2]
+    uint32_t* red_cb = red_x + 3 * kConvWarps * 2;                    // [kEpiWarps]
     __shared__ K4Bars bars;
     volatile int* abort = &bars.abort;
 
@@ -160,6 +168,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             mbar_init(&bars.mm_free[i], 1);
         }
         mbar_init(&bars.epi_sync, kEpiThreads);
+        for (int i = 0; i < NS; ++i) mbar_init(&bars.xready[i], kConvThreads);
+        mbar_init(&bars.conv_sync, kConvThreads);
+        mbar_init(&bars.cbinfo, 1);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
         fence_barrier_init();
@@ -261,7 +272,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 for (int half = 0; half < 2 && ok; ++half) {   // GEMM2: acc += M . X
                     if (!(ok = mbar_wait_or_abort(&bars.mm_ready[half], hi & 1, abort, kWaitNs))) break;
                     tc_fence_after();
-                    const uint32_t id_s2 = bars.use16[hi & 1] ? idesc_f16_f32(128, 64, 0, 1)
+                    const uint32_t id_s2 = bars.use16s[st] ? idesc_f16_f32(128, 64, 0, 1)
                                                               : idesc_bf16_f32(128, 64, 0, 1);
                     const int k0 = half * (KS / 32);
                     for (int kk = k0; kk < k0 + KS / 32; ++kk) {
@@ -279,7 +290,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 mbar_wait(&bars.drain, 0, kWaitNs);
             }
         }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;                       // 0 .. kEpiWarps-1
         const int q = warp & 3;                        // TMEM lane quadrant
@@ -298,20 +309,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
-        // Next head's decay vectors are fetched one head ahead (register prefetch).
-        float pf_cum = 0.f, pf_dt = 0.f, pf_last = 0.f, pf_D = 0.f;
-        auto prefetch = [&](int hh) {
-            const int64_t bh = (int64_t)b * H + h0 + hh;
-            const float* crow = cum2 + bh * T + (int64_t)c * L;
-            pf_last = __ldg(crow + Lc - 1);
-            if (etid < KS && etid < Lc) {
-                pf_cum = __ldg(crow + etid);
-                pf_dt = __ldg(dtT + bh * T + (int64_t)c * L + etid);
-            }
-            pf_D = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
-        };
-        prefetch(0);
-
         // Key blocks above the diagonal are zero for every head: write them once.
         {
             uint32_t z[16];
@@ -338,10 +335,15 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             ok = group_sync();
             const uint32_t mm = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red_cb[lane] : 0u);
             cbmax = __uint_as_float(mm);
+            if (etid == 0) {             // publish for the converter warps
+                bars.cbmax = cbmax;
+                mbar_arrive(&bars.cbinfo);
+            }
         }
 
         uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
         float d_prev = 0.f, d_cur = 0.f;
+        bool x16_prev = false, x16_cur = false;
         // finish(hp): y rows of head hp = acc + D x, bf16, TMA-stored per warp.
         auto finish = [&](int hp) -> bool {
             const int pb = hp & 1;
@@ -357,9 +359,17 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
             for (int e = 0; e < PC / 2; ++e) {
                 const uint32_t xw = xv_prev[e];
-                const float y0 = __uint_as_float(r[2 * e]) + d_prev * __uint_as_float(xw << 16);
-                const float y1 = __uint_as_float(r[2 * e + 1]) + d_prev * __uint_as_float(xw & 0xffff0000u);
-                yv[e] = pack_bf16x2(y0, y1);
+                float x0, x1;
+                if (x16_prev) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw));
+                    x0 = f.x;
+                    x1 = f.y;
+                } else {
+                    x0 = __uint_as_float(xw << 16);
+                    x1 = __uint_as_float(xw & 0xffff0000u);
+                }
+                yv[e] = pack_bf16x2(__uint_as_float(r[2 * e]) + d_prev * x0,
+                                    __uint_as_float(r[2 * e + 1]) + d_prev * x1);
             }
             // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
             // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
@@ -379,24 +389,19 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             return true;
         };
         for (int hi = 0; hi < nh && ok; ++hi) {
-            const int it = NA + hi, st = it % NS, k = it / NS, ab = hi & 1, vb = hi & 1;
-            // ---- tensor-independent part of head hi: decay vectors, x tile.
-            float* ck = cum_k + vb * 256;
-            float* dk = dt_k + vb * 256;
-            if (etid < KS) {
-                const bool in = etid < Lc;
-                ck[etid] = in ? pf_cum : pf_last;
-                dk[etid] = in ? pf_dt : 0.f;
-            }
-            const float dloc = (etid < KS && etid < Lc) ? pf_dt : 0.f;
-            d_cur = pf_D;
-            if (hi + 1 < nh) prefetch(hi + 1);
-
-            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
+            const int it = NA + hi, st = it % NS, ab = hi & 1;
+            // ---- x tile, decay vectors and range decision come from the converters
+            // (phase of xready[st]: one per head item of that stage).
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_or_abort(&bars.xready[st], (hi / NS) & 1, abort, kWaitNs));
             if (!ok) break;
-            uint8_t* xs = sStage + st * C::STAGE;
-            {   // x row t (this group's columns) for the skip term, still bf16
-                const uint8_t* xrow = xs + tc_ * 128;
+            const float* ck = cumv + st * 256;
+            const float* dk = dtv + st * 256;
+            const bool use16 = bars.use16s[st] != 0;
+            d_cur = bars.dvals[st];
+            x16_cur = use16;
+            {   // x row t (this group's columns) for the skip term (fp16 if converted)
+                const uint8_t* xrow = sStage + st * C::STAGE + tc_ * 128;
 #pragma unroll
                 for (int cc = 0; cc < PC / 8; ++cc) {
                     const int chunk = grp * (PC / 8) + cc;
@@ -405,50 +410,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
                 }
             }
-            // This thread's share of the x tile: chunks etid + kEpiThreads * i.
-            constexpr int kMaxChunks = L * 8 / kEpiThreads;
-            const int nch = KS * 8 / kEpiThreads;
-            uint4 xc[kMaxChunks];
-            __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < kMaxChunks; ++i) {
-                if (i < nch) {
-                    xc[i] = *reinterpret_cast<const uint4*>(xs + (etid + kEpiThreads * i) * 16);
-                    const uint32_t w4[4] = {xc[i].x, xc[i].y, xc[i].z, xc[i].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t a = w4[e] & 0x7fff7fffu;   // |x|, two at a time
-                        xm2 = __hmax2(xm2, *reinterpret_cast<const __nv_bfloat162*>(&a));
-                    }
-                }
-            }
-            const uint32_t xm2u = *reinterpret_cast<const uint32_t*>(&xm2);
-            uint32_t xmax = max(xm2u & 0xffffu, xm2u >> 16);
-            xmax = __reduce_max_sync(0xffffffffu, xmax);
-            const uint32_t dmax = __reduce_max_sync(0xffffffffu, __float_as_uint(dloc));
-            if (lane == 0) {
-                red[(vb * kEpiWarps + ew) * 2 + 0] = xmax;
-                red[(vb * kEpiWarps + ew) * 2 + 1] = dmax;
-            }
-            if (!(ok = group_sync())) break;     // vectors and maxima visible to all
-            const uint32_t gx = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red[(vb * kEpiWarps + lane) * 2 + 0] : 0u);
-            const uint32_t gd = __reduce_max_sync(0xffffffffu, lane < kEpiWarps ? red[(vb * kEpiWarps + lane) * 2 + 1] : 0u);
-            const bool use16 = gx <= kF16Limit && cbmax <= 32768.f &&
-                               cbmax * __uint_as_float(gd) <= 32768.f;
-            if (use16) {
-#pragma unroll
-                for (int i = 0; i < kMaxChunks; ++i) {
-                    if (i < nch) {
-                        const uint4 v = xc[i];
-                        *reinterpret_cast<uint4*>(xs + (etid + kEpiThreads * i) * 16) =
-                            make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
-                                       bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-                    }
-                }
-                fence_proxy_async_smem();
-            }
-            if (etid == 0) bars.use16[hi & 1] = use16 ? 1 : 0;
-
             const float ct = ck[tc_];
             const float e_t = ex2(ct);
             const float cr = ck[32 * jd];
@@ -468,6 +429,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
             for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
             d_prev = d_cur;
+            x16_prev = x16_cur;
 
             // ---- rescale the carried-state accumulator row by exp2(cum2_t).
             ok = __all_sync(0xffffffffu,
@@ -559,6 +521,108 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         }
         if (ok && nh > 0) ok = finish(nh - 1);
         if (lane == 0) bulk_wait<0>();
+    }
+    else {
+        // ----------------------------------------------------------- converters
+        // Per head: decay vectors of the chunk into the stage's vector buffers,
+        // the range check (max |x| over the x tile, max dt) and, when fp16 cannot
+        // overflow, the x tile converted to fp16 in place.  They run ahead of the
+        // epilogue warps, which then only build M and write y.
+        const int ctid = threadIdx.x - 64 - kEpiThreads;   // 0 .. kConvThreads-1
+        const int cw = ctid >> 5;
+        uint32_t sync_phase = 0;
+        auto conv_sync = [&]() -> bool {
+            mbar_arrive(&bars.conv_sync);
+            const bool r = mbar_wait_or_abort(&bars.conv_sync, sync_phase, abort, kWaitNs);
+            sync_phase ^= 1u;
+            return __all_sync(0xffffffffu, r);
+        };
+        const int64_t row0 = ((int64_t)b * H + h0) * T + (int64_t)c * L;   // head h0, chunk c
+        constexpr int KPT = L / kConvThreads;                  // keys per thread (at most)
+        float pc[KPT], pd[KPT], plast = 0.f, pD = 0.f;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) { pc[i] = 0.f; pd[i] = 0.f; }
+        auto prefetch = [&](int hh) {
+            const float* crow = cum2 + row0 + (int64_t)hh * T;
+            const float* drow = dtT + row0 + (int64_t)hh * T;
+            plast = __ldg(crow + Lc - 1);
+#pragma unroll
+            for (int i = 0; i < KPT; ++i) {
+                const int s = ctid + kConvThreads * i;
+                if (s < KS && s < Lc) {
+                    pc[i] = __ldg(crow + s);
+                    pd[i] = __ldg(drow + s);
+                }
+            }
+            pD = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
+        };
+        if (nh > 0) prefetch(0);
+        // The C.B^T bound comes from the epilogue (after GEMM1); by then every
+        // C.B^T block item of the ring has landed, so only head items remain.
+        bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cbinfo, 0, abort, kWaitNs));
+        const float cbmax = bars.cbmax;
+        for (int hi = 0; hi < nh && ok; ++hi) {
+            const int it = NA + hi, st = it % NS, k = it / NS;
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
+            if (!ok) break;
+            float* ck = cumv + st * 256;
+            float* dk = dtv + st * 256;
+            float dloc = 0.f;
+#pragma unroll
+            for (int i = 0; i < KPT; ++i) {
+                const int s = ctid + kConvThreads * i;
+                if (s < KS) {
+                    const bool in = s < Lc;
+                    ck[s] = in ? pc[i] : plast;
+                    dk[s] = in ? pd[i] : 0.f;
+                    if (in) dloc = fmaxf(dloc, pd[i]);
+                }
+            }
+            const float dval = pD;
+            if (hi + 1 < nh) prefetch(hi + 1);
+            uint8_t* xs = sStage + st * C::STAGE;
+            const int nch = KS * 8 / kConvThreads;
+            __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll 8
+            for (int i = 0; i < nch; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(xs + (ctid + kConvThreads * i) * 16);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t a = w4[e] & 0x7fff7fffu;   // |x|, two at a time
+                    xm2 = __hmax2(xm2, *reinterpret_cast<const __nv_bfloat162*>(&a));
+                }
+            }
+            const uint32_t xm2u = *reinterpret_cast<const uint32_t*>(&xm2);
+            const uint32_t xmax = __reduce_max_sync(0xffffffffu, max(xm2u & 0xffffu, xm2u >> 16));
+            const uint32_t dmax = __reduce_max_sync(0xffffffffu, __float_as_uint(dloc));
+            if (lane == 0) {
+                red_x[(st * kConvWarps + cw) * 2 + 0] = xmax;
+                red_x[(st * kConvWarps + cw) * 2 + 1] = dmax;
+            }
+            if (!(ok = conv_sync())) break;
+            const uint32_t gx = __reduce_max_sync(
+                0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 0] : 0u);
+            const uint32_t gd = __reduce_max_sync(
+                0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 1] : 0u);
+            const bool use16 = cbmax <= 32768.f && gx <= kF16Limit &&
+                               cbmax * __uint_as_float(gd) <= 32768.f;
+            if (use16) {
+#pragma unroll 8
+                for (int i = 0; i < nch; ++i) {
+                    uint4* p = reinterpret_cast<uint4*>(xs + (ctid + kConvThreads * i) * 16);
+                    const uint4 v = *p;
+                    *p = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                    bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                }
+                fence_proxy_async_smem();
+            }
+            if (ctid == 0) {
+                bars.use16s[st] = use16 ? 1 : 0;
+                bars.dvals[st] = dval;
+            }
+            mbar_arrive(&bars.xready[st]);
+        }
     }
 
     tc_fence_before();
