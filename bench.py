@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiler captures)")
     return ap.parse_args()
 
 
@@ -253,6 +255,8 @@ def config_of(w, n):
 def main():
     args = parse_args()
     w = workload(args.workload)
+    if args.batch > 0:
+        w = w.scaled(batch=args.batch, name=w.name.replace(f" b{w.batch} ", f" b{args.batch} "))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -16,24 +16,27 @@
 // the B/C group:
 //   y[t,:] = sum_s M[t,s] x[s,:] + exp2(cum2_t) (C_t . Sprev_c^T) + D_h x[t,:]
 //   M[t,s] = (C_t . B_s) * exp2(cum2_t - cum2_s) * dt_s  for s <= t, else 0.
-// Tensor-memory plan (512 columns, fp32 unless noted):
-//   [0, KS)         CB = C_tile . B_keys^T      (GEMM1, once per CTA: C.B^T does
-//                                               not depend on the head)
-//   [256, 256+KS/2) M as 16-bit pairs, MMA operand A of GEMM2, in two K-halves
+// Tensor-memory plan (512 columns):
+//   [0, KS/2)       CB = C_tile . B_keys^T as 16-bit pairs (GEMM1 once per CTA,
+//                   in fp32 into [256, 256+KS), then packed by the epilogue:
+//                   C.B^T does not depend on the head)
+//   [128, 128+KS/2) M as 16-bit pairs, MMA operand A of GEMM2, in two K-halves
 //                   (written by the epilogue warps with tcgen05.st)
-//   [384, 512)      two 64-column accumulators, one per head in flight
-// Per head: GEMM3 acc = C . Sprev^T (A = C tile, B = Sprev, both K-major in
-// shared memory); the epilogue rescales each accumulator row t by
-// exp2(cum2_t) in tensor memory and builds M from CB: the causal mask comes
+//   [256, 384)      S: two 64-column fp32 accumulators of C . Sprev^T
+//   [384, 512)      G: two 64-column fp32 accumulators of M . X
+// Per head: GEMM3 S = C . Sprev^T (A = C tile, B = Sprev, both K-major in
+// shared memory); the epilogue builds M from CB: the causal mask comes
 // from the row/column indices and is applied before exp2; below the warp's
 // diagonal 32x32 block the decay is split as
 // exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the warp's first row, so
 // both factors are <= 1 and only the diagonal block needs one exp2 per
 // element; on the fp16 path the two multiplies of a below-diagonal entry are
-// packed fp16 multiplies, two keys per instruction.  GEMM2 acc += M . X in two K-halves (A from tensor memory, X
-// MN-major in shared memory), so that the tensor core works on one half while
-// the epilogue builds the other.  The epilogue adds D_h x_t, rounds to bf16
-// and stores its 32x32 piece of the tile with a TMA store (rows past the
+// packed fp16 multiplies, two keys per instruction.  GEMM2 G = M . X in two
+// K-halves (A from tensor memory, X MN-major in shared memory), so that the
+// tensor core works on one half while
+// the epilogue builds the other.  Once the next head's M is handed over, the
+// epilogue finishes the previous head: y = exp2(cum2_t) S + G + D_h x_t,
+// rounded to bf16, its 32x32 piece stored with a TMA store (rows past the
 // sequence end are clipped by the tensor map).
 //
 // Precision of GEMM2.  M and X enter GEMM2 as fp16 (10-bit mantissa) rather
@@ -72,7 +75,10 @@ constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 constexpr int PC = 64 / EG;                   // y columns per epilogue group
 static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread");
-constexpr uint32_t COL_CB = 0, COL_MM = 256, COL_ACC = 384;
+// Tensor-memory columns: C.B^T as 16-bit pairs, M as 16-bit pairs, and two
+// double-buffered fp32 accumulators (carried-state term S, intra-chunk term G).
+// GEMM1 writes C.B^T in fp32 to [COL_S, COL_S + KS) before any S is live.
+constexpr uint32_t COL_CB = 0, COL_MM = 128, COL_S = 256, COL_G = 384, COL_CB32 = COL_S;
 constexpr uint32_t kF16Limit = 0x4700u;       // bf16 bit pattern of 2^15
 
 template <int L, int NA>   // NA = N / 64
@@ -97,7 +103,8 @@ struct K4Cfg {
 struct K4Bars {
     uint64_t full[3], xfree[3];
     uint64_t cb_full;
-    uint64_t s3_done[2], acc_full[2], acc_empty[2];
+    uint64_t cb_packed;     // C.B^T packed to 16 bits (fp32 copy may be overwritten)
+    uint64_t acc_full[2], acc_empty[2];
     uint64_t mm_ready[2], mm_free[2];   // per K-half of M
     uint64_t epi_sync;      // group barrier of the epilogue warps (abortable, unlike bar.sync)
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
@@ -160,8 +167,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             mbar_init(&bars.xfree[i], 1);
         }
         mbar_init(&bars.cb_full, 1);
+        mbar_init(&bars.cb_packed, kEpiThreads);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars.s3_done[i], 1);
             mbar_init(&bars.acc_full[i], 1);
             mbar_init(&bars.acc_empty[i], kEpiThreads);
             mbar_init(&bars.mm_ready[i], kEpiThreads);
@@ -240,12 +247,17 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t ad = smem_desc_sw128(c_addr + it * 16384 + kk * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(x_addr + kk * 32, 16, 1024);
-                    mma_ss(tmem + COL_CB, ad, bd, id_cb, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ss(tmem + COL_CB32, ad, bd, id_cb, (it > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(&bars.xfree[st]);
                 if (it == NA - 1) mma_commit(&bars.cb_full);
             }
-            // GEMM3 of head hh: acc[hh & 1] = C . Sprev_hh^T.
+            // The fp32 C.B^T is overwritten by GEMM3: wait until the epilogue packed it.
+            if (ok) {
+                ok = mbar_wait_or_abort(&bars.cb_packed, 0, abort, kWaitNs);
+                tc_fence_after();
+            }
+            // GEMM3 of head hh: S[hh & 1] = C . Sprev_hh^T.
             auto gemm3 = [&](int hh) -> bool {
                 const int it = NA + hh, st = it % NS, k = it / NS, ab = hh & 1, ka = hh >> 1;
                 if (!mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs)) return false;
@@ -256,19 +268,17 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 for (int kk = 0; kk < N / 16; ++kk) {
                     const uint64_t ad = smem_desc_sw128(c_addr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(s_addr + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + COL_ACC + 64 * ab, ad, bd, id_s3, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + COL_S + 64 * ab, ad, bd, id_s3, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bars.s3_done[ab]);
                 return true;
             };
             if (ok && nh > 0) ok = gemm3(0);
-            // Per head: GEMM3 of the next head goes first, so that the epilogue's
-            // rescale of head hi+1 never waits behind this head's GEMM2.
+            // Per head: GEMM2 as soon as the epilogue has M, then GEMM3 of the next
+            // head (its S buffer frees up when the epilogue finished head hi-1).
             for (int hi = 0; hi < nh && ok; ++hi) {
-                if (hi + 1 < nh && !(ok = gemm3(hi + 1))) break;
                 const int it = NA + hi, st = it % NS, ab = hi & 1;
                 const uint32_t x_addr = smem_u32(sStage + st * C::STAGE);
-                const uint32_t acc = tmem + COL_ACC + 64 * ab;
+                const uint32_t acc = tmem + COL_G + 64 * ab;
                 for (int half = 0; half < 2 && ok; ++half) {   // GEMM2: acc += M . X
                     if (!(ok = mbar_wait_or_abort(&bars.mm_ready[half], hi & 1, abort, kWaitNs))) break;
                     tc_fence_after();
@@ -277,13 +287,14 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const int k0 = half * (KS / 32);
                     for (int kk = k0; kk < k0 + KS / 32; ++kk) {
                         const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::X_BYTES, 1024);
-                        mma_ts(acc, tmem + COL_MM + 8 * kk, bd, id_s2, 1u);
+                        mma_ts(acc, tmem + COL_MM + 8 * kk, bd, id_s2, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(&bars.mm_free[half]);
                 }
                 if (!ok) break;
                 mma_commit(&bars.acc_full[ab]);
                 mma_commit(&bars.xfree[st]);
+                if (hi + 1 < nh && !(ok = gemm3(hi + 1))) break;
             }
             if (*abort) {   // nothing may be in flight when TMEM is freed
                 mma_commit(&bars.drain);
@@ -325,7 +336,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         if (ok) {
             for (int j = grp; j <= jd; j += EG) {
                 uint32_t r[32];
-                tmem_ld32_sync(tmem + lane_off + COL_CB + 32 * j, r);
+                tmem_ld32_sync(tmem + lane_off + COL_CB32 + 32 * j, r);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) cbmax = fmaxf(cbmax, fabsf(__uint_as_float(r[e])));
             }
@@ -340,9 +351,27 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 mbar_arrive(&bars.cbinfo);
             }
         }
+        // Pack C.B^T to 16-bit pairs: fp16 when it fits (every head may then take
+        // the fp16 path), else bf16 (no head takes the fp16 path).
+        const bool cb16 = cbmax <= 32768.f;
+        if (ok) {
+            for (int j = grp; j <= jd; j += EG) {
+                uint32_t r[32];
+                tmem_ld32_sync(tmem + lane_off + COL_CB32 + 32 * j, r);
+                uint32_t p[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    p[e] = cb16 ? pack_f16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]))
+                                : pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+                tmem_st16(tmem + lane_off + COL_CB + 16 * j, p);
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars.cb_packed);
 
         uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
-        float d_prev = 0.f, d_cur = 0.f;
+        float d_prev = 0.f, d_cur = 0.f, e_prev = 0.f;
         bool x16_prev = false, x16_cur = false;
         // finish(hp): y rows of head hp = acc + D x, bf16, TMA-stored per warp.
         auto finish = [&](int hp) -> bool {
@@ -351,8 +380,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                             mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
                 return false;
             tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32_sync(tmem + lane_off + COL_ACC + 64 * pb + grp * PC, r);
+            uint32_t r[32], rs[32];
+            tmem_ld32(tmem + lane_off + COL_S + 64 * pb + grp * PC, rs);
+            tmem_ld32(tmem + lane_off + COL_G + 64 * pb + grp * PC, r);
+            tmem_wait_ld_regs(rs);
+            tmem_wait_ld_regs(r);
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[pb]);
             uint32_t yv[PC / 2];
@@ -368,8 +400,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     x0 = __uint_as_float(xw << 16);
                     x1 = __uint_as_float(xw & 0xffff0000u);
                 }
-                yv[e] = pack_bf16x2(__uint_as_float(r[2 * e]) + d_prev * x0,
-                                    __uint_as_float(r[2 * e + 1]) + d_prev * x1);
+                yv[e] = pack_bf16x2(
+                    fmaf(e_prev, __uint_as_float(rs[2 * e]), __uint_as_float(r[2 * e])) + d_prev * x0,
+                    fmaf(e_prev, __uint_as_float(rs[2 * e + 1]), __uint_as_float(r[2 * e + 1])) + d_prev * x1);
             }
             // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
             // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
@@ -389,7 +422,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             return true;
         };
         for (int hi = 0; hi < nh && ok; ++hi) {
-            const int it = NA + hi, st = it % NS, ab = hi & 1;
+            const int it = NA + hi, st = it % NS;
             // ---- x tile, decay vectors and range decision come from the converters
             // (phase of xready[st]: one per head item of that stage).
             ok = __all_sync(0xffffffffu,
@@ -424,26 +457,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             __syncwarp();
             const __half2 u2 = __float2half2_rn(u_t);
 
-            // ---- previous head's output while this head's GEMM3 completes.
-            if (hi > 0 && !(ok = finish(hi - 1))) break;
-#pragma unroll
-            for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
-            d_prev = d_cur;
-            x16_prev = x16_cur;
-
-            // ---- rescale the carried-state accumulator row by exp2(cum2_t).
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_or_abort(&bars.s3_done[ab], (hi >> 1) & 1, abort, kWaitNs));
-            if (!ok) break;
-            tc_fence_after();
-            {
-                const uint32_t a = tmem + lane_off + COL_ACC + 64 * ab + grp * PC;
-                uint32_t r[32];
-                tmem_ld32_sync(a, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * e_t);
-                tmem_st32(a, r);
-            }
             // ---- M, in two K-halves.
             for (int half = 0; half < 2 && ok; ++half) {
                 // The half's M columns are free once the previous head's GEMM2 half completed.
@@ -455,8 +468,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
                 const int jlo = half * hblkn, jhi = min(jd, jlo + hblkn - 1);
                 int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own block >= jlo
-                uint32_t r[32];
-                if (j <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * j, r);
+                uint32_t r[16];
+                if (j <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * j, r);
                 for (; j <= jhi; j += EG) {
                     tmem_wait_ld_regs(r);
                     uint32_t m[16];
@@ -468,25 +481,36 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                             const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                             for (int k2 = 0; k2 < 4; ++k2) {
-                                const int e = 8 * e8 + 2 * k2;
-                                const __half2 cb2 = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                                const __half2 cb2 = *reinterpret_cast<const __half2*>(&r[4 * e8 + k2]);
                                 const __half2 uv = __hmul2(u2, *reinterpret_cast<const __half2*>(&vw[k2]));
                                 const __half2 mm2 = __hmul2(cb2, uv);
                                 m[4 * e8 + k2] = *reinterpret_cast<const uint32_t*>(&mm2);
                             }
                         }
-                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
+                        if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
                     } else {
+                        float cbv[32];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            if (cb16) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r[e]));
+                                cbv[2 * e] = f.x;
+                                cbv[2 * e + 1] = f.y;
+                            } else {
+                                cbv[2 * e] = __uint_as_float(r[e] << 16);
+                                cbv[2 * e + 1] = __uint_as_float(r[e] & 0xffff0000u);
+                            }
+                        }
                         float mv[32];
                         if (j < jd) {
                             const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
 #pragma unroll
                             for (int e4 = 0; e4 < 8; ++e4) {
                                 const float4 v = v4[e4];
-                                mv[4 * e4 + 0] = __uint_as_float(r[4 * e4 + 0]) * (u_t * v.x);
-                                mv[4 * e4 + 1] = __uint_as_float(r[4 * e4 + 1]) * (u_t * v.y);
-                                mv[4 * e4 + 2] = __uint_as_float(r[4 * e4 + 2]) * (u_t * v.z);
-                                mv[4 * e4 + 3] = __uint_as_float(r[4 * e4 + 3]) * (u_t * v.w);
+                                mv[4 * e4 + 0] = cbv[4 * e4 + 0] * (u_t * v.x);
+                                mv[4 * e4 + 1] = cbv[4 * e4 + 1] * (u_t * v.y);
+                                mv[4 * e4 + 2] = cbv[4 * e4 + 2] * (u_t * v.z);
+                                mv[4 * e4 + 3] = cbv[4 * e4 + 3] * (u_t * v.w);
                             }
                         } else {
                             const float4* c4 = reinterpret_cast<const float4*>(ck + 32 * j);
@@ -499,11 +523,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
                                 for (int u = 0; u < 4; ++u) {
                                     const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
-                                    mv[e] = e <= lane ? __uint_as_float(r[e]) * ex2(ct - cs[u]) * ds[u] : 0.f;
+                                    mv[e] = e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f;
                                 }
                             }
                         }
-                        if (j + EG <= jhi) tmem_ld32(tmem + lane_off + COL_CB + 32 * (j + EG), r);
+                        if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
                         if (use16) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) m[e] = pack_f16x2(mv[2 * e], mv[2 * e + 1]);
@@ -518,6 +542,14 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 tc_fence_before();
                 mbar_arrive(&bars.mm_ready[half]);
             }
+            if (!ok) break;
+            // ---- previous head's output while the tensor core works on this one.
+            if (hi > 0 && !(ok = finish(hi - 1))) break;
+#pragma unroll
+            for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
+            d_prev = d_cur;
+            e_prev = e_t;
+            x16_prev = x16_cur;
         }
         if (ok && nh > 0) ok = finish(nh - 1);
         if (lane == 0) bulk_wait<0>();
