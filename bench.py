@@ -40,7 +40,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSD fwd tokens/s & TFLOP/s at Mamba-2 2.7B shape; % of roofline on 1 GB300"
-KERNELS = ("chunk_cumsum", "chunk_state", "state_pass", "chunk_out")
+KERNELS_FUSED = ("chunk_cumsum", "chunk_state_pass", "chunk_out")
+KERNELS_SPLIT = ("chunk_cumsum", "chunk_state", "state_pass", "chunk_out")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -55,6 +56,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused-state", action="store_true",
+                    help="time stages 2+3 as the one fused kernel (mamba2_ssd_chunk_state_pass)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiler captures)")
     return ap.parse_args()
@@ -82,6 +85,11 @@ def model(w):
                             flops=2 * th * P * N),
         "state_pass": dict(bytes=4 * st + E * st + 4 * b * H * P * N * (1 + init) + 4 * b * H * nc,
                            flops=0),
+        # stages 2+3 in one kernel: no dS round trip (the carried state moves
+        # between CTAs through L2 and is not counted)
+        "chunk_state_pass": dict(bytes=th * (P * E + 8) + b * T * G * N * E + E * st +
+                                 4 * b * H * P * N * (1 + init),
+                                 flops=2 * th * P * N),
         "chunk_out": dict(bytes=th * (2 * P * E + 8) + 2 * b * T * G * N * E + E * st + 4 * H,
                           flops=b * T * (H * (2 * P * N + P * (L + 1)) + G * N * (L + 1))),
     }
@@ -284,7 +292,13 @@ def main():
     f32 = dict(dtype=torch.float32, device="cuda")
     cum2 = torch.empty((b, H, T), **f32)
     dtT = torch.empty((b, H, T), **f32)
-    dS = torch.empty((b, nc, H, P, N), **f32)
+    fused = args.fused_state and m2.chunk_state_pass_workspace_size(sh) > 0
+    KERNELS = KERNELS_FUSED if fused else KERNELS_SPLIT
+    if fused:
+        dS = None
+        sp_ws = torch.empty(m2.chunk_state_pass_workspace_size(sh), dtype=torch.uint8, device="cuda")
+    else:
+        dS = torch.empty((b, nc, H, P, N), **f32)
     Sprev = torch.empty((b, nc, H, P, N), dtype=w.torch_dtype, device="cuda")
     y = torch.empty((b, T, H, P), dtype=w.torch_dtype, device="cuda")
     fin = torch.empty((b, H, P, N), **f32)
@@ -296,12 +310,16 @@ def main():
         m2.chunk_cumsum(sh, dev["dt"], dev["A"], cum2, dtT, stream)
         if ev is not None:
             ev[1].record(stream)
-        m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS, stream)
+        if fused:
+            m2.chunk_state_pass(sh, dev["x"], dev["B"], cum2, dtT, dev["initial_state"], Sprev, fin,
+                                sp_ws, stream)
+        else:
+            m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS, stream)
+            if ev is not None:
+                ev[2].record(stream)
+            m2.state_pass(sh, dS, cum2, dev["initial_state"], Sprev, fin, stream)
         if ev is not None:
-            ev[2].record(stream)
-        m2.state_pass(sh, dS, cum2, dev["initial_state"], Sprev, fin, stream)
-        if ev is not None:
-            ev[3].record(stream)
+            ev[len(KERNELS) - 1].record(stream)
         m2.chunk_out(sh, dev["x"], dev["B"], dev["C"], cum2, dtT, Sprev, dev["D"], y, stream)
 
     for _ in range(max(3, args.warmup)):
@@ -311,7 +329,7 @@ def main():
         raise RuntimeError("device-side error during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS))] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -343,7 +361,7 @@ def main():
     for i in range(K):
         e = evs[i]
         nxt = evs[i + 1][0] if i + 1 < K else t_end
-        marks = [e[0], e[1], e[2], e[3], nxt]
+        marks = list(e) + [nxt]
         for j, kname in enumerate(KERNELS):
             per[kname] += marks[j].elapsed_time(marks[j + 1])
     per = {k: v / K for k, v in per.items()}
@@ -382,6 +400,32 @@ def main():
         kernels[kname] = {"ms": per[kname], "GB/s": km["bytes"] / tk / 1e9,
                           "TFLOP/s": km["flops"] / tk / 1e12,
                           "hbm_frac": km["bytes"] / tk / 1e9 / pk["hbm_gbs"]}
+
+    # The same work through the whole-path call (mamba2_ssd_fwd), inputs
+    # resident (with --fused-state, stage 1 there clears the fused kernel's words).
+    fwd_ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
+
+    def fwd_step():
+        m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                   dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
+                   y=y, final_state=fin, workspace=fwd_ws, stream=stream,
+                   flags=m2.FLAG_FUSED_STATE if fused else 0)
+
+    for _ in range(3):
+        fwd_step()
+    torch.cuda.synchronize()
+    kf = min(K, 50)
+    fa, fz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fa.record(stream)
+    for _ in range(kf):
+        fwd_step()
+    fz.record(stream)
+    torch.cuda.synchronize()
+    if m2.device_error() != 0:
+        raise RuntimeError("device-side error in the whole-path call")
+    fwd_call = {"ms_per_step": fa.elapsed_time(fz) / kf, "steps": kf,
+                "launches_per_step": 3 if fused else 4}
+    del fwd_ws
 
     # End to end through ssd_fwd with pinned host buffers.
     e2e = None
@@ -439,7 +483,7 @@ def main():
             "tflops": flops * world / (ms_step * 1e-3) / 1e12,
             "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
             "path": "tcgen05" if m2.path(sh) == m2.PATH_TCGEN05 else "simt",
-            "gpu_launches": 4 * K, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+            "gpu_launches": len(KERNELS) * K, "fwd_call": fwd_call, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if dist:

@@ -80,6 +80,11 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
 /* Force the CUDA-core (SIMT) chunk-state and chunk-output kernels even where
  * the tcgen05 tensor-core kernels apply (cross-checks and debugging). */
 #define MAMBA2_FLAG_FORCE_SIMT 1
+/* In mamba2_ssd_fwd on the tensor-core path, run stages 2 and 3 as the one
+ * fused kernel of mamba2_ssd_chunk_state_pass instead of two kernels with dS in
+ * HBM.  Same results bit for bit; slower on GB300 at the 2.7B layer shape
+ * (0.317 ms against 0.243 ms for the pair), so it is not the default. */
+#define MAMBA2_FLAG_FUSED_STATE 2
 
 /* Shape of one call.  Supported set:
  *   batch, seqlen, nheads >= 0 (a zero batch or head count is a no-op; seqlen 0
@@ -88,7 +93,7 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  *   ngroups G >= 1 with nheads % G == 0; chunk_size L in {64, 128, 256};
  *   seqlen need not be a multiple of L (the last chunk is shorter).
  * The tensor-core path is used for dtype BF16 with L in {128, 256},
- * P in {64, 128} and N in {64, 128, 256}; every other supported shape runs on
+ * P = 64 and N in {64, 128, 256}; every other supported shape runs on
  * the CUDA-core kernels (mamba2_ssd_path reports which). */
 typedef struct mamba2_ssd_shape {
     int64_t batch;
@@ -117,7 +122,9 @@ MAMBA2_API int32_t mamba2_ssd_path(const mamba2_ssd_shape* shape);
  * 256-byte aligned.  0 for an invalid shape.  Host-only. */
 MAMBA2_API size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape);
 
-/* The whole forward pass: the four stages below, in order, on `stream`.
+/* The whole forward pass: the four stages below, in order, on `stream`
+ * (stages 2 and 3 as one kernel with MAMBA2_FLAG_FUSED_STATE, tensor-core path,
+ * three or more chunks).
  *   workspace: device buffer of at least mamba2_ssd_workspace_size(shape)
  *   bytes, 256-byte aligned, owned by the caller, contents ignored on entry.
  * Returns MAMBA2_OK once the launches are queued. */
@@ -153,6 +160,28 @@ MAMBA2_API mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape,
                                     const float* dS, const float* cum2,
                                     const float* initial_state,
                                     void* Sprev, float* final_state, void* stream);
+
+/* Stages 2 and 3 fused (tensor-core path only) [P3 section 8: fwd_pass_state
+ * walks the chunks in order, combining the decayed carried state with each
+ * chunk's own contribution]: Sprev and final_state exactly as
+ * mamba2_ssd_chunk_state followed by mamba2_ssd_state_pass compute them (same
+ * fp32 operations in the same order), without writing dS.  Each chunk's CTA
+ * computes dS_c on the tensor cores and takes the state entering its chunk
+ * from the CTA of the previous chunk.
+ *   workspace: mamba2_ssd_chunk_state_pass_workspace_size(shape) bytes,
+ *   256-byte aligned, owned by the caller: a two-slot fp32 ring of states per
+ *   (b, h) and the synchronisation words, which the call clears on `stream`
+ *   first.  Calls sharing one workspace must not overlap on the GPU.
+ * Shapes without the tensor-core path (mamba2_ssd_path) return
+ * MAMBA2_ERR_UNSUPPORTED; they run mamba2_ssd_chunk_state + _state_pass. */
+MAMBA2_API size_t mamba2_ssd_chunk_state_pass_workspace_size(const mamba2_ssd_shape* shape);
+MAMBA2_API mamba2_status mamba2_ssd_chunk_state_pass(const mamba2_ssd_shape* shape,
+                                          const void* x, const void* B,
+                                          const float* cum2, const float* dtT,
+                                          const float* initial_state,
+                                          void* Sprev, float* final_state,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* stream);
 
 /* Stage 4, fused output [P3 sections 9, 11; P2 "세 가지 핵심 커널 구현", compute_out]:
  *   y[t,p] = sum_{s<=t in chunk} (C_t . B_s) exp2(cum2_t - cum2_s) dtT_s x[s,p]

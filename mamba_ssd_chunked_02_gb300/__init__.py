@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmamba2_ssd.so")
 
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
+FLAG_FUSED_STATE = 2
 PATH_SIMT, PATH_TCGEN05 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = range(6)
 
@@ -37,7 +38,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = rang
 SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_size",
            "mamba2_ssd_fwd", "mamba2_ssd_chunk_cumsum", "mamba2_ssd_chunk_state",
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
-           "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc")
+           "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
+           "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size")
 
 
 class Shape(ctypes.Structure):
@@ -99,6 +101,10 @@ def load():
         lib.mamba2_ssd_version.restype = ctypes.c_char_p
         lib.mamba2_ssd_fwd_noalloc.argtypes = [sp] + [vp] * 9 + [vp]
         lib.mamba2_ssd_fwd_noalloc.restype = ctypes.c_int
+        lib.mamba2_ssd_chunk_state_pass_workspace_size.argtypes = [sp]
+        lib.mamba2_ssd_chunk_state_pass_workspace_size.restype = ctypes.c_size_t
+        lib.mamba2_ssd_chunk_state_pass.argtypes = [sp] + [vp] * 7 + [vp, ctypes.c_size_t, vp]
+        lib.mamba2_ssd_chunk_state_pass.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -239,6 +245,30 @@ def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
         _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
         _ptr(Sprev, "Sprev", _io_dtype(shape), (b, nc, H, P, N)),
         _ptr(final_state, "final_state", torch.float32, (b, H, P, N)), _stream(stream)))
+
+
+def chunk_state_pass_workspace_size(shape: Shape) -> int:
+    return int(load().mamba2_ssd_chunk_state_pass_workspace_size(ctypes.byref(shape)))
+
+
+def chunk_state_pass(shape, x, B, cum2, dtT, initial_state, Sprev, final_state, workspace,
+                     stream=None):
+    """Stages 2+3 fused (mamba2_ssd_chunk_state_pass, tensor-core shapes only):
+    Sprev [b,nc,H,P,N] and final_state [b,H,P,N] without dS.  `workspace` is a
+    uint8 device tensor of chunk_state_pass_workspace_size(shape) bytes."""
+    b, T, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
+                        shape.ngroups)
+    io = _io_dtype(shape)
+    nc = shape.nchunks
+    _check("mamba2_ssd_chunk_state_pass", load().mamba2_ssd_chunk_state_pass(
+        ctypes.byref(shape), _ptr(x, "x", io, (b, T, H, P)), _ptr(B, "B", io, (b, T, G, N)),
+        _ptr(cum2, "cum2", torch.float32, (b, H, T)), _ptr(dtT, "dtT", torch.float32, (b, H, T)),
+        _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
+        _ptr(Sprev, "Sprev", io, (b, nc, H, P, N)),
+        _ptr(final_state, "final_state", torch.float32, (b, H, P, N)),
+        _ptr(workspace, "workspace", optional=True),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
+        _stream(stream)))
 
 
 def chunk_out(shape, x, B, C, cum2, dtT, Sprev, D, y, stream=None):

@@ -53,7 +53,7 @@ mamba2_status check(const mamba2_ssd_shape* s) {
     if (s->headdim <= 0 || s->dstate <= 0 || s->ngroups <= 0 || s->chunk_size <= 0)
         return MAMBA2_ERR_INVALID_ARG;
     if (s->dtype != MAMBA2_F32 && s->dtype != MAMBA2_BF16) return MAMBA2_ERR_INVALID_ARG;
-    if (s->flags & ~MAMBA2_FLAG_FORCE_SIMT) return MAMBA2_ERR_INVALID_ARG;
+    if (s->flags & ~(MAMBA2_FLAG_FORCE_SIMT | MAMBA2_FLAG_FUSED_STATE)) return MAMBA2_ERR_INVALID_ARG;
     if (s->nheads % s->ngroups != 0) return MAMBA2_ERR_INVALID_ARG;
     if (!in_set(s->headdim, {16, 32, 64, 128})) return MAMBA2_ERR_UNSUPPORTED;
     if (!in_set(s->dstate, {16, 32, 64, 128, 256})) return MAMBA2_ERR_UNSUPPORTED;
@@ -159,6 +159,47 @@ mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape, const float* 
                                            error_word(), static_cast<cudaStream_t>(stream)));
 }
 
+size_t mamba2_ssd_chunk_state_pass_workspace_size(const mamba2_ssd_shape* shape) {
+    if (check(shape) != MAMBA2_OK) return 0;
+    const Dims d = dims_of(shape);
+    if (!use_tc(shape, d)) return 0;
+    return align256(2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)) +
+           align256(sizeof(int32_t) * (size_t)(m2::fused_flag_words(d) + 1));
+}
+
+mamba2_status mamba2_ssd_chunk_state_pass(const mamba2_ssd_shape* shape, const void* x,
+                                          const void* B, const float* cum2, const float* dtT,
+                                          const float* initial_state, void* Sprev,
+                                          float* final_state, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    if (!use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
+    const bool empty = d.b * d.T * d.H == 0;
+    if (!req(x, empty) || !req(B, empty) || !req(cum2, empty) || !req(dtT, empty) ||
+        !opt(initial_state) || !req(Sprev, empty) || !req(final_state, d.b * d.H == 0))
+        return MAMBA2_ERR_INVALID_ARG;
+    if (d.b * d.H == 0) return MAMBA2_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d.T == 0)
+        return from_cuda(m2::launch_state_pass(d, nullptr, nullptr, initial_state, nullptr,
+                                               final_state, error_word(), s));
+    const size_t ring = align256(2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
+    const size_t nflag = (size_t)m2::fused_flag_words(d);
+    if (!workspace || workspace_bytes < mamba2_ssd_chunk_state_pass_workspace_size(shape) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return MAMBA2_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    int32_t* flags = reinterpret_cast<int32_t*>(ws + ring);
+    cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(int32_t) * (nflag + 1), s);
+    if (e == cudaSuccess)
+        e = m2::launch_chunk_state_pass_tc(d, x, B, cum2, dtT, initial_state,
+                                           reinterpret_cast<float*>(ws), flags, flags + nflag,
+                                           Sprev, final_state, error_word(), s);
+    return from_cuda(e);
+}
+
 mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape, const void* x, const void* B,
                                    const void* C, const float* cum2, const float* dtT,
                                    const void* Sprev, const float* D, void* y, void* stream) {
@@ -203,12 +244,28 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
     float* dS = reinterpret_cast<float*>(ws + cv.dS);
     void* Sprev = ws + cv.Sprev;
     const bool tc = use_tc(shape, d);
+    // Fused stages 2+3 (opt-in): the two-slot carried-state ring, the flag words
+    // and the ticket live in the dS region, which holds them from three chunks on.
+    const size_t ring = 2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N);
+    const size_t nflag = tc ? (size_t)m2::fused_flag_words(d) : 0;
+    const bool fuse = tc && d.nc >= 3 && (shape->flags & MAMBA2_FLAG_FUSED_STATE) &&
+                      ring + sizeof(int32_t) * (nflag + 1) <= cv.Sprev - cv.dS;
+    int32_t* flags = reinterpret_cast<int32_t*>(ws + cv.dS + ring);
 
-    cudaError_t e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
-    if (e == cudaSuccess)
-        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, err, s)
-               : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
-    if (e == cudaSuccess) e = m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state, err, s);
+    cudaError_t e = fuse ? m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s, flags,
+                                                   (int64_t)nflag + 1)
+                         : m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+    if (fuse) {
+        if (e == cudaSuccess)
+            e = m2::launch_chunk_state_pass_tc(d, x, B, cum2, dtT, initial_state, dS, flags,
+                                               flags + nflag, Sprev, final_state, err, s);
+    } else {
+        if (e == cudaSuccess)
+            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, err, s)
+                   : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
+        if (e == cudaSuccess)
+            e = m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state, err, s);
+    }
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s)
                : m2::launch_chunk_out_simt(d, x, B, C, cum2, dtT, Sprev, D, y, err, s);

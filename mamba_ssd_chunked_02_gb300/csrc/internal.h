@@ -18,9 +18,12 @@ inline int64_t n_cum(const Dims& d) { return d.b * d.H * d.T; }
 inline int64_t n_state(const Dims& d) { return d.b * d.nc * d.H * d.P * d.N; }
 inline int64_t esize(const Dims& d) { return d.dtype == 1 ? 2 : 4; }
 
-// Stage 1: chunk-local log2-scaled cumsum + [b,h,t] transpose of dt.
+// Stage 1: chunk-local log2-scaled cumsum + [b,h,t] transpose of dt.  When
+// `zero` is given, the kernel also sets zero[0 .. nzero) to 0 (the ticket and
+// flag words of the fused stage 2+3 kernel that follows on the same stream).
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, float* cum2,
-                                float* dtT, int32_t* err, cudaStream_t st);
+                                float* dtT, int32_t* err, cudaStream_t st,
+                                int32_t* zero = nullptr, int64_t nzero = 0);
 
 // Stage 2: chunk states.  CUDA-core variant (any supported shape / dtype).
 cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
@@ -30,6 +33,21 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,
                                   const float* cum2, const float* dtT, float* dS,
                                   int32_t* err, cudaStream_t st);
+
+// Stages 2 and 3 fused (tcgen05, bf16, tc_supported() shapes): each CTA
+// computes its chunk's dS in tensor memory, then, head by head, takes the state
+// entering its chunk from the CTA of the previous chunk (a two-slot ring `carry`
+// [2][b][H][P][N] fp32 and one flag per (b, h, n-tile, chunk)), writes Sprev
+// (bf16) and passes decay * Sprev + dS on (or writes final_state).  CTAs take
+// their work item from `ticket` in chunk order, so a CTA only waits for CTAs
+// that started before it.  flags[0 .. fused_flag_words(d)) and *ticket must be
+// zero at launch.
+int64_t fused_flag_words(const Dims& d);
+cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void* B,
+                                       const float* cum2, const float* dtT, const float* init,
+                                       float* carry, int32_t* flags, int32_t* ticket,
+                                       void* Sprev, float* final_state, int32_t* err,
+                                       cudaStream_t st);
 
 // Stage 3: sequential state pass over chunks.
 cudaError_t launch_state_pass(const Dims& d, const float* dS, const float* cum2,
@@ -53,6 +71,7 @@ enum : int32_t {
     kErrTimeoutK2 = 1 << 0,    // a bounded wait ran out in the tcgen05 chunk-state kernel
     kErrTimeoutK4 = 1 << 1,    // ... in the tcgen05 chunk-output kernel
     kErrLaunchCfg = 1 << 2,    // a kernel saw a launch configuration it does not support
+    kErrChainK23 = 1 << 3,     // the fused stage 2+3 kernel gave up waiting for the previous chunk
 };
 
 }  // namespace m2

@@ -14,7 +14,8 @@
 // with coalesced 128-byte rows (32 heads of one token), transposed through
 // shared memory, scanned by one warp per head (each lane owns L/32 consecutive
 // tokens; lane totals are combined with a shuffle scan), and written back as
-// coalesced [h][t] rows.  HBM-bound: 12 bytes per (token, head).
+// coalesced [h][t] rows.  HBM-bound: 12 bytes per (token, head).  On the fused
+// path the kernel also clears the next kernel's ticket and flag words.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,10 +28,17 @@ constexpr int kThreads = 256;  // 8 warps
 template <int L>
 __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
-                    float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H) {
+                    float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H,
+                    int32_t* __restrict__ zero, int64_t nzero) {
     constexpr int E = L / 32;  // tokens per lane
     __shared__ float tile[kHB][L + 1];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
+    // Clear the next kernel's synchronisation words (grid-stride).
+    if (zero) {
+        const int64_t cta = c + (int64_t)gridDim.x * (b + (int64_t)gridDim.y * blockIdx.z);
+        const int64_t stride = (int64_t)gridDim.x * gridDim.y * gridDim.z * kThreads;
+        for (int64_t i = cta * kThreads + threadIdx.x; i < nzero; i += stride) zero[i] = 0;
+    }
     const int64_t t0 = c * L;
     const int nt = (int)min((int64_t)L, T - t0);
     const int nh = (int)min((int64_t)kHB, H - h0);
@@ -76,13 +84,20 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
 }  // namespace
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, float* cum2,
-                                float* dtT, int32_t* /*err*/, cudaStream_t st) {
+                                float* dtT, int32_t* /*err*/, cudaStream_t st, int32_t* zero,
+                                int64_t nzero) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     const dim3 grid((unsigned)d.nc, (unsigned)d.b, (unsigned)((d.H + kHB - 1) / kHB));
     switch (d.L) {
-        case 64: chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
-        case 128: chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
-        case 256: chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H); break;
+        case 64:
+            chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            break;
+        case 128:
+            chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            break;
+        case 256:
+            chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

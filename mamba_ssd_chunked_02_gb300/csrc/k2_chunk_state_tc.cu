@@ -29,6 +29,26 @@
 //     (128-byte coalesced stores).
 // Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2-5 = scaling,
 // 6-9 = epilogue.  Stage ring of NS x-buffers; every wait is bounded.
+//
+// Fused variant (stages 2 and 3 in one kernel, used by the whole-path call):
+// the epilogue does not store dS.  Per head it takes the state entering its
+// chunk, Sprev_c, from the CTA that handled chunk c-1 (published through a
+// two-slot fp32 ring in global memory plus one flag word per (b, h, n-tile,
+// chunk) written with release semantics): one TMA load brings the [P x n-tile]
+// tile into shared memory, each lane n updates its column in place
+// (decay_c * Sprev_c + dS_c, with dS_c from tensor memory) and writes the bf16
+// copy of Sprev_c beside it, and two TMA stores write Sprev_c (for stage 4) and
+// the next state (for chunk c+1, or the final state after the last chunk).
+// The CTA raises its heads' flags once all its stores have completed (a CTA of
+// chunk c+1 normally starts a wave later, when they are long set).  Pages: "Accelerating
+// Mamba-2 ..." section 8 (fwd_pass_state walks the chunks in order, combining
+// the decayed carried state with the chunk's own contribution).  The carried
+// state never goes to HBM as a whole tensor: each ring slot is read shortly
+// after it is written, while it is still in L2.  CTAs take their work item from
+// a global ticket counter in chunk-major order, so every CTA a CTA waits for has
+// already started (no dependence on the hardware's CTA launch order); waits are
+// bounded, and a CTA that gives up marks its flags so that its successors stop
+// at once.
 #include "common.cuh"
 #include "internal.h"
 #include "tc5.cuh"
@@ -42,15 +62,18 @@ using namespace tc;
 constexpr int kThreads = 320;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
-template <int L>
+template <int L, bool kFuse>
 struct K2Cfg {
     static constexpr int P = 64;
-    static constexpr int NS = L == 256 ? 3 : 6;           // x stages
+    // x stages (the fused variant spends shared memory on its state tiles).
+    static constexpr int NS = L == 256 ? (kFuse ? 2 : 3) : 6;
     static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
     static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
     static constexpr int X_BYTES = ATOM;                  // P = 64: one block
     static constexpr int D_BYTES = 64 * 128 * 4;          // one dS tile [p][n-tile], fp32
-    static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + 2 * D_BYTES;
+    // fused: two buffers of {carried state fp32 [64][128], Sprev bf16 [64][128]}
+    static constexpr int F_BYTES = 2 * (64 * 128 * 4 + 64 * 128 * 2);
+    static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + (kFuse ? F_BYTES : 2 * D_BYTES);
     static constexpr int TMEM_COLS = 128;                 // 2 accumulators x 64 columns
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 1, 1);
 };
@@ -60,20 +83,63 @@ struct K2Bars {
     uint64_t full[6], scaled[6], xfree[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
+    uint64_t cfull[2];      // fused: carried-state tile landed (per tile buffer)
     uint64_t epi_sync;      // group barrier of the 4 epilogue warps (abortable)
     uint32_t tmem_base;
     int abort;
+    int item;               // work item (ticket on the fused path)
 };
 
-template <int L>
+// Global-memory flag words of the fused variant (gpu scope).
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *f is 1 (published) for at most limit_ns; -1 (the predecessor gave
+// up) or a timeout raise *abort and return false.
+__device__ __forceinline__ bool wait_flag(const int32_t* f, volatile int* abort, uint64_t limit_ns) {
+    int v = ld_acquire_gpu(f);
+    if (v == 1) return true;
+    const uint64_t t0 = globaltimer();
+    while (v != 1) {
+        if (v < 0 || *abort || globaltimer() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(128);
+        v = ld_acquire_gpu(f);
+    }
+    return true;
+}
+
+// Arguments used by the fused variant only (null on the plain one).
+struct FuseArgs {
+    const float* init;        // [b][H][P][N] fp32 or null (zero initial state)
+    float* carry;             // [2][b][H][P][N] fp32 ring
+    int32_t* flags;           // [b][H][n_tiles][nc]
+    int32_t* ticket;          // work-item counter
+    __nv_bfloat16* Sprev;     // [b][nc][H][P][N]
+    float* fin;               // [b][H][P][N]
+    int nb;                   // batch
+};
+
+template <int L, bool kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_d,
+                      const __grid_constant__ CUtensorMap tm_ring,   // fused: [2 b H P][N] f32
+                      const __grid_constant__ CUtensorMap tm_init,   // fused: [b H P][N] f32
+                      const __grid_constant__ CUtensorMap tm_fin,    // fused: [b H P][N] f32
+                      const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       float* __restrict__ dS, int T, int H, int N, int G, int nc, int n_tiles,
-                      int hpc, int n_hblk, int32_t* err) {
-    using C = K2Cfg<L>;
+                      int hpc, int n_hblk, int32_t* err, const FuseArgs fa) {
+    using C = K2Cfg<L, kFuse>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -83,16 +149,6 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     __shared__ K2Bars bars;
     volatile int* abort = &bars.abort;
 
-    // Work item: (b, c, n-tile) outer, head block inner (CTAs sharing B^T run together).
-    int rest = blockIdx.x;
-    const int hblk = rest % n_hblk; rest /= n_hblk;
-    const int nt = rest % n_tiles; rest /= n_tiles;
-    const int c = rest % nc;
-    const int b = rest / nc;
-    const int hpg = H / G;
-    const int h0 = hblk * hpc;
-    const int g = h0 / hpg;
-    const int nh = hpc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -107,8 +163,11 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             mbar_init(&bars.acc_empty[i], 128);
         }
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.cfull[0], 1);
+        mbar_init(&bars.cfull[1], 1);
         mbar_init(&bars.epi_sync, 128);
         bars.abort = 0;
+        bars.item = kFuse ? atomicAdd(fa.ticket, 1) : (int)blockIdx.x;
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -120,12 +179,39 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 0) {
+    // Work item.  Plain: (b, c, n-tile) outer, head block inner (CTAs sharing
+    // B^T run together).  Fused: chunk outermost, in ticket order.
+    int rest = bars.item, b, c, nt, hblk;
+    if (kFuse) {
+        const int per_chunk = fa.nb * n_tiles * n_hblk;
+        c = rest / per_chunk; rest %= per_chunk;
+        b = rest / (n_tiles * n_hblk); rest %= n_tiles * n_hblk;
+        nt = rest / n_hblk;
+        hblk = rest % n_hblk;
+    } else {
+        hblk = rest % n_hblk; rest /= n_hblk;
+        nt = rest % n_tiles; rest /= n_tiles;
+        c = rest % nc;
+        b = rest / nc;
+    }
+    const int hpg = H / G;
+    const int h0 = hblk * hpc;
+    const int g = h0 / hpg;
+    const int nh = hpc;
+
+    if (c >= nc) {
+        // A ticket past the grid (the counter was not cleared): do nothing.
+        if (threadIdx.x == 0) record_error(err, kErrLaunchCfg);
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tm_x);
             prefetch_tmap(&tm_b);
-            prefetch_tmap(&tm_d);
+            if (!kFuse) prefetch_tmap(&tm_d);
+            if (kFuse) {
+                prefetch_tmap(&tm_ring);
+                prefetch_tmap(&tm_sp);
+            }
             mbar_arrive_expect_tx(&bars.bt_full, C::BT_BYTES);
             for (int a = 0; a < 2; ++a) {
                 // N = 64: both halves of the 128-row M tile hold n in [0, 64).
@@ -230,9 +316,11 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        // D[n, p] (lane = n) goes to a shared [p][n] fp32 tile (conflict-free:
-        // a warp writes 32 consecutive n of one p), then one TMA store per head
-        // writes the tile to dS[b, c, h, :, n-tile].
+        // Plain variant: D[n, p] (lane = n) goes to a shared [p][n] fp32 tile
+        // (conflict-free: a warp writes 32 consecutive n of one p), then one TMA
+        // store per head writes the tile to dS[b, c, h, :, n-tile].  Fused
+        // variant: lane n reads Sprev_c[p, n] for every p (a warp covers 128
+        // consecutive bytes), stores it as bf16 and passes the next state on.
         const int q = warp & 3;                          // TMEM lane quadrant
         const int ep = threadIdx.x - 192;                // 0..127
         const int NT = N < 128 ? N : 128;                // n-tile width = tile row pitch
@@ -244,35 +332,125 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
-        for (int i = 0; i < nh; ++i) {
-            const int ab = i & 1, ka = i >> 1;
-            const bool ok = __all_sync(0xffffffffu,
-                                       mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
-            if (!ok) break;
-            tc_fence_after();
-            float* tile = sD + ab * (64 * 128);
-            if (ep == 0) bulk_wait_read<1>();            // the store that used this tile is done
-            if (!group_sync()) break;                    // ... before any warp writes it
+        if constexpr (kFuse) {
+            const int64_t bH = (int64_t)fa.nb * H;
+            const int Lc = min(L, T - c * L);
+            const bool own = nl < NT;
+            const bool has_in = c > 0 || fa.init != nullptr;   // else Sprev_0 = 0
+            const bool last = c == nc - 1;
+            float* sCT = reinterpret_cast<float*>(sX + NS * C::X_BYTES);          // [2][64][NT]
+            __nv_bfloat16* sSP = reinterpret_cast<__nv_bfloat16*>(sCT + 2 * 64 * 128);  // [2][64][NT]
+            auto flag_of = [&](int i) {
+                return fa.flags + (((int64_t)b * H + h0 + i) * n_tiles + nt) * nc + c;
+            };
+            int published = 0;            // ep == 0: heads whose flag is raised (at the end)
+            int pending[2] = {-1, -1};    // ep == 0: head whose tile load is in flight, per buffer
+            for (int i = 0; i < nh; ++i) {
+                const int ab = i & 1, ka = i >> 1, buf = i & 1;
+                const int64_t bh = (int64_t)b * H + h0 + i;
+                float* ct = sCT + buf * (64 * 128);
+                __nv_bfloat16* spt = sSP + buf * (64 * 128);
+                if (ep == 0) {
+                    bulk_wait_read<1>();      // stores of head i-2 (same buffers) have read them
+                    bool go = true;
+                    if (c > 0) go = wait_flag(flag_of(i) - 1, abort, kWaitNs);
+                    if (go && has_in) {
+                        fence_proxy_async();  // the acquire above before the async-proxy read
+                        mbar_arrive_expect_tx(&bars.cfull[buf], (uint32_t)(NT * 64 * 4));
+                        if (c > 0)
+                            tma_load_2d(ct, &tm_ring, &bars.cfull[buf], nt * 128,
+                                        (int)((((int64_t)(c & 1)) * bH + bh) * C::P));
+                        else
+                            tma_load_2d(ct, &tm_init, &bars.cfull[buf], nt * 128, (int)(bh * C::P));
+                        pending[buf] = i;
+                    }
+                }
+                // Without an incoming tile nothing else orders the writes below after
+                // ep 0's wait for the stores that last read these buffers.
+                if (!has_in && i >= 2 && !group_sync()) break;
+                bool ok = __all_sync(0xffffffffu,
+                                     mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
+                if (ok && has_in)
+                    ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cfull[buf], (i >> 1) & 1,
+                                                                    abort, kWaitNs));
+                if (!ok) break;
+                if (ep == 0) pending[buf] = -1;
+                tc_fence_after();
+                const float dec = ex2(__ldg(cum2 + bh * T + (int64_t)c * L + Lc - 1));
 #pragma unroll
-            for (int cc = 0; cc < C::P / 32; ++cc) {
-                uint32_t r[32];
-                tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
-                if (nl < NT) {
+                for (int cc = 0; cc < C::P / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
+                    if (own) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) tile[(32 * cc + j) * NT + nl] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int o = (32 * cc + j) * NT + nl;
+                            const float sv = has_in ? ct[o] : 0.f;
+                            spt[o] = __float2bfloat16_rn(sv);
+                            ct[o] = fmaf(dec, sv, __uint_as_float(r[j]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty[ab]);
+                fence_proxy_async_smem();
+                if (!group_sync()) break;
+                if (ep == 0) {
+                    tma_store_2d(&tm_sp, spt, nt * 128, (int)((((int64_t)b * nc + c) * H + h0 + i) * C::P));
+                    if (last)
+                        tma_store_2d(&tm_fin, ct, nt * 128, (int)(bh * C::P));
+                    else
+                        tma_store_2d(&tm_ring, ct, nt * 128,
+                                     (int)((((int64_t)((c + 1) & 1)) * bH + bh) * C::P));
+                    bulk_commit();
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bars.acc_empty[ab]);
-            fence_proxy_async_smem();
-            if (!group_sync()) break;
             if (ep == 0) {
-                const int row = (int)((((int64_t)b * nc + c) * H + h0 + i) * C::P);
-                tma_store_2d(&tm_d, tile, nt * 128, row);
-                bulk_commit();
+                bulk_wait<0>();
+                if (!last) {
+                    fence_proxy_async();
+                    __threadfence();
+                    // Heads completed without an abort get their flag; after an abort
+                    // the rest are marked so that the next chunk's CTA stops at once.
+                    const int done = *abort ? published : nh;
+                    for (; published < done; ++published) st_release_gpu(flag_of(published), 1);
+                    for (int i = published; i < nh; ++i) st_release_gpu(flag_of(i), -1);
+                }
+                // A tile load still in flight after an abort must land before exit.
+                for (int k = 0; k < 2; ++k)
+                    if (pending[k] >= 0) mbar_wait(&bars.cfull[k], (pending[k] >> 1) & 1, kWaitNs);
             }
+        } else {
+            for (int i = 0; i < nh; ++i) {
+                const int ab = i & 1, ka = i >> 1;
+                const bool ok = __all_sync(0xffffffffu,
+                                           mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
+                if (!ok) break;
+                tc_fence_after();
+                float* tile = sD + ab * (64 * 128);
+                if (ep == 0) bulk_wait_read<1>();            // the store that used this tile is done
+                if (!group_sync()) break;                    // ... before any warp writes it
+#pragma unroll
+                for (int cc = 0; cc < C::P / 32; ++cc) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
+                    if (nl < NT) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) tile[(32 * cc + j) * NT + nl] = __uint_as_float(r[j]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty[ab]);
+                fence_proxy_async_smem();
+                if (!group_sync()) break;
+                if (ep == 0) {
+                    const int row = (int)((((int64_t)b * nc + c) * H + h0 + i) * C::P);
+                    tma_store_2d(&tm_d, tile, nt * 128, row);
+                    bulk_commit();
+                }
+            }
+            if (ep == 0) bulk_wait<0>();
         }
-        if (ep == 0) bulk_wait<0>();
     }
 
     tc_fence_before();
@@ -281,7 +459,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
-    if (threadIdx.x == 0 && bars.abort) record_error(err, kErrTimeoutK2);
+    if (threadIdx.x == 0 && bars.abort) record_error(err, kFuse ? (kErrTimeoutK2 | kErrChainK23) : kErrTimeoutK2);
 }
 
 int num_sms() {
@@ -307,35 +485,67 @@ int pick_hpc(const Dims& d, int64_t outer) {
     return 1;
 }
 
-template <int L>
+// Fused variant: the largest divisor of H/G (at most 16) for which one chunk's
+// CTAs, b * n_tiles * H / hpc, still cover every SM.
+int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
+    const int hpg = (int)(d.H / d.G);
+    for (int v = 16; v >= 1; --v)
+        if (hpg % v == 0 && d.b * n_tiles * (d.H / v) >= num_sms()) return v;
+    return 1;
+}
+
+template <int L, bool kFuse>
 cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
-                      const float* dtT, float* dS, int32_t* err, cudaStream_t st) {
-    using C = K2Cfg<L>;
+                      const float* dtT, float* dS, const FuseArgs& fa, int32_t* err,
+                      cudaStream_t st) {
+    using C = K2Cfg<L, kFuse>;
     CUtensorMap tm_x, tm_b;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
     const uint32_t box[3] = {64, (uint32_t)L, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
-    CUtensorMap tm_d;
-    const uint64_t dd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
-    const uint64_t ds[1] = {(uint64_t)(d.N * 4)};
-    const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
-    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
-        !make_tmap(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dS, 2, dd, ds, dbox,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box))
         return cudaErrorInvalidValue;
+    CUtensorMap tm_d = tm_x;   // the fused variant stores no dS
+    CUtensorMap tm_ring = tm_x, tm_init = tm_x, tm_fin = tm_x, tm_sp = tm_x;   // plain: unused
+    if (kFuse) {
+        const uint32_t tbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
+        const uint64_t rs[1] = {(uint64_t)(d.N * 4)};
+        const uint64_t ring_d[2] = {(uint64_t)d.N, (uint64_t)(2 * d.b * d.H * d.P)};
+        const uint64_t st_d[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.H * d.P)};
+        const uint64_t sp_d[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
+        const uint64_t sps[1] = {(uint64_t)(d.N * 2)};
+        const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        const auto NONE = CU_TENSOR_MAP_SWIZZLE_NONE;
+        if (!make_tmap(&tm_ring, F32, fa.carry, 2, ring_d, rs, tbox, NONE) ||
+            !make_tmap(&tm_fin, F32, fa.fin, 2, st_d, rs, tbox, NONE) ||
+            (fa.init && !make_tmap(&tm_init, F32, fa.init, 2, st_d, rs, tbox, NONE)) ||
+            !make_tmap(&tm_sp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, fa.Sprev, 2, sp_d, sps, tbox, NONE))
+            return cudaErrorInvalidValue;
+    }
+    if (!kFuse) {
+        const uint64_t dd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
+        const uint64_t ds[1] = {(uint64_t)(d.N * 4)};
+        const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
+        if (!make_tmap(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dS, 2, dd, ds, dbox,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
     const int64_t outer = d.b * d.nc * n_tiles;
-    const int hpc = pick_hpc(d, outer);
+    // Fused: one chunk's CTAs should fill the GPU, so that the CTA of chunk c
+    // typically starts after the one of chunk c-1 has finished (no waiting).
+    const int hpc = kFuse ? pick_hpc_fused(d, n_tiles) : pick_hpc(d, outer);
     const int n_hblk = (int)(d.H / hpc);
     const int64_t grid = outer * n_hblk;
-    auto k = chunk_state_tc_kernel<L>;
+    auto k = chunk_state_tc_kernel<L, kFuse>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, cum2, dtT, dS, (int)d.T, (int)d.H,
+    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, tm_ring, tm_init, tm_fin, tm_sp,
+                                                 cum2, dtT, dS, (int)d.T, (int)d.H,
                                                  (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
-                                                 n_hblk, err);
+                                                 n_hblk, err, fa);
     return cudaGetLastError();
 }
 
@@ -352,8 +562,33 @@ cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, c
                                   const float* dtT, float* dS, int32_t* err, cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
-    return d.L == 256 ? launch_k2<256>(d, x, B, cum2, dtT, dS, err, st)
-                      : launch_k2<128>(d, x, B, cum2, dtT, dS, err, st);
+    const FuseArgs none{};
+    return d.L == 256 ? launch_k2<256, false>(d, x, B, cum2, dtT, dS, none, err, st)
+                      : launch_k2<128, false>(d, x, B, cum2, dtT, dS, none, err, st);
+}
+
+int64_t fused_flag_words(const Dims& d) {
+    const int64_t n_tiles = d.N > 128 ? d.N / 128 : 1;
+    return d.b * d.H * n_tiles * d.nc;
+}
+
+cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void* B,
+                                       const float* cum2, const float* dtT, const float* init,
+                                       float* carry, int32_t* flags, int32_t* ticket,
+                                       void* Sprev, float* final_state, int32_t* err,
+                                       cudaStream_t st) {
+    if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
+    if (!tc_supported(d) || d.b > (1 << 20)) return cudaErrorInvalidValue;
+    FuseArgs fa;
+    fa.init = init;
+    fa.carry = carry;
+    fa.flags = flags;
+    fa.ticket = ticket;
+    fa.Sprev = static_cast<__nv_bfloat16*>(Sprev);
+    fa.fin = final_state;
+    fa.nb = (int)d.b;
+    return d.L == 256 ? launch_k2<256, true>(d, x, B, cum2, dtT, nullptr, fa, err, st)
+                      : launch_k2<128, true>(d, x, B, cum2, dtT, nullptr, fa, err, st);
 }
 
 }  // namespace m2

@@ -160,6 +160,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 }
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA store, tcgen05.mma) reads of the same memory.
+// Order this thread's earlier generic-proxy accesses (e.g. an acquire of a flag)
+// before its later async-proxy accesses to global memory (a TMA load).
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -63,6 +63,7 @@ def test_check_shape(lib):
     assert m2.check_shape(shp(headdim=0)) == m2.ERR_INVALID_ARG
     assert m2.check_shape(shp(dtype=7)) == m2.ERR_INVALID_ARG
     assert m2.check_shape(shp(flags=8)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(flags=m2.FLAG_FUSED_STATE | m2.FLAG_FORCE_SIMT)) == m2.OK
     assert m2.check_shape(shp(headdim=48)) == m2.ERR_UNSUPPORTED
     assert m2.check_shape(shp(dstate=96)) == m2.ERR_UNSUPPORTED
     assert m2.check_shape(shp(chunk_size=32)) == m2.ERR_UNSUPPORTED
@@ -136,6 +137,32 @@ def test_stage_entry_points_validate(lib):
                                      None) == m2.ERR_INVALID_ARG
     assert lib.mamba2_ssd_chunk_out(ctypes.byref(s), g, g, g, g, g, g, None, None,
                                     None) == m2.ERR_INVALID_ARG
+
+
+def test_fused_stage_workspace_and_validation(lib):
+    def a256(v):
+        return (v + 255) // 256 * 256
+    s = shp(batch=8, seqlen=4096, nheads=80)                  # the 2.7B layer: one n-tile
+    want = a256(2 * 4 * 8 * 80 * 64 * 128) + a256(4 * (8 * 80 * 1 * 16 + 1))
+    assert m2.chunk_state_pass_workspace_size(s) == want
+    s2 = shp(dstate=256, seqlen=300)                           # two n-tiles, ragged
+    assert m2.chunk_state_pass_workspace_size(s2) == \
+        a256(2 * 4 * 2 * 8 * 64 * 256) + a256(4 * (2 * 8 * 2 * 2 + 1))
+    assert m2.chunk_state_pass_workspace_size(shp(dtype=m2.F32)) == 0   # no tensor-core path
+    vp = ctypes.c_void_p
+    g = vp(1 << 20)
+    rc = lib.mamba2_ssd_chunk_state_pass(ctypes.byref(shp(dtype=m2.F32)), *([g] * 7), g,
+                                         ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_UNSUPPORTED
+    rc = lib.mamba2_ssd_chunk_state_pass(ctypes.byref(shp()), None, *([g] * 6), g,
+                                         ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_INVALID_ARG
+    rc = lib.mamba2_ssd_chunk_state_pass(ctypes.byref(shp()), *([g] * 7), vp((1 << 20) + 64),
+                                         ctypes.c_size_t(1 << 40), None)
+    assert rc == m2.ERR_WORKSPACE                               # misaligned workspace
+    rc = lib.mamba2_ssd_chunk_state_pass(ctypes.byref(shp()), *([g] * 7), g, ctypes.c_size_t(64),
+                                         None)
+    assert rc == m2.ERR_WORKSPACE                               # too small
 
 
 def test_empty_problem_is_a_noop(lib):

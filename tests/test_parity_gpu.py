@@ -123,6 +123,77 @@ def test_tensor_core_path_matches_cuda_core_path(w):
         assert np.abs(d).max() <= 2 * max_tol * rms
 
 
+FUSED = [
+    wl(2, 1024, 8, 64, 128, 1, 256, seed=31),                           # 4 chunks
+    wl(1, 768, 2, 64, 256, 1, 256, seed=32),                            # N = 256: two n-tiles
+    wl(2, 640, 16, 64, 128, 4, 128, init=0.1, seed=33),                 # L = 128, ragged, groups, init
+    wl(1, 2048, 4, 64, 64, 1, 256, seed=34),                            # N = 64, 8 chunks
+]
+
+
+@pytest.mark.parametrize("w", FUSED, ids=_ids(FUSED))
+def test_fused_state_pass_matches_separate_kernels(w):
+    """Stages 2+3 fused (carried state handed from chunk to chunk between CTAs)
+    against the two separate kernels: the same fp32 operations in the same order
+    (S = fma(decay, S, dS), Sprev rounded to bf16), so the outputs are equal bit
+    for bit; both are also checked against the oracle."""
+    assert m2.path(m2.make_shape(w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                                 w.chunk_size)) == m2.PATH_TCGEN05
+    inp = W.make_inputs(w)
+    y0, f0 = run_fwd(inp, w)
+    y1, f1 = run_fwd(inp, w, flags=m2.FLAG_FUSED_STATE)
+    assert torch.equal(y0, y1)
+    assert torch.equal(f0, f1)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
+    assert_close(to_np(y1), yr, w.dtype, f"y {w.name}")
+    assert_close(to_np(f1), fr, w.dtype, f"final_state {w.name}")
+
+
+@pytest.mark.parametrize("w", FUSED[:3], ids=_ids(FUSED[:3]))
+def test_fused_stage_entry_point_matches_stages(w):
+    """mamba2_ssd_chunk_state_pass against mamba2_ssd_chunk_state followed by
+    mamba2_ssd_state_pass: Sprev and final_state equal bit for bit."""
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    b, T, H, P, N, nc = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, sh.nchunks
+    f32 = dict(dtype=torch.float32, device="cuda")
+    cum2, dtT = torch.empty((b, H, T), **f32), torch.empty((b, H, T), **f32)
+    m2.chunk_cumsum(sh, dev["dt"], dev["A"], cum2, dtT)
+    dS = torch.empty((b, nc, H, P, N), **f32)
+    sp0 = torch.empty((b, nc, H, P, N), dtype=torch.bfloat16, device="cuda")
+    f0 = torch.empty((b, H, P, N), **f32)
+    m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS)
+    m2.state_pass(sh, dS, cum2, dev["initial_state"], sp0, f0)
+    sp1, f1 = torch.full_like(sp0, float("nan")), torch.full_like(f0, float("nan"))
+    ws = torch.empty(m2.chunk_state_pass_workspace_size(sh), dtype=torch.uint8, device="cuda")
+    m2.chunk_state_pass(sh, dev["x"], dev["B"], cum2, dtT, dev["initial_state"], sp1, f1, ws)
+    torch.cuda.synchronize()
+    assert m2.device_error() == 0
+    assert torch.equal(sp0, sp1)
+    assert torch.equal(f0, f1)
+
+
+def test_fused_path_repeats_exactly():
+    """The fused kernel's CTAs take work items from a ticket counter and wait for
+    each other through flag words that stage 1 clears: running the same call
+    again (same workspace, flags left set by the first run) gives the same bits."""
+    w = FUSED[0]
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        outs.append(m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                               dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
+                               workspace=ws, flags=m2.FLAG_FUSED_STATE))
+    torch.cuda.synchronize()
+    assert m2.device_error() == 0
+    for y, f in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(f, outs[0][1])
+
+
 def test_chunk_size_independence():
     """The chunking is an evaluation order: L in {64, 128, 256} give the same result."""
     w = wl(1, 1024, 4, 64, 128, 1, 256, seed=31)
