@@ -70,9 +70,10 @@ def workload(name):
 
 
 # ----------------------------------------------------------- algorithmic model ---
-def model(w):
-    """Algorithmic bytes and tensor FLOPs per launch of each stage, and the
-    whole-path figures (fixed four-stage byte model with fp32 states)."""
+def model(w, dsz=4):
+    """Algorithmic bytes and tensor FLOPs per launch of each stage (dS moved
+    between stages 2 and 3 with dsz bytes per element), and the whole-path
+    figures (fixed four-stage byte model with fp32 states)."""
     b, T, H, P, N, G, L = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups, w.chunk_size
     E = 2 if w.dtype == "bf16" else 4
     nc = -(-T // L)
@@ -81,9 +82,9 @@ def model(w):
     init = 1 if w.init_std > 0 else 0
     k = {
         "chunk_cumsum": dict(bytes=12 * th + 4 * H, flops=0),
-        "chunk_state": dict(bytes=th * (P * E + 8) + b * T * G * N * E + 4 * st,
+        "chunk_state": dict(bytes=th * (P * E + 8) + b * T * G * N * E + dsz * st,
                             flops=2 * th * P * N),
-        "state_pass": dict(bytes=4 * st + E * st + 4 * b * H * P * N * (1 + init) + 4 * b * H * nc,
+        "state_pass": dict(bytes=dsz * st + E * st + 4 * b * H * P * N * (1 + init) + 4 * b * H * nc,
                            flops=0),
         # stages 2+3 in one kernel: no dS round trip (the carried state moves
         # between CTAs through L2 and is not counted)
@@ -298,7 +299,10 @@ def main():
         dS = None
         sp_ws = torch.empty(m2.chunk_state_pass_workspace_size(sh), dtype=torch.uint8, device="cuda")
     else:
-        dS = torch.empty((b, nc, H, P, N), **f32)
+        # The whole-path call hands dS from stage 2 to 3 in bf16 on the tensor-core path.
+        ds_bf16 = m2.path(sh) == m2.PATH_TCGEN05
+        dS = torch.empty((b, nc, H, P, N), dtype=torch.bfloat16 if ds_bf16 else torch.float32,
+                         device="cuda")
     Sprev = torch.empty((b, nc, H, P, N), dtype=w.torch_dtype, device="cuda")
     y = torch.empty((b, T, H, P), dtype=w.torch_dtype, device="cuda")
     fin = torch.empty((b, H, P, N), **f32)
@@ -366,7 +370,7 @@ def main():
             per[kname] += marks[j].elapsed_time(marks[j + 1])
     per = {k: v / K for k, v in per.items()}
 
-    kmodel, graded_bytes, flops = model(w)
+    kmodel, graded_bytes, flops = model(w, 2 if (dS is not None and dS.dtype == torch.bfloat16) else 4)
     pk, pk_src = peaks()
     tokens = w.tokens * world
     value = tokens / (ms_step * 1e-3)

@@ -85,6 +85,12 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  * HBM.  Same results bit for bit; slower on GB300 at the 2.7B layer shape
  * (0.317 ms against 0.243 ms for the pair), so it is not the default. */
 #define MAMBA2_FLAG_FUSED_STATE 2
+/* dS is bf16 (not fp32) in mamba2_ssd_chunk_state (output) and
+ * mamba2_ssd_state_pass (input): the hand-off mamba2_ssd_fwd uses on the
+ * tensor-core path (half the bytes; each chunk's dS rounded to bf16).  Needs
+ * the tensor-core path for chunk_state and dtype BF16 for state_pass; other
+ * shapes return MAMBA2_ERR_UNSUPPORTED. */
+#define MAMBA2_FLAG_DS_BF16 4
 
 /* Shape of one call.  Supported set:
  *   batch, seqlen, nheads >= 0 (a zero batch or head count is a no-op; seqlen 0
@@ -124,7 +130,9 @@ MAMBA2_API size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape);
 
 /* The whole forward pass: the four stages below, in order, on `stream`
  * (stages 2 and 3 as one kernel with MAMBA2_FLAG_FUSED_STATE, tensor-core path,
- * three or more chunks).
+ * three or more chunks).  On the tensor-core path dS goes from stage 2 to
+ * stage 3 in bf16 (as with MAMBA2_FLAG_DS_BF16); the carried states themselves
+ * are accumulated in fp32.
  *   workspace: device buffer of at least mamba2_ssd_workspace_size(shape)
  *   bytes, 256-byte aligned, owned by the caller, contents ignored on entry.
  * Returns MAMBA2_OK once the launches are queued. */
@@ -146,18 +154,20 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_cumsum(const mamba2_ssd_shape* shape,
 
 /* Stage 2, chunk states by the jump formula [P3 sections 4, 8]:
  *   dS[b,c,h,p,n] = sum_{s in chunk c} exp2(cum2_last(c) - cum2[s]) dtT[s] x[s,p] B[s,n]
- * (tcgen05 tensor cores where the shape allows). */
+ * (tcgen05 tensor cores where the shape allows).  dS is fp32 (float*), or bf16
+ * with MAMBA2_FLAG_DS_BF16. */
 MAMBA2_API mamba2_status mamba2_ssd_chunk_state(const mamba2_ssd_shape* shape,
                                      const void* x, const void* B,
                                      const float* cum2, const float* dtT,
-                                     float* dS, void* stream);
+                                     void* dS, void* stream);
 
 /* Stage 3, sequential pass over chunks [P2 "세 가지 핵심 커널 구현", fwd_pass_state]:
  *   S = initial_state (or 0); for c: Sprev[c] = S; S = exp2(cum2_last(c)) S + dS[c];
  *   final_state = S.
- * Sprev is rounded to `dtype` (it is the tensor-core operand of stage 4). */
+ * Sprev is rounded to `dtype` (it is the tensor-core operand of stage 4); S is
+ * fp32.  dS is fp32, or bf16 with MAMBA2_FLAG_DS_BF16. */
 MAMBA2_API mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape,
-                                    const float* dS, const float* cum2,
+                                    const void* dS, const float* cum2,
                                     const float* initial_state,
                                     void* Sprev, float* final_state, void* stream);
 

@@ -31,6 +31,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmamba2_ssd.so")
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_FUSED_STATE = 2
+FLAG_DS_BF16 = 4
 PATH_SIMT, PATH_TCGEN05 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = range(6)
 
@@ -224,23 +225,41 @@ def chunk_cumsum(shape, dt, A, cum2, dtT, stream=None):
         _ptr(dtT, "dtT", torch.float32, (b, H, T)), _stream(stream)))
 
 
+def _with_ds_dtype(shape, dS):
+    """A copy of `shape` whose MAMBA2_FLAG_DS_BF16 bit matches dS's dtype."""
+    sh = Shape(*[getattr(shape, f) for f, _ in Shape._fields_])
+    if dS is not None and dS.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"dS must be torch.float32 or torch.bfloat16, got {dS.dtype}")
+    if dS is not None and dS.dtype == torch.bfloat16:
+        sh.flags |= FLAG_DS_BF16
+    else:
+        sh.flags &= ~FLAG_DS_BF16
+    return sh
+
+
 def chunk_state(shape, x, B, cum2, dtT, dS, stream=None):
-    """Stage 2 (mamba2_ssd_chunk_state): dS [b,nc,H,P,N] f32 output."""
+    """Stage 2 (mamba2_ssd_chunk_state): dS [b,nc,H,P,N] output, f32 or bf16
+    (bf16: the hand-off the whole-path call uses on the tensor-core path)."""
     b, T, H, P, N, G = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate,
                         shape.ngroups)
     io = _io_dtype(shape)
+    sh = _with_ds_dtype(shape, dS)
     _check("mamba2_ssd_chunk_state", load().mamba2_ssd_chunk_state(
-        ctypes.byref(shape), _ptr(x, "x", io, (b, T, H, P)), _ptr(B, "B", io, (b, T, G, N)),
+        ctypes.byref(sh), _ptr(x, "x", io, (b, T, H, P)), _ptr(B, "B", io, (b, T, G, N)),
         _ptr(cum2, "cum2", torch.float32, (b, H, T)), _ptr(dtT, "dtT", torch.float32, (b, H, T)),
-        _ptr(dS, "dS", torch.float32, (b, shape.nchunks, H, P, N)), _stream(stream)))
+        _ptr(dS, "dS", dS.dtype if dS is not None else torch.float32, (b, shape.nchunks, H, P, N)),
+        _stream(stream)))
 
 
 def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
-    """Stage 3 (mamba2_ssd_state_pass): Sprev [b,nc,H,P,N] (I/O dtype), final_state f32."""
+    """Stage 3 (mamba2_ssd_state_pass): Sprev [b,nc,H,P,N] (I/O dtype), final_state f32;
+    dS f32 or bf16."""
     b, T, H, P, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.dstate
     nc = shape.nchunks
+    sh = _with_ds_dtype(shape, dS)
     _check("mamba2_ssd_state_pass", load().mamba2_ssd_state_pass(
-        ctypes.byref(shape), _ptr(dS, "dS", torch.float32, (b, nc, H, P, N)),
+        ctypes.byref(sh), _ptr(dS, "dS", dS.dtype if dS is not None else torch.float32,
+                               (b, nc, H, P, N)),
         _ptr(cum2, "cum2", torch.float32, (b, H, T)),
         _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
         _ptr(Sprev, "Sprev", _io_dtype(shape), (b, nc, H, P, N)),

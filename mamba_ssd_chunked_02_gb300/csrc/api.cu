@@ -53,7 +53,8 @@ mamba2_status check(const mamba2_ssd_shape* s) {
     if (s->headdim <= 0 || s->dstate <= 0 || s->ngroups <= 0 || s->chunk_size <= 0)
         return MAMBA2_ERR_INVALID_ARG;
     if (s->dtype != MAMBA2_F32 && s->dtype != MAMBA2_BF16) return MAMBA2_ERR_INVALID_ARG;
-    if (s->flags & ~(MAMBA2_FLAG_FORCE_SIMT | MAMBA2_FLAG_FUSED_STATE)) return MAMBA2_ERR_INVALID_ARG;
+    if (s->flags & ~(MAMBA2_FLAG_FORCE_SIMT | MAMBA2_FLAG_FUSED_STATE | MAMBA2_FLAG_DS_BF16))
+        return MAMBA2_ERR_INVALID_ARG;
     if (s->nheads % s->ngroups != 0) return MAMBA2_ERR_INVALID_ARG;
     if (!in_set(s->headdim, {16, 32, 64, 128})) return MAMBA2_ERR_UNSUPPORTED;
     if (!in_set(s->dstate, {16, 32, 64, 128, 256})) return MAMBA2_ERR_UNSUPPORTED;
@@ -130,32 +131,38 @@ mamba2_status mamba2_ssd_chunk_cumsum(const mamba2_ssd_shape* shape, const float
 }
 
 mamba2_status mamba2_ssd_chunk_state(const mamba2_ssd_shape* shape, const void* x, const void* B,
-                                     const float* cum2, const float* dtT, float* dS,
+                                     const float* cum2, const float* dtT, void* dS,
                                      void* stream) {
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     const Dims d = dims_of(shape);
+    const bool ds16 = shape->flags & MAMBA2_FLAG_DS_BF16;
+    if (ds16 && !use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
     const bool empty = d.b * d.T * d.H == 0;
     if (!req(x, empty) || !req(B, empty) || !req(cum2, empty) || !req(dtT, empty) ||
         !req(dS, empty))
         return MAMBA2_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = use_tc(shape, d) ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, error_word(), s)
-                                     : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, error_word(), s);
+    cudaError_t e = use_tc(shape, d)
+                        ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, ds16, error_word(), s)
+                        : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, static_cast<float*>(dS),
+                                                      error_word(), s);
     return from_cuda(e);
 }
 
-mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape, const float* dS,
+mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape, const void* dS,
                                     const float* cum2, const float* initial_state, void* Sprev,
                                     float* final_state, void* stream) {
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     const Dims d = dims_of(shape);
+    const bool ds16 = shape->flags & MAMBA2_FLAG_DS_BF16;
+    if (ds16 && d.dtype != 1) return MAMBA2_ERR_UNSUPPORTED;
     const bool empty = d.b * d.T * d.H == 0;
     if (!req(dS, empty) || !req(cum2, empty) || !opt(initial_state) || !req(Sprev, empty) ||
         !req(final_state, d.b * d.H == 0))
         return MAMBA2_ERR_INVALID_ARG;
-    return from_cuda(m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state,
+    return from_cuda(m2::launch_state_pass(d, dS, ds16, cum2, initial_state, Sprev, final_state,
                                            error_word(), static_cast<cudaStream_t>(stream)));
 }
 
@@ -183,7 +190,7 @@ mamba2_status mamba2_ssd_chunk_state_pass(const mamba2_ssd_shape* shape, const v
     if (d.b * d.H == 0) return MAMBA2_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d.T == 0)
-        return from_cuda(m2::launch_state_pass(d, nullptr, nullptr, initial_state, nullptr,
+        return from_cuda(m2::launch_state_pass(d, nullptr, false, nullptr, initial_state, nullptr,
                                                final_state, error_word(), s));
     const size_t ring = align256(2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
     const size_t nflag = (size_t)m2::fused_flag_words(d);
@@ -234,7 +241,7 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t* err = error_word();
     if (d.T == 0)   // final_state = initial_state (or 0); nothing else to write
-        return from_cuda(m2::launch_state_pass(d, nullptr, nullptr, initial_state, nullptr,
+        return from_cuda(m2::launch_state_pass(d, nullptr, false, nullptr, initial_state, nullptr,
                                                final_state, err, s));
     if (!workspace || workspace_bytes < cv.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return MAMBA2_ERR_WORKSPACE;
@@ -261,10 +268,11 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
                                                flags + nflag, Sprev, final_state, err, s);
     } else {
         if (e == cudaSuccess)
-            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, err, s)
+            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s)
                    : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
+        // On the tensor-core path dS travels between stages 2 and 3 in bf16.
         if (e == cudaSuccess)
-            e = m2::launch_state_pass(d, dS, cum2, initial_state, Sprev, final_state, err, s);
+            e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, final_state, err, s);
     }
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s)

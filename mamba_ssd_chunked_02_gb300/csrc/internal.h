@@ -29,9 +29,10 @@ cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, 
 cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
                                     const float* cum2, const float* dtT, float* dS,
                                     int32_t* err, cudaStream_t st);
-// Stage 2: tcgen05 variant (bf16, shapes accepted by tc_supported()).
+// Stage 2: tcgen05 variant (bf16, shapes accepted by tc_supported()); dS is
+// written in fp32, or in bf16 when ds16 (the whole-path call).
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,
-                                  const float* cum2, const float* dtT, float* dS,
+                                  const float* cum2, const float* dtT, void* dS, bool ds16,
                                   int32_t* err, cudaStream_t st);
 
 // Stages 2 and 3 fused (tcgen05, bf16, tc_supported() shapes): each CTA
@@ -49,8 +50,8 @@ cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void*
                                        void* Sprev, float* final_state, int32_t* err,
                                        cudaStream_t st);
 
-// Stage 3: sequential state pass over chunks.
-cudaError_t launch_state_pass(const Dims& d, const float* dS, const float* cum2,
+// Stage 3: sequential state pass over chunks (dS in fp32, or bf16 when ds16).
+cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const float* cum2,
                               const float* init, void* Sprev, float* final_state,
                               int32_t* err, cudaStream_t st);
 

@@ -25,8 +25,9 @@
 //     tensor memory instead, to avoid shared-memory contention, which does not
 //     limit this HBM-bound kernel.
 //   * D accumulates in tensor memory (fp32), double buffered across heads; four
-//     warps read it back (tcgen05.ld) and store dS rows of 32 consecutive n
-//     (128-byte coalesced stores).
+//     warps read it back (tcgen05.ld) into a shared [p][n] tile and one TMA
+//     store per head writes it to dS, in fp32 or, on the whole-path call, in
+//     bf16 (the stage-3 kernel reads it back at once; half the bytes).
 // Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2-5 = scaling,
 // 6-9 = epilogue.  Stage ring of NS x-buffers; every wait is bounded.
 //
@@ -70,7 +71,7 @@ struct K2Cfg {
     static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
     static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
     static constexpr int X_BYTES = ATOM;                  // P = 64: one block
-    static constexpr int D_BYTES = 64 * 128 * 4;          // one dS tile [p][n-tile], fp32
+    static constexpr int D_BYTES = 64 * 128 * 4;          // one dS tile [p][n-tile] (fp32 max)
     // fused: two buffers of {carried state fp32 [64][128], Sprev bf16 [64][128]}
     static constexpr int F_BYTES = 2 * (64 * 128 * 4 + 64 * 128 * 2);
     static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + (kFuse ? F_BYTES : 2 * D_BYTES);
@@ -137,7 +138,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_fin,    // fused: [b H P][N] f32
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
-                      float* __restrict__ dS, int T, int H, int N, int G, int nc, int n_tiles,
+                      int ds16, int T, int H, int N, int G, int nc, int n_tiles,
                       int hpc, int n_hblk, int32_t* err, const FuseArgs fa) {
     using C = K2Cfg<L, kFuse>;
     constexpr int NS = C::NS;
@@ -434,7 +435,12 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 for (int cc = 0; cc < C::P / 32; ++cc) {
                     uint32_t r[32];
                     tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
-                    if (nl < NT) {
+                    if (nl < NT && ds16) {
+                        __nv_bfloat16* t16 = reinterpret_cast<__nv_bfloat16*>(tile);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            t16[(32 * cc + j) * NT + nl] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    } else if (nl < NT) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) tile[(32 * cc + j) * NT + nl] = __uint_as_float(r[j]);
                     }
@@ -496,7 +502,7 @@ int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
 
 template <int L, bool kFuse>
 cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
-                      const float* dtT, float* dS, const FuseArgs& fa, int32_t* err,
+                      const float* dtT, void* dS, bool ds16, const FuseArgs& fa, int32_t* err,
                       cudaStream_t st) {
     using C = K2Cfg<L, kFuse>;
     CUtensorMap tm_x, tm_b;
@@ -526,9 +532,10 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     }
     if (!kFuse) {
         const uint64_t dd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
-        const uint64_t ds[1] = {(uint64_t)(d.N * 4)};
+        const uint64_t ds[1] = {(uint64_t)(d.N * (ds16 ? 2 : 4))};
         const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
-        if (!make_tmap(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dS, 2, dd, ds, dbox,
+        if (!make_tmap(&tm_d, ds16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       dS, 2, dd, ds, dbox,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
@@ -543,7 +550,7 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, tm_ring, tm_init, tm_fin, tm_sp,
-                                                 cum2, dtT, dS, (int)d.T, (int)d.H,
+                                                 cum2, dtT, ds16 ? 1 : 0, (int)d.T, (int)d.H,
                                                  (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
                                                  n_hblk, err, fa);
     return cudaGetLastError();
@@ -559,12 +566,13 @@ bool tc_supported(const Dims& d) {
 }
 
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
-                                  const float* dtT, float* dS, int32_t* err, cudaStream_t st) {
+                                  const float* dtT, void* dS, bool ds16, int32_t* err,
+                                  cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     const FuseArgs none{};
-    return d.L == 256 ? launch_k2<256, false>(d, x, B, cum2, dtT, dS, none, err, st)
-                      : launch_k2<128, false>(d, x, B, cum2, dtT, dS, none, err, st);
+    return d.L == 256 ? launch_k2<256, false>(d, x, B, cum2, dtT, dS, ds16, none, err, st)
+                      : launch_k2<128, false>(d, x, B, cum2, dtT, dS, ds16, none, err, st);
 }
 
 int64_t fused_flag_words(const Dims& d) {
@@ -587,8 +595,8 @@ cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void*
     fa.Sprev = static_cast<__nv_bfloat16*>(Sprev);
     fa.fin = final_state;
     fa.nb = (int)d.b;
-    return d.L == 256 ? launch_k2<256, true>(d, x, B, cum2, dtT, nullptr, fa, err, st)
-                      : launch_k2<128, true>(d, x, B, cum2, dtT, nullptr, fa, err, st);
+    return d.L == 256 ? launch_k2<256, true>(d, x, B, cum2, dtT, nullptr, false, fa, err, st)
+                      : launch_k2<128, true>(d, x, B, cum2, dtT, nullptr, false, fa, err, st);
 }
 
 }  // namespace m2

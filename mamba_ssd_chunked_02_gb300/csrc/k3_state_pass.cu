@@ -10,11 +10,13 @@
 //   for c in 0..nc-1:  Sprev[c] = S;  S = exp2(cum2[last token of c]) * S + dS[c]
 //   final_state = S
 //
-// Sequential over chunks, parallel over (b, h, 4-element slices of the P x N
-// state): one thread owns a float4 of the state for the whole chain.  The dS
+// Sequential over chunks, parallel over (b, h, slices of the P x N state): one
+// thread owns 16 bytes' worth of dS elements of the state (4 for fp32 dS, 8 for
+// bf16 dS) for the whole chain.  The dS
 // loads do not depend on the chain, so each thread keeps kDepth chunks of loads
 // in flight (a rolling prefetch) while it walks the chain: a pure HBM stream of
-// 4 + esize bytes per state element per chunk.
+// dS (fp32, or bf16 on the whole-path call) in and Sprev out per state element
+// per chunk.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,30 +26,66 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kDepth = 8;   // chunks of dS loads in flight per thread
 
-__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&lo);
-    u.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(p) = u;
+// A thread owns EPT consecutive state elements, EPT = 16 bytes of dS: one
+// 16-byte load of dS and one store of Sprev per chunk.
+template <typename TD>
+struct Ept {
+    static constexpr int value = 16 / (int)sizeof(TD);
+};
+
+// 16 bytes of dS stay packed while in flight (4 registers) and are widened to
+// fp32 when consumed.
+__device__ __forceinline__ uint4 load16(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void widen(const uint4& u, float (&v)[4]) {   // fp32 dS
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void widen(const uint4& u, float (&v)[8]) {   // bf16 dS
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+}
+template <int E>
+__device__ __forceinline__ void store_state(float* p, const float (&S)[E]) {
+#pragma unroll
+    for (int k = 0; k < E; k += 4)
+        *reinterpret_cast<float4*>(p + k) = make_float4(S[k], S[k + 1], S[k + 2], S[k + 3]);
+}
+template <int E>
+__device__ __forceinline__ void store_state(__nv_bfloat16* p, const float (&S)[E]) {
+    uint32_t w[E / 2];
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+        __nv_bfloat162 t = __floats2bfloat162_rn(S[2 * k], S[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&t);
+    }
+    if constexpr (E == 8)
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
 }
 
-template <typename TS>
+template <typename TS, typename TD>
 __global__ void __launch_bounds__(kThreads)
-state_pass_kernel(const float* __restrict__ dS, const float* __restrict__ cum2,
+state_pass_kernel(const TD* __restrict__ dS, const float* __restrict__ cum2,
                   const float* __restrict__ init, TS* __restrict__ Sprev,
                   float* __restrict__ fin, int64_t T, int64_t H, int64_t L, int64_t nc,
                   int64_t PN, int64_t blocks_per_bh) {
+    constexpr int E = Ept<TD>::value;
     const int64_t bh = blockIdx.x / blocks_per_bh;
-    const int64_t i4 = (blockIdx.x % blocks_per_bh) * kThreads + threadIdx.x;
-    const int64_t e = i4 * 4;
+    const int64_t iv = (blockIdx.x % blocks_per_bh) * kThreads + threadIdx.x;
+    const int64_t e = iv * E;
     if (e >= PN) return;
     const int64_t b = bh / H, h = bh % H;
 
-    float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (init) S = __ldg(reinterpret_cast<const float4*>(init + bh * PN + e));
+    float S[E];
+#pragma unroll
+    for (int k = 0; k < E; ++k) S[k] = init ? __ldg(init + bh * PN + e + k) : 0.f;
 
     const float* crow = cum2 + bh * T;
     const int64_t cstride = H * PN;                       // chunk stride in dS / Sprev
@@ -56,16 +94,16 @@ state_pass_kernel(const float* __restrict__ dS, const float* __restrict__ cum2,
     // Rolling prefetch: the loads of chunk c + kDepth are issued when chunk c is
     // consumed, so kDepth chunks of dS stay in flight for the whole chain.
     // Addresses advance by running pointers (one chunk = cstride elements).
-    const float* pd = dS + base;                 // next chunk of dS to fetch
+    const TD* pd = dS + base;                    // next chunk of dS to fetch
     const float* pl = crow + L - 1;              // its last token's cum2 (clamped below)
     const float* const plend = crow + T - 1;
     TS* ps = Sprev + base;
-    float4 buf[kDepth];
+    uint4 buf[kDepth];
     float cl[kDepth];
 #pragma unroll
     for (int u = 0; u < kDepth; ++u) {
         if (u < nc) {
-            buf[u] = __ldcs(reinterpret_cast<const float4*>(pd));
+            buf[u] = load16(pd);
             cl[u] = __ldg(pl < plend ? pl : plend);
             pd += cstride;
             pl += L;
@@ -75,29 +113,28 @@ state_pass_kernel(const float* __restrict__ dS, const float* __restrict__ cum2,
 #pragma unroll
         for (int u = 0; u < kDepth; ++u) {
             if (c0 + u < nc) {
-                const float4 d = buf[u];
+                float d[E];
+                widen(buf[u], d);
                 const float dec = ex2(cl[u]);
                 if (c0 + u + kDepth < nc) {
-                    buf[u] = __ldcs(reinterpret_cast<const float4*>(pd));
+                    buf[u] = load16(pd);
                     cl[u] = __ldg(pl < plend ? pl : plend);
                     pd += cstride;
                     pl += L;
                 }
-                store4(ps, S);
+                store_state(ps, S);
                 ps += cstride;
-                S.x = fmaf(dec, S.x, d.x);
-                S.y = fmaf(dec, S.y, d.y);
-                S.z = fmaf(dec, S.z, d.z);
-                S.w = fmaf(dec, S.w, d.w);
+#pragma unroll
+                for (int k = 0; k < E; ++k) S[k] = fmaf(dec, S[k], d[k]);
             }
         }
     }
-    *reinterpret_cast<float4*>(fin + bh * PN + e) = S;
+    store_state(fin + bh * PN + e, S);
 }
 
 }  // namespace
 
-cudaError_t launch_state_pass(const Dims& d, const float* dS, const float* cum2,
+cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const float* cum2,
                               const float* init, void* Sprev, float* final_state,
                               int32_t* /*err*/, cudaStream_t st) {
     const int64_t PN = d.P * d.N;   // multiple of 256 for every supported P, N
@@ -108,16 +145,22 @@ cudaError_t launch_state_pass(const Dims& d, const float* dS, const float* cum2,
         return init ? cudaMemcpyAsync(final_state, init, bytes, cudaMemcpyDeviceToDevice, st)
                     : cudaMemsetAsync(final_state, 0, bytes, st);
     }
-    const int64_t blocks_per_bh = (PN / 4 + kThreads - 1) / kThreads;
+    const int64_t ept = ds16 ? Ept<__nv_bfloat16>::value : Ept<float>::value;
+    const int64_t blocks_per_bh = (PN / ept + kThreads - 1) / kThreads;
     const int64_t grid = d.b * d.H * blocks_per_bh;
-    if (d.dtype == 1)
-        state_pass_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, 0, st>>>(
-            dS, cum2, init, static_cast<__nv_bfloat16*>(Sprev), final_state, d.T, d.H, d.L,
-            d.nc, PN, blocks_per_bh);
+    using bf16 = __nv_bfloat16;
+    if (d.dtype == 1 && ds16)
+        state_pass_kernel<bf16, bf16><<<(unsigned)grid, kThreads, 0, st>>>(
+            static_cast<const bf16*>(dS), cum2, init, static_cast<bf16*>(Sprev), final_state, d.T,
+            d.H, d.L, d.nc, PN, blocks_per_bh);
+    else if (d.dtype == 1)
+        state_pass_kernel<bf16, float><<<(unsigned)grid, kThreads, 0, st>>>(
+            static_cast<const float*>(dS), cum2, init, static_cast<bf16*>(Sprev), final_state, d.T,
+            d.H, d.L, d.nc, PN, blocks_per_bh);
     else
-        state_pass_kernel<float><<<(unsigned)grid, kThreads, 0, st>>>(
-            dS, cum2, init, static_cast<float*>(Sprev), final_state, d.T, d.H, d.L, d.nc, PN,
-            blocks_per_bh);
+        state_pass_kernel<float, float><<<(unsigned)grid, kThreads, 0, st>>>(
+            static_cast<const float*>(dS), cum2, init, static_cast<float*>(Sprev), final_state, d.T,
+            d.H, d.L, d.nc, PN, blocks_per_bh);
     return cudaGetLastError();
 }
 
