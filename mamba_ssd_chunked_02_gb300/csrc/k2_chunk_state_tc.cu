@@ -63,15 +63,16 @@ using namespace tc;
 constexpr int kThreads = 320;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
-template <int L, bool kFuse>
+template <int L, bool kFuse, bool kDS16>
 struct K2Cfg {
     static constexpr int P = 64;
-    // x stages (the fused variant spends shared memory on its state tiles).
-    static constexpr int NS = L == 256 ? (kFuse ? 2 : 3) : 6;
+    // x stages: shared memory left after B^T and the dS staging tiles (the
+    // fused variant spends it on its state tiles instead).
+    static constexpr int NS = L == 256 ? (kFuse ? 2 : (kDS16 ? 4 : 3)) : 6;
     static constexpr int ATOM = L * 128;                  // one 64-wide MN block, L rows
     static constexpr int BT_BYTES = 2 * ATOM;             // two 64-n blocks = M of 128
     static constexpr int X_BYTES = ATOM;                  // P = 64: one block
-    static constexpr int D_BYTES = 64 * 128 * 4;          // one dS tile [p][n-tile] (fp32 max)
+    static constexpr int D_BYTES = 64 * 128 * (kDS16 ? 2 : 4);   // one dS tile [p][n-tile]
     // fused: two buffers of {carried state fp32 [64][128], Sprev bf16 [64][128]}
     static constexpr int F_BYTES = 2 * (64 * 128 * 4 + 64 * 128 * 2);
     static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + (kFuse ? F_BYTES : 2 * D_BYTES);
@@ -128,7 +129,7 @@ struct FuseArgs {
     int nb;                   // batch
 };
 
-template <int L, bool kFuse>
+template <int L, bool kFuse, bool kDS16>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_b,
@@ -138,9 +139,9 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_fin,    // fused: [b H P][N] f32
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
-                      int ds16, int T, int H, int N, int G, int nc, int n_tiles,
+                      int T, int H, int N, int G, int nc, int n_tiles,
                       int hpc, int n_hblk, int32_t* err, const FuseArgs fa) {
-    using C = K2Cfg<L, kFuse>;
+    using C = K2Cfg<L, kFuse, kDS16>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -428,14 +429,14 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                            mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
-                float* tile = sD + ab * (64 * 128);
+                float* tile = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sD) + ab * C::D_BYTES);
                 if (ep == 0) bulk_wait_read<1>();            // the store that used this tile is done
                 if (!group_sync()) break;                    // ... before any warp writes it
 #pragma unroll
                 for (int cc = 0; cc < C::P / 32; ++cc) {
                     uint32_t r[32];
                     tmem_ld32_sync(tmem + ((uint32_t)(32 * q) << 16) + ab * C::P + 32 * cc, r);
-                    if (nl < NT && ds16) {
+                    if (kDS16 && nl < NT) {
                         __nv_bfloat16* t16 = reinterpret_cast<__nv_bfloat16*>(tile);
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -481,14 +482,28 @@ int num_sms() {
     return cached[dev];
 }
 
-// Heads per CTA: the largest divisor of H/G (at most 16) that still gives every
-// SM about four CTAs; with too few work items, one head per CTA.
+// Heads per CTA (one CTA per SM at a time): the largest divisor of H/G, at
+// most 16 (B^T is loaded once per CTA), that gives at least four waves of CTAs
+// and keeps the last wave at least 90 % full; otherwise the divisor with the
+// fullest last wave; with too few work items, one head per CTA.
 int pick_hpc(const Dims& d, int64_t outer) {
     const int hpg = (int)(d.H / d.G);
-    const int64_t want = 4LL * num_sms();
-    for (int v = 16; v >= 1; --v)
-        if (hpg % v == 0 && outer * (d.H / v) >= want) return v;
-    return 1;
+    const int64_t sms = num_sms();
+    int best = 1;
+    double best_eff = -1.0;
+    for (int v = 16; v >= 1; --v) {
+        if (hpg % v) continue;
+        const int64_t ctas = outer * (d.H / v);
+        if (ctas < 4 * sms) continue;
+        const double waves = (double)ctas / (double)sms;
+        const double eff = waves / (double)((ctas + sms - 1) / sms);
+        if (eff >= 0.9) return v;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = v;
+        }
+    }
+    return best;
 }
 
 // Fused variant: the largest divisor of H/G (at most 16) for which one chunk's
@@ -500,11 +515,12 @@ int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
     return 1;
 }
 
-template <int L, bool kFuse>
+template <int L, bool kFuse, bool kDS16>
 cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
-                      const float* dtT, void* dS, bool ds16, const FuseArgs& fa, int32_t* err,
+                      const float* dtT, void* dS, const FuseArgs& fa, int32_t* err,
                       cudaStream_t st) {
-    using C = K2Cfg<L, kFuse>;
+    using C = K2Cfg<L, kFuse, kDS16>;
+    constexpr bool ds16 = kDS16;
     CUtensorMap tm_x, tm_b;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
@@ -546,11 +562,11 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     const int hpc = kFuse ? pick_hpc_fused(d, n_tiles) : pick_hpc(d, outer);
     const int n_hblk = (int)(d.H / hpc);
     const int64_t grid = outer * n_hblk;
-    auto k = chunk_state_tc_kernel<L, kFuse>;
+    auto k = chunk_state_tc_kernel<L, kFuse, kDS16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, tm_ring, tm_init, tm_fin, tm_sp,
-                                                 cum2, dtT, ds16 ? 1 : 0, (int)d.T, (int)d.H,
+                                                 cum2, dtT, (int)d.T, (int)d.H,
                                                  (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
                                                  n_hblk, err, fa);
     return cudaGetLastError();
@@ -571,8 +587,11 @@ cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, c
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     const FuseArgs none{};
-    return d.L == 256 ? launch_k2<256, false>(d, x, B, cum2, dtT, dS, ds16, none, err, st)
-                      : launch_k2<128, false>(d, x, B, cum2, dtT, dS, ds16, none, err, st);
+    if (ds16)
+        return d.L == 256 ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st)
+                          : launch_k2<128, false, true>(d, x, B, cum2, dtT, dS, none, err, st);
+    return d.L == 256 ? launch_k2<256, false, false>(d, x, B, cum2, dtT, dS, none, err, st)
+                      : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st);
 }
 
 int64_t fused_flag_words(const Dims& d) {
@@ -595,8 +614,8 @@ cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void*
     fa.Sprev = static_cast<__nv_bfloat16*>(Sprev);
     fa.fin = final_state;
     fa.nb = (int)d.b;
-    return d.L == 256 ? launch_k2<256, true>(d, x, B, cum2, dtT, nullptr, false, fa, err, st)
-                      : launch_k2<128, true>(d, x, B, cum2, dtT, nullptr, false, fa, err, st);
+    return d.L == 256 ? launch_k2<256, true, false>(d, x, B, cum2, dtT, nullptr, fa, err, st)
+                      : launch_k2<128, true, false>(d, x, B, cum2, dtT, nullptr, fa, err, st);
 }
 
 }  // namespace m2
