@@ -11,11 +11,15 @@
 // dtT[b,h,t]  = dt[b,t,h]
 //
 // One CTA per (chunk, batch, block of 32 heads).  The [L x 32] dt tile is read
-// with coalesced 128-byte rows (32 heads of one token), transposed through
-// shared memory, scanned by one warp per head (each lane owns L/32 consecutive
-// tokens; lane totals are combined with a shuffle scan), and written back as
-// coalesced [h][t] rows.  HBM-bound: 12 bytes per (token, head).  On the fused
-// path the kernel also clears the next kernel's ticket and flag words.
+// with coalesced 128-byte rows (32 heads of one token; 16-byte loads, all of a
+// thread's loads issued before any is stored), transposed into shared memory,
+// scanned by one warp per head (each lane owns L/32 consecutive tokens; lane
+// totals are combined with a shuffle scan), and written back as coalesced
+// [h][t] rows.  The shared tile keeps one padding word per 32 tokens and an odd
+// row pitch, which makes the transposing stores, the per-lane scan and the row
+// reads all free of bank conflicts.  HBM-bound: 12 bytes per (token, head).
+// On the fused path the kernel also clears the next kernel's ticket and flag
+// words.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,13 +29,17 @@ namespace {
 constexpr int kHB = 32;        // heads per CTA
 constexpr int kThreads = 256;  // 8 warps
 
+// Token i of a head's row sits at i + i / 32; rows are `pitch` words apart.
+__device__ __forceinline__ int tpos(int i) { return i + (i >> 5); }
+
 template <int L>
 __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H,
                     int32_t* __restrict__ zero, int64_t nzero) {
-    constexpr int E = L / 32;  // tokens per lane
-    __shared__ float tile[kHB][L + 1];
+    constexpr int E = L / 32;                 // tokens per lane
+    constexpr int kPitch = L + L / 32 + 1;    // odd
+    __shared__ float tile[kHB * kPitch];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
     // Clear the next kernel's synchronisation words (grid-stride).
     if (zero) {
@@ -43,27 +51,47 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     const int nt = (int)min((int64_t)L, T - t0);
     const int nh = (int)min((int64_t)kHB, H - h0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* src = dt + (b * T + t0) * H + h0;
 
-    // Load [nt x nh] (token-major in HBM), transpose into tile[head][token].
-    for (int idx = threadIdx.x; idx < L * kHB; idx += kThreads) {
-        const int i = idx / kHB, j = idx % kHB;
-        float v = 0.f;
-        if (i < nt && j < nh) v = __ldg(dt + (b * T + t0 + i) * H + h0 + j);
-        tile[j][i] = v;
+    // Load [nt x nh] (token-major in HBM) and transpose into tile[head][token].
+    if (nh == kHB && (H & 3) == 0) {
+        // 8 float4 per token row; element (token i, quad q) of item idx = i * 8 + q.
+        constexpr int kPer = L * kHB / 4 / kThreads;
+        float4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + kThreads * k, i = idx >> 3, q = idx & 7;
+            v[k] = i < nt ? __ldg(reinterpret_cast<const float4*>(src + (int64_t)i * H) + q)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int idx = threadIdx.x + kThreads * k, i = idx >> 3, j = 4 * (idx & 7);
+            tile[(j + 0) * kPitch + tpos(i)] = v[k].x;
+            tile[(j + 1) * kPitch + tpos(i)] = v[k].y;
+            tile[(j + 2) * kPitch + tpos(i)] = v[k].z;
+            tile[(j + 3) * kPitch + tpos(i)] = v[k].w;
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < L * kHB; idx += kThreads) {
+            const int i = idx / kHB, j = idx % kHB;
+            tile[j * kPitch + tpos(i)] = (i < nt && j < nh) ? __ldg(src + (int64_t)i * H + j) : 0.f;
+        }
     }
     __syncthreads();
 
     for (int j = warp; j < nh; j += kThreads / 32) {
         const int64_t row = (b * H + h0 + j) * T + t0;
+        float* trow = tile + j * kPitch;
         // dtT row: coalesced.
-        for (int i = lane; i < nt; i += 32) dtT[row + i] = tile[j][i];
+        for (int i = lane; i < nt; i += 32) dtT[row + i] = trow[tpos(i)];
         __syncwarp();
         const float a2 = __ldg(A + h0 + j) * kLog2e;
         float s[E];
         float run = 0.f;
 #pragma unroll
         for (int k = 0; k < E; ++k) {
-            run += tile[j][lane * E + k] * a2;   // tokens past T hold 0
+            run += trow[tpos(lane * E + k)] * a2;   // tokens past T hold 0
             s[k] = run;
         }
         float tot = run;
@@ -75,9 +103,9 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
         const float excl = tot - run;
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < E; ++k) tile[j][lane * E + k] = s[k] + excl;
+        for (int k = 0; k < E; ++k) trow[tpos(lane * E + k)] = s[k] + excl;
         __syncwarp();
-        for (int i = lane; i < nt; i += 32) cum2[row + i] = tile[j][i];
+        for (int i = lane; i < nt; i += 32) cum2[row + i] = trow[tpos(i)];
     }
 }
 
