@@ -204,6 +204,14 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
                                    const void* Sprev, const float* D,
                                    void* y, void* stream);
 
+/* Bits of the device-side error word. */
+#define MAMBA2_DEVERR_TIMEOUT_CHUNK_STATE 1   /* a wait ran out in the stage-2 kernel */
+#define MAMBA2_DEVERR_TIMEOUT_CHUNK_OUT 2     /* ... in the stage-4 kernel */
+#define MAMBA2_DEVERR_LAUNCH_CONFIG 4         /* a kernel saw a launch it does not support */
+#define MAMBA2_DEVERR_CHAIN 8                 /* the fused stage 2+3 kernel gave up waiting
+                                                 for the previous chunk's state */
+#define MAMBA2_DEVERR_SELFTEST 16             /* mamba2_ssd_selftest_wait_timeout ran out */
+
 /* Device-side error word.  The tensor-core kernels bound every wait; a wait
  * that runs out sets a bit here and the kernel returns early (its outputs are
  * then invalid).  This call synchronises the current device, reads the word
@@ -211,6 +219,15 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
  * MAMBA2_ERR_DEVICE when the word was nonzero, MAMBA2_ERR_CUDA on a CUDA
  * failure, MAMBA2_OK otherwise. */
 MAMBA2_API mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear);
+
+/* Diagnostic (no counterpart on the pages): launches one small kernel whose
+ * bounded waits -- on an mbarrier nothing arrives at and on a global flag
+ * nothing sets, the two kinds of wait the kernels use -- run out after
+ * `limit_us` microseconds (1 .. 100000).  The kernel then sets
+ * MAMBA2_DEVERR_SELFTEST in the device error word and returns normally; the
+ * context stays usable.  Lets a caller check the failure path without a fault.
+ * Returns MAMBA2_OK once queued, MAMBA2_ERR_INVALID_ARG for a limit out of range. */
+MAMBA2_API mamba2_status mamba2_ssd_selftest_wait_timeout(uint32_t limit_us, void* stream);
 
 /* Forward pass for callers that cannot allocate device memory.
  *

@@ -40,7 +40,8 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_ssd_fwd", "mamba2_ssd_chunk_cumsum", "mamba2_ssd_chunk_state",
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
-           "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size")
+           "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
+           "mamba2_ssd_selftest_wait_timeout")
 
 
 class Shape(ctypes.Structure):
@@ -106,6 +107,8 @@ def load():
         lib.mamba2_ssd_chunk_state_pass_workspace_size.restype = ctypes.c_size_t
         lib.mamba2_ssd_chunk_state_pass.argtypes = [sp] + [vp] * 7 + [vp, ctypes.c_size_t, vp]
         lib.mamba2_ssd_chunk_state_pass.restype = ctypes.c_int
+        lib.mamba2_ssd_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.mamba2_ssd_selftest_wait_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -264,6 +267,16 @@ def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
         _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
         _ptr(Sprev, "Sprev", _io_dtype(shape), (b, nc, H, P, N)),
         _ptr(final_state, "final_state", torch.float32, (b, H, P, N)), _stream(stream)))
+
+
+DEVERR_SELFTEST = 16
+
+
+def selftest_wait_timeout(limit_us=1000, stream=None):
+    """Queue the wait self-test: bounded waits that nothing releases run out after
+    `limit_us` and set DEVERR_SELFTEST in the device error word."""
+    _check("mamba2_ssd_selftest_wait_timeout",
+           load().mamba2_ssd_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def chunk_state_pass_workspace_size(shape: Shape) -> int:

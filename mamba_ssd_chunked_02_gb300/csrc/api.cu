@@ -295,6 +295,12 @@ mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear) {
     return v ? MAMBA2_ERR_DEVICE : MAMBA2_OK;
 }
 
+mamba2_status mamba2_ssd_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 100000) return MAMBA2_ERR_INVALID_ARG;
+    return from_cuda(m2::launch_wait_timeout_selftest((uint64_t)limit_us * 1000, error_word(),
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
 const char* mamba2_status_string(mamba2_status status) {
     switch (status) {
         case MAMBA2_OK: return "ok";

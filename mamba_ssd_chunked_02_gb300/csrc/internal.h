@@ -64,6 +64,9 @@ cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, con
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st);
 
+// Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);
+
 // True when the tcgen05 kernels handle this shape.
 bool tc_supported(const Dims& d);
 
@@ -73,6 +76,7 @@ enum : int32_t {
     kErrTimeoutK4 = 1 << 1,    // ... in the tcgen05 chunk-output kernel
     kErrLaunchCfg = 1 << 2,    // a kernel saw a launch configuration it does not support
     kErrChainK23 = 1 << 3,     // the fused stage 2+3 kernel gave up waiting for the previous chunk
+    kErrSelfTest = 1 << 4,     // the wait self-test's waits ran out (expected)
 };
 
 }  // namespace m2

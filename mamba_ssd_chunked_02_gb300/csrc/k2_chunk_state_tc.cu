@@ -92,32 +92,6 @@ struct K2Bars {
     int item;               // work item (ticket on the fused path)
 };
 
-// Global-memory flag words of the fused variant (gpu scope).
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Wait until *f is 1 (published) for at most limit_ns; -1 (the predecessor gave
-// up) or a timeout raise *abort and return false.
-__device__ __forceinline__ bool wait_flag(const int32_t* f, volatile int* abort, uint64_t limit_ns) {
-    int v = ld_acquire_gpu(f);
-    if (v == 1) return true;
-    const uint64_t t0 = globaltimer();
-    while (v != 1) {
-        if (v < 0 || *abort || globaltimer() - t0 > limit_ns) {
-            *abort = 1;
-            return false;
-        }
-        __nanosleep(128);
-        v = ld_acquire_gpu(f);
-    }
-    return true;
-}
-
 // Arguments used by the fused variant only (null on the plain one).
 struct FuseArgs {
     const float* init;        // [b][H][P][N] fp32 or null (zero initial state)

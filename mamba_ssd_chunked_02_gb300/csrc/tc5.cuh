@@ -104,6 +104,32 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
     return true;
 }
 
+// Flag words in global memory (gpu scope), for hand-offs between CTAs.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *f is 1 (published) for at most limit_ns; -1 (the predecessor gave
+// up) or a timeout raise *abort and return false.
+__device__ __forceinline__ bool wait_flag(const int32_t* f, volatile int* abort, uint64_t limit_ns) {
+    int v = ld_acquire_gpu(f);
+    if (v == 1) return true;
+    const uint64_t t0 = globaltimer();
+    while (v != 1) {
+        if (v < 0 || *abort || globaltimer() - t0 > limit_ns) {
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(128);
+        v = ld_acquire_gpu(f);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");

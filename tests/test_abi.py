@@ -165,6 +165,11 @@ def test_fused_stage_workspace_and_validation(lib):
     assert rc == m2.ERR_WORKSPACE                               # too small
 
 
+def test_selftest_limit_is_validated_on_the_host(lib):
+    assert lib.mamba2_ssd_selftest_wait_timeout(0, None) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_selftest_wait_timeout(100001, None) == m2.ERR_INVALID_ARG
+
+
 def test_empty_problem_is_a_noop(lib):
     # batch 0: nothing to do, no pointer needed, no CUDA call.
     s = shp(batch=0)
