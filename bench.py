@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the single-token decode step on the workload's state instead")
     ap.add_argument("--fused-state", action="store_true",
                     help="time stages 2+3 as the one fused kernel (mamba2_ssd_chunk_state_pass)")
     ap.add_argument("--batch", type=int, default=0,
@@ -261,6 +263,55 @@ def config_of(w, n):
 
 
 # ------------------------------------------------------------------- GPU leg ---
+def run_decode(args, w):
+    """Decode step (mamba2_ssd_decode) on the workload's (b, H, P, N) state: one
+    token per sequence per step; an HBM stream of the state (read + write)."""
+    import torch
+    import mamba_ssd_chunked_02_gb300 as m2
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+    wd = w.scaled(seqlen=1, init_std=0.1)
+    inp = W.make_inputs(wd)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    b, H, P, N, G = wd.batch, wd.nheads, wd.headdim, wd.dstate, wd.ngroups
+    states = [dev["initial_state"].clone() for _ in range(8)]   # 8 x 21 MB > L2: no flush needed
+    x, dt, B, C = dev["x"][:, 0], dev["dt"][:, 0], dev["B"][:, 0], dev["C"][:, 0]
+    y = torch.empty((b, H, P), dtype=x.dtype, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(max(3, args.warmup)):
+        m2.ssd_decode(states[i % 8], x, dt, dev["A"], B, C, dev["D"], y=y)
+    torch.cuda.synchronize()
+    K = args.steps
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    a.record(stream)
+    for i in range(K):
+        m2.ssd_decode(states[i % 8], x, dt, dev["A"], B, C, dev["D"], y=y)
+    z.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(wall0, time.time())
+    if m2.device_error() != 0:
+        raise RuntimeError("device-side error in the decode loop")
+    ms = a.elapsed_time(z) / K
+    E = 2 if wd.dtype == "bf16" else 4
+    nbytes = 8 * b * H * P * N + b * H * (2 * P * E + 4) + 2 * b * G * N * E
+    pk, src = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "SSD decode step: tokens/s (one token per sequence) at the workload's state",
+        "value": b / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16" if wd.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": {"workload": wd.name, "batch": b, "nheads": H, "headdim": P,
+                                         "dstate": N, "ngroups": G,
+                                         "l2": "8 rotating states of 21 MB (> L2 together)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "decode",
+                     "algorithmic_bytes": nbytes},
+        "gpu_launches": K, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse_args()
     w = workload(args.workload)
@@ -280,6 +331,10 @@ def main():
     from mamba_ssd_chunked_02_gb300 import workloads as W
 
     torch.cuda.set_device(local)
+    if args.decode:
+        if rank == 0:
+            run_decode(args, w)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist

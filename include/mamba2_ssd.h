@@ -204,6 +204,22 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
                                    const void* Sprev, const float* D,
                                    void* y, void* stream);
 
+/* Single-token decode step, the recurrent form of the same model
+ * [P2 "Mamba-2 아키텍처의 핵심 연산": y_t = c_t^T h_t + D x_t], on the state layout of
+ * mamba2_ssd_fwd's final_state, for each (b, h):
+ *   state <- exp(dt A) state + dt x B^T   (in place, fp32)
+ *   y      = state C + D x
+ * shape: batch, nheads, headdim, dstate, ngroups, dtype as for mamba2_ssd_fwd;
+ * seqlen must be 1; chunk_size is not used (any supported value); flags 0.
+ *   state [b,H,P,N] fp32, read and written; x [b,H,P] (dtype); dt [b,H] fp32;
+ *   A [H] fp32; B, C [b,G,N] (dtype); D [H] fp32 or NULL (= 0); y [b,H,P] (dtype).
+ * Feeding the final_state of a prefix to this call token by token continues the
+ * sequence (tested against mamba2_ssd_fwd over the whole sequence). */
+MAMBA2_API mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float* state,
+                                const void* x, const float* dt, const float* A,
+                                const void* B, const void* C, const float* D,
+                                void* y, void* stream);
+
 /* Bits of the device-side error word. */
 #define MAMBA2_DEVERR_TIMEOUT_CHUNK_STATE 1   /* a wait ran out in the stage-2 kernel */
 #define MAMBA2_DEVERR_TIMEOUT_CHUNK_OUT 2     /* ... in the stage-4 kernel */

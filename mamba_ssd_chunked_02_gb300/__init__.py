@@ -41,7 +41,7 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
            "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
-           "mamba2_ssd_selftest_wait_timeout")
+           "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode")
 
 
 class Shape(ctypes.Structure):
@@ -109,6 +109,8 @@ def load():
         lib.mamba2_ssd_chunk_state_pass.restype = ctypes.c_int
         lib.mamba2_ssd_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.mamba2_ssd_selftest_wait_timeout.restype = ctypes.c_int
+        lib.mamba2_ssd_decode.argtypes = [sp] + [vp] * 9
+        lib.mamba2_ssd_decode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -270,6 +272,25 @@ def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
 
 
 DEVERR_SELFTEST = 16
+
+
+def ssd_decode(state, x, dt, A, B, C, D=None, *, y=None, stream=None):
+    """One decode step (mamba2_ssd_decode): updates `state` [b,H,P,N] f32 in place
+    and returns y [b,H,P].  x [b,H,P], dt [b,H] f32, A [H] f32, B/C [b,G,N]
+    (x's dtype), D [H] f32 or None."""
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    io = x.dtype
+    sh = make_shape(b, 1, H, P, N, G, 64, _dtype_code(io), 0)
+    if y is None:
+        y = torch.empty((b, H, P), dtype=io, device=x.device)
+    _check("mamba2_ssd_decode", load().mamba2_ssd_decode(
+        ctypes.byref(sh), _ptr(state, "state", torch.float32, (b, H, P, N)),
+        _ptr(x, "x", io, (b, H, P)), _ptr(dt, "dt", torch.float32, (b, H)),
+        _ptr(A, "A", torch.float32, (H,)), _ptr(B, "B", io, (b, G, N)),
+        _ptr(C, "C", io, (b, G, N)), _ptr(D, "D", torch.float32, (H,), optional=True),
+        _ptr(y, "y", io, (b, H, P)), _stream(stream)))
+    return y
 
 
 def selftest_wait_timeout(limit_us=1000, stream=None):

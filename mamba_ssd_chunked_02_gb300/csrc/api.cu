@@ -295,6 +295,22 @@ mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear) {
     return v ? MAMBA2_ERR_DEVICE : MAMBA2_OK;
 }
 
+mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float* state, const void* x,
+                                const float* dt, const float* A, const void* B, const void* C,
+                                const float* D, void* y, void* stream) {
+    if (!shape) return MAMBA2_ERR_INVALID_ARG;
+    if (shape->seqlen != 1 || shape->flags != 0) return MAMBA2_ERR_INVALID_ARG;
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.H == 0;
+    if (!req(state, empty) || !req(x, empty) || !req(dt, empty) || !req(A, empty) ||
+        !req(B, empty) || !req(C, empty) || !opt(D) || !req(y, empty))
+        return MAMBA2_ERR_INVALID_ARG;
+    return from_cuda(m2::launch_decode(d, state, x, dt, A, B, C, D, y,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 mamba2_status mamba2_ssd_selftest_wait_timeout(uint32_t limit_us, void* stream) {
     if (limit_us < 1 || limit_us > 100000) return MAMBA2_ERR_INVALID_ARG;
     return from_cuda(m2::launch_wait_timeout_selftest((uint64_t)limit_us * 1000, error_word(),

@@ -64,6 +64,10 @@ cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, con
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st);
 
+// One recurrent step per (b, h): S <- exp(dt A) S + dt x B^T in place, y = S C + D x.
+cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* dt, const float* A,
+                          const void* B, const void* C, const float* D, void* y, cudaStream_t st);
+
 // Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);
 

@@ -170,6 +170,18 @@ def test_selftest_limit_is_validated_on_the_host(lib):
     assert lib.mamba2_ssd_selftest_wait_timeout(100001, None) == m2.ERR_INVALID_ARG
 
 
+def test_decode_validates_without_launching(lib):
+    vp = ctypes.c_void_p
+    g = vp(1 << 20)
+    s = shp(seqlen=1)
+    assert lib.mamba2_ssd_decode(ctypes.byref(shp(seqlen=2)), *([g] * 9)) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_decode(ctypes.byref(s), None, *([g] * 7), None) == m2.ERR_INVALID_ARG
+    assert lib.mamba2_ssd_decode(ctypes.byref(shp(seqlen=1, dstate=96)), *([g] * 8), None) == \
+        m2.ERR_UNSUPPORTED
+    s0 = shp(seqlen=1, batch=0)
+    assert lib.mamba2_ssd_decode(ctypes.byref(s0), *([None] * 8), None) == m2.OK
+
+
 def test_empty_problem_is_a_noop(lib):
     # batch 0: nothing to do, no pointer needed, no CUDA call.
     s = shp(batch=0)
