@@ -26,12 +26,15 @@
 //   [384, 512)      G: two 64-column fp32 accumulators of M . X
 // Per head: GEMM3 S = C . Sprev^T (A = C tile, B = Sprev, both K-major in
 // shared memory); the epilogue builds M from CB: the causal mask comes
-// from the row/column indices and is applied before exp2; below the warp's
-// diagonal 32x32 block the decay is split as
-// exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the warp's first row, so
-// both factors are <= 1 and only the diagonal block needs one exp2 per
-// element; on the fp16 path the two multiplies of a below-diagonal entry are
-// packed fp16 multiplies, two keys per instruction.  GEMM2 G = M . X in two
+// from the row/column indices; below the warp's diagonal 32x32 block the
+// decay is split as exp2(cum2_t - cum2_r) * exp2(cum2_r - cum2_s) with r the
+// warp's first row, so both factors are <= 1; on the fp16 path the two
+// multiplies of a below-diagonal entry are packed fp16 multiplies, two keys
+// per instruction.  The diagonal block takes its last key m as reference:
+// exp2(cum2_t - cum2_m) in [1, 2^R] times exp2(cum2_m - cum2_s) in [2^-R, 1]
+// times dt_s, packed fp16 and masked after the product, when its cum2 range R
+// is at most 14 and every dt_s of the block is a normal fp16 number; otherwise
+// one exp2 per element in fp32 with the mask applied before the exp2.  GEMM2 G = M . X in two
 // K-halves (A from tensor memory, X MN-major in shared memory), so that the
 // tensor core works on one half while
 // the epilogue builds the other.  Once the next head's M is handed over, the
@@ -454,8 +457,24 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (use16) vh[32 * j + lane] = __float2half_rn(v);
                 else vq[32 * j + lane] = v;
             }
+            // Diagonal block on the fp16 path, with its last key m as reference:
+            // exp2(cum2_t - cum2_s) = u_t w_s, u_t = exp2(cum2_t - cum2_m) in [1, 2^R],
+            // w_s = exp2(cum2_m - cum2_s) in [2^-R, 1] (R = the block's cum2 range),
+            // then times dt_s.  All three stay normal fp16 numbers when R <= 14 and
+            // every dt_s of the block is >= 2^-14; otherwise the fp32 path below.
+            // The causal mask is applied to the final product.
+            const float cml = ck[32 * jd + 31];
+            const bool owner = jd % EG == grp;
+            const float dsd = dk[32 * jd + lane];
+            const bool dpack = use16 && cr - cml <= 14.f &&
+                               !__any_sync(0xffffffffu, owner && dsd < 6.1035156e-5f);
+            if (dpack && owner) {
+                vh[32 * jd + lane] = __float2half_rn(ex2(cml - ck[32 * jd + lane]));
+                vh[32 * jd + 32 + lane] = __float2half_rn(dsd);
+            }
             __syncwarp();
             const __half2 u2 = __float2half2_rn(u_t);
+            const __half2 ud2 = __float2half2_rn(ex2(ct - cml));
 
             // ---- M, in two K-halves.
             for (int half = 0; half < 2 && ok; ++half) {
@@ -485,6 +504,26 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                 const __half2 uv = __hmul2(u2, *reinterpret_cast<const __half2*>(&vw[k2]));
                                 const __half2 mm2 = __hmul2(cb2, uv);
                                 m[4 * e8 + k2] = *reinterpret_cast<const uint32_t*>(&mm2);
+                            }
+                        }
+                        if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
+                    } else if (j == jd && dpack) {
+                        const uint4* w4 = reinterpret_cast<const uint4*>(vh + 32 * j);
+                        const uint4* d4 = reinterpret_cast<const uint4*>(vh + 32 * j + 32);
+#pragma unroll
+                        for (int e8 = 0; e8 < 4; ++e8) {
+                            const uint4 ww = w4[e8], dd = d4[e8];
+                            const uint32_t wv[4] = {ww.x, ww.y, ww.z, ww.w};
+                            const uint32_t dv[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2) {
+                                const int e = 4 * e8 + k2;          // keys 2e, 2e+1 of the block
+                                const __half2 cb2 = *reinterpret_cast<const __half2*>(&r[e]);
+                                const __half2 uw = __hmul2(ud2, *reinterpret_cast<const __half2*>(&wv[k2]));
+                                const __half2 cd = __hmul2(cb2, *reinterpret_cast<const __half2*>(&dv[k2]));
+                                const __half2 mm2 = __hmul2(cd, uw);
+                                const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm2);
+                                m[e] = 2 * e + 1 <= lane ? mw : (2 * e <= lane ? (mw & 0xffffu) : 0u);
                             }
                         }
                         if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
