@@ -49,9 +49,9 @@
 // <= 2^15 (|M| is at most that product, every decay being <= 1) -- and
 // otherwise keep bf16 for that head (x stays untouched, M is packed as bf16).
 //
-// Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner),
-// 2 .. 2+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column group
-// (warp-2)/4), the last kConvWarps = converters.  Loads stream through a ring
+// Warp roles: 0, 1 = converters, 2 = TMA producer, 3 = MMA issuer (+ TMEM
+// owner), 4 .. 4+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column
+// group (warp-4)/4).  Loads stream through a ring
 // of NS stages: first the B blocks of GEMM1 (64 state dims each), then per
 // head x (KS rows) and Sprev.  As soon as a head's stage lands, the converters
 // copy its cum2 and dt rows into that stage's vector buffers, take the range
@@ -76,6 +76,14 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kConvWarps = 2;                 // converter warps
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
+// Warp roles.  A warp issues from sub-partition (warp index % 4); the
+// converters share theirs with the lightly loaded epilogue warps of lane
+// quadrants 0 and 1, the producer and MMA warps (mostly waiting) with the
+// busiest epilogue warps (quadrants 2 and 3, which own the most key blocks).
+constexpr int kWarpProd = kConvWarps;            // converters: warps 0 .. kConvWarps-1
+constexpr int kWarpMma = kConvWarps + 1;
+constexpr int kEpiWarp0 = kConvWarps + 2;        // epilogue: kEpiWarp0 .. kEpiWarp0 + kEpiWarps - 1
+static_assert(kEpiWarp0 % 4 == 0, "epilogue warp w accesses TMEM lane quadrant w % 4");
 constexpr int PC = 64 / EG;                   // y columns per epilogue group
 static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread");
 // Tensor-memory columns: C.B^T as 16-bit pairs, M as 16-bit pairs, and two
@@ -185,7 +193,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         bars.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
     }
@@ -194,7 +202,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 0) {
+    if (warp == kWarpProd) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tm_x);
@@ -233,7 +241,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ----------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t c_addr = smem_u32(sC);
@@ -304,12 +312,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 mbar_wait(&bars.drain, 0, kWaitNs);
             }
         }
-    } else if (warp < 2 + kEpiWarps) {
+    } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 2;                       // 0 .. kEpiWarps-1
+        const int ew = warp - kEpiWarp0;               // 0 .. kEpiWarps-1
         const int q = warp & 3;                        // TMEM lane quadrant
         const int grp = ew >> 2;                       // column group
-        const int etid = threadIdx.x - 64;             // 0 .. kEpiThreads-1
+        const int etid = threadIdx.x - 32 * kEpiWarp0; // 0 .. kEpiThreads-1
         const int tl = 32 * q + lane;                  // row within the tile
         const int tc_ = 128 * qt + tl;                 // row within the chunk
         const int jd = 4 * qt + q;                     // this warp's diagonal key block
@@ -599,7 +607,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // the range check (max |x| over the x tile, max dt) and, when fp16 cannot
         // overflow, the x tile converted to fp16 in place.  They run ahead of the
         // epilogue warps, which then only build M and write y.
-        const int ctid = threadIdx.x - 64 - kEpiThreads;   // 0 .. kConvThreads-1
+        const int ctid = threadIdx.x;                  // 0 .. kConvThreads-1
         const int cw = ctid >> 5;
         uint32_t sync_phase = 0;
         auto conv_sync = [&]() -> bool {
@@ -698,7 +706,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
