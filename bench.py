@@ -486,47 +486,75 @@ def main():
                 "launches_per_step": 3 if fused else 4}
     del fwd_ws
 
-    # End to end through ssd_fwd with pinned host buffers.
+    # End to end through ssd_fwd with pinned host buffers: every step copies its
+    # inputs in (H2D) and its outputs y and final_state out (D2H).  Steps are
+    # pipelined as a serving loop would run them: step i+1's inputs go in and step
+    # i-1's outputs come out on two copy streams while step i computes, with two
+    # device copies of every input and output.
     e2e = None
     if not args.no_e2e:
         host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inp_cpu.items()}
-        y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-        f_host = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+        f_host = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory() for _ in range(2)]
         ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
+        din = [dev, {k: (torch.empty_like(v) if v is not None else None) for k, v in dev.items()}]
+        ydev = [y, torch.empty_like(y)]
+        fdev = [fin, torch.empty_like(fin)]
         h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
-        d2h = y_host.numel() * y_host.element_size() + f_host.numel() * f_host.element_size()
+        d2h = y_host[0].numel() * y_host[0].element_size() + f_host[0].numel() * f_host[0].element_size()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
-        def e2e_step():
-            for k, v in host_in.items():
-                if v is not None:
-                    dev[k].copy_(v, non_blocking=True)
-            m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                       dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
-                       y=y, final_state=fin, workspace=ws)
-            y_host.copy_(y, non_blocking=True)
-            f_host.copy_(fin, non_blocking=True)
+        def run_e2e(n):
+            ev_in = [torch.cuda.Event() for _ in range(n)]
+            ev_comp = [torch.cuda.Event() for _ in range(n)]
+            ev_out = [torch.cuda.Event() for _ in range(n)]
+            a = torch.cuda.Event(enable_timing=True)
+            z = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            s_in.wait_event(a)
+            s_out.wait_event(a)
+            for i in range(n):
+                j = i & 1
+                with torch.cuda.stream(s_in):          # inputs of step i
+                    if i >= 2:
+                        s_in.wait_event(ev_comp[i - 2])   # step i-2 is done reading them
+                    for k, v in host_in.items():
+                        if v is not None:
+                            din[j][k].copy_(v, non_blocking=True)
+                    ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])            # compute of step i
+                if i >= 2:
+                    stream.wait_event(ev_out[i - 2])   # step i-2's outputs are out
+                d = din[j]
+                m2.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
+                           chunk_size=w.chunk_size, ngroups=w.ngroups, y=ydev[j],
+                           final_state=fdev[j], workspace=ws, stream=stream)
+                ev_comp[i].record(stream)
+                with torch.cuda.stream(s_out):         # outputs of step i
+                    s_out.wait_event(ev_comp[i])
+                    y_host[j].copy_(ydev[j], non_blocking=True)
+                    f_host[j].copy_(fdev[j], non_blocking=True)
+                    ev_out[i].record(s_out)
+            stream.wait_event(ev_out[n - 1])
+            z.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(z)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        ke = max(1, args.e2e_steps)
-        a = torch.cuda.Event(enable_timing=True)
-        z = torch.cuda.Event(enable_timing=True)
+        run_e2e(3)
+        ke = max(2, args.e2e_steps)
         if dist:
             dist.barrier()
-        a.record(stream)
-        for _ in range(ke):
-            e2e_step()
-        z.record(stream)
-        torch.cuda.synchronize()
-        ems = a.elapsed_time(z)
+        ems = run_e2e(ke)
         if dist:
             tt = torch.tensor([ems], device="cuda")
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             ems = float(tt.item())
+        if m2.device_error() != 0:
+            raise RuntimeError("device-side error in the end-to-end loop")
         e2e = {"value": tokens / (ems / ke * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": ke,
-               "ms_per_step": ems / ke}
+               "ms_per_step": ems / ke,
+               "pipelined": "H2D of step i+1 and D2H of step i-1 overlap step i"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
