@@ -254,6 +254,28 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------- multi-rank host ---
+def rank_workload(w, rank):
+    """The problem rank `rank` runs: the same shape, its own batch of sequences
+    (inputs drawn from seed + rank), so ranks share no data and need no collective."""
+    return w.scaled(seed=w.seed + rank)
+
+
+def max_over_ranks(value, dist, device):
+    """A time measured on every rank -> the slowest rank's (the job's) time."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens(w, world):
+    """Tokens the whole job processes per step (weak scaling: one batch per rank)."""
+    return w.tokens * world
+
+
 def config_of(w, n):
     return {"workload": w.name, "batch": w.batch, "seq_len": w.seqlen, "nheads": w.nheads,
             "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
@@ -340,7 +362,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    inp_cpu = W.make_inputs(w.scaled(seed=w.seed + rank))
+    inp_cpu = W.make_inputs(rank_workload(w, rank))
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
     b, T, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
     sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
@@ -410,11 +432,7 @@ def main():
     if m2.device_error() != 0:
         raise RuntimeError("device-side error in the timed region")
 
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, "cuda")
     ms_step = total_ms / K
     per = {k: 0.0 for k in KERNELS}
     for i in range(K):
@@ -427,7 +445,7 @@ def main():
 
     kmodel, graded_bytes, flops = model(w, 2 if (dS is not None and dS.dtype == torch.bfloat16) else 4)
     pk, pk_src = peaks()
-    tokens = w.tokens * world
+    tokens = job_tokens(w, world)
     value = tokens / (ms_step * 1e-3)
 
     dom = max(per, key=per.get)
@@ -544,11 +562,7 @@ def main():
         ke = max(2, args.e2e_steps)
         if dist:
             dist.barrier()
-        ems = run_e2e(ke)
-        if dist:
-            tt = torch.tensor([ems], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ems = float(tt.item())
+        ems = max_over_ranks(run_e2e(ke), dist, "cuda")
         if m2.device_error() != 0:
             raise RuntimeError("device-side error in the end-to-end loop")
         e2e = {"value": tokens / (ems / ke * 1e-3), "unit": "tokens/s",
