@@ -50,7 +50,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_run_independent_batches_and_report_the_slowest():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         r0, r1 = out[0], out[1]
