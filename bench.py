@@ -7,9 +7,10 @@ A step is one pass of the whole hot path -- chunk cumsum, chunk states, state
 pass, fused output -- over one batch of the workload (b=8, T=4096, H=80, P=64,
 N=128, G=1, L=256, bf16; x is 335 MB, larger than L2, so nothing is flushed
 between steps).  Inputs are seeded synthetic tensors, resident in HBM before
-the timed region.  The four stages are launched through the C ABI's stage
-entry points with CUDA events between them on the launching stream, so the
-per-kernel times and the whole-step time come from the same timed region.
+the timed region.  Each step is one whole-path call through the C ABI
+(mamba2_ssd_fwd_timed, the same launches as mamba2_ssd_fwd) that records CUDA
+events between its stages on the launching stream, so the per-kernel times and
+the whole-step time come from the same timed region.
 
 Printed (one JSON line, rank 0): tokens/s (value), TFLOP/s, per-kernel times,
 the roofline of the dominant kernel, the whole-path roofline under the fixed
@@ -366,42 +367,22 @@ def main():
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
     b, T, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
     sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
-    nc = sh.nchunks
     f32 = dict(dtype=torch.float32, device="cuda")
-    cum2 = torch.empty((b, H, T), **f32)
-    dtT = torch.empty((b, H, T), **f32)
     fused = args.fused_state and m2.chunk_state_pass_workspace_size(sh) > 0
     KERNELS = KERNELS_FUSED if fused else KERNELS_SPLIT
-    if fused:
-        dS = None
-        sp_ws = torch.empty(m2.chunk_state_pass_workspace_size(sh), dtype=torch.uint8, device="cuda")
-    else:
-        # The whole-path call hands dS from stage 2 to 3 in bf16 on the tensor-core path.
-        ds_bf16 = m2.path(sh) == m2.PATH_TCGEN05
-        dS = torch.empty((b, nc, H, P, N), dtype=torch.bfloat16 if ds_bf16 else torch.float32,
-                         device="cuda")
-    Sprev = torch.empty((b, nc, H, P, N), dtype=w.torch_dtype, device="cuda")
+    flags = m2.FLAG_FUSED_STATE if fused else 0
     y = torch.empty((b, T, H, P), dtype=w.torch_dtype, device="cuda")
     fin = torch.empty((b, H, P, N), **f32)
+    ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    # event k of a step: before stage 1 (k = 0) and after stages 1..4 (k = 1..4)
+    bounds = (0, 1, 3, 4) if fused else (0, 1, 2, 3, 4)
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        m2.chunk_cumsum(sh, dev["dt"], dev["A"], cum2, dtT, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        if fused:
-            m2.chunk_state_pass(sh, dev["x"], dev["B"], cum2, dtT, dev["initial_state"], Sprev, fin,
-                                sp_ws, stream)
-        else:
-            m2.chunk_state(sh, dev["x"], dev["B"], cum2, dtT, dS, stream)
-            if ev is not None:
-                ev[2].record(stream)
-            m2.state_pass(sh, dS, cum2, dev["initial_state"], Sprev, fin, stream)
-        if ev is not None:
-            ev[len(KERNELS) - 1].record(stream)
-        m2.chunk_out(sh, dev["x"], dev["B"], dev["C"], cum2, dtT, Sprev, dev["D"], y, stream)
+        """One step = one whole-path call (mamba2_ssd_fwd, or _fwd_timed with events)."""
+        m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                   dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups, y=y,
+                   final_state=fin, workspace=ws, stream=stream, flags=flags, events=ev)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -410,7 +391,11 @@ def main():
         raise RuntimeError("device-side error during warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS))] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for e in evs:                  # create the CUDA events before the timed region
+        for x_ in e:
+            x_.record(stream)
+    torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -437,13 +422,12 @@ def main():
     per = {k: 0.0 for k in KERNELS}
     for i in range(K):
         e = evs[i]
-        nxt = evs[i + 1][0] if i + 1 < K else t_end
-        marks = list(e) + [nxt]
         for j, kname in enumerate(KERNELS):
-            per[kname] += marks[j].elapsed_time(marks[j + 1])
+            per[kname] += e[bounds[j]].elapsed_time(e[bounds[j + 1]])
     per = {k: v / K for k, v in per.items()}
 
-    kmodel, graded_bytes, flops = model(w, 2 if (dS is not None and dS.dtype == torch.bfloat16) else 4)
+    # the whole-path call hands dS from stage 2 to 3 in bf16 on the tensor-core path
+    kmodel, graded_bytes, flops = model(w, 2 if m2.path(sh) == m2.PATH_TCGEN05 else 4)
     pk, pk_src = peaks()
     tokens = job_tokens(w, world)
     value = tokens / (ms_step * 1e-3)
@@ -478,32 +462,6 @@ def main():
                           "TFLOP/s": km["flops"] / tk / 1e12,
                           "hbm_frac": km["bytes"] / tk / 1e9 / pk["hbm_gbs"]}
 
-    # The same work through the whole-path call (mamba2_ssd_fwd), inputs
-    # resident (with --fused-state, stage 1 there clears the fused kernel's words).
-    fwd_ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
-
-    def fwd_step():
-        m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                   dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
-                   y=y, final_state=fin, workspace=fwd_ws, stream=stream,
-                   flags=m2.FLAG_FUSED_STATE if fused else 0)
-
-    for _ in range(3):
-        fwd_step()
-    torch.cuda.synchronize()
-    kf = min(K, 50)
-    fa, fz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    fa.record(stream)
-    for _ in range(kf):
-        fwd_step()
-    fz.record(stream)
-    torch.cuda.synchronize()
-    if m2.device_error() != 0:
-        raise RuntimeError("device-side error in the whole-path call")
-    fwd_call = {"ms_per_step": fa.elapsed_time(fz) / kf, "steps": kf,
-                "launches_per_step": 3 if fused else 4}
-    del fwd_ws
-
     # End to end through ssd_fwd with pinned host buffers: every step copies its
     # inputs in (H2D) and its outputs y and final_state out (D2H).  Steps are
     # pipelined as a serving loop would run them: step i+1's inputs go in and step
@@ -514,7 +472,6 @@ def main():
         host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inp_cpu.items()}
         y_host = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
         f_host = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory() for _ in range(2)]
-        ws = torch.empty(m2.workspace_size(sh), dtype=torch.uint8, device="cuda")
         din = [dev, {k: (torch.empty_like(v) if v is not None else None) for k, v in dev.items()}]
         ydev = [y, torch.empty_like(y)]
         fdev = [fin, torch.empty_like(fin)]
@@ -546,7 +503,7 @@ def main():
                 d = din[j]
                 m2.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
                            chunk_size=w.chunk_size, ngroups=w.ngroups, y=ydev[j],
-                           final_state=fdev[j], workspace=ws, stream=stream)
+                           final_state=fdev[j], workspace=ws, stream=stream, flags=flags)
                 ev_comp[i].record(stream)
                 with torch.cuda.stream(s_out):         # outputs of step i
                     s_out.wait_event(ev_comp[i])
@@ -584,7 +541,7 @@ def main():
             "tflops": flops * world / (ms_step * 1e-3) / 1e12,
             "roofline": roof, "path_roofline": path_roof, "kernels": kernels,
             "path": "tcgen05" if m2.path(sh) == m2.PATH_TCGEN05 else "simt",
-            "gpu_launches": len(KERNELS) * K, "fwd_call": fwd_call, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
+            "gpu_launches": len(KERNELS) * K, "e2e": e2e, "cpu_baseline": cpu, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if dist:

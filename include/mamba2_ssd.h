@@ -143,6 +143,19 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape,
                              void* y, float* final_state,
                              void* workspace, size_t workspace_bytes, void* stream);
 
+/* mamba2_ssd_fwd that also records stage boundaries, for profiling: events[k]
+ * (a cudaEvent_t created by the caller, or NULL to skip) is recorded on `stream`
+ * before stage 1 (k = 0), after stages 1, 2, 3 (k = 1, 2, 3; with
+ * MAMBA2_FLAG_FUSED_STATE events[2] and events[3] mark the same point) and after
+ * stage 4 (k = 4).  `events` may be NULL. */
+MAMBA2_API mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape,
+                             const void* x, const float* dt, const float* A,
+                             const void* B, const void* C, const float* D,
+                             const float* initial_state,
+                             void* y, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* const* events);
+
 /* Stage 1, chunk_cumsum [P3 section 7; P2 "세 가지 핵심 커널 구현"]:
  *   cum2[b,h,t] = log2(e) * sum_{r = chunk start of t}^{t} dt[b,r,h] * A[h]
  *   dtT[b,h,t]  = dt[b,t,h]

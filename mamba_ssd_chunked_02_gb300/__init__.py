@@ -41,7 +41,7 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
            "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
-           "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode")
+           "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode", "mamba2_ssd_fwd_timed")
 
 
 class Shape(ctypes.Structure):
@@ -111,6 +111,9 @@ def load():
         lib.mamba2_ssd_selftest_wait_timeout.restype = ctypes.c_int
         lib.mamba2_ssd_decode.argtypes = [sp] + [vp] * 9
         lib.mamba2_ssd_decode.restype = ctypes.c_int
+        lib.mamba2_ssd_fwd_timed.argtypes = [sp] + [vp] * 9 + [vp, ctypes.c_size_t, vp,
+                                                                ctypes.POINTER(vp)]
+        lib.mamba2_ssd_fwd_timed.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -190,12 +193,14 @@ def _check(fn, rc):
 
 
 def ssd_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=None, *,
-            y=None, final_state=None, workspace=None, stream=None, flags=0):
+            y=None, final_state=None, workspace=None, stream=None, flags=0, events=None):
     """Forward pass (mamba2_ssd_fwd).  Returns (y, final_state).
 
     x [b,T,H,P] bf16|f32, dt [b,T,H] f32, A [H] f32, B/C [b,T,G,N] (x's dtype),
     D [H] f32 or None, initial_state [b,H,P,N] f32 or None.  y, final_state and
-    workspace are allocated with torch when not given.
+    workspace are allocated with torch when not given.  `events`: five
+    torch.cuda.Event (or None entries) recorded before stage 1, after each stage
+    and after stage 4 (mamba2_ssd_fwd_timed).
     """
     lib = load()
     sh = shape_of(x, B, chunk_size, ngroups, flags)
@@ -217,7 +222,16 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=
         _ptr(workspace, "workspace", optional=True),
         ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
         _stream(stream)]
-    _check("mamba2_ssd_fwd", lib.mamba2_ssd_fwd(ctypes.byref(sh), *args))
+    if events is None:
+        _check("mamba2_ssd_fwd", lib.mamba2_ssd_fwd(ctypes.byref(sh), *args))
+    else:
+        evs = (ctypes.c_void_p * 5)()
+        for k, ev in enumerate(list(events)[:5]):
+            if ev is not None:
+                if not ev.cuda_event:       # torch creates the CUDA event on first use
+                    ev.record()
+                evs[k] = ctypes.c_void_p(ev.cuda_event)
+        _check("mamba2_ssd_fwd_timed", lib.mamba2_ssd_fwd_timed(ctypes.byref(sh), *args, evs))
     return y, final_state
 
 

@@ -82,7 +82,7 @@ bool use_tc(const mamba2_ssd_shape* s, const Dims& d) {
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Carve {
-    size_t cum2, dtT, dS, Sprev, total;
+    size_t cum2, dtT, dS, Sprev, xabs, total;
 };
 
 Carve carve(const Dims& d) {
@@ -91,7 +91,8 @@ Carve carve(const Dims& d) {
     c.dtT = c.cum2 + align256(sizeof(float) * (size_t)m2::n_cum(d));
     c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
     c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
-    c.total = c.Sprev + align256((size_t)m2::esize(d) * (size_t)m2::n_state(d));
+    c.xabs = c.Sprev + align256((size_t)m2::esize(d) * (size_t)m2::n_state(d));
+    c.total = c.xabs + align256(4 * sizeof(uint32_t) * (size_t)(d.b * d.nc * d.H));
     return c;
 }
 
@@ -224,10 +225,16 @@ mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape, const void* x,
     return from_cuda(e);
 }
 
-mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
-                             const float* A, const void* B, const void* C, const float* D,
-                             const float* initial_state, void* y, float* final_state,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The whole path; events (five cudaEvent_t or null) are recorded before stage 1,
+// after each stage and after stage 4 (stages 2 and 3 share one event when fused).
+mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float* dt,
+                       const float* A, const void* B, const void* C, const float* D,
+                       const float* initial_state, void* y, float* final_state, void* workspace,
+                       size_t workspace_bytes, void* stream, void* const* events) {
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     const Dims d = dims_of(shape);
@@ -250,6 +257,7 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
     float* dtT = reinterpret_cast<float*>(ws + cv.dtT);
     float* dS = reinterpret_cast<float*>(ws + cv.dS);
     void* Sprev = ws + cv.Sprev;
+    uint32_t* xabs = reinterpret_cast<uint32_t*>(ws + cv.xabs);   // stage 2 -> stage 4: max |x|
     const bool tc = use_tc(shape, d);
     // Fused stages 2+3 (opt-in): the two-slot carried-state ring, the flag words
     // and the ticket live in the dS region, which holds them from three chunks on.
@@ -259,25 +267,57 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
                       ring + sizeof(int32_t) * (nflag + 1) <= cv.Sprev - cv.dS;
     int32_t* flags = reinterpret_cast<int32_t*>(ws + cv.dS + ring);
 
-    cudaError_t e = fuse ? m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s, flags,
-                                                   (int64_t)nflag + 1)
-                         : m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+    auto mark = [&](int k) -> cudaError_t {
+        return (events && events[k]) ? cudaEventRecord(static_cast<cudaEvent_t>(events[k]), s)
+                                     : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess)
+        e = fuse ? m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s, flags, (int64_t)nflag + 1)
+                 : m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+    if (e == cudaSuccess) e = mark(1);
     if (fuse) {
         if (e == cudaSuccess)
             e = m2::launch_chunk_state_pass_tc(d, x, B, cum2, dtT, initial_state, dS, flags,
                                                flags + nflag, Sprev, final_state, err, s);
+        if (e == cudaSuccess) e = mark(2);
     } else {
         if (e == cudaSuccess)
-            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s)
+            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s, xabs)
                    : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
+        if (e == cudaSuccess) e = mark(2);
         // On the tensor-core path dS travels between stages 2 and 3 in bf16.
         if (e == cudaSuccess)
             e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, final_state, err, s);
     }
+    if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
-        e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s)
+        e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s,
+                                         fuse ? nullptr : xabs)
                : m2::launch_chunk_out_simt(d, x, B, C, cum2, dtT, Sprev, D, y, err, s);
+    if (e == cudaSuccess) e = mark(4);
     return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
+                             const float* A, const void* B, const void* C, const float* D,
+                             const float* initial_state, void* y, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_impl(shape, x, dt, A, B, C, D, initial_state, y, final_state, workspace,
+                    workspace_bytes, stream, nullptr);
+}
+
+mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x, const float* dt,
+                                   const float* A, const void* B, const void* C, const float* D,
+                                   const float* initial_state, void* y, float* final_state,
+                                   void* workspace, size_t workspace_bytes, void* stream,
+                                   void* const* events) {
+    return fwd_impl(shape, x, dt, A, B, C, D, initial_state, y, final_state, workspace,
+                    workspace_bytes, stream, events);
 }
 
 mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear) {

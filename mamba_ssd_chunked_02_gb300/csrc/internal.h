@@ -31,9 +31,11 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
                                     int32_t* err, cudaStream_t st);
 // Stage 2: tcgen05 variant (bf16, shapes accepted by tc_supported()); dS is
 // written in fp32, or in bf16 when ds16 (the whole-path call).
+// When xabs is given it also records max |x| per (b, chunk, head): four words
+// per head ([b][nc][H][4], bf16 bit patterns of |x|; their max is the bound).
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,
                                   const float* cum2, const float* dtT, void* dS, bool ds16,
-                                  int32_t* err, cudaStream_t st);
+                                  int32_t* err, cudaStream_t st, uint32_t* xabs = nullptr);
 
 // Stages 2 and 3 fused (tcgen05, bf16, tc_supported() shapes): each CTA
 // computes its chunk's dS in tensor memory, then, head by head, takes the state
@@ -59,10 +61,12 @@ cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const fl
 cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, const void* C,
                                   const float* cum2, const float* dtT, const void* Sprev,
                                   const float* D, void* y, int32_t* err, cudaStream_t st);
-// Stage 4: tcgen05 variant.
+// Stage 4: tcgen05 variant; xabs: stage 2's max |x| words, or null (then the
+// kernel scans each x tile for its fp16 range check itself).
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
-                                const float* D, void* y, int32_t* err, cudaStream_t st);
+                                const float* D, void* y, int32_t* err, cudaStream_t st,
+                                const uint32_t* xabs = nullptr);
 
 // One recurrent step per (b, h): S <- exp(dt A) S + dt x B^T in place, y = S C + D x.
 cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* dt, const float* A,

@@ -114,7 +114,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       int T, int H, int N, int G, int nc, int n_tiles,
-                      int hpc, int n_hblk, int32_t* err, const FuseArgs fa) {
+                      int hpc, int n_hblk, int32_t* err, const FuseArgs fa,
+                      uint32_t* __restrict__ xabs) {
     using C = K2Cfg<L, kFuse, kDS16>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -267,6 +268,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                                        mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
             if (!ok) break;
             uint8_t* xs = sX + st * C::X_BYTES;
+            __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);   // max |x| (raw), two lanes
 #pragma unroll
             for (int r = 0; r < L / 128; ++r) {
                 const int s = idx + 128 * r;
@@ -280,6 +282,10 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                     uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
+                        if (xabs) {
+                            const uint32_t a = u[e] & 0x7fff7fffu;
+                            xm2 = __hmax2(xm2, *reinterpret_cast<const __nv_bfloat162*>(&a));
+                        }
                         const float lo = __uint_as_float(u[e] << 16) * w[r];
                         const float hi = __uint_as_float(u[e] & 0xffff0000u) * w[r];
                         u[e] = pack_bf16x2(lo, hi);
@@ -289,6 +295,12 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars.scaled[st]);
+            if (xabs) {   // this warp's share of max |x| over the chunk, as bf16 bits
+                const uint32_t m2u = *reinterpret_cast<const uint32_t*>(&xm2);
+                const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2u & 0xffffu, m2u >> 16));
+                if (lane == 0)
+                    xabs[((((int64_t)b * nc + c) * H + h0 + i) << 2) + (warp - 2)] = m;
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -492,7 +504,7 @@ int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
 template <int L, bool kFuse, bool kDS16>
 cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
                       const float* dtT, void* dS, const FuseArgs& fa, int32_t* err,
-                      cudaStream_t st) {
+                      cudaStream_t st, uint32_t* xabs = nullptr) {
     using C = K2Cfg<L, kFuse, kDS16>;
     constexpr bool ds16 = kDS16;
     CUtensorMap tm_x, tm_b;
@@ -542,7 +554,7 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, tm_ring, tm_init, tm_fin, tm_sp,
                                                  cum2, dtT, (int)d.T, (int)d.H,
                                                  (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
-                                                 n_hblk, err, fa);
+                                                 n_hblk, err, fa, xabs);
     return cudaGetLastError();
 }
 
@@ -557,15 +569,15 @@ bool tc_supported(const Dims& d) {
 
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
                                   const float* dtT, void* dS, bool ds16, int32_t* err,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, uint32_t* xabs) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     const FuseArgs none{};
     if (ds16)
-        return d.L == 256 ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st)
-                          : launch_k2<128, false, true>(d, x, B, cum2, dtT, dS, none, err, st);
-    return d.L == 256 ? launch_k2<256, false, false>(d, x, B, cum2, dtT, dS, none, err, st)
-                      : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st);
+        return d.L == 256 ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs)
+                          : launch_k2<128, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs);
+    return d.L == 256 ? launch_k2<256, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs)
+                      : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs);
 }
 
 int64_t fused_flag_words(const Dims& d) {

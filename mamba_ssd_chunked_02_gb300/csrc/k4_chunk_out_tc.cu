@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
-                    const float* __restrict__ dtT, const float* __restrict__ Dvec, int T, int H,
+                    const float* __restrict__ dtT, const float* __restrict__ Dvec,
+                    const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int hpc, int n_hblk, int32_t* err) {
     using C = K4Cfg<L, NA>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
@@ -621,6 +622,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         float pc[KPT], pd[KPT], plast = 0.f, pD = 0.f;
 #pragma unroll
         for (int i = 0; i < KPT; ++i) { pc[i] = 0.f; pd[i] = 0.f; }
+        uint4 pX = make_uint4(0u, 0u, 0u, 0u);
         auto prefetch = [&](int hh) {
             const float* crow = cum2 + row0 + (int64_t)hh * T;
             const float* drow = dtT + row0 + (int64_t)hh * T;
@@ -634,6 +636,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
             pD = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
+            if (xabs)   // stage 2's max |x| of the chunk (four words, bf16 bits)
+                pX = __ldg(reinterpret_cast<const uint4*>(xabs) + ((int64_t)b * nc + c) * H + h0 + hh);
         };
         if (nh > 0) prefetch(0);
         // The C.B^T bound comes from the epilogue (after GEMM1); by then every
@@ -658,12 +662,15 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
             const float dval = pD;
+            const uint32_t xknown = max(max(pX.x, pX.y), max(pX.z, pX.w));
             if (hi + 1 < nh) prefetch(hi + 1);
             uint8_t* xs = sStage + st * C::STAGE;
             const int nch = KS * 8 / kConvThreads;
             __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);
+            // max |x| over the tile: from stage 2 (over the whole chunk, a bound)
+            // when available, else one pass over the tile.
 #pragma unroll 8
-            for (int i = 0; i < nch; ++i) {
+            for (int i = 0; i < (xabs ? 0 : nch); ++i) {
                 const uint4 v = *reinterpret_cast<const uint4*>(xs + (ctid + kConvThreads * i) * 16);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -680,7 +687,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 red_x[(st * kConvWarps + cw) * 2 + 1] = dmax;
             }
             if (!(ok = conv_sync())) break;
-            const uint32_t gx = __reduce_max_sync(
+            const uint32_t gx = xabs ? xknown : __reduce_max_sync(
                 0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 0] : 0u);
             const uint32_t gd = __reduce_max_sync(
                 0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 1] : 0u);
@@ -729,7 +736,7 @@ int num_sms4() {
 template <int L, int NA>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
-                      void* y, int32_t* err, cudaStream_t st) {
+                      void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs) {
     using C = K4Cfg<L, NA>;
     CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
@@ -756,7 +763,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     auto k = chunk_out_tc_kernel<L, NA>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_c, tm_s, tm_y, cum2, dtT, D,
+    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_c, tm_s, tm_y, cum2, dtT, D, xabs,
                                                  (int)d.T, (int)d.H, (int)d.G, (int)d.nc, hpc,
                                                  n_hblk, err);
     return cudaGetLastError();
@@ -765,11 +772,11 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
 template <int L>
 cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void* Cm,
                         const float* cum2, const float* dtT, const void* Sprev, const float* D,
-                        void* y, int32_t* err, cudaStream_t st) {
+                        void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs) {
     switch (d.N) {
-        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
-        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
-        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st);
+        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
+        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
+        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
     }
     return cudaErrorInvalidValue;
 }
@@ -778,11 +785,12 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
 
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
-                                const float* D, void* y, int32_t* err, cudaStream_t st) {
+                                const float* D, void* y, int32_t* err, cudaStream_t st,
+                                const uint32_t* xabs) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
-    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st)
-                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st);
+    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs)
+                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs);
 }
 
 }  // namespace m2
