@@ -44,10 +44,13 @@
 //
 // Precision of GEMM2.  M and X enter GEMM2 as fp16 (10-bit mantissa) rather
 // than bf16 (7-bit): the worst-case error of a large output is then set by the
-// final bf16 rounding of y alone.  Per head the converter warps check that
-// fp16 cannot overflow -- max|x| <= 2^15 over the tile and max|C.B| * max(dt)
-// <= 2^15 (|M| is at most that product, every decay being <= 1) -- and
-// otherwise keep bf16 for that head (x stays untouched, M is packed as bf16).
+// final bf16 rounding of y alone.  The skip term rides along: D_h is added to
+// M's diagonal, so G = M . X includes D_h x_t.  Per head the converter warps
+// check that fp16 holds x and M without overflow and without their
+// significant entries or factors falling to fp16 subnormals -- max|x| in
+// [2^-6, 2^15], |M| <= max|C.B| max(dt) + |D_h| (every decay being <= 1) in
+// [2^-4, 2^15], max|C.B| in [2^-8, 2^15], max dt >= 2^-10 -- and otherwise
+// keep bf16 for that head (x stays untouched, M is packed as bf16).
 //
 // Warp roles: 0, 1 = converters, 2 = TMA producer, 3 = MMA issuer (+ TMEM
 // owner), 4 .. 4+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column
@@ -90,7 +93,11 @@ static_assert(PC == 32, "the epilogue moves one 32-column TMEM slice per thread"
 // double-buffered fp32 accumulators (carried-state term S, intra-chunk term G).
 // GEMM1 writes C.B^T in fp32 to [COL_S, COL_S + KS) before any S is live.
 constexpr uint32_t COL_CB = 0, COL_MM = 128, COL_S = 256, COL_G = 384, COL_CB32 = COL_S;
-constexpr uint32_t kF16Limit = 0x4700u;       // bf16 bit pattern of 2^15
+constexpr uint32_t kF16MinX = 0x3c80u, kF16MaxX = 0x4700u;   // bf16 bits of 2^-6, 2^15
+// C.B^T is packed as fp16 when max|C.B| lies in [2^-8, 2^15] (else bf16).
+__device__ __forceinline__ bool cb_fits_f16(float cbmax) {
+    return cbmax <= 32768.f && cbmax >= 0.00390625f;
+}
 
 template <int L, int NA>   // NA = N / 64
 struct K4Cfg {
@@ -133,6 +140,7 @@ struct K4Bars {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
     return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
+
 
 template <int L, int NA>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -365,7 +373,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         }
         // Pack C.B^T to 16-bit pairs: fp16 when it fits (every head may then take
         // the fp16 path), else bf16 (no head takes the fp16 path).
-        const bool cb16 = cbmax <= 32768.f;
+        const bool cb16 = cb_fits_f16(cbmax);
         if (ok) {
             for (int j = grp; j <= jd; j += EG) {
                 uint32_t r[32];
@@ -382,10 +390,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         tc_fence_before();
         mbar_arrive(&bars.cb_packed);
 
-        uint32_t xv_prev[PC / 2], xv_cur[PC / 2];
-        float d_prev = 0.f, d_cur = 0.f, e_prev = 0.f;
-        bool x16_prev = false, x16_cur = false;
-        // finish(hp): y rows of head hp = acc + D x, bf16, TMA-stored per warp.
+        float e_prev = 0.f;
+        // finish(hp): y rows of head hp = exp2(cum2_t) S + G (the skip term D x
+        // is in G, through M's diagonal), bf16, TMA-stored per warp.
         auto finish = [&](int hp) -> bool {
             const int pb = hp & 1;
             if (!__all_sync(0xffffffffu,
@@ -401,21 +408,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             mbar_arrive(&bars.acc_empty[pb]);
             uint32_t yv[PC / 2];
 #pragma unroll
-            for (int e = 0; e < PC / 2; ++e) {
-                const uint32_t xw = xv_prev[e];
-                float x0, x1;
-                if (x16_prev) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw));
-                    x0 = f.x;
-                    x1 = f.y;
-                } else {
-                    x0 = __uint_as_float(xw << 16);
-                    x1 = __uint_as_float(xw & 0xffff0000u);
-                }
-                yv[e] = pack_bf16x2(
-                    fmaf(e_prev, __uint_as_float(rs[2 * e]), __uint_as_float(r[2 * e])) + d_prev * x0,
-                    fmaf(e_prev, __uint_as_float(rs[2 * e + 1]), __uint_as_float(r[2 * e + 1])) + d_prev * x1);
-            }
+            for (int e = 0; e < PC / 2; ++e)
+                yv[e] = pack_bf16x2(fmaf(e_prev, __uint_as_float(rs[2 * e]), __uint_as_float(r[2 * e])),
+                                    fmaf(e_prev, __uint_as_float(rs[2 * e + 1]), __uint_as_float(r[2 * e + 1])));
             // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
             // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
@@ -443,18 +438,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const float* ck = cumv + st * 256;
             const float* dk = dtv + st * 256;
             const bool use16 = bars.use16s[st] != 0;
-            d_cur = bars.dvals[st];
-            x16_cur = use16;
-            {   // x row t (this group's columns) for the skip term (fp16 if converted)
-                const uint8_t* xrow = sStage + st * C::STAGE + tc_ * 128;
-#pragma unroll
-                for (int cc = 0; cc < PC / 8; ++cc) {
-                    const int chunk = grp * (PC / 8) + cc;
-                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((chunk ^ (tc_ & 7)) << 4));
-                    xv_cur[4 * cc + 0] = v.x; xv_cur[4 * cc + 1] = v.y;
-                    xv_cur[4 * cc + 2] = v.z; xv_cur[4 * cc + 3] = v.w;
-                }
-            }
+            const float dh = bars.dvals[st];           // D of this head: added to M[t, t]
             const float ct = ck[tc_];
             const float e_t = ex2(ct);
             const float cr = ck[32 * jd];
@@ -484,6 +468,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             __syncwarp();
             const __half2 u2 = __float2half2_rn(u_t);
             const __half2 ud2 = __float2half2_rn(ex2(ct - cml));
+            const __half2 dd2 = (lane & 1) ? __floats2half2_rn(0.f, dh) : __floats2half2_rn(dh, 0.f);
 
             // ---- M, in two K-halves.
             for (int half = 0; half < 2 && ok; ++half) {
@@ -530,7 +515,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                 const __half2 cb2 = *reinterpret_cast<const __half2*>(&r[e]);
                                 const __half2 uw = __hmul2(ud2, *reinterpret_cast<const __half2*>(&wv[k2]));
                                 const __half2 cd = __hmul2(cb2, *reinterpret_cast<const __half2*>(&dv[k2]));
-                                const __half2 mm2 = __hmul2(cd, uw);
+                                __half2 mm2 = __hmul2(cd, uw);
+                                if (e == (lane >> 1)) mm2 = __hadd2(mm2, dd2);   // key t: + D
                                 const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm2);
                                 m[e] = 2 * e + 1 <= lane ? mw : (2 * e <= lane ? (mw & 0xffffu) : 0u);
                             }
@@ -572,6 +558,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                 for (int u = 0; u < 4; ++u) {
                                     const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
                                     mv[e] = e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f;
+                                    if (e == lane) mv[e] += dh;          // key t: + D
                                 }
                             }
                         }
@@ -594,10 +581,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             // ---- previous head's output while the tensor core works on this one.
             if (hi > 0 && !(ok = finish(hi - 1))) break;
 #pragma unroll
-            for (int e = 0; e < PC / 2; ++e) xv_prev[e] = xv_cur[e];
-            d_prev = d_cur;
             e_prev = e_t;
-            x16_prev = x16_cur;
         }
         if (ok && nh > 0) ok = finish(nh - 1);
         if (lane == 0) bulk_wait<0>();
@@ -643,7 +627,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // The C.B^T bound comes from the epilogue (after GEMM1); by then every
         // C.B^T block item of the ring has landed, so only head items remain.
         bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cbinfo, 0, abort, kWaitNs));
-        const float cbmax = bars.cbmax;
+        const float cbmax = bars.cbmax;        // C.B^T packed as fp16 iff cb_fits_f16(cbmax)
         for (int hi = 0; hi < nh && ok; ++hi) {
             const int it = NA + hi, st = it % NS, k = it / NS;
             ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
@@ -691,8 +675,13 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 0] : 0u);
             const uint32_t gd = __reduce_max_sync(
                 0xffffffffu, lane < kConvWarps ? red_x[(st * kConvWarps + lane) * 2 + 1] : 0u);
-            const bool use16 = cbmax <= 32768.f && gx <= kF16Limit &&
-                               cbmax * __uint_as_float(gd) <= 32768.f;
+            // fp16 for the head when fp16 holds x and M without overflow and
+            // without their significant entries or factors falling to fp16
+            // subnormals: C.B^T packed as fp16, max|x| in [2^-6, 2^15], the bound
+            // max|C.B| max(dt) + |D| of |M| in [2^-4, 2^15], max dt >= 2^-10.
+            const float mb = cbmax * __uint_as_float(gd) + fabsf(dval);
+            const bool use16 = cb_fits_f16(cbmax) && gx >= kF16MinX && gx <= kF16MaxX &&
+                               mb <= 32768.f && mb >= 0.0625f && __uint_as_float(gd) >= 0.0009765625f;
             if (use16) {
 #pragma unroll 8
                 for (int i = 0; i < nch; ++i) {

@@ -304,6 +304,32 @@ def test_edge_cases():
     assert torch.allclose(f.cpu(), inp["initial_state"], rtol=0, atol=0)
 
 
+# Input magnitudes far from the unit scale of the standard workloads: the
+# tensor-core path picks its 16-bit operand types and scales from the data's
+# range (per CTA for C.B^T, per head for x, dt and D), so each of these must
+# stay within the same tolerance of the fp64 oracle.
+MAGNITUDES = [
+    ("x*1e5", dict(x=1e5), 0.0),            # |x| above the fp16 range
+    ("x*1e-6", dict(x=1e-6), 0.0),          # |x| below the fp16 normal range
+    ("dt*1e-4,D=0", dict(dt=1e-4, D=0.0), 0.0),   # small decay-weighted products
+    ("B,C*0.01", dict(B=0.01, C=0.01), 0.0),      # |C.B| below the fp16 normal range
+    ("B,C*100", dict(B=100.0, C=100.0), 0.0),     # |C.B| above the fp16 range
+    ("D*1e4", dict(D=1e4), 0.0),            # skip term dominates
+]
+
+
+@pytest.mark.parametrize("name,scale,init", MAGNITUDES, ids=[m[0] for m in MAGNITUDES])
+def test_input_magnitudes(name, scale, init):
+    w = wl(2, 640, 4, 64, 128, 1, 256, init=init, seed=41)
+    inp = W.make_inputs(w)
+    for k, s in scale.items():
+        inp[k] = (inp[k].double() * s).to(inp[k].dtype)
+    y, f = run_fwd(inp, w)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
+    assert_close(to_np(y), yr, w.dtype, name + ": y")
+    assert_close(to_np(f), fr, w.dtype, name + ": final state")
+
+
 def test_outputs_do_not_depend_on_workspace_contents():
     w = wl(1, 512, 4, 64, 128, 1, 256, seed=37)
     inp = W.make_inputs(w)
