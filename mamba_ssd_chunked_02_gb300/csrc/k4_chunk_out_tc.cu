@@ -439,16 +439,32 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const float* dk = dtv + st * 256;
             const bool use16 = bars.use16s[st] != 0;
             const float dh = bars.dvals[st];           // D of this head: added to M[t, t]
+            // Every load of the row's vectors first, so that their latencies overlap.
             const float ct = ck[tc_];
-            const float e_t = ex2(ct);
             const float cr = ck[32 * jd];
+            const float cml = ck[32 * jd + 31];
+            const float ckd = ck[32 * jd + lane];
+            const float dsd = dk[32 * jd + lane];
+            constexpr int kMaxOwn = (L / 32 + EG - 1) / EG;   // own blocks below the diagonal
+            float cj[kMaxOwn], dj[kMaxOwn];
+#pragma unroll
+            for (int i = 0; i < kMaxOwn; ++i) {
+                const int j = grp + EG * i;
+                cj[i] = j < jd ? ck[32 * j + lane] : 0.f;
+                dj[i] = j < jd ? dk[32 * j + lane] : 0.f;
+            }
+            const float e_t = ex2(ct);
             const float u_t = ex2(ct - cr);
             float* vq = vdt + q * 256;
             __half* vh = reinterpret_cast<__half*>(vq);
-            for (int j = grp; j < jd; j += EG) {
-                const float v = ex2(cr - ck[32 * j + lane]) * dk[32 * j + lane];
-                if (use16) vh[32 * j + lane] = __float2half_rn(v);
-                else vq[32 * j + lane] = v;
+#pragma unroll
+            for (int i = 0; i < kMaxOwn; ++i) {
+                const int j = grp + EG * i;
+                if (j < jd) {
+                    const float v = ex2(cr - cj[i]) * dj[i];
+                    if (use16) vh[32 * j + lane] = __float2half_rn(v);
+                    else vq[32 * j + lane] = v;
+                }
             }
             // Diagonal block on the fp16 path, with its last key m as reference:
             // exp2(cum2_t - cum2_s) = u_t w_s, u_t = exp2(cum2_t - cum2_m) in [1, 2^R],
@@ -456,13 +472,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             // then times dt_s.  All three stay normal fp16 numbers when R <= 14 and
             // every dt_s of the block is >= 2^-14; otherwise the fp32 path below.
             // The causal mask is applied to the final product.
-            const float cml = ck[32 * jd + 31];
             const bool owner = jd % EG == grp;
-            const float dsd = dk[32 * jd + lane];
             const bool dpack = use16 && cr - cml <= 14.f &&
                                !__any_sync(0xffffffffu, owner && dsd < 6.1035156e-5f);
             if (dpack && owner) {
-                vh[32 * jd + lane] = __float2half_rn(ex2(cml - ck[32 * jd + lane]));
+                vh[32 * jd + lane] = __float2half_rn(ex2(cml - ckd));
                 vh[32 * jd + 32 + lane] = __float2half_rn(dsd);
             }
             __syncwarp();
