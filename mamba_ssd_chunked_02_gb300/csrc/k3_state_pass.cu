@@ -13,7 +13,7 @@
 // Sequential over chunks, parallel over (b, h, slices of the P x N state): one
 // thread owns 16 bytes' worth of dS elements of the state (4 for fp32 dS, 8 for
 // bf16 dS) for the whole chain.  The dS
-// loads do not depend on the chain, so each thread keeps kDepth chunks of loads
+// loads do not depend on the chain, so each thread keeps a few chunks of loads
 // in flight (a rolling prefetch) while it walks the chain: a pure HBM stream of
 // dS (fp32, or bf16 on the whole-path call) in and Sprev out per state element
 // per chunk.
@@ -24,7 +24,12 @@ namespace m2 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kDepth = 8;   // chunks of dS loads in flight per thread
+// Chunks of dS loads in flight per thread: 4 for bf16 dS (40 registers, six
+// blocks per SM), 8 for fp32 dS (measured best for each).
+template <typename TD>
+struct Depth {
+    static constexpr int value = sizeof(TD) == 2 ? 4 : 8;
+};
 
 // A thread owns EPT consecutive state elements, EPT = 16 bytes of dS: one
 // 16-byte load of dS and one store of Sprev per chunk.
@@ -77,6 +82,7 @@ state_pass_kernel(const TD* __restrict__ dS, const float* __restrict__ cum2,
                   float* __restrict__ fin, int64_t T, int64_t H, int64_t L, int64_t nc,
                   int64_t PN, int64_t blocks_per_bh) {
     constexpr int E = Ept<TD>::value;
+    constexpr int kDepth = Depth<TD>::value;
     const int64_t bh = blockIdx.x / blocks_per_bh;
     const int64_t iv = (blockIdx.x % blocks_per_bh) * kThreads + threadIdx.x;
     const int64_t e = iv * E;
