@@ -9,10 +9,11 @@ N=128, G=1, L=256, bf16; x is 335 MB, larger than L2, so nothing is flushed
 between steps).  Inputs are seeded synthetic tensors, resident in HBM before
 the timed region.  Each step is one whole-path call through the C ABI
 (mamba2_ssd_fwd, the call a user makes); every EVENT_EVERY-th step goes through
-mamba2_ssd_fwd_timed (the same launches) and records CUDA events between its
-stages on the launching stream, so the per-kernel times and the whole-step time
-come from the same timed region.  (An event between two kernels of a stream
-costs about 2 us of device time; on every step they would add ~2 % to it.)
+mamba2_ssd_fwd_timed (the same kernels, launched strictly one after another)
+and records CUDA events between its stages on the launching stream, so the
+per-kernel times and the whole-step time come from the same timed region.
+(Events between kernels cost device time and rule out the overlapped launches
+of stages 2-4; on every step they would add ~3 % to it.)
 
 Printed (one JSON line, rank 0): tokens/s (value), TFLOP/s, per-kernel times,
 the roofline of the dominant kernel, the whole-path roofline under the fixed
@@ -43,7 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSD fwd tokens/s & TFLOP/s at Mamba-2 2.7B shape; % of roofline on 1 GB300"
-EVENT_EVERY = 4                    # stage events on every 4th timed step
+EVENT_EVERY = 8                    # stage events on every 8th timed step
 KERNELS_FUSED = ("chunk_cumsum", "chunk_state_pass", "chunk_out")
 KERNELS_SPLIT = ("chunk_cumsum", "chunk_state", "state_pass", "chunk_out")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

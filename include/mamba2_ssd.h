@@ -91,6 +91,12 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  * the tensor-core path for chunk_state and dtype BF16 for state_pass; other
  * shapes return MAMBA2_ERR_UNSUPPORTED. */
 #define MAMBA2_FLAG_DS_BF16 4
+/* In mamba2_ssd_fwd, launch the stages strictly one after another.  By default
+ * stages 2, 3 and 4 of the tensor-core path use programmatic dependent launch:
+ * each may start while the previous stage finishes and reads that stage's
+ * outputs only after it has completed (stage 2 loads x and B early, stage 4
+ * computes C.B^T and prepares x early).  Same results either way. */
+#define MAMBA2_FLAG_SERIAL 8
 
 /* Shape of one call.  Supported set:
  *   batch, seqlen, nheads >= 0 (a zero batch or head count is a no-op; seqlen 0
@@ -130,7 +136,9 @@ MAMBA2_API size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape);
 
 /* The whole forward pass: the four stages below, in order, on `stream`
  * (stages 2 and 3 as one kernel with MAMBA2_FLAG_FUSED_STATE, tensor-core path,
- * three or more chunks).  On the tensor-core path dS goes from stage 2 to
+ * three or more chunks; successive stages overlap their start and end unless
+ * MAMBA2_FLAG_SERIAL is set).  Everything queued on `stream` before the call
+ * has completed before the first stage reads anything.  On the tensor-core path dS goes from stage 2 to
  * stage 3 in bf16 (as with MAMBA2_FLAG_DS_BF16); the carried states themselves
  * are accumulated in fp32.
  *   workspace: device buffer of at least mamba2_ssd_workspace_size(shape)
@@ -143,7 +151,8 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape,
                              void* y, float* final_state,
                              void* workspace, size_t workspace_bytes, void* stream);
 
-/* mamba2_ssd_fwd that also records stage boundaries, for profiling: events[k]
+/* mamba2_ssd_fwd that also records stage boundaries, for profiling (the stages
+ * then run strictly one after another, as with MAMBA2_FLAG_SERIAL): events[k]
  * (a cudaEvent_t created by the caller, or NULL to skip) is recorded on `stream`
  * before stage 1 (k = 0), after stages 1, 2, 3 (k = 1, 2, 3; with
  * MAMBA2_FLAG_FUSED_STATE events[2] and events[3] mark the same point) and after

@@ -32,6 +32,7 @@ F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_FUSED_STATE = 2
 FLAG_DS_BF16 = 4
+FLAG_SERIAL = 8
 PATH_SIMT, PATH_TCGEN05 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_DEVICE = range(6)
 

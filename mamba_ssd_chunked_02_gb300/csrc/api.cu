@@ -53,7 +53,8 @@ mamba2_status check(const mamba2_ssd_shape* s) {
     if (s->headdim <= 0 || s->dstate <= 0 || s->ngroups <= 0 || s->chunk_size <= 0)
         return MAMBA2_ERR_INVALID_ARG;
     if (s->dtype != MAMBA2_F32 && s->dtype != MAMBA2_BF16) return MAMBA2_ERR_INVALID_ARG;
-    if (s->flags & ~(MAMBA2_FLAG_FORCE_SIMT | MAMBA2_FLAG_FUSED_STATE | MAMBA2_FLAG_DS_BF16))
+    if (s->flags & ~(MAMBA2_FLAG_FORCE_SIMT | MAMBA2_FLAG_FUSED_STATE | MAMBA2_FLAG_DS_BF16 |
+                     MAMBA2_FLAG_SERIAL))
         return MAMBA2_ERR_INVALID_ARG;
     if (s->nheads % s->ngroups != 0) return MAMBA2_ERR_INVALID_ARG;
     if (!in_set(s->headdim, {16, 32, 64, 128})) return MAMBA2_ERR_UNSUPPORTED;
@@ -266,6 +267,10 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
     const bool fuse = tc && d.nc >= 3 && (shape->flags & MAMBA2_FLAG_FUSED_STATE) &&
                       ring + sizeof(int32_t) * (nflag + 1) <= cv.Sprev - cv.dS;
     int32_t* flags = reinterpret_cast<int32_t*>(ws + cv.dS + ring);
+    // Programmatic dependent launch of stages 2-4 (not across recorded events).
+    // Stage 1 is an ordinary launch, so everything queued before this call has
+    // completed before any stage reads its inputs.
+    const bool pdl = !(shape->flags & MAMBA2_FLAG_SERIAL) && !events;
 
     auto mark = [&](int k) -> cudaError_t {
         return (events && events[k]) ? cudaEventRecord(static_cast<cudaEvent_t>(events[k]), s)
@@ -283,17 +288,18 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
         if (e == cudaSuccess) e = mark(2);
     } else {
         if (e == cudaSuccess)
-            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s, xabs)
+            e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s, xabs, pdl)
                    : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
         if (e == cudaSuccess) e = mark(2);
         // On the tensor-core path dS travels between stages 2 and 3 in bf16.
         if (e == cudaSuccess)
-            e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, final_state, err, s);
+            e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, final_state, err, s,
+                                      pdl);
     }
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_out_tc(d, x, B, C, cum2, dtT, Sprev, D, y, err, s,
-                                         fuse ? nullptr : xabs)
+                                         fuse ? nullptr : xabs, pdl && !fuse)
                : m2::launch_chunk_out_simt(d, x, B, C, cum2, dtT, Sprev, D, y, err, s);
     if (e == cudaSuccess) e = mark(4);
     return from_cuda(e);

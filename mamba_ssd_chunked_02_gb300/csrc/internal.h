@@ -33,9 +33,12 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
 // written in fp32, or in bf16 when ds16 (the whole-path call).
 // When xabs is given it also records max |x| per (b, chunk, head): four words
 // per head ([b][nc][H][4], bf16 bit patterns of |x|; their max is the bound).
+// pdl: launched with programmatic dependent launch after stage 1 (the
+// whole-path call): x and B are read before stage 1 completes.
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,
                                   const float* cum2, const float* dtT, void* dS, bool ds16,
-                                  int32_t* err, cudaStream_t st, uint32_t* xabs = nullptr);
+                                  int32_t* err, cudaStream_t st, uint32_t* xabs = nullptr,
+                                  bool pdl = false);
 
 // Stages 2 and 3 fused (tcgen05, bf16, tc_supported() shapes): each CTA
 // computes its chunk's dS in tensor memory, then, head by head, takes the state
@@ -53,9 +56,10 @@ cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void*
                                        cudaStream_t st);
 
 // Stage 3: sequential state pass over chunks (dS in fp32, or bf16 when ds16).
+// pdl: launched with programmatic dependent launch after stage 2.
 cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const float* cum2,
                               const float* init, void* Sprev, float* final_state,
-                              int32_t* err, cudaStream_t st);
+                              int32_t* err, cudaStream_t st, bool pdl = false);
 
 // Stage 4: fused output.  CUDA-core variant.
 cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, const void* C,
@@ -63,10 +67,12 @@ cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, c
                                   const float* D, void* y, int32_t* err, cudaStream_t st);
 // Stage 4: tcgen05 variant; xabs: stage 2's max |x| words, or null (then the
 // kernel scans each x tile for its fp16 range check itself).
+// pdl: launched with programmatic dependent launch after stage 3 (the
+// whole-path call): everything but Sprev is read before stage 3 completes.
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st,
-                                const uint32_t* xabs = nullptr);
+                                const uint32_t* xabs = nullptr, bool pdl = false);
 
 // One recurrent step per (b, h): S <- exp(dt A) S + dt x B^T in place, y = S C + D x.
 cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* dt, const float* A,

@@ -41,6 +41,9 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     constexpr int kPitch = L + L / 32 + 1;    // odd
     __shared__ float tile[kHB * kPitch];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
+    // Stage 2, when launched as this kernel's programmatic dependent, may start
+    // its loads of x and B now; it waits for this grid before reading cum2/dtT.
+    if (threadIdx.x == 0) grid_dep_launch();
     // Clear the next kernel's synchronisation words (grid-stride).
     if (zero) {
         const int64_t cta = c + (int64_t)gridDim.x * (b + (int64_t)gridDim.y * blockIdx.z);

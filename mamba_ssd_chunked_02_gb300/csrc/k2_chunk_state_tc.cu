@@ -257,6 +257,11 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 pd[r] = s < Lc ? __ldg(drow + s) : 0.f;
             }
         };
+        // cum2 and dtT come from stage 1: with programmatic dependent launch the
+        // producer's loads of B and x already run; wait for stage 1 here, then
+        // let stage 3 start launching.
+        grid_dep_wait();
+        if (idx == 0) grid_dep_launch();
         prefetch(0);
         for (int i = 0; i < nh; ++i) {
             const int st = i % NS, k = i / NS;
@@ -504,7 +509,7 @@ int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
 template <int L, bool kFuse, bool kDS16>
 cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* cum2,
                       const float* dtT, void* dS, const FuseArgs& fa, int32_t* err,
-                      cudaStream_t st, uint32_t* xabs = nullptr) {
+                      cudaStream_t st, uint32_t* xabs = nullptr, bool pdl = false) {
     using C = K2Cfg<L, kFuse, kDS16>;
     constexpr bool ds16 = kDS16;
     CUtensorMap tm_x, tm_b;
@@ -551,11 +556,9 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     auto k = chunk_state_tc_kernel<L, kFuse, kDS16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_d, tm_ring, tm_init, tm_fin, tm_sp,
-                                                 cum2, dtT, (int)d.T, (int)d.H,
-                                                 (int)d.N, (int)d.G, (int)d.nc, n_tiles, hpc,
-                                                 n_hblk, err, fa, xabs);
-    return cudaGetLastError();
+    return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
+                         tm_ring, tm_init, tm_fin, tm_sp, cum2, dtT, (int)d.T, (int)d.H, (int)d.N,
+                         (int)d.G, (int)d.nc, n_tiles, hpc, n_hblk, err, fa, xabs);
 }
 
 }  // namespace
@@ -569,15 +572,17 @@ bool tc_supported(const Dims& d) {
 
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
                                   const float* dtT, void* dS, bool ds16, int32_t* err,
-                                  cudaStream_t st, uint32_t* xabs) {
+                                  cudaStream_t st, uint32_t* xabs, bool pdl) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     const FuseArgs none{};
     if (ds16)
-        return d.L == 256 ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs)
-                          : launch_k2<128, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs);
-    return d.L == 256 ? launch_k2<256, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs)
-                      : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs);
+        return d.L == 256
+                   ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl)
+                   : launch_k2<128, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl);
+    return d.L == 256
+               ? launch_k2<256, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl)
+               : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl);
 }
 
 int64_t fused_flag_words(const Dims& d) {

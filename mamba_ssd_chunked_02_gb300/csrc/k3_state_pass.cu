@@ -83,6 +83,10 @@ state_pass_kernel(const TD* __restrict__ dS, const float* __restrict__ cum2,
                   int64_t PN, int64_t blocks_per_bh) {
     constexpr int E = Ept<TD>::value;
     constexpr int kDepth = Depth<TD>::value;
+    // dS comes from stage 2 (programmatic dependent launch on the whole-path
+    // call): wait for it, then let stage 4 start launching.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
     const int64_t bh = blockIdx.x / blocks_per_bh;
     const int64_t iv = (blockIdx.x % blocks_per_bh) * kThreads + threadIdx.x;
     const int64_t e = iv * E;
@@ -142,7 +146,7 @@ state_pass_kernel(const TD* __restrict__ dS, const float* __restrict__ cum2,
 
 cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const float* cum2,
                               const float* init, void* Sprev, float* final_state,
-                              int32_t* /*err*/, cudaStream_t st) {
+                              int32_t* /*err*/, cudaStream_t st, bool pdl) {
     const int64_t PN = d.P * d.N;   // multiple of 256 for every supported P, N
     if (d.b == 0 || d.H == 0) return cudaSuccess;
     if (d.nc == 0) {
@@ -155,19 +159,18 @@ cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const fl
     const int64_t blocks_per_bh = (PN / ept + kThreads - 1) / kThreads;
     const int64_t grid = d.b * d.H * blocks_per_bh;
     using bf16 = __nv_bfloat16;
+    const dim3 g((unsigned)grid), blk(kThreads);
     if (d.dtype == 1 && ds16)
-        state_pass_kernel<bf16, bf16><<<(unsigned)grid, kThreads, 0, st>>>(
-            static_cast<const bf16*>(dS), cum2, init, static_cast<bf16*>(Sprev), final_state, d.T,
-            d.H, d.L, d.nc, PN, blocks_per_bh);
-    else if (d.dtype == 1)
-        state_pass_kernel<bf16, float><<<(unsigned)grid, kThreads, 0, st>>>(
-            static_cast<const float*>(dS), cum2, init, static_cast<bf16*>(Sprev), final_state, d.T,
-            d.H, d.L, d.nc, PN, blocks_per_bh);
-    else
-        state_pass_kernel<float, float><<<(unsigned)grid, kThreads, 0, st>>>(
-            static_cast<const float*>(dS), cum2, init, static_cast<float*>(Sprev), final_state, d.T,
-            d.H, d.L, d.nc, PN, blocks_per_bh);
-    return cudaGetLastError();
+        return launch_kernel(state_pass_kernel<bf16, bf16>, g, blk, 0, st, pdl,
+                             static_cast<const bf16*>(dS), cum2, init, static_cast<bf16*>(Sprev),
+                             final_state, d.T, d.H, d.L, d.nc, PN, blocks_per_bh);
+    if (d.dtype == 1)
+        return launch_kernel(state_pass_kernel<bf16, float>, g, blk, 0, st, pdl,
+                             static_cast<const float*>(dS), cum2, init, static_cast<bf16*>(Sprev),
+                             final_state, d.T, d.H, d.L, d.nc, PN, blocks_per_bh);
+    return launch_kernel(state_pass_kernel<float, float>, g, blk, 0, st, pdl,
+                         static_cast<const float*>(dS), cum2, init, static_cast<float*>(Sprev),
+                         final_state, d.T, d.H, d.L, d.nc, PN, blocks_per_bh);
 }
 
 }  // namespace m2

@@ -241,6 +241,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], h * C::P,
                                     c * L + 128 * r, b);
                     const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
+                    // Sprev comes from stage 3: with programmatic dependent launch
+                    // everything before this point ran while it was finishing.
+                    if (it == NA) grid_dep_wait();
                     for (int a = 0; a < NA; ++a)
                         tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
                 }
@@ -594,7 +597,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (!ok) break;
             // ---- previous head's output while the tensor core works on this one.
             if (hi > 0 && !(ok = finish(hi - 1))) break;
-#pragma unroll
             e_prev = e_t;
         }
         if (ok && nh > 0) ok = finish(nh - 1);
@@ -739,7 +741,7 @@ int num_sms4() {
 template <int L, int NA>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
-                      void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs) {
+                      void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
     using C = K4Cfg<L, NA>;
     CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
@@ -766,20 +768,19 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     auto k = chunk_out_tc_kernel<L, NA>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)grid, kThreads, C::SMEM, st>>>(tm_x, tm_b, tm_c, tm_s, tm_y, cum2, dtT, D, xabs,
-                                                 (int)d.T, (int)d.H, (int)d.G, (int)d.nc, hpc,
-                                                 n_hblk, err);
-    return cudaGetLastError();
+    return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
+                         tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
+                         hpc, n_hblk, err);
 }
 
 template <int L>
 cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void* Cm,
                         const float* cum2, const float* dtT, const void* Sprev, const float* D,
-                        void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs) {
+                        void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
     switch (d.N) {
-        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
-        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
-        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs);
+        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
     }
     return cudaErrorInvalidValue;
 }
@@ -789,11 +790,11 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st,
-                                const uint32_t* xabs) {
+                                const uint32_t* xabs, bool pdl) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
-    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs)
-                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs);
+    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl)
+                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
 }
 
 }  // namespace m2

@@ -62,8 +62,9 @@ def test_check_shape(lib):
     assert m2.check_shape(shp(batch=-1)) == m2.ERR_INVALID_ARG
     assert m2.check_shape(shp(headdim=0)) == m2.ERR_INVALID_ARG
     assert m2.check_shape(shp(dtype=7)) == m2.ERR_INVALID_ARG
-    assert m2.check_shape(shp(flags=8)) == m2.ERR_INVALID_ARG
+    assert m2.check_shape(shp(flags=16)) == m2.ERR_INVALID_ARG
     assert m2.check_shape(shp(flags=m2.FLAG_FUSED_STATE | m2.FLAG_FORCE_SIMT)) == m2.OK
+    assert m2.check_shape(shp(flags=m2.FLAG_SERIAL | m2.FLAG_DS_BF16)) == m2.OK
     assert m2.check_shape(shp(headdim=48)) == m2.ERR_UNSUPPORTED
     assert m2.check_shape(shp(dstate=96)) == m2.ERR_UNSUPPORTED
     assert m2.check_shape(shp(chunk_size=32)) == m2.ERR_UNSUPPORTED

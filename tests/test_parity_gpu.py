@@ -233,6 +233,18 @@ def test_fused_path_repeats_exactly():
         assert torch.equal(y, outs[0][0]) and torch.equal(f, outs[0][1])
 
 
+@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+def test_overlapped_launches_match_serial(w):
+    """Stages 2-4 start early by programmatic dependent launch and read their
+    predecessor's outputs only after it completed: the outputs equal those of
+    strictly serial launches bit for bit, on every repetition."""
+    inp = W.make_inputs(w)
+    y0, f0 = run_fwd(inp, w, flags=m2.FLAG_SERIAL)
+    for _ in range(3):
+        y1, f1 = run_fwd(inp, w)
+        assert torch.equal(y0, y1) and torch.equal(f0, f1)
+
+
 def test_chunk_size_independence():
     """The chunking is an evaluation order: L in {64, 128, 256} give the same result."""
     w = wl(1, 1024, 4, 64, 128, 1, 256, seed=31)
