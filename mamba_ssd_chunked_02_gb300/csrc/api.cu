@@ -93,7 +93,7 @@ Carve carve(const Dims& d) {
     c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
     c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
     c.xabs = c.Sprev + align256((size_t)m2::esize(d) * (size_t)m2::n_state(d));
-    c.total = c.xabs + align256(4 * sizeof(uint32_t) * (size_t)(d.b * d.nc * d.H));
+    c.total = c.xabs + align256(8 * sizeof(uint32_t) * (size_t)(d.b * d.nc * d.H));
     return c;
 }
 

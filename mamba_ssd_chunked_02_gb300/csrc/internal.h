@@ -31,8 +31,8 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
                                     int32_t* err, cudaStream_t st);
 // Stage 2: tcgen05 variant (bf16, shapes accepted by tc_supported()); dS is
 // written in fp32, or in bf16 when ds16 (the whole-path call).
-// When xabs is given it also records max |x| per (b, chunk, head): four words
-// per head ([b][nc][H][4], bf16 bit patterns of |x|; their max is the bound).
+// When xabs is given it also records max |x| per (b, chunk, head): eight words
+// per head ([b][nc][H][8], bf16 bit patterns of |x|; their max is the bound).
 // pdl: launched with programmatic dependent launch after stage 1 (the
 // whole-path call): x and B are read before stage 1 completes.
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,

@@ -28,8 +28,10 @@
 //     warps read it back (tcgen05.ld) into a shared [p][n] tile and one TMA
 //     store per head writes it to dS, in fp32 or, on the whole-path call, in
 //     bf16 (the stage-3 kernel reads it back at once; half the bytes).
-// Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), 2-5 = scaling,
-// 6-9 = epilogue.  Stage ring of NS x-buffers; every wait is bounded.
+// Warp roles: 0 = TMA producer, 1 = MMA issuer (+ TMEM owner), then L / 32
+// scaling warps (one x row per thread: two per sub-partition at L = 256, so that
+// one warp's load latency hides behind the other's), then 4 epilogue warps.
+// Stage ring of NS x-buffers; every wait is bounded.
 //
 // Fused variant (stages 2 and 3 in one kernel, used by the whole-path call):
 // the epilogue does not store dS.  Per head it takes the state entering its
@@ -60,12 +62,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
 template <int L, bool kFuse, bool kDS16>
 struct K2Cfg {
     static constexpr int P = 64;
+    static constexpr int kSW = L / 32;                    // scaling warps: one x row per thread
+    static constexpr int kThreads = 64 + 32 * kSW + 128;  // producer, MMA, scaling, epilogue
     // x stages: shared memory left after B^T and the dS staging tiles (the
     // fused variant spends it on its state tiles instead).
     static constexpr int NS = L == 256 ? (kFuse ? 2 : (kDS16 ? 4 : 3)) : 6;
@@ -104,7 +107,7 @@ struct FuseArgs {
 };
 
 template <int L, bool kFuse, bool kDS16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(K2Cfg<L, kFuse, kDS16>::kThreads, 1)
 chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_d,
@@ -132,7 +135,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         mbar_init(&bars.bt_full, 1);
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bars.full[i], 1);
-            mbar_init(&bars.scaled[i], 128);
+            mbar_init(&bars.scaled[i], 32 * C::kSW);
             mbar_init(&bars.xfree[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -239,20 +242,22 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 mbar_wait(&bars.drain, 0, kWaitNs);
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + C::kSW) {
         // ------------------------------------------------------------- scaling
-        const int idx = threadIdx.x - 64;                // 0..127
+        constexpr int kST = 32 * C::kSW;                 // scaling threads
+        constexpr int RPT = L / kST;                     // x rows per thread (1)
+        const int idx = threadIdx.x - 64;                // 0 .. kST - 1
         const int Lc = min(L, T - c * L);
         // Raw decay inputs of the next head, fetched one head ahead.
-        float pc[L / 128], pd[L / 128], plast = 0.f;
+        float pc[RPT], pd[RPT], plast = 0.f;
         auto prefetch = [&](int hh) {
             const int64_t bh = (int64_t)b * H + h0 + hh;
             const float* crow = cum2 + bh * T + (int64_t)c * L;
             const float* drow = dtT + bh * T + (int64_t)c * L;
             plast = __ldg(crow + Lc - 1);
 #pragma unroll
-            for (int r = 0; r < L / 128; ++r) {
-                const int s = idx + 128 * r;
+            for (int r = 0; r < RPT; ++r) {
+                const int s = idx + kST * r;
                 pc[r] = s < Lc ? __ldg(crow + s) : 0.f;
                 pd[r] = s < Lc ? __ldg(drow + s) : 0.f;
             }
@@ -265,9 +270,9 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         prefetch(0);
         for (int i = 0; i < nh; ++i) {
             const int st = i % NS, k = i / NS;
-            float w[L / 128];
+            float w[RPT];
 #pragma unroll
-            for (int r = 0; r < L / 128; ++r) w[r] = pd[r] * ex2(plast - pc[r]);   // 0 past Lc
+            for (int r = 0; r < RPT; ++r) w[r] = pd[r] * ex2(plast - pc[r]);   // 0 past Lc
             if (i + 1 < nh) prefetch(i + 1);
             const bool ok = __all_sync(0xffffffffu,
                                        mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
@@ -275,8 +280,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             uint8_t* xs = sX + st * C::X_BYTES;
             __nv_bfloat162 xm2 = __floats2bfloat162_rn(0.f, 0.f);   // max |x| (raw), two lanes
 #pragma unroll
-            for (int r = 0; r < L / 128; ++r) {
-                const int s = idx + 128 * r;
+            for (int r = 0; r < RPT; ++r) {
+                const int s = idx + kST * r;
                 uint4* row = reinterpret_cast<uint4*>(xs + s * 128);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -303,8 +308,11 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             if (xabs) {   // this warp's share of max |x| over the chunk, as bf16 bits
                 const uint32_t m2u = *reinterpret_cast<const uint32_t*>(&xm2);
                 const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2u & 0xffffu, m2u >> 16));
-                if (lane == 0)
-                    xabs[((((int64_t)b * nc + c) * H + h0 + i) << 2) + (warp - 2)] = m;
+                if (lane == 0) {   // eight words per head; with four scaling warps the rest are 0
+                    uint32_t* xw = xabs + ((((int64_t)b * nc + c) * H + h0 + i) << 3);
+                    xw[warp - 2] = m;
+                    if (C::kSW == 4) xw[warp + 2] = 0u;
+                }
             }
         }
     } else {
@@ -315,7 +323,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // variant: lane n reads Sprev_c[p, n] for every p (a warp covers 128
         // consecutive bytes), stores it as bf16 and passes the next state on.
         const int q = warp & 3;                          // TMEM lane quadrant
-        const int ep = threadIdx.x - 192;                // 0..127
+        const int ep = threadIdx.x - 64 - 32 * C::kSW;   // 0..127
         const int NT = N < 128 ? N : 128;                // n-tile width = tile row pitch
         const int nl = 32 * q + lane;                    // n within the tile
         uint32_t sync_phase = 0;
@@ -556,7 +564,7 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     auto k = chunk_state_tc_kernel<L, kFuse, kDS16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
+    return launch_kernel(k, dim3((unsigned)grid), dim3(C::kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
                          tm_ring, tm_init, tm_fin, tm_sp, cum2, dtT, (int)d.T, (int)d.H, (int)d.N,
                          (int)d.G, (int)d.nc, n_tiles, hpc, n_hblk, err, fa, xabs);
 }

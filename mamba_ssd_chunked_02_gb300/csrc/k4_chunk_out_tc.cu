@@ -622,7 +622,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         float pc[KPT], pd[KPT], plast = 0.f, pD = 0.f;
 #pragma unroll
         for (int i = 0; i < KPT; ++i) { pc[i] = 0.f; pd[i] = 0.f; }
-        uint4 pX = make_uint4(0u, 0u, 0u, 0u);
+        uint4 pX = make_uint4(0u, 0u, 0u, 0u), pX2 = pX;
         auto prefetch = [&](int hh) {
             const float* crow = cum2 + row0 + (int64_t)hh * T;
             const float* drow = dtT + row0 + (int64_t)hh * T;
@@ -636,8 +636,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
             pD = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
-            if (xabs)   // stage 2's max |x| of the chunk (four words, bf16 bits)
-                pX = __ldg(reinterpret_cast<const uint4*>(xabs) + ((int64_t)b * nc + c) * H + h0 + hh);
+            if (xabs) {   // stage 2's max |x| of the chunk (eight words, bf16 bits)
+                const uint4* xw = reinterpret_cast<const uint4*>(xabs) + 2 * (((int64_t)b * nc + c) * H + h0 + hh);
+                pX = __ldg(xw);
+                pX2 = __ldg(xw + 1);
+            }
         };
         if (nh > 0) prefetch(0);
         // The C.B^T bound comes from the epilogue (after GEMM1); by then every
@@ -662,7 +665,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
             }
             const float dval = pD;
-            const uint32_t xknown = max(max(pX.x, pX.y), max(pX.z, pX.w));
+            const uint32_t xknown = max(max(max(pX.x, pX.y), max(pX.z, pX.w)),
+                                        max(max(pX2.x, pX2.y), max(pX2.z, pX2.w)));
             if (hi + 1 < nh) prefetch(hi + 1);
             uint8_t* xs = sStage + st * C::STAGE;
             const int nch = KS * 8 / kConvThreads;

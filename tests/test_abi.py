@@ -80,13 +80,13 @@ def test_workspace_size(lib):
         nc = -(-T // L)
         es = 2 if s.dtype == m2.BF16 else 4
         want = 2 * a256(4 * b * H * T) + a256(4 * b * nc * H * P * N) + \
-            a256(es * b * nc * H * P * N) + a256(16 * b * nc * H)
+            a256(es * b * nc * H * P * N) + a256(32 * b * nc * H)
         assert m2.workspace_size(s) == want
     assert m2.workspace_size(shp(headdim=48)) == 0
     # The 2.7B-layer workload: cum2 + dtT (2 x 10.5 MB), dS (335.5 MB fp32), Sprev (167.8 MB bf16),
     # max |x| words (160 KB).
     s = shp(batch=8, seqlen=4096, nheads=80)
-    assert m2.workspace_size(s) == 2 * 10_485_760 + 335_544_320 + 167_772_160 + 163_840
+    assert m2.workspace_size(s) == 2 * 10_485_760 + 335_544_320 + 167_772_160 + 327_680
 
 
 def test_path_selection(lib):
