@@ -481,25 +481,22 @@ int num_sms() {
     return cached[dev];
 }
 
-// Heads per CTA (one CTA per SM at a time): the largest divisor of H/G, at
-// most 16 (B^T is loaded once per CTA), that gives at least four waves of CTAs
-// and keeps the last wave at least 90 % full; otherwise the divisor with the
-// fullest last wave; with too few work items, one head per CTA.
+// Heads per CTA (one CTA per SM at a time): the divisor v of H/G that
+// minimises (waves of CTAs) x (v + 4), i.e. per-SM time in head units with a
+// CTA's fixed work (loading B^T, filling and draining the x ring) counted as
+// about four heads (fitted to measurements: at b8 T4096 H80 N128 whole-path
+// times of 440, 437, 429 and 423 us for 10, 20, 40 and 80 heads per CTA).
 int pick_hpc(const Dims& d, int64_t outer) {
-    const int hpg = (int)(d.H / d.G);
-    const int64_t sms = num_sms();
+    const int64_t hpg = d.H / d.G, sms = num_sms();
     int best = 1;
-    double best_eff = -1.0;
-    for (int v = 16; v >= 1; --v) {
+    int64_t best_cost = -1;
+    for (int64_t v = 1; v <= hpg; ++v) {
         if (hpg % v) continue;
         const int64_t ctas = outer * (d.H / v);
-        if (ctas < 4 * sms) continue;
-        const double waves = (double)ctas / (double)sms;
-        const double eff = waves / (double)((ctas + sms - 1) / sms);
-        if (eff >= 0.9) return v;
-        if (eff > best_eff) {
-            best_eff = eff;
-            best = v;
+        const int64_t cost = (ctas + sms - 1) / sms * (v + 4);
+        if (best_cost < 0 || cost <= best_cost) {
+            best_cost = cost;
+            best = (int)v;
         }
     }
     return best;

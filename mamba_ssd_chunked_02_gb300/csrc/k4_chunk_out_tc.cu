@@ -742,6 +742,27 @@ int num_sms4() {
     return cached[dev];
 }
 
+// Heads per CTA: the divisor v of H/G that minimises (waves of CTAs) x (v + 2),
+// i.e. per-SM time in head units with a CTA's fixed work (the C.B^T product and
+// its packing, the pipeline's fill and drain) counted as about two heads.  At
+// b8 T4096 H80: 20 heads, 1024 CTAs (440 us for the whole path, against 445 with
+// 16 and 462 with 10).
+int pick_hpc4(const Dims& d, int64_t outer) {
+    const int64_t hpg = d.H / d.G, sms = num_sms4();
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int64_t v = 1; v <= hpg && v <= 64; ++v) {
+        if (hpg % v) continue;
+        const int64_t ctas = outer * (d.H / v);
+        const int64_t cost = (ctas + sms - 1) / sms * (v + 2);
+        if (best_cost < 0 || cost <= best_cost) {
+            best_cost = cost;
+            best = (int)v;
+        }
+    }
+    return best;
+}
+
 template <int L, int NA>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
@@ -763,10 +784,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
         return cudaErrorInvalidValue;
     const int NQ = L / 128;
     const int64_t outer = d.b * d.nc * NQ;
-    const int hpg = (int)(d.H / d.G);
-    int hpc = 1;
-    for (int v = 16; v >= 1; --v)
-        if (hpg % v == 0 && outer * (d.H / v) >= 4LL * num_sms4()) { hpc = v; break; }
+    const int hpc = pick_hpc4(d, outer);
     const int n_hblk = (int)(d.H / hpc);
     const int64_t grid = outer * n_hblk;
     auto k = chunk_out_tc_kernel<L, NA>;
