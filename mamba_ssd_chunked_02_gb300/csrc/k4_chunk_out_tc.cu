@@ -62,6 +62,14 @@
 // set the pace, only build M, rescale and write y.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <array>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc5.cuh"
@@ -149,7 +157,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
-                    int G, int nc, int hpc, int n_hblk, int32_t* err) {
+                    int G, int nc, int v1, int n1, int v2, int32_t* err) {
     using C = K4Cfg<L, NA>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -166,12 +174,20 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     volatile int* abort = &bars.abort;
 
     // Work item: (b, c, head block) outer; the query tiles of one item are
-    // adjacent (heaviest first) so that they share x and Sprev through L2.
-    int rest = blockIdx.x;
+    // adjacent (heaviest first) so that they share x and Sprev through L2.  The
+    // first n1 CTAs take blocks of v1 heads, the rest (the last (b, c) pairs)
+    // blocks of v2 heads, so that the last wave of CTAs ends evenly.
+    int rest = blockIdx.x, hpc = v1, bc0 = 0;
+    if (rest >= n1) {
+        rest -= n1;
+        hpc = v2;
+        bc0 = n1 / (NQ * (H / v1));
+    }
+    const int n_hblk = H / hpc;
     const int qt = NQ - 1 - rest % NQ; rest /= NQ;
     const int hblk = rest % n_hblk; rest /= n_hblk;
-    const int c = rest % nc;
-    const int b = rest / nc;
+    const int c = (bc0 + rest) % nc;
+    const int b = (bc0 + rest) / nc;
     const int KS = 128 * (qt + 1);
     const int h0 = hblk * hpc;
     const int g = h0 / (H / G);
@@ -742,24 +758,80 @@ int num_sms4() {
     return cached[dev];
 }
 
-// Heads per CTA: the divisor v of H/G that minimises (waves of CTAs) x (v + 2),
-// i.e. per-SM time in head units with a CTA's fixed work (the C.B^T product and
-// its packing, the pipeline's fill and drain) counted as about two heads.  At
-// b8 T4096 H80: 20 heads, 1024 CTAs (440 us for the whole path, against 445 with
-// 16 and 462 with 10).
-int pick_hpc4(const Dims& d, int64_t outer) {
-    const int64_t hpg = d.H / d.G, sms = num_sms4();
-    int best = 1;
-    int64_t best_cost = -1;
-    for (int64_t v = 1; v <= hpg && v <= 64; ++v) {
-        if (hpg % v) continue;
-        const int64_t ctas = outer * (d.H / v);
-        const int64_t cost = (ctas + sms - 1) / sms * (v + 2);
-        if (best_cost < 0 || cost <= best_cost) {
-            best_cost = cost;
-            best = (int)v;
+// Head blocks per CTA.  One CTA per SM at a time, each with a fixed cost (the
+// C.B^T product and its packing, the pipeline's fill and drain) of about two
+// heads; the second query tile costs about 1.25 times the first per head.  The
+// grid is cut in two regions: the first n1 CTAs take blocks of v1 heads (the
+// first (b, c) pairs), the rest blocks of v2 heads, both dividing H/G.  The
+// choice minimises the makespan of a simulation of greedy CTA scheduling over
+// the SMs: single sizes, and mixes whose first region fills whole waves.  At
+// b8 T4096 H80 it takes 40 heads for 114 of the 128 (b, c) pairs and 16 for the
+// rest (1 024 CTAs of 20 heads simulate to 179 head units, the mix to 168).
+struct Split4 {
+    int v1, v2;
+    int64_t n1, ctas;
+};
+
+double makespan4(int64_t bc, int64_t n1_bc, int v1, int v2, int64_t H, int NQ, int sms) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> q;
+    for (int i = 0; i < sms; ++i) q.push(0.0);
+    double mk = 0.0;
+    auto run = [&](int64_t nbc, int v) {
+        for (int64_t i = 0; i < nbc * (H / v); ++i)
+            for (int qt = NQ - 1; qt >= 0; --qt) {
+                const double t = q.top() + v * (qt ? 1.25 : 1.0) + 2.0;
+                q.pop();
+                q.push(t);
+                mk = std::max(mk, t);
+            }
+    };
+    run(n1_bc, v1);
+    run(bc - n1_bc, v2);
+    return mk;
+}
+
+Split4 pick_split4(const Dims& d, int NQ) {
+    static std::mutex mu;
+    static std::map<std::array<int64_t, 5>, Split4> cache;
+    const int sms = num_sms4();
+    const std::array<int64_t, 5> key = {d.b * d.nc, d.H, d.G, NQ, sms};
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int64_t bc = d.b * d.nc, hpg = d.H / d.G, cap = 32LL * sms;   // CTAs simulated at most
+    std::vector<int> divs;
+    for (int64_t v = 1; v <= hpg; ++v)
+        if (hpg % v == 0 && bc * NQ * (d.H / v) <= cap) divs.push_back((int)v);
+    if (divs.empty()) divs.push_back((int)hpg);
+    Split4 best{divs.back(), divs.back(), bc * NQ * (d.H / divs.back()), bc * NQ * (d.H / divs.back())};
+    double best_t = -1.0;
+    auto consider = [&](int64_t n1_bc, int v1, int v2) {
+        const double t = makespan4(bc, n1_bc, v1, v2, d.H, NQ, sms);
+        const int64_t n1 = n1_bc * NQ * (d.H / v1), ctas = n1 + (bc - n1_bc) * NQ * (d.H / v2);
+        if (best_t < 0.0 || t < best_t * 0.999 || (t <= best_t * 1.001 && ctas < best.ctas)) {
+            best_t = t;
+            best = {v1, v2, n1, ctas};
+        }
+    };
+    int vsingle = divs.front();
+    double tsingle = -1.0;
+    for (int v : divs) {
+        const double t = makespan4(bc, bc, v, v, d.H, NQ, sms);
+        if (tsingle < 0.0 || t <= tsingle) { tsingle = t; vsingle = v; }
+        consider(bc, v, v);
+    }
+    for (int v1 : divs) {
+        if (v1 < vsingle) continue;
+        const int64_t per_bc = NQ * (d.H / v1);
+        for (int64_t k = 1; k <= 32; ++k) {
+            const int64_t n1_bc = k * sms / per_bc;
+            if (n1_bc <= 0) continue;
+            if (n1_bc >= bc) break;
+            for (int v2 : divs)
+                if (v2 < v1) consider(n1_bc, v1, v2);
         }
     }
+    cache[key] = best;
     return best;
 }
 
@@ -783,16 +855,14 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
         !make_tmap_bf16(&tm_y, y, 3, xd, xs, ybox, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     const int NQ = L / 128;
-    const int64_t outer = d.b * d.nc * NQ;
-    const int hpc = pick_hpc4(d, outer);
-    const int n_hblk = (int)(d.H / hpc);
-    const int64_t grid = outer * n_hblk;
+    const Split4 sp = pick_split4(d, NQ);
+    const int64_t grid = sp.ctas;
     auto k = chunk_out_tc_kernel<L, NA>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
-                         hpc, n_hblk, err);
+                         sp.v1, (int)sp.n1, sp.v2, err);
 }
 
 template <int L>
