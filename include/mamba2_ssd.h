@@ -165,6 +165,33 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape,
                              void* workspace, size_t workspace_bytes, void* stream,
                              void* const* events);
 
+/* Element strides of the large input/output tensors for mamba2_ssd_fwd_strided:
+ * for each tensor, {batch stride, token stride} in elements.  Within one token
+ * the data stay contiguous: H*P elements (head-major) for x and y, G*N for B and
+ * C, H for dt.  Contiguous tensors have x = y = {T*H*P, H*P}, B = C = {T*G*N,
+ * G*N}, dt = {T*H, H}, with which the call equals mamba2_ssd_fwd.  The typical
+ * use is x, B and C as column slices of one projection output [b, T, H*P +
+ * 2*G*N] (token stride H*P + 2*G*N) and y written into a wider buffer.
+ * Requirements (else MAMBA2_ERR_INVALID_ARG): token stride >= the token's
+ * extent, batch stride >= T * token stride, both > 0 (batch stride ignored when
+ * batch == 1); y must not overlap any input.  Strides whose byte size is not a
+ * multiple of 16 take the CUDA-core kernels (the tensor-memory-accelerator
+ * copies of the tensor-core kernels need 16-byte strides); results are the same
+ * as for contiguous tensors either way. */
+typedef struct mamba2_ssd_strides {
+    int64_t x[2], dt[2], B[2], C[2], y[2];
+} mamba2_ssd_strides;
+
+/* mamba2_ssd_fwd on strided x, dt, B, C and y (see mamba2_ssd_strides);
+ * initial_state and final_state stay contiguous [b, H, P, N]. */
+MAMBA2_API mamba2_status mamba2_ssd_fwd_strided(const mamba2_ssd_shape* shape,
+                             const mamba2_ssd_strides* strides,
+                             const void* x, const float* dt, const float* A,
+                             const void* B, const void* C, const float* D,
+                             const float* initial_state,
+                             void* y, float* final_state,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /* Stage 1, chunk_cumsum [P3 section 7; P2 "세 가지 핵심 커널 구현"]:
  *   cum2[b,h,t] = log2(e) * sum_{r = chunk start of t}^{t} dt[b,r,h] * A[h]
  *   dtT[b,h,t]  = dt[b,t,h]

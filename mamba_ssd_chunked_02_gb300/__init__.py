@@ -42,7 +42,8 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_ssd_state_pass", "mamba2_ssd_chunk_out", "mamba2_ssd_device_error",
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
            "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
-           "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode", "mamba2_ssd_fwd_timed")
+           "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode", "mamba2_ssd_fwd_timed",
+           "mamba2_ssd_fwd_strided")
 
 
 class Shape(ctypes.Structure):
@@ -56,6 +57,11 @@ class Shape(ctypes.Structure):
     @property
     def nchunks(self) -> int:
         return (self.seqlen + self.chunk_size - 1) // self.chunk_size
+
+
+class Strides(ctypes.Structure):
+    """mirror of struct mamba2_ssd_strides: {batch, token} element strides"""
+    _fields_ = [(n, ctypes.c_int64 * 2) for n in ("x", "dt", "B", "C", "y")]
 
 
 class Mamba2Error(RuntimeError):
@@ -88,6 +94,9 @@ def load():
         lib.mamba2_ssd_workspace_size.restype = ctypes.c_size_t
         lib.mamba2_ssd_fwd.argtypes = [sp] + [vp] * 9 + [vp, ctypes.c_size_t, vp]
         lib.mamba2_ssd_fwd.restype = ctypes.c_int
+        lib.mamba2_ssd_fwd_strided.argtypes = [sp, ctypes.POINTER(Strides)] + [vp] * 9 + \
+            [vp, ctypes.c_size_t, vp]
+        lib.mamba2_ssd_fwd_strided.restype = ctypes.c_int
         lib.mamba2_ssd_chunk_cumsum.argtypes = [sp, vp, vp, vp, vp, vp]
         lib.mamba2_ssd_chunk_cumsum.restype = ctypes.c_int
         lib.mamba2_ssd_chunk_state.argtypes = [sp, vp, vp, vp, vp, vp, vp]
@@ -178,6 +187,34 @@ def _ptr(t, name, dtype=None, shape=None, optional=False):
     return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
 
 
+def _token_strided(t, inner):
+    """True when t is a view whose last `inner` dims are contiguous (a token's
+    data in one piece) but whose batch/token strides are not the contiguous
+    ones: the layout mamba2_ssd_fwd_strided takes."""
+    if t is None or t.is_contiguous():
+        return False
+    st, sz = t.stride(), t.shape
+    want = 1
+    for k in range(t.dim() - 1, t.dim() - 1 - inner, -1):
+        if sz[k] != 1 and st[k] != want:
+            return False
+        want *= sz[k]
+    return True
+
+
+def _strided_ptr(t, name, dtype, shape, inner):
+    """Pointer of a token-strided tensor and its {batch, token} element strides."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not (t.is_contiguous() or _token_strided(t, inner)):
+        raise ValueError(f"{name}: each token's data must be contiguous")
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0), (t.stride(0), t.stride(1))
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -199,9 +236,12 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=
 
     x [b,T,H,P] bf16|f32, dt [b,T,H] f32, A [H] f32, B/C [b,T,G,N] (x's dtype),
     D [H] f32 or None, initial_state [b,H,P,N] f32 or None.  y, final_state and
-    workspace are allocated with torch when not given.  `events`: five
-    torch.cuda.Event (or None entries) recorded before stage 1, after each stage
-    and after stage 4 (mamba2_ssd_fwd_timed).
+    workspace are allocated with torch when not given.  x, dt, B, C and y may be
+    views with any batch and token strides as long as each token's data is
+    contiguous (e.g. column slices of one projection output): they go through
+    mamba2_ssd_fwd_strided.  `events`: five torch.cuda.Event (or None entries)
+    recorded before stage 1, after each stage and after stage 4
+    (mamba2_ssd_fwd_timed; contiguous tensors only).
     """
     lib = load()
     sh = shape_of(x, B, chunk_size, ngroups, flags)
@@ -214,6 +254,24 @@ def ssd_fwd(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=
     need = workspace_size(sh)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if any(_token_strided(t, k) for t, k in ((x, 2), (dt, 1), (B, 2), (C, 2), (y, 2))):
+        if events is not None:
+            raise ValueError("events: contiguous tensors only")
+        st = Strides()
+        px, st.x[:] = _strided_ptr(x, "x", io, (b, T, H, P), 2)
+        pd, st.dt[:] = _strided_ptr(dt, "dt", torch.float32, (b, T, H), 1)
+        pb, st.B[:] = _strided_ptr(B, "B", io, (b, T, G, N), 2)
+        pc, st.C[:] = _strided_ptr(C, "C", io, (b, T, G, N), 2)
+        py, st.y[:] = _strided_ptr(y, "y", io, (b, T, H, P), 2)
+        _check("mamba2_ssd_fwd_strided", lib.mamba2_ssd_fwd_strided(
+            ctypes.byref(sh), ctypes.byref(st), px, pd, _ptr(A, "A", torch.float32, (H,)), pb, pc,
+            _ptr(D, "D", torch.float32, (H,), optional=True),
+            _ptr(initial_state, "initial_state", torch.float32, (b, H, P, N), optional=True),
+            py, _ptr(final_state, "final_state", torch.float32, (b, H, P, N)),
+            _ptr(workspace, "workspace", optional=True),
+            ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
+            _stream(stream)))
+        return y, final_state
     args = [
         _ptr(x, "x", io, (b, T, H, P)), _ptr(dt, "dt", torch.float32, (b, T, H)),
         _ptr(A, "A", torch.float32, (H,)), _ptr(B, "B", io, (b, T, G, N)),

@@ -73,7 +73,39 @@ Dims dims_of(const mamba2_ssd_shape* s) {
     d.b = s->batch; d.T = s->seqlen; d.H = s->nheads; d.P = s->headdim; d.N = s->dstate;
     d.G = s->ngroups; d.L = s->chunk_size; d.nc = (d.T + d.L - 1) / d.L;
     d.dtype = s->dtype == MAMBA2_BF16 ? 1 : 0;
+    m2::set_contiguous(d);
     return d;
+}
+
+// Strides of mamba2_ssd_fwd_strided into d: each token stride at least the
+// token's extent, each batch stride at least T token strides (batch strides are
+// not used with one batch entry and are set to that then), T token strides and
+// each batch stride below 2^40 elements.
+mamba2_status set_strides(Dims& d, const mamba2_ssd_strides* st) {
+    auto one = [&](const int64_t (&in)[2], int64_t extent, int64_t (&out)[2]) -> bool {
+        const int64_t lim = int64_t(1) << 40;
+        if (in[1] < extent || in[1] <= 0) return false;
+        if (d.T > 0 && in[1] > (lim - 1) / d.T) return false;
+        const int64_t bs = d.b > 1 ? in[0] : d.T * in[1];
+        if (bs < d.T * in[1] || bs >= lim) return false;
+        out[0] = bs;
+        out[1] = in[1];
+        return true;
+    };
+    if (!st) return MAMBA2_ERR_INVALID_ARG;
+    return one(st->x, d.H * d.P, d.sx) && one(st->y, d.H * d.P, d.sy) && one(st->B, d.G * d.N, d.sB) &&
+                   one(st->C, d.G * d.N, d.sC) && one(st->dt, d.H, d.sdt)
+               ? MAMBA2_OK
+               : MAMBA2_ERR_INVALID_ARG;
+}
+
+// The tensor-core kernels move x, y, B and C with tensor-memory-accelerator
+// copies, whose global strides must be multiples of 16 bytes.
+bool tma_strides(const Dims& d) {
+    const int64_t es = m2::esize(d);
+    for (const int64_t* v : {d.sx, d.sy, d.sB, d.sC})
+        if ((v[0] * es) % 16 || (v[1] * es) % 16) return false;
+    return true;
 }
 
 bool use_tc(const mamba2_ssd_shape* s, const Dims& d) {
@@ -235,10 +267,12 @@ namespace {
 mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float* dt,
                        const float* A, const void* B, const void* C, const float* D,
                        const float* initial_state, void* y, float* final_state, void* workspace,
-                       size_t workspace_bytes, void* stream, void* const* events) {
+                       size_t workspace_bytes, void* stream, void* const* events,
+                       const mamba2_ssd_strides* strides = nullptr) {
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
-    const Dims d = dims_of(shape);
+    Dims d = dims_of(shape);
+    if (strides && (st = set_strides(d, strides)) != MAMBA2_OK) return st;
     const bool empty = d.b * d.T * d.H == 0;
     if (!req(x, empty) || !req(dt, empty) || !req(A, empty) || !req(B, empty) ||
         !req(C, empty) || !opt(D) || !opt(initial_state) || !req(y, empty) ||
@@ -259,7 +293,7 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
     float* dS = reinterpret_cast<float*>(ws + cv.dS);
     void* Sprev = ws + cv.Sprev;
     uint32_t* xabs = reinterpret_cast<uint32_t*>(ws + cv.xabs);   // stage 2 -> stage 4: max |x|
-    const bool tc = use_tc(shape, d);
+    const bool tc = use_tc(shape, d) && tma_strides(d);
     // Fused stages 2+3 (opt-in): the two-slot carried-state ring, the flag words
     // and the ticket live in the dS region, which holds them from three chunks on.
     const size_t ring = 2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N);
@@ -315,6 +349,17 @@ mamba2_status mamba2_ssd_fwd(const mamba2_ssd_shape* shape, const void* x, const
                              void* workspace, size_t workspace_bytes, void* stream) {
     return fwd_impl(shape, x, dt, A, B, C, D, initial_state, y, final_state, workspace,
                     workspace_bytes, stream, nullptr);
+}
+
+mamba2_status mamba2_ssd_fwd_strided(const mamba2_ssd_shape* shape,
+                                     const mamba2_ssd_strides* strides, const void* x,
+                                     const float* dt, const float* A, const void* B, const void* C,
+                                     const float* D, const float* initial_state, void* y,
+                                     float* final_state, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+    if (!strides) return MAMBA2_ERR_INVALID_ARG;
+    return fwd_impl(shape, x, dt, A, B, C, D, initial_state, y, final_state, workspace,
+                    workspace_bytes, stream, nullptr, strides);
 }
 
 mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x, const float* dt,

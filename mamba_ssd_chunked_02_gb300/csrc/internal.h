@@ -11,7 +11,21 @@ namespace m2 {
 struct Dims {
     int64_t b, T, H, P, N, G, L, nc;
     int dtype;   // 0 = f32, 1 = bf16 (element type of x, B, C, y, Sprev)
+    // Element strides {batch, token} of x, y ([.., H*P] contiguous per token),
+    // B, C ([.., G*N]) and dt ([.., H]); contiguous unless set by the strided
+    // whole-path call (the stage entry points take contiguous tensors).
+    int64_t sx[2], sy[2], sB[2], sC[2], sdt[2];
 };
+
+// Contiguous strides for the sizes in d.
+inline void set_contiguous(Dims& d) {
+    d.sx[1] = d.sy[1] = d.H * d.P;
+    d.sx[0] = d.sy[0] = d.T * d.H * d.P;
+    d.sB[1] = d.sC[1] = d.G * d.N;
+    d.sB[0] = d.sC[0] = d.T * d.G * d.N;
+    d.sdt[1] = d.H;
+    d.sdt[0] = d.T * d.H;
+}
 
 // Element counts and byte sizes of the intermediates.
 inline int64_t n_cum(const Dims& d) { return d.b * d.H * d.T; }

@@ -36,7 +36,7 @@ template <int L>
 __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H,
-                    int32_t* __restrict__ zero, int64_t nzero) {
+                    int64_t sb, int64_t stt, int32_t* __restrict__ zero, int64_t nzero) {
     constexpr int E = L / 32;                 // tokens per lane
     constexpr int kPitch = L + L / 32 + 1;    // odd
     __shared__ float tile[kHB * kPitch];
@@ -54,17 +54,17 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     const int nt = (int)min((int64_t)L, T - t0);
     const int nh = (int)min((int64_t)kHB, H - h0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float* src = dt + (b * T + t0) * H + h0;
+    const float* src = dt + b * sb + t0 * stt + h0;   // dt[b, t, h]: strides sb, stt, 1
 
     // Load [nt x nh] (token-major in HBM) and transpose into tile[head][token].
-    if (nh == kHB && (H & 3) == 0) {
+    if (nh == kHB && (H & 3) == 0 && (stt & 3) == 0 && (sb & 3) == 0) {
         // 8 float4 per token row; element (token i, quad q) of item idx = i * 8 + q.
         constexpr int kPer = L * kHB / 4 / kThreads;
         float4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int idx = threadIdx.x + kThreads * k, i = idx >> 3, q = idx & 7;
-            v[k] = i < nt ? __ldg(reinterpret_cast<const float4*>(src + (int64_t)i * H) + q)
+            v[k] = i < nt ? __ldg(reinterpret_cast<const float4*>(src + (int64_t)i * stt) + q)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -78,7 +78,7 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     } else {
         for (int idx = threadIdx.x; idx < L * kHB; idx += kThreads) {
             const int i = idx / kHB, j = idx % kHB;
-            tile[j * kPitch + tpos(i)] = (i < nt && j < nh) ? __ldg(src + (int64_t)i * H + j) : 0.f;
+            tile[j * kPitch + tpos(i)] = (i < nt && j < nh) ? __ldg(src + (int64_t)i * stt + j) : 0.f;
         }
     }
     __syncthreads();
@@ -121,13 +121,16 @@ cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, 
     const dim3 grid((unsigned)d.nc, (unsigned)d.b, (unsigned)((d.H + kHB - 1) / kHB));
     switch (d.L) {
         case 64:
-            chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
+                                                                d.sdt[1], zero, nzero);
             break;
         case 128:
-            chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
+                                                                d.sdt[1], zero, nzero);
             break;
         case 256:
-            chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, zero, nzero);
+            chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
+                                                                d.sdt[1], zero, nzero);
             break;
         default: return cudaErrorInvalidValue;
     }

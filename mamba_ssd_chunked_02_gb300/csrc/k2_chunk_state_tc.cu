@@ -519,10 +519,10 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     constexpr bool ds16 = kDS16;
     CUtensorMap tm_x, tm_b;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
-    const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
+    const uint64_t xs[2] = {(uint64_t)(d.sx[1] * 2), (uint64_t)(d.sx[0] * 2)};   // token, batch
     const uint32_t box[3] = {64, (uint32_t)L, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
-    const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
+    const uint64_t bs[2] = {(uint64_t)(d.sB[1] * 2), (uint64_t)(d.sB[0] * 2)};
     if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box))
         return cudaErrorInvalidValue;
     CUtensorMap tm_d = tm_x;   // the fused variant stores no dS

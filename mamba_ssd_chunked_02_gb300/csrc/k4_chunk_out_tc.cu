@@ -842,17 +842,19 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     using C = K4Cfg<L, NA>;
     CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
-    const uint64_t xs[2] = {(uint64_t)(d.H * d.P * 2), (uint64_t)(d.T * d.H * d.P * 2)};
+    const uint64_t xs[2] = {(uint64_t)(d.sx[1] * 2), (uint64_t)(d.sx[0] * 2)};   // token, batch
+    const uint64_t ys[2] = {(uint64_t)(d.sy[1] * 2), (uint64_t)(d.sy[0] * 2)};
     const uint32_t box[3] = {64, 128, 1};
     const uint32_t ybox[3] = {32, 32, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
-    const uint64_t bs[2] = {(uint64_t)(d.G * d.N * 2), (uint64_t)(d.T * d.G * d.N * 2)};
+    const uint64_t bs[2] = {(uint64_t)(d.sB[1] * 2), (uint64_t)(d.sB[0] * 2)};
+    const uint64_t cs[2] = {(uint64_t)(d.sC[1] * 2), (uint64_t)(d.sC[0] * 2)};
     const uint64_t sd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
     const uint64_t ss[1] = {(uint64_t)(d.N * 2)};
     const uint32_t sbox[2] = {64, 64};
     if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
-        !make_tmap_bf16(&tm_c, Cm, 3, bd, bs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
-        !make_tmap_bf16(&tm_y, y, 3, xd, xs, ybox, CU_TENSOR_MAP_SWIZZLE_64B))
+        !make_tmap_bf16(&tm_c, Cm, 3, bd, cs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
+        !make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     const int NQ = L / 128;
     const Split4 sp = pick_split4(d, NQ);

@@ -21,6 +21,15 @@ constexpr int kThreads = 256;
 // ------------------------------------------------------------------ stage 2 ---
 // dS[b,c,h,p,n] = sum_{s in chunk c} w_s x[s,p] B[s,n],
 // w_s = dtT[s] * exp2(cum2[last] - cum2[s]).
+// Element strides {batch, token} of x, y, B and C (a token's H*P or G*N
+// elements are contiguous).
+struct IoStrides {
+    int64_t xb, xt, yb, yt, Bb, Bt, Cb, Ct;
+};
+IoStrides io_strides(const Dims& d) {
+    return {d.sx[0], d.sx[1], d.sy[0], d.sy[1], d.sB[0], d.sB[1], d.sC[0], d.sC[1]};
+}
+
 // CTA per (b, c, h) x (64-wide p tile) x (64-wide n tile); each thread owns a
 // 4 x 4 register tile; s is consumed in blocks of 32 staged in shared memory.
 template <typename T>
@@ -28,7 +37,7 @@ __global__ void __launch_bounds__(kThreads)
 chunk_state_simt_kernel(const T* __restrict__ x, const T* __restrict__ B,
                         const float* __restrict__ cum2, const float* __restrict__ dtT,
                         float* __restrict__ dS, int64_t Tlen, int64_t H, int64_t P, int64_t N,
-                        int64_t G, int64_t L, int64_t nc) {
+                        int64_t G, int64_t L, int64_t nc, IoStrides io) {
     constexpr int TP = 64, TN = 64, SB = 32;
     __shared__ float xs[SB][TP];
     __shared__ float bs[SB][TN];
@@ -55,12 +64,12 @@ chunk_state_simt_kernel(const T* __restrict__ x, const T* __restrict__ B,
         for (int idx = threadIdx.x; idx < SB * TP; idx += kThreads) {
             const int i = idx / TP, j = idx % TP;
             const int64_t s = s0 + i, p = p0 + j;
-            xs[i][j] = (s < t1 && p < P) ? ws[i] * to_f32(x[((b * Tlen + s) * H + h) * P + p]) : 0.f;
+            xs[i][j] = (s < t1 && p < P) ? ws[i] * to_f32(x[b * io.xb + s * io.xt + h * P + p]) : 0.f;
         }
         for (int idx = threadIdx.x; idx < SB * TN; idx += kThreads) {
             const int i = idx / TN, j = idx % TN;
             const int64_t s = s0 + i, n = n0 + j;
-            bs[i][j] = (s < t1 && n < N) ? to_f32(B[((b * Tlen + s) * G + g) * N + n]) : 0.f;
+            bs[i][j] = (s < t1 && n < N) ? to_f32(B[b * io.Bb + s * io.Bt + g * N + n]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -100,7 +109,7 @@ chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T*
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       const T* __restrict__ Sprev, const float* __restrict__ D,
                       T* __restrict__ y, int64_t Tlen, int64_t H, int64_t P, int64_t N,
-                      int64_t G, int64_t L, int64_t nc) {
+                      int64_t G, int64_t L, int64_t nc, IoStrides io) {
     constexpr int TT = 32, SB = 32;
     extern __shared__ float smem[];
     const int NP = (int)N + 1;                 // padded rows (bank spread)
@@ -126,7 +135,7 @@ chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T*
     for (int idx = threadIdx.x; idx < TT * N; idx += kThreads) {
         const int i = idx / (int)N, n = idx % (int)N;
         const int64_t t = q0 + i;
-        Cs[idx] = t < q1 ? to_f32(C[((b * Tlen + t) * G + g) * N + n]) : 0.f;
+        Cs[idx] = t < q1 ? to_f32(C[b * io.Cb + t * io.Ct + g * N + n]) : 0.f;
     }
     if (threadIdx.x < TT) ct[threadIdx.x] = (q0 + threadIdx.x < q1) ? crow[q0 + threadIdx.x] : 0.f;
 
@@ -143,12 +152,12 @@ chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T*
         for (int idx = threadIdx.x; idx < SB * N; idx += kThreads) {
             const int j = idx / (int)N, n = idx % (int)N;
             const int64_t s = s0 + j;
-            Bs[j * NP + n] = s < q1 ? to_f32(B[((b * Tlen + s) * G + g) * N + n]) : 0.f;
+            Bs[j * NP + n] = s < q1 ? to_f32(B[b * io.Bb + s * io.Bt + g * N + n]) : 0.f;
         }
         for (int idx = threadIdx.x; idx < SB * P; idx += kThreads) {
             const int j = idx / (int)P, pp = idx % (int)P;
             const int64_t s = s0 + j;
-            Xs[j * XP + pp] = s < q1 ? to_f32(x[((b * Tlen + s) * H + h) * P + pp]) : 0.f;
+            Xs[j * XP + pp] = s < q1 ? to_f32(x[b * io.xb + s * io.xt + h * P + pp]) : 0.f;
         }
         if (threadIdx.x < SB) {
             const int64_t s = s0 + threadIdx.x;
@@ -209,9 +218,8 @@ chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T*
         const int i = r0 + k * rs;
         const int64_t t = q0 + i;
         if (t >= q1) continue;
-        const int64_t off = ((b * Tlen + t) * H + h) * P + p;
-        const float v = acc[k] + ex2(ct[i]) * accs[k] + Dh * to_f32(x[off]);
-        y[off] = from_f32<T>(v);
+        const float v = acc[k] + ex2(ct[i]) * accs[k] + Dh * to_f32(x[b * io.xb + t * io.xt + h * P + p]);
+        y[b * io.yb + t * io.yt + h * P + p] = from_f32<T>(v);
     }
 }
 
@@ -231,11 +239,11 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
     if (d.dtype == 1)
         chunk_state_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B), cum2,
-            dtT, dS, d.T, d.H, d.P, d.N, d.G, d.L, d.nc);
+            dtT, dS, d.T, d.H, d.P, d.N, d.G, d.L, d.nc, io_strides(d));
     else
         chunk_state_simt_kernel<float><<<grid, kThreads, 0, st>>>(
             static_cast<const float*>(x), static_cast<const float*>(B), cum2, dtT, dS, d.T, d.H,
-            d.P, d.N, d.G, d.L, d.nc);
+            d.P, d.N, d.G, d.L, d.nc, io_strides(d));
     return cudaGetLastError();
 }
 
@@ -254,7 +262,7 @@ cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, c
             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
             static_cast<const __nv_bfloat16*>(C), cum2, dtT,
             static_cast<const __nv_bfloat16*>(Sprev), D, static_cast<__nv_bfloat16*>(y), d.T,
-            d.H, d.P, d.N, d.G, d.L, d.nc);
+            d.H, d.P, d.N, d.G, d.L, d.nc, io_strides(d));
     } else {
         auto k = chunk_out_simt_kernel<float>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -262,7 +270,7 @@ cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, c
         k<<<grid, kThreads, smem, st>>>(
             static_cast<const float*>(x), static_cast<const float*>(B),
             static_cast<const float*>(C), cum2, dtT, static_cast<const float*>(Sprev), D,
-            static_cast<float*>(y), d.T, d.H, d.P, d.N, d.G, d.L, d.nc);
+            static_cast<float*>(y), d.T, d.H, d.P, d.N, d.G, d.L, d.nc, io_strides(d));
     }
     return cudaGetLastError();
 }

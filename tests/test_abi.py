@@ -199,3 +199,35 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         m2.ssd_fwd(x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 16),
                    torch.zeros(1, 64, 1, 16), chunk_size=64)
+
+
+def test_fwd_strided_validates_strides_without_launching(lib):
+    s = shp()
+    b, T, H, P, N, G = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)       # aligned, never dereferenced: validation fails first
+    args = [good] * 9 + [good, ctypes.c_size_t(1 << 40), None]
+
+    def strides(**over):
+        st = m2.Strides()
+        st.x[:] = st.y[:] = (T * H * P, H * P)
+        st.B[:] = st.C[:] = (T * G * N, G * N)
+        st.dt[:] = (T * H, H)
+        for k, v in over.items():
+            getattr(st, k)[:] = v
+        return st
+
+    def call(st):
+        return lib.mamba2_ssd_fwd_strided(ctypes.byref(s), ctypes.byref(st) if st is not None else None,
+                                          *args)
+
+    assert call(None) == m2.ERR_INVALID_ARG
+    assert call(strides(x=(T * H * P, H * P - 1))) == m2.ERR_INVALID_ARG      # token overlap
+    assert call(strides(y=(T * H * P - 1, H * P))) == m2.ERR_INVALID_ARG      # batch overlap
+    assert call(strides(B=(T * G * N, 0))) == m2.ERR_INVALID_ARG
+    assert call(strides(dt=(T * H, -H))) == m2.ERR_INVALID_ARG
+    assert call(strides(C=(1 << 41, G * N))) == m2.ERR_INVALID_ARG           # beyond 2^40 elements
+    # valid strides, then a bad pointer: the pointer check still fails first
+    st = strides(x=(T * (H * P + 2 * G * N), H * P + 2 * G * N))
+    rc = lib.mamba2_ssd_fwd_strided(ctypes.byref(s), ctypes.byref(st), None, *args[1:])
+    assert rc == m2.ERR_INVALID_ARG

@@ -245,6 +245,53 @@ def test_overlapped_launches_match_serial(w):
         assert torch.equal(y0, y1) and torch.equal(f0, f1)
 
 
+STRIDED = [
+    wl(2, 640, 4, 64, 128, 1, 256, seed=51),                            # tensor-core shape
+    wl(1, 300, 4, 32, 32, 2, 64, dtype="f32", init=0.1, seed=52),       # CUDA-core shape
+]
+
+
+@pytest.mark.parametrize("pad", [0, 1], ids=["pitch16", "odd-pitch"])
+@pytest.mark.parametrize("w", STRIDED, ids=_ids(STRIDED))
+def test_strided_inputs_and_output(w, pad):
+    """x, B and C as column slices of one projection output [b, T, H*P + 2*G*N
+    (+1)], dt a slice of [b, T, H + 3] and y written into a wider buffer, through
+    mamba2_ssd_fwd_strided.  With row pitches that are multiples of 16 bytes the
+    same kernels run as for contiguous tensors and the outputs are equal bit for
+    bit; an odd pitch takes the CUDA-core kernels (the tensor-core kernels' copies
+    need 16-byte strides) and is checked against the oracle.  The padding of the
+    output buffer is left untouched."""
+    inp = W.make_inputs(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    b, T, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    HP, GN = H * P, G * N
+    xbc = torch.zeros((b, T, HP + 2 * GN + pad), dtype=w.torch_dtype, device="cuda")
+    xbc[..., :HP] = dev["x"].reshape(b, T, HP)
+    xbc[..., HP:HP + GN] = dev["B"].reshape(b, T, GN)
+    xbc[..., HP + GN:HP + 2 * GN] = dev["C"].reshape(b, T, GN)
+    x = xbc[..., :HP].view(b, T, H, P)
+    Bv = xbc[..., HP:HP + GN].view(b, T, G, N)
+    Cv = xbc[..., HP + GN:HP + 2 * GN].view(b, T, G, N)
+    dtb = torch.zeros((b, T, H + 3), dtype=torch.float32, device="cuda")
+    dtb[..., :H] = dev["dt"]
+    ypitch = HP + (1 if pad else 8)
+    yb = torch.full((b, T, ypitch), float("nan"), dtype=w.torch_dtype, device="cuda")
+    y = yb[..., :HP].view(b, T, H, P)
+    _, f1 = m2.ssd_fwd(x, dtb[..., :H], dev["A"], Bv, Cv, dev["D"], dev["initial_state"],
+                       chunk_size=w.chunk_size, ngroups=G, y=y)
+    torch.cuda.synchronize()
+    assert m2.device_error() == 0
+    assert torch.isnan(yb[..., HP:].float()).all()
+    y0, f0 = run_fwd(inp, w)
+    simt = m2.path(m2.make_shape(b, T, H, P, N, G, w.chunk_size, m2.BF16 if w.dtype == "bf16"
+                                 else m2.F32)) == m2.PATH_SIMT
+    if pad == 0 or simt:
+        assert torch.equal(y, y0) and torch.equal(f1, f0)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=G)
+    assert_close(to_np(y), yr, w.dtype, "strided y")
+    assert_close(to_np(f1), fr, w.dtype, "strided final_state")
+
+
 def test_chunk_size_independence():
     """The chunking is an evaluation order: L in {64, 128, 256} give the same result."""
     w = wl(1, 1024, 4, 64, 128, 1, 256, seed=31)
