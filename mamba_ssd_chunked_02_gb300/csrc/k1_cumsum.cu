@@ -10,9 +10,10 @@
 // cum2[b,h,t] = log2(e) * sum_{r = chunk start}^{t} dt[b,r,h] * A[h]   (inclusive)
 // dtT[b,h,t]  = dt[b,t,h]
 //
-// One CTA per (chunk, batch, block of 32 heads).  The [L x 32] dt tile is read
-// with coalesced 128-byte rows (32 heads of one token; 16-byte loads, all of a
-// thread's loads issued before any is stored), transposed into shared memory,
+// One CTA per (chunk, batch, block of 16 heads; more CTAs than with 32 hide
+// more of the load latency of this one-wave kernel).  The [L x 16] dt tile is
+// read with coalesced 64-byte rows (16 heads of one token; 16-byte loads, all of
+// a thread's loads issued before any is stored), transposed into shared memory,
 // scanned by one warp per head (each lane owns L/32 consecutive tokens; lane
 // totals are combined with a shuffle scan), and written back as coalesced
 // [h][t] rows.  The shared tile keeps one padding word per 32 tokens and an odd
@@ -26,7 +27,7 @@
 namespace m2 {
 namespace {
 
-constexpr int kHB = 32;        // heads per CTA
+constexpr int kHB = 16;        // heads per CTA
 constexpr int kThreads = 256;  // 8 warps
 
 // Token i of a head's row sits at i + i / 32; rows are `pitch` words apart.
@@ -58,18 +59,19 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
 
     // Load [nt x nh] (token-major in HBM) and transpose into tile[head][token].
     if (nh == kHB && (H & 3) == 0 && (stt & 3) == 0 && (sb & 3) == 0) {
-        // 8 float4 per token row; element (token i, quad q) of item idx = i * 8 + q.
+        // kHB/4 float4 per token row; element (token i, quad q) of item idx = i * kQ + q.
+        constexpr int kQ = kHB / 4;
         constexpr int kPer = L * kHB / 4 / kThreads;
         float4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int idx = threadIdx.x + kThreads * k, i = idx >> 3, q = idx & 7;
+            const int idx = threadIdx.x + kThreads * k, i = idx / kQ, q = idx % kQ;
             v[k] = i < nt ? __ldg(reinterpret_cast<const float4*>(src + (int64_t)i * stt) + q)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int idx = threadIdx.x + kThreads * k, i = idx >> 3, j = 4 * (idx & 7);
+            const int idx = threadIdx.x + kThreads * k, i = idx / kQ, j = 4 * (idx % kQ);
             tile[(j + 0) * kPitch + tpos(i)] = v[k].x;
             tile[(j + 1) * kPitch + tpos(i)] = v[k].y;
             tile[(j + 2) * kPitch + tpos(i)] = v[k].z;
