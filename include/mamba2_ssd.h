@@ -263,7 +263,12 @@ MAMBA2_API mamba2_status mamba2_ssd_chunk_out(const mamba2_ssd_shape* shape,
  *   state [b,H,P,N] fp32, read and written; x [b,H,P] (dtype); dt [b,H] fp32;
  *   A [H] fp32; B, C [b,G,N] (dtype); D [H] fp32 or NULL (= 0); y [b,H,P] (dtype).
  * Feeding the final_state of a prefix to this call token by token continues the
- * sequence (tested against mamba2_ssd_fwd over the whole sequence). */
+ * sequence (tested against mamba2_ssd_fwd over the whole sequence).
+ * Pointers are device memory, 16-byte aligned, owned by the caller; state must
+ * not overlap the other arrays.  Returns MAMBA2_OK once queued on `stream`,
+ * MAMBA2_ERR_INVALID_ARG for a bad shape or pointer.  For dstate 128 and 256 the
+ * kernel stages the state through shared memory behind a bounded wait; a wait
+ * that runs out sets MAMBA2_DEVERR_TIMEOUT_DECODE in the device error word. */
 MAMBA2_API mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float* state,
                                 const void* x, const float* dt, const float* A,
                                 const void* B, const void* C, const float* D,
@@ -276,6 +281,7 @@ MAMBA2_API mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float*
 #define MAMBA2_DEVERR_CHAIN 8                 /* the fused stage 2+3 kernel gave up waiting
                                                  for the previous chunk's state */
 #define MAMBA2_DEVERR_SELFTEST 16             /* mamba2_ssd_selftest_wait_timeout ran out */
+#define MAMBA2_DEVERR_TIMEOUT_DECODE 32       /* a wait ran out in the decode kernel */
 
 /* Device-side error word.  The tensor-core kernels bound every wait; a wait
  * that runs out sets a bit here and the kernel returns early (its outputs are

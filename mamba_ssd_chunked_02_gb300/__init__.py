@@ -345,6 +345,7 @@ def state_pass(shape, dS, cum2, initial_state, Sprev, final_state, stream=None):
 
 
 DEVERR_SELFTEST = 16
+DEVERR_TIMEOUT_DECODE = 32
 
 
 def ssd_decode(state, x, dt, A, B, C, D=None, *, y=None, stream=None):

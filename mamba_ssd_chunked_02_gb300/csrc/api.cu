@@ -398,7 +398,7 @@ mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float* state, con
     if (!req(state, empty) || !req(x, empty) || !req(dt, empty) || !req(A, empty) ||
         !req(B, empty) || !req(C, empty) || !opt(D) || !req(y, empty))
         return MAMBA2_ERR_INVALID_ARG;
-    return from_cuda(m2::launch_decode(d, state, x, dt, A, B, C, D, y,
+    return from_cuda(m2::launch_decode(d, state, x, dt, A, B, C, D, y, error_word(),
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -89,8 +89,10 @@ cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, con
                                 const uint32_t* xabs = nullptr, bool pdl = false);
 
 // One recurrent step per (b, h): S <- exp(dt A) S + dt x B^T in place, y = S C + D x.
+// A bounded wait that runs out sets kErrTimeoutDecode in *err.
 cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* dt, const float* A,
-                          const void* B, const void* C, const float* D, void* y, cudaStream_t st);
+                          const void* B, const void* C, const float* D, void* y, int32_t* err,
+                          cudaStream_t st);
 
 // Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);
@@ -105,6 +107,7 @@ enum : int32_t {
     kErrLaunchCfg = 1 << 2,    // a kernel saw a launch configuration it does not support
     kErrChainK23 = 1 << 3,     // the fused stage 2+3 kernel gave up waiting for the previous chunk
     kErrSelfTest = 1 << 4,     // the wait self-test's waits ran out (expected)
+    kErrTimeoutDecode = 1 << 5,  // a bounded wait ran out in the decode kernel
 };
 
 }  // namespace m2

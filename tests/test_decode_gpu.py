@@ -34,6 +34,9 @@ DECODE = [
     wl(1, 4, 128, 16, 2, seed=53),
     wl(2, 4, 16, 64, 4, dtype="f32", seed=54),
     wl(8, 80, 64, 128, 1, seed=55),            # the 2.7B layer's heads
+    wl(1, 3, 16, 128, 1, seed=57),             # staged: one CTA per head, 4 rows a warp
+    wl(2, 4, 128, 256, 2, dtype="f32", seed=58),   # staged: eight CTAs per head
+    wl(2, 2, 128, 128, 1, dtype="f32", seed=59),   # staged: four CTAs per head
 ]
 
 
@@ -45,6 +48,7 @@ def test_decode_step_matches_oracle(w):
     y = m2.ssd_decode(state, dev["x"][:, 0], dev["dt"][:, 0], dev["A"], dev["B"][:, 0],
                       dev["C"][:, 0], dev["D"])
     torch.cuda.synchronize()
+    assert m2.device_error() == 0
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
     assert_close(to_np(y), yr[:, 0], w.dtype, "decode y")
     rel, mx = assert_close(to_np(state), fr, "f32", "decode state")   # fp32 state
