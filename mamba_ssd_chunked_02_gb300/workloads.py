@@ -10,6 +10,10 @@ drawn in float32 and rounded to the run dtype; dt = exp(U(ln lo, ln hi)) per
 workload carries one, ~ N(0, 0.1^2) in float32.  A torch CPU generator is
 seeded per workload and the tensors are drawn in the fixed order
 x, B, C, dt, A, D, initial_state.
+
+For the backward pass, ``make_grads`` draws the incoming gradients from a
+second generator (seed + 500 000, so that the forward inputs stay the same):
+dy ~ N(0, 1) in the run dtype and, when asked for, dfinal ~ N(0, 1) in float32.
 """
 from __future__ import annotations
 
@@ -92,6 +96,20 @@ def make_inputs(w: Workload, device="cpu"):
     if w.init_std > 0:
         init = torch.randn((b, H, P, N), generator=g, dtype=torch.float32) * w.init_std
     out = dict(x=x, dt=dt, A=A, B=B, C=C, D=D, initial_state=init)
+    if device != "cpu":
+        out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
+    return out
+
+
+def make_grads(w: Workload, with_dfinal: bool = True, device="cpu"):
+    """Incoming gradients for the backward pass of workload ``w``: a dict with
+    dy [b,T,H,P] (dtype w.torch_dtype) and dfinal [b,H,P,N] float32 (or None)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + 500_000)
+    b, T, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    dy = torch.randn((b, T, H, P), generator=g, dtype=torch.float32).to(w.torch_dtype)
+    dfinal = torch.randn((b, H, P, N), generator=g, dtype=torch.float32) if with_dfinal else None
+    out = dict(dy=dy, dfinal=dfinal)
     if device != "cpu":
         out = {k: (v.to(device) if v is not None else None) for k, v in out.items()}
     return out

@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the Mamba-2 SSD forward pass (ctypes wrapper of ssd_oracle.c).
+"""fp64 CPU oracle for the Mamba-2 SSD forward and backward passes (ctypes wrapper
+of ssd_oracle.c).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's ``cpu_baseline`` / reference leg may import this package.  The CUDA
@@ -22,7 +23,9 @@ final_state [b,H,P,N]; cum2 [b,H,T]; dS and Sprev [b,nc,H,P,N].
 Parity pins (tests/test_oracle.py): brute force (quadratic form), chunk-size
 independence including L = 1 and L = T, the A = 0 causal-linear-attention
 closed form, the impulse response, dt = 0, the scalar geometric-series closed
-form, linearity, group mapping and split-and-resume.
+form, linearity, group mapping and split-and-resume.  The backward pass
+(``ssd_backward``) is pinned by finite differences of the forward oracle and
+by the homogeneity identities of the loss (tests/test_oracle_bwd.py).
 """
 from __future__ import annotations
 
@@ -64,6 +67,8 @@ def _bind(path):
     lib.oracle_ssd_chunked.restype = ctypes.c_int
     lib.oracle_ssd_quadratic.argtypes = [i64] * 6 + [vp] * 7 + [vp, vp]
     lib.oracle_ssd_quadratic.restype = ctypes.c_int
+    lib.oracle_ssd_backward.argtypes = [i64] * 6 + [vp] * 9 + [vp, i64] + [vp] * 7 + [ctypes.c_int]
+    lib.oracle_ssd_backward.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -172,3 +177,35 @@ def ssd_quadratic(x, dt, A, B, C, D=None, initial_state=None, ngroups=1, lib=Non
     if rc != 0:
         raise ValueError("oracle_ssd_quadratic: invalid arguments")
     return y, fin
+
+
+def ssd_backward(x, dt, A, B, C, D=None, initial_state=None, dy=None, dfinal=None, ngroups=1,
+                 pairs=None, nthreads=0, lib=None):
+    """Gradients of L = sum(dy * y) + sum(dfinal * final_state) by reverse-mode
+    differentiation of the recurrence (the chain rule on the definition; the
+    pages give no backward method).  Returns a dict of float64 arrays:
+    dx [b,T,H,P], ddt [b,T,H], dA [H], dB and dC [b,T,G,N], dD [H],
+    dinit [b,H,P,N].  ``pairs``: optional (b, h) pairs; dx, ddt and dinit of
+    other pairs are NaN and dA, dD, dB, dC sum the listed pairs only.
+    """
+    lib = lib or _load()
+    x, dt, A, B, C, D, S0, dy, dfinal = map(_f32, (x, dt, A, B, C, D, initial_state, dy, dfinal))
+    b, T, H, P, N = _dims(x, B, ngroups)
+    if dy is None or dy.shape != x.shape:
+        raise ValueError("ssd_backward: dy must have x's shape")
+    out = dict(dx=np.full((b, T, H, P), np.nan), ddt=np.full((b, T, H), np.nan),
+               dA=np.empty(H), dB=np.empty((b, T, ngroups, N)), dC=np.empty((b, T, ngroups, N)),
+               dD=np.empty(H), dinit=np.full((b, H, P, N), np.nan))
+    pr = None
+    npairs = 0
+    if pairs is not None:
+        pr = np.ascontiguousarray(np.asarray(list(pairs), dtype=np.int64).reshape(-1, 2))
+        npairs = pr.shape[0]
+    rc = lib.oracle_ssd_backward(b, T, H, P, N, ngroups, _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                 _ptr(C), _ptr(D), _ptr(S0), _ptr(dy), _ptr(dfinal), _ptr(pr),
+                                 npairs, _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]),
+                                 _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                 _ptr(out["dinit"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_ssd_backward: invalid arguments")
+    return out

@@ -36,6 +36,14 @@
  *                            before exponentiation [P3 sections 9, 11].
  *   oracle_ssd_quadratic  -- brute force "attention" view: every decay is the
  *                            explicit sum of a_r between the two tokens.
+ *   oracle_ssd_backward   -- gradients of the recurrence: reverse-mode
+ *                            differentiation of the token-by-token definition,
+ *                            step by step in reverse order.  The pages give no
+ *                            method for the backward pass; they only note that
+ *                            end-to-end training speed also depends on it [P1
+ *                            "開発現場への影響と未確認事項"; P2 "성능 벤치마크
+ *                            결과 및 활용"].  This is the chain rule applied to
+ *                            the definition above.
  *
  * Inputs are float (the exact values the GPU sees: bf16 and fp32 both widen
  * to float exactly); every operation is done in double.
@@ -307,4 +315,164 @@ int oracle_ssd_quadratic(int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N,
         }
     }
     return 0;
+}
+
+/*
+ * Backward pass of the recurrence (reverse-mode, the chain rule on the
+ * definition).  For a scalar loss with dL/dy = dy [b,T,H,P] and
+ * dL/dfinal_state = dfin [b,H,P,N] (NULL = 0), per (b,h), with
+ * G = dL/dS_t accumulated from the end:
+ *     G <- dfin
+ *     for t = T-1 .. 0:
+ *         G        += dy_t C_t^T                       (read-out of S_t)
+ *         dC_t     += S_t^T dy_t                       (summed over the group's heads)
+ *         dx_t      = dt_t G B_t + D dy_t
+ *         dB_t     += dt_t G^T x_t                     (summed over the group's heads)
+ *         ddt_t     = x_t^T G B_t + A e_t <G, S_{t-1}>   (e_t = exp(dt_t A))
+ *         dA       += dt_t e_t <G, S_{t-1}>
+ *         dD       += dy_t . x_t
+ *         G        <- e_t G                            (dL/dS_{t-1})
+ *     dinit = G
+ * The states S_t are taken from a forward sweep: every K-th state is kept
+ * (K ~ sqrt(T)) and the K states of a segment are recomputed from it with the
+ * same operations in the same order, so they are the forward sweep's values.
+ *
+ * `pairs` (2*npairs int64, or NULL = all) restricts the (b,h) pairs; dx, ddt,
+ * dinit of other pairs are left untouched and dA, dD, dB, dC then sum the
+ * listed pairs only.  Outputs are fully written (dA, dD, dB, dC zeroed first).
+ */
+int oracle_ssd_backward(int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, int64_t G,
+                        const float* x, const float* dt, const float* A, const float* B,
+                        const float* C, const float* D, const float* init, const float* dy,
+                        const float* dfin, const int64_t* pairs, int64_t npairs,
+                        double* dx, double* ddt, double* dA, double* dB, double* dC,
+                        double* dD, double* dinit, int nthreads) {
+    if (!shape_ok(Bt, T, H, P, N, G)) return -1;
+    if (!x || !dt || !A || !B || !C || !dy || !dx || !ddt || !dA || !dB || !dC || !dD || !dinit)
+        return -1;
+    const int64_t hpg = H / G, PN = P * N;
+    const int64_t total = pairs ? npairs : Bt * H;
+    int64_t K = 1;
+    while (K * K < T) ++K;
+    const int64_t nseg = (T + K - 1) / K;
+    /* Per-pair contributions to the group and head sums, reduced afterwards in a
+     * fixed order. */
+    double* pdB = (double*)calloc((size_t)(total * T * N), sizeof(double));
+    double* pdC = (double*)calloc((size_t)(total * T * N), sizeof(double));
+    double* pdA = (double*)calloc((size_t)(total > 0 ? total : 1), sizeof(double));
+    double* pdD = (double*)calloc((size_t)(total > 0 ? total : 1), sizeof(double));
+    if ((total > 0 && (!pdB || !pdC)) || !pdA || !pdD) { free(pdB); free(pdC); free(pdA); free(pdD); return -1; }
+    set_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t i = 0; i < total; ++i) {
+        const int64_t b = pairs ? pairs[2 * i] : i / H;
+        const int64_t h = pairs ? pairs[2 * i + 1] : i % H;
+        if (b < 0 || b >= Bt || h < 0 || h >= H) { bad |= 1; continue; }
+        const int64_t g = h / hpg;
+        const double Ah = (double)A[h];
+        const double Dh = D ? (double)D[h] : 0.0;
+        double* ck = (double*)malloc((size_t)(nseg * PN) * sizeof(double));   /* S_{sK-1} */
+        double* seg = (double*)malloc((size_t)((K + 1) * PN) * sizeof(double));
+        double* Gs = (double*)malloc((size_t)PN * sizeof(double));
+        if (!ck || !seg || !Gs) { bad |= 1; free(ck); free(seg); free(Gs); continue; }
+        /* Forward sweep, keeping the state entering every segment. */
+        double* S = seg;
+        for (int64_t k = 0; k < PN; ++k) S[k] = init ? (double)init[(b * H + h) * PN + k] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            if (t % K == 0) memcpy(ck + (t / K) * PN, S, (size_t)PN * sizeof(double));
+            const double dtv = (double)dt[(b * T + t) * H + h];
+            const double e = exp(dtv * Ah);
+            const float* xt = x + ((b * T + t) * H + h) * P;
+            const float* Bt_ = B + ((b * T + t) * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                const double u = dtv * (double)xt[p];
+                for (int64_t n = 0; n < N; ++n) S[p * N + n] = e * S[p * N + n] + u * (double)Bt_[n];
+            }
+        }
+        for (int64_t k = 0; k < PN; ++k) Gs[k] = dfin ? (double)dfin[(b * H + h) * PN + k] : 0.0;
+        double sA = 0.0, sD = 0.0;
+        double* qB = pdB + i * T * N;
+        double* qC = pdC + i * T * N;
+        for (int64_t sg = nseg - 1; sg >= 0; --sg) {
+            const int64_t t0 = sg * K, t1 = (sg + 1) * K < T ? (sg + 1) * K : T;
+            /* seg[j] = S_{t0+j-1}, j = 0 .. t1-t0 (recomputed as in the sweep). */
+            memcpy(seg, ck + sg * PN, (size_t)PN * sizeof(double));
+            for (int64_t t = t0; t < t1; ++t) {
+                const double dtv = (double)dt[(b * T + t) * H + h];
+                const double e = exp(dtv * Ah);
+                const float* xt = x + ((b * T + t) * H + h) * P;
+                const float* Bt_ = B + ((b * T + t) * G + g) * N;
+                const double* Sa = seg + (t - t0) * PN;
+                double* Sb = seg + (t - t0 + 1) * PN;
+                for (int64_t p = 0; p < P; ++p) {
+                    const double u = dtv * (double)xt[p];
+                    for (int64_t n = 0; n < N; ++n) Sb[p * N + n] = e * Sa[p * N + n] + u * (double)Bt_[n];
+                }
+            }
+            for (int64_t t = t1 - 1; t >= t0; --t) {
+                const double dtv = (double)dt[(b * T + t) * H + h];
+                const double e = exp(dtv * Ah);
+                const float* xt = x + ((b * T + t) * H + h) * P;
+                const float* dyt = dy + ((b * T + t) * H + h) * P;
+                const float* Bt_ = B + ((b * T + t) * G + g) * N;
+                const float* Ct = C + ((b * T + t) * G + g) * N;
+                const double* Sprev = seg + (t - t0) * PN;   /* S_{t-1} */
+                const double* Scur = seg + (t - t0 + 1) * PN; /* S_t */
+                /* G += dy_t C_t^T */
+                for (int64_t p = 0; p < P; ++p)
+                    for (int64_t n = 0; n < N; ++n) Gs[p * N + n] += (double)dyt[p] * (double)Ct[n];
+                /* dC_t += S_t^T dy_t ; dB_t += dt_t G^T x_t */
+                for (int64_t n = 0; n < N; ++n) {
+                    double ac = 0.0, ab = 0.0;
+                    for (int64_t p = 0; p < P; ++p) {
+                        ac += Scur[p * N + n] * (double)dyt[p];
+                        ab += Gs[p * N + n] * (double)xt[p];
+                    }
+                    qC[t * N + n] += ac;
+                    qB[t * N + n] += dtv * ab;
+                }
+                /* dx_t = dt_t G B_t + D dy_t ; x^T G B */
+                double xgb = 0.0;
+                for (int64_t p = 0; p < P; ++p) {
+                    double gb = 0.0;
+                    for (int64_t n = 0; n < N; ++n) gb += Gs[p * N + n] * (double)Bt_[n];
+                    dx[((b * T + t) * H + h) * P + p] = dtv * gb + Dh * (double)dyt[p];
+                    xgb += (double)xt[p] * gb;
+                }
+                /* <G, S_{t-1}> */
+                double gs = 0.0;
+                for (int64_t k = 0; k < PN; ++k) gs += Gs[k] * Sprev[k];
+                ddt[(b * T + t) * H + h] = xgb + Ah * e * gs;
+                sA += dtv * e * gs;
+                double yx = 0.0;
+                for (int64_t p = 0; p < P; ++p) yx += (double)dyt[p] * (double)xt[p];
+                sD += yx;
+                /* G <- e_t G */
+                for (int64_t k = 0; k < PN; ++k) Gs[k] *= e;
+            }
+        }
+        memcpy(dinit + (b * H + h) * PN, Gs, (size_t)PN * sizeof(double));
+        pdA[i] = sA;
+        pdD[i] = sD;
+        free(ck); free(seg); free(Gs);
+    }
+    if (!bad) {
+        for (int64_t k = 0; k < H; ++k) { dA[k] = 0.0; dD[k] = 0.0; }
+        for (int64_t k = 0; k < Bt * T * G * N; ++k) { dB[k] = 0.0; dC[k] = 0.0; }
+        for (int64_t i = 0; i < total; ++i) {
+            const int64_t b = pairs ? pairs[2 * i] : i / H;
+            const int64_t h = pairs ? pairs[2 * i + 1] : i % H;
+            const int64_t g = h / hpg;
+            dA[h] += pdA[i];
+            dD[h] += pdD[i];
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t n = 0; n < N; ++n) {
+                    dB[((b * T + t) * G + g) * N + n] += pdB[(i * T + t) * N + n];
+                    dC[((b * T + t) * G + g) * N + n] += pdC[(i * T + t) * N + n];
+                }
+        }
+    }
+    free(pdB); free(pdC); free(pdA); free(pdD);
+    return bad ? -1 : 0;
 }
