@@ -386,8 +386,8 @@ int oracle_ssd_backward(int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, 
             const float* xt = x + ((b * T + t) * H + h) * P;
             const float* Bt_ = B + ((b * T + t) * G + g) * N;
             for (int64_t p = 0; p < P; ++p) {
-                const double u = dtv * (double)xt[p];
-                for (int64_t n = 0; n < N; ++n) S[p * N + n] = e * S[p * N + n] + u * (double)Bt_[n];
+                const double in = dtv * (double)xt[p];
+                for (int64_t n = 0; n < N; ++n) S[p * N + n] = e * S[p * N + n] + in * (double)Bt_[n];
             }
         }
         for (int64_t k = 0; k < PN; ++k) Gs[k] = dfin ? (double)dfin[(b * H + h) * PN + k] : 0.0;
@@ -406,8 +406,8 @@ int oracle_ssd_backward(int64_t Bt, int64_t T, int64_t H, int64_t P, int64_t N, 
                 const double* Sa = seg + (t - t0) * PN;
                 double* Sb = seg + (t - t0 + 1) * PN;
                 for (int64_t p = 0; p < P; ++p) {
-                    const double u = dtv * (double)xt[p];
-                    for (int64_t n = 0; n < N; ++n) Sb[p * N + n] = e * Sa[p * N + n] + u * (double)Bt_[n];
+                    const double in = dtv * (double)xt[p];
+                    for (int64_t n = 0; n < N; ++n) Sb[p * N + n] = e * Sa[p * N + n] + in * (double)Bt_[n];
                 }
             }
             for (int64_t t = t1 - 1; t >= t0; --t) {
