@@ -63,6 +63,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time the single-token decode step on the workload's state instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (mamba2_ssd_bwd) on the workload instead")
     ap.add_argument("--fused-state", action="store_true",
                     help="time stages 2+3 as the one fused kernel (mamba2_ssd_chunk_state_pass)")
     ap.add_argument("--batch", type=int, default=0,
@@ -353,6 +355,73 @@ def run_decode(args, w):
         "gpu_launches": K, "clocks": clk}), flush=True)
 
 
+def bwd_flops(w):
+    """Contraction work of one backward call as the kernels do it (causal halves of
+    the L x L products, forward recompute of the chunk states included):
+    per (b, chunk, head) 3 L^2 P (dy.x^T twice, M^T dy) + 12 L P N (chunk adjoint,
+    Gn B, Sprev C, the two carried-state parts of dB and dC, the recomputed chunk
+    state); per (b, chunk, group) 3 L^2 N (C B^T and the two head-summed dCB
+    products)."""
+    b, T, H, P, N, G, L = (w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                           w.chunk_size)
+    nc = -(-T // L)
+    return b * nc * (H * (3 * L * L * P + 12 * L * P * N) + G * 3 * L * L * N)
+
+
+def run_backward(args, w):
+    """Backward pass (mamba2_ssd_bwd) on the workload, inputs and incoming gradients
+    resident in HBM; CUDA-core fp32 kernels, so the roofline is the fp32 FMA rate."""
+    import torch
+    import mamba_ssd_chunked_02_gb300 as m2
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+    inp = W.make_inputs(w)
+    gr = W.make_grads(w)
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    dy, dfin = gr["dy"].cuda(), gr["dfinal"].cuda()
+    sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+    ws = torch.empty(m2.bwd_workspace_size(sh), dtype=torch.uint8, device="cuda")
+    grads = None
+
+    def step():
+        nonlocal grads
+        grads = m2.ssd_bwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                           dev["initial_state"], dy, dfin, chunk_size=w.chunk_size,
+                           ngroups=w.ngroups, grads=grads, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    a.record(stream)
+    for _ in range(K):
+        step()
+    z.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(wall0, time.time())
+    if m2.device_error() != 0:
+        raise RuntimeError("device-side error in the backward loop")
+    ms = a.elapsed_time(z) / K
+    F = bwd_flops(w)
+    tf = F / (ms * 1e-3) / 1e12
+    # fp32 FMA peak from unit counts and clock: 152 SMs x 128 lanes x 2 flop x f_max.
+    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    print(json.dumps({
+        "metric": "SSD backward: tokens/s", "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32 (bf16 inputs)" if w.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": dict(config_of(w, 1), what="backward, forward recompute included"),
+        "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf / peak, "traffic": None, "kernel": "whole backward",
+                     "algorithmic_flops": F},
+        "gpu_launches": 8 * K, "clocks": clk}), flush=True)
+
+
 def main():
     args = parse_args()
     w = workload(args.workload)
@@ -375,6 +444,10 @@ def main():
     if args.decode:
         if rank == 0:
             run_decode(args, w)
+        return
+    if args.backward:
+        if rank == 0:
+            run_backward(args, w)
         return
     dist = None
     if world > 1:

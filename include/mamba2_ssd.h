@@ -274,6 +274,42 @@ MAMBA2_API mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float*
                                 const void* B, const void* C, const float* D,
                                 void* y, void* stream);
 
+/* Backward pass: gradients of a scalar loss given dL/dy and dL/dfinal_state.
+ *
+ * The pages give no backward method; they only note that end-to-end training
+ * speed also depends on one [P1 "開発現場への影響と未確認事項"; P2 "성능 벤치마크 결과
+ * 및 활용"].  This call computes the chain rule applied to the same chunked
+ * forward [P3 sections 4, 5, 8, 9], which equals the gradient of the
+ * token-by-token recurrence of mamba2_ssd_fwd (tested against an fp64 reverse
+ * sweep of the recurrence).  It recomputes the forward's chunk states itself,
+ * so it takes the forward's inputs, not its outputs.
+ *
+ * shape: as for mamba2_ssd_fwd; flags 0 or MAMBA2_FLAG_FORCE_SIMT (the forward
+ *   recompute on CUDA cores); headdim <= 128.
+ * Inputs (device, 16-byte aligned, caller-owned, read only): x, dt, A, B, C, D
+ *   (or NULL = 0), initial_state (or NULL = 0) in the layouts and types of
+ *   mamba2_ssd_fwd; dy [b,T,H,P] in x's type; dfinal_state [b,H,P,N] fp32 or
+ *   NULL (= 0).
+ * Outputs (device, 16-byte aligned, fp32 whatever the input type, fully written):
+ *   dx [b,T,H,P], ddt [b,T,H], dA [H], dB and dC [b,T,G,N] (summed over the
+ *   heads of each group), dD [H] (required when D is given, else may be NULL),
+ *   dinitial_state [b,H,P,N] (NULL when not wanted).
+ * workspace: mamba2_ssd_bwd_workspace_size(shape) bytes, 256-byte aligned.
+ * Asynchronous on `stream`; argument errors are returned before any launch
+ * (MAMBA2_ERR_INVALID_ARG, MAMBA2_ERR_UNSUPPORTED, MAMBA2_ERR_WORKSPACE);
+ * MAMBA2_ERR_CUDA for a failed launch.  dA and dD are accumulated with atomic
+ * adds across chunks, so their last bits may vary from run to run. */
+MAMBA2_API size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape);
+MAMBA2_API mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape,
+                                        const void* x, const float* dt, const float* A,
+                                        const void* B, const void* C, const float* D,
+                                        const float* initial_state, const void* dy,
+                                        const float* dfinal_state,
+                                        float* dx, float* ddt, float* dA, float* dB,
+                                        float* dC, float* dD, float* dinitial_state,
+                                        void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
 /* Bits of the device-side error word. */
 #define MAMBA2_DEVERR_TIMEOUT_CHUNK_STATE 1   /* a wait ran out in the stage-2 kernel */
 #define MAMBA2_DEVERR_TIMEOUT_CHUNK_OUT 2     /* ... in the stage-4 kernel */

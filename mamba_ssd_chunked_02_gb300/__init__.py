@@ -43,7 +43,7 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
            "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
            "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode", "mamba2_ssd_fwd_timed",
-           "mamba2_ssd_fwd_strided")
+           "mamba2_ssd_fwd_strided", "mamba2_ssd_bwd", "mamba2_ssd_bwd_workspace_size")
 
 
 class Shape(ctypes.Structure):
@@ -124,6 +124,10 @@ def load():
         lib.mamba2_ssd_fwd_timed.argtypes = [sp] + [vp] * 9 + [vp, ctypes.c_size_t, vp,
                                                                 ctypes.POINTER(vp)]
         lib.mamba2_ssd_fwd_timed.restype = ctypes.c_int
+        lib.mamba2_ssd_bwd_workspace_size.argtypes = [sp]
+        lib.mamba2_ssd_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.mamba2_ssd_bwd.argtypes = [sp] + [vp] * 16 + [vp, ctypes.c_size_t, vp]
+        lib.mamba2_ssd_bwd.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -413,6 +417,50 @@ def chunk_out(shape, x, B, C, cum2, dtT, Sprev, D, y, stream=None):
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def bwd_workspace_size(shape: Shape) -> int:
+    return int(load().mamba2_ssd_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def ssd_bwd(x, dt, A, B, C, D=None, initial_state=None, dy=None, dfinal=None, chunk_size=256,
+            ngroups=None, *, grads=None, workspace=None, stream=None, flags=0):
+    """Backward pass (mamba2_ssd_bwd): gradients of a loss with dL/dy = dy and
+    dL/dfinal_state = dfinal (None = 0), for the inputs of ssd_fwd.  Returns a
+    dict of fp32 tensors dx [b,T,H,P], ddt [b,T,H], dA [H], dB, dC [b,T,G,N],
+    dD [H] (None when D is None) and dinit [b,H,P,N] (None when initial_state
+    is None).  `grads`: an optional dict of preallocated outputs (same keys)."""
+    lib = load()
+    sh = shape_of(x, B, chunk_size, ngroups, flags)
+    b, T, H, P, N, G = sh.batch, sh.seqlen, sh.nheads, sh.headdim, sh.dstate, sh.ngroups
+    io = _io_dtype(sh)
+    dev = x.device
+    f32 = torch.float32
+    shapes = dict(dx=(b, T, H, P), ddt=(b, T, H), dA=(H,), dB=(b, T, G, N), dC=(b, T, G, N),
+                  dD=(H,), dinit=(b, H, P, N))
+    g = dict(grads or {})
+    for k, shp in shapes.items():
+        if k == "dD" and D is None:
+            g.setdefault(k, None)
+        elif k == "dinit" and initial_state is None:
+            g.setdefault(k, None)
+        elif g.get(k) is None:
+            g[k] = torch.empty(shp, dtype=f32, device=dev)
+    need = bwd_workspace_size(sh)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check("mamba2_ssd_bwd", lib.mamba2_ssd_bwd(
+        ctypes.byref(sh), _ptr(x, "x", io, (b, T, H, P)), _ptr(dt, "dt", f32, (b, T, H)),
+        _ptr(A, "A", f32, (H,)), _ptr(B, "B", io, (b, T, G, N)), _ptr(C, "C", io, (b, T, G, N)),
+        _ptr(D, "D", f32, (H,), optional=True),
+        _ptr(initial_state, "initial_state", f32, (b, H, P, N), optional=True),
+        _ptr(dy, "dy", io, (b, T, H, P)),
+        _ptr(dfinal, "dfinal", f32, (b, H, P, N), optional=True),
+        *[_ptr(g[k], k, f32, shapes[k], optional=k in ("dD", "dinit")) for k in shapes],
+        _ptr(workspace, "workspace", optional=True),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
+        _stream(stream)))
+    return g
 
 
 def ssd_fwd_noalloc(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=None,

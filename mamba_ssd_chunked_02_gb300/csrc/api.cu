@@ -129,6 +129,28 @@ Carve carve(const Dims& d) {
     return c;
 }
 
+// Workspace of the backward pass: the forward's cum2, dtT, dS (fp32; reused
+// for the chunk adjoints dSout / Gn), an fp32 Sprev, C.B^T and the head-summed
+// dCB per (b, chunk, group), and a final-state scratch.
+struct BwdCarve {
+    size_t cum2, dtT, dS, Sprev, CB, SdCB, fin, total;
+};
+
+BwdCarve bwd_carve(const Dims& d) {
+    BwdCarve c;
+    const size_t st = align256(sizeof(float) * (size_t)m2::n_state(d));
+    const size_t tile = align256(sizeof(float) * (size_t)(d.b * d.nc * d.G * d.L * d.L));
+    c.cum2 = 0;
+    c.dtT = c.cum2 + align256(sizeof(float) * (size_t)m2::n_cum(d));
+    c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
+    c.Sprev = c.dS + st;
+    c.CB = c.Sprev + st;
+    c.SdCB = c.CB + tile;
+    c.fin = c.SdCB + tile;
+    c.total = c.fin + align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
+    return c;
+}
+
 mamba2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MAMBA2_OK : MAMBA2_ERR_CUDA; }
 
 // A required pointer: non-null and 16-byte aligned, unless the tensor is empty.
@@ -369,6 +391,71 @@ mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x,
                                    void* const* events) {
     return fwd_impl(shape, x, dt, A, B, C, D, initial_state, y, final_state, workspace,
                     workspace_bytes, stream, events);
+}
+
+size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape) {
+    if (check(shape) != MAMBA2_OK) return 0;
+    return bwd_carve(dims_of(shape)).total;
+}
+
+mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
+                             const float* A, const void* B, const void* C, const float* D,
+                             const float* initial_state, const void* dy,
+                             const float* dfinal_state, float* dx, float* ddt, float* dA,
+                             float* dB, float* dC, float* dD, float* dinitial_state,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    if (shape->flags & ~MAMBA2_FLAG_FORCE_SIMT) return MAMBA2_ERR_INVALID_ARG;
+    const Dims d = dims_of(shape);
+    const bool empty = d.b * d.T * d.H == 0;
+    const bool nostate = d.b * d.H == 0;
+    if (!req(x, empty) || !req(dt, empty) || !req(A, d.H == 0) || !req(B, empty) ||
+        !req(C, empty) || !opt(D) || !opt(initial_state) || !req(dy, empty) ||
+        !opt(dfinal_state) || !req(dx, empty) || !req(ddt, empty) || !req(dA, d.H == 0) ||
+        !req(dB, empty) || !req(dC, empty) || !opt(dD) || !opt(dinitial_state))
+        return MAMBA2_ERR_INVALID_ARG;
+    if (D && !dD) return MAMBA2_ERR_INVALID_ARG;
+    if (d.L > 256 || d.P > 128) return MAMBA2_ERR_UNSUPPORTED;
+    const BwdCarve cv = bwd_carve(d);
+    if (!empty && (!workspace || workspace_bytes < cv.total ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return MAMBA2_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (d.H > 0) e = cudaMemsetAsync(dA, 0, sizeof(float) * (size_t)d.H, s);
+    if (e == cudaSuccess && dD && d.H > 0) e = cudaMemsetAsync(dD, 0, sizeof(float) * (size_t)d.H, s);
+    if (e != cudaSuccess || nostate) return from_cuda(e);
+    const size_t sbytes = sizeof(float) * (size_t)(d.b * d.H * d.P * d.N);
+    if (d.T == 0) {   // dinitial_state = dfinal_state (or 0)
+        if (!dinitial_state) return MAMBA2_OK;
+        return from_cuda(dfinal_state ? cudaMemcpyAsync(dinitial_state, dfinal_state, sbytes,
+                                                        cudaMemcpyDeviceToDevice, s)
+                                      : cudaMemsetAsync(dinitial_state, 0, sbytes, s));
+    }
+    char* ws = static_cast<char*>(workspace);
+    float* cum2 = reinterpret_cast<float*>(ws + cv.cum2);
+    float* dtT = reinterpret_cast<float*>(ws + cv.dtT);
+    float* dS = reinterpret_cast<float*>(ws + cv.dS);
+    float* Sprev = reinterpret_cast<float*>(ws + cv.Sprev);
+    int32_t* err = error_word();
+    // Forward stages 1-3: cum2, dtT, dS (fp32) and the fp32 state entering each chunk.
+    const bool tc = use_tc(shape, d);
+    e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+    if (e == cudaSuccess)
+        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, false, err, s)
+               : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
+    Dims d32 = d;
+    d32.dtype = 0;   // Sprev in fp32
+    if (e == cudaSuccess)
+        e = m2::launch_state_pass(d32, dS, false, cum2, initial_state, Sprev,
+                                  reinterpret_cast<float*>(ws + cv.fin), err, s);
+    if (e == cudaSuccess)
+        e = m2::launch_backward(d, x, B, C, dy, A, D, cum2, dtT, Sprev, dS,
+                                reinterpret_cast<float*>(ws + cv.CB),
+                                reinterpret_cast<float*>(ws + cv.SdCB), dfinal_state, dx, ddt, dA,
+                                dB, dC, dD, dinitial_state, s);
+    return from_cuda(e);
 }
 
 mamba2_status mamba2_ssd_device_error(int32_t* code, int32_t clear) {

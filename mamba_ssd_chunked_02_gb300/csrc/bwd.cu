@@ -1,0 +1,670 @@
+// bwd.cu -- backward pass of the SSD in the chunked form (CUDA cores, fp32).
+//
+// The pages give no backward method; they only note that end-to-end training
+// speed also depends on one ("NVIDIA、cuTileでMamba-2フォワードパスを高速化"
+// (ai.newsbites.today), "開発現場への影響と未確認事項"; "NVIDIA CUDA Tile로 Mamba-2
+// 순방향 전달 커널 가속화" (devin.kr), "성능 벤치마크 결과 및 활용").  What is
+// computed here is the chain rule applied to the chunked forward of the same
+// pages ("Accelerating Mamba-2 with High-Performance Forward Pass Kernels in
+// NVIDIA CUDA Tile" (brifing.si), sections 4, 5, 8 and 9), so that it equals
+// the gradient of the token-by-token recurrence.
+//
+// Notation for one (b, h) and chunk c with Lc tokens i, j (chunk-local), the
+// forward's log2-scaled chunk-local cumsum c2_i, e_i = exp2(c2_i), the chunk
+// decay E = exp2(c2_last), w_j = dt_j exp2(c2_last - c2_j), the state entering
+// the chunk Sprev (P x N) and the adjoint of the state leaving it Gn (P x N):
+//
+//   forward:  y_i = sum_{j<=i} CB_ij exp2(c2_i - c2_j) dt_j x_j + e_i Sprev C_i + D x_i
+//             S_next = E Sprev + sum_j w_j x_j B_j^T
+//   adjoint of the state entering chunk c (reverse pass over chunks):
+//             dSprev_c = sum_i e_i dy_i C_i^T + E_c dSprev_{c+1},  dSprev_nc = dfinal
+//             Gn_c = dSprev_{c+1},  dinitial_state = dSprev_0
+//   with DX_ij = dy_i . x_j and Q_ij = CB_ij exp2(c2_i - c2_j) DX_ij (j <= i):
+//     dx_j   = sum_{i>=j} CB_ij exp2(c2_i - c2_j) dt_j dy_i + w_j Gn B_j + D dy_j
+//     ddt_j  = sum_i Q_ij + exp2(c2_last - c2_j) x_j.(Gn B_j) + A sum_{i>=j} dcum_i
+//     dcum_i = sum_j Q_ij dt_j - dt_i sum_k Q_ki + e_i dy_i.(Sprev C_i) - w_i x_i.(Gn B_i)
+//              + [i = last] (sum_j w_j x_j.(Gn B_j) + E <Gn, Sprev>)
+//     dA     = sum over (b, chunks, j) of dt_j sum_{i>=j} dcum_i
+//     dD     = sum over (b, t) of dy . x
+//   and, summed over the heads of the group (dCB_ij = exp2(c2_i - c2_j) dt_j DX_ij):
+//     dC_i   = sum_{j<=i} (sum_h dCB_ij) B_j + sum_h e_i Sprev^T dy_i
+//     dB_j   = sum_{i>=j} (sum_h dCB_ij) C_i + sum_h w_j Gn^T x_j
+// (dcum is the gradient with respect to the natural-log cumsum; cum_t = A sum dt.)
+//
+// Kernels (after the forward's stages 1-3 recompute cum2, dtT and an fp32 Sprev):
+//   bwd_chunk_adjoint   sum_i e_i dy_i C_i^T per (b, c, h)            -> dSout
+//   bwd_state_pass_rev  reverse pass over chunks, in place            -> Gn, dinit
+//   bwd_pair_tiles      per (b, c, g) and 64x64 tile pair (j <= i): CB and
+//                       sum_h dCB (the head loop inside the CTA)       -> CB, SdCB
+//   bwd_head            per (b, c, h): dx, ddt, and dA, dD partial sums
+//   bwd_group_bc        per (b, c, g), 64-token tile, 64-column tile: dC or dB,
+//                       one GEMM over the chunk's tokens and one over (head, p)
+// Every contraction goes through mm_tile, a 64x64 fp32 tile on 256 threads
+// (4x4 outputs each) with operands staged through shared memory 16 k at a time.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace m2 {
+namespace {
+
+constexpr int kT = 64;         // tile edge (tokens, p, n)
+constexpr int kK = 16;         // k per shared-memory stage
+constexpr int kThreads = 256;  // 16 x 16 threads, 4 x 4 outputs each
+
+struct MMSmem {
+    float a[kK][kT + 4];
+    float b[kK][kT + 4];
+};
+
+// acc[r][q] += sum_{k in [k0, k1)} A(4 ty + r, k) * B(k, 4 tx + q), with
+// ty = threadIdx.x / 16, tx = threadIdx.x % 16.  fa(m, k) / fb(k, n) return the
+// operand elements (0 outside the operand); AK / BK: the operand is contiguous
+// in memory along k (else along m / n), which sets the load order so that
+// neighbouring threads read neighbouring addresses.  Every thread of the block
+// must call it (it synchronises).
+template <bool AK, bool BK, class FA, class FB>
+__device__ __forceinline__ void mm_tile(float (&acc)[4][4], MMSmem& s, int k0, int k1, FA fa,
+                                        FB fb) {
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    for (int kb = k0; kb < k1; kb += kK) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = tid + kThreads * r;
+            const int am = AK ? (e >> 4) : (e & 63), ak = AK ? (e & 15) : (e >> 6);
+            const int bn = BK ? (e >> 4) : (e & 63), bk = BK ? (e & 15) : (e >> 6);
+            s.a[ak][am] = (kb + ak < k1) ? fa(am, kb + ak) : 0.f;
+            s.b[bk][bn] = (kb + bk < k1) ? fb(kb + bk, bn) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(&s.a[k][4 * ty]);
+            const float4 b = *reinterpret_cast<const float4*>(&s.b[k][4 * tx]);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+            const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+        }
+        __syncthreads();
+    }
+}
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+}
+
+// Sum over the block (256 threads); `red` holds 8 floats; the result is
+// returned to every thread.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+    return s;
+}
+
+// Suffix sum over the block: thread j gets sum_{k >= j} v_k.  `red` holds 8 floats.
+__device__ __forceinline__ float block_suffix_sum(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_down_sync(0xffffffffu, s, o);
+        if (lane + o < 32) s += n;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = s;   // the warp's total
+    __syncthreads();
+    for (int w = warp + 1; w < kThreads / 32; ++w) s += red[w];
+    return s;
+}
+
+// Decode a lower-triangular tile pair index into (ti, tj), tj <= ti.
+__device__ __forceinline__ void pair_of(int k, int& ti, int& tj) {
+    ti = 0;
+    while ((ti + 1) * (ti + 2) / 2 <= k) ++ti;
+    tj = k - ti * (ti + 1) / 2;
+}
+
+struct BwdArgs {
+    const void* x;      // [b,T,H,P] TI
+    const void* B;      // [b,T,G,N] TI
+    const void* C;      // [b,T,G,N] TI
+    const void* dy;     // [b,T,H,P] TI
+    const float* A;     // [H]
+    const float* D;     // [H] or null
+    const float* cum2;  // [b,H,T]
+    const float* dtT;   // [b,H,T]
+    const float* Sprev; // [b,nc,H,P,N] fp32
+    float* Gn;          // [b,nc,H,P,N] fp32: dSout, then Gn
+    float* CB;          // [b,nc,G,L,L] fp32
+    float* SdCB;        // [b,nc,G,L,L] fp32
+    float* dx;          // [b,T,H,P]
+    float* ddt;         // [b,T,H]
+    float* dA;          // [H] (accumulated)
+    float* dD;          // [H] (accumulated) or null
+    float* dB;          // [b,T,G,N]
+    float* dC;          // [b,T,G,N]
+    int T, H, P, N, G, L, nc;
+};
+
+// --- dSout[b,c,h] = sum_i e_i dy_i C_i^T  (P x N).  Grid: b*nc*H * ceil(P/64) * ceil(N/64).
+template <typename TI>
+__global__ void __launch_bounds__(kThreads) bwd_chunk_adjoint(BwdArgs a) {
+    __shared__ MMSmem sm;
+    __shared__ float s_e[256];
+    const int npt = (a.P + kT - 1) / kT, nnt = (a.N + kT - 1) / kT;
+    int id = blockIdx.x;
+    const int nt = id % nnt; id /= nnt;
+    const int pt = id % npt; id /= npt;
+    const int h = id % a.H; id /= a.H;
+    const int c = id % a.nc, b = id / a.nc;
+    const int g = h / (a.H / a.G);
+    const int64_t t0 = (int64_t)c * a.L;
+    const int Lc = (int)min((int64_t)a.L, a.T - t0);
+    const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
+    for (int i = threadIdx.x; i < a.L; i += kThreads) s_e[i] = i < Lc ? ex2(c2[i]) : 0.f;
+    __syncthreads();
+    const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * a.H * a.P + (int64_t)h * a.P;
+    const TI* C = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * a.G * a.N + (int64_t)g * a.N;
+    const int64_t sdy = (int64_t)a.H * a.P, sC = (int64_t)a.G * a.N;
+    const int P = a.P, N = a.N;
+    float acc[4][4];
+    zero(acc);
+    mm_tile<false, false>(
+        acc, sm, 0, Lc,
+        [&](int m, int k) {
+            const int p = pt * kT + m;
+            return p < P ? s_e[k] * to_f32(dy[k * sdy + p]) : 0.f;
+        },
+        [&](int k, int n) {
+            const int nn = nt * kT + n;
+            return nn < N ? to_f32(C[k * sC + nn]) : 0.f;
+        });
+    float* out = a.Gn + (((int64_t)b * a.nc + c) * a.H + h) * (int64_t)P * N;
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int p = pt * kT + 4 * ty + r;
+        if (p >= P) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int nn = nt * kT + 4 * tx + q;
+            if (nn < N) out[(int64_t)p * N + nn] = acc[r][q];
+        }
+    }
+}
+
+// --- Reverse pass over chunks, in place: buf[c] holds dSout_c on entry and
+// Gn_c = dSprev_{c+1} on exit; dinit = dSprev_0.  One thread per (b, h, p, n).
+__global__ void __launch_bounds__(kThreads)
+bwd_state_pass_rev(float* __restrict__ buf, const float* __restrict__ cum2,
+                   const float* __restrict__ dfinal, float* __restrict__ dinit, int64_t total,
+                   int H, int64_t PN, int T, int L, int nc) {
+    for (int64_t idx = blockIdx.x * (int64_t)kThreads + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * kThreads) {
+        const int64_t k = idx % PN, bh = idx / PN;
+        const int64_t b = bh / H, h = bh % H;
+        float gv = dfinal ? dfinal[idx] : 0.f;
+        const float* c2 = cum2 + bh * T;
+        for (int c = nc - 1; c >= 0; --c) {
+            const int64_t off = ((b * nc + c) * H + h) * PN + k;
+            const float v = buf[off];
+            buf[off] = gv;
+            const int last = min(T, (c + 1) * L) - 1;
+            gv = fmaf(ex2(c2[last]), gv, v);
+        }
+        if (dinit) dinit[idx] = gv;
+    }
+}
+
+// --- Per (b, c, g) and tile pair (ti >= tj): CB = C_i . B_j and
+// SdCB = sum_h exp2(c2_i - c2_j) dt_j (dy_i . x_j), masked to j <= i < Lc
+// (0 elsewhere in the tile).  Grid: b*nc*G * (nt (nt + 1) / 2), nt = ceil(L/64).
+template <typename TI>
+__global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
+    __shared__ MMSmem sm;
+    __shared__ float s_c2i[kT], s_c2j[kT], s_dtj[kT];
+    const int ntl = (a.L + kT - 1) / kT, npair = ntl * (ntl + 1) / 2;
+    int id = blockIdx.x;
+    const int pair = id % npair; id /= npair;
+    const int g = id % a.G; id /= a.G;
+    const int c = id % a.nc, b = id / a.nc;
+    int ti, tj;
+    pair_of(pair, ti, tj);
+    const int64_t t0 = (int64_t)c * a.L;
+    const int Lc = (int)min((int64_t)a.L, a.T - t0);
+    if (ti * kT >= Lc) return;   // no token of the chunk in this row tile
+    const int hpg = a.H / a.G, P = a.P, N = a.N;
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * a.G * N + (int64_t)g * N;
+    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * a.G * N + (int64_t)g * N;
+    const int64_t sBC = (int64_t)a.G * N;
+    float acc[4][4];
+    zero(acc);
+    mm_tile<true, true>(
+        acc, sm, 0, N,
+        [&](int m, int k) {
+            const int i = ti * kT + m;
+            return i < Lc ? to_f32(Cg[i * sBC + k]) : 0.f;
+        },
+        [&](int k, int n) {
+            const int j = tj * kT + n;
+            return j < Lc ? to_f32(Bg[j * sBC + k]) : 0.f;
+        });
+    const int64_t toff = (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)a.L * a.L;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = ti * kT + 4 * ty + r;
+        if (i >= a.L) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = tj * kT + 4 * tx + q;
+            if (j < a.L) a.CB[toff + (int64_t)i * a.L + j] = acc[r][q];
+        }
+    }
+    float sd[4][4];
+    zero(sd);
+    const int64_t sxy = (int64_t)a.H * P;
+    for (int hh = 0; hh < hpg; ++hh) {
+        const int h = g * hpg + hh;
+        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
+        const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
+        if (threadIdx.x < kT) {
+            const int i = ti * kT + threadIdx.x, j = tj * kT + threadIdx.x;
+            s_c2i[threadIdx.x] = i < Lc ? c2[i] : 0.f;
+            s_c2j[threadIdx.x] = j < Lc ? c2[j] : 0.f;
+            s_dtj[threadIdx.x] = j < Lc ? dth[j] : 0.f;
+        }
+        // (mm_tile's first barrier orders these stores before their use below.)
+        const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+        const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+        float dxa[4][4];
+        zero(dxa);
+        mm_tile<true, true>(
+            dxa, sm, 0, P,
+            [&](int m, int k) {
+                const int i = ti * kT + m;
+                return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
+            },
+            [&](int k, int n) {
+                const int j = tj * kT + n;
+                return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
+            });
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int il = 4 * ty + r, i = ti * kT + il;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int jl = 4 * tx + q, j = tj * kT + jl;
+                if (i < Lc && j <= i)
+                    sd[r][q] = fmaf(ex2(s_c2i[il] - s_c2j[jl]) * s_dtj[jl], dxa[r][q], sd[r][q]);
+            }
+        }
+        __syncthreads();   // s_c2i/s_c2j/s_dtj are rewritten for the next head
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = ti * kT + 4 * ty + r;
+        if (i >= a.L) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = tj * kT + 4 * tx + q;
+            if (j < a.L) a.SdCB[toff + (int64_t)i * a.L + j] = sd[r][q];
+        }
+    }
+}
+
+// --- Per (b, c, h): dx, ddt and the dA, dD partial sums.  Grid: b*nc*H.
+template <typename TI>
+__global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
+    __shared__ MMSmem sm;
+    __shared__ float Mt[kT][kT + 1];
+    __shared__ float s_c2[256], s_dt[256], s_dcum[256], s_ddt[256], s_xgb[256];
+    __shared__ float red[kThreads / 32];
+    int id = blockIdx.x;
+    const int h = id % a.H; id /= a.H;
+    const int c = id % a.nc, b = id / a.nc;
+    const int g = h / (a.H / a.G);
+    const int P = a.P, N = a.N, L = a.L;
+    const int64_t t0 = (int64_t)c * L;
+    const int Lc = (int)min((int64_t)L, a.T - t0);
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    {
+        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
+        const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
+        for (int i = tid; i < 256; i += kThreads) {
+            s_c2[i] = i < Lc ? c2[i] : 0.f;
+            s_dt[i] = i < Lc ? dth[i] : 0.f;
+            s_dcum[i] = 0.f;
+            s_ddt[i] = 0.f;
+            s_xgb[i] = 0.f;
+        }
+    }
+    __syncthreads();
+    const float c2last = s_c2[Lc - 1];
+    const float Ah = a.A[h];
+    const float Dh = a.D ? a.D[h] : 0.f;
+    const int64_t sxy = (int64_t)a.H * P, sBC = (int64_t)a.G * N;
+    const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+    const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
+    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
+    const int64_t soff = (((int64_t)b * a.nc + c) * a.H + h) * (int64_t)P * N;
+    const float* Sp = a.Sprev + soff;
+    const float* Gn = a.Gn + soff;
+    const float* CB = a.CB + (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)L * L;
+    float* dx = a.dx + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+    const int ntile = (Lc + kT - 1) / kT, npt = (P + kT - 1) / kT;
+
+    for (int tj = 0; tj < ntile; ++tj) {
+        float accx[2][4][4];
+        zero(accx[0]);
+        zero(accx[1]);
+        for (int ti = tj; ti < ntile; ++ti) {
+            float dxa[4][4];
+            zero(dxa);
+            mm_tile<true, true>(
+                dxa, sm, 0, P,
+                [&](int m, int k) {
+                    const int i = ti * kT + m;
+                    return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int j = tj * kT + n;
+                    return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
+                });
+            float rowq[4] = {0.f, 0.f, 0.f, 0.f}, colq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int il = 4 * ty + r, i = ti * kT + il;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int jl = 4 * tx + q, j = tj * kT + jl;
+                    float m = 0.f;
+                    if (i < Lc && j <= i) {
+                        const float base = CB[(int64_t)i * L + j] * ex2(s_c2[i] - s_c2[j]);
+                        const float qv = base * dxa[r][q];
+                        m = base * s_dt[j];
+                        rowq[r] = fmaf(qv, s_dt[j], rowq[r]);
+                        colq[q] += qv;
+                    }
+                    Mt[il][jl] = m;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = ti * kT + 4 * ty + r;
+                if (i < Lc) atomicAdd(&s_dcum[i], rowq[r]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = tj * kT + 4 * tx + q;
+                if (j < Lc) {
+                    atomicAdd(&s_ddt[j], colq[q]);
+                    atomicAdd(&s_dcum[j], -colq[q] * s_dt[j]);
+                }
+            }
+            __syncthreads();   // Mt complete
+#pragma unroll
+            for (int pt = 0; pt < 2; ++pt)
+                if (pt < npt)
+                    mm_tile<false, false>(
+                    accx[pt], sm, 0, kT, [&](int m, int k) { return Mt[k][m]; },
+                    [&](int k, int n) {
+                        const int i = ti * kT + k, p = pt * kT + n;
+                        return (i < Lc && p < P) ? to_f32(dy[i * sxy + p]) : 0.f;
+                    });
+        }
+        // dx_j = (M^T dy)_j + w_j Gn B_j + D dy_j; x_j . (Gn B_j) for ddt and dcum.
+#pragma unroll
+        for (int pt = 0; pt < 2; ++pt) {
+            if (pt >= npt) break;
+            float gb[4][4];
+            zero(gb);
+            mm_tile<true, true>(
+                gb, sm, 0, N,
+                [&](int m, int k) {
+                    const int j = tj * kT + m;
+                    return j < Lc ? to_f32(Bg[j * sBC + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int p = pt * kT + n;
+                    return p < P ? Gn[(int64_t)p * N + k] : 0.f;
+                });
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int j = tj * kT + 4 * ty + r;
+                if (j >= Lc) continue;
+                const float wj = s_dt[j] * ex2(c2last - s_c2[j]);
+                float xg = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int p = pt * kT + 4 * tx + q;
+                    if (p < P) {
+                        const float dyv = to_f32(dy[j * sxy + p]);
+                        dx[j * sxy + p] = accx[pt][r][q] + wj * gb[r][q] + Dh * dyv;
+                        xg = fmaf(to_f32(x[j * sxy + p]), gb[r][q], xg);
+                    }
+                }
+                atomicAdd(&s_xgb[j], xg);
+            }
+        }
+    }
+    // dcum_i += e_i dy_i . (Sprev C_i)
+    for (int ti = 0; ti < ntile; ++ti) {
+        for (int pt = 0; pt < npt; ++pt) {
+            float yo[4][4];
+            zero(yo);
+            mm_tile<true, true>(
+                yo, sm, 0, N,
+                [&](int m, int k) {
+                    const int i = ti * kT + m;
+                    return i < Lc ? to_f32(Cg[i * sBC + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int p = pt * kT + n;
+                    return p < P ? Sp[(int64_t)p * N + k] : 0.f;
+                });
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = ti * kT + 4 * ty + r;
+                if (i >= Lc) continue;
+                float s = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int p = pt * kT + 4 * tx + q;
+                    if (p < P) s = fmaf(to_f32(dy[i * sxy + p]), yo[r][q], s);
+                }
+                atomicAdd(&s_dcum[i], ex2(s_c2[i]) * s);
+            }
+        }
+    }
+    // <Gn, Sprev> and sum dy . x over the chunk.
+    float gs = 0.f, yx = 0.f;
+    for (int64_t k = tid; k < (int64_t)P * N; k += kThreads) gs = fmaf(Gn[k], Sp[k], gs);
+    for (int k = tid; k < Lc * P; k += kThreads) {
+        const int i = k / P, p = k % P;
+        yx = fmaf(to_f32(dy[i * sxy + p]), to_f32(x[i * sxy + p]), yx);
+    }
+    gs = block_sum(gs, red);
+    yx = block_sum(yx, red);
+    __syncthreads();   // every s_xgb / s_dcum / s_ddt update is in
+    // Per token j (one thread each): the state-side terms of ddt and dcum.
+    const int j = tid;
+    float wxg = 0.f;
+    if (j < Lc) {
+        const float ed = ex2(c2last - s_c2[j]);
+        const float xg = s_xgb[j];
+        s_ddt[j] = fmaf(ed, xg, s_ddt[j]);
+        wxg = s_dt[j] * ed * xg;
+        s_dcum[j] -= wxg;
+    }
+    const float W = block_sum(wxg, red);
+    if (tid == 0) s_dcum[Lc - 1] += W + ex2(c2last) * gs;
+    __syncthreads();
+    const float rcs = block_suffix_sum(j < Lc ? s_dcum[j] : 0.f, red);
+    float da = 0.f;
+    if (j < Lc) {
+        a.ddt[((int64_t)b * a.T + t0 + j) * a.H + h] = fmaf(Ah, rcs, s_ddt[j]);
+        da = s_dt[j] * rcs;
+    }
+    da = block_sum(da, red);
+    if (tid == 0) {
+        atomicAdd(a.dA + h, da);
+        if (a.dD) atomicAdd(a.dD + h, yx);
+    }
+}
+
+// --- dC (blockIdx.y == 0) or dB (blockIdx.y == 1) for one 64-token tile and one
+// 64-column tile of (b, c, g).  Grid: (b*nc*G * ceil(L/64) * ceil(N/64), 2).
+template <typename TI>
+__global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
+    __shared__ MMSmem sm;
+    const int ntl = (a.L + kT - 1) / kT, nnt = (a.N + kT - 1) / kT;
+    int id = blockIdx.x;
+    const int nt = id % nnt; id /= nnt;
+    const int tt = id % ntl; id /= ntl;
+    const int g = id % a.G; id /= a.G;
+    const int c = id % a.nc, b = id / a.nc;
+    const bool isB = blockIdx.y == 1;
+    const int P = a.P, N = a.N, L = a.L, H = a.H;
+    const int hpg = H / a.G;
+    const int64_t t0 = (int64_t)c * L;
+    const int Lc = (int)min((int64_t)L, a.T - t0);
+    if (tt * kT >= Lc) return;
+    const int64_t sxy = (int64_t)H * P, sBC = (int64_t)a.G * N;
+    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
+    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
+    const float* Sd = a.SdCB + (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)L * L;
+    const int h0 = g * hpg;
+    // Rows of (head, p) for the second contraction: heads h0 .. h0+hpg-1 are
+    // contiguous in x / dy ([.., H, P]) and in Sprev / Gn ([.., H, P, N]).
+    const TI* xg = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h0 * P;
+    const TI* dyg = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h0 * P;
+    const int64_t soff = (((int64_t)b * a.nc + c) * H + h0) * (int64_t)P * N;
+    const float* c2g = a.cum2 + ((int64_t)b * H + h0) * a.T + t0;   // head stride a.T
+    const float* dtg = a.dtT + ((int64_t)b * H + h0) * a.T + t0;
+    const int64_t T = a.T;
+    const int KP = hpg * P;
+    float acc[4][4];
+    zero(acc);
+    if (!isB) {
+        // dC_i = sum_{j <= i} SdCB_ij B_j + sum_{h,p} e_hi dy_hi[p] Sprev_h[p, :]
+        mm_tile<true, false>(
+            acc, sm, 0, min(Lc, (tt + 1) * kT),
+            [&](int m, int k) {
+                const int i = tt * kT + m;
+                return i < Lc ? Sd[(int64_t)i * L + k] : 0.f;
+            },
+            [&](int k, int n) {
+                const int nn = nt * kT + n;
+                return nn < N ? to_f32(Bg[k * sBC + nn]) : 0.f;
+            });
+        const float* Sp = a.Sprev + soff;
+        mm_tile<true, false>(
+            acc, sm, 0, KP,
+            [&](int m, int k) {
+                const int i = tt * kT + m;
+                if (i >= Lc) return 0.f;
+                const int hh = k / P;
+                return ex2(c2g[hh * T + i]) * to_f32(dyg[i * sxy + k]);
+            },
+            [&](int k, int n) {
+                const int nn = nt * kT + n;
+                return nn < N ? Sp[(int64_t)k * N + nn] : 0.f;
+            });
+    } else {
+        // dB_j = sum_{i >= j} SdCB_ij C_i + sum_{h,p} w_hj x_hj[p] Gn_h[p, :]
+        mm_tile<false, false>(
+            acc, sm, tt * kT, Lc,
+            [&](int m, int k) {
+                const int j = tt * kT + m;
+                return j < Lc ? Sd[(int64_t)k * L + j] : 0.f;
+            },
+            [&](int k, int n) {
+                const int nn = nt * kT + n;
+                return nn < N ? to_f32(Cg[k * sBC + nn]) : 0.f;
+            });
+        const float* Gn = a.Gn + soff;
+        mm_tile<true, false>(
+            acc, sm, 0, KP,
+            [&](int m, int k) {
+                const int j = tt * kT + m;
+                if (j >= Lc) return 0.f;
+                const int hh = k / P;
+                const float w = dtg[hh * T + j] * ex2(c2g[hh * T + Lc - 1] - c2g[hh * T + j]);
+                return w * to_f32(xg[j * sxy + k]);
+            },
+            [&](int k, int n) {
+                const int nn = nt * kT + n;
+                return nn < N ? Gn[(int64_t)k * N + nn] : 0.f;
+            });
+    }
+    float* out = (isB ? a.dB : a.dC) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
+    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int i = tt * kT + 4 * ty + r;
+        if (i >= Lc) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int nn = nt * kT + 4 * tx + q;
+            if (nn < N) out[i * sBC + nn] = acc[r][q];
+        }
+    }
+}
+
+template <typename TI>
+cudaError_t launch_t(const Dims& d, const BwdArgs& a, const float* dfinal, float* dinit,
+                     cudaStream_t st) {
+    const int64_t bnc = d.b * d.nc;
+    const int npt = (int)((d.P + kT - 1) / kT), nnt = (int)((d.N + kT - 1) / kT);
+    const int ntl = (int)((d.L + kT - 1) / kT);
+    const int64_t g1 = bnc * d.H * npt * nnt;
+    const int64_t g3 = bnc * d.G * (ntl * (ntl + 1) / 2);
+    const int64_t g4 = bnc * d.H;
+    const int64_t g5 = bnc * d.G * ntl * nnt;
+    if (g1 >= (int64_t(1) << 31) || g3 >= (int64_t(1) << 31) || g4 >= (int64_t(1) << 31) ||
+        g5 >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
+    bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
+    const int64_t total = d.b * d.H * d.P * d.N;
+    const int64_t blocks = std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
+    bwd_state_pass_rev<<<(unsigned)blocks, kThreads, 0, st>>>(a.Gn, a.cum2, dfinal, dinit, total,
+                                                              (int)d.H, d.P * d.N, (int)d.T,
+                                                              (int)d.L, (int)d.nc);
+    bwd_pair_tiles<TI><<<(unsigned)g3, kThreads, 0, st>>>(a);
+    bwd_head<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
+    bwd_group_bc<TI><<<dim3((unsigned)g5, 2), kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const Dims& d, const void* x, const void* B, const void* C,
+                            const void* dy, const float* A, const float* D, const float* cum2,
+                            const float* dtT, const float* Sprev, float* Gn, float* CB, float* SdCB,
+                            const float* dfinal, float* dx, float* ddt, float* dA, float* dB,
+                            float* dC, float* dD, float* dinit, cudaStream_t st) {
+    if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
+    if (d.L > 256 || d.P > 2 * kT) return cudaErrorInvalidValue;   // bwd_head's token / p tiles
+    BwdArgs a{x,   B,   C,  dy, A,  D,  cum2, dtT, Sprev, Gn,         CB,         SdCB,
+              dx,  ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
+              (int)d.L, (int)d.nc};
+    return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, dfinal, dinit, st)
+                        : launch_t<float>(d, a, dfinal, dinit, st);
+}
+
+}  // namespace m2

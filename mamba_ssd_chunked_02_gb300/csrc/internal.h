@@ -94,6 +94,15 @@ cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* d
                           const void* B, const void* C, const float* D, void* y, int32_t* err,
                           cudaStream_t st);
 
+// Backward pass after the forward's stages 1-3 (cum2, dtT, fp32 Sprev): Gn
+// [b,nc,H,P,N], CB and SdCB [b,nc,G,L,L] are fp32 scratch; dA and dD (if
+// given) are accumulated into (zero them first); dinit may be null.
+cudaError_t launch_backward(const Dims& d, const void* x, const void* B, const void* C,
+                            const void* dy, const float* A, const float* D, const float* cum2,
+                            const float* dtT, const float* Sprev, float* Gn, float* CB, float* SdCB,
+                            const float* dfinal, float* dx, float* ddt, float* dA, float* dB,
+                            float* dC, float* dD, float* dinit, cudaStream_t st);
+
 // Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);
 

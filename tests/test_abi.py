@@ -231,3 +231,39 @@ def test_fwd_strided_validates_strides_without_launching(lib):
     st = strides(x=(T * (H * P + 2 * G * N), H * P + 2 * G * N))
     rc = lib.mamba2_ssd_fwd_strided(ctypes.byref(s), ctypes.byref(st), None, *args[1:])
     assert rc == m2.ERR_INVALID_ARG
+
+
+def test_bwd_workspace_size_formula(lib):
+    """Backward workspace: cum2 and dtT, fp32 dS and Sprev, C.B^T and the
+    head-summed dCB per (b, chunk, group), and a final-state scratch, each
+    rounded up to 256 bytes."""
+    a256 = lambda v: (v + 255) // 256 * 256
+    s = shp()
+    b, T, H, P, N, G, L = 2, 512, 8, 64, 128, 1, 256
+    nc = T // L
+    want = 2 * a256(4 * b * H * T) + 2 * a256(4 * b * nc * H * P * N) + \
+        2 * a256(4 * b * nc * G * L * L) + a256(4 * b * H * P * N)
+    assert m2.bwd_workspace_size(s) == want
+    assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
+
+
+def test_bwd_validates_arguments_without_launching(lib):
+    s = shp()
+    vp = ctypes.c_void_p
+    good = vp(1 << 20)       # aligned, never dereferenced: validation fails first
+    ws = m2.bwd_workspace_size(s)
+
+    def call(shape=s, D=good, dD=good, x=good, workspace=good, nbytes=ws):
+        return lib.mamba2_ssd_bwd(ctypes.byref(shape), x, good, good, good, good, D, None, good,
+                                  None, good, good, good, good, good, dD, None, workspace,
+                                  ctypes.c_size_t(nbytes), None)
+
+    assert call(shape=shp(flags=m2.FLAG_FUSED_STATE)) == m2.ERR_INVALID_ARG
+    assert call(shape=shp(flags=m2.FLAG_SERIAL)) == m2.ERR_INVALID_ARG
+    assert call(dD=None) == m2.ERR_INVALID_ARG                     # D given, dD missing
+    assert call(x=vp((1 << 20) + 4)) == m2.ERR_INVALID_ARG         # misaligned
+    assert call(x=None) == m2.ERR_INVALID_ARG
+    assert call(workspace=None) == m2.ERR_WORKSPACE
+    assert call(nbytes=ws - 1) == m2.ERR_WORKSPACE
+    assert call(workspace=vp((1 << 20) + 16)) == m2.ERR_WORKSPACE  # not 256-byte aligned
+    assert call(shape=shp(headdim=3)) == m2.ERR_UNSUPPORTED

@@ -1,0 +1,142 @@
+"""The backward pass (mamba2_ssd_bwd) against the oracle's reverse sweep of the
+recurrence, element by element, on the forward's tolerance rule applied to each
+gradient (bf16 inputs: relL2 <= 1e-2 and max|err| <= 5e-2 rms; fp32 inputs:
+relL2 <= 1e-4).  The pages give no backward method ("NVIDIA、cuTileでMamba-2
+フォワードパスを高速化", "開発現場への影響と未確認事項"); the oracle's is the chain rule
+on the recurrence, pinned by finite differences of the forward
+(tests/test_oracle_bwd.py).
+
+At the 2.7B layer's size the oracle takes sampled (b, h) pairs (dx, ddt), and the
+homogeneity of the loss L = sum(dy*y) + sum(dfinal*final_state) ties the GPU
+gradients to the GPU's fp32 forward over every element: sum(dx*x) +
+sum(dinit*init) = L and sum(dC*C) = sum(dy*(y - D x)), whatever the size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mamba_ssd_chunked_02_gb300 as m2
+import oracle
+from mamba_ssd_chunked_02_gb300 import workloads as W
+from parity import assert_close, metrics, sample_pairs, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mamba_ssd_chunked_02_gb300 import build
+    build.build()
+    m2.load()
+    m2.device_error(clear=True)
+
+
+def wl(b, T, H, P, N, G, L, dtype="bf16", init=0.0, seed=1):
+    return W.Workload(f"bwd b{b} T{T} H{H} P{P} N{N} G{G} L{L} {dtype} init{init}",
+                      b, T, H, P, N, G, L, dtype=dtype, init_std=init, seed=seed)
+
+
+# (workload, with D, with dfinal)
+CASES = [
+    (wl(1, 256, 2, 16, 16, 1, 64, "f32", seed=71), True, True),        # the fp32 tiny shape
+    (wl(2, 512, 4, 64, 128, 1, 256, init=0.1, seed=72), True, True),   # tensor-core recompute
+    (wl(2, 384, 8, 64, 128, 2, 128, init=0.1, seed=73), True, False),  # groups, no dfinal
+    (wl(2, 300, 4, 32, 64, 1, 128, seed=74), False, True),             # ragged tail, no D
+    (wl(1, 200, 2, 128, 256, 1, 64, "f32", init=0.1, seed=75), True, True),   # two p tiles
+    (wl(1, 192, 3, 64, 32, 3, 64, seed=76), True, True),               # one head per group
+]
+
+
+def run_bwd(w, inp, gr, flags=0):
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    dy = gr["dy"].cuda()
+    dfin = gr["dfinal"].cuda() if gr["dfinal"] is not None else None
+    g = m2.ssd_bwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                   dev["initial_state"], dy, dfin, chunk_size=w.chunk_size, ngroups=w.ngroups,
+                   flags=flags)
+    torch.cuda.synchronize()
+    assert m2.device_error() == 0
+    return {k: (to_np(v) if v is not None else None) for k, v in g.items()}
+
+
+def inputs(w, with_D, with_dfinal):
+    inp = W.make_inputs(w)
+    if not with_D:
+        inp["D"] = None
+    gr = W.make_grads(w, with_dfinal=with_dfinal)
+    return inp, gr
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0].name[4:] + ("" if c[1] else " noD") +
+                                             ("" if c[2] else " nodfinal") for c in CASES])
+def test_backward_matches_oracle(case):
+    w, with_D, with_dfinal = case
+    inp, gr = inputs(w, with_D, with_dfinal)
+    got = run_bwd(w, inp, gr)
+    ref = oracle.ssd_backward(**inp, **gr, ngroups=w.ngroups)
+    for k in ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit"):
+        if ref[k] is None or (k == "dD" and not with_D) or (k == "dinit" and w.init_std == 0):
+            assert got[k] is None, k
+            continue
+        assert_close(got[k], ref[k], w.dtype, k)
+
+
+def test_backward_simt_recompute_matches_tensor_core_recompute():
+    """FORCE_SIMT only changes how the forward's chunk states are recomputed."""
+    w = CASES[1][0]
+    inp, gr = inputs(w, True, True)
+    a = run_bwd(w, inp, gr)
+    b = run_bwd(w, inp, gr, flags=m2.FLAG_FORCE_SIMT)
+    for k in a:
+        if a[k] is not None:
+            rel, _ = metrics(b[k], a[k])
+            assert rel < 1e-2, (k, rel)
+
+
+def test_backward_empty_sequence():
+    """T = 0: dinit = dfinal, dA = dD = 0, nothing else to write."""
+    w = wl(2, 0, 4, 16, 16, 2, 64, "f32", init=0.1, seed=77)
+    inp = W.make_inputs(w)
+    gr = W.make_grads(w)
+    got = run_bwd(w, inp, gr)
+    assert np.array_equal(got["dinit"], to_np(gr["dfinal"]))
+    assert not got["dA"].any() and not got["dD"].any()
+
+
+def test_backward_full_size_sampled_and_identities():
+    """The 2.7B layer (b8 T4096 H80 P64 N128 L256): dx and ddt of sampled (b, h)
+    pairs against the oracle, and the homogeneity identities against the GPU
+    forward over every element."""
+    w = W.MAMBA2_2P7B
+    inp = W.make_inputs(w)
+    gr = W.make_grads(w)
+    got = run_bwd(w, inp, gr)
+    pairs = sample_pairs(w.batch, w.nheads, 3, seed=3)
+    ref = oracle.ssd_backward(**inp, **gr, ngroups=w.ngroups, pairs=pairs)
+    for (b, h) in pairs:
+        assert_close(got["dx"][b, :, h], ref["dx"][b, :, h], w.dtype, f"dx {b},{h}")
+        assert_close(got["ddt"][b, :, h], ref["ddt"][b, :, h], w.dtype, f"ddt {b},{h}")
+    # L from the fp32 forward on the same values (bf16 widens exactly), so that
+    # the identity measures the backward, not the bf16 rounding of y.  Scale of
+    # the sums: S = sqrt(sum (dy*y)^2) + sqrt(sum (dfinal*final)^2), the size of
+    # the random rounding errors' sum.
+    dev = {k: (v.cuda().float() if v is not None else None) for k, v in inp.items()}
+    y, fin = m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], None,
+                        chunk_size=w.chunk_size, ngroups=w.ngroups)
+    torch.cuda.synchronize()
+    assert m2.device_error() == 0
+    y, fin = to_np(y), to_np(fin)
+    x = to_np(inp["x"])
+    dy, dfin = to_np(gr["dy"]), to_np(gr["dfinal"])
+    L = np.sum(dy * y) + np.sum(dfin * fin)
+    S = np.sqrt(np.sum((dy * y) ** 2)) + np.sqrt(np.sum((dfin * fin) ** 2))
+    lhs = np.sum(got["dx"] * x)
+    assert abs(lhs - L) <= 1e-3 * S, (lhs, L, S)
+    dxD = np.sum(dy * x * to_np(inp["D"])[None, None, :, None])
+    lc = np.sum(got["dC"] * to_np(inp["C"]))
+    # dC's carried-state part uses the recomputed states (bf16 operands in stage 2)
+    assert abs(lc - (np.sum(dy * y) - dxD)) <= 1e-2 * S, (lc, np.sum(dy * y) - dxD, S)
+    ref_dD = np.einsum("bthp,bthp->h", dy, x)
+    assert_close(got["dD"], ref_dD, w.dtype, "dD")
