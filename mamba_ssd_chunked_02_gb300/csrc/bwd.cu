@@ -52,36 +52,59 @@ namespace {
 constexpr int kT = 64;         // tile edge (tokens, p, n)
 constexpr int kK = 16;         // k per shared-memory stage
 constexpr int kThreads = 256;  // 16 x 16 threads, 4 x 4 outputs each
+constexpr int kHB = 16;        // heads per block of the (head, p) contractions
 
 struct MMSmem {
-    float a[kK][kT + 4];
-    float b[kK][kT + 4];
+    float a[2][kK][kT + 4];
+    float b[2][kK][kT + 4];
 };
 
 // acc[r][q] += sum_{k in [k0, k1)} A(4 ty + r, k) * B(k, 4 tx + q), with
 // ty = threadIdx.x / 16, tx = threadIdx.x % 16.  fa(m, k) / fb(k, n) return the
 // operand elements (0 outside the operand); AK / BK: the operand is contiguous
 // in memory along k (else along m / n), which sets the load order so that
-// neighbouring threads read neighbouring addresses.  Every thread of the block
-// must call it (it synchronises).
+// neighbouring threads read neighbouring addresses.  Two shared-memory stages:
+// the next 16 k are fetched into registers while the current ones are used.
+// Every thread of the block must call it; it synchronises on entry (after the
+// first fetch) and on exit, so shared memory the functors read may be written
+// right before the call and rewritten right after it.
 template <bool AK, bool BK, class FA, class FB>
 __device__ __forceinline__ void mm_tile(float (&acc)[4][4], MMSmem& s, int k0, int k1, FA fa,
                                         FB fb) {
+    if (k0 >= k1) return;
     const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    for (int kb = k0; kb < k1; kb += kK) {
+    float ra[4], rb[4];
+    auto fetch = [&](int kb) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int e = tid + kThreads * r;
             const int am = AK ? (e >> 4) : (e & 63), ak = AK ? (e & 15) : (e >> 6);
             const int bn = BK ? (e >> 4) : (e & 63), bk = BK ? (e & 15) : (e >> 6);
-            s.a[ak][am] = (kb + ak < k1) ? fa(am, kb + ak) : 0.f;
-            s.b[bk][bn] = (kb + bk < k1) ? fb(kb + bk, bn) : 0.f;
+            ra[r] = (kb + ak < k1) ? fa(am, kb + ak) : 0.f;
+            rb[r] = (kb + bk < k1) ? fb(kb + bk, bn) : 0.f;
         }
-        __syncthreads();
+    };
+    auto put = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = tid + kThreads * r;
+            const int am = AK ? (e >> 4) : (e & 63), ak = AK ? (e & 15) : (e >> 6);
+            const int bn = BK ? (e >> 4) : (e & 63), bk = BK ? (e & 15) : (e >> 6);
+            s.a[buf][ak][am] = ra[r];
+            s.b[buf][bk][bn] = rb[r];
+        }
+    };
+    fetch(k0);
+    put(0);
+    __syncthreads();
+    int buf = 0;
+    for (int kb = k0; kb < k1; kb += kK) {
+        const bool more = kb + kK < k1;
+        if (more) fetch(kb + kK);
 #pragma unroll
         for (int k = 0; k < kK; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(&s.a[k][4 * ty]);
-            const float4 b = *reinterpret_cast<const float4*>(&s.b[k][4 * tx]);
+            const float4 a = *reinterpret_cast<const float4*>(&s.a[buf][k][4 * ty]);
+            const float4 b = *reinterpret_cast<const float4*>(&s.b[buf][k][4 * tx]);
             const float av[4] = {a.x, a.y, a.z, a.w};
             const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -89,7 +112,9 @@ __device__ __forceinline__ void mm_tile(float (&acc)[4][4], MMSmem& s, int k0, i
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
         }
+        if (more) put(buf ^ 1);
         __syncthreads();
+        buf ^= 1;
     }
 }
 
@@ -157,6 +182,7 @@ struct BwdArgs {
     float* dB;          // [b,T,G,N]
     float* dC;          // [b,T,G,N]
     int T, H, P, N, G, L, nc;
+    int lp;             // log2(P)
 };
 
 // --- dSout[b,c,h] = sum_i e_i dy_i C_i^T  (P x N).  Grid: b*nc*H * ceil(P/64) * ceil(N/64).
@@ -207,23 +233,42 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_adjoint(BwdArgs a) {
 }
 
 // --- Reverse pass over chunks, in place: buf[c] holds dSout_c on entry and
-// Gn_c = dSprev_{c+1} on exit; dinit = dSprev_0.  One thread per (b, h, p, n).
+// Gn_c = dSprev_{c+1} on exit; dinit = dSprev_0.  One thread per (b, h) and
+// four consecutive (p, n); the loads of four chunks are issued before their
+// values are used (the chain through the chunks is the only dependence).
 __global__ void __launch_bounds__(kThreads)
-bwd_state_pass_rev(float* __restrict__ buf, const float* __restrict__ cum2,
-                   const float* __restrict__ dfinal, float* __restrict__ dinit, int64_t total,
-                   int H, int64_t PN, int T, int L, int nc) {
-    for (int64_t idx = blockIdx.x * (int64_t)kThreads + threadIdx.x; idx < total;
+bwd_state_pass_rev(float4* __restrict__ buf, const float* __restrict__ cum2,
+                   const float4* __restrict__ dfinal, float4* __restrict__ dinit, int64_t total4,
+                   int H, int64_t PN4, int T, int L, int nc) {
+    constexpr int kU = 4;
+    for (int64_t idx = blockIdx.x * (int64_t)kThreads + threadIdx.x; idx < total4;
          idx += (int64_t)gridDim.x * kThreads) {
-        const int64_t k = idx % PN, bh = idx / PN;
+        const int64_t k = idx % PN4, bh = idx / PN4;
         const int64_t b = bh / H, h = bh % H;
-        float gv = dfinal ? dfinal[idx] : 0.f;
+        float4 gv = dfinal ? dfinal[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
         const float* c2 = cum2 + bh * T;
-        for (int c = nc - 1; c >= 0; --c) {
-            const int64_t off = ((b * nc + c) * H + h) * PN + k;
-            const float v = buf[off];
-            buf[off] = gv;
-            const int last = min(T, (c + 1) * L) - 1;
-            gv = fmaf(ex2(c2[last]), gv, v);
+        for (int c0 = nc - 1; c0 >= 0; c0 -= kU) {
+            float4 v[kU];
+            float dec[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int c = c0 - u;
+                if (c >= 0) {
+                    v[u] = buf[((b * nc + c) * H + h) * PN4 + k];
+                    dec[u] = ex2(c2[min(T, (c + 1) * L) - 1]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int c = c0 - u;
+                if (c >= 0) {
+                    buf[((b * nc + c) * H + h) * PN4 + k] = gv;
+                    gv.x = fmaf(dec[u], gv.x, v[u].x);
+                    gv.y = fmaf(dec[u], gv.y, v[u].y);
+                    gv.z = fmaf(dec[u], gv.z, v[u].z);
+                    gv.w = fmaf(dec[u], gv.w, v[u].w);
+                }
+            }
         }
         if (dinit) dinit[idx] = gv;
     }
@@ -235,7 +280,7 @@ bwd_state_pass_rev(float* __restrict__ buf, const float* __restrict__ cum2,
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
     __shared__ MMSmem sm;
-    __shared__ float s_c2i[kT], s_c2j[kT], s_dtj[kT];
+    __shared__ float s_sci[kHB][kT], s_scj[kHB][kT];
     const int ntl = (a.L + kT - 1) / kT, npair = ntl * (ntl + 1) / 2;
     int id = blockIdx.x;
     const int pair = id % npair; id /= npair;
@@ -277,42 +322,83 @@ __global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
     float sd[4][4];
     zero(sd);
     const int64_t sxy = (int64_t)a.H * P;
-    for (int hh = 0; hh < hpg; ++hh) {
-        const int h = g * hpg + hh;
-        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
-        const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
-        if (threadIdx.x < kT) {
-            const int i = ti * kT + threadIdx.x, j = tj * kT + threadIdx.x;
-            s_c2i[threadIdx.x] = i < Lc ? c2[i] : 0.f;
-            s_c2j[threadIdx.x] = j < Lc ? c2[j] : 0.f;
-            s_dtj[threadIdx.x] = j < Lc ? dth[j] : 0.f;
-        }
-        // (mm_tile's first barrier orders these stores before their use below.)
-        const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-        const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-        float dxa[4][4];
-        zero(dxa);
-        mm_tile<true, true>(
-            dxa, sm, 0, P,
-            [&](int m, int k) {
-                const int i = ti * kT + m;
-                return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
-            },
-            [&](int k, int n) {
-                const int j = tj * kT + n;
-                return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
-            });
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int il = 4 * ty + r, i = ti * kT + il;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int jl = 4 * tx + q, j = tj * kT + jl;
-                if (i < Lc && j <= i)
-                    sd[r][q] = fmaf(ex2(s_c2i[il] - s_c2j[jl]) * s_dtj[jl], dxa[r][q], sd[r][q]);
+    const int h0 = g * hpg;
+    if (ti > tj) {
+        // Off the diagonal every j of the tile precedes every i, so with r = ti*64
+        // exp2(c2_i - c2_j) = exp2(c2_i - c2_r) exp2(c2_r - c2_j), both factors
+        // <= 1, and the head sum is one contraction over (head, p) with the
+        // factors folded into the operands.
+        for (int hb = 0; hb < hpg; hb += kHB) {
+            const int nh = min(kHB, hpg - hb);
+            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
+                const int hl = e / kT, m = e % kT;
+                float si = 0.f, sj = 0.f;
+                if (hl < nh) {
+                    const int64_t row = ((int64_t)b * a.H + h0 + hb + hl) * a.T + t0;
+                    const float c2r = a.cum2[row + ti * kT];
+                    const int i = ti * kT + m, j = tj * kT + m;
+                    if (i < Lc) si = ex2(a.cum2[row + i] - c2r);
+                    if (j < Lc) sj = ex2(c2r - a.cum2[row + j]) * a.dtT[row + j];
+                }
+                s_sci[hl][m] = si;
+                s_scj[hl][m] = sj;
             }
+            __syncthreads();
+            const TI* dyb = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy +
+                            (int64_t)(h0 + hb) * P;
+            const TI* xb = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy +
+                           (int64_t)(h0 + hb) * P;
+            const int lp = a.lp;
+            mm_tile<true, true>(
+                sd, sm, 0, nh * P,
+                [&](int m, int k) {
+                    const int i = ti * kT + m;
+                    return i < Lc ? s_sci[k >> lp][m] * to_f32(dyb[i * sxy + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int j = tj * kT + n;
+                    return j < Lc ? s_scj[k >> lp][n] * to_f32(xb[j * sxy + k]) : 0.f;
+                });
         }
-        __syncthreads();   // s_c2i/s_c2j/s_dtj are rewritten for the next head
+    } else {
+        // The diagonal tile: one head at a time, the decay per element (masked).
+        for (int hh = 0; hh < hpg; ++hh) {
+            const int h = h0 + hh;
+            const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
+            const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
+            if (threadIdx.x < kT) {
+                const int i = ti * kT + threadIdx.x;
+                s_sci[0][threadIdx.x] = i < Lc ? c2[i] : 0.f;
+                s_scj[0][threadIdx.x] = i < Lc ? dth[i] : 0.f;
+            }
+            // (mm_tile's entry barrier orders these stores before the epilogue.)
+            const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+            const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+            float dxa[4][4];
+            zero(dxa);
+            mm_tile<true, true>(
+                dxa, sm, 0, P,
+                [&](int m, int k) {
+                    const int i = ti * kT + m;
+                    return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int j = tj * kT + n;
+                    return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
+                });
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int il = 4 * ty + r, i = ti * kT + il;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int jl = 4 * tx + q, j = tj * kT + jl;
+                    if (i < Lc && j <= i)
+                        sd[r][q] = fmaf(ex2(s_sci[0][il] - s_sci[0][jl]) * s_scj[0][jl], dxa[r][q],
+                                        sd[r][q]);
+                }
+            }
+            __syncthreads();   // the next head rewrites s_sci / s_scj
+        }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -532,6 +618,7 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
     __shared__ MMSmem sm;
+    __shared__ float s_sc[kHB][kT];   // per (head of the block, row) operand scale
     const int ntl = (a.L + kT - 1) / kT, nnt = (a.N + kT - 1) / kT;
     int id = blockIdx.x;
     const int nt = id % nnt; id /= nnt;
@@ -557,7 +644,7 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
     const float* c2g = a.cum2 + ((int64_t)b * H + h0) * a.T + t0;   // head stride a.T
     const float* dtg = a.dtT + ((int64_t)b * H + h0) * a.T + t0;
     const int64_t T = a.T;
-    const int KP = hpg * P;
+    const int lp = a.lp;
     float acc[4][4];
     zero(acc);
     if (!isB) {
@@ -573,18 +660,26 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
                 return nn < N ? to_f32(Bg[k * sBC + nn]) : 0.f;
             });
         const float* Sp = a.Sprev + soff;
-        mm_tile<true, false>(
-            acc, sm, 0, KP,
-            [&](int m, int k) {
-                const int i = tt * kT + m;
-                if (i >= Lc) return 0.f;
-                const int hh = k / P;
-                return ex2(c2g[hh * T + i]) * to_f32(dyg[i * sxy + k]);
-            },
-            [&](int k, int n) {
-                const int nn = nt * kT + n;
-                return nn < N ? Sp[(int64_t)k * N + nn] : 0.f;
-            });
+        for (int hb = 0; hb < hpg; hb += kHB) {
+            const int nh = min(kHB, hpg - hb);
+            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
+                const int hl = e / kT, i = tt * kT + e % kT;
+                s_sc[hl][e % kT] = (hl < nh && i < Lc) ? ex2(c2g[(hb + hl) * T + i]) : 0.f;
+            }
+            __syncthreads();
+            const TI* dyb = dyg + (int64_t)hb * P;
+            const float* Spb = Sp + (int64_t)hb * P * N;
+            mm_tile<true, false>(
+                acc, sm, 0, nh * P,
+                [&](int m, int k) {
+                    const int i = tt * kT + m;
+                    return i < Lc ? s_sc[k >> lp][m] * to_f32(dyb[i * sxy + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int nn = nt * kT + n;
+                    return nn < N ? Spb[(int64_t)k * N + nn] : 0.f;
+                });
+        }
     } else {
         // dB_j = sum_{i >= j} SdCB_ij C_i + sum_{h,p} w_hj x_hj[p] Gn_h[p, :]
         mm_tile<false, false>(
@@ -598,19 +693,31 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
                 return nn < N ? to_f32(Cg[k * sBC + nn]) : 0.f;
             });
         const float* Gn = a.Gn + soff;
-        mm_tile<true, false>(
-            acc, sm, 0, KP,
-            [&](int m, int k) {
-                const int j = tt * kT + m;
-                if (j >= Lc) return 0.f;
-                const int hh = k / P;
-                const float w = dtg[hh * T + j] * ex2(c2g[hh * T + Lc - 1] - c2g[hh * T + j]);
-                return w * to_f32(xg[j * sxy + k]);
-            },
-            [&](int k, int n) {
-                const int nn = nt * kT + n;
-                return nn < N ? Gn[(int64_t)k * N + nn] : 0.f;
-            });
+        for (int hb = 0; hb < hpg; hb += kHB) {
+            const int nh = min(kHB, hpg - hb);
+            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
+                const int hl = e / kT, j = tt * kT + e % kT;
+                float w = 0.f;
+                if (hl < nh && j < Lc) {
+                    const int64_t o = (int64_t)(hb + hl) * T;
+                    w = dtg[o + j] * ex2(c2g[o + Lc - 1] - c2g[o + j]);
+                }
+                s_sc[hl][e % kT] = w;
+            }
+            __syncthreads();
+            const TI* xb = xg + (int64_t)hb * P;
+            const float* Gnb = Gn + (int64_t)hb * P * N;
+            mm_tile<true, false>(
+                acc, sm, 0, nh * P,
+                [&](int m, int k) {
+                    const int j = tt * kT + m;
+                    return j < Lc ? s_sc[k >> lp][m] * to_f32(xb[j * sxy + k]) : 0.f;
+                },
+                [&](int k, int n) {
+                    const int nn = nt * kT + n;
+                    return nn < N ? Gnb[(int64_t)k * N + nn] : 0.f;
+                });
+        }
     }
     float* out = (isB ? a.dB : a.dC) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
     const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -640,11 +747,12 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const float* dfinal, float
         g5 >= (int64_t(1) << 31))
         return cudaErrorInvalidValue;
     bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
-    const int64_t total = d.b * d.H * d.P * d.N;
-    const int64_t blocks = std::min<int64_t>((total + kThreads - 1) / kThreads, 152 * 16);
-    bwd_state_pass_rev<<<(unsigned)blocks, kThreads, 0, st>>>(a.Gn, a.cum2, dfinal, dinit, total,
-                                                              (int)d.H, d.P * d.N, (int)d.T,
-                                                              (int)d.L, (int)d.nc);
+    const int64_t total4 = d.b * d.H * d.P * d.N / 4;   // N is a multiple of 16
+    const int64_t blocks = std::min<int64_t>((total4 + kThreads - 1) / kThreads, 152 * 16);
+    bwd_state_pass_rev<<<(unsigned)blocks, kThreads, 0, st>>>(
+        reinterpret_cast<float4*>(a.Gn), a.cum2, reinterpret_cast<const float4*>(dfinal),
+        reinterpret_cast<float4*>(dinit), total4, (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L,
+        (int)d.nc);
     bwd_pair_tiles<TI><<<(unsigned)g3, kThreads, 0, st>>>(a);
     bwd_head<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_group_bc<TI><<<dim3((unsigned)g5, 2), kThreads, 0, st>>>(a);
@@ -660,9 +768,12 @@ cudaError_t launch_backward(const Dims& d, const void* x, const void* B, const v
                             float* dC, float* dD, float* dinit, cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     if (d.L > 256 || d.P > 2 * kT) return cudaErrorInvalidValue;   // bwd_head's token / p tiles
+    int lp = 0;
+    while ((int64_t(1) << lp) < d.P) ++lp;
+    if ((int64_t(1) << lp) != d.P) return cudaErrorInvalidValue;   // P is a power of two
     BwdArgs a{x,   B,   C,  dy, A,  D,  cum2, dtT, Sprev, Gn,         CB,         SdCB,
               dx,  ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
-              (int)d.L, (int)d.nc};
+              (int)d.L, (int)d.nc, lp};
     return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, dfinal, dinit, st)
                         : launch_t<float>(d, a, dfinal, dinit, st);
 }
