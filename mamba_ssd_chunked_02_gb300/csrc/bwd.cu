@@ -413,8 +413,10 @@ __global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
 }
 
 // --- Per (b, c, h): dx, ddt and the dA, dD partial sums.  Grid: b*nc*H.
-template <typename TI>
-__global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
+// Three CTAs per SM for P <= 64 (80 registers), two for P = 128: the kernel is
+// bound by load latency, so resident warps matter more than registers.
+template <typename TI, int NPT>   // NPT = ceil(P / 64) p tiles
+__global__ void __launch_bounds__(kThreads, NPT == 1 ? 3 : 2) bwd_head(BwdArgs a) {
     __shared__ MMSmem sm;
     __shared__ float Mt[kT][kT + 1];
     __shared__ float s_c2[256], s_dt[256], s_dcum[256], s_ddt[256], s_xgb[256];
@@ -452,13 +454,24 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
     const float* Gn = a.Gn + soff;
     const float* CB = a.CB + (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)L * L;
     float* dx = a.dx + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-    const int ntile = (Lc + kT - 1) / kT, npt = (P + kT - 1) / kT;
+    const int ntile = (Lc + kT - 1) / kT;
 
     for (int tj = 0; tj < ntile; ++tj) {
-        float accx[2][4][4];
-        zero(accx[0]);
-        zero(accx[1]);
+        float accx[NPT][4][4];
+#pragma unroll
+        for (int pt = 0; pt < NPT; ++pt) zero(accx[pt]);
         for (int ti = tj; ti < ntile; ++ti) {
+            // C.B^T of the tile pair: loads issued here, used after dy.x^T.
+            float cbv[4][4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = ti * kT + 4 * ty + r;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = tj * kT + 4 * tx + q;
+                    cbv[r][q] = (i < Lc && j <= i) ? CB[(int64_t)i * L + j] : 0.f;
+                }
+            }
             float dxa[4][4];
             zero(dxa);
             mm_tile<true, true>(
@@ -480,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
                     const int jl = 4 * tx + q, j = tj * kT + jl;
                     float m = 0.f;
                     if (i < Lc && j <= i) {
-                        const float base = CB[(int64_t)i * L + j] * ex2(s_c2[i] - s_c2[j]);
+                        const float base = cbv[r][q] * ex2(s_c2[i] - s_c2[j]);
                         const float qv = base * dxa[r][q];
                         m = base * s_dt[j];
                         rowq[r] = fmaf(qv, s_dt[j], rowq[r]);
@@ -489,10 +502,13 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
                     Mt[il][jl] = m;
                 }
             }
+            // Row sums: the 16 threads of a row (tx) are 16 lanes of one warp.
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) rowq[r] += __shfl_xor_sync(0xffffffffu, rowq[r], o);
                 const int i = ti * kT + 4 * ty + r;
-                if (i < Lc) atomicAdd(&s_dcum[i], rowq[r]);
+                if (tx == 0 && i < Lc) atomicAdd(&s_dcum[i], rowq[r]);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -504,8 +520,7 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
             }
             __syncthreads();   // Mt complete
 #pragma unroll
-            for (int pt = 0; pt < 2; ++pt)
-                if (pt < npt)
+            for (int pt = 0; pt < NPT; ++pt)
                     mm_tile<false, false>(
                     accx[pt], sm, 0, kT, [&](int m, int k) { return Mt[k][m]; },
                     [&](int k, int n) {
@@ -515,8 +530,7 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
         }
         // dx_j = (M^T dy)_j + w_j Gn B_j + D dy_j; x_j . (Gn B_j) for ddt and dcum.
 #pragma unroll
-        for (int pt = 0; pt < 2; ++pt) {
-            if (pt >= npt) break;
+        for (int pt = 0; pt < NPT; ++pt) {
             float gb[4][4];
             zero(gb);
             mm_tile<true, true>(
@@ -550,7 +564,8 @@ __global__ void __launch_bounds__(kThreads) bwd_head(BwdArgs a) {
     }
     // dcum_i += e_i dy_i . (Sprev C_i)
     for (int ti = 0; ti < ntile; ++ti) {
-        for (int pt = 0; pt < npt; ++pt) {
+#pragma unroll
+        for (int pt = 0; pt < NPT; ++pt) {
             float yo[4][4];
             zero(yo);
             mm_tile<true, true>(
@@ -754,7 +769,10 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const float* dfinal, float
         reinterpret_cast<float4*>(dinit), total4, (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L,
         (int)d.nc);
     bwd_pair_tiles<TI><<<(unsigned)g3, kThreads, 0, st>>>(a);
-    bwd_head<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
+    if (npt == 1)
+        bwd_head<TI, 1><<<(unsigned)g4, kThreads, 0, st>>>(a);
+    else
+        bwd_head<TI, 2><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_group_bc<TI><<<dim3((unsigned)g5, 2), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
