@@ -24,6 +24,12 @@ region, and the fp64 oracle timed on the host cores on a bounded sample.
 --impl reference times the oracle (the reference arm of this method: a plain
 CPU fp64 recurrence) on the same workload, metric and unit.
 
+Other modes (one JSON line each, not the step above): --decode times the
+single-token decode step on the workload's state (a CUDA graph of 8 steps);
+--backward times mamba2_ssd_bwd on the workload; --all-configs prints the
+whole-path forward on every measured workload (median per-call device time,
+L2 flushed between calls where the inputs fit in it).
+
 Multi-GPU (torchrun, N > 1): each rank runs its own batch of the workload
 (independent (b, h) problems, no collective on the data path): weak scaling.
 """
@@ -63,6 +69,10 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time the single-token decode step on the workload's state instead")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="print one JSON line per measured workload (forward whole path): "
+                         "median per-call device time, L2 flushed between calls when the "
+                         "inputs fit in it")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (mamba2_ssd_bwd) on the workload instead")
     ap.add_argument("--fused-state", action="store_true",
@@ -355,6 +365,62 @@ def run_decode(args, w):
         "gpu_launches": K, "clocks": clk}), flush=True)
 
 
+def run_all_configs(args):
+    """Every measured workload through mamba2_ssd_fwd: each call timed alone with
+    CUDA events on the launching stream; when the workload's inputs and outputs
+    fit in L2 twice over, a 512 MB buffer is written between calls (outside the
+    timed region), so every call starts with cold inputs."""
+    import torch
+    import mamba_ssd_chunked_02_gb300 as m2
+    from mamba_ssd_chunked_02_gb300 import workloads as W
+    pk, src = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for w in W.ALL:
+        inp = W.make_inputs(w)
+        dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+        sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
+        ws = torch.empty(max(1, m2.workspace_size(sh)), dtype=torch.uint8, device="cuda")
+        y = torch.empty_like(dev["x"])
+        fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device="cuda")
+        E = 2 if w.dtype == "bf16" else 4
+        io = (2 * w.batch * w.seqlen * w.nheads * w.headdim + 2 * w.batch * w.seqlen * w.ngroups *
+              w.dstate) * E
+        cold = io < 2 * (129 << 20)
+
+        def call():
+            m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                       dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups, y=y,
+                       final_state=fin, workspace=ws)
+
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(5, min(args.steps, 50))):
+            if cold:
+                flush.fill_(1)
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            z.record(stream)
+            z.synchronize()
+            ts.append(a.elapsed_time(z))
+        if m2.device_error() != 0:
+            raise RuntimeError(f"device-side error on {w.name}")
+        ms = sorted(ts)[len(ts) // 2]
+        _, graded, flops = model(w)
+        t_path = max(graded / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+        print(json.dumps({"workload": w.name, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
+                          "tflops": flops / (ms * 1e-3) / 1e12, "path_roofline_ms": t_path * 1e3,
+                          "path_frac": t_path / (ms * 1e-3), "peaks": src,
+                          "path": "tcgen05" if m2.path(sh) == m2.PATH_TCGEN05 else "simt",
+                          "l2": "flushed between calls" if cold else "inputs larger than L2",
+                          "calls": len(ts)}), flush=True)
+        del dev, ws, y, fin
+        torch.cuda.empty_cache()
+
+
 def bwd_flops(w):
     """Contraction work of one backward call as the kernels do it (causal halves of
     the L x L products, forward recompute of the chunk states included):
@@ -448,6 +514,10 @@ def main():
     if args.backward:
         if rank == 0:
             run_backward(args, w)
+        return
+    if args.all_configs:
+        if rank == 0:
+            run_all_configs(args)
         return
     dist = None
     if world > 1:
