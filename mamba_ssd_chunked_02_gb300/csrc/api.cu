@@ -129,25 +129,39 @@ Carve carve(const Dims& d) {
     return c;
 }
 
-// Workspace of the backward pass: the forward's cum2, dtT, dS (fp32; reused
-// for the chunk adjoints dSout / Gn), an fp32 Sprev, C.B^T and the head-summed
-// dCB per (b, chunk, group), and a final-state scratch.
+// Workspace of the backward pass: the forward's cum2, dtT, dS (fp32; reused for
+// the chunk adjoints dSout / Gn), Sprev in the I/O type, C.B^T and the
+// head-summed dCB per (b, chunk, group), the final state, an I/O-type copy of
+// Gn, y without the skip term and the reversed run's output y' (both fp32), and
+// the reversed run's inputs (dy, B, C, cum2', dt' = 1).
 struct BwdCarve {
-    size_t cum2, dtT, dS, Sprev, CB, SdCB, fin, total;
+    size_t cum2, dtT, dS, Sprev, CB, SdCB, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, total;
 };
 
 BwdCarve bwd_carve(const Dims& d) {
     BwdCarve c;
-    const size_t st = align256(sizeof(float) * (size_t)m2::n_state(d));
+    const size_t E = (size_t)m2::esize(d);
+    const size_t cum = align256(sizeof(float) * (size_t)m2::n_cum(d));
     const size_t tile = align256(sizeof(float) * (size_t)(d.b * d.nc * d.G * d.L * d.L));
+    const size_t xy = align256(E * (size_t)(d.b * d.T * d.H * d.P));
+    const size_t bc = align256(E * (size_t)(d.b * d.T * d.G * d.N));
     c.cum2 = 0;
-    c.dtT = c.cum2 + align256(sizeof(float) * (size_t)m2::n_cum(d));
-    c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
-    c.Sprev = c.dS + st;
-    c.CB = c.Sprev + st;
+    c.dtT = c.cum2 + cum;
+    c.dS = c.dtT + cum;
+    c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
+    c.CB = c.Sprev + align256(E * (size_t)m2::n_state(d));
     c.SdCB = c.CB + tile;
     c.fin = c.SdCB + tile;
-    c.total = c.fin + align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
+    c.GnIO = c.fin + align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
+    c.yno = c.GnIO + align256(E * (size_t)m2::n_state(d));
+    const size_t xy32 = align256(sizeof(float) * (size_t)(d.b * d.T * d.H * d.P));
+    c.yr = c.yno + xy32;
+    c.dyr = c.yr + xy32;
+    c.Br = c.dyr + xy;
+    c.Cr = c.Br + bc;
+    c.cum2r = c.Cr + bc;
+    c.ones = c.cum2r + cum;
+    c.total = c.ones + cum;
     return c;
 }
 
@@ -437,24 +451,32 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     float* cum2 = reinterpret_cast<float*>(ws + cv.cum2);
     float* dtT = reinterpret_cast<float*>(ws + cv.dtT);
     float* dS = reinterpret_cast<float*>(ws + cv.dS);
-    float* Sprev = reinterpret_cast<float*>(ws + cv.Sprev);
+    void* Sprev = ws + cv.Sprev;
+    float* fin = reinterpret_cast<float*>(ws + cv.fin);
     int32_t* err = error_word();
-    // Forward stages 1-3: cum2, dtT, dS (fp32) and the fp32 state entering each chunk.
+    // Forward stages 1-3: cum2, dtT, dS (fp32), the state entering each chunk (in
+    // the I/O type, stage 4's operand) and the final state.
     const bool tc = use_tc(shape, d);
     e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, false, err, s)
                : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
-    Dims d32 = d;
-    d32.dtype = 0;   // Sprev in fp32
     if (e == cudaSuccess)
-        e = m2::launch_state_pass(d32, dS, false, cum2, initial_state, Sprev,
-                                  reinterpret_cast<float*>(ws + cv.fin), err, s);
+        e = m2::launch_state_pass(d, dS, false, cum2, initial_state, Sprev, fin, err, s);
+    m2::BwdWork w{dS,
+                  ws + cv.GnIO,
+                  ws + cv.yno,
+                  ws + cv.yr,
+                  reinterpret_cast<float*>(ws + cv.CB),
+                  reinterpret_cast<float*>(ws + cv.SdCB),
+                  ws + cv.dyr,
+                  ws + cv.Br,
+                  ws + cv.Cr,
+                  reinterpret_cast<float*>(ws + cv.cum2r),
+                  reinterpret_cast<float*>(ws + cv.ones)};
     if (e == cudaSuccess)
-        e = m2::launch_backward(d, x, B, C, dy, A, D, cum2, dtT, Sprev, dS,
-                                reinterpret_cast<float*>(ws + cv.CB),
-                                reinterpret_cast<float*>(ws + cv.SdCB), dfinal_state, dx, ddt, dA,
-                                dB, dC, dD, dinitial_state, s);
+        e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
+                                dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);
     return from_cuda(e);
 }
 

@@ -12,35 +12,44 @@
 // Notation for one (b, h) and chunk c with Lc tokens i, j (chunk-local), the
 // forward's log2-scaled chunk-local cumsum c2_i, e_i = exp2(c2_i), the chunk
 // decay E = exp2(c2_last), w_j = dt_j exp2(c2_last - c2_j), the state entering
-// the chunk Sprev (P x N) and the adjoint of the state leaving it Gn (P x N):
+// the chunk Sprev, the state leaving it S_after, and Gn, the adjoint of S_after:
 //
 //   forward:  y_i = sum_{j<=i} CB_ij exp2(c2_i - c2_j) dt_j x_j + e_i Sprev C_i + D x_i
-//             S_next = E Sprev + sum_j w_j x_j B_j^T
+//             S_after = E Sprev + sum_j w_j x_j B_j^T
 //   adjoint of the state entering chunk c (reverse pass over chunks):
 //             dSprev_c = sum_i e_i dy_i C_i^T + E_c dSprev_{c+1},  dSprev_nc = dfinal
 //             Gn_c = dSprev_{c+1},  dinitial_state = dSprev_0
-//   with DX_ij = dy_i . x_j and Q_ij = CB_ij exp2(c2_i - c2_j) DX_ij (j <= i):
-//     dx_j   = sum_{i>=j} CB_ij exp2(c2_i - c2_j) dt_j dy_i + w_j Gn B_j + D dy_j
-//     ddt_j  = sum_i Q_ij + exp2(c2_last - c2_j) x_j.(Gn B_j) + A sum_{i>=j} dcum_i
-//     dcum_i = sum_j Q_ij dt_j - dt_i sum_k Q_ki + e_i dy_i.(Sprev C_i) - w_i x_i.(Gn B_i)
-//              + [i = last] (sum_j w_j x_j.(Gn B_j) + E <Gn, Sprev>)
+//   dx and the decay terms come from the forward's own output kernel run
+//   backwards in time: with the tokens of each chunk reversed, B and C swapped,
+//   dt' = 1, cum2' = c2_last - c2 and Gn as the carried state, stage 4 computes
+//             y'_j = sum_{i>=j} (B_j.C_i) exp2(c2_i - c2_j) dy_i + exp2(c2_last - c2_j) Gn B_j
+//   and then
+//     dx_j   = dt_j y'_j + D dy_j
+//     ddt_j  = x_j.y'_j + A sum_{i>=j} dcum_i
+//     dcum_i = dy_i.(y_i - D x_i) - dt_i x_i.y'_i + [i = last] <Gn, S_after>
 //     dA     = sum over (b, chunks, j) of dt_j sum_{i>=j} dcum_i
 //     dD     = sum over (b, t) of dy . x
-//   and, summed over the heads of the group (dCB_ij = exp2(c2_i - c2_j) dt_j DX_ij):
+//   (dcum is the gradient with respect to the natural-log cumsum, cum_t = A sum dt:
+//   the row and column sums of dCB (.) CB (.) decay collapse into the two dots.)
+//   The group gradients, summed over the group's heads with
+//   dCB_ij = exp2(c2_i - c2_j) dt_j (dy_i . x_j):
 //     dC_i   = sum_{j<=i} (sum_h dCB_ij) B_j + sum_h e_i Sprev^T dy_i
 //     dB_j   = sum_{i>=j} (sum_h dCB_ij) C_i + sum_h w_j Gn^T x_j
-// (dcum is the gradient with respect to the natural-log cumsum; cum_t = A sum dt.)
 //
-// Kernels (after the forward's stages 1-3 recompute cum2, dtT and an fp32 Sprev):
+// Kernels, after the forward's stages 1-4 recompute cum2, dtT, Sprev, S_after
+// and y without the skip term:
 //   bwd_chunk_adjoint   sum_i e_i dy_i C_i^T per (b, c, h)            -> dSout
 //   bwd_state_pass_rev  reverse pass over chunks, in place            -> Gn, dinit
+//   bwd_reverse         dy, B, C with each chunk's tokens reversed; cum2', dt' = 1
+//   (stage 4)           y' from the reversed inputs (tensor cores where the
+//                       forward uses them)
+//   bwd_token           per (b, c, h): dx, ddt, and dA, dD partial sums
 //   bwd_pair_tiles      per (b, c, g) and 64x64 tile pair (j <= i): CB and
-//                       sum_h dCB (the head loop inside the CTA)       -> CB, SdCB
-//   bwd_head            per (b, c, h): dx, ddt, and dA, dD partial sums
+//                       sum_h dCB                                       -> CB, SdCB
 //   bwd_group_bc        per (b, c, g), 64-token tile, 64-column tile: dC or dB,
 //                       one GEMM over the chunk's tokens and one over (head, p)
-// Every contraction goes through mm_tile, a 64x64 fp32 tile on 256 threads
-// (4x4 outputs each) with operands staged through shared memory 16 k at a time.
+// The contractions of the last two go through mm_tile, a 64x64 fp32 tile on 256
+// threads (4x4 outputs each) with operands staged through shared memory.
 #include <algorithm>
 
 #include "common.cuh"
@@ -171,8 +180,12 @@ struct BwdArgs {
     const float* D;     // [H] or null
     const float* cum2;  // [b,H,T]
     const float* dtT;   // [b,H,T]
-    const float* Sprev; // [b,nc,H,P,N] fp32
+    const void* Sprev;  // [b,nc,H,P,N] TI (the state entering each chunk)
+    const float* fin;   // [b,H,P,N] fp32 (the final state)
     float* Gn;          // [b,nc,H,P,N] fp32: dSout, then Gn
+    void* GnIO;         // [b,nc,H,P,N] TI copy of Gn (stage 4's carried-state operand)
+    const float* yno;   // [b,T,H,P] fp32: y without the skip term
+    const float* yr;    // [b,T,H,P] fp32: y' with each chunk's tokens reversed
     float* CB;          // [b,nc,G,L,L] fp32
     float* SdCB;        // [b,nc,G,L,L] fp32
     float* dx;          // [b,T,H,P]
@@ -233,11 +246,13 @@ __global__ void __launch_bounds__(kThreads) bwd_chunk_adjoint(BwdArgs a) {
 }
 
 // --- Reverse pass over chunks, in place: buf[c] holds dSout_c on entry and
-// Gn_c = dSprev_{c+1} on exit; dinit = dSprev_0.  One thread per (b, h) and
-// four consecutive (p, n); the loads of four chunks are issued before their
-// values are used (the chain through the chunks is the only dependence).
+// Gn_c = dSprev_{c+1} on exit (and in the I/O type in gio, unless TI is fp32);
+// dinit = dSprev_0.  One thread per (b, h) and four consecutive (p, n); the
+// loads of four chunks are issued before their values are used (the chain
+// through the chunks is the only dependence).
+template <typename TI>
 __global__ void __launch_bounds__(kThreads)
-bwd_state_pass_rev(float4* __restrict__ buf, const float* __restrict__ cum2,
+bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* __restrict__ cum2,
                    const float4* __restrict__ dfinal, float4* __restrict__ dinit, int64_t total4,
                    int H, int64_t PN4, int T, int L, int nc) {
     constexpr int kU = 4;
@@ -262,7 +277,15 @@ bwd_state_pass_rev(float4* __restrict__ buf, const float* __restrict__ cum2,
             for (int u = 0; u < kU; ++u) {
                 const int c = c0 - u;
                 if (c >= 0) {
-                    buf[((b * nc + c) * H + h) * PN4 + k] = gv;
+                    const int64_t o = ((b * nc + c) * H + h) * PN4 + k;
+                    buf[o] = gv;
+                    if constexpr (sizeof(TI) == 2) {
+                        TI* q = gio + 4 * o;
+                        q[0] = from_f32<TI>(gv.x);
+                        q[1] = from_f32<TI>(gv.y);
+                        q[2] = from_f32<TI>(gv.z);
+                        q[3] = from_f32<TI>(gv.w);
+                    }
                     gv.x = fmaf(dec[u], gv.x, v[u].x);
                     gv.y = fmaf(dec[u], gv.y, v[u].y);
                     gv.z = fmaf(dec[u], gv.z, v[u].z);
@@ -271,6 +294,37 @@ bwd_state_pass_rev(float4* __restrict__ buf, const float* __restrict__ cum2,
             }
         }
         if (dinit) dinit[idx] = gv;
+    }
+}
+
+// --- Stage 4's inputs for y': token k of chunk c (Lc tokens) goes to position
+// Lc-1-k of the same chunk; x' = dy, B' = C, C' = B; cum2'[k'] = c2_last - c2[Lc-1-k'];
+// dt' = 1.  One CTA per (token, b).
+template <typename TI>
+__global__ void __launch_bounds__(kThreads)
+bwd_reverse(const TI* __restrict__ dy, const TI* __restrict__ B, const TI* __restrict__ C,
+            const float* __restrict__ cum2, TI* __restrict__ dyr, TI* __restrict__ Br,
+            TI* __restrict__ Cr, float* __restrict__ cum2r, float* __restrict__ ones, int T, int H,
+            int64_t rowx, int64_t rowbc, int L) {
+    const int t = blockIdx.x, b = blockIdx.y;
+    const int c = t / L, k = t - c * L;
+    const int Lc = min(L, T - c * L);
+    const int ts = c * L + (Lc - 1 - k);   // the source token
+    // Rows are 16-byte multiples (P, N >= 16 elements) at 16-byte aligned starts.
+    auto copy = [&](const TI* src, TI* dst, int64_t row) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + ((int64_t)b * T + ts) * row);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + ((int64_t)b * T + t) * row);
+        const int64_t n = row * (int64_t)sizeof(TI) / 16;
+        for (int64_t i = threadIdx.x; i < n; i += kThreads) d4[i] = s4[i];
+    };
+    copy(dy, dyr, rowx);
+    copy(C, Br, rowbc);
+    copy(B, Cr, rowbc);
+    for (int h = threadIdx.x; h < H; h += kThreads) {
+        const float* c2 = cum2 + ((int64_t)b * H + h) * T;
+        const int64_t o = ((int64_t)b * H + h) * T + t;
+        cum2r[o] = c2[c * L + Lc - 1] - c2[ts];
+        ones[o] = 1.f;
     }
 }
 
@@ -412,213 +466,78 @@ __global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
     }
 }
 
-// --- Per (b, c, h): dx, ddt and the dA, dD partial sums.  Grid: b*nc*H.
-// Three CTAs per SM for P <= 64 (80 registers), two for P = 128: the kernel is
-// bound by load latency, so resident warps matter more than registers.
-template <typename TI, int NPT>   // NPT = ceil(P / 64) p tiles
-__global__ void __launch_bounds__(kThreads, NPT == 1 ? 3 : 2) bwd_head(BwdArgs a) {
-    __shared__ MMSmem sm;
-    __shared__ float Mt[kT][kT + 1];
-    __shared__ float s_c2[256], s_dt[256], s_dcum[256], s_ddt[256], s_xgb[256];
+// --- Per (b, c, h): dx, ddt and the dA, dD partial sums from y' (reversed) and
+// y without the skip term.  A warp per token, lanes over p.  Grid: b*nc*H.
+template <typename TI>
+__global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
+    __shared__ float s_dt[256], s_dcum[256], s_ddt[256];
     __shared__ float red[kThreads / 32];
     int id = blockIdx.x;
     const int h = id % a.H; id /= a.H;
     const int c = id % a.nc, b = id / a.nc;
-    const int g = h / (a.H / a.G);
     const int P = a.P, N = a.N, L = a.L;
     const int64_t t0 = (int64_t)c * L;
     const int Lc = (int)min((int64_t)L, a.T - t0);
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t PN = (int64_t)P * N;
+    // <Gn_c, S_after_c>: S_after is the next chunk's Sprev, or the final state.
+    float gs = 0.f;
     {
-        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
-        const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
-        for (int i = tid; i < 256; i += kThreads) {
-            s_c2[i] = i < Lc ? c2[i] : 0.f;
-            s_dt[i] = i < Lc ? dth[i] : 0.f;
-            s_dcum[i] = 0.f;
-            s_ddt[i] = 0.f;
-            s_xgb[i] = 0.f;
+        const float* Gn = a.Gn + (((int64_t)b * a.nc + c) * a.H + h) * PN;
+        if (c + 1 < a.nc) {
+            const TI* Sa = static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN;
+            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(Gn[k], to_f32(Sa[k]), gs);
+        } else {
+            const float* Sa = a.fin + ((int64_t)b * a.H + h) * PN;
+            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(Gn[k], Sa[k], gs);
         }
     }
+    const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
+    for (int i = tid; i < 256; i += kThreads) s_dt[i] = i < Lc ? dth[i] : 0.f;
     __syncthreads();
-    const float c2last = s_c2[Lc - 1];
-    const float Ah = a.A[h];
     const float Dh = a.D ? a.D[h] : 0.f;
-    const int64_t sxy = (int64_t)a.H * P, sBC = (int64_t)a.G * N;
-    const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-    const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
-    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
-    const int64_t soff = (((int64_t)b * a.nc + c) * a.H + h) * (int64_t)P * N;
-    const float* Sp = a.Sprev + soff;
-    const float* Gn = a.Gn + soff;
-    const float* CB = a.CB + (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)L * L;
-    float* dx = a.dx + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-    const int ntile = (Lc + kT - 1) / kT;
-
-    for (int tj = 0; tj < ntile; ++tj) {
-        float accx[NPT][4][4];
-#pragma unroll
-        for (int pt = 0; pt < NPT; ++pt) zero(accx[pt]);
-        for (int ti = tj; ti < ntile; ++ti) {
-            // C.B^T of the tile pair: loads issued here, used after dy.x^T.
-            float cbv[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = ti * kT + 4 * ty + r;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = tj * kT + 4 * tx + q;
-                    cbv[r][q] = (i < Lc && j <= i) ? CB[(int64_t)i * L + j] : 0.f;
-                }
-            }
-            float dxa[4][4];
-            zero(dxa);
-            mm_tile<true, true>(
-                dxa, sm, 0, P,
-                [&](int m, int k) {
-                    const int i = ti * kT + m;
-                    return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int j = tj * kT + n;
-                    return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
-                });
-            float rowq[4] = {0.f, 0.f, 0.f, 0.f}, colq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int il = 4 * ty + r, i = ti * kT + il;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int jl = 4 * tx + q, j = tj * kT + jl;
-                    float m = 0.f;
-                    if (i < Lc && j <= i) {
-                        const float base = cbv[r][q] * ex2(s_c2[i] - s_c2[j]);
-                        const float qv = base * dxa[r][q];
-                        m = base * s_dt[j];
-                        rowq[r] = fmaf(qv, s_dt[j], rowq[r]);
-                        colq[q] += qv;
-                    }
-                    Mt[il][jl] = m;
-                }
-            }
-            // Row sums: the 16 threads of a row (tx) are 16 lanes of one warp.
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) rowq[r] += __shfl_xor_sync(0xffffffffu, rowq[r], o);
-                const int i = ti * kT + 4 * ty + r;
-                if (tx == 0 && i < Lc) atomicAdd(&s_dcum[i], rowq[r]);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = tj * kT + 4 * tx + q;
-                if (j < Lc) {
-                    atomicAdd(&s_ddt[j], colq[q]);
-                    atomicAdd(&s_dcum[j], -colq[q] * s_dt[j]);
-                }
-            }
-            __syncthreads();   // Mt complete
-#pragma unroll
-            for (int pt = 0; pt < NPT; ++pt)
-                    mm_tile<false, false>(
-                    accx[pt], sm, 0, kT, [&](int m, int k) { return Mt[k][m]; },
-                    [&](int k, int n) {
-                        const int i = ti * kT + k, p = pt * kT + n;
-                        return (i < Lc && p < P) ? to_f32(dy[i * sxy + p]) : 0.f;
-                    });
+    const int64_t sxy = (int64_t)a.H * P;
+    const int64_t base = ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
+    const TI* x = static_cast<const TI*>(a.x) + base;
+    const TI* dy = static_cast<const TI*>(a.dy) + base;
+    const float* yno = a.yno + base;
+    const float* yr = a.yr + base;
+    float* dx = a.dx + base;
+    float yx = 0.f;
+    for (int j = warp; j < Lc; j += kThreads / 32) {
+        const int jr = Lc - 1 - j;   // where the reversed run wrote token j
+        const float dtj = s_dt[j];
+        float xy = 0.f, dyy = 0.f, dyx = 0.f;
+        for (int p = lane; p < P; p += 32) {
+            const float yp = yr[jr * sxy + p];
+            const float xv = to_f32(x[j * sxy + p]);
+            const float dv = to_f32(dy[j * sxy + p]);
+            dx[j * sxy + p] = fmaf(dtj, yp, Dh * dv);
+            xy = fmaf(xv, yp, xy);
+            dyy = fmaf(dv, yno[j * sxy + p], dyy);
+            dyx = fmaf(dv, xv, dyx);
         }
-        // dx_j = (M^T dy)_j + w_j Gn B_j + D dy_j; x_j . (Gn B_j) for ddt and dcum.
 #pragma unroll
-        for (int pt = 0; pt < NPT; ++pt) {
-            float gb[4][4];
-            zero(gb);
-            mm_tile<true, true>(
-                gb, sm, 0, N,
-                [&](int m, int k) {
-                    const int j = tj * kT + m;
-                    return j < Lc ? to_f32(Bg[j * sBC + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int p = pt * kT + n;
-                    return p < P ? Gn[(int64_t)p * N + k] : 0.f;
-                });
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int j = tj * kT + 4 * ty + r;
-                if (j >= Lc) continue;
-                const float wj = s_dt[j] * ex2(c2last - s_c2[j]);
-                float xg = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int p = pt * kT + 4 * tx + q;
-                    if (p < P) {
-                        const float dyv = to_f32(dy[j * sxy + p]);
-                        dx[j * sxy + p] = accx[pt][r][q] + wj * gb[r][q] + Dh * dyv;
-                        xg = fmaf(to_f32(x[j * sxy + p]), gb[r][q], xg);
-                    }
-                }
-                atomicAdd(&s_xgb[j], xg);
-            }
+        for (int o = 16; o > 0; o >>= 1) {
+            xy += __shfl_xor_sync(0xffffffffu, xy, o);
+            dyy += __shfl_xor_sync(0xffffffffu, dyy, o);
+            dyx += __shfl_xor_sync(0xffffffffu, dyx, o);
         }
-    }
-    // dcum_i += e_i dy_i . (Sprev C_i)
-    for (int ti = 0; ti < ntile; ++ti) {
-#pragma unroll
-        for (int pt = 0; pt < NPT; ++pt) {
-            float yo[4][4];
-            zero(yo);
-            mm_tile<true, true>(
-                yo, sm, 0, N,
-                [&](int m, int k) {
-                    const int i = ti * kT + m;
-                    return i < Lc ? to_f32(Cg[i * sBC + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int p = pt * kT + n;
-                    return p < P ? Sp[(int64_t)p * N + k] : 0.f;
-                });
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = ti * kT + 4 * ty + r;
-                if (i >= Lc) continue;
-                float s = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int p = pt * kT + 4 * tx + q;
-                    if (p < P) s = fmaf(to_f32(dy[i * sxy + p]), yo[r][q], s);
-                }
-                atomicAdd(&s_dcum[i], ex2(s_c2[i]) * s);
-            }
+        if (lane == 0) {
+            s_ddt[j] = xy;
+            s_dcum[j] = dyy - dtj * xy;
+            yx += dyx;
         }
-    }
-    // <Gn, Sprev> and sum dy . x over the chunk.
-    float gs = 0.f, yx = 0.f;
-    for (int64_t k = tid; k < (int64_t)P * N; k += kThreads) gs = fmaf(Gn[k], Sp[k], gs);
-    for (int k = tid; k < Lc * P; k += kThreads) {
-        const int i = k / P, p = k % P;
-        yx = fmaf(to_f32(dy[i * sxy + p]), to_f32(x[i * sxy + p]), yx);
     }
     gs = block_sum(gs, red);
-    yx = block_sum(yx, red);
-    __syncthreads();   // every s_xgb / s_dcum / s_ddt update is in
-    // Per token j (one thread each): the state-side terms of ddt and dcum.
-    const int j = tid;
-    float wxg = 0.f;
-    if (j < Lc) {
-        const float ed = ex2(c2last - s_c2[j]);
-        const float xg = s_xgb[j];
-        s_ddt[j] = fmaf(ed, xg, s_ddt[j]);
-        wxg = s_dt[j] * ed * xg;
-        s_dcum[j] -= wxg;
-    }
-    const float W = block_sum(wxg, red);
-    if (tid == 0) s_dcum[Lc - 1] += W + ex2(c2last) * gs;
+    yx = block_sum(yx, red);   // (its barriers also publish s_ddt / s_dcum)
+    if (tid == 0) s_dcum[Lc - 1] += gs;
     __syncthreads();
+    const int j = tid;
     const float rcs = block_suffix_sum(j < Lc ? s_dcum[j] : 0.f, red);
     float da = 0.f;
     if (j < Lc) {
-        a.ddt[((int64_t)b * a.T + t0 + j) * a.H + h] = fmaf(Ah, rcs, s_ddt[j]);
+        a.ddt[((int64_t)b * a.T + t0 + j) * a.H + h] = fmaf(a.A[h], rcs, s_ddt[j]);
         da = s_dt[j] * rcs;
     }
     da = block_sum(da, red);
@@ -674,7 +593,7 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
                 const int nn = nt * kT + n;
                 return nn < N ? to_f32(Bg[k * sBC + nn]) : 0.f;
             });
-        const float* Sp = a.Sprev + soff;
+        const TI* Sp = static_cast<const TI*>(a.Sprev) + soff;
         for (int hb = 0; hb < hpg; hb += kHB) {
             const int nh = min(kHB, hpg - hb);
             for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
@@ -683,7 +602,7 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
             }
             __syncthreads();
             const TI* dyb = dyg + (int64_t)hb * P;
-            const float* Spb = Sp + (int64_t)hb * P * N;
+            const TI* Spb = Sp + (int64_t)hb * P * N;
             mm_tile<true, false>(
                 acc, sm, 0, nh * P,
                 [&](int m, int k) {
@@ -692,7 +611,7 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
                 },
                 [&](int k, int n) {
                     const int nn = nt * kT + n;
-                    return nn < N ? Spb[(int64_t)k * N + nn] : 0.f;
+                    return nn < N ? to_f32(Spb[(int64_t)k * N + nn]) : 0.f;
                 });
         }
     } else {
@@ -749,8 +668,8 @@ __global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
 }
 
 template <typename TI>
-cudaError_t launch_t(const Dims& d, const BwdArgs& a, const float* dfinal, float* dinit,
-                     cudaStream_t st) {
+cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
+                     const float* dfinal, float* dinit, int32_t* err, cudaStream_t st) {
     const int64_t bnc = d.b * d.nc;
     const int npt = (int)((d.P + kT - 1) / kT), nnt = (int)((d.N + kT - 1) / kT);
     const int ntl = (int)((d.L + kT - 1) / kT);
@@ -759,41 +678,64 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const float* dfinal, float
     const int64_t g4 = bnc * d.H;
     const int64_t g5 = bnc * d.G * ntl * nnt;
     if (g1 >= (int64_t(1) << 31) || g3 >= (int64_t(1) << 31) || g4 >= (int64_t(1) << 31) ||
-        g5 >= (int64_t(1) << 31))
+        g5 >= (int64_t(1) << 31) || d.T >= (int64_t(1) << 31) || d.b >= 65536)
         return cudaErrorInvalidValue;
+    // Stage 4 with y in fp32 (tensor cores where the forward uses them; the
+    // CUDA-core kernel where that variant does not fit).
+    auto out4 = [&](const void* x4, const void* B4, const void* C4, const float* c4,
+                    const float* d4, const void* S4, const float* y4) {
+        float* yo = const_cast<float*>(y4);
+        if (tc) {
+            const cudaError_t r = launch_chunk_out_tc(d, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st,
+                                                      nullptr, false, true);
+            if (r != cudaErrorNotSupported) return r;
+        }
+        return launch_chunk_out_simt(d, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, true);
+    };
+    // y without the skip term.
+    cudaError_t e = out4(a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno);
+    if (e != cudaSuccess) return e;
     bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
     const int64_t total4 = d.b * d.H * d.P * d.N / 4;   // N is a multiple of 16
     const int64_t blocks = std::min<int64_t>((total4 + kThreads - 1) / kThreads, 152 * 16);
-    bwd_state_pass_rev<<<(unsigned)blocks, kThreads, 0, st>>>(
-        reinterpret_cast<float4*>(a.Gn), a.cum2, reinterpret_cast<const float4*>(dfinal),
-        reinterpret_cast<float4*>(dinit), total4, (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L,
-        (int)d.nc);
+    bwd_state_pass_rev<TI><<<(unsigned)blocks, kThreads, 0, st>>>(
+        reinterpret_cast<float4*>(a.Gn), static_cast<TI*>(a.GnIO), a.cum2,
+        reinterpret_cast<const float4*>(dfinal), reinterpret_cast<float4*>(dinit), total4,
+        (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc);
+    bwd_reverse<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
+        static_cast<const TI*>(a.dy), static_cast<const TI*>(a.B), static_cast<const TI*>(a.C),
+        a.cum2, static_cast<TI*>(w.dyr), static_cast<TI*>(w.Br), static_cast<TI*>(w.Cr), w.cum2r,
+        w.ones, (int)d.T, (int)d.H, d.H * d.P, d.G * d.N, (int)d.L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // y' = stage 4 on the reversed inputs: x' = dy, B' = C, C' = B, Gn carried.
+    const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
+    e = out4(w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr);
+    if (e != cudaSuccess) return e;
+    bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_pair_tiles<TI><<<(unsigned)g3, kThreads, 0, st>>>(a);
-    if (npt == 1)
-        bwd_head<TI, 1><<<(unsigned)g4, kThreads, 0, st>>>(a);
-    else
-        bwd_head<TI, 2><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_group_bc<TI><<<dim3((unsigned)g5, 2), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_backward(const Dims& d, const void* x, const void* B, const void* C,
+cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,
                             const void* dy, const float* A, const float* D, const float* cum2,
-                            const float* dtT, const float* Sprev, float* Gn, float* CB, float* SdCB,
-                            const float* dfinal, float* dx, float* ddt, float* dA, float* dB,
-                            float* dC, float* dD, float* dinit, cudaStream_t st) {
+                            const float* dtT, const void* Sprev, const float* fin,
+                            const BwdWork& w, const float* dfinal, float* dx, float* ddt,
+                            float* dA, float* dB, float* dC, float* dD, float* dinit,
+                            int32_t* err, cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
-    if (d.L > 256 || d.P > 2 * kT) return cudaErrorInvalidValue;   // bwd_head's token / p tiles
+    if (d.L > 256) return cudaErrorInvalidValue;   // bwd_token's tokens: one per thread
     int lp = 0;
     while ((int64_t(1) << lp) < d.P) ++lp;
     if ((int64_t(1) << lp) != d.P) return cudaErrorInvalidValue;   // P is a power of two
-    BwdArgs a{x,   B,   C,  dy, A,  D,  cum2, dtT, Sprev, Gn,         CB,         SdCB,
-              dx,  ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
+    BwdArgs a{x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w.Gn, w.GnIO,
+              static_cast<const float*>(w.yno), static_cast<const float*>(w.yr), w.CB, w.SdCB,
+              dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
               (int)d.L, (int)d.nc, lp};
-    return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, dfinal, dinit, st)
-                        : launch_t<float>(d, a, dfinal, dinit, st);
+    return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, w, tc, dfinal, dinit, err, st)
+                        : launch_t<float>(d, a, w, tc, dfinal, dinit, err, st);
 }
 
 }  // namespace m2

@@ -76,17 +76,22 @@ cudaError_t launch_state_pass(const Dims& d, const void* dS, bool ds16, const fl
                               int32_t* err, cudaStream_t st, bool pdl = false);
 
 // Stage 4: fused output.  CUDA-core variant.
+// y32: y is written in fp32 whatever the input type (the backward pass's use).
 cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, const void* C,
                                   const float* cum2, const float* dtT, const void* Sprev,
-                                  const float* D, void* y, int32_t* err, cudaStream_t st);
+                                  const float* D, void* y, int32_t* err, cudaStream_t st,
+                                  bool y32 = false);
 // Stage 4: tcgen05 variant; xabs: stage 2's max |x| words, or null (then the
 // kernel scans each x tile for its fp16 range check itself).
 // pdl: launched with programmatic dependent launch after stage 3 (the
 // whole-path call): everything but Sprev is read before stage 3 completes.
+// y32: y is written in fp32 (the backward pass's use); cudaErrorNotSupported
+// when that variant's staging does not fit in shared memory (L = 256, N = 256).
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st,
-                                const uint32_t* xabs = nullptr, bool pdl = false);
+                                const uint32_t* xabs = nullptr, bool pdl = false,
+                                bool y32 = false);
 
 // One recurrent step per (b, h): S <- exp(dt A) S + dt x B^T in place, y = S C + D x.
 // A bounded wait that runs out sets kErrTimeoutDecode in *err.
@@ -94,14 +99,29 @@ cudaError_t launch_decode(const Dims& d, float* S, const void* x, const float* d
                           const void* B, const void* C, const float* D, void* y, int32_t* err,
                           cudaStream_t st);
 
-// Backward pass after the forward's stages 1-3 (cum2, dtT, fp32 Sprev): Gn
-// [b,nc,H,P,N], CB and SdCB [b,nc,G,L,L] are fp32 scratch; dA and dD (if
-// given) are accumulated into (zero them first); dinit may be null.
-cudaError_t launch_backward(const Dims& d, const void* x, const void* B, const void* C,
+// Backward pass, after the forward's stages 1-3 (cum2, dtT, Sprev in the I/O
+// type, the final state in fp32).  Scratch, all in the workspace:
+struct BwdWork {
+    float* Gn;      // [b,nc,H,P,N] fp32 (chunk adjoints, then Gn)
+    void* GnIO;     // [b,nc,H,P,N] I/O type copy of Gn (unused when the I/O type is fp32)
+    void* yno;      // [b,T,H,P] fp32: y without the skip term
+    void* yr;       // [b,T,H,P] fp32: y' of the reversed run
+    float* CB;      // [b,nc,G,L,L]
+    float* SdCB;    // [b,nc,G,L,L]
+    void* dyr;      // [b,T,H,P] dy, each chunk's tokens reversed
+    void* Br;       // [b,T,G,N] C reversed (the reversed run's B)
+    void* Cr;       // [b,T,G,N] B reversed (the reversed run's C)
+    float* cum2r;   // [b,H,T]
+    float* ones;    // [b,H,T]
+};
+// tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
+// dA and dD (if given) are accumulated into (zero them first); dinit may be null.
+cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,
                             const void* dy, const float* A, const float* D, const float* cum2,
-                            const float* dtT, const float* Sprev, float* Gn, float* CB, float* SdCB,
-                            const float* dfinal, float* dx, float* ddt, float* dA, float* dB,
-                            float* dC, float* dD, float* dinit, cudaStream_t st);
+                            const float* dtT, const void* Sprev, const float* fin,
+                            const BwdWork& w, const float* dfinal, float* dx, float* ddt,
+                            float* dA, float* dB, float* dC, float* dD, float* dinit,
+                            int32_t* err, cudaStream_t st);
 
 // Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);

@@ -107,14 +107,14 @@ __device__ __forceinline__ bool cb_fits_f16(float cbmax) {
     return cbmax <= 32768.f && cbmax >= 0.00390625f;
 }
 
-template <int L, int NA>   // NA = N / 64
+template <int L, int NA, bool Y32 = false>   // NA = N / 64; Y32: y stored in fp32
 struct K4Cfg {
     static constexpr int P = 64;
     static constexpr int C_BYTES = NA * 128 * 128;         // C tile: NA K-major atoms
     static constexpr int X_BYTES = L * 128;                 // x rows [0, L) (or a B block)
     static constexpr int S_BYTES = NA * 64 * 128;           // Sprev: NA K-major atoms, 64 rows
     static constexpr int STAGE = X_BYTES + S_BYTES;
-    static constexpr int YW_BYTES = 32 * 64;                // one warp's 32x32 bf16 piece of y
+    static constexpr int YW_BYTES = Y32 ? 32 * 128 : 32 * 64;   // one warp's 32x32 piece of y
     static constexpr int Y_BYTES = kEpiWarps * YW_BYTES;    // one y buffer for all warps
     // cumv[3][256], dtv[3][256] (per stage), vdt[4][256], red_x[3][kConvWarps][2], red_cb[warps]
     static constexpr int VEC_BYTES = (3 * 256 + 3 * 256 + 4 * 256 + 3 * kConvWarps * 2 + kEpiWarps) * 4;
@@ -150,7 +150,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 
-template <int L, int NA>
+template <int L, int NA, bool kY32>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
@@ -158,7 +158,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int32_t* err) {
-    using C = K4Cfg<L, NA>;
+    using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -425,20 +425,35 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             tmem_wait_ld_regs(r);
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[pb]);
-            uint32_t yv[PC / 2];
-#pragma unroll
-            for (int e = 0; e < PC / 2; ++e)
-                yv[e] = pack_bf16x2(fmaf(e_prev, __uint_as_float(rs[2 * e]), __uint_as_float(r[2 * e])),
-                                    fmaf(e_prev, __uint_as_float(rs[2 * e + 1]), __uint_as_float(r[2 * e + 1])));
-            // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
-            // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
-            if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
-            __syncwarp();
+            if constexpr (kY32) {
+                // fp32 piece: 128-byte rows, 128-byte swizzled (16-byte chunk k
+                // of row r at k ^ (r & 7); the buffer is 1024-byte aligned).
+                uint32_t yv[PC];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(yw + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
-                    make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
+                for (int e = 0; e < PC; ++e)
+                    yv[e] = __float_as_uint(fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e])));
+                if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
+                __syncwarp();
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4*>(yw + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                        make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
+            } else {
+                uint32_t yv[PC / 2];
+#pragma unroll
+                for (int e = 0; e < PC / 2; ++e)
+                    yv[e] = pack_bf16x2(fmaf(e_prev, __uint_as_float(rs[2 * e]), __uint_as_float(r[2 * e])),
+                                        fmaf(e_prev, __uint_as_float(rs[2 * e + 1]), __uint_as_float(r[2 * e + 1])));
+                // This warp's 32 x 32 piece, 64-byte swizzled (16-byte chunk k of
+                // row r at k ^ ((r >> 1) & 3)), stored by one lane with TMA.
+                if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
+                __syncwarp();
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(yw + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
+                        make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -835,15 +850,19 @@ Split4 pick_split4(const Dims& d, int NQ) {
     return best;
 }
 
-template <int L, int NA>
+template <int L, int NA, bool kY32>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
                       void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
-    using C = K4Cfg<L, NA>;
+    using C = K4Cfg<L, NA, kY32>;
+    if constexpr (C::SMEM > 232448) {   // the fp32 y staging does not fit (L = 256, N = 256)
+        return cudaErrorNotSupported;
+    } else {
     CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.sx[1] * 2), (uint64_t)(d.sx[0] * 2)};   // token, batch
-    const uint64_t ys[2] = {(uint64_t)(d.sy[1] * 2), (uint64_t)(d.sy[0] * 2)};
+    constexpr uint64_t ye = kY32 ? 4 : 2;   // bytes per y element
+    const uint64_t ys[2] = {(uint64_t)(d.sy[1] * ye), (uint64_t)(d.sy[0] * ye)};
     const uint32_t box[3] = {64, 128, 1};
     const uint32_t ybox[3] = {32, 32, 1};
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
@@ -854,27 +873,30 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint32_t sbox[2] = {64, 64};
     if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
         !make_tmap_bf16(&tm_c, Cm, 3, bd, cs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
-        !make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B))
+        !(kY32 ? make_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, 3, xd, ys, ybox,
+                           CU_TENSOR_MAP_SWIZZLE_128B)
+               : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
     const int NQ = L / 128;
     const Split4 sp = pick_split4(d, NQ);
     const int64_t grid = sp.ctas;
-    auto k = chunk_out_tc_kernel<L, NA>;
+    auto k = chunk_out_tc_kernel<L, NA, kY32>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, err);
+    }
 }
 
-template <int L>
+template <int L, bool kY32>
 cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void* Cm,
                         const float* cum2, const float* dtT, const void* Sprev, const float* D,
                         void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
     switch (d.N) {
-        case 64: return launch_k4<L, 1>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
-        case 128: return launch_k4<L, 2>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
-        case 256: return launch_k4<L, 4>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 64: return launch_k4<L, 1, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 128: return launch_k4<L, 2, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 256: return launch_k4<L, 4, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
     }
     return cudaErrorInvalidValue;
 }
@@ -884,11 +906,14 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st,
-                                const uint32_t* xabs, bool pdl) {
+                                const uint32_t* xabs, bool pdl, bool y32) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
-    return d.L == 256 ? launch_k4_n<256>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl)
-                      : launch_k4_n<128>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+    if (y32)
+        return d.L == 256 ? launch_k4_n<256, true>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl)
+                          : launch_k4_n<128, true>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+    return d.L == 256 ? launch_k4_n<256, false>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl)
+                      : launch_k4_n<128, false>(d, x, B, C, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
 }
 
 }  // namespace m2

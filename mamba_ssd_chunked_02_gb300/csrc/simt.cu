@@ -103,12 +103,12 @@ chunk_state_simt_kernel(const T* __restrict__ x, const T* __restrict__ B,
 // memory), masked with s <= t from the indices before exp2, scaled by
 // exp2(cum2_t - cum2_s) dt_s, then accumulated against x_s.  The carried term
 // exp2(cum2_t) Sprev C_t and the skip term D x_t are added before the store.
-template <typename T>
+template <typename T, typename TY>   // TY: element type of y (T, or fp32)
 __global__ void __launch_bounds__(kThreads)
 chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T* __restrict__ C,
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       const T* __restrict__ Sprev, const float* __restrict__ D,
-                      T* __restrict__ y, int64_t Tlen, int64_t H, int64_t P, int64_t N,
+                      TY* __restrict__ y, int64_t Tlen, int64_t H, int64_t P, int64_t N,
                       int64_t G, int64_t L, int64_t nc, IoStrides io) {
     constexpr int TT = 32, SB = 32;
     extern __shared__ float smem[];
@@ -219,7 +219,7 @@ chunk_out_simt_kernel(const T* __restrict__ x, const T* __restrict__ B, const T*
         const int64_t t = q0 + i;
         if (t >= q1) continue;
         const float v = acc[k] + ex2(ct[i]) * accs[k] + Dh * to_f32(x[b * io.xb + t * io.xt + h * P + p]);
-        y[b * io.yb + t * io.yt + h * P + p] = from_f32<T>(v);
+        y[b * io.yb + t * io.yt + h * P + p] = from_f32<TY>(v);
     }
 }
 
@@ -249,13 +249,23 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
 
 cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, const void* C,
                                   const float* cum2, const float* dtT, const void* Sprev,
-                                  const float* D, void* y, int32_t* /*err*/, cudaStream_t st) {
+                                  const float* D, void* y, int32_t* /*err*/, cudaStream_t st,
+                                  bool y32) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     const size_t smem = chunk_out_smem(d);
     const dim3 grid((unsigned)(d.b * d.nc * d.H), (unsigned)(d.L / 32));
     cudaError_t e;
-    if (d.dtype == 1) {
-        auto k = chunk_out_simt_kernel<__nv_bfloat16>;
+    if (d.dtype == 1 && y32) {
+        auto k = chunk_out_simt_kernel<__nv_bfloat16, float>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kThreads, smem, st>>>(
+            static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(B),
+            static_cast<const __nv_bfloat16*>(C), cum2, dtT,
+            static_cast<const __nv_bfloat16*>(Sprev), D, static_cast<float*>(y), d.T,
+            d.H, d.P, d.N, d.G, d.L, d.nc, io_strides(d));
+    } else if (d.dtype == 1) {
+        auto k = chunk_out_simt_kernel<__nv_bfloat16, __nv_bfloat16>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(
@@ -264,7 +274,7 @@ cudaError_t launch_chunk_out_simt(const Dims& d, const void* x, const void* B, c
             static_cast<const __nv_bfloat16*>(Sprev), D, static_cast<__nv_bfloat16*>(y), d.T,
             d.H, d.P, d.N, d.G, d.L, d.nc, io_strides(d));
     } else {
-        auto k = chunk_out_simt_kernel<float>;
+        auto k = chunk_out_simt_kernel<float, float>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         k<<<grid, kThreads, smem, st>>>(

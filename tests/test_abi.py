@@ -234,15 +234,18 @@ def test_fwd_strided_validates_strides_without_launching(lib):
 
 
 def test_bwd_workspace_size_formula(lib):
-    """Backward workspace: cum2 and dtT, fp32 dS and Sprev, C.B^T and the
-    head-summed dCB per (b, chunk, group), and a final-state scratch, each
-    rounded up to 256 bytes."""
+    """Backward workspace: cum2 and dtT, fp32 dS, Sprev in the I/O type, C.B^T
+    and the head-summed dCB per (b, chunk, group), the final state, an I/O-type
+    copy of Gn, y without the skip term and the reversed run's output (fp32),
+    its inputs (dy, B, C, cum2', dt' = 1), each rounded up to 256 bytes."""
     a256 = lambda v: (v + 255) // 256 * 256
     s = shp()
-    b, T, H, P, N, G, L = 2, 512, 8, 64, 128, 1, 256
+    b, T, H, P, N, G, L, E = 2, 512, 8, 64, 128, 1, 256, 2
     nc = T // L
-    want = 2 * a256(4 * b * H * T) + 2 * a256(4 * b * nc * H * P * N) + \
-        2 * a256(4 * b * nc * G * L * L) + a256(4 * b * H * P * N)
+    st = b * nc * H * P * N
+    want = (4 * a256(4 * b * H * T) + a256(4 * st) + 2 * a256(E * st) +
+            2 * a256(4 * b * nc * G * L * L) + a256(4 * b * H * P * N) +
+            2 * a256(4 * b * T * H * P) + a256(E * b * T * H * P) + 2 * a256(E * b * T * G * N))
     assert m2.bwd_workspace_size(s) == want
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
 
