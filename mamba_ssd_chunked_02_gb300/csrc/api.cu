@@ -130,38 +130,55 @@ Carve carve(const Dims& d) {
 }
 
 // Workspace of the backward pass: the forward's cum2, dtT, dS (fp32; reused for
-// the chunk adjoints dSout / Gn), Sprev in the I/O type, C.B^T and the
-// head-summed dCB per (b, chunk, group), the final state, an I/O-type copy of
-// Gn, y without the skip term and the reversed run's output y' (both fp32), and
-// the reversed run's inputs (dy, B, C, cum2', dt' = 1).
+// the chunk adjoints dSout / Gn), Sprev in the I/O type, the final state, an
+// I/O-type copy of Gn, y without the skip term and y' (fp32), the reordered
+// inputs of the three output runs, Sprev^T and Gn^T, the per-run-head cum2 /
+// dt rows, and the dC / dB runs' per-head outputs (fp32).
 struct BwdCarve {
-    size_t cum2, dtT, dS, Sprev, CB, SdCB, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, total;
+    size_t cum2, dtT, dS, Sprev, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, xB, xCr, xr,
+        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, total;
 };
 
 BwdCarve bwd_carve(const Dims& d) {
     BwdCarve c;
     const size_t E = (size_t)m2::esize(d);
+    const size_t Q = d.N >= 64 ? (size_t)(d.N / 64) : 1;
     const size_t cum = align256(sizeof(float) * (size_t)m2::n_cum(d));
-    const size_t tile = align256(sizeof(float) * (size_t)(d.b * d.nc * d.G * d.L * d.L));
-    const size_t xy = align256(E * (size_t)(d.b * d.T * d.H * d.P));
-    const size_t bc = align256(E * (size_t)(d.b * d.T * d.G * d.N));
-    c.cum2 = 0;
-    c.dtT = c.cum2 + cum;
-    c.dS = c.dtT + cum;
-    c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
-    c.CB = c.Sprev + align256(E * (size_t)m2::n_state(d));
-    c.SdCB = c.CB + tile;
-    c.fin = c.SdCB + tile;
-    c.GnIO = c.fin + align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N));
-    c.yno = c.GnIO + align256(E * (size_t)m2::n_state(d));
+    const size_t cumq = align256(sizeof(float) * Q * (size_t)m2::n_cum(d));
+    const size_t st32 = align256(sizeof(float) * (size_t)m2::n_state(d));
+    const size_t stE = align256(E * (size_t)m2::n_state(d));
+    const size_t xyE = align256(E * (size_t)(d.b * d.T * d.H * d.P));
     const size_t xy32 = align256(sizeof(float) * (size_t)(d.b * d.T * d.H * d.P));
-    c.yr = c.yno + xy32;
-    c.dyr = c.yr + xy32;
-    c.Br = c.dyr + xy;
-    c.Cr = c.Br + bc;
-    c.cum2r = c.Cr + bc;
-    c.ones = c.cum2r + cum;
-    c.total = c.ones + cum;
+    const size_t bcE = align256(E * (size_t)(d.b * d.T * d.G * d.N));
+    const size_t hnE = align256(E * (size_t)(d.b * d.T * d.H * d.N));
+    const size_t hn32 = align256(sizeof(float) * (size_t)(d.b * d.T * d.H * d.N));
+    size_t o = 0;
+    auto take = [&](size_t& f, size_t n) { f = o; o += n; };
+    take(c.cum2, cum);
+    take(c.dtT, cum);
+    take(c.dS, st32);
+    take(c.Sprev, stE);
+    take(c.fin, align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)));
+    take(c.GnIO, stE);
+    take(c.yno, xy32);
+    take(c.yr, xy32);
+    take(c.dyr, xyE);
+    take(c.Br, bcE);
+    take(c.Cr, bcE);
+    take(c.cum2r, cum);
+    take(c.ones, cum);
+    take(c.xB, hnE);
+    take(c.xCr, hnE);
+    take(c.xr, xyE);
+    take(c.SprevT, stE);
+    take(c.GnT, stE);
+    take(c.cum2d, cumq);
+    take(c.dtTd, cumq);
+    take(c.cum2rd, cumq);
+    take(c.onesd, cumq);
+    take(c.yC, hn32);
+    take(c.zB, hn32);
+    c.total = o;
     return c;
 }
 
@@ -463,17 +480,12 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
                : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
     if (e == cudaSuccess)
         e = m2::launch_state_pass(d, dS, false, cum2, initial_state, Sprev, fin, err, s);
-    m2::BwdWork w{dS,
-                  ws + cv.GnIO,
-                  ws + cv.yno,
-                  ws + cv.yr,
-                  reinterpret_cast<float*>(ws + cv.CB),
-                  reinterpret_cast<float*>(ws + cv.SdCB),
-                  ws + cv.dyr,
-                  ws + cv.Br,
-                  ws + cv.Cr,
-                  reinterpret_cast<float*>(ws + cv.cum2r),
-                  reinterpret_cast<float*>(ws + cv.ones)};
+    auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
+    auto atf = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    m2::BwdWork w{dS,           at(cv.GnIO),     at(cv.yno),      at(cv.yr),    at(cv.dyr),
+                  at(cv.Br),    at(cv.Cr),       atf(cv.cum2r),   atf(cv.ones), at(cv.xB),
+                  at(cv.xCr),   at(cv.xr),       at(cv.SprevT),   at(cv.GnT),   atf(cv.cum2d),
+                  atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   atf(cv.yC),   atf(cv.zB)};
     if (e == cudaSuccess)
         e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
                                 dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);

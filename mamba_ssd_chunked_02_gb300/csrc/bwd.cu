@@ -36,20 +36,30 @@
 //     dC_i   = sum_{j<=i} (sum_h dCB_ij) B_j + sum_h e_i Sprev^T dy_i
 //     dB_j   = sum_{i>=j} (sum_h dCB_ij) C_i + sum_h w_j Gn^T x_j
 //
-// Kernels, after the forward's stages 1-4 recompute cum2, dtT, Sprev, S_after
-// and y without the skip term:
-//   bwd_chunk_adjoint   sum_i e_i dy_i C_i^T per (b, c, h)            -> dSout
+//   The group gradients are forward-output runs too, with the state
+//   transposed: dC_i = sum_h S_i^T dy_i (S_i the state after token i) is stage 4
+//   with x'' = B, B'' = x, C'' = dy and carried state Sprev^T; dB_j =
+//   sum_h dt_j G_j^T x_j (G_j the adjoint of S_j) is the reversed run with
+//   x'' = C, B'' = dy, C'' = x and carried state Gn^T.  In both, the N columns of
+//   the output are split into Q = N/64 heads of 64 (the tensor-core shape), so a
+//   run has Q*H heads in H groups of Q, and the head sum follows.
+//
+// Kernels, after the forward's stages 1-3 recompute cum2, dtT, Sprev and the
+// final state:
+//   (stage 4)           y without the skip term
+//   (stage 2) or        sum_i e_i dy_i C_i^T per (b, c, h)            -> dSout
+//   bwd_chunk_adjoint   (stage 2's tensor-core kernel in its adjoint weight mode
+//                       where the shape allows it)
 //   bwd_state_pass_rev  reverse pass over chunks, in place            -> Gn, dinit
-//   bwd_reverse         dy, B, C with each chunk's tokens reversed; cum2', dt' = 1
-//   (stage 4)           y' from the reversed inputs (tensor cores where the
-//                       forward uses them)
+//   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
+//                       copies of B and C, cum2' and dt' rows)
+//   bwd_transpose       Sprev^T and Gn^T
+//   (stage 4, 3 runs)   y', the dC run and the dB run (tensor cores where the
+//                       forward uses them, fp32 outputs)
 //   bwd_token           per (b, c, h): dx, ddt, and dA, dD partial sums
-//   bwd_pair_tiles      per (b, c, g) and 64x64 tile pair (j <= i): CB and
-//                       sum_h dCB                                       -> CB, SdCB
-//   bwd_group_bc        per (b, c, g), 64-token tile, 64-column tile: dC or dB,
-//                       one GEMM over the chunk's tokens and one over (head, p)
-// The contractions of the last two go through mm_tile, a 64x64 fp32 tile on 256
-// threads (4x4 outputs each) with operands staged through shared memory.
+//   bwd_bc_reduce       dC and dB summed over each group's heads
+// bwd_chunk_adjoint's contraction goes through mm_tile, a 64x64 fp32 tile on
+// 256 threads (4x4 outputs each) with operands staged through shared memory.
 #include <algorithm>
 
 #include "common.cuh"
@@ -61,7 +71,6 @@ namespace {
 constexpr int kT = 64;         // tile edge (tokens, p, n)
 constexpr int kK = 16;         // k per shared-memory stage
 constexpr int kThreads = 256;  // 16 x 16 threads, 4 x 4 outputs each
-constexpr int kHB = 16;        // heads per block of the (head, p) contractions
 
 struct MMSmem {
     float a[2][kK][kT + 4];
@@ -164,13 +173,6 @@ __device__ __forceinline__ float block_suffix_sum(float v, float* red) {
     return s;
 }
 
-// Decode a lower-triangular tile pair index into (ti, tj), tj <= ti.
-__device__ __forceinline__ void pair_of(int k, int& ti, int& tj) {
-    ti = 0;
-    while ((ti + 1) * (ti + 2) / 2 <= k) ++ti;
-    tj = k - ti * (ti + 1) / 2;
-}
-
 struct BwdArgs {
     const void* x;      // [b,T,H,P] TI
     const void* B;      // [b,T,G,N] TI
@@ -186,8 +188,6 @@ struct BwdArgs {
     void* GnIO;         // [b,nc,H,P,N] TI copy of Gn (stage 4's carried-state operand)
     const float* yno;   // [b,T,H,P] fp32: y without the skip term
     const float* yr;    // [b,T,H,P] fp32: y' with each chunk's tokens reversed
-    float* CB;          // [b,nc,G,L,L] fp32
-    float* SdCB;        // [b,nc,G,L,L] fp32
     float* dx;          // [b,T,H,P]
     float* ddt;         // [b,T,H]
     float* dA;          // [H] (accumulated)
@@ -195,7 +195,6 @@ struct BwdArgs {
     float* dB;          // [b,T,G,N]
     float* dC;          // [b,T,G,N]
     int T, H, P, N, G, L, nc;
-    int lp;             // log2(P)
 };
 
 // --- dSout[b,c,h] = sum_i e_i dy_i C_i^T  (P x N).  Grid: b*nc*H * ceil(P/64) * ceil(N/64).
@@ -297,172 +296,120 @@ bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* 
     }
 }
 
-// --- Stage 4's inputs for y': token k of chunk c (Lc tokens) goes to position
-// Lc-1-k of the same chunk; x' = dy, B' = C, C' = B; cum2'[k'] = c2_last - c2[Lc-1-k'];
-// dt' = 1.  One CTA per (token, b).
+// --- Inputs of the three stage-4 runs, one CTA per (token t, b).  Token k of
+// chunk c (Lc tokens) is reversed to position Lc-1-k of the same chunk.
+//   y' run (H heads):         dyr = dy reversed, Br = C reversed, Cr = B reversed,
+//                             cum2r = c2_last - c2 (reversed), ones
+//   dC run (Q*H heads of N/Q): xB[h] = B of the head's group
+//   dB run (Q*H heads, reversed): xCr[h] = C of the group reversed, xr = x reversed
+//   per (Q*H)-head rows: cum2d, dtTd (natural order), cum2rd, onesd (reversed).
+struct PrepArgs {
+    const void *dy, *B, *C, *x;
+    const float *cum2, *dtT;
+    void *dyr, *Br, *Cr, *xB, *xCr, *xr;
+    float *cum2r, *ones, *cum2d, *dtTd, *cum2rd, *onesd;
+    int T, H, G, P, N, L, Q;
+};
+
 template <typename TI>
-__global__ void __launch_bounds__(kThreads)
-bwd_reverse(const TI* __restrict__ dy, const TI* __restrict__ B, const TI* __restrict__ C,
-            const float* __restrict__ cum2, TI* __restrict__ dyr, TI* __restrict__ Br,
-            TI* __restrict__ Cr, float* __restrict__ cum2r, float* __restrict__ ones, int T, int H,
-            int64_t rowx, int64_t rowbc, int L) {
+__global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     const int t = blockIdx.x, b = blockIdx.y;
-    const int c = t / L, k = t - c * L;
-    const int Lc = min(L, T - c * L);
-    const int ts = c * L + (Lc - 1 - k);   // the source token
+    const int c = t / a.L, k = t - c * a.L;
+    const int Lc = min(a.L, a.T - c * a.L);
+    const int ts = c * a.L + (Lc - 1 - k);   // the source token of reversed position t
+    const int hpg = a.H / a.G;
     // Rows are 16-byte multiples (P, N >= 16 elements) at 16-byte aligned starts.
-    auto copy = [&](const TI* src, TI* dst, int64_t row) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + ((int64_t)b * T + ts) * row);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + ((int64_t)b * T + t) * row);
-        const int64_t n = row * (int64_t)sizeof(TI) / 16;
-        for (int64_t i = threadIdx.x; i < n; i += kThreads) d4[i] = s4[i];
+    auto copy = [&](const void* src, int64_t srow, void* dst, int64_t drow, int64_t n16) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(static_cast<const TI*>(src) + srow);
+        uint4* d4 = reinterpret_cast<uint4*>(static_cast<TI*>(dst) + drow);
+        for (int64_t i = threadIdx.x; i < n16; i += kThreads) d4[i] = s4[i];
     };
-    copy(dy, dyr, rowx);
-    copy(C, Br, rowbc);
-    copy(B, Cr, rowbc);
-    for (int h = threadIdx.x; h < H; h += kThreads) {
-        const float* c2 = cum2 + ((int64_t)b * H + h) * T;
-        const int64_t o = ((int64_t)b * H + h) * T + t;
-        cum2r[o] = c2[c * L + Lc - 1] - c2[ts];
-        ones[o] = 1.f;
+    const int64_t rowx = (int64_t)a.H * a.P, rowbc = (int64_t)a.G * a.N, rowhn = (int64_t)a.H * a.N;
+    const int64_t E = sizeof(TI);
+    const int64_t bt = (int64_t)b * a.T;
+    copy(a.dy, (bt + ts) * rowx, a.dyr, (bt + t) * rowx, rowx * E / 16);
+    copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
+    copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
+    copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
+    // Per-head copies of the group's B (natural order) and C (reversed).
+    {
+        const int64_t n16 = (int64_t)a.N * E / 16;
+        const uint4* Bs = reinterpret_cast<const uint4*>(static_cast<const TI*>(a.B) + (bt + t) * rowbc);
+        const uint4* Cs = reinterpret_cast<const uint4*>(static_cast<const TI*>(a.C) + (bt + ts) * rowbc);
+        uint4* xb = reinterpret_cast<uint4*>(static_cast<TI*>(a.xB) + (bt + t) * rowhn);
+        uint4* xc = reinterpret_cast<uint4*>(static_cast<TI*>(a.xCr) + (bt + t) * rowhn);
+        for (int64_t i = threadIdx.x; i < a.H * n16; i += kThreads) {
+            const int64_t h = i / n16, e = i - h * n16;
+            const int64_t src = (h / hpg) * n16 + e;
+            xb[i] = Bs[src];
+            xc[i] = Cs[src];
+        }
+    }
+    for (int h = threadIdx.x; h < a.H; h += kThreads) {
+        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
+        const int64_t o = ((int64_t)b * a.H + h) * a.T + t;
+        a.cum2r[o] = c2[c * a.L + Lc - 1] - c2[ts];
+        a.ones[o] = 1.f;
+    }
+    for (int hq = threadIdx.x; hq < a.Q * a.H; hq += kThreads) {
+        const int h = hq / a.Q;
+        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
+        const int64_t o = ((int64_t)b * a.Q * a.H + hq) * a.T + t;
+        a.cum2d[o] = c2[t];
+        a.dtTd[o] = a.dtT[((int64_t)b * a.H + h) * a.T + t];
+        a.cum2rd[o] = c2[c * a.L + Lc - 1] - c2[ts];
+        a.onesd[o] = 1.f;
     }
 }
 
-// --- Per (b, c, g) and tile pair (ti >= tj): CB = C_i . B_j and
-// SdCB = sum_h exp2(c2_i - c2_j) dt_j (dy_i . x_j), masked to j <= i < Lc
-// (0 elsewhere in the tile).  Grid: b*nc*G * (nt (nt + 1) / 2), nt = ceil(L/64).
-template <typename TI>
-__global__ void __launch_bounds__(kThreads) bwd_pair_tiles(BwdArgs a) {
-    __shared__ MMSmem sm;
-    __shared__ float s_sci[kHB][kT], s_scj[kHB][kT];
-    const int ntl = (a.L + kT - 1) / kT, npair = ntl * (ntl + 1) / 2;
-    int id = blockIdx.x;
-    const int pair = id % npair; id /= npair;
-    const int g = id % a.G; id /= a.G;
-    const int c = id % a.nc, b = id / a.nc;
-    int ti, tj;
-    pair_of(pair, ti, tj);
-    const int64_t t0 = (int64_t)c * a.L;
-    const int Lc = (int)min((int64_t)a.L, a.T - t0);
-    if (ti * kT >= Lc) return;   // no token of the chunk in this row tile
-    const int hpg = a.H / a.G, P = a.P, N = a.N;
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * a.G * N + (int64_t)g * N;
-    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * a.G * N + (int64_t)g * N;
-    const int64_t sBC = (int64_t)a.G * N;
-    float acc[4][4];
-    zero(acc);
-    mm_tile<true, true>(
-        acc, sm, 0, N,
-        [&](int m, int k) {
-            const int i = ti * kT + m;
-            return i < Lc ? to_f32(Cg[i * sBC + k]) : 0.f;
-        },
-        [&](int k, int n) {
-            const int j = tj * kT + n;
-            return j < Lc ? to_f32(Bg[j * sBC + k]) : 0.f;
-        });
-    const int64_t toff = (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)a.L * a.L;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = ti * kT + 4 * ty + r;
-        if (i >= a.L) continue;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = tj * kT + 4 * tx + q;
-            if (j < a.L) a.CB[toff + (int64_t)i * a.L + j] = acc[r][q];
-        }
+// --- Batched transpose of P x N blocks into N x P blocks (I/O type out).
+// One CTA per (block, 32 x 32 tile).
+template <typename TS, typename TI>
+__global__ void __launch_bounds__(kThreads)
+bwd_transpose(const TS* __restrict__ in, TI* __restrict__ out, int P, int N) {
+    __shared__ float tile[32][33];
+    const int ntn = (N + 31) / 32, ntp = (P + 31) / 32;
+    const int64_t blk = blockIdx.x / (ntn * ntp);
+    const int tn = (blockIdx.x % (ntn * ntp)) % ntn, tp = (blockIdx.x % (ntn * ntp)) / ntn;
+    const TS* src = in + blk * (int64_t)P * N;
+    TI* dst = out + blk * (int64_t)P * N;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+    for (int r = ty; r < 32; r += 8) {
+        const int p = tp * 32 + r, n = tn * 32 + tx;
+        if (p < P && n < N) tile[r][tx] = to_f32(src[(int64_t)p * N + n]);
     }
-    float sd[4][4];
-    zero(sd);
-    const int64_t sxy = (int64_t)a.H * P;
-    const int h0 = g * hpg;
-    if (ti > tj) {
-        // Off the diagonal every j of the tile precedes every i, so with r = ti*64
-        // exp2(c2_i - c2_j) = exp2(c2_i - c2_r) exp2(c2_r - c2_j), both factors
-        // <= 1, and the head sum is one contraction over (head, p) with the
-        // factors folded into the operands.
-        for (int hb = 0; hb < hpg; hb += kHB) {
-            const int nh = min(kHB, hpg - hb);
-            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
-                const int hl = e / kT, m = e % kT;
-                float si = 0.f, sj = 0.f;
-                if (hl < nh) {
-                    const int64_t row = ((int64_t)b * a.H + h0 + hb + hl) * a.T + t0;
-                    const float c2r = a.cum2[row + ti * kT];
-                    const int i = ti * kT + m, j = tj * kT + m;
-                    if (i < Lc) si = ex2(a.cum2[row + i] - c2r);
-                    if (j < Lc) sj = ex2(c2r - a.cum2[row + j]) * a.dtT[row + j];
-                }
-                s_sci[hl][m] = si;
-                s_scj[hl][m] = sj;
-            }
-            __syncthreads();
-            const TI* dyb = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy +
-                            (int64_t)(h0 + hb) * P;
-            const TI* xb = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy +
-                           (int64_t)(h0 + hb) * P;
-            const int lp = a.lp;
-            mm_tile<true, true>(
-                sd, sm, 0, nh * P,
-                [&](int m, int k) {
-                    const int i = ti * kT + m;
-                    return i < Lc ? s_sci[k >> lp][m] * to_f32(dyb[i * sxy + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int j = tj * kT + n;
-                    return j < Lc ? s_scj[k >> lp][n] * to_f32(xb[j * sxy + k]) : 0.f;
-                });
-        }
-    } else {
-        // The diagonal tile: one head at a time, the decay per element (masked).
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int n = tn * 32 + r, p = tp * 32 + tx;
+        if (p < P && n < N) dst[(int64_t)n * P + p] = from_f32<TI>(tile[tx][r]);
+    }
+}
+
+// --- dC and dB from the two transposed-state runs, summed over each group's
+// heads: dC[t] = sum_h yC[h, t]; dB[t] = sum_h dt_h[t] zB[h, reversed t].
+// One CTA per (token, b).
+__global__ void __launch_bounds__(kThreads)
+bwd_bc_reduce(const float* __restrict__ yC, const float* __restrict__ zB,
+              const float* __restrict__ dtT, float* __restrict__ dB, float* __restrict__ dC,
+              int T, int H, int G, int N, int L) {
+    const int t = blockIdx.x, b = blockIdx.y;
+    const int c = t / L, k = t - c * L;
+    const int Lc = min(L, T - c * L);
+    const int tr = c * L + (Lc - 1 - k);   // where the reversed run wrote token t
+    const int hpg = H / G;
+    const int64_t rowhn = (int64_t)H * N, bt = (int64_t)b * T;
+    const float* yc = yC + (bt + t) * rowhn;
+    const float* zb = zB + (bt + tr) * rowhn;
+    for (int e = threadIdx.x; e < G * N; e += kThreads) {
+        const int g = e / N, n = e - g * N;
+        float sc = 0.f, sb = 0.f;
         for (int hh = 0; hh < hpg; ++hh) {
-            const int h = h0 + hh;
-            const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T + t0;
-            const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
-            if (threadIdx.x < kT) {
-                const int i = ti * kT + threadIdx.x;
-                s_sci[0][threadIdx.x] = i < Lc ? c2[i] : 0.f;
-                s_scj[0][threadIdx.x] = i < Lc ? dth[i] : 0.f;
-            }
-            // (mm_tile's entry barrier orders these stores before the epilogue.)
-            const TI* dy = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-            const TI* x = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-            float dxa[4][4];
-            zero(dxa);
-            mm_tile<true, true>(
-                dxa, sm, 0, P,
-                [&](int m, int k) {
-                    const int i = ti * kT + m;
-                    return i < Lc ? to_f32(dy[i * sxy + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int j = tj * kT + n;
-                    return j < Lc ? to_f32(x[j * sxy + k]) : 0.f;
-                });
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int il = 4 * ty + r, i = ti * kT + il;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int jl = 4 * tx + q, j = tj * kT + jl;
-                    if (i < Lc && j <= i)
-                        sd[r][q] = fmaf(ex2(s_sci[0][il] - s_sci[0][jl]) * s_scj[0][jl], dxa[r][q],
-                                        sd[r][q]);
-                }
-            }
-            __syncthreads();   // the next head rewrites s_sci / s_scj
+            const int h = g * hpg + hh;
+            sc += yc[(int64_t)h * N + n];
+            sb = fmaf(dtT[((int64_t)b * H + h) * T + t], zb[(int64_t)h * N + n], sb);
         }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = ti * kT + 4 * ty + r;
-        if (i >= a.L) continue;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int j = tj * kT + 4 * tx + q;
-            if (j < a.L) a.SdCB[toff + (int64_t)i * a.L + j] = sd[r][q];
-        }
+        dC[(bt + t) * (int64_t)G * N + e] = sc;
+        dB[(bt + t) * (int64_t)G * N + e] = sb;
     }
 }
 
@@ -504,29 +451,40 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const float* yr = a.yr + base;
     float* dx = a.dx + base;
     float yx = 0.f;
-    for (int j = warp; j < Lc; j += kThreads / 32) {
-        const int jr = Lc - 1 - j;   // where the reversed run wrote token j
-        const float dtj = s_dt[j];
-        float xy = 0.f, dyy = 0.f, dyx = 0.f;
-        for (int p = lane; p < P; p += 32) {
-            const float yp = yr[jr * sxy + p];
-            const float xv = to_f32(x[j * sxy + p]);
-            const float dv = to_f32(dy[j * sxy + p]);
-            dx[j * sxy + p] = fmaf(dtj, yp, Dh * dv);
-            xy = fmaf(xv, yp, xy);
-            dyy = fmaf(dv, yno[j * sxy + p], dyy);
-            dyx = fmaf(dv, xv, dyx);
+    // Two tokens per warp per iteration (j and j + 8), their loads issued together.
+    constexpr int kW = kThreads / 32;
+    for (int j0 = warp; j0 < Lc; j0 += 2 * kW) {
+        float xy[2] = {0.f, 0.f}, dyy[2] = {0.f, 0.f}, dyx[2] = {0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int j = j0 + u * kW;
+            if (j >= Lc) break;
+            const int jr = Lc - 1 - j;   // where the reversed run wrote token j
+            const float dtj = s_dt[j];
+            for (int p = lane; p < P; p += 32) {
+                const float yp = yr[jr * sxy + p];
+                const float xv = to_f32(x[j * sxy + p]);
+                const float dv = to_f32(dy[j * sxy + p]);
+                dx[j * sxy + p] = fmaf(dtj, yp, Dh * dv);
+                xy[u] = fmaf(xv, yp, xy[u]);
+                dyy[u] = fmaf(dv, yno[j * sxy + p], dyy[u]);
+                dyx[u] = fmaf(dv, xv, dyx[u]);
+            }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            xy += __shfl_xor_sync(0xffffffffu, xy, o);
-            dyy += __shfl_xor_sync(0xffffffffu, dyy, o);
-            dyx += __shfl_xor_sync(0xffffffffu, dyx, o);
-        }
-        if (lane == 0) {
-            s_ddt[j] = xy;
-            s_dcum[j] = dyy - dtj * xy;
-            yx += dyx;
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                xy[u] += __shfl_xor_sync(0xffffffffu, xy[u], o);
+                dyy[u] += __shfl_xor_sync(0xffffffffu, dyy[u], o);
+                dyx[u] += __shfl_xor_sync(0xffffffffu, dyx[u], o);
+            }
+            const int j = j0 + u * kW;
+            if (lane == 0 && j < Lc) {
+                s_ddt[j] = xy[u];
+                s_dcum[j] = dyy[u] - s_dt[j] * xy[u];
+                yx += dyx[u];
+            }
         }
     }
     gs = block_sum(gs, red);
@@ -547,173 +505,76 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     }
 }
 
-// --- dC (blockIdx.y == 0) or dB (blockIdx.y == 1) for one 64-token tile and one
-// 64-column tile of (b, c, g).  Grid: (b*nc*G * ceil(L/64) * ceil(N/64), 2).
-template <typename TI>
-__global__ void __launch_bounds__(kThreads) bwd_group_bc(BwdArgs a) {
-    __shared__ MMSmem sm;
-    __shared__ float s_sc[kHB][kT];   // per (head of the block, row) operand scale
-    const int ntl = (a.L + kT - 1) / kT, nnt = (a.N + kT - 1) / kT;
-    int id = blockIdx.x;
-    const int nt = id % nnt; id /= nnt;
-    const int tt = id % ntl; id /= ntl;
-    const int g = id % a.G; id /= a.G;
-    const int c = id % a.nc, b = id / a.nc;
-    const bool isB = blockIdx.y == 1;
-    const int P = a.P, N = a.N, L = a.L, H = a.H;
-    const int hpg = H / a.G;
-    const int64_t t0 = (int64_t)c * L;
-    const int Lc = (int)min((int64_t)L, a.T - t0);
-    if (tt * kT >= Lc) return;
-    const int64_t sxy = (int64_t)H * P, sBC = (int64_t)a.G * N;
-    const TI* Bg = static_cast<const TI*>(a.B) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
-    const TI* Cg = static_cast<const TI*>(a.C) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
-    const float* Sd = a.SdCB + (((int64_t)b * a.nc + c) * a.G + g) * (int64_t)L * L;
-    const int h0 = g * hpg;
-    // Rows of (head, p) for the second contraction: heads h0 .. h0+hpg-1 are
-    // contiguous in x / dy ([.., H, P]) and in Sprev / Gn ([.., H, P, N]).
-    const TI* xg = static_cast<const TI*>(a.x) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h0 * P;
-    const TI* dyg = static_cast<const TI*>(a.dy) + ((int64_t)b * a.T + t0) * sxy + (int64_t)h0 * P;
-    const int64_t soff = (((int64_t)b * a.nc + c) * H + h0) * (int64_t)P * N;
-    const float* c2g = a.cum2 + ((int64_t)b * H + h0) * a.T + t0;   // head stride a.T
-    const float* dtg = a.dtT + ((int64_t)b * H + h0) * a.T + t0;
-    const int64_t T = a.T;
-    const int lp = a.lp;
-    float acc[4][4];
-    zero(acc);
-    if (!isB) {
-        // dC_i = sum_{j <= i} SdCB_ij B_j + sum_{h,p} e_hi dy_hi[p] Sprev_h[p, :]
-        mm_tile<true, false>(
-            acc, sm, 0, min(Lc, (tt + 1) * kT),
-            [&](int m, int k) {
-                const int i = tt * kT + m;
-                return i < Lc ? Sd[(int64_t)i * L + k] : 0.f;
-            },
-            [&](int k, int n) {
-                const int nn = nt * kT + n;
-                return nn < N ? to_f32(Bg[k * sBC + nn]) : 0.f;
-            });
-        const TI* Sp = static_cast<const TI*>(a.Sprev) + soff;
-        for (int hb = 0; hb < hpg; hb += kHB) {
-            const int nh = min(kHB, hpg - hb);
-            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
-                const int hl = e / kT, i = tt * kT + e % kT;
-                s_sc[hl][e % kT] = (hl < nh && i < Lc) ? ex2(c2g[(hb + hl) * T + i]) : 0.f;
-            }
-            __syncthreads();
-            const TI* dyb = dyg + (int64_t)hb * P;
-            const TI* Spb = Sp + (int64_t)hb * P * N;
-            mm_tile<true, false>(
-                acc, sm, 0, nh * P,
-                [&](int m, int k) {
-                    const int i = tt * kT + m;
-                    return i < Lc ? s_sc[k >> lp][m] * to_f32(dyb[i * sxy + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int nn = nt * kT + n;
-                    return nn < N ? to_f32(Spb[(int64_t)k * N + nn]) : 0.f;
-                });
-        }
-    } else {
-        // dB_j = sum_{i >= j} SdCB_ij C_i + sum_{h,p} w_hj x_hj[p] Gn_h[p, :]
-        mm_tile<false, false>(
-            acc, sm, tt * kT, Lc,
-            [&](int m, int k) {
-                const int j = tt * kT + m;
-                return j < Lc ? Sd[(int64_t)k * L + j] : 0.f;
-            },
-            [&](int k, int n) {
-                const int nn = nt * kT + n;
-                return nn < N ? to_f32(Cg[k * sBC + nn]) : 0.f;
-            });
-        const float* Gn = a.Gn + soff;
-        for (int hb = 0; hb < hpg; hb += kHB) {
-            const int nh = min(kHB, hpg - hb);
-            for (int e = threadIdx.x; e < kHB * kT; e += kThreads) {
-                const int hl = e / kT, j = tt * kT + e % kT;
-                float w = 0.f;
-                if (hl < nh && j < Lc) {
-                    const int64_t o = (int64_t)(hb + hl) * T;
-                    w = dtg[o + j] * ex2(c2g[o + Lc - 1] - c2g[o + j]);
-                }
-                s_sc[hl][e % kT] = w;
-            }
-            __syncthreads();
-            const TI* xb = xg + (int64_t)hb * P;
-            const float* Gnb = Gn + (int64_t)hb * P * N;
-            mm_tile<true, false>(
-                acc, sm, 0, nh * P,
-                [&](int m, int k) {
-                    const int j = tt * kT + m;
-                    return j < Lc ? s_sc[k >> lp][m] * to_f32(xb[j * sxy + k]) : 0.f;
-                },
-                [&](int k, int n) {
-                    const int nn = nt * kT + n;
-                    return nn < N ? Gnb[(int64_t)k * N + nn] : 0.f;
-                });
-        }
-    }
-    float* out = (isB ? a.dB : a.dC) + ((int64_t)b * a.T + t0) * sBC + (int64_t)g * N;
-    const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int i = tt * kT + 4 * ty + r;
-        if (i >= Lc) continue;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int nn = nt * kT + 4 * tx + q;
-            if (nn < N) out[i * sBC + nn] = acc[r][q];
-        }
-    }
-}
-
 template <typename TI>
 cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
                      const float* dfinal, float* dinit, int32_t* err, cudaStream_t st) {
     const int64_t bnc = d.b * d.nc;
     const int npt = (int)((d.P + kT - 1) / kT), nnt = (int)((d.N + kT - 1) / kT);
-    const int ntl = (int)((d.L + kT - 1) / kT);
     const int64_t g1 = bnc * d.H * npt * nnt;
-    const int64_t g3 = bnc * d.G * (ntl * (ntl + 1) / 2);
     const int64_t g4 = bnc * d.H;
-    const int64_t g5 = bnc * d.G * ntl * nnt;
-    if (g1 >= (int64_t(1) << 31) || g3 >= (int64_t(1) << 31) || g4 >= (int64_t(1) << 31) ||
-        g5 >= (int64_t(1) << 31) || d.T >= (int64_t(1) << 31) || d.b >= 65536)
+    const int64_t ntile = ((d.P + 31) / 32) * ((d.N + 31) / 32);
+    const int64_t gt = bnc * d.H * ntile;
+    if (g1 >= (int64_t(1) << 31) || g4 >= (int64_t(1) << 31) || gt >= (int64_t(1) << 31) ||
+        d.T >= (int64_t(1) << 31) || d.b >= 65536)
         return cudaErrorInvalidValue;
-    // Stage 4 with y in fp32 (tensor cores where the forward uses them; the
-    // CUDA-core kernel where that variant does not fit).
-    auto out4 = [&](const void* x4, const void* B4, const void* C4, const float* c4,
+    // Stage 4 with y in fp32 (tensor cores where the shape allows them; the
+    // CUDA-core kernel otherwise or where that variant does not fit).
+    auto out4 = [&](const Dims& dd, const void* x4, const void* B4, const void* C4, const float* c4,
                     const float* d4, const void* S4, const float* y4) {
         float* yo = const_cast<float*>(y4);
-        if (tc) {
-            const cudaError_t r = launch_chunk_out_tc(d, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st,
-                                                      nullptr, false, true);
+        if (tc && tc_supported(dd)) {
+            const cudaError_t r = launch_chunk_out_tc(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err,
+                                                      st, nullptr, false, true);
             if (r != cudaErrorNotSupported) return r;
         }
-        return launch_chunk_out_simt(d, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, true);
+        return launch_chunk_out_simt(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, true);
     };
     // y without the skip term.
-    cudaError_t e = out4(a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno);
+    cudaError_t e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno);
     if (e != cudaSuccess) return e;
-    bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
+    // Chunk adjoints sum_i e_i dy_i C_i^T: stage 2's tensor-core contraction in
+    // its adjoint weight mode where the shape allows it.
+    if (tc && tc_supported(d)) {
+        e = launch_chunk_state_tc(d, a.dy, a.C, a.cum2, a.dtT, a.Gn, false, err, st, nullptr,
+                                  false, true);
+        if (e != cudaSuccess) return e;
+    } else {
+        bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
+    }
     const int64_t total4 = d.b * d.H * d.P * d.N / 4;   // N is a multiple of 16
     const int64_t blocks = std::min<int64_t>((total4 + kThreads - 1) / kThreads, 152 * 16);
     bwd_state_pass_rev<TI><<<(unsigned)blocks, kThreads, 0, st>>>(
         reinterpret_cast<float4*>(a.Gn), static_cast<TI*>(a.GnIO), a.cum2,
         reinterpret_cast<const float4*>(dfinal), reinterpret_cast<float4*>(dinit), total4,
         (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc);
-    bwd_reverse<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
-        static_cast<const TI*>(a.dy), static_cast<const TI*>(a.B), static_cast<const TI*>(a.C),
-        a.cum2, static_cast<TI*>(w.dyr), static_cast<TI*>(w.Br), static_cast<TI*>(w.Cr), w.cum2r,
-        w.ones, (int)d.T, (int)d.H, d.H * d.P, d.G * d.N, (int)d.L);
+    // The dC / dB runs: Q heads of N/Q columns per head (64 wide when N >= 64).
+    const int Q = d.N >= 64 ? (int)(d.N / 64) : 1;
+    PrepArgs pa{a.dy, a.B, a.C, a.x, a.cum2, a.dtT, w.dyr, w.Br, w.Cr, w.xB, w.xCr, w.xr,
+                w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
+                (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q};
+    bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
+    bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
+                                                             static_cast<TI*>(w.SprevT),
+                                                             (int)d.P, (int)d.N);
+    bwd_transpose<float, TI><<<(unsigned)gt, kThreads, 0, st>>>(a.Gn, static_cast<TI*>(w.GnT),
+                                                                (int)d.P, (int)d.N);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // y' = stage 4 on the reversed inputs: x' = dy, B' = C, C' = B, Gn carried.
     const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
-    e = out4(w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr);
+    e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr);
+    if (e != cudaSuccess) return e;
+    Dims d2 = d;   // Q*H heads of N/Q, H groups of Q, state dimension P
+    d2.H = Q * d.H;
+    d2.P = d.N / Q;
+    d2.N = d.P;
+    d2.G = d.H;
+    set_contiguous(d2);
+    e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC);          // S^T dy
+    if (e == cudaSuccess) e = out4(d2, w.xCr, w.dyr, w.xr, w.cum2rd, w.onesd, w.GnT, w.zB);   // G^T x
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
-    bwd_pair_tiles<TI><<<(unsigned)g3, kThreads, 0, st>>>(a);
-    bwd_group_bc<TI><<<dim3((unsigned)g5, 2), kThreads, 0, st>>>(a);
+    bwd_bc_reduce<<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
+        w.yC, w.zB, a.dtT, a.dB, a.dC, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
     return cudaGetLastError();
 }
 
@@ -727,13 +588,10 @@ cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B
                             int32_t* err, cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     if (d.L > 256) return cudaErrorInvalidValue;   // bwd_token's tokens: one per thread
-    int lp = 0;
-    while ((int64_t(1) << lp) < d.P) ++lp;
-    if ((int64_t(1) << lp) != d.P) return cudaErrorInvalidValue;   // P is a power of two
     BwdArgs a{x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w.Gn, w.GnIO,
-              static_cast<const float*>(w.yno), static_cast<const float*>(w.yr), w.CB, w.SdCB,
+              static_cast<const float*>(w.yno), static_cast<const float*>(w.yr),
               dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
-              (int)d.L, (int)d.nc, lp};
+              (int)d.L, (int)d.nc};
     return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, w, tc, dfinal, dinit, err, st)
                         : launch_t<float>(d, a, w, tc, dfinal, dinit, err, st);
 }

@@ -49,10 +49,11 @@ cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,
 // per head ([b][nc][H][8], bf16 bit patterns of |x|; their max is the bound).
 // pdl: launched with programmatic dependent launch after stage 1 (the
 // whole-path call): x and B are read before stage 1 completes.
+// adj: weight mode of the backward's chunk adjoint, w_s = exp2(cum2_s) (dtT unused).
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B,
                                   const float* cum2, const float* dtT, void* dS, bool ds16,
                                   int32_t* err, cudaStream_t st, uint32_t* xabs = nullptr,
-                                  bool pdl = false);
+                                  bool pdl = false, bool adj = false);
 
 // Stages 2 and 3 fused (tcgen05, bf16, tc_supported() shapes): each CTA
 // computes its chunk's dS in tensor memory, then, head by head, takes the state
@@ -106,13 +107,22 @@ struct BwdWork {
     void* GnIO;     // [b,nc,H,P,N] I/O type copy of Gn (unused when the I/O type is fp32)
     void* yno;      // [b,T,H,P] fp32: y without the skip term
     void* yr;       // [b,T,H,P] fp32: y' of the reversed run
-    float* CB;      // [b,nc,G,L,L]
-    float* SdCB;    // [b,nc,G,L,L]
     void* dyr;      // [b,T,H,P] dy, each chunk's tokens reversed
     void* Br;       // [b,T,G,N] C reversed (the reversed run's B)
     void* Cr;       // [b,T,G,N] B reversed (the reversed run's C)
     float* cum2r;   // [b,H,T]
     float* ones;    // [b,H,T]
+    void* xB;       // [b,T,H,N] the group's B per head (the dC run's x)
+    void* xCr;      // [b,T,H,N] the group's C per head, reversed (the dB run's x)
+    void* xr;       // [b,T,H,P] x reversed (the dB run's C)
+    void* SprevT;   // [b,nc,H,N,P] Sprev transposed (the dC run's carried state)
+    void* GnT;      // [b,nc,H,N,P] Gn transposed (the dB run's carried state)
+    float* cum2d;   // [b,Q*H,T] cum2 per run head (Q = N/64, or 1 when N < 64)
+    float* dtTd;    // [b,Q*H,T]
+    float* cum2rd;  // [b,Q*H,T]
+    float* onesd;   // [b,Q*H,T]
+    float* yC;      // [b,T,H,N] fp32: S^T dy per head
+    float* zB;      // [b,T,H,N] fp32: G^T x per head (reversed chunks)
 };
 // tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
 // dA and dD (if given) are accumulated into (zero them first); dinit may be null.

@@ -12,6 +12,9 @@
 //   dS[b,c,h,p,n] = sum_{s in chunk c} B[s,n] * w_s * x[s,p],
 //   w_s = dtT[s] * exp2(cum2[last token of c] - cum2[s])
 //
+// The same contraction with w_s = exp2(cum2[s]), x = dy and B = C is the
+// backward pass's chunk adjoint sum_s exp2(cum2_s) dy_s C_s^T (weight mode 1).
+//
 // As a GEMM per (b, c, h): D[n, p] = A[n, s] * X~[s, p] with M = n (a 128-wide
 // tile of the state dimension), N = P = 64, K = L (the chunk).
 //   * A = B_chunk^T straight from HBM: B is [s][n] with n contiguous, i.e. an
@@ -104,6 +107,7 @@ struct FuseArgs {
     __nv_bfloat16* Sprev;     // [b][nc][H][P][N]
     float* fin;               // [b][H][P][N]
     int nb;                   // batch
+    int adj = 0;              // weight mode: 0 = w_s above, 1 = w_s = exp2(cum2[s])
 };
 
 template <int L, bool kFuse, bool kDS16>
@@ -272,7 +276,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int st = i % NS, k = i / NS;
             float w[RPT];
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) w[r] = pd[r] * ex2(plast - pc[r]);   // 0 past Lc
+            for (int r = 0; r < RPT; ++r)   // 0 past Lc (the x rows there are zero-filled)
+                w[r] = fa.adj ? ex2(pc[r]) : pd[r] * ex2(plast - pc[r]);
             if (i + 1 < nh) prefetch(i + 1);
             const bool ok = __all_sync(0xffffffffu,
                                        mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
@@ -577,10 +582,11 @@ bool tc_supported(const Dims& d) {
 
 cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
                                   const float* dtT, void* dS, bool ds16, int32_t* err,
-                                  cudaStream_t st, uint32_t* xabs, bool pdl) {
+                                  cudaStream_t st, uint32_t* xabs, bool pdl, bool adj) {
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
-    const FuseArgs none{};
+    FuseArgs none{};
+    none.adj = adj ? 1 : 0;
     if (ds16)
         return d.L == 256
                    ? launch_k2<256, false, true>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl)
