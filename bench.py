@@ -421,22 +421,35 @@ def run_all_configs(args):
         torch.cuda.empty_cache()
 
 
-def bwd_flops(w):
-    """Contraction work of one backward call as the kernels do it (causal halves of
-    the L x L products, forward recompute of the chunk states included):
-    per (b, chunk, head) 3 L^2 P (dy.x^T twice, M^T dy) + 12 L P N (chunk adjoint,
-    Gn B, Sprev C, the two carried-state parts of dB and dC, the recomputed chunk
-    state); per (b, chunk, group) 3 L^2 N (C B^T and the two head-summed dCB
-    products)."""
+def bwd_bytes(w):
+    """Fixed HBM byte model of one backward call: read x and dy, write dx (fp32);
+    read dt, write ddt; read B and C, write dB and dC (fp32); the chunk states
+    handed between kernels counted at fp32 twice (the recomputed forward's dS /
+    Sprev and the adjoint pass's dSout / Gn: 16 P N / L bytes per token-head
+    each); read dfinal, write dinit (and read the initial state) when present."""
     b, T, H, P, N, G, L = (w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
                            w.chunk_size)
-    nc = -(-T // L)
-    return b * nc * (H * (3 * L * L * P + 12 * L * P * N) + G * 3 * L * L * N)
+    E = 2 if w.dtype == "bf16" else 4
+    init = 1 if w.init_std > 0 else 0
+    per_th = 2 * P * E + 4 * P + 8 + 2 * 16 * P * N / L
+    per_tg = 2 * N * E + 8 * N
+    return b * T * (H * per_th + G * per_tg) + 4 * b * H * P * N * (1 + 2 * init)
+
+
+def bwd_flops(w):
+    """Contraction work of the backward: the forward's (chunk states, C.B^T,
+    the intra-chunk and carried-state products) three more times over -- the
+    reversed output run for dx, and the two transposed-state runs for dC and
+    dB -- plus the chunk adjoints (2 P N per token-head); causal halves."""
+    b, T, H, P, N, G, L = (w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups,
+                           w.chunk_size)
+    fwd = T * (H * (4 * P * N + P * (L + 1)) + G * N * (L + 1))
+    return b * (4 * fwd + T * H * 2 * P * N)
 
 
 def run_backward(args, w):
     """Backward pass (mamba2_ssd_bwd) on the workload, inputs and incoming gradients
-    resident in HBM; CUDA-core fp32 kernels, so the roofline is the fp32 FMA rate."""
+    resident in HBM; reported against a fixed HBM byte model of the backward."""
     import torch
     import mamba_ssd_chunked_02_gb300 as m2
     from mamba_ssd_chunked_02_gb300 import workloads as W
@@ -474,18 +487,21 @@ def run_backward(args, w):
         raise RuntimeError("device-side error in the backward loop")
     ms = a.elapsed_time(z) / K
     F = bwd_flops(w)
-    tf = F / (ms * 1e-3) / 1e12
-    # fp32 FMA peak from unit counts and clock: 152 SMs x 128 lanes x 2 flop x f_max.
-    peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    nbytes = bwd_bytes(w)
+    pk, src = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
     print(json.dumps({
         "metric": "SSD backward: tokens/s", "value": w.tokens / (ms * 1e-3), "unit": "tokens/s",
         "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "dtype": "f32 (bf16 inputs)" if w.dtype == "bf16" else "f32",
-        "data": "synthetic", "config": dict(config_of(w, 1), what="backward, forward recompute included"),
-        "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tf / peak, "traffic": None, "kernel": "whole backward",
-                     "algorithmic_flops": F},
-        "gpu_launches": 8 * K, "clocks": clk}), flush=True)
+        "higher_is_better": True, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": dict(config_of(w, 1), what="backward, forward recompute included",
+                                            grads="fp32"),
+        "tflops": F / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "whole backward",
+                     "model": "backward I/O + chunk states at fp32 twice (bench.bwd_bytes)",
+                     "algorithmic_bytes": nbytes, "peak_source": src},
+        "gpu_launches": 14 * K, "clocks": clk}), flush=True)
 
 
 def main():
