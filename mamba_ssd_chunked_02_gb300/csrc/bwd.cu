@@ -1,4 +1,5 @@
-// bwd.cu -- backward pass of the SSD in the chunked form (CUDA cores, fp32).
+// bwd.cu -- backward pass of the SSD in the chunked form: the orchestration
+// around the forward's stage 2 and stage 4 kernels, and the kernels between them.
 //
 // The pages give no backward method; they only note that end-to-end training
 // speed also depends on one ("NVIDIA、cuTileでMamba-2フォワードパスを高速化"
@@ -31,12 +32,8 @@
 //     dD     = sum over (b, t) of dy . x
 //   (dcum is the gradient with respect to the natural-log cumsum, cum_t = A sum dt:
 //   the row and column sums of dCB (.) CB (.) decay collapse into the two dots.)
-//   The group gradients, summed over the group's heads with
-//   dCB_ij = exp2(c2_i - c2_j) dt_j (dy_i . x_j):
-//     dC_i   = sum_{j<=i} (sum_h dCB_ij) B_j + sum_h e_i Sprev^T dy_i
-//     dB_j   = sum_{i>=j} (sum_h dCB_ij) C_i + sum_h w_j Gn^T x_j
-//
-//   The group gradients are forward-output runs too, with the state
+//   The group gradients (summed over the group's heads) are forward-output
+//   runs too, with the state
 //   transposed: dC_i = sum_h S_i^T dy_i (S_i the state after token i) is stage 4
 //   with x'' = B, B'' = x, C'' = dy and carried state Sprev^T; dB_j =
 //   sum_h dt_j G_j^T x_j (G_j the adjoint of S_j) is the reversed run with
@@ -47,9 +44,9 @@
 // Kernels, after the forward's stages 1-3 recompute cum2, dtT, Sprev and the
 // final state:
 //   (stage 4)           y without the skip term
-//   (stage 2) or        sum_i e_i dy_i C_i^T per (b, c, h)            -> dSout
-//   bwd_chunk_adjoint   (stage 2's tensor-core kernel in its adjoint weight mode
-//                       where the shape allows it)
+//   (stage 2)           sum_i e_i dy_i C_i^T per (b, c, h) -> dSout: stage 2's
+//                       tensor-core kernel in its adjoint weight mode, or
+//                       bwd_chunk_adjoint where the shape does not allow it
 //   bwd_state_pass_rev  reverse pass over chunks, in place            -> Gn, dinit
 //   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
 //                       copies of B and C, cum2' and dt' rows)
