@@ -46,6 +46,13 @@ CASES = [
     (wl(2, 300, 4, 32, 64, 1, 128, seed=74), False, True),             # ragged tail, no D
     (wl(1, 200, 2, 128, 256, 1, 64, "f32", init=0.1, seed=75), True, True),   # two p tiles
     (wl(1, 192, 3, 64, 32, 3, 64, seed=76), True, True),               # one head per group
+    # L = 256 with N = 256: stage 4's fp32-output staging does not fit, the y and
+    # y' runs fall back to the CUDA cores while the split-head runs (N'' = 64) and
+    # the chunk adjoints stay on the tensor cores
+    (wl(1, 512, 2, 64, 256, 1, 256, init=0.1, seed=78), True, True),
+    # P = 128: the forward kernels run on the CUDA cores, the split-head runs
+    # (P'' = 64, N'' = P = 128) on the tensor cores
+    (wl(1, 256, 2, 128, 128, 1, 128, seed=79), True, True),
 ]
 
 
