@@ -133,7 +133,7 @@ Carve carve(const Dims& d) {
 // the chunk adjoints dSout / Gn), Sprev in the I/O type, the final state, an
 // I/O-type copy of Gn, y without the skip term and y' (fp32), the reordered
 // inputs of the three output runs, Sprev^T and Gn^T, the per-run-head cum2 /
-// dt rows, and the dC / dB runs' per-head outputs (fp32).
+// dt rows, and the dC / dB runs' per-head outputs (I/O type).
 struct BwdCarve {
     size_t cum2, dtT, dS, Sprev, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, xB, xCr, xr,
         SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, total;
@@ -151,7 +151,6 @@ BwdCarve bwd_carve(const Dims& d) {
     const size_t xy32 = align256(sizeof(float) * (size_t)(d.b * d.T * d.H * d.P));
     const size_t bcE = align256(E * (size_t)(d.b * d.T * d.G * d.N));
     const size_t hnE = align256(E * (size_t)(d.b * d.T * d.H * d.N));
-    const size_t hn32 = align256(sizeof(float) * (size_t)(d.b * d.T * d.H * d.N));
     size_t o = 0;
     auto take = [&](size_t& f, size_t n) { f = o; o += n; };
     take(c.cum2, cum);
@@ -176,8 +175,8 @@ BwdCarve bwd_carve(const Dims& d) {
     take(c.dtTd, cumq);
     take(c.cum2rd, cumq);
     take(c.onesd, cumq);
-    take(c.yC, hn32);
-    take(c.zB, hn32);
+    take(c.yC, hnE);
+    take(c.zB, hnE);
     c.total = o;
     return c;
 }
@@ -485,7 +484,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     m2::BwdWork w{dS,           at(cv.GnIO),     at(cv.yno),      at(cv.yr),    at(cv.dyr),
                   at(cv.Br),    at(cv.Cr),       atf(cv.cum2r),   atf(cv.ones), at(cv.xB),
                   at(cv.xCr),   at(cv.xr),       at(cv.SprevT),   at(cv.GnT),   atf(cv.cum2d),
-                  atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   atf(cv.yC),   atf(cv.zB)};
+                  atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   at(cv.yC),    at(cv.zB)};
     if (e == cudaSuccess)
         e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
                                 dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);

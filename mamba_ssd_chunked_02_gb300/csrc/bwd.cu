@@ -51,8 +51,8 @@
 //   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
 //                       copies of B and C, cum2' and dt' rows)
 //   bwd_transpose       Sprev^T and Gn^T
-//   (stage 4, 3 runs)   y', the dC run and the dB run (tensor cores where the
-//                       forward uses them, fp32 outputs)
+//   (stage 4, 3 runs)   y' (fp32), the dC run and the dB run (per-head outputs in
+//                       the I/O type; tensor cores where the shape allows them)
 //   bwd_token           per (b, c, h): dx, ddt, and dA, dD partial sums
 //   bwd_bc_reduce       dC and dB summed over each group's heads
 // bwd_chunk_adjoint's contraction goes through mm_tile, a 64x64 fp32 tile on
@@ -382,11 +382,12 @@ bwd_transpose(const TS* __restrict__ in, TI* __restrict__ out, int P, int N) {
     }
 }
 
-// --- dC and dB from the two transposed-state runs, summed over each group's
-// heads: dC[t] = sum_h yC[h, t]; dB[t] = sum_h dt_h[t] zB[h, reversed t].
-// One CTA per (token, b).
+// --- dC and dB from the two transposed-state runs (their per-head outputs in
+// the I/O type), summed over each group's heads in fp32: dC[t] = sum_h yC[h, t];
+// dB[t] = sum_h dt_h[t] zB[h, reversed t].  One CTA per (token, b).
+template <typename TI>
 __global__ void __launch_bounds__(kThreads)
-bwd_bc_reduce(const float* __restrict__ yC, const float* __restrict__ zB,
+bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
               const float* __restrict__ dtT, float* __restrict__ dB, float* __restrict__ dC,
               int T, int H, int G, int N, int L) {
     const int t = blockIdx.x, b = blockIdx.y;
@@ -395,15 +396,15 @@ bwd_bc_reduce(const float* __restrict__ yC, const float* __restrict__ zB,
     const int tr = c * L + (Lc - 1 - k);   // where the reversed run wrote token t
     const int hpg = H / G;
     const int64_t rowhn = (int64_t)H * N, bt = (int64_t)b * T;
-    const float* yc = yC + (bt + t) * rowhn;
-    const float* zb = zB + (bt + tr) * rowhn;
+    const TI* yc = yC + (bt + t) * rowhn;
+    const TI* zb = zB + (bt + tr) * rowhn;
     for (int e = threadIdx.x; e < G * N; e += kThreads) {
         const int g = e / N, n = e - g * N;
         float sc = 0.f, sb = 0.f;
         for (int hh = 0; hh < hpg; ++hh) {
             const int h = g * hpg + hh;
-            sc += yc[(int64_t)h * N + n];
-            sb = fmaf(dtT[((int64_t)b * H + h) * T + t], zb[(int64_t)h * N + n], sb);
+            sc += to_f32(yc[(int64_t)h * N + n]);
+            sb = fmaf(dtT[((int64_t)b * H + h) * T + t], to_f32(zb[(int64_t)h * N + n]), sb);
         }
         dC[(bt + t) * (int64_t)G * N + e] = sc;
         dB[(bt + t) * (int64_t)G * N + e] = sb;
@@ -514,20 +515,21 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     if (g1 >= (int64_t(1) << 31) || g4 >= (int64_t(1) << 31) || gt >= (int64_t(1) << 31) ||
         d.T >= (int64_t(1) << 31) || d.b >= 65536)
         return cudaErrorInvalidValue;
-    // Stage 4 with y in fp32 (tensor cores where the shape allows them; the
-    // CUDA-core kernel otherwise or where that variant does not fit).
+    // Stage 4 with y in fp32 (y32) or the I/O type (tensor cores where the shape
+    // allows them; the CUDA-core kernel otherwise or where the fp32 variant's
+    // staging does not fit).
     auto out4 = [&](const Dims& dd, const void* x4, const void* B4, const void* C4, const float* c4,
-                    const float* d4, const void* S4, const float* y4) {
-        float* yo = const_cast<float*>(y4);
+                    const float* d4, const void* S4, const void* y4, bool y32) {
+        void* yo = const_cast<void*>(y4);
         if (tc && tc_supported(dd)) {
             const cudaError_t r = launch_chunk_out_tc(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err,
-                                                      st, nullptr, false, true);
+                                                      st, nullptr, false, y32);
             if (r != cudaErrorNotSupported) return r;
         }
-        return launch_chunk_out_simt(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, true);
+        return launch_chunk_out_simt(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, y32);
     };
-    // y without the skip term.
-    cudaError_t e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno);
+    // y without the skip term (fp32: its dots with dy set the decay gradients).
+    cudaError_t e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno, true);
     if (e != cudaSuccess) return e;
     // Chunk adjoints sum_i e_i dy_i C_i^T: stage 2's tensor-core contraction in
     // its adjoint weight mode where the shape allows it.
@@ -558,7 +560,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // y' = stage 4 on the reversed inputs: x' = dy, B' = C, C' = B, Gn carried.
     const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
-    e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr);
+    e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
     if (e != cudaSuccess) return e;
     Dims d2 = d;   // Q*H heads of N/Q, H groups of Q, state dimension P
     d2.H = Q * d.H;
@@ -566,12 +568,14 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     d2.N = d.P;
     d2.G = d.H;
     set_contiguous(d2);
-    e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC);          // S^T dy
-    if (e == cudaSuccess) e = out4(d2, w.xCr, w.dyr, w.xr, w.cum2rd, w.onesd, w.GnT, w.zB);   // G^T x
+    // The per-head outputs in the I/O type: the head sum that follows is in fp32.
+    e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC, false);          // S^T dy
+    if (e == cudaSuccess)
+        e = out4(d2, w.xCr, w.dyr, w.xr, w.cum2rd, w.onesd, w.GnT, w.zB, false);   // G^T x
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
-    bwd_bc_reduce<<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
-        w.yC, w.zB, a.dtT, a.dB, a.dC, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
+    bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
+        static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
     return cudaGetLastError();
 }
 

@@ -121,8 +121,8 @@ struct BwdWork {
     float* dtTd;    // [b,Q*H,T]
     float* cum2rd;  // [b,Q*H,T]
     float* onesd;   // [b,Q*H,T]
-    float* yC;      // [b,T,H,N] fp32: S^T dy per head
-    float* zB;      // [b,T,H,N] fp32: G^T x per head (reversed chunks)
+    void* yC;       // [b,T,H,N] S^T dy per head (I/O type)
+    void* zB;       // [b,T,H,N] G^T x per head, reversed chunks (I/O type)
 };
 // tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
 // dA and dD (if given) are accumulated into (zero them first); dinit may be null.

@@ -239,7 +239,7 @@ def test_bwd_workspace_size_formula(lib):
     the reordered inputs of the three output runs (dy, x reversed; B, C reversed;
     per-head B and reversed C; cum2' and dt' = 1), Sprev^T and Gn^T, cum2 / dt
     rows per run head (Q = N/64 of them per head), and the dC / dB runs' per-head
-    outputs (fp32), each rounded up to 256 bytes."""
+    outputs (I/O type), each rounded up to 256 bytes."""
     a256 = lambda v: (v + 255) // 256 * 256
     s = shp()
     b, T, H, P, N, G, L, E = 2, 512, 8, 64, 128, 1, 256, 2
@@ -249,7 +249,7 @@ def test_bwd_workspace_size_formula(lib):
     want = (4 * cum + a256(4 * st) + 4 * a256(E * st) + a256(4 * b * H * P * N) +
             2 * a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
             2 * a256(E * b * T * G * N) + 2 * a256(E * b * T * H * N) +
-            4 * a256(4 * Q * b * H * T) + 2 * a256(4 * b * T * H * N))
+            4 * a256(4 * Q * b * H * T) + 2 * a256(E * b * T * H * N))
     assert m2.bwd_workspace_size(s) == want
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
 
