@@ -411,6 +411,14 @@ bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
     }
 }
 
+// Elements 2 pp and 2 pp + 1 of a row, as floats (4- or 8-byte load).
+__device__ __forceinline__ float2 load_pair(const float* __restrict__ p, int pp) {
+    return reinterpret_cast<const float2*>(p)[pp];
+}
+__device__ __forceinline__ float2 load_pair(const __nv_bfloat16* __restrict__ p, int pp) {
+    return __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(p)[pp]);
+}
+
 // --- Per (b, c, h): dx, ddt and the dA, dD partial sums from y' (reversed) and
 // y without the skip term.  A warp per token, lanes over p.  Grid: b*nc*H.
 template <typename TI>
@@ -443,45 +451,49 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const float Dh = a.D ? a.D[h] : 0.f;
     const int64_t sxy = (int64_t)a.H * P;
     const int64_t base = ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
-    const TI* x = static_cast<const TI*>(a.x) + base;
-    const TI* dy = static_cast<const TI*>(a.dy) + base;
-    const float* yno = a.yno + base;
-    const float* yr = a.yr + base;
-    float* dx = a.dx + base;
+    const TI* __restrict__ x = static_cast<const TI*>(a.x) + base;
+    const TI* __restrict__ dy = static_cast<const TI*>(a.dy) + base;
+    const float* __restrict__ yno = a.yno + base;
+    const float* __restrict__ yr = a.yr + base;
+    float* __restrict__ dx = a.dx + base;
     float yx = 0.f;
-    // Two tokens per warp per iteration (j and j + 8), their loads issued together.
-    constexpr int kW = kThreads / 32;
-    for (int j0 = warp; j0 < Lc; j0 += 2 * kW) {
-        float xy[2] = {0.f, 0.f}, dyy[2] = {0.f, 0.f}, dyx[2] = {0.f, 0.f};
+    // Four tokens per warp per iteration (j0 + 8 u), p in pairs (8-byte loads),
+    // all of an iteration's loads issued before their values are used.
+    constexpr int kW = kThreads / 32, kU = 4;
+    const int P2 = P / 2;   // P is even
+    for (int j0 = warp; j0 < Lc; j0 += kU * kW) {
+        float xy[kU], dyy[kU];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kU; ++u) {
+            xy[u] = 0.f;
+            dyy[u] = 0.f;
             const int j = j0 + u * kW;
-            if (j >= Lc) break;
+            if (j >= Lc) continue;
             const int jr = Lc - 1 - j;   // where the reversed run wrote token j
             const float dtj = s_dt[j];
-            for (int p = lane; p < P; p += 32) {
-                const float yp = yr[jr * sxy + p];
-                const float xv = to_f32(x[j * sxy + p]);
-                const float dv = to_f32(dy[j * sxy + p]);
-                dx[j * sxy + p] = fmaf(dtj, yp, Dh * dv);
-                xy[u] = fmaf(xv, yp, xy[u]);
-                dyy[u] = fmaf(dv, yno[j * sxy + p], dyy[u]);
-                dyx[u] = fmaf(dv, xv, dyx[u]);
+            for (int pp = lane; pp < P2; pp += 32) {
+                const float2 yp = reinterpret_cast<const float2*>(yr + jr * sxy)[pp];
+                const float2 yn = reinterpret_cast<const float2*>(yno + j * sxy)[pp];
+                const float2 xv = load_pair(x + j * sxy, pp);
+                const float2 dv = load_pair(dy + j * sxy, pp);
+                reinterpret_cast<float2*>(dx + j * sxy)[pp] =
+                    make_float2(fmaf(dtj, yp.x, Dh * dv.x), fmaf(dtj, yp.y, Dh * dv.y));
+                xy[u] = fmaf(xv.x, yp.x, fmaf(xv.y, yp.y, xy[u]));
+                dyy[u] = fmaf(dv.x, yn.x, fmaf(dv.y, yn.y, dyy[u]));
+                yx = fmaf(dv.x, xv.x, fmaf(dv.y, xv.y, yx));
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kU; ++u) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 xy[u] += __shfl_xor_sync(0xffffffffu, xy[u], o);
                 dyy[u] += __shfl_xor_sync(0xffffffffu, dyy[u], o);
-                dyx[u] += __shfl_xor_sync(0xffffffffu, dyx[u], o);
             }
             const int j = j0 + u * kW;
             if (lane == 0 && j < Lc) {
                 s_ddt[j] = xy[u];
                 s_dcum[j] = dyy[u] - s_dt[j] * xy[u];
-                yx += dyx[u];
             }
         }
     }
