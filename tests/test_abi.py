@@ -274,3 +274,15 @@ def test_bwd_validates_arguments_without_launching(lib):
     assert call(nbytes=ws - 1) == m2.ERR_WORKSPACE
     assert call(workspace=vp((1 << 20) + 16)) == m2.ERR_WORKSPACE  # not 256-byte aligned
     assert call(shape=shp(headdim=3)) == m2.ERR_UNSUPPORTED
+
+
+def test_backward_and_decode_bindings_refuse_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 64, 2, 16)
+    args = (x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 16),
+            torch.zeros(1, 64, 1, 16))
+    with pytest.raises(ValueError, match="CUDA"):
+        m2.ssd_bwd(*args, dy=torch.zeros_like(x), chunk_size=64)
+    with pytest.raises(ValueError, match="CUDA"):
+        m2.ssd_decode(torch.zeros(1, 2, 16, 16), torch.zeros(1, 2, 16), torch.zeros(1, 2),
+                      torch.zeros(2), torch.zeros(1, 1, 16), torch.zeros(1, 1, 16))
