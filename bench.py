@@ -79,6 +79,11 @@ def parse_args():
                     help="time stages 2+3 as the one fused kernel (mamba2_ssd_chunk_state_pass)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiler captures)")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="override the workload's sequence length (profiler captures)")
+    ap.add_argument("--nheads", type=int, default=0,
+                    help="override the workload's head count, a multiple of its groups "
+                         "(profiler captures)")
     return ap.parse_args()
 
 
@@ -509,6 +514,12 @@ def main():
     w = workload(args.workload)
     if args.batch > 0:
         w = w.scaled(batch=args.batch, name=w.name.replace(f" b{w.batch} ", f" b{args.batch} "))
+    if args.seqlen > 0:
+        w = w.scaled(seqlen=args.seqlen, name=w.name.replace(f" T{w.seqlen} ", f" T{args.seqlen} "))
+    if args.nheads > 0:
+        if args.nheads % w.ngroups:
+            raise SystemExit("--nheads must be a multiple of the workload's groups")
+        w = w.scaled(nheads=args.nheads, name=w.name.replace(f" H{w.nheads} ", f" H{args.nheads} "))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
