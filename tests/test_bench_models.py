@@ -51,3 +51,24 @@ def test_backward_byte_model_term_by_term():
     want_i = b * T * (H * (2 * P * 2 + 4 * P + 8 + 2 * 16 * P * N / L) + G * (2 * N * 2 + 8 * N)) + \
         3 * 4 * b * H * P * N
     assert bench.bwd_bytes(wi) == want_i
+
+
+def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+    """bench.traffic_from_profile returns the committed ncu traffic of a kernel
+    while its source hash matches the summary, and None once the source differs
+    (counters taken on another kernel say nothing about this one)."""
+    w = W.MAMBA2_2P7B
+    for k in ("chunk_out", "chunk_state", "state_pass", "chunk_cumsum"):
+        t = bench.traffic_from_profile(k, w)
+        assert t is not None and t > 0, k
+    # the same summary against a copy of the repository whose stage-4 source differs
+    root = tmp_path / "repo"
+    (root / "profiles").mkdir(parents=True)
+    src = "mamba_ssd_chunked_02_gb300/csrc/k4_chunk_out_tc.cu"
+    (root / src).parent.mkdir(parents=True)
+    summary = (bench.os.path.join(bench.ROOT, "profiles", "chunk_out_mamba2-2.7b-layer.md"))
+    (root / "profiles" / "chunk_out_mamba2-2.7b-layer.md").write_text(open(summary).read())
+    (root / src).write_text(open(bench.os.path.join(bench.ROOT, src)).read() + "\n// edited\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.traffic_from_profile("chunk_out", w) is None
+    assert bench.traffic_from_profile("chunk_state", w) is None       # no summary there
