@@ -102,8 +102,36 @@ def pin_skip_closed_form(lib=None):
     return bool(np.abs(g["dD"] - dD).max() < 1e-12 * (np.abs(dD).max() + 1))
 
 
+def pin_quadratic_closed_forms(lib=None):
+    """Brute force from the quadratic view of the recurrence (every decay the
+    explicit sum of a_r = dt_r A between the two tokens):
+        dinit = sum_t e^{a_0 + .. + a_t} dy_t C_t^T + e^{a_0 + .. + a_{T-1}} dfinal
+        dx_s  = dt_s [sum_{t>=s} e^{a_{s+1} + .. + a_t} (C_t . B_s) dy_t
+                      + e^{a_{s+1} + .. + a_{T-1}} dfinal B_s] + D dy_s"""
+    inp, gr, G = problem(b=1, T=9, H=2, P=2, N=3, G=2, seed=17)
+    g = oracle.ssd_backward(**inp, **gr, ngroups=G, lib=lib)
+    x, dt, A, B, C, D = inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"]
+    dy, dfin = gr["dy"], gr["dfinal"]
+    T, H = x.shape[1], x.shape[2]
+    ok = True
+    for h in range(H):
+        gg = h // (H // G)
+        a = dt[0, :, h] * A[h]
+        dinit = np.exp(a.sum()) * dfin[0, h]
+        for t in range(T):
+            dinit = dinit + np.exp(a[:t + 1].sum()) * np.outer(dy[0, t, h], C[0, t, gg])
+        ok &= np.abs(g["dinit"][0, h] - dinit).max() < 1e-12 * (np.abs(dinit).max() + 1)
+        for s_ in range(T):
+            acc = np.exp(a[s_ + 1:].sum()) * (dfin[0, h] @ B[0, s_, gg])
+            for t in range(s_, T):
+                acc = acc + np.exp(a[s_ + 1:t + 1].sum()) * (C[0, t, gg] @ B[0, s_, gg]) * dy[0, t, h]
+            dx = dt[0, s_, h] * acc + D[h] * dy[0, s_, h]
+            ok &= np.abs(g["dx"][0, s_, h] - dx).max() < 1e-12 * (np.abs(dx).max() + 1)
+    return bool(ok)
+
+
 PINS = {"finite_differences": pin_finite_differences, "homogeneity": pin_homogeneity,
-        "skip_closed_form": pin_skip_closed_form}
+        "skip_closed_form": pin_skip_closed_form, "quadratic_closed_forms": pin_quadratic_closed_forms}
 
 
 @pytest.mark.parametrize("name", sorted(PINS))
