@@ -135,25 +135,35 @@ def peaks():
 
 
 def traffic_from_profile(kernel, w):
-    """DRAM bytes per launch recorded by the committed ncu summary of this kernel
-    and workload, or None when absent or taken on a different kernel source."""
+    """DRAM bytes per launch recorded with the committed ncu summary of this kernel
+    and workload (profiles/<kernel>_<workload>.json), or None when absent or taken
+    on a different kernel source."""
     tag = w.name.split()[0]
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{tag}.json")
     if not os.path.exists(path):
         return None
-    fields = {}
-    for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    src = fields.get("source")
-    if not src or "traffic_bytes_per_launch" not in fields:
+    try:
+        with open(path) as fh:
+            fields = json.load(fh)
+        src = fields["source"]
+        want = fields["source_sha256_16"]
+        traffic = float(fields["traffic_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
         return None
     spath = os.path.join(ROOT, src)
-    if not os.path.exists(spath) or hashlib.sha256(open(spath, "rb").read()).hexdigest()[:16] \
-            != fields.get("source_sha256_16"):
+    if not os.path.exists(spath) or hashlib.sha256(open(spath, "rb").read()).hexdigest()[:16] != want:
         return None
-    return float(fields["traffic_bytes_per_launch"])
+    return traffic
+
+
+def io_floor(w):
+    """Bytes a single fused kernel would have to move at least: read x, dt, B, C
+    once, write y once, plus the state I/O (final_state, and the initial state
+    when given); no intermediate in HBM."""
+    b, T, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    E = 2 if w.dtype == "bf16" else 4
+    init = 1 if w.init_std > 0 else 0
+    return b * T * (H * (2 * P * E + 4) + 2 * G * N * E) + 4 * b * H * P * N * (1 + init)
 
 
 # --------------------------------------------------------------------- clocks ---
@@ -640,9 +650,18 @@ def main():
                  else "fallback"})
 
     t_path = max(graded_bytes / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    # Three byte counts for the same measured step: the graded four-stage model
+    # (dS and Sprev at fp32), the bytes the path's kernels are specified to move
+    # (the sum of the per-kernel models, with its actual hand-off types), and the
+    # I/O floor of a single fused kernel.
+    moved = sum(kmodel[k]["bytes"] for k in KERNELS)
+    floor = io_floor(w)
+    hbm = pk["hbm_gbs"] * 1e9
     path_roof = {"model": "four-stage HBM hand-off, dS and Sprev counted at fp32",
                  "graded_bytes": graded_bytes, "flops": flops, "roofline_ms": t_path * 1e3,
-                 "frac": t_path / (ms_step * 1e-3)}
+                 "frac": t_path / (ms_step * 1e-3),
+                 "bytes_moved": moved, "bytes_moved_frac": moved / hbm / (ms_step * 1e-3),
+                 "io_floor_bytes": floor, "io_floor_frac": floor / hbm / (ms_step * 1e-3)}
     kernels = {}
     for kname in KERNELS:
         km = kmodel[kname]

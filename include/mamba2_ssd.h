@@ -27,7 +27,13 @@
  *   - All tensors are dense, row-major, contiguous device memory, owned by the
  *     caller.  The library allocates nothing and keeps no per-call host state;
  *     it may be called concurrently from several host threads on different
- *     streams with disjoint buffers.
+ *     streams with disjoint buffers.  The one piece of state it shares between
+ *     calls is the device error word (mamba2_ssd_device_error): one 32-bit
+ *     word per device, into which every kernel of every call on that device
+ *     ORs its error bits.  A bounded wait that runs out in one stream's call is
+ *     therefore seen by every caller that reads the word, and reading it with
+ *     `clear` set clears it for all of them; callers that run several streams
+ *     at once should read and clear it from one place.
  *   - Every pointer must be 16-byte aligned (tensor-memory-accelerator copies).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronise.  Argument errors are detected on the host,
@@ -83,7 +89,7 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
 /* In mamba2_ssd_fwd on the tensor-core path, run stages 2 and 3 as the one
  * fused kernel of mamba2_ssd_chunk_state_pass instead of two kernels with dS in
  * HBM.  Same results bit for bit; slower on GB300 at the 2.7B layer shape
- * (0.317 ms against 0.243 ms for the pair), so it is not the default. */
+ * (0.321 ms against 0.244 ms for the pair), so it is not the default. */
 #define MAMBA2_FLAG_FUSED_STATE 2
 /* dS is bf16 (not fp32) in mamba2_ssd_chunk_state (output) and
  * mamba2_ssd_state_pass (input): the hand-off mamba2_ssd_fwd uses on the
@@ -353,7 +359,10 @@ MAMBA2_API mamba2_status mamba2_ssd_selftest_wait_timeout(uint32_t limit_us, voi
  *   - The call allocates nothing: no cudaMalloc, cudaFree or allocating
  *     library routine.  The first call on each device looks up the array's
  *     device address (cudaGetSymbolAddress, with that device current); make
- *     that first call before any stream capture on the device.
+ *     that first call before any stream capture on the device.  The address
+ *     is kept for the life of the process and belongs to the device's primary
+ *     context (the one the CUDA runtime uses): do not call this entry point
+ *     after cudaDeviceReset, or with another context current on the device.
  *   - Every call on a device shares the one array.  Nothing in it needs to
  *     start at zero (each stage writes what the next reads), but two calls
  *     that overlap on the GPU (different streams, no ordering between them)

@@ -416,9 +416,6 @@ def chunk_out(shape, x, B, C, cum2, dtT, Sprev, D, y, stream=None):
         _stream(stream)))
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
-
-
 def bwd_workspace_size(shape: Shape) -> int:
     return int(load().mamba2_ssd_bwd_workspace_size(ctypes.byref(shape)))
 
@@ -461,6 +458,11 @@ def ssd_bwd(x, dt, A, B, C, D=None, initial_state=None, dy=None, dfinal=None, ch
         ctypes.c_size_t(workspace.numel() * workspace.element_size() if workspace is not None else 0),
         _stream(stream)))
     return g
+
+
+# Size of the library's fixed scratch array (MAMBA2_NOALLOC_SCRATCH_BYTES in
+# include/mamba2_ssd.h; a CPU test checks that the two agree).
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def ssd_fwd_noalloc(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, ngroups=None,

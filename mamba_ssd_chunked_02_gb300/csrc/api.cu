@@ -33,7 +33,10 @@ int32_t* error_word() {
     std::lock_guard<std::mutex> lk(g_sym_mu);
     if (!g_sym_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+            cudaGetLastError();   // the failed lookup must not surface in a later launch check
+            return nullptr;
+        }
         g_sym_addr[dev] = static_cast<int32_t*>(p);
     }
     return g_sym_addr[dev];

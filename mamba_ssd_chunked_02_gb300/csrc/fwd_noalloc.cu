@@ -21,15 +21,24 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device; looked up once per
-// device (the first call on a device), with that device current.
+// device (the first call on a device), with that device current.  The cached
+// address belongs to the device's primary context, the one the CUDA runtime
+// uses; it stays valid for the life of the process unless that context is
+// destroyed (cudaDeviceReset).
 mamba2_status scratch_address(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MAMBA2_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();   // leave no error pending for the caller's next call
+        return MAMBA2_ERR_CUDA;
+    }
     if (dev < 0 || dev >= kMaxDevices) return MAMBA2_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MAMBA2_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();   // the failed lookup must not surface in a later launch check
+            return MAMBA2_ERR_CUDA;
+        }
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];

@@ -24,7 +24,7 @@ namespace m2 {
 namespace {
 
 constexpr int kThreads = 256;
-// Chunks of dS loads in flight per thread: 4 for bf16 dS (40 registers, six
+// Chunks of dS loads in flight per thread: 4 for bf16 dS (48 registers, five
 // blocks per SM), 8 for fp32 dS (measured best for each).
 template <typename TD>
 struct Depth {

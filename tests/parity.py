@@ -55,3 +55,11 @@ def sample_pairs(b, H, k, seed=0):
     while len(pairs) < min(k, b * H):
         pairs.add((int(rng.integers(b)), int(rng.integers(H))))
     return sorted(pairs)
+
+
+def sample_pairs_with_row(b, H, k, row=None, seed=0):
+    """Every head of batch row `row` (default: the last one, whose chunks are the
+    last work items of the output kernel's grid) plus `k` random (b, h) pairs."""
+    row = b - 1 if row is None else row
+    return sorted(set(sample_pairs(b, H, k, seed=seed)) | {(row, h) for h in range(H)})
+

@@ -39,6 +39,14 @@ def test_exports_every_declared_symbol(lib):
     assert set(m2.SYMBOLS) <= set(names)
 
 
+def test_noalloc_scratch_size_matches_the_header():
+    """The binding's NOALLOC_SCRATCH_BYTES is the header's MAMBA2_NOALLOC_SCRATCH_BYTES."""
+    src = open(os.path.join(ROOT, "include", "mamba2_ssd.h")).read()
+    m = re.search(r"#define\s+MAMBA2_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", src)
+    assert m, "MAMBA2_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert m2.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
 def test_version_and_status_strings(lib):
     assert re.match(r"\d+\.\d+\.\d+", m2.version())
     for code in range(6):

@@ -66,9 +66,22 @@ def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     (root / "profiles").mkdir(parents=True)
     src = "mamba_ssd_chunked_02_gb300/csrc/k4_chunk_out_tc.cu"
     (root / src).parent.mkdir(parents=True)
-    summary = (bench.os.path.join(bench.ROOT, "profiles", "chunk_out_mamba2-2.7b-layer.md"))
-    (root / "profiles" / "chunk_out_mamba2-2.7b-layer.md").write_text(open(summary).read())
+    summary = (bench.os.path.join(bench.ROOT, "profiles", "chunk_out_mamba2-2.7b-layer.json"))
+    (root / "profiles" / "chunk_out_mamba2-2.7b-layer.json").write_text(open(summary).read())
     (root / src).write_text(open(bench.os.path.join(bench.ROOT, src)).read() + "\n// edited\n")
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.traffic_from_profile("chunk_out", w) is None
     assert bench.traffic_from_profile("chunk_state", w) is None       # no summary there
+
+
+def test_io_floor_and_moved_bytes_at_the_2p7b_layer():
+    """The I/O floor (x, dt, B, C read once, y written once, final state) and the
+    bytes the path's four kernels move with the bf16 hand-off, at the 2.7B layer."""
+    w = W.MAMBA2_2P7B
+    th, tg = 8 * 4096 * 80, 8 * 4096
+    assert bench.io_floor(w) == th * (2 * 64 * 2 + 4) + tg * 2 * 128 * 2 + 8 * 80 * 64 * 128 * 4
+    k, _, _ = bench.model(w, 2)
+    moved = sum(k[n]["bytes"] for n in bench.KERNELS_SPLIT)
+    assert abs(moved / 1e6 - 1797) < 1.0
+    assert abs(bench.io_floor(w) / 1e6 - 719) < 1.0
+

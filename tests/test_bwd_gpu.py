@@ -6,7 +6,9 @@ relL2 <= 1e-4).  The pages give no backward method ("NVIDIA、cuTileでMamba-2
 on the recurrence, pinned by finite differences of the forward
 (tests/test_oracle_bwd.py).
 
-At the 2.7B layer's size the oracle takes sampled (b, h) pairs (dx, ddt), and the
+At the 2.7B layer's size the oracle takes every head of one batch row plus
+sampled (b, h) pairs (dx, ddt of each; dB and dC of that row, complete sums over
+its heads), and the
 homogeneity of the loss L = sum(dy*y) + sum(dfinal*final_state) ties the GPU
 gradients to the GPU's fp32 forward over every element: sum(dx*x) +
 sum(dinit*init) = L and sum(dC*C) = sum(dy*(y - D x)), whatever the size.
@@ -18,7 +20,7 @@ import torch
 import mamba_ssd_chunked_02_gb300 as m2
 import oracle
 from mamba_ssd_chunked_02_gb300 import workloads as W
-from parity import assert_close, metrics, sample_pairs, to_np
+from parity import assert_close, metrics, sample_pairs, sample_pairs_with_row, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -114,17 +116,23 @@ def test_backward_empty_sequence():
 
 def test_backward_full_size_sampled_and_identities():
     """The 2.7B layer (b8 T4096 H80 P64 N128 L256): dx and ddt of sampled (b, h)
-    pairs against the oracle, and the homogeneity identities against the GPU
-    forward over every element."""
+    pairs and dB, dC of one whole batch row against the oracle, and the
+    homogeneity identities against the GPU forward over every element."""
     w = W.MAMBA2_2P7B
     inp = W.make_inputs(w)
     gr = W.make_grads(w)
     got = run_bwd(w, inp, gr)
-    pairs = sample_pairs(w.batch, w.nheads, 3, seed=3)
+    # Every head of batch row 0 plus random pairs: dB and dC of row 0 sum over
+    # all of its heads (one group), so with the whole row in the oracle's pair
+    # list they are complete and are compared element by element.
+    pairs = sample_pairs_with_row(w.batch, w.nheads, 8, row=0, seed=3)
     ref = oracle.ssd_backward(**inp, **gr, ngroups=w.ngroups, pairs=pairs)
     for (b, h) in pairs:
         assert_close(got["dx"][b, :, h], ref["dx"][b, :, h], w.dtype, f"dx {b},{h}")
         assert_close(got["ddt"][b, :, h], ref["ddt"][b, :, h], w.dtype, f"ddt {b},{h}")
+    assert w.ngroups == 1
+    assert_close(got["dB"][0], ref["dB"][0], w.dtype, "dB, batch row 0")
+    assert_close(got["dC"][0], ref["dC"][0], w.dtype, "dC, batch row 0")
     # L from the fp32 forward on the same values (bf16 widens exactly), so that
     # the identity measures the backward, not the bf16 rounding of y.  Scale of
     # the sums: S = sqrt(sum (dy*y)^2) + sqrt(sum (dfinal*final)^2), the size of

@@ -12,7 +12,8 @@ import torch
 import mamba_ssd_chunked_02_gb300 as m2
 import oracle
 from mamba_ssd_chunked_02_gb300 import workloads as W
-from parity import TOL, assert_close, metrics, run_fwd, sample_pairs, to_np
+from parity import (TOL, assert_close, metrics, run_fwd, sample_pairs,
+                    sample_pairs_with_row, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -422,18 +423,56 @@ FULL = [W.MAMBA2_2P7B, W.GROUPED_INIT, W.LONG_PREFILL] + W.sweep_workloads()
 @pytest.mark.parametrize("w", FULL, ids=[w.name.split()[0] + "-" + "-".join(w.name.split()[1:3])
                                          + f"-N{w.dstate}" for w in FULL])
 def test_full_size_sampled(w):
-    """Full-size workload in the benchmark's launch configuration; sampled
-    (batch, head) pairs recomputed by the recurrent oracle."""
+    """Full-size workload in the benchmark's launch configuration, on the
+    tensor-core path; every head of the last batch row (so every head block of
+    the output kernel, both block sizes, and the grid's last work items) plus
+    32 random (batch, head) pairs recomputed by the recurrent oracle (4 random
+    pairs and one full row for the 131 k-token prefill)."""
     inp = W.make_inputs(w)
-    if w.dtype == "bf16":
-        assert m2.path(m2.shape_of(inp["x"], inp["B"], w.chunk_size, w.ngroups)) in (
-            m2.PATH_TCGEN05, m2.PATH_SIMT)
+    assert w.dtype == "bf16"
+    assert m2.path(m2.shape_of(inp["x"], inp["B"], w.chunk_size, w.ngroups)) == m2.PATH_TCGEN05
     y, f = run_fwd(inp, w)
-    k = 4 if w.seqlen >= 65536 else 8
-    pairs = sample_pairs(w.batch, w.nheads, k, seed=w.seed)
+    k = 4 if w.seqlen >= 65536 else 32
+    pairs = sample_pairs_with_row(w.batch, w.nheads, k, seed=w.seed)
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups, pairs=pairs)
     yg, fg = to_np(y), to_np(f)
     for (b, h) in pairs:
         assert_close(yg[b, :, h], yr[b, :, h], w.dtype, f"y {w.name} (b={b}, h={h})")
         assert_close(fg[b, h], fr[b, h], w.dtype, f"final {w.name} (b={b}, h={h})")
     assert np.isfinite(yg).all() and np.isfinite(fg).all()
+
+
+def test_split_and_resume_at_grouped_init_size():
+    """The grouped workload with a carried initial state (b2 T8192 H64 G8 L128,
+    initial state ~ N(0, 0.1)) run as two halves of 4096 tokens, the second
+    started from the first's final state, against one run of all 8192 tokens:
+    sampled pairs of the concatenated halves against the oracle, and the two GPU
+    results against each other over every element (each within the bound of the
+    oracle, so within twice it of each other)."""
+    w = W.GROUPED_INIT
+    assert (w.batch, w.seqlen, w.nheads, w.ngroups, w.chunk_size) == (2, 8192, 64, 8, 128)
+    inp = W.make_inputs(w)
+    y, f = run_fwd(inp, w)
+    half = w.seqlen // 2
+    h1, h2 = dict(inp), dict(inp)
+    for k_ in ("x", "dt", "B", "C"):
+        h1[k_] = inp[k_][:, :half].contiguous()
+        h2[k_] = inp[k_][:, half:].contiguous()
+    w2 = w.scaled(seqlen=half)
+    y1, f1 = run_fwd(h1, w2)
+    h2["initial_state"] = f1.cpu()
+    y2, f2 = run_fwd(h2, w2)
+    ys = to_np(torch.cat([y1, y2], dim=1))
+    del y1, y2
+    pairs = sample_pairs_with_row(w.batch, w.nheads, 32, seed=w.seed + 7)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups, pairs=pairs)
+    yg, fg, f2g = to_np(y), to_np(f), to_np(f2)
+    for (b, h) in pairs:
+        assert_close(ys[b, :, h], yr[b, :, h], w.dtype, f"split y (b={b}, h={h})")
+        assert_close(f2g[b, h], fr[b, h], w.dtype, f"split final (b={b}, h={h})")
+        assert_close(yg[b, :, h], yr[b, :, h], w.dtype, f"single y (b={b}, h={h})")
+    rel_tol, max_tol = TOL["bf16"]
+    for a, b_ in ((ys, yg), (f2g, fg)):
+        ref_rms = np.sqrt(np.mean(b_ ** 2))
+        assert np.linalg.norm(a - b_) <= 2 * rel_tol * np.linalg.norm(b_)
+        assert np.abs(a - b_).max() <= 2 * max_tol * ref_rms
