@@ -12,7 +12,7 @@ import torch
 import mamba_ssd_chunked_02_gb300 as m2
 import oracle
 from mamba_ssd_chunked_02_gb300 import workloads as W
-from parity import (TOL, assert_close, metrics, run_fwd, sample_pairs,
+from parity import (TOL, assert_close, assert_close_sampled, metrics, run_fwd, sample_pairs,
                     sample_pairs_with_row, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -436,9 +436,10 @@ def test_full_size_sampled(w):
     pairs = sample_pairs_with_row(w.batch, w.nheads, k, seed=w.seed)
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups, pairs=pairs)
     yg, fg = to_np(y), to_np(f)
-    for (b, h) in pairs:
-        assert_close(yg[b, :, h], yr[b, :, h], w.dtype, f"y {w.name} (b={b}, h={h})")
-        assert_close(fg[b, h], fr[b, h], w.dtype, f"final {w.name} (b={b}, h={h})")
+    assert_close_sampled([yg[b, :, h] for b, h in pairs], [yr[b, :, h] for b, h in pairs],
+                         pairs, w.dtype, f"y {w.name}")
+    assert_close_sampled([fg[b, h] for b, h in pairs], [fr[b, h] for b, h in pairs],
+                         pairs, w.dtype, f"final {w.name}")
     assert np.isfinite(yg).all() and np.isfinite(fg).all()
 
 
@@ -467,10 +468,11 @@ def test_split_and_resume_at_grouped_init_size():
     pairs = sample_pairs_with_row(w.batch, w.nheads, 32, seed=w.seed + 7)
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups, pairs=pairs)
     yg, fg, f2g = to_np(y), to_np(f), to_np(f2)
-    for (b, h) in pairs:
-        assert_close(ys[b, :, h], yr[b, :, h], w.dtype, f"split y (b={b}, h={h})")
-        assert_close(f2g[b, h], fr[b, h], w.dtype, f"split final (b={b}, h={h})")
-        assert_close(yg[b, :, h], yr[b, :, h], w.dtype, f"single y (b={b}, h={h})")
+    sl = lambda a: [a[b, :, h] for b, h in pairs]  # noqa: E731
+    assert_close_sampled(sl(ys), sl(yr), pairs, w.dtype, "split y")
+    assert_close_sampled(sl(yg), sl(yr), pairs, w.dtype, "single y")
+    assert_close_sampled([f2g[b, h] for b, h in pairs], [fr[b, h] for b, h in pairs], pairs,
+                         w.dtype, "split final")
     rel_tol, max_tol = TOL["bf16"]
     for a, b_ in ((ys, yg), (f2g, fg)):
         ref_rms = np.sqrt(np.mean(b_ ** 2))
