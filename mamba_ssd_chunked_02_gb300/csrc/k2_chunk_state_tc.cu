@@ -222,20 +222,21 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         if (lane == 0) {
             int last = -1;
             if (mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs)) {
-                const uint32_t bt_addr = smem_u32(sBt);
+                // Descriptors formed once; each MMA adds a constant offset / 16 (an MMA
+                // issue waits for the scalar work in front of it).
+                const uint64_t bt_desc = smem_desc_sw128(smem_u32(sBt), C::ATOM, 1024);
+                const uint64_t x_desc0 = smem_desc_sw128(smem_u32(sX), C::ATOM, 1024);
                 for (int i = 0; i < nh; ++i) {
                     const int st = i % NS, k = i / NS, ab = i & 1, ka = i >> 1;
                     if (!mbar_wait_or_abort(&bars.scaled[st], k & 1, abort, kWaitNs)) break;
                     if (!mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs)) break;
                     tc_fence_after();
-                    const uint32_t x_addr = smem_u32(sX + st * C::X_BYTES);
+                    const uint64_t xd = x_desc0 + (uint64_t)st * (C::X_BYTES >> 4);
                     const uint32_t d = tmem + ab * C::P;
 #pragma unroll
-                    for (int kk = 0; kk < L / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(bt_addr + kk * 2048, C::ATOM, 1024);
-                        const uint64_t bd = smem_desc_sw128(x_addr + kk * 2048, C::ATOM, 1024);
-                        mma_ss(d, ad, bd, C::IDESC, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < L / 16; ++kk)
+                        mma_ss(d, bt_desc + (uint64_t)(kk * (2048 >> 4)), xd + (uint64_t)(kk * (2048 >> 4)),
+                               C::IDESC, kk > 0 ? 1u : 0u);
                     mma_commit(&bars.acc_full[ab]);
                     mma_commit(&bars.xfree[st]);
                     last = i;

@@ -59,6 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe: true when the phase with the given parity has completed.
+// (try_wait may suspend the thread for a while before it returns false; a loop
+// that polls several barriers in turn needs this form.)
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // try_wait with a suspend-time hint: the thread sleeps in hardware until the
 // phase completes or about `hint_ns` pass, so a waiting warp does not spin
 // and steal issue slots from the warps doing the work.

@@ -57,10 +57,15 @@ def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     """bench.traffic_from_profile returns the committed ncu traffic of a kernel
     while its source hash matches the summary, and None once the source differs
     (counters taken on another kernel say nothing about this one)."""
+    import hashlib
+    import json
     w = W.MAMBA2_2P7B
     for k in ("chunk_out", "chunk_state", "state_pass", "chunk_cumsum"):
+        meta = json.load(open(bench.os.path.join(bench.ROOT, "profiles", f"{k}_mamba2-2.7b-layer.json")))
+        src = open(bench.os.path.join(bench.ROOT, meta["source"]), "rb").read()
+        current = hashlib.sha256(src).hexdigest()[:16] == meta["source_sha256_16"]
         t = bench.traffic_from_profile(k, w)
-        assert t is not None and t > 0, k
+        assert (t is not None and t > 0) if current else t is None, k
     # the same summary against a copy of the repository whose stage-4 source differs
     root = tmp_path / "repo"
     (root / "profiles").mkdir(parents=True)
@@ -68,9 +73,14 @@ def test_profile_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
     (root / src).parent.mkdir(parents=True)
     summary = (bench.os.path.join(bench.ROOT, "profiles", "chunk_out_mamba2-2.7b-layer.json"))
     (root / "profiles" / "chunk_out_mamba2-2.7b-layer.json").write_text(open(summary).read())
+    meta = json.load(open(summary))
     (root / src).write_text(open(bench.os.path.join(bench.ROOT, src)).read() + "\n// edited\n")
     monkeypatch.setattr(bench, "ROOT", str(root))
     assert bench.traffic_from_profile("chunk_out", w) is None
+    # the same summary against a source whose hash matches it is used
+    (root / "profiles" / "chunk_out_mamba2-2.7b-layer.json").write_text(json.dumps(
+        dict(meta, source_sha256_16=hashlib.sha256((root / src).read_bytes()).hexdigest()[:16])))
+    assert bench.traffic_from_profile("chunk_out", w) == meta["traffic_bytes_per_launch"]
     assert bench.traffic_from_profile("chunk_state", w) is None       # no summary there
 
 
