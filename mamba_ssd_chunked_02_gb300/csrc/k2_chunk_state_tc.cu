@@ -82,12 +82,16 @@ struct K2Cfg {
     // fused: two buffers of {carried state fp32 [64][128], Sprev bf16 [64][128]}
     static constexpr int F_BYTES = 2 * (64 * 128 * 4 + 64 * 128 * 2);
     static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + (kFuse ? F_BYTES : 2 * D_BYTES);
-    static constexpr int TMEM_COLS = 128;                 // 2 accumulators x 64 columns
-    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 1, 1);
+    // Tensor memory: 2 accumulators x 64 columns, then B^T as the MMA's A operand
+    // (lane = state dim n, L keys as 16-bit pairs: L / 2 columns).
+    static constexpr int TMEM_COLS = 256;
+    static constexpr uint32_t COL_BT = 128;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 0, 1);   // A in tensor memory, B MN-major
 };
 
 struct K2Bars {
     uint64_t bt_full;
+    uint64_t bt_tmem;       // B^T copied into tensor memory by the epilogue warps
     uint64_t full[6], scaled[6], xfree[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
@@ -137,6 +141,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 
     if (threadIdx.x == 0) {
         mbar_init(&bars.bt_full, 1);
+        mbar_init(&bars.bt_tmem, 128);
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bars.full[i], 1);
             mbar_init(&bars.scaled[i], 32 * C::kSW);
@@ -221,10 +226,10 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // ----------------------------------------------------------- MMA issue
         if (lane == 0) {
             int last = -1;
-            if (mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs)) {
+            if (mbar_wait_or_abort(&bars.bt_tmem, 0, abort, kWaitNs)) {
+                tc_fence_after();
                 // Descriptors formed once; each MMA adds a constant offset / 16 (an MMA
                 // issue waits for the scalar work in front of it).
-                const uint64_t bt_desc = smem_desc_sw128(smem_u32(sBt), C::ATOM, 1024);
                 const uint64_t x_desc0 = smem_desc_sw128(smem_u32(sX), C::ATOM, 1024);
                 for (int i = 0; i < nh; ++i) {
                     const int st = i % NS, k = i / NS, ab = i & 1, ka = i >> 1;
@@ -235,8 +240,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                     const uint32_t d = tmem + ab * C::P;
 #pragma unroll
                     for (int kk = 0; kk < L / 16; ++kk)
-                        mma_ss(d, bt_desc + (uint64_t)(kk * (2048 >> 4)), xd + (uint64_t)(kk * (2048 >> 4)),
-                               C::IDESC, kk > 0 ? 1u : 0u);
+                        mma_ts(d, tmem + C::COL_BT + 8 * kk, xd + (uint64_t)(kk * (2048 >> 4)), C::IDESC,
+                               kk > 0 ? 1u : 0u);
                     mma_commit(&bars.acc_full[ab]);
                     mma_commit(&bars.xfree[st]);
                     last = i;
@@ -339,6 +344,36 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
+        // B^T into tensor memory, once per CTA: lane n takes B[s][n] for every key s
+        // from the TMA-loaded tile (64-wide MN blocks, 128-byte swizzled: piece k
+        // of row s at k ^ (s & 7)) and writes the pairs (s, s+1) as 32-bit
+        // columns.  The tensor core then reads only x~ from shared memory: an
+        // M128 N64 MMA with both operands there would take the whole shared-memory
+        // bandwidth, which the scaling warps also need.
+        {
+            const bool okb = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs));
+            if (okb) {
+                const uint8_t* base = sBt + (nl >> 6) * C::ATOM + ((nl & 7) << 1);
+                const int k16 = (nl & 63) >> 3;                 // this n's 16-byte piece of a row
+#pragma unroll 1
+                for (int s0 = 0; s0 < L; s0 += 64) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int sa = s0 + 2 * e, sb = sa + 1;
+                        const uint32_t lo = *reinterpret_cast<const uint16_t*>(
+                            base + sa * 128 + ((k16 ^ (sa & 7)) << 4));
+                        const uint32_t hi = *reinterpret_cast<const uint16_t*>(
+                            base + sb * 128 + ((k16 ^ (sb & 7)) << 4));
+                        w[e] = lo | (hi << 16);
+                    }
+                    tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + C::COL_BT + (s0 >> 1), w);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.bt_tmem);
+        }
         if constexpr (kFuse) {
             const int64_t bH = (int64_t)fa.nb * H;
             const int Lc = min(L, T - c * L);
