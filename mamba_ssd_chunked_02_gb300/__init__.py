@@ -8,8 +8,10 @@ is no CPU path: calling any entry point without the built library or without a
 CUDA device raises.
 
 Entry points (same names as the C ABI, minus the ``mamba2_ssd_`` prefix):
-  ssd_fwd, chunk_cumsum, chunk_state, state_pass, chunk_out,
-  workspace_size, path, check_shape, device_error, version.
+  ssd_fwd, ssd_fwd_noalloc, chunk_cumsum, chunk_state, state_pass,
+  chunk_state_pass, chunk_out, ssd_bwd, ssd_decode, workspace_size,
+  bwd_workspace_size, chunk_state_pass_workspace_size, path, check_shape,
+  tile_choice, tile_override, device_error, selftest_wait_timeout, version.
 
 Pages: "NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr),
 "Mamba-2 아키텍처의 핵심 연산" (y_t = c_t^T h_t + D x_t) and "세 가지 핵심 커널
@@ -43,7 +45,8 @@ SYMBOLS = ("mamba2_ssd_check_shape", "mamba2_ssd_path", "mamba2_ssd_workspace_si
            "mamba2_status_string", "mamba2_ssd_version", "mamba2_ssd_fwd_noalloc",
            "mamba2_ssd_chunk_state_pass", "mamba2_ssd_chunk_state_pass_workspace_size",
            "mamba2_ssd_selftest_wait_timeout", "mamba2_ssd_decode", "mamba2_ssd_fwd_timed",
-           "mamba2_ssd_fwd_strided", "mamba2_ssd_bwd", "mamba2_ssd_bwd_workspace_size")
+           "mamba2_ssd_fwd_strided", "mamba2_ssd_bwd", "mamba2_ssd_bwd_workspace_size",
+           "mamba2_ssd_tile_choice", "mamba2_ssd_tile_override")
 
 
 class Shape(ctypes.Structure):
@@ -128,6 +131,10 @@ def load():
         lib.mamba2_ssd_bwd_workspace_size.restype = ctypes.c_size_t
         lib.mamba2_ssd_bwd.argtypes = [sp] + [vp] * 16 + [vp, ctypes.c_size_t, vp]
         lib.mamba2_ssd_bwd.restype = ctypes.c_int
+        lib.mamba2_ssd_tile_choice.argtypes = [sp, ctypes.POINTER(i32)]
+        lib.mamba2_ssd_tile_choice.restype = ctypes.c_int
+        lib.mamba2_ssd_tile_override.argtypes = [i32] * 4
+        lib.mamba2_ssd_tile_override.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -484,6 +491,23 @@ def ssd_fwd_noalloc(x, dt, A, B, C, D=None, initial_state=None, chunk_size=256, 
         _stream(stream)]
     _check("mamba2_ssd_fwd_noalloc", load().mamba2_ssd_fwd_noalloc(ctypes.byref(sh), *args))
     return y, final_state
+
+
+SOURCE_MODEL, SOURCE_TABLE, SOURCE_OVERRIDE = 0, 1, 2
+
+
+def tile_choice(shape: Shape) -> dict:
+    """Launch choices of the tensor-core kernels for `shape` (mamba2_ssd_tile_choice)."""
+    out = (ctypes.c_int32 * 6)()
+    _check("mamba2_ssd_tile_choice", load().mamba2_ssd_tile_choice(ctypes.byref(shape), out))
+    return {"stage2_heads": out[0], "stage2_source": out[1], "stage4_v1": out[2],
+            "stage4_v2": out[3], "stage4_pairs1": out[4], "stage4_source": out[5]}
+
+
+def tile_override(stage2_heads=0, stage4_v1=0, stage4_v2=0, stage4_waves1=0):
+    """Force launch choices for later calls (mamba2_ssd_tile_override); zeros clear."""
+    _check("mamba2_ssd_tile_override",
+           load().mamba2_ssd_tile_override(stage2_heads, stage4_v1, stage4_v2, stage4_waves1))
 
 
 def device_error(clear=True) -> int:

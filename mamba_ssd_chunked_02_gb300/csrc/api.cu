@@ -531,6 +531,23 @@ mamba2_status mamba2_ssd_selftest_wait_timeout(uint32_t limit_us, void* stream) 
                                                       static_cast<cudaStream_t>(stream)));
 }
 
+mamba2_status mamba2_ssd_tile_choice(const mamba2_ssd_shape* shape, int32_t* out) {
+    const mamba2_status st = check(shape);
+    if (st != MAMBA2_OK) return st;
+    if (!out) return MAMBA2_ERR_INVALID_ARG;
+    const Dims d = dims_of(shape);
+    if (!use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
+    int src2 = 0;
+    out[0] = m2::k2_heads_per_cta(d, &src2);
+    out[1] = src2;
+    const m2::Split4 sp = m2::k4_split(d);
+    out[2] = sp.v1;
+    out[3] = sp.v2;
+    out[4] = (int32_t)sp.n1_bc;
+    out[5] = sp.src;
+    return MAMBA2_OK;
+}
+
 const char* mamba2_status_string(mamba2_status status) {
     switch (status) {
         case MAMBA2_OK: return "ok";

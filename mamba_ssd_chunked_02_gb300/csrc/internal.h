@@ -139,6 +139,38 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaSt
 // True when the tcgen05 kernels handle this shape.
 bool tc_supported(const Dims& d);
 
+// SMs of the current device (cached per device); kFallbackSMs, a GB300's
+// count, when no device can be queried.
+constexpr int kFallbackSMs = 152;
+int sm_count();
+
+// Per-shape launch choices found by the offline sweep (tiles.cu, tile_table.inc).
+struct TileChoice {
+    int32_t N, P, L, hpg;      // state size, head dim, chunk size, heads per group
+    int64_t bnc_lo, bnc_hi;    // range of b * nc the entry covers
+    int32_t k2_hpc;            // stage 2: heads per CTA
+    int32_t k4_v1, k4_v2;      // stage 4: head-block sizes of the two grid regions
+    int32_t k4_waves1;         // stage 4: SM waves the v1 region fills (0: v1 everywhere)
+};
+// The table entry for this shape, or null.
+const TileChoice* find_tile(const Dims& d);
+// Tuning override k (0: stage-2 heads per CTA, 1/2: stage-4 v1/v2, 3: stage-4
+// v1-region waves), 0 when not set (mamba2_ssd_tile_override).
+int tile_override(int k);
+
+// Where a launch choice comes from.
+enum : int { kFromModel = 0, kFromTable = 1, kFromOverride = 2 };
+// Stage 2 (tensor-core, unfused): heads per CTA and its source.
+int k2_heads_per_cta(const Dims& d, int* src);
+// Stage 4 (tensor-core): head-block sizes v1, v2, CTAs of the v1 region (n1),
+// all CTAs, the (b, c) pairs of the v1 region and the source.
+struct Split4 {
+    int v1, v2;
+    int64_t n1, ctas, n1_bc;
+    int src;
+};
+Split4 k4_split(const Dims& d);
+
 // Device-side error bits (OR-ed into the library's error word).
 enum : int32_t {
     kErrTimeoutK2 = 1 << 0,    // a bounded wait ran out in the tcgen05 chunk-state kernel

@@ -509,26 +509,13 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (threadIdx.x == 0 && bars.abort) record_error(err, kFuse ? (kErrTimeoutK2 | kErrChainK23) : kErrTimeoutK2);
 }
 
-int num_sms() {
-    static int cached[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 148;
-    }
-    return cached[dev];
-}
-
 // Heads per CTA (one CTA per SM at a time): the divisor v of H/G that
 // minimises (waves of CTAs) x (v + 4), i.e. per-SM time in head units with a
 // CTA's fixed work (loading B^T, filling and draining the x ring) counted as
 // about four heads (fitted to measurements: at b8 T4096 H80 N128 whole-path
 // times of 440, 437, 429 and 423 us for 10, 20, 40 and 80 heads per CTA).
 int pick_hpc(const Dims& d, int64_t outer) {
-    const int64_t hpg = d.H / d.G, sms = num_sms();
+    const int64_t hpg = d.H / d.G, sms = sm_count();
     int best = 1;
     int64_t best_cost = -1;
     for (int64_t v = 1; v <= hpg; ++v) {
@@ -548,7 +535,7 @@ int pick_hpc(const Dims& d, int64_t outer) {
 int pick_hpc_fused(const Dims& d, int64_t n_tiles) {
     const int hpg = (int)(d.H / d.G);
     for (int v = 16; v >= 1; --v)
-        if (hpg % v == 0 && d.b * n_tiles * (d.H / v) >= num_sms()) return v;
+        if (hpg % v == 0 && d.b * n_tiles * (d.H / v) >= sm_count()) return v;
     return 1;
 }
 
@@ -596,7 +583,8 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     const int64_t outer = d.b * d.nc * n_tiles;
     // Fused: one chunk's CTAs should fill the GPU, so that the CTA of chunk c
     // typically starts after the one of chunk c-1 has finished (no waiting).
-    const int hpc = kFuse ? pick_hpc_fused(d, n_tiles) : pick_hpc(d, outer);
+    int src = kFromModel;
+    const int hpc = kFuse ? pick_hpc_fused(d, n_tiles) : k2_heads_per_cta(d, &src);
     const int n_hblk = (int)(d.H / hpc);
     const int64_t grid = outer * n_hblk;
     auto k = chunk_state_tc_kernel<L, kFuse, kDS16>;
@@ -608,6 +596,23 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
 }
 
 }  // namespace
+
+int k2_heads_per_cta(const Dims& d, int* src) {
+    const int64_t hpg = d.H / d.G;
+    const int o = tile_override(0);
+    if (o > 0 && hpg % o == 0) {
+        *src = kFromOverride;
+        return o;
+    }
+    const TileChoice* t = o < 0 ? nullptr : find_tile(d);   // -1: the cost model only
+    if (t && t->k2_hpc > 0 && hpg % t->k2_hpc == 0) {
+        *src = kFromTable;
+        return t->k2_hpc;
+    }
+    *src = kFromModel;
+    const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
+    return pick_hpc(d, d.b * d.nc * n_tiles);
+}
 
 bool tc_supported(const Dims& d) {
     return d.dtype == 1 && (d.L == 128 || d.L == 256) && d.P == 64 &&

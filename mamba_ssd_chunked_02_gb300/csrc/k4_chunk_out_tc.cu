@@ -777,19 +777,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     if (threadIdx.x == 0 && bars.abort) record_error(err, kErrTimeoutK4);
 }
 
-int num_sms4() {
-    static int cached[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return 148;
-    if (!cached[dev]) {
-        int v = 0;
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = v > 0 ? v : 148;
-    }
-    return cached[dev];
-}
-
 // Head blocks per CTA.  One CTA per SM at a time, each with a fixed cost (the
 // C.B^T product and its packing, the pipeline's fill and drain) of about two
 // heads; the second query tile costs about 1.25 times the first per head.  The
@@ -799,10 +786,6 @@ int num_sms4() {
 // the SMs: single sizes, and mixes whose first region fills whole waves.  At
 // b8 T4096 H80 it takes 40 heads for 114 of the 128 (b, c) pairs and 16 for the
 // rest (1 024 CTAs of 20 heads simulate to 179 head units, the mix to 168).
-struct Split4 {
-    int v1, v2;
-    int64_t n1, ctas;
-};
 
 double makespan4(int64_t bc, int64_t n1_bc, int v1, int v2, int64_t H, int NQ, int sms) {
     std::priority_queue<double, std::vector<double>, std::greater<double>> q;
@@ -825,7 +808,7 @@ double makespan4(int64_t bc, int64_t n1_bc, int v1, int v2, int64_t H, int NQ, i
 Split4 pick_split4(const Dims& d, int NQ) {
     static std::mutex mu;
     static std::map<std::array<int64_t, 5>, Split4> cache;
-    const int sms = num_sms4();
+    const int sms = sm_count();
     const std::array<int64_t, 5> key = {d.b * d.nc, d.H, d.G, NQ, sms};
     std::lock_guard<std::mutex> lock(mu);
     const auto it = cache.find(key);
@@ -835,14 +818,15 @@ Split4 pick_split4(const Dims& d, int NQ) {
     for (int64_t v = 1; v <= hpg; ++v)
         if (hpg % v == 0 && bc * NQ * (d.H / v) <= cap) divs.push_back((int)v);
     if (divs.empty()) divs.push_back((int)hpg);
-    Split4 best{divs.back(), divs.back(), bc * NQ * (d.H / divs.back()), bc * NQ * (d.H / divs.back())};
+    Split4 best{divs.back(), divs.back(), bc * NQ * (d.H / divs.back()), bc * NQ * (d.H / divs.back()), bc,
+                kFromModel};
     double best_t = -1.0;
     auto consider = [&](int64_t n1_bc, int v1, int v2) {
         const double t = makespan4(bc, n1_bc, v1, v2, d.H, NQ, sms);
         const int64_t n1 = n1_bc * NQ * (d.H / v1), ctas = n1 + (bc - n1_bc) * NQ * (d.H / v2);
         if (best_t < 0.0 || t < best_t * 0.999 || (t <= best_t * 1.001 && ctas < best.ctas)) {
             best_t = t;
-            best = {v1, v2, n1, ctas};
+            best = {v1, v2, n1, ctas, n1_bc, kFromModel};
         }
     };
     int vsingle = divs.front();
@@ -894,8 +878,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
                            CU_TENSOR_MAP_SWIZZLE_128B)
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
-    const int NQ = L / 128;
-    const Split4 sp = pick_split4(d, NQ);
+    const Split4 sp = k4_split(d);
     const int64_t grid = sp.ctas;
     auto k = chunk_out_tc_kernel<L, NA, kY32>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -919,6 +902,30 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
 }
 
 }  // namespace
+
+// A forced or tabled split: v1 and v2 divide H/G, and the v1 region takes the
+// (b, c) pairs that fill `waves` waves of the SMs (all pairs when waves is 0).
+bool fixed_split4(const Dims& d, int v1, int v2, int waves, int src, Split4* out) {
+    const int64_t hpg = d.H / d.G, bc = d.b * d.nc, NQ = d.L / 128;
+    if (v1 <= 0 || hpg % v1) return false;
+    if (waves > 0 && (v2 <= 0 || hpg % v2)) return false;
+    int64_t n1_bc = bc;
+    if (waves > 0) n1_bc = std::min<int64_t>(bc, (int64_t)waves * sm_count() / (NQ * (d.H / v1)));
+    if (n1_bc == bc) v2 = v1;
+    const int64_t n1 = n1_bc * NQ * (d.H / v1);
+    *out = {v1, v2, n1, n1 + (bc - n1_bc) * NQ * (d.H / v2), n1_bc, src};
+    return true;
+}
+
+Split4 k4_split(const Dims& d) {
+    if (d.H == 0 || d.b * d.nc == 0) return {1, 1, 0, 0, 0, kFromModel};   // nothing to launch
+    Split4 sp;
+    const int o1 = tile_override(1);
+    if (fixed_split4(d, o1, tile_override(2), tile_override(3), kFromOverride, &sp)) return sp;
+    const TileChoice* t = o1 < 0 ? nullptr : find_tile(d);   // -1: the cost model only
+    if (t && fixed_split4(d, t->k4_v1, t->k4_v2, t->k4_waves1, kFromTable, &sp)) return sp;
+    return pick_split4(d, (int)(d.L / 128));
+}
 
 cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,

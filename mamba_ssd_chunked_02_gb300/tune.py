@@ -1,0 +1,259 @@
+"""Offline sweep of the tensor-core kernels' launch choices; writes the table
+that the library compiles in (csrc/tile_table.inc).
+
+    python -m mamba_ssd_chunked_02_gb300.tune [--out PATH] [--log PATH] [--reps R]
+
+Runs on one GPU.  For every swept shape it times, through
+mamba2_ssd_fwd_timed (CUDA events between the stages, recorded on the
+launching stream),
+
+  * stage 2 (chunk states) at every heads-per-CTA count that divides H/G;
+  * stage 4 (fused output) at every single head-block size v dividing H/G and
+    every two-region split (v1 for the (b, c) pairs of the first k waves of
+    CTAs, v2 < v1 for the rest, k = 1 .. while the first region leaves pairs
+    over),
+
+each candidate forced with mamba2_ssd_tile_override, the mean of R calls (the
+event timer of a GB300 ticks in steps of about 2 us, so medians of short
+stages tie; means of dithered readings resolve below the tick).
+The fastest candidate per stage is then checked on the whole forward pass as
+the library runs it (programmatic dependent launch, no events inside) against
+the launch-time cost models' choice, the two timed alternately; the table takes
+the candidate only where the whole pass is faster by more than the noise
+margin, and the model's own choice otherwise (so that every swept shape has an
+entry and the entry never loses to the model it replaces).
+
+Inputs are drawn as in workloads.make_inputs (the distributions of the
+measured workloads).  Between calls a 512 MB buffer is written when the inputs
+fit in L2, so every timed call starts with cold inputs.  The table's b * nc
+ranges are power-of-two buckets: an entry found at b * nc = n covers
+[2^k, 2^(k+1) - 1] with 2^k <= n < 2^(k+1); shapes in unswept buckets keep the
+cost models.
+
+Pages: "NVIDIA、cuTileでMamba-2フォワードパスを高速化" (ai.newsbites.today),
+the optimisation table (per-input autotuning of the launch configuration);
+"NVIDIA CUDA Tile로 Mamba-2 순방향 전달 커널 가속화" (devin.kr), "cuTile 기반 성능
+최적화 기법" (exhaustive search over block size and occupancy).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+
+import torch
+
+import mamba_ssd_chunked_02_gb300 as m2
+from mamba_ssd_chunked_02_gb300 import workloads as W
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+TABLE = os.path.join(_PKG, "csrc", "tile_table.inc")
+
+
+def swept_workloads():
+    """The measured tensor-core workloads plus batch variants of the 2.7B layer."""
+    out = [W.MAMBA2_2P7B] + W.sweep_workloads() + [W.GROUPED_INIT, W.LONG_PREFILL]
+    for b in (1, 2, 4, 16):
+        out.append(W.MAMBA2_2P7B.scaled(name=f"mamba2-2.7b-layer b{b} T4096 H80 P64 N128 G1 L256 bf16",
+                                        batch=b))
+    return out
+
+
+def divisors(n):
+    return [v for v in range(1, n + 1) if n % v == 0]
+
+
+class Runner:
+    """One workload's device buffers and timed calls."""
+
+    def __init__(self, w, flush):
+        self.w = w
+        inp = W.make_inputs(w)
+        self.dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+        self.sh = m2.shape_of(self.dev["x"], self.dev["B"], w.chunk_size, w.ngroups)
+        self.ws = torch.empty(max(1, m2.workspace_size(self.sh)), dtype=torch.uint8, device="cuda")
+        self.y = torch.empty_like(self.dev["x"])
+        self.fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device="cuda")
+        io = 2 * (2 * w.batch * w.seqlen * w.nheads * w.headdim +
+                  2 * w.batch * w.seqlen * w.ngroups * w.dstate)
+        self.cold = io < 2 * (129 << 20)
+        self.flush = flush
+        self.stream = torch.cuda.current_stream()
+
+    def call(self, events=None):
+        d = self.dev
+        m2.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
+                   chunk_size=self.w.chunk_size, ngroups=self.w.ngroups, y=self.y,
+                   final_state=self.fin, workspace=self.ws, events=events)
+
+    def stage_times(self, reps):
+        """Mean per-stage milliseconds [stage1, stage2, stage3, stage4]."""
+        for _ in range(2):
+            self.call()
+        ts = []
+        for _ in range(reps):
+            if self.cold:
+                self.flush.fill_(1)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            self.call(events=evs)
+            evs[4].synchronize()
+            ts.append([evs[k].elapsed_time(evs[k + 1]) for k in range(4)])
+        return [statistics.fmean(t[k] for t in ts) for k in range(4)]
+
+    def whole_time(self):
+        """One whole-path call (the library's own launch sequence), milliseconds."""
+        if self.cold:
+            self.flush.fill_(1)
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.stream)
+        self.call()
+        z.record(self.stream)
+        z.synchronize()
+        return a.elapsed_time(z)
+
+
+def stage4_candidates(w, sms):
+    """(v1, v2, waves1) splits: single sizes, and two regions whose first fills
+    k whole waves of CTAs while leaving pairs to the second."""
+    hpg = w.nheads // w.ngroups
+    nq = w.chunk_size // 128
+    bc = w.batch * ((w.seqlen + w.chunk_size - 1) // w.chunk_size)
+    divs = [v for v in divisors(hpg) if bc * nq * (w.nheads // v) <= 32 * sms] or [hpg]
+    out = [(v, 0, 0) for v in divs]
+    for v1 in divs:
+        per_bc = nq * (w.nheads // v1)
+        for k in range(1, 33):
+            n1 = min(bc, k * sms // per_bc)
+            if n1 <= 0:
+                continue
+            if n1 >= bc:
+                break
+            out += [(v1, v2, k) for v2 in divs if v2 < v1]
+    return out
+
+
+def sweep(w, flush, reps, margin, log):
+    r = Runner(w, flush)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hpg = w.nheads // w.ngroups
+    rec = {"workload": w.name, "sms": sms, "stage2": [], "stage4": []}
+    m2.tile_override(-1, -1)
+    model = m2.tile_choice(r.sh)
+    base = r.stage_times(reps)
+    rec["model"] = {"choice": model, "stage_ms": base}
+    for v in divisors(hpg):
+        m2.tile_override(v, -1)
+        rec["stage2"].append({"heads": v, "ms": r.stage_times(reps)[1]})
+    for (v1, v2, k) in stage4_candidates(w, sms):
+        m2.tile_override(-1, v1, v2, k)
+        c = m2.tile_choice(r.sh)
+        rec["stage4"].append({"v1": v1, "v2": v2, "waves1": k, "pairs1": c["stage4_pairs1"],
+                              "ms": r.stage_times(reps)[3]})
+    b2 = min(rec["stage2"], key=lambda e: e["ms"])
+    b4 = min(rec["stage4"], key=lambda e: e["ms"])
+    # Whole forward pass: the sweep's winners against the cost models' choice,
+    # timed alternately so that drift hits both alike.
+    tuned = (b2["heads"], b4["v1"], b4["v2"], b4["waves1"])
+    ta, tb = [], []
+    for _ in range(3):
+        r.call()
+    for _ in range(max(20, 2 * reps)):
+        m2.tile_override(-1, -1)
+        ta.append(r.whole_time())
+        m2.tile_override(*tuned)
+        tb.append(r.whole_time())
+    m2.tile_override()
+    if m2.device_error() != 0:
+        raise RuntimeError(f"device-side error while sweeping {w.name}")
+    t_model, t_tuned = statistics.fmean(ta), statistics.fmean(tb)
+    same = (model["stage2_heads"], model["stage4_v1"], model["stage4_pairs1"]) == \
+        (b2["heads"], b4["v1"], b4["pairs1"]) and \
+        (model["stage4_v2"] == b4["v2"] or b4["pairs1"] == r.sh.batch * r.sh.nchunks)
+    keep = not same and t_tuned < t_model * (1.0 - margin)
+    if keep:
+        entry = tuned
+    else:   # table the model's own choice
+        entry = (model["stage2_heads"], model["stage4_v1"],
+                 model["stage4_v2"] if model["stage4_v2"] != model["stage4_v1"] else 0,
+                 0)
+        if model["stage4_v2"] != model["stage4_v1"]:
+            # express the model's split in waves: the smallest k giving its pairs
+            per_bc = (w.chunk_size // 128) * (w.nheads // model["stage4_v1"])
+            k = next((k for k in range(1, 64) if k * sms // per_bc >= model["stage4_pairs1"]), 0)
+            if k and min(k * sms // per_bc, r.sh.batch * r.sh.nchunks) == model["stage4_pairs1"]:
+                entry = (model["stage2_heads"], model["stage4_v1"], model["stage4_v2"], k)
+            else:
+                entry = None    # not expressible in waves: leave the shape to the model
+    rec.update({"best_stage2": b2, "best_stage4": b4, "whole_model_ms": t_model,
+                "whole_tuned_ms": t_tuned, "tabled": "sweep" if keep else "model",
+                "entry": entry})
+    log.write(json.dumps(rec) + "\n")
+    log.flush()
+    print(f"{w.name}: model {t_model:.4f} ms, tuned {t_tuned:.4f} ms "
+          f"(stage2 {b2['heads']} heads {b2['ms']:.4f} vs {base[1]:.4f}; stage4 "
+          f"{b4['v1']}/{b4['v2']}/{b4['waves1']} {b4['ms']:.4f} vs {base[3]:.4f}) -> "
+          f"{rec['tabled']} {entry}", flush=True)
+    del r
+    torch.cuda.empty_cache()
+    return rec
+
+
+def bucket(n):
+    lo = 1
+    while lo * 2 <= n:
+        lo *= 2
+    return lo, lo * 2 - 1
+
+
+def write_table(recs, path, ws):
+    lines = [
+        "// Generated by mamba_ssd_chunked_02_gb300/tune.py from timings on one GB300; do",
+        "// not edit by hand.  One entry per swept shape:",
+        "//   {N, P, L, heads per group, b*nc low, b*nc high, stage-2 heads per CTA,",
+        "//    stage-4 block sizes v1, v2, SM waves of the v1 region (0: v1 everywhere)}",
+    ]
+    seen = set()
+    for w, rec in zip(ws, recs):
+        if rec["entry"] is None:
+            continue
+        nc = (w.seqlen + w.chunk_size - 1) // w.chunk_size
+        lo, hi = bucket(w.batch * nc)
+        key = (w.dstate, w.headdim, w.chunk_size, w.nheads // w.ngroups, lo)
+        if key in seen:
+            continue
+        seen.add(key)
+        k2, v1, v2, k = rec["entry"]
+        lines.append(f"    {{{w.dstate}, {w.headdim}, {w.chunk_size}, {w.nheads // w.ngroups}, "
+                     f"{lo}, {hi}, {k2}, {v1}, {v2}, {k}}},   // {w.name}: "
+                     f"{rec['whole_tuned_ms' if rec['tabled'] == 'sweep' else 'whole_model_ms']:.4f} ms "
+                     f"({rec['tabled']}; model {rec['whole_model_ms']:.4f})")
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=TABLE, help="table to write (C initialiser lines)")
+    ap.add_argument("--log", default="tune_log.jsonl", help="every timing, one JSON line per shape")
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--margin", type=float, default=0.005,
+                    help="relative whole-pass gain the sweep's choice needs over the model's")
+    ap.add_argument("--only", default="", help="substring of the workload names to sweep")
+    a = ap.parse_args()
+    if not torch.cuda.is_available():
+        raise SystemExit("tune.py needs a CUDA device")
+    m2.load()
+    m2.device_error(clear=True)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    ws = [w for w in swept_workloads() if a.only in w.name]
+    recs = []
+    with open(a.log, "w") as log:
+        for w in ws:
+            recs.append(sweep(w, flush, a.reps, a.margin, log))
+    write_table(recs, a.out, ws)
+    print(f"wrote {a.out}")
+
+
+if __name__ == "__main__":
+    main()
