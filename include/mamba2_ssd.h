@@ -381,8 +381,11 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_ssd_shape* shape,
  * search runs offline (mamba_ssd_chunked_02_gb300/tune.py, which times every
  * candidate on the GPU through mamba2_ssd_tile_override) and its winners are
  * compiled into the library as a table keyed by (N, P, L, H/G, a range of
- * b * nc).  Two choices are tabled: the heads per CTA of the chunk-state
- * kernel (stage 2), and the head-block sizes of the output kernel (stage 4),
+ * b * nc).  Two choices are tabled: the work per CTA of the chunk-state
+ * kernel (stage 2: a CTA takes a contiguous range of units, a unit being one
+ * head of one (b, chunk, 128-wide state tile), in the order b, chunk, state
+ * tile, head; either blocks of heads of one group, or one wave of CTAs over
+ * ceil(units / SMs)-unit ranges), and the head-block sizes of the output kernel (stage 4),
  * whose grid has two regions -- the first (b, c) pairs, filling `waves1` whole
  * waves of the SMs, take blocks of v1 heads, the rest blocks of v2.  A shape
  * with no table entry (or an entry that does not divide its H/G) takes the
@@ -390,7 +393,7 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_ssd_shape* shape,
  * regroup independent work.
  *
  * mamba2_ssd_tile_choice writes, for a shape on the tensor-core path,
- *   out[0] stage-2 heads per CTA, out[1] its source,
+ *   out[0] stage-2 units per CTA, out[1] its source,
  *   out[2] stage-4 v1, out[3] v2, out[4] (b, c) pairs in the v1 region,
  *   out[5] its source,
  * with source 0 = cost model, 1 = table, 2 = override.  `out` holds 6 words
@@ -400,18 +403,19 @@ MAMBA2_API mamba2_status mamba2_ssd_fwd_noalloc(const mamba2_ssd_shape* shape,
  *
  * mamba2_ssd_tile_override forces choices for every later launch in the
  * process (all threads, all devices) until it is called again with zeros:
- * stage2_heads > 0 forces the heads per CTA; stage4_v1 > 0 forces stage 4's
+ * stage2_units > 0 forces the units per CTA (capped at the shape's units), -2
+ * one wave of even ranges; stage4_v1 > 0 forces stage 4's
  * split, v1 for the pairs of the first stage4_waves1 waves and stage4_v2 for
  * the rest (stage4_waves1 = 0: v1 for every pair, stage4_v2 ignored).  A
- * forced value that does not divide a shape's H/G is ignored for that shape.
- * stage2_heads = -1 or stage4_v1 = -1 bypasses the table for that stage (the
+ * forced head-block size that does not divide a shape's H/G is ignored for
+ * that shape.  stage2_units = -1 or stage4_v1 = -1 bypasses the table for that stage (the
  * cost model decides), so that the sweep can time the model's choice.  Meant
  * for the offline sweep, not for concurrent use with other callers.  Returns
- * MAMBA2_ERR_INVALID_ARG for a value below -1 (below 0 for stage4_v2 and
- * stage4_waves1) or for v2 / waves1 set without a positive v1, MAMBA2_OK
+ * MAMBA2_ERR_INVALID_ARG for stage2_units below -2, stage4_v1 below -1,
+ * stage4_v2 or stage4_waves1 below 0, or v2 / waves1 set without a positive v1, MAMBA2_OK
  * otherwise. */
 MAMBA2_API mamba2_status mamba2_ssd_tile_choice(const mamba2_ssd_shape* shape, int32_t* out);
-MAMBA2_API mamba2_status mamba2_ssd_tile_override(int32_t stage2_heads, int32_t stage4_v1,
+MAMBA2_API mamba2_status mamba2_ssd_tile_override(int32_t stage2_units, int32_t stage4_v1,
                                                   int32_t stage4_v2, int32_t stage4_waves1);
 
 /* Static description of a status code. */

@@ -500,14 +500,19 @@ def tile_choice(shape: Shape) -> dict:
     """Launch choices of the tensor-core kernels for `shape` (mamba2_ssd_tile_choice)."""
     out = (ctypes.c_int32 * 6)()
     _check("mamba2_ssd_tile_choice", load().mamba2_ssd_tile_choice(ctypes.byref(shape), out))
-    return {"stage2_heads": out[0], "stage2_source": out[1], "stage4_v1": out[2],
+    return {"stage2_units": out[0], "stage2_source": out[1], "stage4_v1": out[2],
             "stage4_v2": out[3], "stage4_pairs1": out[4], "stage4_source": out[5]}
 
 
-def tile_override(stage2_heads=0, stage4_v1=0, stage4_v2=0, stage4_waves1=0):
-    """Force launch choices for later calls (mamba2_ssd_tile_override); zeros clear."""
+MODEL_ONLY, EVEN_SPLIT = -1, -2
+
+
+def tile_override(stage2_units=0, stage4_v1=0, stage4_v2=0, stage4_waves1=0):
+    """Force launch choices for later calls (mamba2_ssd_tile_override); zeros clear.
+    MODEL_ONLY (-1) bypasses the table; EVEN_SPLIT (-2, stage 2) forces one wave of
+    even unit ranges."""
     _check("mamba2_ssd_tile_override",
-           load().mamba2_ssd_tile_override(stage2_heads, stage4_v1, stage4_v2, stage4_waves1))
+           load().mamba2_ssd_tile_override(stage2_units, stage4_v1, stage4_v2, stage4_waves1))
 
 
 def device_error(clear=True) -> int:

@@ -538,7 +538,7 @@ mamba2_status mamba2_ssd_tile_choice(const mamba2_ssd_shape* shape, int32_t* out
     const Dims d = dims_of(shape);
     if (!use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
     int src2 = 0;
-    out[0] = m2::k2_heads_per_cta(d, &src2);
+    out[0] = m2::k2_units_per_cta(d, &src2);
     out[1] = src2;
     const m2::Split4 sp = m2::k4_split(d);
     out[2] = sp.v1;

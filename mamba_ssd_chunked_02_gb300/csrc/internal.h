@@ -148,20 +148,23 @@ int sm_count();
 struct TileChoice {
     int32_t N, P, L, hpg;      // state size, head dim, chunk size, heads per group
     int64_t bnc_lo, bnc_hi;    // range of b * nc the entry covers
-    int32_t k2_hpc;            // stage 2: heads per CTA
+    int32_t k2_hpc;            // stage 2: units per CTA (0: one wave of even ranges)
     int32_t k4_v1, k4_v2;      // stage 4: head-block sizes of the two grid regions
     int32_t k4_waves1;         // stage 4: SM waves the v1 region fills (0: v1 everywhere)
 };
 // The table entry for this shape, or null.
 const TileChoice* find_tile(const Dims& d);
-// Tuning override k (0: stage-2 heads per CTA, 1/2: stage-4 v1/v2, 3: stage-4
-// v1-region waves), 0 when not set (mamba2_ssd_tile_override).
+// Tuning override k (0: stage-2 units per CTA, 1/2: stage-4 v1/v2, 3: stage-4
+// v1-region waves), 0 when not set (mamba2_ssd_tile_override); -1 bypasses the
+// table, kEvenSplit (stage 2 only) forces one wave of even ranges.
 int tile_override(int k);
+constexpr int kEvenSplit = -2;
 
 // Where a launch choice comes from.
 enum : int { kFromModel = 0, kFromTable = 1, kFromOverride = 2 };
-// Stage 2 (tensor-core, unfused): heads per CTA and its source.
-int k2_heads_per_cta(const Dims& d, int* src);
+// Stage 2 (tensor-core, unfused): units per CTA (a unit is one head of one
+// (b, chunk, 128-wide state tile); a CTA takes a contiguous range) and its source.
+int k2_units_per_cta(const Dims& d, int* src);
 // Stage 4 (tensor-core): head-block sizes v1, v2, CTAs of the v1 region (n1),
 // all CTAs, the (b, c) pairs of the v1 region and the source.
 struct Split4 {

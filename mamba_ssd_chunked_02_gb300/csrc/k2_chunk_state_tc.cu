@@ -83,15 +83,18 @@ struct K2Cfg {
     static constexpr int F_BYTES = 2 * (64 * 128 * 4 + 64 * 128 * 2);
     static constexpr int SMEM = 1024 + BT_BYTES + NS * X_BYTES + (kFuse ? F_BYTES : 2 * D_BYTES);
     // Tensor memory: 2 accumulators x 64 columns, then B^T as the MMA's A operand
-    // (lane = state dim n, L keys as 16-bit pairs: L / 2 columns).
-    static constexpr int TMEM_COLS = 256;
+    // (lane = state dim n, L keys as 16-bit pairs: L / 2 columns); the plain
+    // variant keeps two B^T slots, so that the next group segment's B^T is copied
+    // in while the MMAs of the current one still read theirs.
     static constexpr uint32_t COL_BT = 128;
+    static constexpr uint32_t BT_COLS = L / 2;
+    static constexpr int TMEM_COLS = (kFuse || L == 128) ? 256 : 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 64, 0, 1);   // A in tensor memory, B MN-major
 };
 
 struct K2Bars {
     uint64_t bt_full;
-    uint64_t bt_tmem;       // B^T copied into tensor memory by the epilogue warps
+    uint64_t bt_tmem[2];    // B^T copied into tensor-memory slot 0 / 1 by the epilogue warps
     uint64_t full[6], scaled[6], xfree[6];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t drain;         // commit target used to drain in-flight MMAs on abort
@@ -114,6 +117,30 @@ struct FuseArgs {
     int adj = 0;              // weight mode: 0 = w_s above, 1 = w_s = exp2(cum2[s])
 };
 
+// Plain variant's work order: unit u = ((b * nc + c) * n_tiles + nt) * H + h, one
+// head of one (b, chunk, state tile); a CTA takes units [u0, u0 + upc).  The heads
+// of one group with the same (b, c, nt) form a segment, which shares B^T.
+struct UnitIt {
+    int b, c, nt, h;
+    __device__ void init(int64_t u, int H, int n_tiles, int nc) {
+        h = (int)(u % H);
+        u /= H;
+        nt = (int)(u % n_tiles);
+        u /= n_tiles;
+        c = (int)(u % nc);
+        b = (int)(u / nc);
+    }
+    __device__ void next(int H, int n_tiles, int nc) {   // carries instead of divisions
+        if (++h < H) return;
+        h = 0;
+        if (++nt < n_tiles) return;
+        nt = 0;
+        if (++c < nc) return;
+        c = 0;
+        ++b;
+    }
+};
+
 template <int L, bool kFuse, bool kDS16>
 __global__ void __launch_bounds__(K2Cfg<L, kFuse, kDS16>::kThreads, 1)
 chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -125,8 +152,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
                       int T, int H, int N, int G, int nc, int n_tiles,
-                      int hpc, int n_hblk, int32_t* err, const FuseArgs fa,
-                      uint32_t* __restrict__ xabs) {
+                      int hpc, int n_hblk, int upc, int64_t units, int32_t* err,
+                      const FuseArgs fa, uint32_t* __restrict__ xabs) {
     using C = K2Cfg<L, kFuse, kDS16>;
     constexpr int NS = C::NS;
     extern __shared__ uint8_t smem_raw[];
@@ -141,7 +168,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
 
     if (threadIdx.x == 0) {
         mbar_init(&bars.bt_full, 1);
-        mbar_init(&bars.bt_tmem, 128);
+        mbar_init(&bars.bt_tmem[0], 128);
+        mbar_init(&bars.bt_tmem[1], 128);
         for (int i = 0; i < NS; ++i) {
             mbar_init(&bars.full[i], 1);
             mbar_init(&bars.scaled[i], 32 * C::kSW);
@@ -168,25 +196,28 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    // Work item.  Plain: (b, c, n-tile) outer, head block inner (CTAs sharing
-    // B^T run together).  Fused: chunk outermost, in ticket order.
-    int rest = bars.item, b, c, nt, hblk;
+    // Work item.  Plain: units [u0, u0 + nh) in unit order (the first unit's
+    // position below; later ones from UnitIt).  Fused: a block of hpc heads of one
+    // (b, c, n-tile), chunk outermost, in ticket order.
+    const int hpg = H / G;
+    int b, c, nt, h0, nh;
+    int64_t u0 = 0;
     if (kFuse) {
+        int rest = bars.item;
         const int per_chunk = fa.nb * n_tiles * n_hblk;
         c = rest / per_chunk; rest %= per_chunk;
         b = rest / (n_tiles * n_hblk); rest %= n_tiles * n_hblk;
         nt = rest / n_hblk;
-        hblk = rest % n_hblk;
+        h0 = (rest % n_hblk) * hpc;
+        nh = hpc;
     } else {
-        hblk = rest % n_hblk; rest /= n_hblk;
-        nt = rest % n_tiles; rest /= n_tiles;
-        c = rest % nc;
-        b = rest / nc;
+        u0 = (int64_t)bars.item * upc;
+        nh = (int)(units - u0 < upc ? units - u0 : upc);
+        UnitIt first;
+        first.init(u0, H, n_tiles, nc);
+        b = first.b; c = first.c; nt = first.nt; h0 = first.h;
     }
-    const int hpg = H / G;
-    const int h0 = hblk * hpc;
     const int g = h0 / hpg;
-    const int nh = hpc;
 
     if (c >= nc) {
         // A ticket past the grid (the counter was not cleared): do nothing.
@@ -208,16 +239,23 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 tma_load_3d(sBt + a * C::ATOM, &tm_b, &bars.bt_full, g * N + n_off, c * L, b);
             }
             int issued = 0;
+            UnitIt it;
+            it.init(u0, H, n_tiles, nc);   // plain: the unit's head and chunk
             for (int i = 0; i < nh; ++i) {
                 const int st = i % NS, k = i / NS;
                 if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
                 mbar_arrive_expect_tx(&bars.full[st], C::X_BYTES);
-                tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], (h0 + i) * C::P, c * L, b);
+                if (kFuse)
+                    tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], (h0 + i) * C::P, c * L, b);
+                else
+                    tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], it.h * C::P, it.c * L, it.b);
                 issued = i + 1;
+                if (!kFuse) it.next(H, n_tiles, nc);
             }
             if (*abort) {
-                // Let every copy already issued land before the CTA can exit.
-                mbar_wait(&bars.bt_full, 0, kWaitNs);
+                // Let every copy already issued land before the CTA can exit (plain:
+                // the epilogue warps wait for the B^T loads, which they also issue).
+                if (kFuse) mbar_wait(&bars.bt_full, 0, kWaitNs);
                 for (int i = issued - 1; i >= 0 && i >= issued - NS; --i)
                     mbar_wait(&bars.full[i % NS], (i / NS) & 1, kWaitNs);
             }
@@ -226,26 +264,31 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // ----------------------------------------------------------- MMA issue
         if (lane == 0) {
             int last = -1;
-            if (mbar_wait_or_abort(&bars.bt_tmem, 0, abort, kWaitNs)) {
-                tc_fence_after();
-                // Descriptors formed once; each MMA adds a constant offset / 16 (an MMA
-                // issue waits for the scalar work in front of it).
-                const uint64_t x_desc0 = smem_desc_sw128(smem_u32(sX), C::ATOM, 1024);
-                for (int i = 0; i < nh; ++i) {
-                    const int st = i % NS, k = i / NS, ab = i & 1, ka = i >> 1;
-                    if (!mbar_wait_or_abort(&bars.scaled[st], k & 1, abort, kWaitNs)) break;
-                    if (!mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs)) break;
+            // Descriptors formed once; each MMA adds a constant offset / 16 (an MMA
+            // issue waits for the scalar work in front of it).
+            const uint64_t x_desc0 = smem_desc_sw128(smem_u32(sX), C::ATOM, 1024);
+            int seg = -1;                  // segment of head i (its B^T slot: seg & 1)
+            int hh = kFuse ? 0 : h0;       // head of unit i (plain), to find segment starts
+            for (int i = 0; i < nh; ++i) {
+                if (i == 0 || (!kFuse && hh % hpg == 0)) {
+                    ++seg;
+                    if (!mbar_wait_or_abort(&bars.bt_tmem[seg & 1], (seg >> 1) & 1, abort, kWaitNs)) break;
                     tc_fence_after();
-                    const uint64_t xd = x_desc0 + (uint64_t)st * (C::X_BYTES >> 4);
-                    const uint32_t d = tmem + ab * C::P;
-#pragma unroll
-                    for (int kk = 0; kk < L / 16; ++kk)
-                        mma_ts(d, tmem + C::COL_BT + 8 * kk, xd + (uint64_t)(kk * (2048 >> 4)), C::IDESC,
-                               kk > 0 ? 1u : 0u);
-                    mma_commit(&bars.acc_full[ab]);
-                    mma_commit(&bars.xfree[st]);
-                    last = i;
                 }
+                if (!kFuse && ++hh == H) hh = 0;
+                const int st = i % NS, k = i / NS, ab = i & 1, ka = i >> 1;
+                if (!mbar_wait_or_abort(&bars.scaled[st], k & 1, abort, kWaitNs)) break;
+                if (!mbar_wait_or_abort(&bars.acc_empty[ab], (ka & 1) ^ 1, abort, kWaitNs)) break;
+                tc_fence_after();
+                const uint64_t xd = x_desc0 + (uint64_t)st * (C::X_BYTES >> 4);
+                const uint32_t d = tmem + ab * C::P;
+                const uint32_t a = tmem + C::COL_BT + (uint32_t)(seg & 1) * C::BT_COLS;
+#pragma unroll
+                for (int kk = 0; kk < L / 16; ++kk)
+                    mma_ts(d, a + 8 * kk, xd + (uint64_t)(kk * (2048 >> 4)), C::IDESC, kk > 0 ? 1u : 0u);
+                mma_commit(&bars.acc_full[ab]);
+                mma_commit(&bars.xfree[st]);
+                last = i;
             }
             if (last >= 0 && *abort) {   // nothing may be in flight when TMEM is freed
                 mma_commit(&bars.drain);
@@ -257,13 +300,13 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         constexpr int kST = 32 * C::kSW;                 // scaling threads
         constexpr int RPT = L / kST;                     // x rows per thread (1)
         const int idx = threadIdx.x - 64;                // 0 .. kST - 1
-        const int Lc = min(L, T - c * L);
         // Raw decay inputs of the next head, fetched one head ahead.
         float pc[RPT], pd[RPT], plast = 0.f;
-        auto prefetch = [&](int hh) {
-            const int64_t bh = (int64_t)b * H + h0 + hh;
-            const float* crow = cum2 + bh * T + (int64_t)c * L;
-            const float* drow = dtT + bh * T + (int64_t)c * L;
+        auto prefetch = [&](int bb, int cc, int hh) {
+            const int Lc = min(L, T - cc * L);
+            const int64_t bh = (int64_t)bb * H + hh;
+            const float* crow = cum2 + bh * T + (int64_t)cc * L;
+            const float* drow = dtT + bh * T + (int64_t)cc * L;
             plast = __ldg(crow + Lc - 1);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
@@ -277,14 +320,26 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // let stage 3 start launching.
         grid_dep_wait();
         if (idx == 0) grid_dep_launch();
-        prefetch(0);
+        // Plain: (b, c, h) of unit i and of unit i + 1; fused: h0 + i of (b, c).
+        UnitIt cur, nxt;
+        cur.init(u0, H, n_tiles, nc);
+        if (kFuse) {
+            cur.b = b;
+            cur.c = c;
+            cur.nt = nt;
+            cur.h = h0;
+        }
+        nxt = cur;
+        prefetch(nxt.b, nxt.c, nxt.h);
         for (int i = 0; i < nh; ++i) {
             const int st = i % NS, k = i / NS;
             float w[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r)   // 0 past Lc (the x rows there are zero-filled)
                 w[r] = fa.adj ? ex2(pc[r]) : pd[r] * ex2(plast - pc[r]);
-            if (i + 1 < nh) prefetch(i + 1);
+            if (kFuse) ++nxt.h;
+            else nxt.next(H, n_tiles, nc);
+            if (i + 1 < nh) prefetch(nxt.b, nxt.c, nxt.h);
             const bool ok = __all_sync(0xffffffffu,
                                        mbar_wait_or_abort(&bars.full[st], k & 1, abort, kWaitNs));
             if (!ok) break;
@@ -320,11 +375,12 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 const uint32_t m2u = *reinterpret_cast<const uint32_t*>(&xm2);
                 const uint32_t m = __reduce_max_sync(0xffffffffu, max(m2u & 0xffffu, m2u >> 16));
                 if (lane == 0) {   // eight words per head; with four scaling warps the rest are 0
-                    uint32_t* xw = xabs + ((((int64_t)b * nc + c) * H + h0 + i) << 3);
+                    uint32_t* xw = xabs + ((((int64_t)cur.b * nc + cur.c) * H + cur.h) << 3);
                     xw[warp - 2] = m;
                     if (C::kSW == 4) xw[warp + 2] = 0u;
                 }
             }
+            cur = nxt;
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -350,31 +406,32 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         // columns.  The tensor core then reads only x~ from shared memory: an
         // M128 N64 MMA with both operands there would take the whole shared-memory
         // bandwidth, which the scaling warps also need.
-        {
-            const bool okb = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs));
-            if (okb) {
-                const uint8_t* base = sBt + (nl >> 6) * C::ATOM + ((nl & 7) << 1);
-                const int k16 = (nl & 63) >> 3;                 // this n's 16-byte piece of a row
+        auto copy_bt = [&](uint32_t col) {
+            const uint8_t* base = sBt + (nl >> 6) * C::ATOM + ((nl & 7) << 1);
+            const int k16 = (nl & 63) >> 3;                 // this n's 16-byte piece of a row
 #pragma unroll 1
-                for (int s0 = 0; s0 < L; s0 += 64) {
-                    uint32_t w[32];
+            for (int s0 = 0; s0 < L; s0 += 64) {
+                uint32_t w[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int sa = s0 + 2 * e, sb = sa + 1;
-                        const uint32_t lo = *reinterpret_cast<const uint16_t*>(
-                            base + sa * 128 + ((k16 ^ (sa & 7)) << 4));
-                        const uint32_t hi = *reinterpret_cast<const uint16_t*>(
-                            base + sb * 128 + ((k16 ^ (sb & 7)) << 4));
-                        w[e] = lo | (hi << 16);
-                    }
-                    tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + C::COL_BT + (s0 >> 1), w);
+                for (int e = 0; e < 32; ++e) {
+                    const int sa = s0 + 2 * e, sb = sa + 1;
+                    const uint32_t lo = *reinterpret_cast<const uint16_t*>(
+                        base + sa * 128 + ((k16 ^ (sa & 7)) << 4));
+                    const uint32_t hi = *reinterpret_cast<const uint16_t*>(
+                        base + sb * 128 + ((k16 ^ (sb & 7)) << 4));
+                    w[e] = lo | (hi << 16);
                 }
-                tmem_wait_st();
+                tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + col + (s0 >> 1), w);
             }
-            tc_fence_before();
-            mbar_arrive(&bars.bt_tmem);
-        }
+            tmem_wait_st();
+        };
         if constexpr (kFuse) {
+            {
+                const bool okb = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.bt_full, 0, abort, kWaitNs));
+                if (okb) copy_bt(C::COL_BT);
+                tc_fence_before();
+                mbar_arrive(&bars.bt_tmem[0]);
+            }
             const int64_t bH = (int64_t)fa.nb * H;
             const int Lc = min(L, T - c * L);
             const bool own = nl < NT;
@@ -463,7 +520,48 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                     if (pending[k] >= 0) mbar_wait(&bars.cfull[k], (pending[k] >> 1) & 1, kWaitNs);
             }
         } else {
-            for (int i = 0; i < nh; ++i) {
+            // B^T per segment (the heads of one group of one (b, c, n-tile) in this
+            // CTA's range): segment k's tile is copied into tensor-memory slot k & 1
+            // after the epilogue has finished head f_k - 2 (f_k: the segment's first
+            // head), when the MMAs of segment k - 2 -- the slot's last user -- have
+            // completed; the shared tile is then free, and segment k + 1's B^T is
+            // loaded into it at once, so the MMAs never wait for a reload.
+            const int64_t seg0 = u0 / hpg;
+            const int nseg = (int)((u0 + nh - 1) / hpg - seg0) + 1;
+            auto seg_first = [&](int k) { return k == 0 ? 0 : (int)((seg0 + k) * hpg - u0); };
+            int bt_issued = 1, bt_done = 0;   // B^T loads issued (the producer's first) / landed
+            auto copy_seg = [&](int k) -> bool {
+                if (!__all_sync(0xffffffffu, mbar_wait_or_abort(&bars.bt_full, k & 1, abort, kWaitNs)))
+                    return false;
+                bt_done = k + 1;
+                copy_bt(C::COL_BT + (uint32_t)(k & 1) * C::BT_COLS);
+                tc_fence_before();
+                mbar_arrive(&bars.bt_tmem[k & 1]);
+                if (k + 1 < nseg) {
+                    if (!group_sync()) return false;           // every lane has read the tile
+                    if (ep == 0) {
+                        int64_t sg = seg0 + k + 1;
+                        const int gg = (int)(sg % G);
+                        sg /= G;
+                        const int tt = (int)(sg % n_tiles);
+                        sg /= n_tiles;
+                        const int cc = (int)(sg % nc), bb = (int)(sg / nc);
+                        mbar_arrive_expect_tx(&bars.bt_full, C::BT_BYTES);
+                        for (int a = 0; a < 2; ++a) {
+                            const int n_off = (N == 64) ? 0 : tt * 128 + 64 * a;
+                            tma_load_3d(sBt + a * C::ATOM, &tm_b, &bars.bt_full, gg * N + n_off, cc * L, bb);
+                        }
+                    }
+                    bt_issued = k + 2;
+                }
+                return true;
+            };
+            bool run = copy_seg(0);
+            int kc = 1;
+            while (run && kc < nseg && seg_first(kc) <= 1) run = copy_seg(kc++);
+            UnitIt it;
+            it.init(u0, H, n_tiles, nc);
+            for (int i = 0; run && i < nh; ++i) {
                 const int ab = i & 1, ka = i >> 1;
                 const bool ok = __all_sync(0xffffffffu,
                                            mbar_wait_or_abort(&bars.acc_full[ab], ka & 1, abort, kWaitNs));
@@ -491,12 +589,18 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 fence_proxy_async_smem();
                 if (!group_sync()) break;
                 if (ep == 0) {
-                    const int row = (int)((((int64_t)b * nc + c) * H + h0 + i) * C::P);
-                    tma_store_2d(&tm_d, tile, nt * 128, row);
+                    const int row = (int)((((int64_t)it.b * nc + it.c) * H + it.h) * C::P);
+                    tma_store_2d(&tm_d, tile, it.nt * 128, row);
                     bulk_commit();
                 }
+                it.next(H, n_tiles, nc);
+                while (run && kc < nseg && seg_first(kc) - 2 <= i) run = copy_seg(kc++);
             }
-            if (ep == 0) bulk_wait<0>();
+            if (ep == 0) {
+                bulk_wait<0>();
+                // After an abort: B^T loads still in flight land before the CTA exits.
+                for (int k = bt_done; k < bt_issued; ++k) mbar_wait(&bars.bt_full, k & 1, kWaitNs);
+            }
         }
     }
 
@@ -509,25 +613,33 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
     if (threadIdx.x == 0 && bars.abort) record_error(err, kFuse ? (kErrTimeoutK2 | kErrChainK23) : kErrTimeoutK2);
 }
 
-// Heads per CTA (one CTA per SM at a time): the divisor v of H/G that
-// minimises (waves of CTAs) x (v + 4), i.e. per-SM time in head units with a
-// CTA's fixed work (loading B^T, filling and draining the x ring) counted as
-// about four heads (fitted to measurements: at b8 T4096 H80 N128 whole-path
-// times of 440, 437, 429 and 423 us for 10, 20, 40 and 80 heads per CTA).
-int pick_hpc(const Dims& d, int64_t outer) {
+// Heads per CTA in blocks of one group (one CTA per SM at a time): the divisor
+// v of H/G that minimises (waves of CTAs) x (v + 4), i.e. per-SM time in head
+// units with a CTA's fixed work (loading B^T, filling and draining the x ring)
+// counted as about four heads (fitted to measurements: at b8 T4096 H80 N128
+// whole-path times of 440, 437, 429 and 423 us for 10, 20, 40 and 80 heads per
+// CTA).  *cost receives the minimum.
+int pick_hpc(const Dims& d, int64_t outer, int64_t* cost) {
     const int64_t hpg = d.H / d.G, sms = sm_count();
     int best = 1;
     int64_t best_cost = -1;
     for (int64_t v = 1; v <= hpg; ++v) {
         if (hpg % v) continue;
         const int64_t ctas = outer * (d.H / v);
-        const int64_t cost = (ctas + sms - 1) / sms * (v + 4);
-        if (best_cost < 0 || cost <= best_cost) {
-            best_cost = cost;
+        const int64_t c = (ctas + sms - 1) / sms * (v + 4);
+        if (best_cost < 0 || c <= best_cost) {
+            best_cost = c;
             best = (int)v;
         }
     }
+    *cost = best_cost;
     return best;
+}
+
+// One wave of CTAs over all units: ceil(U / SMs) units each.
+int even_upc(const Dims& d, int64_t units) {
+    const int64_t sms = sm_count();
+    return (int)std::max<int64_t>(1, (units + sms - 1) / sms);
 }
 
 // Fused variant: the largest divisor of H/G (at most 16) for which one chunk's
@@ -580,38 +692,60 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
             return cudaErrorInvalidValue;
     }
     const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
-    const int64_t outer = d.b * d.nc * n_tiles;
+    const int64_t outer = d.b * d.nc * n_tiles, units = outer * d.H;
     // Fused: one chunk's CTAs should fill the GPU, so that the CTA of chunk c
     // typically starts after the one of chunk c-1 has finished (no waiting).
-    int src = kFromModel;
-    const int hpc = kFuse ? pick_hpc_fused(d, n_tiles) : k2_heads_per_cta(d, &src);
-    const int n_hblk = (int)(d.H / hpc);
-    const int64_t grid = outer * n_hblk;
+    // Plain: contiguous ranges of upc units.
+    int hpc = 0, n_hblk = 0, upc = 0;
+    int64_t grid;
+    if (kFuse) {
+        hpc = pick_hpc_fused(d, n_tiles);
+        n_hblk = (int)(d.H / hpc);
+        grid = outer * n_hblk;
+    } else {
+        int src = kFromModel;
+        upc = k2_units_per_cta(d, &src);
+        grid = (units + upc - 1) / upc;
+    }
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     auto k = chunk_state_tc_kernel<L, kFuse, kDS16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(C::kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
                          tm_ring, tm_init, tm_fin, tm_sp, cum2, dtT, (int)d.T, (int)d.H, (int)d.N,
-                         (int)d.G, (int)d.nc, n_tiles, hpc, n_hblk, err, fa, xabs);
+                         (int)d.G, (int)d.nc, n_tiles, hpc, n_hblk, upc, units, err, fa, xabs);
 }
 
 }  // namespace
 
-int k2_heads_per_cta(const Dims& d, int* src) {
-    const int64_t hpg = d.H / d.G;
+int k2_units_per_cta(const Dims& d, int* src) {
+    const int64_t n_tiles = d.N > 128 ? d.N / 128 : 1, outer = d.b * d.nc * n_tiles;
+    const int64_t units = outer * d.H, hpg = d.H / d.G;
+    if (units == 0) {
+        *src = kFromModel;
+        return 1;
+    }
     const int o = tile_override(0);
-    if (o > 0 && hpg % o == 0) {
+    if (o > 0 || o == kEvenSplit) {
         *src = kFromOverride;
-        return o;
+        return o > 0 ? (int)std::min<int64_t>(o, units) : even_upc(d, units);
     }
-    const TileChoice* t = o < 0 ? nullptr : find_tile(d);   // -1: the cost model only
-    if (t && t->k2_hpc > 0 && hpg % t->k2_hpc == 0) {
+    const TileChoice* t = o == -1 ? nullptr : find_tile(d);   // -1: the cost model only
+    if (t && t->k2_hpc >= 0) {
         *src = kFromTable;
-        return t->k2_hpc;
+        return t->k2_hpc > 0 ? (int)std::min<int64_t>(t->k2_hpc, units) : even_upc(d, units);
     }
+    // Cost model: blocks of one group's heads against one wave of even ranges.
+    // A range of u units touches at most 1 + ceil((u - 1) / (H/G)) segments; the
+    // B^T of each further segment is loaded behind the MMAs and its copy into
+    // tensor memory costs about one head.
     *src = kFromModel;
-    const int n_tiles = d.N > 128 ? (int)(d.N / 128) : 1;
-    return pick_hpc(d, d.b * d.nc * n_tiles);
+    int64_t cost_blk = 0;
+    const int hpc = pick_hpc(d, outer, &cost_blk);
+    const int upc = even_upc(d, units);
+    const int64_t segs = 1 + (upc - 1 + hpg - 1) / hpg;
+    const int64_t cost_even = upc + 4 + (segs - 1);
+    return cost_even < cost_blk ? upc : hpc;
 }
 
 bool tc_supported(const Dims& d) {

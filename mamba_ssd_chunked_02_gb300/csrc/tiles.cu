@@ -64,12 +64,12 @@ int tile_override(int k) { return (k >= 0 && k < 4) ? g_override[k].load(std::me
 
 extern "C" {
 
-mamba2_status mamba2_ssd_tile_override(int32_t stage2_heads, int32_t stage4_v1, int32_t stage4_v2,
+mamba2_status mamba2_ssd_tile_override(int32_t stage2_units, int32_t stage4_v1, int32_t stage4_v2,
                                        int32_t stage4_waves1) {
-    if (stage2_heads < -1 || stage4_v1 < -1 || stage4_v2 < 0 || stage4_waves1 < 0)
+    if (stage2_units < m2::kEvenSplit || stage4_v1 < -1 || stage4_v2 < 0 || stage4_waves1 < 0)
         return MAMBA2_ERR_INVALID_ARG;
     if (stage4_v1 <= 0 && (stage4_v2 != 0 || stage4_waves1 != 0)) return MAMBA2_ERR_INVALID_ARG;
-    m2::g_override[0].store(stage2_heads);
+    m2::g_override[0].store(stage2_units);
     m2::g_override[1].store(stage4_v1);
     m2::g_override[2].store(stage4_v2);
     m2::g_override[3].store(stage4_waves1);

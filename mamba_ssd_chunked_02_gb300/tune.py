@@ -7,7 +7,9 @@ Runs on one GPU.  For every swept shape it times, through
 mamba2_ssd_fwd_timed (CUDA events between the stages, recorded on the
 launching stream),
 
-  * stage 2 (chunk states) at every heads-per-CTA count that divides H/G;
+  * stage 2 (chunk states) with blocks of v heads of one group per CTA, for
+    every v dividing H/G, and with one wave of CTAs over even ranges of units
+    (a unit: one head of one (b, chunk, state tile));
   * stage 4 (fused output) at every single head-block size v dividing H/G and
     every two-region split (v1 for the (b, c) pairs of the first k waves of
     CTAs, v2 < v1 for the rest, k = 1 .. while the first region leaves pairs
@@ -138,15 +140,19 @@ def sweep(w, flush, reps, margin, log):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     hpg = w.nheads // w.ngroups
     rec = {"workload": w.name, "sms": sms, "stage2": [], "stage4": []}
-    m2.tile_override(-1, -1)
+    m2.tile_override(m2.MODEL_ONLY, m2.MODEL_ONLY)
     model = m2.tile_choice(r.sh)
     base = r.stage_times(reps)
     rec["model"] = {"choice": model, "stage_ms": base}
-    for v in divisors(hpg):
-        m2.tile_override(v, -1)
-        rec["stage2"].append({"heads": v, "ms": r.stage_times(reps)[1]})
+    # table code of the model's stage-2 choice: blocks of v heads, or 0 = even ranges
+    model_k2 = model["stage2_units"] if hpg % model["stage2_units"] == 0 else 0
+    for v in divisors(hpg) + [m2.EVEN_SPLIT]:
+        m2.tile_override(v, m2.MODEL_ONLY)
+        units = m2.tile_choice(r.sh)["stage2_units"]
+        rec["stage2"].append({"code": v if v > 0 else 0, "units": units,
+                              "ms": r.stage_times(reps)[1]})
     for (v1, v2, k) in stage4_candidates(w, sms):
-        m2.tile_override(-1, v1, v2, k)
+        m2.tile_override(m2.MODEL_ONLY, v1, v2, k)
         c = m2.tile_choice(r.sh)
         rec["stage4"].append({"v1": v1, "v2": v2, "waves1": k, "pairs1": c["stage4_pairs1"],
                               "ms": r.stage_times(reps)[3]})
@@ -154,27 +160,28 @@ def sweep(w, flush, reps, margin, log):
     b4 = min(rec["stage4"], key=lambda e: e["ms"])
     # Whole forward pass: the sweep's winners against the cost models' choice,
     # timed alternately so that drift hits both alike.
-    tuned = (b2["heads"], b4["v1"], b4["v2"], b4["waves1"])
+    tuned = (b2["code"], b4["v1"], b4["v2"], b4["waves1"])
+    force2 = b2["code"] if b2["code"] > 0 else m2.EVEN_SPLIT
     ta, tb = [], []
     for _ in range(3):
         r.call()
     for _ in range(max(20, 2 * reps)):
-        m2.tile_override(-1, -1)
+        m2.tile_override(m2.MODEL_ONLY, m2.MODEL_ONLY)
         ta.append(r.whole_time())
-        m2.tile_override(*tuned)
+        m2.tile_override(force2, *tuned[1:])
         tb.append(r.whole_time())
     m2.tile_override()
     if m2.device_error() != 0:
         raise RuntimeError(f"device-side error while sweeping {w.name}")
     t_model, t_tuned = statistics.fmean(ta), statistics.fmean(tb)
-    same = (model["stage2_heads"], model["stage4_v1"], model["stage4_pairs1"]) == \
-        (b2["heads"], b4["v1"], b4["pairs1"]) and \
+    same = (model["stage2_units"], model["stage4_v1"], model["stage4_pairs1"]) == \
+        (b2["units"], b4["v1"], b4["pairs1"]) and \
         (model["stage4_v2"] == b4["v2"] or b4["pairs1"] == r.sh.batch * r.sh.nchunks)
     keep = not same and t_tuned < t_model * (1.0 - margin)
     if keep:
         entry = tuned
     else:   # table the model's own choice
-        entry = (model["stage2_heads"], model["stage4_v1"],
+        entry = (model_k2, model["stage4_v1"],
                  model["stage4_v2"] if model["stage4_v2"] != model["stage4_v1"] else 0,
                  0)
         if model["stage4_v2"] != model["stage4_v1"]:
@@ -182,7 +189,7 @@ def sweep(w, flush, reps, margin, log):
             per_bc = (w.chunk_size // 128) * (w.nheads // model["stage4_v1"])
             k = next((k for k in range(1, 64) if k * sms // per_bc >= model["stage4_pairs1"]), 0)
             if k and min(k * sms // per_bc, r.sh.batch * r.sh.nchunks) == model["stage4_pairs1"]:
-                entry = (model["stage2_heads"], model["stage4_v1"], model["stage4_v2"], k)
+                entry = (model_k2, model["stage4_v1"], model["stage4_v2"], k)
             else:
                 entry = None    # not expressible in waves: leave the shape to the model
     rec.update({"best_stage2": b2, "best_stage4": b4, "whole_model_ms": t_model,
@@ -191,7 +198,7 @@ def sweep(w, flush, reps, margin, log):
     log.write(json.dumps(rec) + "\n")
     log.flush()
     print(f"{w.name}: model {t_model:.4f} ms, tuned {t_tuned:.4f} ms "
-          f"(stage2 {b2['heads']} heads {b2['ms']:.4f} vs {base[1]:.4f}; stage4 "
+          f"(stage2 {b2['units']} units {b2['ms']:.4f} vs {base[1]:.4f}; stage4 "
           f"{b4['v1']}/{b4['v2']}/{b4['waves1']} {b4['ms']:.4f} vs {base[3]:.4f}) -> "
           f"{rec['tabled']} {entry}", flush=True)
     del r
@@ -210,7 +217,8 @@ def write_table(recs, path, ws):
     lines = [
         "// Generated by mamba_ssd_chunked_02_gb300/tune.py from timings on one GB300; do",
         "// not edit by hand.  One entry per swept shape:",
-        "//   {N, P, L, heads per group, b*nc low, b*nc high, stage-2 heads per CTA,",
+        "//   {N, P, L, heads per group, b*nc low, b*nc high, stage-2 units per CTA",
+        "//    (0: one wave of even ranges),",
         "//    stage-4 block sizes v1, v2, SM waves of the v1 region (0: v1 everywhere)}",
     ]
     seen = set()

@@ -55,7 +55,7 @@ def test_table_entries_are_valid_and_disjoint():
         assert N in (64, 128, 256) and P == 64 and L in (128, 256)
         assert 1 <= lo <= hi
         assert lo & (lo - 1) == 0 and hi == 2 * lo - 1, "power-of-two buckets"
-        assert hpg % k2 == 0 and hpg % v1 == 0
+        assert k2 >= 0 and hpg % v1 == 0
         assert k >= 0 and (k == 0 or (v2 > 0 and hpg % v2 == 0))
         for (a, b) in seen.get((N, P, L, hpg), []):
             assert hi < a or lo > b, "overlapping buckets"
@@ -67,7 +67,9 @@ def test_tabled_shapes_report_their_entry(lib):
         for bnc in sorted({lo, hi, (lo + hi) // 2}):
             c = m2.tile_choice(shape_for(N, P, L, hpg, bnc))
             assert c["stage2_source"] == m2.SOURCE_TABLE and c["stage4_source"] == m2.SOURCE_TABLE
-            assert c["stage2_heads"] == k2 and c["stage4_v1"] == v1
+            units = bnc * (N // 128 if N > 128 else 1) * hpg
+            assert c["stage2_units"] == (min(k2, units) if k2 else -(-units // SMS))
+            assert c["stage4_v1"] == v1
             nq, H = L // 128, hpg
             pairs = bnc if k == 0 else min(bnc, k * SMS // (nq * (H // v1)))
             assert c["stage4_pairs1"] == pairs
@@ -79,7 +81,10 @@ def test_model_choice_outside_the_table(lib):
     sh = m2.make_shape(3, 4096, 12, 64, 128, 2, 256, dtype=m2.BF16)
     c = m2.tile_choice(sh)
     assert c["stage2_source"] == m2.SOURCE_MODEL and c["stage4_source"] == m2.SOURCE_MODEL
-    assert 6 % c["stage2_heads"] == 0 and 6 % c["stage4_v1"] == 0 and 6 % c["stage4_v2"] == 0
+    # stage 2: blocks of heads of one group, or one wave of even ranges
+    units = 3 * 16 * 12
+    assert 6 % c["stage2_units"] == 0 or c["stage2_units"] == -(-units // SMS)
+    assert 6 % c["stage4_v1"] == 0 and 6 % c["stage4_v2"] == 0
     assert 0 <= c["stage4_pairs1"] <= 3 * 16
 
 
@@ -87,14 +92,20 @@ def test_override_forces_and_bypasses(lib):
     sh = m2.make_shape(8, 4096, 80, 64, 128, 1, 256, dtype=m2.BF16)
     m2.tile_override(20, 40, 16, 1)
     c = m2.tile_choice(sh)
-    assert (c["stage2_heads"], c["stage2_source"]) == (20, m2.SOURCE_OVERRIDE)
+    assert (c["stage2_units"], c["stage2_source"]) == (20, m2.SOURCE_OVERRIDE)
     # one wave of 152 SMs at 2 query tiles x 2 head blocks per (b, c) pair: 38 pairs
     assert (c["stage4_v1"], c["stage4_v2"], c["stage4_pairs1"], c["stage4_source"]) == \
         (40, 16, 38, m2.SOURCE_OVERRIDE)
-    # a value that does not divide H/G = 80 is ignored for the shape
+    # stage 2 takes any range length; a stage-4 block size that does not divide
+    # H/G = 80 is ignored for the shape
     m2.tile_override(3, 3)
     c = m2.tile_choice(sh)
-    assert c["stage2_source"] != m2.SOURCE_OVERRIDE and c["stage4_source"] != m2.SOURCE_OVERRIDE
+    assert (c["stage2_units"], c["stage2_source"]) == (3, m2.SOURCE_OVERRIDE)
+    assert c["stage4_source"] != m2.SOURCE_OVERRIDE
+    # one wave of even ranges: 8 * 16 chunks * 80 heads over 152 SMs
+    m2.tile_override(m2.EVEN_SPLIT)
+    c = m2.tile_choice(sh)
+    assert (c["stage2_units"], c["stage2_source"]) == (-(-10240 // SMS), m2.SOURCE_OVERRIDE)
     # -1: the cost model, whatever the table says
     m2.tile_override(-1, -1)
     c = m2.tile_choice(sh)
@@ -106,7 +117,7 @@ def test_override_forces_and_bypasses(lib):
 
 
 def test_override_validation(lib):
-    for args in ((-2, 0, 0, 0), (0, -2, 0, 0), (0, 8, -1, 0), (0, 8, 4, -1), (0, 0, 4, 0),
+    for args in ((-3, 0, 0, 0), (0, -2, 0, 0), (0, 8, -1, 0), (0, 8, 4, -1), (0, 0, 4, 0),
                  (0, 0, 0, 1), (0, -1, 4, 0), (0, -1, 0, 2)):
         with pytest.raises(m2.Mamba2Error) as e:
             m2.tile_override(*args)
