@@ -111,8 +111,10 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  *   ngroups G >= 1 with nheads % G == 0; chunk_size L in {64, 128, 256};
  *   seqlen need not be a multiple of L (the last chunk is shorter).
  * The tensor-core path is used for dtype BF16 with L in {128, 256},
- * P = 64 and N in {64, 128, 256}; every other supported shape runs on
- * the CUDA-core kernels (mamba2_ssd_path reports which). */
+ * P in {64, 128} and N in {64, 128, 256} (P = 128 runs as twice the heads
+ * of 64: the tensors hold the same bytes in either view); every other
+ * supported shape runs on the CUDA-core kernels (mamba2_ssd_path reports
+ * which).  mamba2_ssd_bwd keeps P = 128 on the CUDA-core kernels. */
 typedef struct mamba2_ssd_shape {
     int64_t batch;
     int64_t seqlen;

@@ -128,7 +128,8 @@ Carve carve(const Dims& d) {
     c.dS = c.dtT + align256(sizeof(float) * (size_t)m2::n_cum(d));
     c.Sprev = c.dS + align256(sizeof(float) * (size_t)m2::n_state(d));
     c.xabs = c.Sprev + align256((size_t)m2::esize(d) * (size_t)m2::n_state(d));
-    c.total = c.xabs + align256(8 * sizeof(uint32_t) * (size_t)(d.b * d.nc * d.H));
+    // max |x| per (b, chunk, tensor-core head): H heads, or 2H at P = 128 (tc_view)
+    c.total = c.xabs + align256(8 * sizeof(uint32_t) * (size_t)(d.b * d.nc * m2::tc_view(d).H));
     return c;
 }
 
@@ -474,8 +475,11 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     float* fin = reinterpret_cast<float*>(ws + cv.fin);
     int32_t* err = error_word();
     // Forward stages 1-3: cum2, dtT, dS (fp32), the state entering each chunk (in
-    // the I/O type, stage 4's operand) and the final state.
-    const bool tc = use_tc(shape, d);
+    // the I/O type, stage 4's operand) and the final state.  P = 128 runs the
+    // whole backward on the CUDA cores: with the tensor-core kernels (16-bit
+    // operands, each head as two heads of 64) dA, a signed sum over every token,
+    // missed the fp32 reading by 1.4e-2 relative L2 on a two-head case.
+    const bool tc = use_tc(shape, d) && d.P == 64;
     e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, false, err, s)
@@ -535,8 +539,9 @@ mamba2_status mamba2_ssd_tile_choice(const mamba2_ssd_shape* shape, int32_t* out
     const mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     if (!out) return MAMBA2_ERR_INVALID_ARG;
-    const Dims d = dims_of(shape);
-    if (!use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
+    const Dims d0 = dims_of(shape);
+    if (!use_tc(shape, d0)) return MAMBA2_ERR_UNSUPPORTED;
+    const Dims d = m2::tc_view(d0);   // the launchers choose on this view
     int src2 = 0;
     out[0] = m2::k2_units_per_cta(d, &src2);
     out[1] = src2;

@@ -15,6 +15,9 @@ struct Dims {
     // B, C ([.., G*N]) and dt ([.., H]); contiguous unless set by the strided
     // whole-path call (the stage entry points take contiguous tensors).
     int64_t sx[2], sy[2], sB[2], sC[2], sdt[2];
+    // Tensor-core view only (tc_view): each head is split into 2^pts heads of 64
+    // of its P dimension; per-head inputs (cum2, dtT, D) are read at head >> pts.
+    int pts = 0;
 };
 
 // Contiguous strides for the sizes in d.
@@ -138,6 +141,19 @@ cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaSt
 
 // True when the tcgen05 kernels handle this shape.
 bool tc_supported(const Dims& d);
+
+// The shape the tcgen05 kernels run: P = 128 as twice the heads of P = 64.  x, y
+// ([.., H, P] per token), Sprev and dS ([.., H, P, N]) hold the same bytes in
+// either view; only cum2, dtT and D stay per original head (read at h >> pts).
+inline Dims tc_view(const Dims& d) {
+    Dims v = d;
+    if (d.P == 128) {
+        v.H = 2 * d.H;
+        v.P = 64;
+        v.pts = 1;
+    }
+    return v;
+}
 
 // SMs of the current device (cached per device); kFallbackSMs, a GB300's
 // count, when no device can be queried.

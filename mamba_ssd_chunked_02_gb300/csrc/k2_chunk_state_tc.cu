@@ -151,7 +151,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_fin,    // fused: [b H P][N] f32
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
-                      int T, int H, int N, int G, int nc, int n_tiles,
+                      int T, int H, int N, int G, int nc, int n_tiles, int pts,
                       int hpc, int n_hblk, int upc, int64_t units, int32_t* err,
                       const FuseArgs fa, uint32_t* __restrict__ xabs) {
     using C = K2Cfg<L, kFuse, kDS16>;
@@ -304,7 +304,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
         float pc[RPT], pd[RPT], plast = 0.f;
         auto prefetch = [&](int bb, int cc, int hh) {
             const int Lc = min(L, T - cc * L);
-            const int64_t bh = (int64_t)bb * H + hh;
+            const int64_t bh = (int64_t)bb * (H >> pts) + (hh >> pts);   // the head's cum2 / dt row
             const float* crow = cum2 + bh * T + (int64_t)cc * L;
             const float* drow = dtT + bh * T + (int64_t)cc * L;
             plast = __ldg(crow + Lc - 1);
@@ -475,7 +475,8 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 if (!ok) break;
                 if (ep == 0) pending[buf] = -1;
                 tc_fence_after();
-                const float dec = ex2(__ldg(cum2 + bh * T + (int64_t)c * L + Lc - 1));
+                const int64_t bho = (int64_t)b * (H >> pts) + ((h0 + i) >> pts);
+                const float dec = ex2(__ldg(cum2 + bho * T + (int64_t)c * L + Lc - 1));
 #pragma unroll
                 for (int cc = 0; cc < C::P / 32; ++cc) {
                     uint32_t r[32];
@@ -713,7 +714,7 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(C::kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
                          tm_ring, tm_init, tm_fin, tm_sp, cum2, dtT, (int)d.T, (int)d.H, (int)d.N,
-                         (int)d.G, (int)d.nc, n_tiles, hpc, n_hblk, upc, units, err, fa, xabs);
+                         (int)d.G, (int)d.nc, n_tiles, d.pts, hpc, n_hblk, upc, units, err, fa, xabs);
 }
 
 }  // namespace
@@ -749,15 +750,16 @@ int k2_units_per_cta(const Dims& d, int* src) {
 }
 
 bool tc_supported(const Dims& d) {
-    return d.dtype == 1 && (d.L == 128 || d.L == 256) && d.P == 64 &&
+    return d.dtype == 1 && (d.L == 128 || d.L == 256) && (d.P == 64 || d.P == 128) &&
            (d.N == 64 || d.N == 128 || d.N == 256) && d.T < (int64_t(1) << 31) &&
            d.b * d.nc * d.H * d.P < (int64_t(1) << 31) &&      // TMA row coordinate of Sprev
            d.H * d.P < (int64_t(1) << 31) && d.G * d.N < (int64_t(1) << 31);
 }
 
-cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, const float* cum2,
+cudaError_t launch_chunk_state_tc(const Dims& dq, const void* x, const void* B, const float* cum2,
                                   const float* dtT, void* dS, bool ds16, int32_t* err,
                                   cudaStream_t st, uint32_t* xabs, bool pdl, bool adj) {
+    const Dims d = tc_view(dq);
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     FuseArgs none{};
@@ -771,16 +773,18 @@ cudaError_t launch_chunk_state_tc(const Dims& d, const void* x, const void* B, c
                : launch_k2<128, false, false>(d, x, B, cum2, dtT, dS, none, err, st, xabs, pdl);
 }
 
-int64_t fused_flag_words(const Dims& d) {
+int64_t fused_flag_words(const Dims& dq) {
+    const Dims d = tc_view(dq);
     const int64_t n_tiles = d.N > 128 ? d.N / 128 : 1;
     return d.b * d.H * n_tiles * d.nc;
 }
 
-cudaError_t launch_chunk_state_pass_tc(const Dims& d, const void* x, const void* B,
+cudaError_t launch_chunk_state_pass_tc(const Dims& dq, const void* x, const void* B,
                                        const float* cum2, const float* dtT, const float* init,
                                        float* carry, int32_t* flags, int32_t* ticket,
                                        void* Sprev, float* final_state, int32_t* err,
                                        cudaStream_t st) {
+    const Dims d = tc_view(dq);
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d) || d.b > (1 << 20)) return cudaErrorInvalidValue;
     FuseArgs fa;

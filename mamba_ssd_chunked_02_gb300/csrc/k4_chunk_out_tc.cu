@@ -157,7 +157,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
-                    int G, int nc, int v1, int n1, int v2, int32_t* err) {
+                    int G, int nc, int v1, int n1, int v2, int pts, int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -665,15 +665,15 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
-        const int64_t row0 = ((int64_t)b * H + h0) * T + (int64_t)c * L;   // head h0, chunk c
+        const int64_t row0 = (int64_t)b * (H >> pts) * T + (int64_t)c * L;  // chunk c of batch b
         constexpr int KPT = L / kConvThreads;                  // keys per thread (at most)
         float pc[KPT], pd[KPT], plast = 0.f, pD = 0.f;
 #pragma unroll
         for (int i = 0; i < KPT; ++i) { pc[i] = 0.f; pd[i] = 0.f; }
         uint4 pX = make_uint4(0u, 0u, 0u, 0u), pX2 = pX;
         auto prefetch = [&](int hh) {
-            const float* crow = cum2 + row0 + (int64_t)hh * T;
-            const float* drow = dtT + row0 + (int64_t)hh * T;
+            const float* crow = cum2 + row0 + (int64_t)((h0 + hh) >> pts) * T;   // the head's rows
+            const float* drow = dtT + row0 + (int64_t)((h0 + hh) >> pts) * T;
             plast = __ldg(crow + Lc - 1);
 #pragma unroll
             for (int i = 0; i < KPT; ++i) {
@@ -683,7 +683,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     pd[i] = __ldg(drow + s);
                 }
             }
-            pD = Dvec ? __ldg(Dvec + h0 + hh) : 0.f;
+            pD = Dvec ? __ldg(Dvec + ((h0 + hh) >> pts)) : 0.f;
             if (xabs) {   // stage 2's max |x| of the chunk (eight words, bf16 bits)
                 const uint4* xw = reinterpret_cast<const uint4*>(xabs) + 2 * (((int64_t)b * nc + c) * H + h0 + hh);
                 pX = __ldg(xw);
@@ -885,7 +885,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
-                         sp.v1, (int)sp.n1, sp.v2, err);
+                         sp.v1, (int)sp.n1, sp.v2, d.pts, err);
     }
 }
 
@@ -927,10 +927,11 @@ Split4 k4_split(const Dims& d) {
     return pick_split4(d, (int)(d.L / 128));
 }
 
-cudaError_t launch_chunk_out_tc(const Dims& d, const void* x, const void* B, const void* C,
+cudaError_t launch_chunk_out_tc(const Dims& dq, const void* x, const void* B, const void* C,
                                 const float* cum2, const float* dtT, const void* Sprev,
                                 const float* D, void* y, int32_t* err, cudaStream_t st,
                                 const uint32_t* xabs, bool pdl, bool y32) {
+    const Dims d = tc_view(dq);
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
     if (!tc_supported(d)) return cudaErrorInvalidValue;
     if (y32)

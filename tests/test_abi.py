@@ -102,7 +102,7 @@ def test_path_selection(lib):
     assert m2.path(shp()) == m2.PATH_TCGEN05                  # the 2.7B layer shape
     assert m2.path(shp(chunk_size=128, dstate=64)) == m2.PATH_TCGEN05
     assert m2.path(shp(dstate=256, seqlen=300)) == m2.PATH_TCGEN05
-    assert m2.path(shp(headdim=128)) == m2.PATH_SIMT
+    assert m2.path(shp(headdim=128)) == m2.PATH_TCGEN05       # as twice the heads of P = 64
     assert m2.path(shp(dtype=m2.F32)) == m2.PATH_SIMT
     assert m2.path(shp(chunk_size=64)) == m2.PATH_SIMT
     assert m2.path(shp(headdim=32)) == m2.PATH_SIMT

@@ -52,8 +52,8 @@ CASES = [
     # y' runs fall back to the CUDA cores while the split-head runs (N'' = 64) and
     # the chunk adjoints stay on the tensor cores
     (wl(1, 512, 2, 64, 256, 1, 256, init=0.1, seed=78), True, True),
-    # P = 128: the forward kernels run on the CUDA cores, the split-head runs
-    # (P'' = 64, N'' = P = 128) on the tensor cores
+    # P = 128: the backward's runs stay on the CUDA cores (the forward runs P = 128
+    # on the tensor cores as twice the heads of 64)
     (wl(1, 256, 2, 128, 128, 1, 128, seed=79), True, True),
 ]
 

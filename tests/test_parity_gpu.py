@@ -42,6 +42,7 @@ SMALL = [
     wl(1, 512, 2, 64, 256, 1, 256, seed=15),                            # N = 256
     wl(1, 640, 2, 64, 128, 1, 256, seed=16, dt_lo=1e-4),                # wide decay range
     wl(1, 300, 4, 128, 64, 2, 128, init=0.1, seed=17),                  # P = 128, ragged
+    wl(2, 600, 4, 128, 128, 2, 256, init=0.1, seed=22),                 # P = 128, L = 256, groups
     wl(1, 200, 4, 32, 32, 2, 64, seed=18),                              # small P/N, bf16 SIMT
     wl(2, 192, 3, 16, 16, 3, 64, dtype="f32", init=0.1, seed=19),       # fp32, G = H
     wl(1, 100, 2, 64, 128, 1, 256, seed=20),                            # T < L
@@ -64,7 +65,10 @@ def test_fwd_matches_oracle(w):
     assert_close(to_np(f), fr, w.dtype, f"final_state {w.name}")
 
 
-@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+TC_SMALL = SMALL[1:9]   # bf16 shapes on the tensor-core path (P = 128 as 2H heads of 64)
+
+
+@pytest.mark.parametrize("w", TC_SMALL, ids=_ids(TC_SMALL))
 def test_stages_match_oracle(w):
     """Each stage against the oracle's chunked intermediates."""
     inp = W.make_inputs(w)
@@ -105,7 +109,7 @@ def test_stages_match_oracle(w):
     assert m2.device_error() == 0
 
 
-@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+@pytest.mark.parametrize("w", TC_SMALL, ids=_ids(TC_SMALL))
 def test_tensor_core_path_matches_cuda_core_path(w):
     """Both paths are within the tolerance of the oracle (checked above); by the
     triangle inequality they are within twice that tolerance of each other (two
@@ -129,6 +133,7 @@ FUSED = [
     wl(1, 768, 2, 64, 256, 1, 256, seed=32),                            # N = 256: two n-tiles
     wl(2, 640, 16, 64, 128, 4, 128, init=0.1, seed=33),                 # L = 128, ragged, groups, init
     wl(1, 2048, 4, 64, 64, 1, 256, seed=34),                            # N = 64, 8 chunks
+    wl(1, 1024, 4, 128, 128, 2, 256, seed=35),                          # P = 128: 8 heads of 64
 ]
 
 
@@ -234,7 +239,7 @@ def test_fused_path_repeats_exactly():
         assert torch.equal(y, outs[0][0]) and torch.equal(f, outs[0][1])
 
 
-@pytest.mark.parametrize("w", SMALL[1:8], ids=_ids(SMALL[1:8]))
+@pytest.mark.parametrize("w", TC_SMALL, ids=_ids(TC_SMALL))
 def test_overlapped_launches_match_serial(w):
     """Stages 2-4 start early by programmatic dependent launch and read their
     predecessor's outputs only after it completed: the outputs equal those of
@@ -248,6 +253,7 @@ def test_overlapped_launches_match_serial(w):
 
 STRIDED = [
     wl(2, 640, 4, 64, 128, 1, 256, seed=51),                            # tensor-core shape
+    wl(1, 520, 2, 128, 64, 1, 128, seed=53),                            # tensor cores, P = 128
     wl(1, 300, 4, 32, 32, 2, 64, dtype="f32", init=0.1, seed=52),       # CUDA-core shape
 ]
 
