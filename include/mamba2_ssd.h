@@ -114,7 +114,12 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  * P in {64, 128} and N in {64, 128, 256} (P = 128 runs as twice the heads
  * of 64: the tensors hold the same bytes in either view); every other
  * supported shape runs on the CUDA-core kernels (mamba2_ssd_path reports
- * which).  mamba2_ssd_bwd keeps P = 128 on the CUDA-core kernels. */
+ * which).  mamba2_ssd_bwd keeps P = 128 on the CUDA-core kernels.
+ * The whole-path calls (mamba2_ssd_fwd, _fwd_strided, _fwd_timed,
+ * _fwd_noalloc) run chunk_size 64 as 128-token chunks on shapes the tensor
+ * cores take at 128: y and final_state do not depend on the chunk length.
+ * The stage entry points, whose intermediates are laid out per chunk, keep
+ * L = 64 on the CUDA cores. */
 typedef struct mamba2_ssd_shape {
     int64_t batch;
     int64_t seqlen;

@@ -115,6 +115,23 @@ bool use_tc(const mamba2_ssd_shape* s, const Dims& d) {
     return !(s->flags & MAMBA2_FLAG_FORCE_SIMT) && m2::tc_supported(d);
 }
 
+// The dimensions the whole-path call runs with.  A chunk length of 64 on a shape
+// the tensor cores take at 128 runs as 128-token chunks: y and the final state
+// do not depend on the chunk length (only the intermediates do, and the
+// whole-path call does not return them), and a 64-row query tile would leave
+// half of every tcgen05 MMA's rows idle.  The workspace this needs is never
+// larger than the one mamba2_ssd_workspace_size reports for the shape.
+Dims whole_dims(const mamba2_ssd_shape* s) {
+    Dims d = dims_of(s);
+    if (d.L == 64 && !(s->flags & MAMBA2_FLAG_FORCE_SIMT)) {
+        Dims e = d;
+        e.L = 128;
+        e.nc = (d.T + 127) / 128;
+        if (m2::tc_supported(e)) return e;
+    }
+    return d;
+}
+
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Carve {
@@ -200,7 +217,7 @@ mamba2_status mamba2_ssd_check_shape(const mamba2_ssd_shape* shape) { return che
 
 int32_t mamba2_ssd_path(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return -1;
-    return use_tc(shape, dims_of(shape)) ? MAMBA2_PATH_TCGEN05 : MAMBA2_PATH_SIMT;
+    return use_tc(shape, whole_dims(shape)) ? MAMBA2_PATH_TCGEN05 : MAMBA2_PATH_SIMT;
 }
 
 size_t mamba2_ssd_workspace_size(const mamba2_ssd_shape* shape) {
@@ -327,7 +344,7 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
                        const mamba2_ssd_strides* strides = nullptr) {
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
-    Dims d = dims_of(shape);
+    Dims d = whole_dims(shape);
     if (strides && (st = set_strides(d, strides)) != MAMBA2_OK) return st;
     const bool empty = d.b * d.T * d.H == 0;
     if (!req(x, empty) || !req(dt, empty) || !req(A, empty) || !req(B, empty) ||
@@ -539,7 +556,7 @@ mamba2_status mamba2_ssd_tile_choice(const mamba2_ssd_shape* shape, int32_t* out
     const mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     if (!out) return MAMBA2_ERR_INVALID_ARG;
-    const Dims d0 = dims_of(shape);
+    const Dims d0 = whole_dims(shape);
     if (!use_tc(shape, d0)) return MAMBA2_ERR_UNSUPPORTED;
     const Dims d = m2::tc_view(d0);   // the launchers choose on this view
     int src2 = 0;

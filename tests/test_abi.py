@@ -104,7 +104,8 @@ def test_path_selection(lib):
     assert m2.path(shp(dstate=256, seqlen=300)) == m2.PATH_TCGEN05
     assert m2.path(shp(headdim=128)) == m2.PATH_TCGEN05       # as twice the heads of P = 64
     assert m2.path(shp(dtype=m2.F32)) == m2.PATH_SIMT
-    assert m2.path(shp(chunk_size=64)) == m2.PATH_SIMT
+    assert m2.path(shp(chunk_size=64)) == m2.PATH_TCGEN05     # the whole path: 128-token chunks
+    assert m2.path(shp(chunk_size=64, dtype=m2.F32)) == m2.PATH_SIMT
     assert m2.path(shp(headdim=32)) == m2.PATH_SIMT
     assert m2.path(shp(flags=m2.FLAG_FORCE_SIMT)) == m2.PATH_SIMT
 

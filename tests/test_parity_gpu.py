@@ -43,6 +43,7 @@ SMALL = [
     wl(1, 640, 2, 64, 128, 1, 256, seed=16, dt_lo=1e-4),                # wide decay range
     wl(1, 300, 4, 128, 64, 2, 128, init=0.1, seed=17),                  # P = 128, ragged
     wl(2, 600, 4, 128, 128, 2, 256, init=0.1, seed=22),                 # P = 128, L = 256, groups
+    wl(2, 500, 4, 64, 128, 2, 64, init=0.1, seed=23),                   # L = 64 (whole path: 128)
     wl(1, 200, 4, 32, 32, 2, 64, seed=18),                              # small P/N, bf16 SIMT
     wl(2, 192, 3, 16, 16, 3, 64, dtype="f32", init=0.1, seed=19),       # fp32, G = H
     wl(1, 100, 2, 64, 128, 1, 256, seed=20),                            # T < L
@@ -65,7 +66,7 @@ def test_fwd_matches_oracle(w):
     assert_close(to_np(f), fr, w.dtype, f"final_state {w.name}")
 
 
-TC_SMALL = SMALL[1:9]   # bf16 shapes on the tensor-core path (P = 128 as 2H heads of 64)
+TC_SMALL = SMALL[1:10]  # bf16 shapes on the tensor-core path (P = 128 as 2H heads of 64)
 
 
 @pytest.mark.parametrize("w", TC_SMALL, ids=_ids(TC_SMALL))
@@ -297,6 +298,20 @@ def test_strided_inputs_and_output(w, pad):
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=G)
     assert_close(to_np(y), yr, w.dtype, "strided y")
     assert_close(to_np(f1), fr, w.dtype, "strided final_state")
+
+
+def test_chunk_size_64_runs_as_128():
+    """A bf16 whole-path call with chunk_size 64 on a tensor-core shape runs as
+    128-token chunks: the same bits as the call with chunk_size 128."""
+    w64 = wl(2, 700, 4, 64, 128, 2, 64, init=0.1, seed=24)
+    assert m2.path(m2.make_shape(2, 700, 4, 64, 128, 2, 64, dtype=m2.BF16)) == m2.PATH_TCGEN05
+    inp = W.make_inputs(w64)
+    y64, f64 = run_fwd(inp, w64)
+    y128, f128 = run_fwd(inp, w64.scaled(chunk_size=128))
+    assert torch.equal(y64, y128) and torch.equal(f64, f128)
+    yr, fr = oracle.ssd_recurrent(**inp, ngroups=w64.ngroups)
+    assert_close(to_np(y64), yr, w64.dtype, "y")
+    assert_close(to_np(f64), fr, w64.dtype, "final_state")
 
 
 def test_chunk_size_independence():
