@@ -160,7 +160,10 @@ struct BwdCarve {
         SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, total;
 };
 
-BwdCarve bwd_carve(const Dims& d) {
+// copies: the dC / dB runs take the CUDA cores and read per-head copies (xB,
+// xCr) and per-run-head rows (cum2d, dtTd, cum2rd, onesd); the tensor-core runs
+// read B, C reversed and the per-head rows directly.
+BwdCarve bwd_carve(const Dims& d, bool copies) {
     BwdCarve c;
     const size_t E = (size_t)m2::esize(d);
     const size_t Q = d.N >= 64 ? (size_t)(d.N / 64) : 1;
@@ -187,15 +190,15 @@ BwdCarve bwd_carve(const Dims& d) {
     take(c.Cr, bcE);
     take(c.cum2r, cum);
     take(c.ones, cum);
-    take(c.xB, hnE);
-    take(c.xCr, hnE);
+    take(c.xB, copies ? hnE : 0);
+    take(c.xCr, copies ? hnE : 0);
     take(c.xr, xyE);
     take(c.SprevT, stE);
     take(c.GnT, stE);
-    take(c.cum2d, cumq);
-    take(c.dtTd, cumq);
-    take(c.cum2rd, cumq);
-    take(c.onesd, cumq);
+    take(c.cum2d, copies ? cumq : 0);
+    take(c.dtTd, copies ? cumq : 0);
+    take(c.cum2rd, copies ? cumq : 0);
+    take(c.onesd, copies ? cumq : 0);
     take(c.yC, hnE);
     take(c.zB, hnE);
     c.total = o;
@@ -203,6 +206,13 @@ BwdCarve bwd_carve(const Dims& d) {
 }
 
 mamba2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MAMBA2_OK : MAMBA2_ERR_CUDA; }
+
+// The backward's tensor-core choices: its own runs (P = 64 only), and whether
+// its dC / dB runs take the tensor cores (then without per-head copies).
+bool bwd_tc(const mamba2_ssd_shape* s, const Dims& d) { return use_tc(s, d) && d.P == 64; }
+bool bwd_copies(const mamba2_ssd_shape* s, const Dims& d) {
+    return !(bwd_tc(s, d) && m2::tc_supported(m2::bwd_run_dims(d)));
+}
 
 // A required pointer: non-null and 16-byte aligned, unless the tensor is empty.
 bool req(const void* p, bool empty) { return empty || (p && aligned16(p)); }
@@ -446,7 +456,8 @@ mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x,
 
 size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return 0;
-    return bwd_carve(dims_of(shape)).total;
+    const Dims d = dims_of(shape);
+    return bwd_carve(d, bwd_copies(shape, d)).total;
 }
 
 mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
@@ -468,7 +479,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
         return MAMBA2_ERR_INVALID_ARG;
     if (D && !dD) return MAMBA2_ERR_INVALID_ARG;
     if (d.L > 256 || d.P > 128) return MAMBA2_ERR_UNSUPPORTED;
-    const BwdCarve cv = bwd_carve(d);
+    const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d));
     if (!empty && (!workspace || workspace_bytes < cv.total ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MAMBA2_ERR_WORKSPACE;
@@ -496,7 +507,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     // whole backward on the CUDA cores: with the tensor-core kernels (16-bit
     // operands, each head as two heads of 64) dA, a signed sum over every token,
     // missed the fp32 reading by 1.4e-2 relative L2 on a two-head case.
-    const bool tc = use_tc(shape, d) && d.P == 64;
+    const bool tc = bwd_tc(shape, d);
     e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
     if (e == cudaSuccess)
         e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, false, err, s)

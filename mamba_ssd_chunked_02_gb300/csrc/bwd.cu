@@ -306,6 +306,7 @@ struct PrepArgs {
     void *dyr, *Br, *Cr, *xB, *xCr, *xr;
     float *cum2r, *ones, *cum2d, *dtTd, *cum2rd, *onesd;
     int T, H, G, P, N, L, Q;
+    int copies;   // write xB, xCr and the per-(Q*H)-head rows (the CUDA-core dC / dB runs)
 };
 
 template <typename TI>
@@ -328,6 +329,13 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
     copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
     copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
+    for (int h = threadIdx.x; h < a.H; h += kThreads) {
+        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
+        const int64_t o = ((int64_t)b * a.H + h) * a.T + t;
+        a.cum2r[o] = c2[c * a.L + Lc - 1] - c2[ts];
+        a.ones[o] = 1.f;
+    }
+    if (!a.copies) return;   // the tensor-core runs read B, Br, cum2, dtT, cum2r, ones directly
     // Per-head copies of the group's B (natural order) and C (reversed).
     {
         const int64_t n16 = (int64_t)a.N * E / 16;
@@ -341,12 +349,6 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
             xb[i] = Bs[src];
             xc[i] = Cs[src];
         }
-    }
-    for (int h = threadIdx.x; h < a.H; h += kThreads) {
-        const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
-        const int64_t o = ((int64_t)b * a.H + h) * a.T + t;
-        a.cum2r[o] = c2[c * a.L + Lc - 1] - c2[ts];
-        a.ones[o] = 1.f;
     }
     for (int hq = threadIdx.x; hq < a.Q * a.H; hq += kThreads) {
         const int h = hq / a.Q;
@@ -560,9 +562,11 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc);
     // The dC / dB runs: Q heads of N/Q columns per head (64 wide when N >= 64).
     const int Q = d.N >= 64 ? (int)(d.N / 64) : 1;
+    const Dims d2 = bwd_run_dims(d);
+    const bool tc2 = tc && tc_supported(d2);
     PrepArgs pa{a.dy, a.B, a.C, a.x, a.cum2, a.dtT, w.dyr, w.Br, w.Cr, w.xB, w.xCr, w.xr,
                 w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
-                (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q};
+                (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1};
     bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
     bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
                                                              static_cast<TI*>(w.SprevT),
@@ -574,16 +578,26 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
     e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
     if (e != cudaSuccess) return e;
-    Dims d2 = d;   // Q*H heads of N/Q, H groups of Q, state dimension P
-    d2.H = Q * d.H;
-    d2.P = d.N / Q;
-    d2.N = d.P;
-    d2.G = d.H;
-    set_contiguous(d2);
     // The per-head outputs in the I/O type: the head sum that follows is in fp32.
-    e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC, false);          // S^T dy
-    if (e == cudaSuccess)
-        e = out4(d2, w.xCr, w.dyr, w.xr, w.cum2rd, w.onesd, w.GnT, w.zB, false);   // G^T x
+    if (tc2) {
+        // Run head h*Q + q reads columns 64 q .. of its group's B (dC run) or of Br,
+        // the group's C reversed (dB run), and cum2 / dt rows of head h.
+        Dims dm = d2;
+        dm.pts = Q == 4 ? 2 : (Q == 2 ? 1 : 0);
+        dm.xcols = d.G * d.N;
+        dm.xdiv = Q * (int)(d.H / d.G);
+        dm.xmul = d.N;
+        dm.xmod = Q;
+        dm.sx[1] = d.G * d.N;
+        dm.sx[0] = d.T * d.G * d.N;
+        e = out4(dm, a.B, a.x, a.dy, a.cum2, a.dtT, w.SprevT, w.yC, false);           // S^T dy
+        if (e == cudaSuccess)
+            e = out4(dm, w.Br, w.dyr, w.xr, w.cum2r, w.ones, w.GnT, w.zB, false);     // G^T x
+    } else {
+        e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC, false);        // S^T dy
+        if (e == cudaSuccess)
+            e = out4(d2, w.xCr, w.dyr, w.xr, w.cum2rd, w.onesd, w.GnT, w.zB, false); // G^T x
+    }
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
@@ -592,6 +606,17 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
 }
 
 }  // namespace
+
+Dims bwd_run_dims(const Dims& d) {
+    const int64_t Q = d.N >= 64 ? d.N / 64 : 1;
+    Dims d2 = d;   // Q*H heads of N/Q, H groups of Q, state dimension P
+    d2.H = Q * d.H;
+    d2.P = d.N / Q;
+    d2.N = d.P;
+    d2.G = d.H;
+    set_contiguous(d2);
+    return d2;
+}
 
 cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,
                             const void* dy, const float* A, const float* D, const float* cum2,

@@ -18,6 +18,12 @@ struct Dims {
     // Tensor-core view only (tc_view): each head is split into 2^pts heads of 64
     // of its P dimension; per-head inputs (cum2, dtT, D) are read at head >> pts.
     int pts = 0;
+    // Tensor-core output stage only: x of head h starts at column
+    // (h / xdiv) * xmul + (h % xmod) * 64 of an x tensor xcols wide (0: xmul = P,
+    // xcols = H * P, i.e. x laid out [.., H, P]).  The backward's runs read B and C
+    // of a head's group this way instead of per-head copies.
+    int xdiv = 1, xmod = 1;
+    int64_t xmul = 0, xcols = 0;
 };
 
 // Contiguous strides for the sizes in d.
@@ -127,6 +133,9 @@ struct BwdWork {
     void* yC;       // [b,T,H,N] S^T dy per head (I/O type)
     void* zB;       // [b,T,H,N] G^T x per head, reversed chunks (I/O type)
 };
+// The dC / dB runs of the backward: Q = N/64 heads of 64 columns per head (one
+// when N < 64), H groups of Q, state dimension P.
+Dims bwd_run_dims(const Dims& d);
 // tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
 // dA and dD (if given) are accumulated into (zero them first); dinit may be null.
 cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,

@@ -157,7 +157,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
-                    int G, int nc, int v1, int n1, int v2, int pts, int32_t* err) {
+                    int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
+                    int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -252,10 +253,10 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                         c * L + 128 * qt, b);
                 } else {
                     const int h = h0 + it - NA;
+                    const int xcol = (h / xdiv) * xmul + (h % xmod) * C::P;
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
                     for (int r = 0; r < KS / 128; ++r)
-                        tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], h * C::P,
-                                    c * L + 128 * r, b);
+                        tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + 128 * r, b);
                     const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
                     // Sprev comes from stage 3: with programmatic dependent launch
                     // everything before this point ran while it was finishing.
@@ -860,7 +861,8 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
         return cudaErrorNotSupported;
     } else {
     CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
-    const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
+    const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};     // y
+    const uint64_t xin[3] = {(uint64_t)(d.xcols ? d.xcols : d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.sx[1] * 2), (uint64_t)(d.sx[0] * 2)};   // token, batch
     constexpr uint64_t ye = kY32 ? 4 : 2;   // bytes per y element
     const uint64_t ys[2] = {(uint64_t)(d.sy[1] * ye), (uint64_t)(d.sy[0] * ye)};
@@ -872,7 +874,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint64_t sd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
     const uint64_t ss[1] = {(uint64_t)(d.N * 2)};
     const uint32_t sbox[2] = {64, 64};
-    if (!make_tmap_bf16(&tm_x, x, 3, xd, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
+    if (!make_tmap_bf16(&tm_x, x, 3, xin, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
         !make_tmap_bf16(&tm_c, Cm, 3, bd, cs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
         !(kY32 ? make_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, 3, xd, ys, ybox,
                            CU_TENSOR_MAP_SWIZZLE_128B)
@@ -885,7 +887,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
-                         sp.v1, (int)sp.n1, sp.v2, d.pts, err);
+                         sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod, err);
     }
 }
 
