@@ -199,7 +199,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies) {
     take(c.dtTd, copies ? cumq : 0);
     take(c.cum2rd, copies ? cumq : 0);
     take(c.onesd, copies ? cumq : 0);
-    take(c.yC, hnE);
+    take(c.yC, copies ? hnE : 0);   // the tensor-core dC run adds into dC directly
     take(c.zB, hnE);
     c.total = o;
     return c;

@@ -391,7 +391,7 @@ template <typename TI>
 __global__ void __launch_bounds__(kThreads)
 bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
               const float* __restrict__ dtT, float* __restrict__ dB, float* __restrict__ dC,
-              int T, int H, int G, int N, int L) {
+              int T, int H, int G, int N, int L, int with_dc) {
     const int t = blockIdx.x, b = blockIdx.y;
     const int c = t / L, k = t - c * L;
     const int Lc = min(L, T - c * L);
@@ -405,10 +405,10 @@ bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
         float sc = 0.f, sb = 0.f;
         for (int hh = 0; hh < hpg; ++hh) {
             const int h = g * hpg + hh;
-            sc += to_f32(yc[(int64_t)h * N + n]);
+            if (with_dc) sc += to_f32(yc[(int64_t)h * N + n]);
             sb = fmaf(dtT[((int64_t)b * H + h) * T + t], to_f32(zb[(int64_t)h * N + n]), sb);
         }
-        dC[(bt + t) * (int64_t)G * N + e] = sc;
+        if (with_dc) dC[(bt + t) * (int64_t)G * N + e] = sc;
         dB[(bt + t) * (int64_t)G * N + e] = sb;
     }
 }
@@ -590,7 +590,17 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dm.xmod = Q;
         dm.sx[1] = d.G * d.N;
         dm.sx[0] = d.T * d.G * d.N;
-        e = out4(dm, a.B, a.x, a.dy, a.cum2, a.dtT, w.SprevT, w.yC, false);           // S^T dy
+        // dC = sum over the group's heads of S^T dy: each run head adds its fp32
+        // output straight into dC (columns 64 q .. of its group).  The fp32-output
+        // variant fits shared memory here (N'' = P <= 128).
+        Dims dr = dm;
+        dr.yred = 1;
+        dr.sy[1] = d.G * d.N;
+        dr.sy[0] = d.T * d.G * d.N;
+        e = cudaMemsetAsync(a.dC, 0, sizeof(float) * (size_t)(d.b * d.T * d.G * d.N), st);
+        if (e == cudaSuccess)
+            e = launch_chunk_out_tc(dr, a.B, a.x, a.dy, a.cum2, a.dtT, w.SprevT, nullptr, a.dC, err, st,
+                                    nullptr, false, true);
         if (e == cudaSuccess)
             e = out4(dm, w.Br, w.dyr, w.xr, w.cum2r, w.ones, w.GnT, w.zB, false);     // G^T x
     } else {
@@ -601,7 +611,8 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
     bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
-        static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
+        static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T, (int)d.H,
+        (int)d.G, (int)d.N, (int)d.L, tc2 ? 0 : 1);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,10 @@ struct Dims {
     // of a head's group this way instead of per-head copies.
     int xdiv = 1, xmod = 1;
     int64_t xmul = 0, xcols = 0;
+    // Tensor-core output stage with fp32 y only: add y of head h into the fp32
+    // tensor y (xcols wide, element strides sy) at the x column of head h,
+    // instead of storing it (the backward's head sums).
+    int yred = 0;
 };
 
 // Contiguous strides for the sizes in d.

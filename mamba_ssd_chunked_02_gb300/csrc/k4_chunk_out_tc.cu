@@ -158,7 +158,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
-                    int32_t* err) {
+                    int yred, int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -475,7 +475,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_3d(&tm_y, yw, (h0 + hp) * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
+                const int hy = h0 + hp;
+                if (kY32 && yred)   // add into the head's columns of the summed tensor
+                    tma_reduce_add_3d(&tm_y, yw, (hy / xdiv) * xmul + (hy % xmod) * C::P + grp * PC,
+                                      c * L + 128 * qt + 32 * q, b);
+                else
+                    tma_store_3d(&tm_y, yw, hy * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
                 bulk_commit();
             }
             return true;
@@ -876,7 +881,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint32_t sbox[2] = {64, 64};
     if (!make_tmap_bf16(&tm_x, x, 3, xin, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
         !make_tmap_bf16(&tm_c, Cm, 3, bd, cs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
-        !(kY32 ? make_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, 3, xd, ys, ybox,
+        !(kY32 ? make_tmap(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, y, 3, d.yred ? xin : xd, ys, ybox,
                            CU_TENSOR_MAP_SWIZZLE_128B)
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
@@ -887,7 +892,8 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
-                         sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod, err);
+                         sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
+                         d.yred, err);
     }
 }
 

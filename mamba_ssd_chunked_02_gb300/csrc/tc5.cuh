@@ -177,6 +177,15 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
         "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// Shared -> global tiled reduction: adds the tile to the tensor's elements
+// (element type from the tensor map; rows past its extent are clipped).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, const void* src, int x, int y,
+                                                  int z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(m),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
