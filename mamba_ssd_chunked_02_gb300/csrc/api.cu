@@ -193,8 +193,8 @@ BwdCarve bwd_carve(const Dims& d, bool copies) {
     take(c.xB, copies ? hnE : 0);
     take(c.xCr, copies ? hnE : 0);
     take(c.xr, xyE);
-    take(c.SprevT, stE);
-    take(c.GnT, stE);
+    take(c.SprevT, copies ? stE : 0);   // the tensor-core runs read them untransposed
+    take(c.GnT, copies ? stE : 0);
     take(c.cum2d, copies ? cumq : 0);
     take(c.dtTd, copies ? cumq : 0);
     take(c.cum2rd, copies ? cumq : 0);

@@ -568,11 +568,13 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
                 w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
                 (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1};
     bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
-    bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
-                                                             static_cast<TI*>(w.SprevT),
-                                                             (int)d.P, (int)d.N);
-    bwd_transpose<float, TI><<<(unsigned)gt, kThreads, 0, st>>>(a.Gn, static_cast<TI*>(w.GnT),
-                                                                (int)d.P, (int)d.N);
+    if (!tc2) {   // the tensor-core runs read Sprev and Gn untransposed
+        bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
+                                                                 static_cast<TI*>(w.SprevT),
+                                                                 (int)d.P, (int)d.N);
+        bwd_transpose<float, TI><<<(unsigned)gt, kThreads, 0, st>>>(a.Gn, static_cast<TI*>(w.GnT),
+                                                                    (int)d.P, (int)d.N);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // y' = stage 4 on the reversed inputs: x' = dy, B' = C, C' = B, Gn carried.
     const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
@@ -583,6 +585,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         // Run head h*Q + q reads columns 64 q .. of its group's B (dC run) or of Br,
         // the group's C reversed (dB run), and cum2 / dt rows of head h.
         Dims dm = d2;
+        dm.st_mn = 1;   // Sprev / Gn untransposed: rows of head h, columns 64 q ..
         dm.pts = Q == 4 ? 2 : (Q == 2 ? 1 : 0);
         dm.xcols = d.G * d.N;
         dm.xdiv = Q * (int)(d.H / d.G);
@@ -599,10 +602,10 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dr.sy[0] = d.T * d.G * d.N;
         e = cudaMemsetAsync(a.dC, 0, sizeof(float) * (size_t)(d.b * d.T * d.G * d.N), st);
         if (e == cudaSuccess)
-            e = launch_chunk_out_tc(dr, a.B, a.x, a.dy, a.cum2, a.dtT, w.SprevT, nullptr, a.dC, err, st,
+            e = launch_chunk_out_tc(dr, a.B, a.x, a.dy, a.cum2, a.dtT, a.Sprev, nullptr, a.dC, err, st,
                                     nullptr, false, true);
         if (e == cudaSuccess)
-            e = out4(dm, w.Br, w.dyr, w.xr, w.cum2r, w.ones, w.GnT, w.zB, false);     // G^T x
+            e = out4(dm, w.Br, w.dyr, w.xr, w.cum2r, w.ones, a.GnIO, w.zB, false);   // G^T x
     } else {
         e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC, false);        // S^T dy
         if (e == cudaSuccess)

@@ -28,6 +28,11 @@ struct Dims {
     // tensor y (xcols wide, element strides sy) at the x column of head h,
     // instead of storing it (the backward's head sums).
     int yred = 0;
+    // Tensor-core output stage only: the carried state of head h is read
+    // untransposed, as GEMM3's operand in MN-major form: rows (h / xmod) * N .. of
+    // a [.., P' = N, N' = xmod * 64] state tensor (P', N' the state's own sizes), the
+    // 64 columns from (h % xmod) * 64 (the backward's runs on transposed states).
+    int st_mn = 0;
 };
 
 // Contiguous strides for the sizes in d.

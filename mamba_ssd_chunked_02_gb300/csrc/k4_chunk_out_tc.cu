@@ -158,7 +158,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
-                    int yred, int32_t* err) {
+                    int yred, int st_mn, int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -257,12 +257,19 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
                     for (int r = 0; r < KS / 128; ++r)
                         tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + 128 * r, b);
-                    const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
                     // Sprev comes from stage 3: with programmatic dependent launch
                     // everything before this point ran while it was finishing.
                     if (it == NA) grid_dep_wait();
-                    for (int a = 0; a < NA; ++a)
-                        tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
+                    if (st_mn) {   // untransposed state: N rows of (h / xmod), 64 columns
+                        const int srow = (int)((((int64_t)b * nc + c) * (H / xmod) + h / xmod) * N);
+                        for (int a = 0; a < NA; ++a)
+                            tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], (h % xmod) * 64,
+                                        srow + 64 * a);
+                    } else {
+                        const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
+                        for (int a = 0; a < NA; ++a)
+                            tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
+                    }
                 }
                 issued = it + 1;
             }
@@ -276,6 +283,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const uint32_t c_addr = smem_u32(sC);
             const uint32_t id_cb = idesc_bf16_f32(128, KS, 0, 0);
             constexpr uint32_t id_s3 = idesc_bf16_f32(128, 64, 0, 0);
+            constexpr uint32_t id_s3mn = idesc_bf16_f32(128, 64, 0, 1);   // B MN-major
             // Descriptors are formed once here; each MMA only adds a constant byte
             // offset / 16 to the start-address field: an MMA issue waits for the
             // scalar work in front of it, so that work is kept out of the chains
@@ -314,10 +322,17 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 tc_fence_after();
                 const uint64_t sd = sk_desc0 + (uint64_t)st * kStageD;
                 const uint32_t acc = tmem + COL_S + 64 * ab;
+                if (st_mn) {   // B = the state tile as [K rows][64 columns], MN-major
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk)
-                    mma_ss(acc, c_desc + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                           sd + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id_s3, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < N / 16; ++kk)
+                        mma_ss(acc, c_desc + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                               sd + (uint64_t)(kk * (2048 >> 4)), id_s3mn, kk > 0 ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < N / 16; ++kk)
+                        mma_ss(acc, c_desc + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                               sd + (uint64_t)(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), id_s3, kk > 0 ? 1u : 0u);
+                }
                 return true;
             };
             if (ok && nh > 0) ok = gemm3(0);
@@ -876,8 +891,11 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     const uint64_t bd[3] = {(uint64_t)(d.G * d.N), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t bs[2] = {(uint64_t)(d.sB[1] * 2), (uint64_t)(d.sB[0] * 2)};
     const uint64_t cs[2] = {(uint64_t)(d.sC[1] * 2), (uint64_t)(d.sC[0] * 2)};
-    const uint64_t sd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
-    const uint64_t ss[1] = {(uint64_t)(d.N * 2)};
+    // state rows of 64 x 64 tiles: [(b, c, h, p)][n], or untransposed (st_mn)
+    const uint64_t scols = d.st_mn ? (uint64_t)(d.xmod * 64) : (uint64_t)d.N;
+    const uint64_t srows = d.st_mn ? (uint64_t)(d.b * d.nc * (d.H / d.xmod) * d.N) : (uint64_t)(d.b * d.nc * d.H * d.P);
+    const uint64_t sd[2] = {scols, srows};
+    const uint64_t ss[1] = {scols * 2};
     const uint32_t sbox[2] = {64, 64};
     if (!make_tmap_bf16(&tm_x, x, 3, xin, xs, box) || !make_tmap_bf16(&tm_b, B, 3, bd, bs, box) ||
         !make_tmap_bf16(&tm_c, Cm, 3, bd, cs, box) || !make_tmap_bf16(&tm_s, Sprev, 2, sd, ss, sbox) ||
@@ -893,7 +911,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
-                         d.yred, err);
+                         d.yred, d.st_mn, err);
     }
 }
 

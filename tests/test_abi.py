@@ -246,21 +246,21 @@ def test_bwd_workspace_size_formula(lib):
     """Backward workspace: cum2 and dtT, fp32 dS, Sprev in the I/O type, the
     final state, an I/O-type copy of Gn, y without the skip term and y' (fp32),
     the reordered inputs of the three output runs (dy, x reversed; B, C
-    reversed), cum2' and dt' = 1, Sprev^T and Gn^T, and the dB run's per-head
-    output (I/O type), each rounded up to 256 bytes.  When the dC / dB runs take
-    the CUDA cores (here: forced) they also need per-head copies of B and
-    reversed C, cum2 / dt rows per run head (Q = N/64 of them per head) and the
-    dC run's per-head output; the tensor-core runs read B, C reversed and the
-    per-head rows directly, and the dC run adds into dC."""
+    reversed), cum2' and dt' = 1, and the dB run's per-head output (I/O type),
+    each rounded up to 256 bytes.  When the dC / dB runs take the CUDA cores
+    (here: forced) they also need per-head copies of B and reversed C, cum2 / dt
+    rows per run head (Q = N/64 of them per head), the dC run's per-head output
+    and Sprev^T, Gn^T; the tensor-core runs read B, C reversed, the per-head rows
+    and the states directly, and the dC run adds into dC."""
     a256 = lambda v: (v + 255) // 256 * 256
     b, T, H, P, N, G, L, E = 2, 512, 8, 64, 128, 1, 256, 2
     nc, Q = T // L, N // 64
     st = b * nc * H * P * N
     cum = a256(4 * b * H * T)
-    base = (4 * cum + a256(4 * st) + 4 * a256(E * st) + a256(4 * b * H * P * N) +
+    base = (4 * cum + a256(4 * st) + 2 * a256(E * st) + a256(4 * b * H * P * N) +
             2 * a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
             2 * a256(E * b * T * G * N) + a256(E * b * T * H * N))
-    copies = 3 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T)
+    copies = 3 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
     assert m2.bwd_workspace_size(shp()) == base
     assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + copies
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
