@@ -275,12 +275,10 @@ bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* 
                 if (c >= 0) {
                     const int64_t o = ((b * nc + c) * H + h) * PN4 + k;
                     buf[o] = gv;
-                    if constexpr (sizeof(TI) == 2) {
-                        TI* q = gio + 4 * o;
-                        q[0] = from_f32<TI>(gv.x);
-                        q[1] = from_f32<TI>(gv.y);
-                        q[2] = from_f32<TI>(gv.z);
-                        q[3] = from_f32<TI>(gv.w);
+                    if constexpr (sizeof(TI) == 2) {   // one 8-byte store of the four bf16
+                        TI q[4] = {from_f32<TI>(gv.x), from_f32<TI>(gv.y), from_f32<TI>(gv.z),
+                                   from_f32<TI>(gv.w)};
+                        *reinterpret_cast<uint2*>(gio + 4 * o) = *reinterpret_cast<const uint2*>(q);
                     }
                     gv.x = fmaf(dec[u], gv.x, v[u].x);
                     gv.y = fmaf(dec[u], gv.y, v[u].y);
@@ -410,6 +408,52 @@ bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
         }
         if (with_dc) dC[(bt + t) * (int64_t)G * N + e] = sc;
         dB[(bt + t) * (int64_t)G * N + e] = sb;
+    }
+}
+
+// dB[t] = sum_h dt_h[t] zB[h, reversed t] (the tensor-core runs: dC is added into
+// directly).  One CTA per (token, b); thread j owns 16-byte piece j % (N / V) of
+// a head's row (V elements) for heads j / (N / V), + R, + 2R, ... of each group,
+// and the R partial sums of a piece meet in shared memory.
+template <typename TI>
+__global__ void __launch_bounds__(kThreads)
+bwd_db_reduce(const TI* __restrict__ zB, const float* __restrict__ dtT, float* __restrict__ dB,
+              int T, int H, int G, int N, int L) {
+    constexpr int V = 16 / sizeof(TI);          // elements per 16-byte piece
+    __shared__ float part[kThreads * V];
+    const int t = blockIdx.x, b = blockIdx.y;
+    const int c = t / L, k = t - c * L;
+    const int Lc = min(L, T - c * L);
+    const int tr = c * L + (Lc - 1 - k);        // where the reversed run wrote token t
+    const int hpg = H / G, npc = N / V;         // pieces per head row (N is a multiple of 16)
+    const int R = kThreads / npc;               // head slots
+    const int j = threadIdx.x, pc = j % npc, slot = j / npc;
+    const int64_t bt = (int64_t)b * T;
+    const TI* zb = zB + (bt + tr) * (int64_t)H * N;
+    for (int g = 0; g < G; ++g) {
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        if (slot < R) {
+            for (int hh = slot; hh < hpg; hh += R) {
+                const int h = g * hpg + hh;
+                const float w = __ldg(dtT + ((int64_t)b * H + h) * T + t);
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(zb + (int64_t)h * N) + pc);
+                const TI* e = reinterpret_cast<const TI*>(&q);
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v] = fmaf(w, to_f32(e[v]), acc[v]);
+            }
+        }
+        __syncthreads();                        // part[] of the previous group is consumed
+#pragma unroll
+        for (int v = 0; v < V; ++v) part[j * V + v] = slot < R ? acc[v] : 0.f;
+        __syncthreads();
+        for (int n = j; n < N; n += kThreads) {  // n = V * pc' + v of slot 0 .. R-1
+            const int pn = n / V, v = n - pn * V;
+            float sum = 0.f;
+            for (int r = 0; r < R; ++r) sum += part[(r * npc + pn) * V + v];
+            dB[(bt + t) * (int64_t)G * N + (int64_t)g * N + n] = sum;
+        }
     }
 }
 
@@ -613,9 +657,13 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     }
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
-    bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
-        static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T, (int)d.H,
-        (int)d.G, (int)d.N, (int)d.L, tc2 ? 0 : 1);
+    if (tc2)
+        bwd_db_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
+            static_cast<const TI*>(w.zB), a.dtT, a.dB, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
+    else
+        bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
+            static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T,
+            (int)d.H, (int)d.G, (int)d.N, (int)d.L, 1);
     return cudaGetLastError();
 }
 
