@@ -157,13 +157,13 @@ Carve carve(const Dims& d) {
 // dt rows, and the dC / dB runs' per-head outputs (I/O type).
 struct BwdCarve {
     size_t cum2, dtT, dS, Sprev, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, xB, xCr, xr,
-        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, total;
+        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, ydot2, total;
 };
 
 // copies: the dC / dB runs take the CUDA cores and read per-head copies (xB,
 // xCr) and per-run-head rows (cum2d, dtTd, cum2rd, onesd); the tensor-core runs
 // read B, C reversed and the per-head rows directly.
-BwdCarve bwd_carve(const Dims& d, bool copies) {
+BwdCarve bwd_carve(const Dims& d, bool copies, bool dot) {
     BwdCarve c;
     const size_t E = (size_t)m2::esize(d);
     const size_t Q = d.N >= 64 ? (size_t)(d.N / 64) : 1;
@@ -183,7 +183,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies) {
     take(c.Sprev, stE);
     take(c.fin, align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)));
     take(c.GnIO, stE);
-    take(c.yno, xy32);
+    take(c.yno, dot ? 0 : xy32);   // dot mode: the y run writes only dy . y (ydot2)
     take(c.yr, xy32);
     take(c.dyr, xyE);
     take(c.Br, bcE);
@@ -201,6 +201,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies) {
     take(c.onesd, copies ? cumq : 0);
     take(c.yC, copies ? hnE : 0);   // the tensor-core dC run adds into dC directly
     take(c.zB, hnE);
+    take(c.ydot2, dot ? align256(sizeof(float) * 2 * (size_t)(d.b * d.H * d.T)) : 0);
     c.total = o;
     return c;
 }
@@ -457,7 +458,7 @@ mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x,
 size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return 0;
     const Dims d = dims_of(shape);
-    return bwd_carve(d, bwd_copies(shape, d)).total;
+    return bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d))).total;
 }
 
 mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
@@ -479,7 +480,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
         return MAMBA2_ERR_INVALID_ARG;
     if (D && !dD) return MAMBA2_ERR_INVALID_ARG;
     if (d.L > 256 || d.P > 128) return MAMBA2_ERR_UNSUPPORTED;
-    const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d));
+    const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)));
     if (!empty && (!workspace || workspace_bytes < cv.total ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MAMBA2_ERR_WORKSPACE;
@@ -519,7 +520,8 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     m2::BwdWork w{dS,           at(cv.GnIO),     at(cv.yno),      at(cv.yr),    at(cv.dyr),
                   at(cv.Br),    at(cv.Cr),       atf(cv.cum2r),   atf(cv.ones), at(cv.xB),
                   at(cv.xCr),   at(cv.xr),       at(cv.SprevT),   at(cv.GnT),   atf(cv.cum2d),
-                  atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   at(cv.yC),    at(cv.zB)};
+                  atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   at(cv.yC),    at(cv.zB),
+                  atf(cv.ydot2)};
     if (e == cudaSuccess)
         e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
                                 dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);

@@ -183,7 +183,8 @@ struct BwdArgs {
     const float* fin;   // [b,H,P,N] fp32 (the final state)
     float* Gn;          // [b,nc,H,P,N] fp32: dSout, then Gn
     void* GnIO;         // [b,nc,H,P,N] TI copy of Gn (stage 4's carried-state operand)
-    const float* yno;   // [b,T,H,P] fp32: y without the skip term
+    const float* yno;   // [b,T,H,P] fp32: y without the skip term (or null: ydot2)
+    const float* ydot2; // [b,H,T,2] fp32: partial sums of dy . y without the skip term, or null
     const float* yr;    // [b,T,H,P] fp32: y' with each chunk's tokens reversed
     float* dx;          // [b,T,H,P]
     float* ddt;         // [b,T,H]
@@ -499,7 +500,8 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const int64_t base = ((int64_t)b * a.T + t0) * sxy + (int64_t)h * P;
     const TI* __restrict__ x = static_cast<const TI*>(a.x) + base;
     const TI* __restrict__ dy = static_cast<const TI*>(a.dy) + base;
-    const float* __restrict__ yno = a.yno + base;
+    const float* __restrict__ yno = a.ydot2 ? nullptr : a.yno + base;
+    const float* __restrict__ yd = a.ydot2 ? a.ydot2 + (((int64_t)b * a.H + h) * a.T + t0) * 2 : nullptr;
     const float* __restrict__ yr = a.yr + base;
     float* __restrict__ dx = a.dx + base;
     float yx = 0.f;
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
             const float dtj = s_dt[j];
             for (int pp = lane; pp < P2; pp += 32) {
                 const float2 yp = reinterpret_cast<const float2*>(yr + jr * sxy)[pp];
-                const float2 yn = reinterpret_cast<const float2*>(yno + j * sxy)[pp];
+                const float2 yn = yno ? reinterpret_cast<const float2*>(yno + j * sxy)[pp] : make_float2(0.f, 0.f);
                 const float2 xv = load_pair(x + j * sxy, pp);
                 const float2 dv = load_pair(dy + j * sxy, pp);
                 reinterpret_cast<float2*>(dx + j * sxy)[pp] =
@@ -539,7 +541,8 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
             const int j = j0 + u * kW;
             if (lane == 0 && j < Lc) {
                 s_ddt[j] = xy[u];
-                s_dcum[j] = dyy[u] - s_dt[j] * xy[u];
+                const float dsum = yd ? yd[2 * j] + yd[2 * j + 1] : dyy[u];
+                s_dcum[j] = dsum - s_dt[j] * xy[u];
             }
         }
     }
@@ -587,7 +590,16 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         return launch_chunk_out_simt(dd, x4, B4, C4, c4, d4, S4, nullptr, yo, err, st, y32);
     };
     // y without the skip term (fp32: its dots with dy set the decay gradients).
-    cudaError_t e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno, true);
+    cudaError_t e;
+    if (a.ydot2) {   // the tensor-core y run writes only the dots dy . y the per-token kernel needs
+        Dims dd = d;
+        dd.ydot_dy = a.dy;
+        dd.ydot_out = const_cast<float*>(a.ydot2);
+        e = launch_chunk_out_tc(dd, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, nullptr, dd.ydot_out, err, st,
+                                nullptr, false, true);
+    } else {
+        e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno, true);
+    }
     if (e != cudaSuccess) return e;
     // Chunk adjoints sum_i e_i dy_i C_i^T: stage 2's tensor-core contraction in
     // its adjoint weight mode where the shape allows it.
@@ -669,6 +681,10 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
 
 }  // namespace
 
+bool bwd_dot_mode(const Dims& d, bool tc) {
+    return tc && tc_supported(d) && d.P == 64 && !(d.L == 256 && d.N == 256);   // fp32-y variant fits
+}
+
 Dims bwd_run_dims(const Dims& d) {
     const int64_t Q = d.N >= 64 ? d.N / 64 : 1;
     Dims d2 = d;   // Q*H heads of N/Q, H groups of Q, state dimension P
@@ -689,7 +705,8 @@ cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     if (d.L > 256) return cudaErrorInvalidValue;   // bwd_token's tokens: one per thread
     BwdArgs a{x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w.Gn, w.GnIO,
-              static_cast<const float*>(w.yno), static_cast<const float*>(w.yr),
+              static_cast<const float*>(w.yno), bwd_dot_mode(d, tc) ? w.ydot2 : nullptr,
+              static_cast<const float*>(w.yr),
               dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
               (int)d.L, (int)d.nc};
     return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, w, tc, dfinal, dinit, err, st)

@@ -33,6 +33,11 @@ struct Dims {
     // a [.., P' = N, N' = xmod * 64] state tensor (P', N' the state's own sizes), the
     // 64 columns from (h % xmod) * 64 (the backward's runs on transposed states).
     int st_mn = 0;
+    // Tensor-core output stage with fp32 y only (dot mode): instead of y, write
+    // ydot_out[((b * H + h) * T + t) * 2 + g] = sum over the 32 columns of group g
+    // of dy[b, t, h, p] * y[b, t, h, p] (dy bf16, contiguous [b, T, H, P]).
+    const void* ydot_dy = nullptr;
+    float* ydot_out = nullptr;
 };
 
 // Contiguous strides for the sizes in d.
@@ -141,10 +146,13 @@ struct BwdWork {
     float* onesd;   // [b,Q*H,T]
     void* yC;       // [b,T,H,N] S^T dy per head (I/O type)
     void* zB;       // [b,T,H,N] G^T x per head, reversed chunks (I/O type)
+    float* ydot2;   // [b,H,T,2] dy . y partial sums (dot mode, bwd_dot_mode)
 };
 // The dC / dB runs of the backward: Q = N/64 heads of 64 columns per head (one
 // when N < 64), H groups of Q, state dimension P.
 Dims bwd_run_dims(const Dims& d);
+// True when the backward's y run takes the tensor cores in dot mode (no fp32 y).
+bool bwd_dot_mode(const Dims& d, bool tc);
 // tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
 // dA and dD (if given) are accumulated into (zero them first); dinit may be null.
 cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,

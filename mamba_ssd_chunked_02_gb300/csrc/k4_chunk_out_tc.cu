@@ -158,7 +158,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
-                    int yred, int st_mn, int32_t* err) {
+                    int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
+                    float* __restrict__ ydot2, int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -458,6 +459,32 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             tmem_wait_ld_regs(r);
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[pb]);
+            if (kY32 && dyv) {
+                // Dot mode: sum_p dy[t, h, p] y[t, p] over this warp's 32 columns, one fp32
+                // partial per (b, h, t, column group); y itself is not written.
+                const int64_t t = (int64_t)c * L + 128 * qt + 32 * q + lane;
+                const int hh = h0 + hp;
+                if (t < T) {
+                    const uint4* dp = reinterpret_cast<const uint4*>(
+                        dyv + ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC);
+                    float part = 0.f;
+#pragma unroll
+                    for (int k4 = 0; k4 < PC / 8; ++k4) {
+                        const uint4 w = __ldg(dp + k4);
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int e = 8 * k4 + 2 * e2;
+                            part = fmaf(__uint_as_float(wv[e2] << 16),
+                                        fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e])), part);
+                            part = fmaf(__uint_as_float(wv[e2] & 0xffff0000u),
+                                        fmaf(e_prev, __uint_as_float(rs[e + 1]), __uint_as_float(r[e + 1])), part);
+                        }
+                    }
+                    ydot2[(((int64_t)b * H + hh) * T + t) * 2 + grp] = part;
+                }
+                return true;
+            }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
             if constexpr (kY32) {
                 // fp32 piece: 128-byte rows, 128-byte swizzled (16-byte chunk k
@@ -911,7 +938,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
-                         d.yred, d.st_mn, err);
+                         d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out, err);
     }
 }
 

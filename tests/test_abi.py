@@ -244,7 +244,9 @@ def test_fwd_strided_validates_strides_without_launching(lib):
 
 def test_bwd_workspace_size_formula(lib):
     """Backward workspace: cum2 and dtT, fp32 dS, Sprev in the I/O type, the
-    final state, an I/O-type copy of Gn, y without the skip term and y' (fp32),
+    final state, an I/O-type copy of Gn, y' (fp32), the dots dy . y of y without
+    the skip term (two partials per token and head; the fp32 y itself on the
+    CUDA-core path),
     the reordered inputs of the three output runs (dy, x reversed; B, C
     reversed), cum2' and dt' = 1, and the dB run's per-head output (I/O type),
     each rounded up to 256 bytes.  When the dC / dB runs take the CUDA cores
@@ -258,11 +260,13 @@ def test_bwd_workspace_size_formula(lib):
     st = b * nc * H * P * N
     cum = a256(4 * b * H * T)
     base = (4 * cum + a256(4 * st) + 2 * a256(E * st) + a256(4 * b * H * P * N) +
-            2 * a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
+            a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
             2 * a256(E * b * T * G * N) + a256(E * b * T * H * N))
+    dots = a256(4 * 2 * b * H * T)           # dy . y partials of the tensor-core y run
+    y_no_skip = a256(4 * b * T * H * P)      # the CUDA-core y run's fp32 y
     copies = 3 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
-    assert m2.bwd_workspace_size(shp()) == base
-    assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + copies
+    assert m2.bwd_workspace_size(shp()) == base + dots
+    assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + y_no_skip + copies
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
 
 
