@@ -200,7 +200,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot) {
     take(c.cum2rd, copies ? cumq : 0);
     take(c.onesd, copies ? cumq : 0);
     take(c.yC, copies ? hnE : 0);   // the tensor-core dC run adds into dC directly
-    take(c.zB, hnE);
+    take(c.zB, copies ? hnE : 0);   // the tensor-core dB run adds into dB directly
     take(c.ydot2, dot ? align256(sizeof(float) * 2 * (size_t)(d.b * d.H * d.T)) : 0);
     c.total = o;
     return c;

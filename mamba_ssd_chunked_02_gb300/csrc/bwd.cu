@@ -325,7 +325,25 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     const int64_t E = sizeof(TI);
     const int64_t bt = (int64_t)b * a.T;
     copy(a.dy, (bt + ts) * rowx, a.dyr, (bt + t) * rowx, rowx * E / 16);
-    copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
+    if (a.copies) {
+        copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
+    } else {
+        // The tensor-core dB run adds dt_h[t] * (its row) into dB: its C operand is
+        // x reversed, each head's row scaled by dt of the source token.
+        constexpr int V = 16 / sizeof(TI);
+        const int pv = a.P / V;                          // 16-byte pieces per head row
+        const uint4* s4 = reinterpret_cast<const uint4*>(static_cast<const TI*>(a.x) + (bt + ts) * rowx);
+        uint4* d4 = reinterpret_cast<uint4*>(static_cast<TI*>(a.xr) + (bt + t) * rowx);
+        for (int64_t i = threadIdx.x; i < rowx / V; i += kThreads) {
+            const int h = (int)(i / pv);
+            const float w = a.dtT[((int64_t)b * a.H + h) * a.T + ts];
+            uint4 q = s4[i];
+            TI* e = reinterpret_cast<TI*>(&q);
+#pragma unroll
+            for (int v = 0; v < V; ++v) e[v] = from_f32<TI>(w * to_f32(e[v]));
+            d4[i] = q;
+        }
+    }
     copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
     copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
     for (int h = threadIdx.x; h < a.H; h += kThreads) {
@@ -412,51 +430,6 @@ bwd_bc_reduce(const TI* __restrict__ yC, const TI* __restrict__ zB,
     }
 }
 
-// dB[t] = sum_h dt_h[t] zB[h, reversed t] (the tensor-core runs: dC is added into
-// directly).  One CTA per (token, b); thread j owns 16-byte piece j % (N / V) of
-// a head's row (V elements) for heads j / (N / V), + R, + 2R, ... of each group,
-// and the R partial sums of a piece meet in shared memory.
-template <typename TI>
-__global__ void __launch_bounds__(kThreads)
-bwd_db_reduce(const TI* __restrict__ zB, const float* __restrict__ dtT, float* __restrict__ dB,
-              int T, int H, int G, int N, int L) {
-    constexpr int V = 16 / sizeof(TI);          // elements per 16-byte piece
-    __shared__ float part[kThreads * V];
-    const int t = blockIdx.x, b = blockIdx.y;
-    const int c = t / L, k = t - c * L;
-    const int Lc = min(L, T - c * L);
-    const int tr = c * L + (Lc - 1 - k);        // where the reversed run wrote token t
-    const int hpg = H / G, npc = N / V;         // pieces per head row (N is a multiple of 16)
-    const int R = kThreads / npc;               // head slots
-    const int j = threadIdx.x, pc = j % npc, slot = j / npc;
-    const int64_t bt = (int64_t)b * T;
-    const TI* zb = zB + (bt + tr) * (int64_t)H * N;
-    for (int g = 0; g < G; ++g) {
-        float acc[V];
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        if (slot < R) {
-            for (int hh = slot; hh < hpg; hh += R) {
-                const int h = g * hpg + hh;
-                const float w = __ldg(dtT + ((int64_t)b * H + h) * T + t);
-                const uint4 q = __ldg(reinterpret_cast<const uint4*>(zb + (int64_t)h * N) + pc);
-                const TI* e = reinterpret_cast<const TI*>(&q);
-#pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] = fmaf(w, to_f32(e[v]), acc[v]);
-            }
-        }
-        __syncthreads();                        // part[] of the previous group is consumed
-#pragma unroll
-        for (int v = 0; v < V; ++v) part[j * V + v] = slot < R ? acc[v] : 0.f;
-        __syncthreads();
-        for (int n = j; n < N; n += kThreads) {  // n = V * pc' + v of slot 0 .. R-1
-            const int pn = n / V, v = n - pn * V;
-            float sum = 0.f;
-            for (int r = 0; r < R; ++r) sum += part[(r * npc + pn) * V + v];
-            dB[(bt + t) * (int64_t)G * N + (int64_t)g * N + n] = sum;
-        }
-    }
-}
 
 // Elements 2 pp and 2 pp + 1 of a row, as floats (4- or 8-byte load).
 __device__ __forceinline__ float2 load_pair(const float* __restrict__ p, int pp) {
@@ -660,8 +633,18 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         if (e == cudaSuccess)
             e = launch_chunk_out_tc(dr, a.B, a.x, a.dy, a.cum2, a.dtT, a.Sprev, nullptr, a.dC, err, st,
                                     nullptr, false, true);
+        // dB = sum over the group's heads of dt G^T x: C'' = dt x reversed (bwd_prep), and
+        // each run head adds its fp32 rows, reversed back to token order, into dB.
+        Dims db = dm;
+        db.yred = 1;
+        db.yrev = 1;
+        db.sy[1] = d.G * d.N;
+        db.sy[0] = d.T * d.G * d.N;
         if (e == cudaSuccess)
-            e = out4(dm, w.Br, w.dyr, w.xr, w.cum2r, w.ones, a.GnIO, w.zB, false);   // G^T x
+            e = cudaMemsetAsync(a.dB, 0, sizeof(float) * (size_t)(d.b * d.T * d.G * d.N), st);
+        if (e == cudaSuccess)
+            e = launch_chunk_out_tc(db, w.Br, w.dyr, w.xr, w.cum2r, w.ones, a.GnIO, nullptr, a.dB, err, st,
+                                    nullptr, false, true);
     } else {
         e = out4(d2, w.xB, a.x, a.dy, w.cum2d, w.dtTd, w.SprevT, w.yC, false);        // S^T dy
         if (e == cudaSuccess)
@@ -669,10 +652,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     }
     if (e != cudaSuccess) return e;
     bwd_token<TI><<<(unsigned)g4, kThreads, 0, st>>>(a);
-    if (tc2)
-        bwd_db_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
-            static_cast<const TI*>(w.zB), a.dtT, a.dB, (int)d.T, (int)d.H, (int)d.G, (int)d.N, (int)d.L);
-    else
+    if (!tc2)
         bwd_bc_reduce<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(
             static_cast<const TI*>(w.yC), static_cast<const TI*>(w.zB), a.dtT, a.dB, a.dC, (int)d.T,
             (int)d.H, (int)d.G, (int)d.N, (int)d.L, 1);

@@ -38,6 +38,9 @@ struct Dims {
     // of dy[b, t, h, p] * y[b, t, h, p] (dy bf16, contiguous [b, T, H, P]).
     const void* ydot_dy = nullptr;
     float* ydot_out = nullptr;
+    // With yred: the run's rows are each chunk's tokens in reverse order (row k of
+    // a chunk of Lc tokens adds into token Lc - 1 - k).
+    int yrev = 0;
 };
 
 // Contiguous strides for the sizes in d.

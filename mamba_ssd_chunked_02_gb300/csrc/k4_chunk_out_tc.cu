@@ -159,7 +159,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
                     int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
-                    float* __restrict__ ydot2, int32_t* err) {
+                    float* __restrict__ ydot2, int yrev, float* __restrict__ yacc, int ycols,
+                    int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -486,6 +487,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 return true;
             }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
+            // Reversed rows (yrev, with yred): the run's row k of the chunk is token
+            // Lc - 1 - k, so this warp's 32 rows are 32 consecutive tokens in reverse
+            // order, starting at row0; a block that would start before token 0 (only
+            // when T < L) is added element by element instead.
+            const int row0 = yrev ? c * L + Lc - 32 - (128 * qt + 32 * q) : c * L + 128 * qt + 32 * q;
+            const int rr = yrev ? 31 - lane : lane;          // staging row of this lane
             if constexpr (kY32) {
                 // fp32 piece: 128-byte rows, 128-byte swizzled (16-byte chunk k
                 // of row r at k ^ (r & 7); the buffer is 1024-byte aligned).
@@ -493,11 +500,22 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
                 for (int e = 0; e < PC; ++e)
                     yv[e] = __float_as_uint(fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e])));
+                if (yrev && row0 < 0) {
+                    const int k = 128 * qt + 32 * q + lane;
+                    if (k < Lc) {
+                        const int hy = h0 + hp;
+                        float* dst = yacc + ((int64_t)b * T + (c * L + Lc - 1 - k)) * ycols +
+                                     (hy / xdiv) * xmul + (hy % xmod) * C::P + grp * PC;
+#pragma unroll
+                        for (int e = 0; e < PC; ++e) atomicAdd(dst + e, __uint_as_float(yv[e]));
+                    }
+                    return true;
+                }
                 if (lane == 0) bulk_wait_read<YB - 1>();   // this warp's store from YB heads ago
                 __syncwarp();
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
-                    *reinterpret_cast<uint4*>(yw + lane * 128 + ((cc ^ (lane & 7)) << 4)) =
+                    *reinterpret_cast<uint4*>(yw + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
                         make_uint4(yv[4 * cc], yv[4 * cc + 1], yv[4 * cc + 2], yv[4 * cc + 3]);
             } else {
                 uint32_t yv[PC / 2];
@@ -519,8 +537,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (lane == 0) {
                 const int hy = h0 + hp;
                 if (kY32 && yred)   // add into the head's columns of the summed tensor
-                    tma_reduce_add_3d(&tm_y, yw, (hy / xdiv) * xmul + (hy % xmod) * C::P + grp * PC,
-                                      c * L + 128 * qt + 32 * q, b);
+                    tma_reduce_add_3d(&tm_y, yw, (hy / xdiv) * xmul + (hy % xmod) * C::P + grp * PC, row0, b);
                 else
                     tma_store_3d(&tm_y, yw, hy * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
                 bulk_commit();
@@ -938,7 +955,8 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
-                         d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out, err);
+                         d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out,
+                         d.yrev, static_cast<float*>(y), (int)(d.xcols ? d.xcols : d.H * d.P), err);
     }
 }
 

@@ -251,9 +251,9 @@ def test_bwd_workspace_size_formula(lib):
     reversed), cum2' and dt' = 1, and the dB run's per-head output (I/O type),
     each rounded up to 256 bytes.  When the dC / dB runs take the CUDA cores
     (here: forced) they also need per-head copies of B and reversed C, cum2 / dt
-    rows per run head (Q = N/64 of them per head), the dC run's per-head output
-    and Sprev^T, Gn^T; the tensor-core runs read B, C reversed, the per-head rows
-    and the states directly, and the dC run adds into dC."""
+    rows per run head (Q = N/64 of them per head), the dC and dB runs' per-head
+    outputs and Sprev^T, Gn^T; the tensor-core runs read B, C reversed, the
+    per-head rows and the states directly, and add into dC and dB."""
     a256 = lambda v: (v + 255) // 256 * 256
     b, T, H, P, N, G, L, E = 2, 512, 8, 64, 128, 1, 256, 2
     nc, Q = T // L, N // 64
@@ -261,10 +261,10 @@ def test_bwd_workspace_size_formula(lib):
     cum = a256(4 * b * H * T)
     base = (4 * cum + a256(4 * st) + 2 * a256(E * st) + a256(4 * b * H * P * N) +
             a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
-            2 * a256(E * b * T * G * N) + a256(E * b * T * H * N))
+            2 * a256(E * b * T * G * N))
     dots = a256(4 * 2 * b * H * T)           # dy . y partials of the tensor-core y run
     y_no_skip = a256(4 * b * T * H * P)      # the CUDA-core y run's fp32 y
-    copies = 3 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
+    copies = 4 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
     assert m2.bwd_workspace_size(shp()) == base + dots
     assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + y_no_skip + copies
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
