@@ -163,7 +163,9 @@ struct BwdCarve {
 // copies: the dC / dB runs take the CUDA cores and read per-head copies (xB,
 // xCr) and per-run-head rows (cum2d, dtTd, cum2rd, onesd); the tensor-core runs
 // read B, C reversed and the per-head rows directly.
-BwdCarve bwd_carve(const Dims& d, bool copies, bool dot) {
+// half: the tensor-core path, where dS and then the chunk adjoints are held in
+// bf16 (the forward's hand-off of R15; Gn itself only in the I/O type).
+BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half) {
     BwdCarve c;
     const size_t E = (size_t)m2::esize(d);
     const size_t Q = d.N >= 64 ? (size_t)(d.N / 64) : 1;
@@ -179,7 +181,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot) {
     auto take = [&](size_t& f, size_t n) { f = o; o += n; };
     take(c.cum2, cum);
     take(c.dtT, cum);
-    take(c.dS, st32);
+    take(c.dS, half ? stE : st32);
     take(c.Sprev, stE);
     take(c.fin, align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)));
     take(c.GnIO, stE);
@@ -458,7 +460,7 @@ mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x,
 size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return 0;
     const Dims d = dims_of(shape);
-    return bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d))).total;
+    return bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)), bwd_tc(shape, d)).total;
 }
 
 mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
@@ -480,7 +482,8 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
         return MAMBA2_ERR_INVALID_ARG;
     if (D && !dD) return MAMBA2_ERR_INVALID_ARG;
     if (d.L > 256 || d.P > 128) return MAMBA2_ERR_UNSUPPORTED;
-    const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)));
+    const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)),
+                                  bwd_tc(shape, d));
     if (!empty && (!workspace || workspace_bytes < cv.total ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MAMBA2_ERR_WORKSPACE;
@@ -511,10 +514,10 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     const bool tc = bwd_tc(shape, d);
     e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
     if (e == cudaSuccess)
-        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, false, err, s)
+        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s)   // bf16 dS
                : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
     if (e == cudaSuccess)
-        e = m2::launch_state_pass(d, dS, false, cum2, initial_state, Sprev, fin, err, s);
+        e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, fin, err, s);
     auto at = [&](size_t off) { return static_cast<void*>(ws + off); };
     auto atf = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     m2::BwdWork w{dS,           at(cv.GnIO),     at(cv.yno),      at(cv.yr),    at(cv.dyr),

@@ -193,6 +193,7 @@ struct BwdArgs {
     float* dB;          // [b,T,G,N]
     float* dC;          // [b,T,G,N]
     int T, H, P, N, G, L, nc;
+    int gn16;           // tensor-core path: adjoints in bf16 in Gn's buffer, Gn only in GnIO
 };
 
 // --- dSout[b,c,h] = sum_i e_i dy_i C_i^T  (P x N).  Grid: b*nc*H * ceil(P/64) * ceil(N/64).
@@ -251,7 +252,9 @@ template <typename TI>
 __global__ void __launch_bounds__(kThreads)
 bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* __restrict__ cum2,
                    const float4* __restrict__ dfinal, float4* __restrict__ dinit, int64_t total4,
-                   int H, int64_t PN4, int T, int L, int nc) {
+                   int H, int64_t PN4, int T, int L, int nc, const uint2* __restrict__ adj16) {
+    // adj16: the chunk adjoints in bf16 (four per 8 bytes); then only the I/O-type
+    // copy of Gn is written (buf unused).  Else adjoints and Gn in fp32 in buf.
     constexpr int kU = 4;
     for (int64_t idx = blockIdx.x * (int64_t)kThreads + threadIdx.x; idx < total4;
          idx += (int64_t)gridDim.x * kThreads) {
@@ -266,7 +269,14 @@ bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* 
             for (int u = 0; u < kU; ++u) {
                 const int c = c0 - u;
                 if (c >= 0) {
-                    v[u] = buf[((b * nc + c) * H + h) * PN4 + k];
+                    const int64_t o = ((b * nc + c) * H + h) * PN4 + k;
+                    if (adj16) {
+                        const uint2 q = adj16[o];
+                        v[u] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                                           __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+                    } else {
+                        v[u] = buf[o];
+                    }
                     dec[u] = ex2(c2[min(T, (c + 1) * L) - 1]);
                 }
             }
@@ -275,7 +285,7 @@ bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* 
                 const int c = c0 - u;
                 if (c >= 0) {
                     const int64_t o = ((b * nc + c) * H + h) * PN4 + k;
-                    buf[o] = gv;
+                    if (!adj16) buf[o] = gv;
                     if constexpr (sizeof(TI) == 2) {   // one 8-byte store of the four bf16
                         TI q[4] = {from_f32<TI>(gv.x), from_f32<TI>(gv.y), from_f32<TI>(gv.z),
                                    from_f32<TI>(gv.w)};
@@ -456,13 +466,16 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     // <Gn_c, S_after_c>: S_after is the next chunk's Sprev, or the final state.
     float gs = 0.f;
     {
-        const float* Gn = a.Gn + (((int64_t)b * a.nc + c) * a.H + h) * PN;
+        const int64_t go = (((int64_t)b * a.nc + c) * a.H + h) * PN;
+        const float* Gn = a.Gn + go;
+        const TI* G16 = static_cast<const TI*>(a.GnIO) + go;   // when only the I/O-type Gn exists
+        auto gn = [&](int64_t k) { return a.gn16 ? to_f32(G16[k]) : Gn[k]; };
         if (c + 1 < a.nc) {
             const TI* Sa = static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN;
-            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(Gn[k], to_f32(Sa[k]), gs);
+            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), to_f32(Sa[k]), gs);
         } else {
             const float* Sa = a.fin + ((int64_t)b * a.H + h) * PN;
-            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(Gn[k], Sa[k], gs);
+            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), Sa[k], gs);
         }
     }
     const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
@@ -577,7 +590,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     // Chunk adjoints sum_i e_i dy_i C_i^T: stage 2's tensor-core contraction in
     // its adjoint weight mode where the shape allows it.
     if (tc && tc_supported(d)) {
-        e = launch_chunk_state_tc(d, a.dy, a.C, a.cum2, a.dtT, a.Gn, false, err, st, nullptr,
+        e = launch_chunk_state_tc(d, a.dy, a.C, a.cum2, a.dtT, a.Gn, a.gn16 != 0, err, st, nullptr,
                                   false, true);
         if (e != cudaSuccess) return e;
     } else {
@@ -588,7 +601,8 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     bwd_state_pass_rev<TI><<<(unsigned)blocks, kThreads, 0, st>>>(
         reinterpret_cast<float4*>(a.Gn), static_cast<TI*>(a.GnIO), a.cum2,
         reinterpret_cast<const float4*>(dfinal), reinterpret_cast<float4*>(dinit), total4,
-        (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc);
+        (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc,
+        a.gn16 ? reinterpret_cast<const uint2*>(a.Gn) : nullptr);
     // The dC / dB runs: Q heads of N/Q columns per head (64 wide when N >= 64).
     const int Q = d.N >= 64 ? (int)(d.N / 64) : 1;
     const Dims d2 = bwd_run_dims(d);
@@ -688,7 +702,7 @@ cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B
               static_cast<const float*>(w.yno), bwd_dot_mode(d, tc) ? w.ydot2 : nullptr,
               static_cast<const float*>(w.yr),
               dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
-              (int)d.L, (int)d.nc};
+              (int)d.L, (int)d.nc, tc ? 1 : 0};
     return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, w, tc, dfinal, dinit, err, st)
                         : launch_t<float>(d, a, w, tc, dfinal, dinit, err, st);
 }

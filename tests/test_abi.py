@@ -243,7 +243,8 @@ def test_fwd_strided_validates_strides_without_launching(lib):
 
 
 def test_bwd_workspace_size_formula(lib):
-    """Backward workspace: cum2 and dtT, fp32 dS, Sprev in the I/O type, the
+    """Backward workspace: cum2 and dtT, dS (then the chunk adjoints; bf16 on the
+    tensor-core path, fp32 on the CUDA cores), Sprev in the I/O type, the
     final state, an I/O-type copy of Gn, y' (fp32), the dots dy . y of y without
     the skip term (two partials per token and head; the fp32 y itself on the
     CUDA-core path),
@@ -259,14 +260,15 @@ def test_bwd_workspace_size_formula(lib):
     nc, Q = T // L, N // 64
     st = b * nc * H * P * N
     cum = a256(4 * b * H * T)
-    base = (4 * cum + a256(4 * st) + 2 * a256(E * st) + a256(4 * b * H * P * N) +
+    base = (4 * cum + 3 * a256(E * st) + a256(4 * b * H * P * N) +
             a256(4 * b * T * H * P) + 2 * a256(E * b * T * H * P) +
             2 * a256(E * b * T * G * N))
     dots = a256(4 * 2 * b * H * T)           # dy . y partials of the tensor-core y run
     y_no_skip = a256(4 * b * T * H * P)      # the CUDA-core y run's fp32 y
     copies = 4 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
     assert m2.bwd_workspace_size(shp()) == base + dots
-    assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + y_no_skip + copies
+    fp32_states = a256(4 * st) - a256(E * st)   # dS / chunk adjoints in fp32 on the CUDA cores
+    assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == base + y_no_skip + copies + fp32_states
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
 
 
