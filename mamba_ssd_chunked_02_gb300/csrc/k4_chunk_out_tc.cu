@@ -255,14 +255,16 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                         c * L + 128 * qt, b);
                 } else {
                     const int h = h0 + it - NA;
-                    const int xcol = (h / xdiv) * xmul + (h % xmod) * C::P;
+                    // The backward's options (x mapping, untransposed states, reduced or dotted
+                    // output) come with fp32 y only: the forward's variant keeps none of them.
+                    const int xcol = kY32 ? (h / xdiv) * xmul + (h % xmod) * C::P : h * C::P;
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
                     for (int r = 0; r < KS / 128; ++r)
                         tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + 128 * r, b);
                     // Sprev comes from stage 3: with programmatic dependent launch
                     // everything before this point ran while it was finishing.
                     if (it == NA) grid_dep_wait();
-                    if (st_mn) {   // untransposed state: N rows of (h / xmod), 64 columns
+                    if (kY32 && st_mn) {   // untransposed state: N rows of (h / xmod), 64 columns
                         const int srow = (int)((((int64_t)b * nc + c) * (H / xmod) + h / xmod) * N);
                         for (int a = 0; a < NA; ++a)
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], (h % xmod) * 64,
@@ -324,7 +326,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 tc_fence_after();
                 const uint64_t sd = sk_desc0 + (uint64_t)st * kStageD;
                 const uint32_t acc = tmem + COL_S + 64 * ab;
-                if (st_mn) {   // B = the state tile as [K rows][64 columns], MN-major
+                if (kY32 && st_mn) {   // B = the state tile as [K rows][64 columns], MN-major
 #pragma unroll
                     for (int kk = 0; kk < N / 16; ++kk)
                         mma_ss(acc, c_desc + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
@@ -491,8 +493,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             // Lc - 1 - k, so this warp's 32 rows are 32 consecutive tokens in reverse
             // order, starting at row0; a block that would start before token 0 (only
             // when T < L) is added element by element instead.
-            const int row0 = yrev ? c * L + Lc - 32 - (128 * qt + 32 * q) : c * L + 128 * qt + 32 * q;
-            const int rr = yrev ? 31 - lane : lane;          // staging row of this lane
+            const bool rev = kY32 && yrev;
+            const int row0 = rev ? c * L + Lc - 32 - (128 * qt + 32 * q) : c * L + 128 * qt + 32 * q;
+            const int rr = rev ? 31 - lane : lane;           // staging row of this lane
             if constexpr (kY32) {
                 // fp32 piece: 128-byte rows, 128-byte swizzled (16-byte chunk k
                 // of row r at k ^ (r & 7); the buffer is 1024-byte aligned).
@@ -500,7 +503,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
                 for (int e = 0; e < PC; ++e)
                     yv[e] = __float_as_uint(fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e])));
-                if (yrev && row0 < 0) {
+                if (rev && row0 < 0) {
                     const int k = 128 * qt + 32 * q + lane;
                     if (k < Lc) {
                         const int hy = h0 + hp;
