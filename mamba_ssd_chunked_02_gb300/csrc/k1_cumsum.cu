@@ -15,8 +15,8 @@
 // read with coalesced 64-byte rows (16 heads of one token; 16-byte loads, all of
 // a thread's loads issued before any is stored), transposed into shared memory,
 // scanned by one warp per head (each lane owns L/32 consecutive tokens; lane
-// totals are combined with a shuffle scan), and written back as coalesced
-// [h][t] rows.  The shared tile keeps one padding word per 32 tokens and an odd
+// totals are combined with a shuffle scan), and each lane writes its tokens of
+// the [h][t] rows straight from registers (16-byte stores).  The shared tile keeps one padding word per 32 tokens and an odd
 // row pitch, which makes the transposing stores, the per-lane scan and the row
 // reads all free of bank conflicts.  HBM-bound: 12 bytes per (token, head).
 // On the fused path the kernel also clears the next kernel's ticket and flag
@@ -38,7 +38,6 @@ __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H,
                     int64_t sb, int64_t stt, int32_t* __restrict__ zero, int64_t nzero) {
-    constexpr int E = L / 32;                 // tokens per lane
     constexpr int kPitch = L + L / 32 + 1;    // odd
     __shared__ float tile[kHB * kPitch];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
@@ -85,32 +84,52 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     }
     __syncthreads();
 
+    // One warp per head.  L >= 128: the row is cut into L/128 segments of 128
+    // tokens, lane l owning tokens 4l .. 4l+3 of each; the segments are scanned in
+    // order (a 4-token local sum per lane, a shuffle scan of the lane totals, the
+    // running total carried to the next segment), so that each lane writes its
+    // four dtT and cum2 values of a segment with one 16-byte store each and a
+    // warp's stores cover 512 contiguous bytes.  L = 64: two tokens per lane.
+    constexpr int kSeg = L >= 128 ? L / 128 : 1, kPer = L >= 128 ? 4 : L / 32;
+    const bool vec = L >= 128 && (T & 3) == 0;   // row starts (b H + h) T + c L 16-byte aligned
     for (int j = warp; j < nh; j += kThreads / 32) {
         const int64_t row = (b * H + h0 + j) * T + t0;
-        float* trow = tile + j * kPitch;
-        // dtT row: coalesced.
-        for (int i = lane; i < nt; i += 32) dtT[row + i] = trow[tpos(i)];
-        __syncwarp();
+        const float* trow = tile + j * kPitch;
         const float a2 = __ldg(A + h0 + j) * kLog2e;
-        float s[E];
-        float run = 0.f;
+        float carry = 0.f;
 #pragma unroll
-        for (int k = 0; k < E; ++k) {
-            run += trow[tpos(lane * E + k)] * a2;   // tokens past T hold 0
-            s[k] = run;
+        for (int sg = 0; sg < kSeg; ++sg) {
+            const int i0 = sg * 128 + lane * kPer;
+            float dv[kPer], sv[kPer];
+            float run = 0.f;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                dv[k] = trow[tpos(i0 + k)];   // tokens past T hold 0
+                run += dv[k] * a2;
+                sv[k] = run;
+            }
+            float tot = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, tot, o);
+                if (lane >= o) tot += n;
+            }
+            const float excl = carry + tot - run;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) sv[k] += excl;
+            carry += __shfl_sync(0xffffffffu, tot, 31);
+            if (vec && i0 + kPer <= nt) {
+                *reinterpret_cast<float4*>(dtT + row + i0) = make_float4(dv[0], dv[1], dv[2], dv[3 % kPer]);
+                *reinterpret_cast<float4*>(cum2 + row + i0) = make_float4(sv[0], sv[1], sv[2], sv[3 % kPer]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPer; ++k)
+                    if (i0 + k < nt) {
+                        dtT[row + i0 + k] = dv[k];
+                        cum2[row + i0 + k] = sv[k];
+                    }
+            }
         }
-        float tot = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, tot, o);
-            if (lane >= o) tot += n;
-        }
-        const float excl = tot - run;
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < E; ++k) trow[tpos(lane * E + k)] = s[k] + excl;
-        __syncwarp();
-        for (int i = lane; i < nt; i += 32) cum2[row + i] = trow[tpos(i)];
     }
 }
 
