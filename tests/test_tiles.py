@@ -146,3 +146,15 @@ def test_tile_choice_of_empty_shapes(lib):
         m2.tile_choice(sh)
     m2.tile_override()
     m2.tile_choice(m2.make_shape(2, 512, 0, 64, 128, 1, 256, dtype=m2.BF16))
+
+
+def test_choices_follow_the_tensor_core_view(lib):
+    """P = 128 runs as twice the heads of P = 64, and a whole-path chunk length of
+    64 as 128-token chunks: their launch choices are those of that view."""
+    a = m2.tile_choice(m2.make_shape(4, 4096, 40, 128, 128, 1, 256, dtype=m2.BF16))
+    b = m2.tile_choice(m2.make_shape(4, 4096, 80, 64, 128, 1, 256, dtype=m2.BF16))
+    assert a == b
+    c = m2.tile_choice(m2.make_shape(2, 4096, 32, 64, 128, 2, 64, dtype=m2.BF16))
+    d = m2.tile_choice(m2.make_shape(2, 4096, 32, 64, 128, 2, 128, dtype=m2.BF16))
+    assert c == d
+    assert m2.path(m2.make_shape(2, 4096, 32, 64, 128, 2, 64, dtype=m2.BF16)) == m2.PATH_TCGEN05
