@@ -28,7 +28,8 @@ Other modes (one JSON line each, not the step above): --decode times the
 single-token decode step on the workload's state (a CUDA graph of 8 steps);
 --backward times mamba2_ssd_bwd on the workload; --all-configs prints the
 whole-path forward on every measured workload (median per-call device time,
-L2 flushed between calls where the inputs fit in it).
+L2 flushed between calls where the inputs fit in it; on tensor-core shapes the
+same call forced onto the CUDA-core kernels is timed beside it).
 
 Multi-GPU (torchrun, N > 1): each rank runs its own batch of the workload
 (independent (b, h) problems, no collective on the data path): weak scaling.
@@ -395,7 +396,9 @@ def run_all_configs(args):
         inp = W.make_inputs(w)
         dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
         sh = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups)
-        ws = torch.empty(max(1, m2.workspace_size(sh)), dtype=torch.uint8, device="cuda")
+        sh_cc = m2.shape_of(dev["x"], dev["B"], w.chunk_size, w.ngroups, m2.FLAG_FORCE_SIMT)
+        ws = torch.empty(max(1, m2.workspace_size(sh), m2.workspace_size(sh_cc)),
+                         dtype=torch.uint8, device="cuda")
         y = torch.empty_like(dev["x"])
         fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), device="cuda")
         E = 2 if w.dtype == "bf16" else 4
@@ -403,35 +406,47 @@ def run_all_configs(args):
               w.dstate) * E
         cold = io < 2 * (129 << 20)
 
-        def call():
-            m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
-                       dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups, y=y,
-                       final_state=fin, workspace=ws)
+        def timed(flags):
+            def call():
+                m2.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"],
+                           dev["initial_state"], chunk_size=w.chunk_size, ngroups=w.ngroups,
+                           y=y, final_state=fin, workspace=ws, flags=flags)
 
-        for _ in range(max(3, args.warmup)):
-            call()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(max(5, min(args.steps, 50))):
-            if cold:
-                flush.fill_(1)
-            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            call()
-            z.record(stream)
-            z.synchronize()
-            ts.append(a.elapsed_time(z))
-        if m2.device_error() != 0:
-            raise RuntimeError(f"device-side error on {w.name}")
-        ms = sorted(ts)[len(ts) // 2]
-        _, graded, flops = model(w)
+            for _ in range(max(3, args.warmup)):
+                call()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(max(5, min(args.steps, 50))):
+                if cold:
+                    flush.fill_(1)
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call()
+                z.record(stream)
+                z.synchronize()
+                ts.append(a.elapsed_time(z))
+            if m2.device_error() != 0:
+                raise RuntimeError(f"device-side error on {w.name}")
+            return sorted(ts)[len(ts) // 2], len(ts)
+
+        tc = m2.path(sh) == m2.PATH_TCGEN05
+        ms, calls = timed(0)
+        # A bf16 whole-path call with 64-token chunks on a tensor-core shape runs
+        # as 128-token chunks (same y and final state, half the chunk states):
+        # grade it against the byte model of the chunk length it runs.
+        wm = w.scaled(chunk_size=128) if tc and w.chunk_size == 64 else w
+        _, graded, flops = model(wm)
         t_path = max(graded / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
-        print(json.dumps({"workload": w.name, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
-                          "tflops": flops / (ms * 1e-3) / 1e12, "path_roofline_ms": t_path * 1e3,
-                          "path_frac": t_path / (ms * 1e-3), "peaks": src,
-                          "path": "tcgen05" if m2.path(sh) == m2.PATH_TCGEN05 else "simt",
-                          "l2": "flushed between calls" if cold else "inputs larger than L2",
-                          "calls": len(ts)}), flush=True)
+        line = {"workload": w.name, "ms": ms, "tokens_per_s": w.tokens / (ms * 1e-3),
+                "tflops": flops / (ms * 1e-3) / 1e12, "path_roofline_ms": t_path * 1e3,
+                "path_frac": t_path / (ms * 1e-3), "peaks": src,
+                "path": "tcgen05" if tc else "simt", "model_chunk_size": wm.chunk_size,
+                "l2": "flushed between calls" if cold else "inputs larger than L2",
+                "calls": calls}
+        if tc:
+            # the same call on the CUDA-core kernels, for comparison
+            line["cuda_core_ms"] = timed(m2.FLAG_FORCE_SIMT)[0]
+        print(json.dumps(line), flush=True)
         del dev, ws, y, fin
         torch.cuda.empty_cache()
 

@@ -16,9 +16,12 @@
 // a thread's loads issued before any is stored), transposed into shared memory,
 // scanned by one warp per head (each lane owns L/32 consecutive tokens; lane
 // totals are combined with a shuffle scan), and each lane writes its tokens of
-// the [h][t] rows straight from registers (16-byte stores).  The shared tile keeps one padding word per 32 tokens and an odd
-// row pitch, which makes the transposing stores, the per-lane scan and the row
-// reads all free of bank conflicts.  HBM-bound: 12 bytes per (token, head).
+// the [h][t] rows straight from registers (16-byte stores).  The shared tile
+// keeps one padding word per 32 tokens, which keeps a warp's reads of one row
+// free of bank conflicts, and a row pitch of 2 mod 8 words: a warp's
+// transposing stores cover 8 tokens of 4 heads, and heads 4 apart then sit 8
+// banks apart, so those stores are conflict-free too.  HBM-bound: 12 bytes per
+// (token, head).
 // On the fused path the kernel also clears the next kernel's ticket and flag
 // words.
 #include "common.cuh"
@@ -38,7 +41,8 @@ __global__ void __launch_bounds__(kThreads)
 chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
                     float* __restrict__ cum2, float* __restrict__ dtT, int64_t T, int64_t H,
                     int64_t sb, int64_t stt, int32_t* __restrict__ zero, int64_t nzero) {
-    constexpr int kPitch = L + L / 32 + 1;    // odd
+    constexpr int kRow = L + L / 32;
+    constexpr int kPitch = kRow + ((2 - kRow) & 7);   // 2 mod 8
     __shared__ float tile[kHB * kPitch];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
     // Stage 2, when launched as this kernel's programmatic dependent, may start

@@ -51,7 +51,7 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five measured workloads.
+# Measured workloads.
 TINY_F32 = Workload("tiny-fp32 b1 T256 H2 P16 N16 G1 L64", 1, 256, 2, 16, 16, 1, 64,
                     dtype="f32", seed=1001)
 MAMBA2_2P7B = Workload("mamba2-2.7b-layer b8 T4096 H80 P64 N128 G1 L256 bf16",
@@ -72,7 +72,16 @@ def sweep_workloads():
     return out
 
 
-ALL = [TINY_F32, MAMBA2_2P7B] + sweep_workloads() + [GROUPED_INIT, LONG_PREFILL]
+# Layer shapes for the other tensor-core views: head dimension 128 (the same
+# inner width as the 2.7B layer, 40 heads of 128) and 64-token chunks.
+HEADDIM128 = Workload("headdim128-layer b4 T4096 H40 P128 N128 G1 L256 bf16",
+                      4, 4096, 40, 128, 128, 1, 256, seed=1006)
+CHUNK64 = Workload("chunk64-layer b4 T4096 H32 P64 N128 G1 L64 bf16",
+                   4, 4096, 32, 64, 128, 1, 64, seed=1007)
+
+
+ALL = ([TINY_F32, MAMBA2_2P7B] + sweep_workloads() + [GROUPED_INIT, LONG_PREFILL]
+       + [HEADDIM128, CHUNK64])
 
 
 def make_inputs(w: Workload, device="cpu"):

@@ -438,7 +438,8 @@ def test_workspace_too_small_is_rejected():
 
 
 # --------------------------------------------------------------- full size -----------
-FULL = [W.MAMBA2_2P7B, W.GROUPED_INIT, W.LONG_PREFILL] + W.sweep_workloads()
+FULL = ([W.MAMBA2_2P7B, W.GROUPED_INIT, W.LONG_PREFILL] + W.sweep_workloads()
+        + [W.HEADDIM128, W.CHUNK64])
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name.split()[0] + "-" + "-".join(w.name.split()[1:3])
