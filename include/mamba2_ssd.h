@@ -311,7 +311,9 @@ MAMBA2_API mamba2_status mamba2_ssd_decode(const mamba2_ssd_shape* shape, float*
  * Asynchronous on `stream`; argument errors are returned before any launch
  * (MAMBA2_ERR_INVALID_ARG, MAMBA2_ERR_UNSUPPORTED, MAMBA2_ERR_WORKSPACE);
  * MAMBA2_ERR_CUDA for a failed launch.  dA and dD are accumulated with atomic
- * adds across chunks, so their last bits may vary from run to run. */
+ * adds across chunks, and on the tensor-core path dB and dC with fp32
+ * reduce-adds across blocks of heads, so their last bits may vary from run to
+ * run. */
 MAMBA2_API size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape);
 MAMBA2_API mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape,
                                         const void* x, const float* dt, const float* A,
@@ -325,7 +327,8 @@ MAMBA2_API mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape,
 
 /* Bits of the device-side error word. */
 #define MAMBA2_DEVERR_TIMEOUT_CHUNK_STATE 1   /* a wait ran out in the stage-2 kernel */
-#define MAMBA2_DEVERR_TIMEOUT_CHUNK_OUT 2     /* ... in the stage-4 kernel */
+#define MAMBA2_DEVERR_TIMEOUT_CHUNK_OUT 2     /* ... in the stage-4 kernel or the
+                                                 backward's dB / dC kernel */
 #define MAMBA2_DEVERR_LAUNCH_CONFIG 4         /* a kernel saw a launch it does not support */
 #define MAMBA2_DEVERR_CHAIN 8                 /* the fused stage 2+3 kernel gave up waiting
                                                  for the previous chunk's state */

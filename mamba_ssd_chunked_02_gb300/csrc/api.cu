@@ -165,7 +165,8 @@ struct BwdCarve {
 // read B, C reversed and the per-head rows directly.
 // half: the tensor-core path, where dS and then the chunk adjoints are held in
 // bf16 (the forward's hand-off of R15; Gn itself only in the I/O type).
-BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half) {
+// xr: the dB run reads x reversed (not when dC and dB come from bwd_bc_tc).
+BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     BwdCarve c;
     const size_t E = (size_t)m2::esize(d);
     const size_t Q = d.N >= 64 ? (size_t)(d.N / 64) : 1;
@@ -194,7 +195,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half) {
     take(c.ones, cum);
     take(c.xB, copies ? hnE : 0);
     take(c.xCr, copies ? hnE : 0);
-    take(c.xr, xyE);
+    take(c.xr, xr ? xyE : 0);
     take(c.SprevT, copies ? stE : 0);   // the tensor-core runs read them untransposed
     take(c.GnT, copies ? stE : 0);
     take(c.cum2d, copies ? cumq : 0);
@@ -215,6 +216,10 @@ mamba2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MAMBA2_OK : M
 bool bwd_tc(const mamba2_ssd_shape* s, const Dims& d) { return use_tc(s, d) && d.P == 64; }
 bool bwd_copies(const mamba2_ssd_shape* s, const Dims& d) {
     return !(bwd_tc(s, d) && m2::tc_supported(m2::bwd_run_dims(d)));
+}
+// dC and dB from their own tensor-core kernel (no reversed copy of x).
+bool bwd_bc(const mamba2_ssd_shape* s, const Dims& d) {
+    return !bwd_copies(s, d) && m2::bwd_bc_tc_supported(d);
 }
 
 // A required pointer: non-null and 16-byte aligned, unless the tensor is empty.
@@ -460,7 +465,8 @@ mamba2_status mamba2_ssd_fwd_timed(const mamba2_ssd_shape* shape, const void* x,
 size_t mamba2_ssd_bwd_workspace_size(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return 0;
     const Dims d = dims_of(shape);
-    return bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)), bwd_tc(shape, d)).total;
+    return bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)), bwd_tc(shape, d),
+                     !bwd_bc(shape, d)).total;
 }
 
 mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const float* dt,
@@ -483,7 +489,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     if (D && !dD) return MAMBA2_ERR_INVALID_ARG;
     if (d.L > 256 || d.P > 128) return MAMBA2_ERR_UNSUPPORTED;
     const BwdCarve cv = bwd_carve(d, bwd_copies(shape, d), m2::bwd_dot_mode(d, bwd_tc(shape, d)),
-                                  bwd_tc(shape, d));
+                                  bwd_tc(shape, d), !bwd_bc(shape, d));
     if (!empty && (!workspace || workspace_bytes < cv.total ||
                    (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MAMBA2_ERR_WORKSPACE;

@@ -39,7 +39,11 @@
 //   sum_h dt_j G_j^T x_j (G_j the adjoint of S_j) is the reversed run with
 //   x'' = C, B'' = dy, C'' = x and carried state Gn^T.  In both, the N columns of
 //   the output are split into Q = N/64 heads of 64 (the tensor-core shape), so a
-//   run has Q*H heads in H groups of Q, and the head sum follows.
+//   run has Q*H heads in H groups of Q, and the head sum follows.  On the
+//   tensor-core path (bf16, P = 64) dC and dB instead come from bwd_bc_tc.cu:
+//   B (or C) is shared by the group's heads, so one kernel loops over the heads
+//   and sums them in its accumulator, reading x, dy, B, C, Sprev and Gn as they
+//   are (dB anti-causal, in token order).
 //
 // Kernels, after the forward's stages 1-3 recompute cum2, dtT, Sprev and the
 // final state:
@@ -51,10 +55,13 @@
 //   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
 //                       copies of B and C, cum2' and dt' rows)
 //   bwd_transpose       Sprev^T and Gn^T
-//   (stage 4, 3 runs)   y' (fp32), the dC run and the dB run (per-head outputs in
-//                       the I/O type; tensor cores where the shape allows them)
+//   (stage 4)           y' (fp32)
+//   bwd_bc_tc (2 runs)  dC and dB, summed over the heads in the kernel (tensor
+//                       cores: bf16, P = 64, L in {128, 256}, N in {64, 128, 256})
+//   (stage 4, 2 runs)   otherwise the dC run and the dB run (per-head outputs in
+//                       the I/O type, or added into dC / dB on the tensor cores)
 //   bwd_token           per (b, c, h): dx, ddt, and dA, dD partial sums
-//   bwd_bc_reduce       dC and dB summed over each group's heads
+//   bwd_bc_reduce       dC and dB summed over each group's heads (CUDA-core runs)
 // bwd_chunk_adjoint's contraction goes through mm_tile, a 64x64 fp32 tile on
 // 256 threads (4x4 outputs each) with operands staged through shared memory.
 #include <algorithm>
@@ -316,6 +323,7 @@ struct PrepArgs {
     float *cum2r, *ones, *cum2d, *dtTd, *cum2rd, *onesd;
     int T, H, G, P, N, L, Q;
     int copies;   // write xB, xCr and the per-(Q*H)-head rows (the CUDA-core dC / dB runs)
+    int with_xr;  // write xr (not needed when dC and dB come from bwd_bc_tc)
 };
 
 template <typename TI>
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     copy(a.dy, (bt + ts) * rowx, a.dyr, (bt + t) * rowx, rowx * E / 16);
     if (a.copies) {
         copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
-    } else {
+    } else if (a.with_xr) {
         // The tensor-core dB run adds dt_h[t] * (its row) into dB: its C operand is
         // x reversed, each head's row scaled by dt of the source token.
         constexpr int V = 16 / sizeof(TI);
@@ -607,9 +615,12 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     const int Q = d.N >= 64 ? (int)(d.N / 64) : 1;
     const Dims d2 = bwd_run_dims(d);
     const bool tc2 = tc && tc_supported(d2);
+    // dC and dB straight from the inputs, summed over the heads in the kernel.
+    const bool bc = tc2 && bwd_bc_tc_supported(d);
     PrepArgs pa{a.dy, a.B, a.C, a.x, a.cum2, a.dtT, w.dyr, w.Br, w.Cr, w.xB, w.xCr, w.xr,
                 w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
-                (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1};
+                (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1,
+                bc ? 0 : 1};
     bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
     if (!tc2) {   // the tensor-core runs read Sprev and Gn untransposed
         bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
@@ -624,7 +635,15 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
     if (e != cudaSuccess) return e;
     // The per-head outputs in the I/O type: the head sum that follows is in fp32.
-    if (tc2) {
+    const size_t bcbytes = sizeof(float) * (size_t)(d.b * d.T * d.G * d.N);
+    if (bc) {
+        e = cudaMemsetAsync(a.dC, 0, bcbytes, st);
+        if (e == cudaSuccess)
+            e = launch_bwd_bc_tc(d, false, a.dy, a.x, a.B, a.Sprev, a.cum2, a.dtT, a.dC, err, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a.dB, 0, bcbytes, st);
+        if (e == cudaSuccess)
+            e = launch_bwd_bc_tc(d, true, a.x, a.dy, a.C, a.GnIO, a.cum2, a.dtT, a.dB, err, st);
+    } else if (tc2) {
         // Run head h*Q + q reads columns 64 q .. of its group's B (dC run) or of Br,
         // the group's C reversed (dB run), and cum2 / dt rows of head h.
         Dims dm = d2;

@@ -151,6 +151,15 @@ struct BwdWork {
     void* zB;       // [b,T,H,N] G^T x per head, reversed chunks (I/O type)
     float* ydot2;   // [b,H,T,2] dy . y partial sums (dot mode, bwd_dot_mode)
 };
+// The backward's dC (rev = false: Q = dy, K = x, O = B, S = Sprev) or dB (rev =
+// true: Q = x, K = dy, O = C, S = Gn) on tcgen05, summed over each group's heads
+// in the kernel and added into out (fp32 [b,T,G,N]: zero it first).  bf16, P = 64,
+// L in {128, 256}, N in {64, 128, 256} (bwd_bc_tc_supported).
+bool bwd_bc_tc_supported(const Dims& d);
+int bwd_bc_heads_per_cta(const Dims& d);
+cudaError_t launch_bwd_bc_tc(const Dims& d, bool rev, const void* q, const void* k, const void* o,
+                             const void* s, const float* cum2, const float* dtT, float* out,
+                             int32_t* err, cudaStream_t st);
 // The dC / dB runs of the backward: Q = N/64 heads of 64 columns per head (one
 // when N < 64), H groups of Q, state dimension P.
 Dims bwd_run_dims(const Dims& d);

@@ -60,14 +60,20 @@ CASES = [
     # second chunk of 44 tokens (its reversed blocks reach into chunk 0 with zeros)
     (wl(2, 100, 4, 64, 128, 2, 256, init=0.1, seed=80), True, True),
     (wl(1, 300, 4, 64, 128, 1, 256, seed=81), True, False),
+    # N = 64: dC / dB with 64 output columns per CTA (groups and a ragged last
+    # chunk at L = 128; one group at L = 256)
+    (wl(2, 600, 4, 64, 64, 2, 128, init=0.1, seed=82), True, True),
+    (wl(1, 512, 4, 64, 64, 1, 256, seed=83), False, True),
 ]
 
-# dA of the last case: 4 values, each a sum over 300 tokens of dt_j times a suffix
-# sum of signed per-token terms, which largely cancel; the 16-bit operands of the
-# tensor-core y and y' runs leave it at 2.2e-2 relative L2 (the same before the
-# runs read B, C and the states without copies).  Its max error stays within the
-# 5e-2 rms bound; relative L2 is checked at 3e-2 for it.
-TOL_OVERRIDE = {("b1 T300 H4 P64 N128 G1 L256 bf16 init0.0", "dA"): (3e-2, 5e-2)}
+# dA of the T300 case and of the T512 N64 case without D: 4 values, each a sum
+# over the tokens of dt_j times a suffix sum of signed per-token terms, which
+# largely cancel; the 16-bit operands of the tensor-core y and y' runs leave them
+# at 2.2e-2 and 2.1e-2 relative L2 (the same on the source before dC and dB
+# moved to their own kernel: dA does not depend on them).  Their max errors stay
+# within the 5e-2 rms bound; relative L2 is checked at 3e-2 for them.
+TOL_OVERRIDE = {("b1 T300 H4 P64 N128 G1 L256 bf16 init0.0", "dA"): (3e-2, 5e-2),
+                ("b1 T512 H4 P64 N64 G1 L256 bf16 init0.0", "dA"): (3e-2, 5e-2)}
 
 
 def run_bwd(w, inp, gr, flags=0):
