@@ -152,12 +152,13 @@ Carve carve(const Dims& d) {
 
 // Workspace of the backward pass: the forward's cum2, dtT, dS (fp32; reused for
 // the chunk adjoints dSout / Gn), Sprev in the I/O type, the final state, an
-// I/O-type copy of Gn, y without the skip term and y' (fp32), the reordered
-// inputs of the three output runs, Sprev^T and Gn^T, the per-run-head cum2 /
-// dt rows, and the dC / dB runs' per-head outputs (I/O type).
+// I/O-type copy of Gn, y without the skip term and y' (fp32; on the tensor-core
+// path instead three per-token dots: dy . y, x . y' and dy . x), the reordered
+// inputs of the output runs, Sprev^T and Gn^T, the per-run-head cum2 / dt rows,
+// and the dC / dB runs' per-head outputs (I/O type).
 struct BwdCarve {
     size_t cum2, dtT, dS, Sprev, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, xB, xCr, xr,
-        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, ydot2, total;
+        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, ydot2, xyd2, dyxd2, total;
 };
 
 // copies: the dC / dB runs take the CUDA cores and read per-head copies (xB,
@@ -187,7 +188,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     take(c.fin, align256(sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)));
     take(c.GnIO, stE);
     take(c.yno, dot ? 0 : xy32);   // dot mode: the y run writes only dy . y (ydot2)
-    take(c.yr, xy32);
+    take(c.yr, dot ? 0 : xy32);   // dot mode: the y' run writes dx and two dots per token
     take(c.dyr, xyE);
     take(c.Br, bcE);
     take(c.Cr, bcE);
@@ -204,7 +205,10 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     take(c.onesd, copies ? cumq : 0);
     take(c.yC, copies ? hnE : 0);   // the tensor-core dC run adds into dC directly
     take(c.zB, copies ? hnE : 0);   // the tensor-core dB run adds into dB directly
-    take(c.ydot2, dot ? align256(sizeof(float) * 2 * (size_t)(d.b * d.H * d.T)) : 0);
+    const size_t dots = dot ? align256(sizeof(float) * 2 * (size_t)(d.b * d.H * d.T)) : 0;
+    take(c.ydot2, dots);
+    take(c.xyd2, dots);
+    take(c.dyxd2, dots);
     c.total = o;
     return c;
 }
@@ -530,7 +534,7 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
                   at(cv.Br),    at(cv.Cr),       atf(cv.cum2r),   atf(cv.ones), at(cv.xB),
                   at(cv.xCr),   at(cv.xr),       at(cv.SprevT),   at(cv.GnT),   atf(cv.cum2d),
                   atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   at(cv.yC),    at(cv.zB),
-                  atf(cv.ydot2)};
+                  atf(cv.ydot2),  atf(cv.xyd2),    atf(cv.dyxd2)};
     if (e == cudaSuccess)
         e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
                                 dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);

@@ -55,12 +55,14 @@
 //   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
 //                       copies of B and C, cum2' and dt' rows)
 //   bwd_transpose       Sprev^T and Gn^T
-//   (stage 4)           y' (fp32)
+//   (stage 4)           y' (fp32), or on the tensor cores (dx mode) dx itself
+//                       and the per-token dots x . y' and dy . x
 //   bwd_bc_tc (2 runs)  dC and dB, summed over the heads in the kernel (tensor
 //                       cores: bf16, P = 64, L in {128, 256}, N in {64, 128, 256})
 //   (stage 4, 2 runs)   otherwise the dC run and the dB run (per-head outputs in
 //                       the I/O type, or added into dC / dB on the tensor cores)
-//   bwd_token           per (b, c, h): dx, ddt, and dA, dD partial sums
+//   bwd_token           per (b, c, h): dx (unless the y' run wrote it), ddt, and
+//                       dA, dD partial sums
 //   bwd_bc_reduce       dC and dB summed over each group's heads (CUDA-core runs)
 // bwd_chunk_adjoint's contraction goes through mm_tile, a 64x64 fp32 tile on
 // 256 threads (4x4 outputs each) with operands staged through shared memory.
@@ -192,7 +194,10 @@ struct BwdArgs {
     void* GnIO;         // [b,nc,H,P,N] TI copy of Gn (stage 4's carried-state operand)
     const float* yno;   // [b,T,H,P] fp32: y without the skip term (or null: ydot2)
     const float* ydot2; // [b,H,T,2] fp32: partial sums of dy . y without the skip term, or null
-    const float* yr;    // [b,T,H,P] fp32: y' with each chunk's tokens reversed
+    const float* yr;    // [b,T,H,P] fp32: y' with each chunk's tokens reversed (or null:
+                        // the y' run wrote dx and the dots below itself)
+    float* xyd;         // [b,H,T,2] fp32: partial sums of x . y' (with ydot2), or null
+    float* dyxd;        // [b,H,T,2] fp32: partial sums of dy . x (with ydot2), or null
     float* dx;          // [b,T,H,P]
     float* ddt;         // [b,T,H]
     float* dA;          // [H] (accumulated)
@@ -496,9 +501,23 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const TI* __restrict__ dy = static_cast<const TI*>(a.dy) + base;
     const float* __restrict__ yno = a.ydot2 ? nullptr : a.yno + base;
     const float* __restrict__ yd = a.ydot2 ? a.ydot2 + (((int64_t)b * a.H + h) * a.T + t0) * 2 : nullptr;
+    float yx = 0.f;
+    if (a.xyd) {
+        // The y' run wrote dx and the per-token dots x . y' and dy . x.
+        const int64_t po = (((int64_t)b * a.H + h) * a.T + t0) * 2;
+        const float2* xy2 = reinterpret_cast<const float2*>(a.xyd + po);
+        const float2* dx2 = reinterpret_cast<const float2*>(a.dyxd + po);
+        const float2* yd2 = reinterpret_cast<const float2*>(yd);
+        for (int j = tid; j < Lc; j += kThreads) {
+            const float2 v = xy2[j], w = dx2[j], u = yd2[j];
+            const float xy = v.x + v.y;
+            s_ddt[j] = xy;
+            s_dcum[j] = (u.x + u.y) - s_dt[j] * xy;
+            yx += w.x + w.y;
+        }
+    } else {
     const float* __restrict__ yr = a.yr + base;
     float* __restrict__ dx = a.dx + base;
-    float yx = 0.f;
     // Four tokens per warp per iteration (j0 + 8 u), p in pairs (8-byte loads),
     // all of an iteration's loads issued before their values are used.
     constexpr int kW = kThreads / 32, kU = 4;
@@ -539,6 +558,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
                 s_dcum[j] = dsum - s_dt[j] * xy[u];
             }
         }
+    }
     }
     gs = block_sum(gs, red);
     yx = block_sum(yx, red);   // (its barriers also publish s_ddt / s_dcum)
@@ -632,7 +652,20 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // y' = stage 4 on the reversed inputs: x' = dy, B' = C, C' = B, Gn carried.
     const void* gio = sizeof(TI) == 2 ? a.GnIO : static_cast<const void*>(a.Gn);
-    e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
+    if (a.xyd) {   // dx mode: the run writes dx and the dots x . y', dy . x instead of y'
+        Dims dd = d;
+        dd.dxm_x = a.x;
+        dd.dxm_dy = a.dy;
+        dd.dxm_dt = a.dtT;
+        dd.dxm_D = a.D;
+        dd.dxm_dx = a.dx;
+        dd.dxm_xy = a.xyd;
+        dd.dxm_dyx = a.dyxd;
+        e = launch_chunk_out_tc(dd, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, nullptr, a.dx, err, st,
+                                nullptr, false, true);
+    } else {
+        e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
+    }
     if (e != cudaSuccess) return e;
     // The per-head outputs in the I/O type: the head sum that follows is in fp32.
     const size_t bcbytes = sizeof(float) * (size_t)(d.b * d.T * d.G * d.N);
@@ -695,7 +728,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
 }  // namespace
 
 bool bwd_dot_mode(const Dims& d, bool tc) {
-    return tc && tc_supported(d) && d.P == 64 && !(d.L == 256 && d.N == 256);   // fp32-y variant fits
+    return tc && tc_supported(d) && d.P == 64 && k4_dx_fits(d);   // the fp32-y variant and dx mode fit
 }
 
 Dims bwd_run_dims(const Dims& d) {
@@ -717,10 +750,11 @@ cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B
                             int32_t* err, cudaStream_t st) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     if (d.L > 256) return cudaErrorInvalidValue;   // bwd_token's tokens: one per thread
+    const bool dot = bwd_dot_mode(d, tc);
     BwdArgs a{x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w.Gn, w.GnIO,
-              static_cast<const float*>(w.yno), bwd_dot_mode(d, tc) ? w.ydot2 : nullptr,
-              static_cast<const float*>(w.yr),
-              dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
+              static_cast<const float*>(w.yno), dot ? w.ydot2 : nullptr,
+              dot ? nullptr : static_cast<const float*>(w.yr), dot ? w.xyd2 : nullptr,
+              dot ? w.dyxd2 : nullptr, dx, ddt, dA, dD, dB, dC, (int)d.T, (int)d.H, (int)d.P, (int)d.N, (int)d.G,
               (int)d.L, (int)d.nc, tc ? 1 : 0};
     return d.dtype == 1 ? launch_t<__nv_bfloat16>(d, a, w, tc, dfinal, dinit, err, st)
                         : launch_t<float>(d, a, w, tc, dfinal, dinit, err, st);

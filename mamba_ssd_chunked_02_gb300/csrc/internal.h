@@ -41,6 +41,30 @@ struct Dims {
     // With yred: the run's rows are each chunk's tokens in reverse order (row k of
     // a chunk of Lc tokens adds into token Lc - 1 - k).
     int yrev = 0;
+    // Tensor-core output stage with fp32 y only (dx mode, the backward's y' run,
+    // whose row k of a chunk of Lc tokens is token j = Lc - 1 - k): instead of y',
+    // write dx[b, t, h, :] = dt[b, h, t] y' + D[h] dy[b, t, h, :] (fp32) and the
+    // partial dots dxm_xy[((b * H + h) * T + t) * 2 + g] = sum over the 32 columns
+    // of group g of x y', dxm_dyx[...] = the same of dy x (x, dy bf16, contiguous
+    // [b, T, H, 64]; dt [b, H, T]; D [H] or null).
+    const void* dxm_x = nullptr;
+    const void* dxm_dy = nullptr;
+    const float* dxm_dt = nullptr;
+    const float* dxm_D = nullptr;
+    float* dxm_dx = nullptr;
+    float* dxm_xy = nullptr;
+    float* dxm_dyx = nullptr;
+};
+
+// The dx-mode pointers of Dims, as one kernel argument.
+struct DxArgs {
+    const void* x;    // bf16
+    const void* dy;   // bf16
+    const float* dt;
+    const float* D;
+    float* dx;
+    float* xy;
+    float* dyx;
 };
 
 // Contiguous strides for the sizes in d.
@@ -150,6 +174,8 @@ struct BwdWork {
     void* yC;       // [b,T,H,N] S^T dy per head (I/O type)
     void* zB;       // [b,T,H,N] G^T x per head, reversed chunks (I/O type)
     float* ydot2;   // [b,H,T,2] dy . y partial sums (dot mode, bwd_dot_mode)
+    float* xyd2;    // [b,H,T,2] x . y' partial sums (the y' run in dx mode, same condition)
+    float* dyxd2;   // [b,H,T,2] dy . x partial sums (same)
 };
 // The backward's dC (rev = false: Q = dy, K = x, O = B, S = Sprev) or dB (rev =
 // true: Q = x, K = dy, O = C, S = Gn) on tcgen05, summed over each group's heads
@@ -163,8 +189,12 @@ cudaError_t launch_bwd_bc_tc(const Dims& d, bool rev, const void* q, const void*
 // The dC / dB runs of the backward: Q = N/64 heads of 64 columns per head (one
 // when N < 64), H groups of Q, state dimension P.
 Dims bwd_run_dims(const Dims& d);
-// True when the backward's y run takes the tensor cores in dot mode (no fp32 y).
+// True when the backward's y run takes the tensor cores in dot mode (no fp32 y)
+// and its y' run in dx mode (no fp32 y').
 bool bwd_dot_mode(const Dims& d, bool tc);
+// True when the fp32-output stage-4 variant for d's shape can stage dx mode's x
+// and dy tiles (two 32 KB slots in its y buffers).
+bool k4_dx_fits(const Dims& d);
 // tc: run stage 4 on the tensor cores (the shapes tc_supported() accepts).
 // dA and dD (if given) are accumulated into (zero them first); dinit may be null.
 cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B, const void* C,

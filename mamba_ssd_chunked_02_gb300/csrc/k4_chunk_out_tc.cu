@@ -142,6 +142,7 @@ struct K4Bars {
     float cbmax;
     int use16s[3];          // per stage: GEMM2 operands of that head in fp16 (1) or bf16 (0)
     float dvals[3];         // per stage: D of that head
+    uint64_t dfull[2], dfree[2];   // dx mode: the head's x and dy tiles in the y staging area
 };
 
 // Two bf16 (one word) -> f16x2, exactly when |v| is in the fp16 normal range.
@@ -154,13 +155,14 @@ template <int L, int NA, bool kY32>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
-                    const __grid_constant__ CUtensorMap tm_y, const float* __restrict__ cum2,
+                    const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_dxx,
+                    const __grid_constant__ CUtensorMap tm_ddy, const float* __restrict__ cum2,
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
                     int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
                     float* __restrict__ ydot2, int yrev, float* __restrict__ yacc, int ycols,
-                    int32_t* err) {
+                    const DxArgs dxa, int32_t* err) {
     using C = K4Cfg<L, NA, kY32>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     extern __shared__ uint8_t smem_raw[];
@@ -218,6 +220,10 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         mbar_init(&bars.conv_sync, kConvThreads);
         mbar_init(&bars.cbinfo, 1);
         mbar_init(&bars.drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.dfull[i], 1);
+            mbar_init(&bars.dfree[i], kEpiThreads);
+        }
         bars.abort = 0;
         fence_barrier_init();
     }
@@ -238,7 +244,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             prefetch_tmap(&tm_c);
             prefetch_tmap(&tm_s);
             prefetch_tmap(&tm_y);
-            int issued = 0;
+            int issued = 0, dissued = 0;   // ring items, dx-mode tile pairs
             for (int it = 0; it < n_items; ++it) {
                 const int st = it % NS, k = it / NS;
                 if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
@@ -274,12 +280,30 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         for (int a = 0; a < NA; ++a)
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
                     }
+                    if (kY32 && dxa.dx) {
+                        // dx mode: the head's x and dy rows of this tile's tokens (the run's
+                        // rows reversed: tokens Lc - 128 (qt + 1) .. Lc - 128 qt - 1 of the
+                        // chunk; a start before token 0 reads zeros) into slot hi & 1.
+                        issued = it + 1;
+                        const int hi = it - NA, sl = hi & 1;
+                        if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
+                        uint8_t* ds = sY + sl * 32768;
+                        const int row = c * L + Lc - 128 * (qt + 1);
+                        mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
+                        tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
+                        tma_load_3d(ds + 16384, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
+                        dissued = hi + 1;
+                    }
                 }
                 issued = it + 1;
             }
-            if (*abort)
+            if (*abort) {
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
+                if (kY32 && dxa.dx)   // the x / dy tiles of the last two heads issued
+                    for (int hi = dissued - 1; hi >= 0 && hi >= dissued - 2; --hi)
+                        mbar_wait(&bars.dfull[hi & 1], (hi >> 1) & 1, kWaitNs);
+            }
         }
     } else if (warp == kWarpMma) {
         // ----------------------------------------------------------- MMA issue
@@ -462,6 +486,65 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             tmem_wait_ld_regs(r);
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[pb]);
+            if (kY32 && dxa.dx) {
+                // dx mode (the backward's y' run): row k of the chunk is token
+                // j = Lc - 1 - k; write dx = dt y' + D dy there and the partial dots
+                // x . y' and dy . x over this warp's 32 columns.
+                const int k = 128 * qt + 32 * q + lane;
+                const int sl = hp & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
+                    return false;
+                // This row's token sits at row 127 - tl of the staged tiles (128-byte
+                // swizzled rows: 16-byte chunk cc of row r at cc ^ (r & 7)).
+                const int sr = 127 - (32 * q + lane);
+                const uint8_t* xs = sY + sl * 32768 + sr * 128;
+                uint4 xw4[PC / 8], dw4[PC / 8];
+#pragma unroll
+                for (int k4 = 0; k4 < PC / 8; ++k4) {
+                    const int cc = (grp * PC / 8 + k4) ^ (sr & 7);
+                    xw4[k4] = *reinterpret_cast<const uint4*>(xs + (cc << 4));
+                    dw4[k4] = *reinterpret_cast<const uint4*>(xs + 16384 + (cc << 4));
+                }
+                if (k < Lc) {
+                    const int hh = h0 + hp;
+                    const int64_t t = (int64_t)c * L + (Lc - 1 - k);
+                    const int64_t ro = ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC;
+                    const float dtj = __ldg(dxa.dt + ((int64_t)b * H + hh) * T + t);
+                    const float dh = dxa.D ? __ldg(dxa.D + hh) : 0.f;
+                    float4* op = reinterpret_cast<float4*>(dxa.dx + ro);
+                    float xy = 0.f, dyx = 0.f;
+#pragma unroll
+                    for (int k4 = 0; k4 < PC / 8; ++k4) {
+                        const uint4 xw = xw4[k4], dw = dw4[k4];
+                        const uint32_t xv[4] = {xw.x, xw.y, xw.z, xw.w};
+                        const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+                        float o[8];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int e = 8 * k4 + 2 * e2;
+                            const float y0 = fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e]));
+                            const float y1 = fmaf(e_prev, __uint_as_float(rs[e + 1]), __uint_as_float(r[e + 1]));
+                            const float x0 = __uint_as_float(xv[e2] << 16), x1 = __uint_as_float(xv[e2] & 0xffff0000u);
+                            const float d0 = __uint_as_float(dv[e2] << 16), d1 = __uint_as_float(dv[e2] & 0xffff0000u);
+                            o[2 * e2] = fmaf(dtj, y0, dh * d0);
+                            o[2 * e2 + 1] = fmaf(dtj, y1, dh * d1);
+                            xy = fmaf(x0, y0, fmaf(x1, y1, xy));
+                            dyx = fmaf(d0, x0, fmaf(d1, x1, dyx));
+                        }
+                        op[2 * k4] = make_float4(o[0], o[1], o[2], o[3]);
+                        op[2 * k4 + 1] = make_float4(o[4], o[5], o[6], o[7]);
+                    }
+                    const int64_t po = (((int64_t)b * H + hh) * T + t) * 2 + grp;
+                    dxa.xy[po] = xy;
+                    dxa.dyx[po] = dyx;
+                }
+                // Release the slot to the next head's TMA loads: this thread's reads
+                // (generic proxy) are ordered before those writes (async proxy).
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.dfree[sl]);
+                return true;
+            }
             if (kY32 && dyv) {
                 // Dot mode: sum_p dy[t, h, p] y[t, p] over this warp's 32 columns, one fp32
                 // partial per (b, h, t, column group); y itself is not written.
@@ -927,7 +1010,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     if constexpr (C::SMEM > 232448) {   // the fp32 y staging does not fit (L = 256, N = 256)
         return cudaErrorNotSupported;
     } else {
-    CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y;
+    CUtensorMap tm_x, tm_b, tm_c, tm_s, tm_y, tm_dxx, tm_ddy;
     const uint64_t xd[3] = {(uint64_t)(d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};     // y
     const uint64_t xin[3] = {(uint64_t)(d.xcols ? d.xcols : d.H * d.P), (uint64_t)d.T, (uint64_t)d.b};
     const uint64_t xs[2] = {(uint64_t)(d.sx[1] * 2), (uint64_t)(d.sx[0] * 2)};   // token, batch
@@ -950,16 +1033,27 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
                            CU_TENSOR_MAP_SWIZZLE_128B)
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
+    if (d.dxm_dx) {   // dx mode: x and dy tiles staged in the two y buffers
+        if (!kY32 || C::YB * C::Y_BYTES < 65536) return cudaErrorNotSupported;
+        const uint64_t dd[3] = {(uint64_t)(d.H * 64), (uint64_t)d.T, (uint64_t)d.b};
+        const uint64_t ds[2] = {(uint64_t)(d.H * 64 * 2), (uint64_t)(d.T * d.H * 64 * 2)};
+        if (!make_tmap_bf16(&tm_dxx, d.dxm_x, 3, dd, ds, box) || !make_tmap_bf16(&tm_ddy, d.dxm_dy, 3, dd, ds, box))
+            return cudaErrorInvalidValue;
+    } else {
+        tm_dxx = tm_x;   // unused
+        tm_ddy = tm_x;
+    }
     const Split4 sp = k4_split(d);
     const int64_t grid = sp.ctas;
     auto k = chunk_out_tc_kernel<L, NA, kY32>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
-                         tm_s, tm_y, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
+                         tm_s, tm_y, tm_dxx, tm_ddy, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
                          d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out,
-                         d.yrev, static_cast<float*>(y), (int)(d.xcols ? d.xcols : d.H * d.P), err);
+                         d.yrev, static_cast<float*>(y), (int)(d.xcols ? d.xcols : d.H * d.P),
+                         DxArgs{d.dxm_x, d.dxm_dy, d.dxm_dt, d.dxm_D, d.dxm_dx, d.dxm_xy, d.dxm_dyx}, err);
     }
 }
 
@@ -975,7 +1069,21 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
     return cudaErrorInvalidValue;
 }
 
+template <int L, int NA>
+constexpr bool dx_fits() {
+    using C = K4Cfg<L, NA, true>;
+    return C::SMEM <= 232448 && C::YB * C::Y_BYTES >= 65536;
+}
+
 }  // namespace
+
+bool k4_dx_fits(const Dims& dq) {
+    const Dims d = tc_view(dq);
+    const int64_t na = d.N / 64;
+    if (d.L == 256) return na == 1 ? dx_fits<256, 1>() : na == 2 ? dx_fits<256, 2>() : na == 4 && dx_fits<256, 4>();
+    if (d.L == 128) return na == 1 ? dx_fits<128, 1>() : na == 2 ? dx_fits<128, 2>() : na == 4 && dx_fits<128, 4>();
+    return false;
+}
 
 // A forced or tabled split: v1 and v2 divide H/G, and the v1 region takes the
 // (b, c) pairs that fill `waves` waves of the SMs (all pairs when waves is 0).
