@@ -107,7 +107,9 @@ __device__ __forceinline__ bool cb_fits_f16(float cbmax) {
     return cbmax <= 32768.f && cbmax >= 0.00390625f;
 }
 
-template <int L, int NA, bool Y32 = false>   // NA = N / 64; Y32: y stored in fp32
+// NA = N / 64; Y32: y stored in fp32; DOT: the backward's dot mode (no y stored:
+// one y buffer, holding two 16 KB slots of staged dy, so that a third ring stage fits).
+template <int L, int NA, bool Y32 = false, bool DOT = false>
 struct K4Cfg {
     static constexpr int P = 64;
     static constexpr int C_BYTES = NA * 128 * 128;         // C tile: NA K-major atoms
@@ -121,8 +123,8 @@ struct K4Cfg {
     static constexpr int budget(int ns, int yb) {
         return 1024 + C_BYTES + ns * STAGE + yb * Y_BYTES + VEC_BYTES;
     }
-    static constexpr int NS = budget(3, 2) <= 220 * 1024 ? 3 : 2;
-    static constexpr int YB = budget(NS, 2) <= 220 * 1024 ? 2 : 1;
+    static constexpr int NS = budget(3, DOT ? 1 : 2) <= 220 * 1024 ? 3 : 2;
+    static constexpr int YB = DOT ? 1 : (budget(NS, 2) <= 220 * 1024 ? 2 : 1);
     static constexpr int SMEM = budget(NS, YB);
 };
 
@@ -151,7 +153,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 
-template <int L, int NA, bool kY32>
+template <int L, int NA, bool kY32, bool kDot = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
@@ -163,8 +165,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
                     float* __restrict__ ydot2, int yrev, float* __restrict__ yacc, int ycols,
                     const DxArgs dxa, int32_t* err) {
-    using C = K4Cfg<L, NA, kY32>;
+    using C = K4Cfg<L, NA, kY32, kDot>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
+    // Staging slots of dx / dot mode in the y buffers: x at +0 and dy at +16384 of
+    // a 32 KB slot (dx), or dy alone in a 16 KB slot (dot).
+    constexpr int kSlot = kDot ? 16384 : 32768, kSlotDy = kDot ? 0 : 16384;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* sC = smem;
@@ -280,18 +285,24 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         for (int a = 0; a < NA; ++a)
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
                     }
-                    if (kY32 && dxa.dx) {
+                    if (kY32 && (dxa.dx || dyv)) {
                         // dx mode: the head's x and dy rows of this tile's tokens (the run's
                         // rows reversed: tokens Lc - 128 (qt + 1) .. Lc - 128 qt - 1 of the
-                        // chunk; a start before token 0 reads zeros) into slot hi & 1.
+                        // chunk; a start before token 0 reads zeros) into slot hi & 1.  Dot
+                        // mode: the head's dy rows of the tile (tokens in order).
                         issued = it + 1;
                         const int hi = it - NA, sl = hi & 1;
                         if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
-                        uint8_t* ds = sY + sl * 32768;
-                        const int row = c * L + Lc - 128 * (qt + 1);
-                        mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
-                        tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
-                        tma_load_3d(ds + 16384, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
+                        uint8_t* ds = sY + sl * kSlot;
+                        if (dxa.dx) {
+                            const int row = c * L + Lc - 128 * (qt + 1);
+                            mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
+                            tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
+                            tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
+                        } else {
+                            mbar_arrive_expect_tx(&bars.dfull[sl], 16384);
+                            tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, c * L + 128 * qt, b);
+                        }
                         dissued = hi + 1;
                     }
                 }
@@ -300,7 +311,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (*abort) {
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
-                if (kY32 && dxa.dx)   // the x / dy tiles of the last two heads issued
+                if (kY32 && (dxa.dx || dyv))   // the staged tiles of the last two heads issued
                     for (int hi = dissued - 1; hi >= 0 && hi >= dissued - 2; --hi)
                         mbar_wait(&bars.dfull[hi & 1], (hi >> 1) & 1, kWaitNs);
             }
@@ -471,6 +482,16 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         mbar_arrive(&bars.cb_packed);
 
         float e_prev = 0.f;
+        // dx mode: dt of this thread's token and D for the head finish() handles
+        // next, loaded one head ahead so that finish() does not wait for them.
+        float pf_dt = 0.f, pf_D = 0.f;
+        auto prefetch_dt = [&](int hp) {
+            if (!(kY32 && dxa.dx) || hp >= nh) return;
+            const int k = 128 * qt + 32 * q + lane;
+            if (k < Lc) pf_dt = __ldg(dxa.dt + ((int64_t)b * H + h0 + hp) * T + (int64_t)c * L + (Lc - 1 - k));
+            pf_D = dxa.D ? __ldg(dxa.D + h0 + hp) : 0.f;
+        };
+        prefetch_dt(0);
         // finish(hp): y rows of head hp = exp2(cum2_t) S + G (the skip term D x
         // is in G, through M's diagonal), bf16, TMA-stored per warp.
         auto finish = [&](int hp) -> bool {
@@ -498,7 +519,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 // This row's token sits at row 127 - tl of the staged tiles (128-byte
                 // swizzled rows: 16-byte chunk cc of row r at cc ^ (r & 7)).
                 const int sr = 127 - (32 * q + lane);
-                const uint8_t* xs = sY + sl * 32768 + sr * 128;
+                const uint8_t* xs = sY + sl * kSlot + sr * 128;
                 uint4 xw4[PC / 8], dw4[PC / 8];
 #pragma unroll
                 for (int k4 = 0; k4 < PC / 8; ++k4) {
@@ -510,8 +531,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const int hh = h0 + hp;
                     const int64_t t = (int64_t)c * L + (Lc - 1 - k);
                     const int64_t ro = ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC;
-                    const float dtj = __ldg(dxa.dt + ((int64_t)b * H + hh) * T + t);
-                    const float dh = dxa.D ? __ldg(dxa.D + hh) : 0.f;
+                    const float dtj = pf_dt, dh = pf_D;
                     float4* op = reinterpret_cast<float4*>(dxa.dx + ro);
                     float xy = 0.f, dyx = 0.f;
 #pragma unroll
@@ -543,6 +563,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 // (generic proxy) are ordered before those writes (async proxy).
                 fence_proxy_async_smem();
                 mbar_arrive(&bars.dfree[sl]);
+                prefetch_dt(hp + 1);
                 return true;
             }
             if (kY32 && dyv) {
@@ -550,13 +571,23 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 // partial per (b, h, t, column group); y itself is not written.
                 const int64_t t = (int64_t)c * L + 128 * qt + 32 * q + lane;
                 const int hh = h0 + hp;
+                // dy of this row from the slot the producer staged (row tl, 128-byte
+                // swizzled: 16-byte chunk cc of row r at cc ^ (r & 7)).
+                const int sl = hp & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
+                    return false;
+                const int sr = 32 * q + lane;
+                const uint8_t* dsr = sY + sl * kSlot + kSlotDy + sr * 128;
+                uint4 dw4[PC / 8];
+#pragma unroll
+                for (int k4 = 0; k4 < PC / 8; ++k4)
+                    dw4[k4] = *reinterpret_cast<const uint4*>(dsr + (((grp * PC / 8 + k4) ^ (sr & 7)) << 4));
                 if (t < T) {
-                    const uint4* dp = reinterpret_cast<const uint4*>(
-                        dyv + ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC);
                     float part = 0.f;
 #pragma unroll
                     for (int k4 = 0; k4 < PC / 8; ++k4) {
-                        const uint4 w = __ldg(dp + k4);
+                        const uint4 w = dw4[k4];
                         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                         for (int e2 = 0; e2 < 4; ++e2) {
@@ -569,6 +600,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     }
                     ydot2[(((int64_t)b * H + hh) * T + t) * 2 + grp] = part;
                 }
+                fence_proxy_async_smem();   // the slot's reads before the next TMA load into it
+                mbar_arrive(&bars.dfree[sl]);
                 return true;
             }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
@@ -909,8 +942,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     *p = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
                                     bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
                 }
-                fence_proxy_async_smem();
             }
+            // The tile's generic-proxy accesses (the range check's reads, the fp16
+            // rewrite) before the async proxy's: GEMM2 reads it, the next TMA load
+            // into this stage overwrites it.
+            fence_proxy_async_smem();
             if (ctid == 0) {
                 bars.use16s[st] = use16 ? 1 : 0;
                 bars.dvals[st] = dval;
@@ -1002,11 +1038,11 @@ Split4 pick_split4(const Dims& d, int NQ) {
     return best;
 }
 
-template <int L, int NA, bool kY32>
+template <int L, int NA, bool kY32, bool kDot = false>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
                       void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
-    using C = K4Cfg<L, NA, kY32>;
+    using C = K4Cfg<L, NA, kY32, kDot>;
     if constexpr (C::SMEM > 232448) {   // the fp32 y staging does not fit (L = 256, N = 256)
         return cudaErrorNotSupported;
     } else {
@@ -1033,11 +1069,14 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
                            CU_TENSOR_MAP_SWIZZLE_128B)
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
-    if (d.dxm_dx) {   // dx mode: x and dy tiles staged in the two y buffers
-        if (!kY32 || C::YB * C::Y_BYTES < 65536) return cudaErrorNotSupported;
+    if (d.dxm_dx || d.ydot_dy) {   // dx / dot mode: x and dy tiles staged in the two y buffers
+        if (!kY32 || (d.ydot_dy && !kDot) || C::YB * C::Y_BYTES < 2 * (kDot ? 16384 : 32768))
+            return cudaErrorNotSupported;
         const uint64_t dd[3] = {(uint64_t)(d.H * 64), (uint64_t)d.T, (uint64_t)d.b};
         const uint64_t ds[2] = {(uint64_t)(d.H * 64 * 2), (uint64_t)(d.T * d.H * 64 * 2)};
-        if (!make_tmap_bf16(&tm_dxx, d.dxm_x, 3, dd, ds, box) || !make_tmap_bf16(&tm_ddy, d.dxm_dy, 3, dd, ds, box))
+        const void* xs = d.dxm_dx ? d.dxm_x : d.ydot_dy;   // dot mode: x unused
+        const void* dys = d.dxm_dx ? d.dxm_dy : d.ydot_dy;
+        if (!make_tmap_bf16(&tm_dxx, xs, 3, dd, ds, box) || !make_tmap_bf16(&tm_ddy, dys, 3, dd, ds, box))
             return cudaErrorInvalidValue;
     } else {
         tm_dxx = tm_x;   // unused
@@ -1045,7 +1084,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     }
     const Split4 sp = k4_split(d);
     const int64_t grid = sp.ctas;
-    auto k = chunk_out_tc_kernel<L, NA, kY32>;
+    auto k = chunk_out_tc_kernel<L, NA, kY32, kDot>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
@@ -1062,9 +1101,18 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
                         const float* cum2, const float* dtT, const void* Sprev, const float* D,
                         void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
     switch (d.N) {
-        case 64: return launch_k4<L, 1, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
-        case 128: return launch_k4<L, 2, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
-        case 256: return launch_k4<L, 4, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 64:
+            if constexpr (kY32)
+                if (d.ydot_dy) return launch_k4<L, 1, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            return launch_k4<L, 1, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 128:
+            if constexpr (kY32)
+                if (d.ydot_dy) return launch_k4<L, 2, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            return launch_k4<L, 2, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+        case 256:
+            if constexpr (kY32)
+                if (d.ydot_dy) return launch_k4<L, 4, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            return launch_k4<L, 4, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
     }
     return cudaErrorInvalidValue;
 }
