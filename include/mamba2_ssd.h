@@ -111,10 +111,12 @@ typedef enum mamba2_dtype { MAMBA2_F32 = 0, MAMBA2_BF16 = 1 } mamba2_dtype;
  *   ngroups G >= 1 with nheads % G == 0; chunk_size L in {64, 128, 256};
  *   seqlen need not be a multiple of L (the last chunk is shorter).
  * The tensor-core path is used for dtype BF16 with L in {128, 256},
- * P in {64, 128} and N in {64, 128, 256} (P = 128 runs as twice the heads
- * of 64: the tensors hold the same bytes in either view); every other
- * supported shape runs on the CUDA-core kernels (mamba2_ssd_path reports
- * which).  mamba2_ssd_bwd keeps P = 128 on the CUDA-core kernels.
+ * P in {32, 64, 128} and N in {64, 128, 256} (P = 128 runs as twice the heads
+ * of 64: the tensors hold the same bytes in either view; P = 32 runs on
+ * 64-column tiles that also hold the next head's columns, of which only the
+ * head's own outputs are kept); every other supported shape runs on the
+ * CUDA-core kernels (mamba2_ssd_path reports which).  mamba2_ssd_bwd keeps
+ * P in {32, 128} on the CUDA-core kernels.
  * The whole-path calls (mamba2_ssd_fwd, _fwd_strided, _fwd_timed,
  * _fwd_noalloc) run chunk_size 64 as 128-token chunks on shapes the tensor
  * cores take at 128: y and final_state do not depend on the chunk length.
@@ -244,8 +246,9 @@ MAMBA2_API mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape,
  *   256-byte aligned, owned by the caller: a two-slot fp32 ring of states per
  *   (b, h) and the synchronisation words, which the call clears on `stream`
  *   first.  Calls sharing one workspace must not overlap on the GPU.
- * Shapes without the tensor-core path (mamba2_ssd_path) return
- * MAMBA2_ERR_UNSUPPORTED; they run mamba2_ssd_chunk_state + _state_pass. */
+ * Shapes without the tensor-core path (mamba2_ssd_path), and P = 32, return
+ * MAMBA2_ERR_UNSUPPORTED (workspace size 0); they run mamba2_ssd_chunk_state +
+ * _state_pass. */
 MAMBA2_API size_t mamba2_ssd_chunk_state_pass_workspace_size(const mamba2_ssd_shape* shape);
 MAMBA2_API mamba2_status mamba2_ssd_chunk_state_pass(const mamba2_ssd_shape* shape,
                                           const void* x, const void* B,

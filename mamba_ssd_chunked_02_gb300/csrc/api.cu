@@ -298,7 +298,7 @@ mamba2_status mamba2_ssd_state_pass(const mamba2_ssd_shape* shape, const void* d
 size_t mamba2_ssd_chunk_state_pass_workspace_size(const mamba2_ssd_shape* shape) {
     if (check(shape) != MAMBA2_OK) return 0;
     const Dims d = dims_of(shape);
-    if (!use_tc(shape, d)) return 0;
+    if (!use_tc(shape, d) || !m2::tc_fused_supported(d)) return 0;
     return align256(2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N)) +
            align256(sizeof(int32_t) * (size_t)(m2::fused_flag_words(d) + 1));
 }
@@ -311,7 +311,7 @@ mamba2_status mamba2_ssd_chunk_state_pass(const mamba2_ssd_shape* shape, const v
     mamba2_status st = check(shape);
     if (st != MAMBA2_OK) return st;
     const Dims d = dims_of(shape);
-    if (!use_tc(shape, d)) return MAMBA2_ERR_UNSUPPORTED;
+    if (!use_tc(shape, d) || !m2::tc_fused_supported(d)) return MAMBA2_ERR_UNSUPPORTED;
     const bool empty = d.b * d.T * d.H == 0;
     if (!req(x, empty) || !req(B, empty) || !req(cum2, empty) || !req(dtT, empty) ||
         !opt(initial_state) || !req(Sprev, empty) || !req(final_state, d.b * d.H == 0))
@@ -393,7 +393,7 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
     // and the ticket live in the dS region, which holds them from three chunks on.
     const size_t ring = 2 * sizeof(float) * (size_t)(d.b * d.H * d.P * d.N);
     const size_t nflag = tc ? (size_t)m2::fused_flag_words(d) : 0;
-    const bool fuse = tc && d.nc >= 3 && (shape->flags & MAMBA2_FLAG_FUSED_STATE) &&
+    const bool fuse = tc && m2::tc_fused_supported(d) && d.nc >= 3 && (shape->flags & MAMBA2_FLAG_FUSED_STATE) &&
                       ring + sizeof(int32_t) * (nflag + 1) <= cv.Sprev - cv.dS;
     int32_t* flags = reinterpret_cast<int32_t*>(ws + cv.dS + ring);
     // Programmatic dependent launch of stages 2-4 (not across recorded events).

@@ -207,8 +207,11 @@ cudaError_t launch_backward(const Dims& d, bool tc, const void* x, const void* B
 // Diagnostic: waits that nothing releases, bounded by limit_ns; sets kErrSelfTest.
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, int32_t* err, cudaStream_t st);
 
-// True when the tcgen05 kernels handle this shape.
+// True when the tcgen05 kernels handle this shape.  P = 32 runs on 64-column
+// tiles that also hold the next head's columns (only the head's own outputs are
+// kept): stages 2 and 4, not the fused stages 2+3.
 bool tc_supported(const Dims& d);
+bool tc_fused_supported(const Dims& d);
 
 // The shape the tcgen05 kernels run: P = 128 as twice the heads of P = 64.  x, y
 // ([.., H, P] per token), Sprev and dS ([.., H, P, N]) hold the same bytes in

@@ -151,7 +151,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                       const __grid_constant__ CUtensorMap tm_fin,    // fused: [b H P][N] f32
                       const __grid_constant__ CUtensorMap tm_sp,     // fused: [b nc H P][N] bf16
                       const float* __restrict__ cum2, const float* __restrict__ dtT,
-                      int T, int H, int N, int G, int nc, int n_tiles, int pts,
+                      int T, int H, int N, int G, int nc, int n_tiles, int pts, int pst,
                       int hpc, int n_hblk, int upc, int64_t units, int32_t* err,
                       const FuseArgs fa, uint32_t* __restrict__ xabs) {
     using C = K2Cfg<L, kFuse, kDS16>;
@@ -248,7 +248,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 if (kFuse)
                     tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], (h0 + i) * C::P, c * L, b);
                 else
-                    tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], it.h * C::P, it.c * L, it.b);
+                    tma_load_3d(sX + st * C::X_BYTES, &tm_x, &bars.full[st], it.h * pst, it.c * L, it.b);
                 issued = i + 1;
                 if (!kFuse) it.next(H, n_tiles, nc);
             }
@@ -590,7 +590,7 @@ chunk_state_tc_kernel(const __grid_constant__ CUtensorMap tm_x,
                 fence_proxy_async_smem();
                 if (!group_sync()) break;
                 if (ep == 0) {
-                    const int row = (int)((((int64_t)it.b * nc + it.c) * H + it.h) * C::P);
+                    const int row = (int)((((int64_t)it.b * nc + it.c) * H + it.h) * pst);
                     tma_store_2d(&tm_d, tile, it.nt * 128, row);
                     bulk_commit();
                 }
@@ -686,7 +686,9 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     if (!kFuse) {
         const uint64_t dd[2] = {(uint64_t)d.N, (uint64_t)(d.b * d.nc * d.H * d.P)};
         const uint64_t ds[1] = {(uint64_t)(d.N * (ds16 ? 2 : 4))};
-        const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), 64};
+        // P = 32: the 64-column x tile also holds the next head's columns; only
+        // the head's own 32 rows of the dS tile are stored.
+        const uint32_t dbox[2] = {(uint32_t)(d.N < 128 ? d.N : 128), (uint32_t)(d.P < 64 ? d.P : 64)};
         if (!make_tmap(&tm_d, ds16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                        dS, 2, dd, ds, dbox,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -714,7 +716,8 @@ cudaError_t launch_k2(const Dims& d, const void* x, const void* B, const float* 
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(C::kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_d,
                          tm_ring, tm_init, tm_fin, tm_sp, cum2, dtT, (int)d.T, (int)d.H, (int)d.N,
-                         (int)d.G, (int)d.nc, n_tiles, d.pts, hpc, n_hblk, upc, units, err, fa, xabs);
+                         (int)d.G, (int)d.nc, n_tiles, d.pts, (int)d.P, hpc, n_hblk, upc, units, err, fa,
+                         xabs);
 }
 
 }  // namespace
@@ -750,11 +753,14 @@ int k2_units_per_cta(const Dims& d, int* src) {
 }
 
 bool tc_supported(const Dims& d) {
-    return d.dtype == 1 && (d.L == 128 || d.L == 256) && (d.P == 64 || d.P == 128) &&
+    return d.dtype == 1 && (d.L == 128 || d.L == 256) && (d.P == 32 || d.P == 64 || d.P == 128) &&
            (d.N == 64 || d.N == 128 || d.N == 256) && d.T < (int64_t(1) << 31) &&
            d.b * d.nc * d.H * d.P < (int64_t(1) << 31) &&      // TMA row coordinate of Sprev
            d.H * d.P < (int64_t(1) << 31) && d.G * d.N < (int64_t(1) << 31);
 }
+
+// The fused stages 2+3 keep a head's 64 columns to itself: P >= 64.
+bool tc_fused_supported(const Dims& d) { return tc_supported(d) && d.P >= 64; }
 
 cudaError_t launch_chunk_state_tc(const Dims& dq, const void* x, const void* B, const float* cum2,
                                   const float* dtT, void* dS, bool ds16, int32_t* err,
@@ -786,7 +792,7 @@ cudaError_t launch_chunk_state_pass_tc(const Dims& dq, const void* x, const void
                                        cudaStream_t st) {
     const Dims d = tc_view(dq);
     if (d.b == 0 || d.H == 0 || d.nc == 0) return cudaSuccess;
-    if (!tc_supported(d) || d.b > (1 << 20)) return cudaErrorInvalidValue;
+    if (!tc_fused_supported(d) || d.b > (1 << 20)) return cudaErrorInvalidValue;
     FuseArgs fa;
     fa.init = init;
     fa.carry = carry;

@@ -161,7 +161,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const __grid_constant__ CUtensorMap tm_ddy, const float* __restrict__ cum2,
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
-                    int G, int nc, int v1, int n1, int v2, int pts, int xdiv, int xmul, int xmod,
+                    int G, int nc, int v1, int n1, int v2, int pts, int pst, int xdiv, int xmul, int xmod,
                     int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
                     float* __restrict__ ydot2, int yrev, float* __restrict__ yacc, int ycols,
                     const DxArgs dxa, int32_t* err) {
@@ -268,7 +268,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const int h = h0 + it - NA;
                     // The backward's options (x mapping, untransposed states, reduced or dotted
                     // output) come with fp32 y only: the forward's variant keeps none of them.
-                    const int xcol = kY32 ? (h / xdiv) * xmul + (h % xmod) * C::P : h * C::P;
+                    // pst: columns per head (32: the tile also holds the next head's columns)
+                    const int xcol = kY32 ? (h / xdiv) * xmul + (h % xmod) * C::P : h * pst;
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
                     for (int r = 0; r < KS / 128; ++r)
                         tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + 128 * r, b);
@@ -281,7 +282,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], (h % xmod) * 64,
                                         srow + 64 * a);
                     } else {
-                        const int srow = (int)((((int64_t)b * nc + c) * H + h) * C::P);
+                        const int srow = (int)((((int64_t)b * nc + c) * H + h) * pst);
                         for (int a = 0; a < NA; ++a)
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
                     }
@@ -657,8 +658,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 const int hy = h0 + hp;
                 if (kY32 && yred)   // add into the head's columns of the summed tensor
                     tma_reduce_add_3d(&tm_y, yw, (hy / xdiv) * xmul + (hy % xmod) * C::P + grp * PC, row0, b);
-                else
-                    tma_store_3d(&tm_y, yw, hy * C::P + grp * PC, c * L + 128 * qt + 32 * q, b);
+                else if (grp * PC < pst)   // P = 32: the second group's columns are the next head's
+                    tma_store_3d(&tm_y, yw, hy * pst + grp * PC, c * L + 128 * qt + 32 * q, b);
                 bulk_commit();
             }
             return true;
@@ -1089,7 +1090,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, tm_dxx, tm_ddy, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
-                         sp.v1, (int)sp.n1, sp.v2, d.pts, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
+                         sp.v1, (int)sp.n1, sp.v2, d.pts, (int)d.P, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
                          d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out,
                          d.yrev, static_cast<float*>(y), (int)(d.xcols ? d.xcols : d.H * d.P),
                          DxArgs{d.dxm_x, d.dxm_dy, d.dxm_dt, d.dxm_D, d.dxm_dx, d.dxm_xy, d.dxm_dyx}, err);

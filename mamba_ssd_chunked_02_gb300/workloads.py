@@ -73,15 +73,19 @@ def sweep_workloads():
 
 
 # Layer shapes for the other tensor-core views: head dimension 128 (the same
-# inner width as the 2.7B layer, 40 heads of 128) and 64-token chunks.
+# inner width as the 2.7B layer, 40 heads of 128), 64-token chunks and head
+# dimension 32.
 HEADDIM128 = Workload("headdim128-layer b4 T4096 H40 P128 N128 G1 L256 bf16",
                       4, 4096, 40, 128, 128, 1, 256, seed=1006)
 CHUNK64 = Workload("chunk64-layer b4 T4096 H32 P64 N128 G1 L64 bf16",
                    4, 4096, 32, 64, 128, 1, 64, seed=1007)
+# Head dimension 32 (64 heads of 32: half the inner width of the 2.7B layer).
+HEADDIM32 = Workload("headdim32-layer b4 T4096 H64 P32 N128 G1 L256 bf16",
+                     4, 4096, 64, 32, 128, 1, 256, seed=1008)
 
 
 ALL = ([TINY_F32, MAMBA2_2P7B] + sweep_workloads() + [GROUPED_INIT, LONG_PREFILL]
-       + [HEADDIM128, CHUNK64])
+       + [HEADDIM128, CHUNK64, HEADDIM32])
 
 
 def make_inputs(w: Workload, device="cpu"):

@@ -106,7 +106,8 @@ def test_path_selection(lib):
     assert m2.path(shp(dtype=m2.F32)) == m2.PATH_SIMT
     assert m2.path(shp(chunk_size=64)) == m2.PATH_TCGEN05     # the whole path: 128-token chunks
     assert m2.path(shp(chunk_size=64, dtype=m2.F32)) == m2.PATH_SIMT
-    assert m2.path(shp(headdim=32)) == m2.PATH_SIMT
+    assert m2.path(shp(headdim=32)) == m2.PATH_TCGEN05        # 64-column tiles, 32 kept
+    assert m2.path(shp(headdim=16)) == m2.PATH_SIMT
     assert m2.path(shp(flags=m2.FLAG_FORCE_SIMT)) == m2.PATH_SIMT
 
 

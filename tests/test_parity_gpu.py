@@ -44,6 +44,12 @@ SMALL = [
     wl(1, 300, 4, 128, 64, 2, 128, init=0.1, seed=17),                  # P = 128, ragged
     wl(2, 600, 4, 128, 128, 2, 256, init=0.1, seed=22),                 # P = 128, L = 256, groups
     wl(2, 500, 4, 64, 128, 2, 64, init=0.1, seed=23),                   # L = 64 (whole path: 128)
+    # P = 32 on 64-column tiles that also hold the next head's columns: groups
+    # (the next head in another group), a ragged tail and the last head (its
+    # neighbour columns past the tensor); L = 128 with N = 64; L = 64 (whole path)
+    wl(2, 600, 6, 32, 128, 2, 256, init=0.1, seed=24),
+    wl(1, 384, 4, 32, 64, 1, 128, seed=25),
+    wl(1, 500, 2, 32, 128, 1, 64, init=0.1, seed=26),
     wl(1, 200, 4, 32, 32, 2, 64, seed=18),                              # small P/N, bf16 SIMT
     wl(2, 192, 3, 16, 16, 3, 64, dtype="f32", init=0.1, seed=19),       # fp32, G = H
     wl(1, 100, 2, 64, 128, 1, 256, seed=20),                            # T < L
@@ -66,7 +72,7 @@ def test_fwd_matches_oracle(w):
     assert_close(to_np(f), fr, w.dtype, f"final_state {w.name}")
 
 
-TC_SMALL = SMALL[1:10]  # bf16 shapes on the tensor-core path (P = 128 as 2H heads of 64)
+TC_SMALL = SMALL[1:13]  # bf16 shapes on the tensor-core path (P = 128 as 2H heads of 64)
 
 
 @pytest.mark.parametrize("w", TC_SMALL, ids=_ids(TC_SMALL))
@@ -439,7 +445,7 @@ def test_workspace_too_small_is_rejected():
 
 # --------------------------------------------------------------- full size -----------
 FULL = ([W.MAMBA2_2P7B, W.GROUPED_INIT, W.LONG_PREFILL] + W.sweep_workloads()
-        + [W.HEADDIM128, W.CHUNK64])
+        + [W.HEADDIM128, W.CHUNK64, W.HEADDIM32])
 
 
 @pytest.mark.parametrize("w", FULL, ids=[w.name.split()[0] + "-" + "-".join(w.name.split()[1:3])

@@ -128,7 +128,7 @@ def test_override_validation(lib):
 def test_tile_choice_off_the_tensor_core_path(lib):
     for sh in (m2.make_shape(2, 512, 8, 64, 128, 1, 256, dtype=m2.F32),
                m2.make_shape(2, 512, 8, 64, 128, 1, 256, dtype=m2.BF16, flags=m2.FLAG_FORCE_SIMT),
-               m2.make_shape(2, 512, 8, 32, 128, 1, 256, dtype=m2.BF16)):
+               m2.make_shape(2, 512, 8, 16, 128, 1, 256, dtype=m2.BF16)):
         with pytest.raises(m2.Mamba2Error) as e:
             m2.tile_choice(sh)
         assert e.value.status == m2.ERR_UNSUPPORTED
