@@ -158,7 +158,7 @@ Carve carve(const Dims& d) {
 // and the dC / dB runs' per-head outputs (I/O type).
 struct BwdCarve {
     size_t cum2, dtT, dS, Sprev, fin, GnIO, yno, yr, dyr, Br, Cr, cum2r, ones, xB, xCr, xr,
-        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, ydot2, xyd2, dyxd2, total;
+        SprevT, GnT, cum2d, dtTd, cum2rd, onesd, yC, zB, ydot2, xyd2, dyxd2, xabs_x, xabs_dy, total;
 };
 
 // copies: the dC / dB runs take the CUDA cores and read per-head copies (xB,
@@ -209,6 +209,11 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     take(c.ydot2, dots);
     take(c.xyd2, dots);
     take(c.dyxd2, dots);
+    // max |x| and max |dy| per (b, chunk, head) from the stage-2 runs, for the y and
+    // y' runs' fp16 range check (the forward's hand-off of the same bound)
+    const size_t xab = half ? align256(8 * sizeof(uint32_t) * (size_t)(d.b * d.nc * d.H)) : 0;
+    take(c.xabs_x, xab);
+    take(c.xabs_dy, xab);
     c.total = o;
     return c;
 }
@@ -524,7 +529,8 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
     const bool tc = bwd_tc(shape, d);
     e = m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
     if (e == cudaSuccess)
-        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s)   // bf16 dS
+        e = tc ? m2::launch_chunk_state_tc(d, x, B, cum2, dtT, dS, true, err, s,   // bf16 dS
+                                           reinterpret_cast<uint32_t*>(ws + cv.xabs_x))
                : m2::launch_chunk_state_simt(d, x, B, cum2, dtT, dS, err, s);
     if (e == cudaSuccess)
         e = m2::launch_state_pass(d, dS, tc, cum2, initial_state, Sprev, fin, err, s);
@@ -534,7 +540,9 @@ mamba2_status mamba2_ssd_bwd(const mamba2_ssd_shape* shape, const void* x, const
                   at(cv.Br),    at(cv.Cr),       atf(cv.cum2r),   atf(cv.ones), at(cv.xB),
                   at(cv.xCr),   at(cv.xr),       at(cv.SprevT),   at(cv.GnT),   atf(cv.cum2d),
                   atf(cv.dtTd), atf(cv.cum2rd),  atf(cv.onesd),   at(cv.yC),    at(cv.zB),
-                  atf(cv.ydot2),  atf(cv.xyd2),    atf(cv.dyxd2)};
+                  atf(cv.ydot2),  atf(cv.xyd2),    atf(cv.dyxd2),
+                  tc ? reinterpret_cast<uint32_t*>(ws + cv.xabs_x) : nullptr,
+                  tc ? reinterpret_cast<uint32_t*>(ws + cv.xabs_dy) : nullptr};
     if (e == cudaSuccess)
         e = m2::launch_backward(d, tc, x, B, C, dy, A, D, cum2, dtT, Sprev, fin, w, dfinal_state,
                                 dx, ddt, dA, dB, dC, dD, dinitial_state, err, s);

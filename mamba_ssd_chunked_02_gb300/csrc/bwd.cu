@@ -610,7 +610,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dd.ydot_dy = a.dy;
         dd.ydot_out = const_cast<float*>(a.ydot2);
         e = launch_chunk_out_tc(dd, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, nullptr, dd.ydot_out, err, st,
-                                nullptr, false, true);
+                                w.xabs_x, false, true);
     } else {
         e = out4(d, a.x, a.B, a.C, a.cum2, a.dtT, a.Sprev, a.yno, true);
     }
@@ -618,7 +618,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     // Chunk adjoints sum_i e_i dy_i C_i^T: stage 2's tensor-core contraction in
     // its adjoint weight mode where the shape allows it.
     if (tc && tc_supported(d)) {
-        e = launch_chunk_state_tc(d, a.dy, a.C, a.cum2, a.dtT, a.Gn, a.gn16 != 0, err, st, nullptr,
+        e = launch_chunk_state_tc(d, a.dy, a.C, a.cum2, a.dtT, a.Gn, a.gn16 != 0, err, st, w.xabs_dy,
                                   false, true);
         if (e != cudaSuccess) return e;
     } else {
@@ -661,8 +661,9 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dd.dxm_dx = a.dx;
         dd.dxm_xy = a.xyd;
         dd.dxm_dyx = a.dyxd;
+        // dy reversed within each chunk: the adjoint run's max |dy| per chunk holds
         e = launch_chunk_out_tc(dd, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, nullptr, a.dx, err, st,
-                                nullptr, false, true);
+                                w.xabs_dy, false, true);
     } else {
         e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);
     }

@@ -176,6 +176,8 @@ struct BwdWork {
     float* ydot2;   // [b,H,T,2] dy . y partial sums (dot mode, bwd_dot_mode)
     float* xyd2;    // [b,H,T,2] x . y' partial sums (the y' run in dx mode, same condition)
     float* dyxd2;   // [b,H,T,2] dy . x partial sums (same)
+    uint32_t* xabs_x;    // [b,nc,H][8] max |x| per chunk from stage 2 (tensor-core path), or null
+    uint32_t* xabs_dy;   // [b,nc,H][8] max |dy| per chunk from the adjoint stage-2 run, or null
 };
 // The backward's dC (rev = false: Q = dy, K = x, O = B, S = Sprev) or dB (rev =
 // true: Q = x, K = dy, O = C, S = Gn) on tcgen05, summed over each group's heads

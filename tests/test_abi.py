@@ -250,7 +250,8 @@ def test_bwd_workspace_size_formula(lib):
     reversed; B, C reversed), cum2' and dt' = 1, each rounded up to 256 bytes.
     On the tensor-core path the y and y' runs leave three per-token dots (two
     partials per token and head each: dy . y, x . y', dy . x; the y' run writes
-    dx itself), and dC and dB come from their own kernel, which reads x, dy, B,
+    dx itself), stage 2 hands them max |x| and max |dy| per (b, chunk, head) for
+    their fp16 range check, and dC and dB come from their own kernel, which reads x, dy, B,
     C and the states directly.  On the CUDA cores (here: forced) the runs
     instead need fp32 y and y', x reversed, per-head copies of B and reversed C,
     cum2 / dt rows per run head (Q = N/64 of them per head), the dC and dB runs'
@@ -267,7 +268,8 @@ def test_bwd_workspace_size_formula(lib):
     y_rev = a256(4 * b * T * H * P)          # the CUDA-core y' run's fp32 y'
     xr = a256(E * b * T * H * P)             # x reversed, read by the dB run
     copies = 4 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
-    assert m2.bwd_workspace_size(shp()) == base + 3 * dots
+    xabs = a256(32 * b * nc * H)             # max |x|, max |dy| per (b, chunk, head) from stage 2
+    assert m2.bwd_workspace_size(shp()) == base + 3 * dots + 2 * xabs
     fp32_states = a256(4 * st) - a256(E * st)   # dS / chunk adjoints in fp32 on the CUDA cores
     assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == \
         base + y_rev + xr + y_no_skip + copies + fp32_states
