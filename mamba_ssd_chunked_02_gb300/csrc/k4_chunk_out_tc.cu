@@ -249,7 +249,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             prefetch_tmap(&tm_c);
             prefetch_tmap(&tm_s);
             prefetch_tmap(&tm_y);
-            int issued = 0, dissued = 0;   // ring items, dx-mode tile pairs
+            int issued = 0;
             for (int it = 0; it < n_items; ++it) {
                 const int st = it % NS, k = it / NS;
                 if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
@@ -286,36 +286,39 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         for (int a = 0; a < NA; ++a)
                             tma_load_2d(sx + C::X_BYTES + a * 8192, &tm_s, &bars.full[st], 64 * a, srow);
                     }
-                    if (kY32 && (dxa.dx || dyv)) {
-                        // dx mode: the head's x and dy rows of this tile's tokens (the run's
-                        // rows reversed: tokens Lc - 128 (qt + 1) .. Lc - 128 qt - 1 of the
-                        // chunk; a start before token 0 reads zeros) into slot hi & 1.  Dot
-                        // mode: the head's dy rows of the tile (tokens in order).
-                        issued = it + 1;
-                        const int hi = it - NA, sl = hi & 1;
-                        if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
-                        uint8_t* ds = sY + sl * kSlot;
-                        if (dxa.dx) {
-                            const int row = c * L + Lc - 128 * (qt + 1);
-                            mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
-                            tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
-                            tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
-                        } else {
-                            mbar_arrive_expect_tx(&bars.dfull[sl], 16384);
-                            tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, c * L + 128 * qt, b);
-                        }
-                        dissued = hi + 1;
-                    }
                 }
                 issued = it + 1;
             }
-            if (*abort) {
+            if (*abort)
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
-                if (kY32 && (dxa.dx || dyv))   // the staged tiles of the last two heads issued
-                    for (int hi = dissued - 1; hi >= 0 && hi >= dissued - 2; --hi)
-                        mbar_wait(&bars.dfull[hi & 1], (hi >> 1) & 1, kWaitNs);
+        } else if (lane == 1 && kY32 && (dxa.dx || dyv)) {
+            // dx / dot mode: the staged tiles, from a thread of their own so that the
+            // ring's loads never wait for a slot.  dx mode: the head's x and dy rows of
+            // this tile's tokens (the run's rows reversed: tokens Lc - 128 (qt + 1) ..
+            // Lc - 128 qt - 1 of the chunk; a start before token 0 reads zeros) into
+            // slot hi & 1.  Dot mode: the head's dy rows of the tile (tokens in order).
+            prefetch_tmap(&tm_dxx);
+            prefetch_tmap(&tm_ddy);
+            int dissued = 0;
+            for (int hi = 0; hi < nh; ++hi) {
+                const int sl = hi & 1, h = h0 + hi;
+                if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
+                uint8_t* ds = sY + sl * kSlot;
+                if (dxa.dx) {
+                    const int row = c * L + Lc - 128 * (qt + 1);
+                    mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
+                    tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
+                    tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
+                } else {
+                    mbar_arrive_expect_tx(&bars.dfull[sl], 16384);
+                    tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, c * L + 128 * qt, b);
+                }
+                dissued = hi + 1;
             }
+            if (*abort)   // the staged tiles of the last two heads issued
+                for (int hi = dissued - 1; hi >= 0 && hi >= dissued - 2; --hi)
+                    mbar_wait(&bars.dfull[hi & 1], (hi >> 1) & 1, kWaitNs);
         }
     } else if (warp == kWarpMma) {
         // ----------------------------------------------------------- MMA issue
