@@ -193,7 +193,7 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     take(c.Br, bcE);
     take(c.Cr, bcE);
     take(c.cum2r, cum);
-    take(c.ones, cum);
+    take(c.ones, dot ? 0 : cum);   // dot mode: the y' run takes dt' = 1 without rows
     take(c.xB, copies ? hnE : 0);
     take(c.xCr, copies ? hnE : 0);
     take(c.xr, xr ? xyE : 0);

@@ -329,7 +329,23 @@ struct PrepArgs {
     int T, H, G, P, N, L, Q;
     int copies;   // write xB, xCr and the per-(Q*H)-head rows (the CUDA-core dC / dB runs)
     int with_xr;  // write xr (not needed when dC and dB come from bwd_bc_tc)
+    int with_cr;  // write cum2r and ones (else bwd_rev_cum writes cum2r and the y' run takes dt' = 1)
 };
+
+// --- cum2' of the reversed run, one CTA per (b, h, chunk): the token of reversed
+// position k of chunk c (Lc tokens) is Lc - 1 - k, and cum2'_k = cum2[Lc - 1] -
+// cum2[Lc - 1 - k] (coalesced in both directions; bwd_prep would write it with
+// one scattered 4-byte store per head and token).
+__global__ void __launch_bounds__(256) bwd_rev_cum(const float* __restrict__ cum2,
+                                                   float* __restrict__ cum2r, int T, int L, int nc) {
+    const int64_t row = blockIdx.x / nc;   // (b, h)
+    const int c = (int)(blockIdx.x % nc);
+    const int Lc = min(L, T - c * L);
+    const float* src = cum2 + row * T + (int64_t)c * L;
+    float* dst = cum2r + row * T + (int64_t)c * L;
+    const float last = __ldg(src + Lc - 1);
+    for (int k = threadIdx.x; k < Lc; k += blockDim.x) dst[k] = last - __ldg(src + (Lc - 1 - k));
+}
 
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
@@ -369,7 +385,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     }
     copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
     copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
-    for (int h = threadIdx.x; h < a.H; h += kThreads) {
+    for (int h = threadIdx.x; a.with_cr && h < a.H; h += kThreads) {
         const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
         const int64_t o = ((int64_t)b * a.H + h) * a.T + t;
         a.cum2r[o] = c2[c * a.L + Lc - 1] - c2[ts];
@@ -640,7 +656,7 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     PrepArgs pa{a.dy, a.B, a.C, a.x, a.cum2, a.dtT, w.dyr, w.Br, w.Cr, w.xB, w.xCr, w.xr,
                 w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
                 (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1,
-                bc ? 0 : 1};
+                bc ? 0 : 1, a.xyd ? 0 : 1};
     bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
     if (!tc2) {   // the tensor-core runs read Sprev and Gn untransposed
         bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
@@ -661,8 +677,11 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dd.dxm_dx = a.dx;
         dd.dxm_xy = a.xyd;
         dd.dxm_dyx = a.dyxd;
+        dd.dt1 = 1;   // dt' = 1: no rows of ones
+        bwd_rev_cum<<<(unsigned)(d.b * d.H * d.nc), 256, 0, st>>>(a.cum2, w.cum2r, (int)d.T, (int)d.L,
+                                                                 (int)d.nc);
         // dy reversed within each chunk: the adjoint run's max |dy| per chunk holds
-        e = launch_chunk_out_tc(dd, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, nullptr, a.dx, err, st,
+        e = launch_chunk_out_tc(dd, w.dyr, w.Br, w.Cr, w.cum2r, a.dtT, gio, nullptr, a.dx, err, st,
                                 w.xabs_dy, false, true);
     } else {
         e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);

@@ -47,6 +47,9 @@ struct Dims {
     // partial dots dxm_xy[((b * H + h) * T + t) * 2 + g] = sum over the 32 columns
     // of group g of x y', dxm_dyx[...] = the same of dy x (x, dy bf16, contiguous
     // [b, T, H, 64]; dt [b, H, T]; D [H] or null).
+    // Tensor-core output stage with fp32 y only: dt is 1 everywhere (the
+    // backward's y' run); dtT is not read.
+    int dt1 = 0;
     const void* dxm_x = nullptr;
     const void* dxm_dy = nullptr;
     const float* dxm_dt = nullptr;

@@ -162,7 +162,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const float* __restrict__ dtT, const float* __restrict__ Dvec,
                     const uint32_t* __restrict__ xabs, int T, int H,
                     int G, int nc, int v1, int n1, int v2, int pts, int pst, int xdiv, int xmul, int xmod,
-                    int yred, int st_mn, const __nv_bfloat16* __restrict__ dyv,
+                    int yred, int st_mn, int dt1, const __nv_bfloat16* __restrict__ dyv,
                     float* __restrict__ ydot2, int yrev, float* __restrict__ yacc, int ycols,
                     const DxArgs dxa, int32_t* err) {
     using C = K4Cfg<L, NA, kY32, kDot>;
@@ -868,7 +868,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 const int s = ctid + kConvThreads * i;
                 if (s < KS && s < Lc) {
                     pc[i] = __ldg(crow + s);
-                    pd[i] = __ldg(drow + s);
+                    pd[i] = (kY32 && dt1) ? 1.f : __ldg(drow + s);
                 }
             }
             pD = Dvec ? __ldg(Dvec + ((h0 + hh) >> pts)) : 0.f;
@@ -1094,7 +1094,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
                          tm_s, tm_y, tm_dxx, tm_ddy, cum2, dtT, D, xabs, (int)d.T, (int)d.H, (int)d.G, (int)d.nc,
                          sp.v1, (int)sp.n1, sp.v2, d.pts, (int)d.P, d.xdiv, (int)(d.xmul ? d.xmul : d.P), d.xmod,
-                         d.yred, d.st_mn, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out,
+                         d.yred, d.st_mn, d.dt1, static_cast<const __nv_bfloat16*>(d.ydot_dy), d.ydot_out,
                          d.yrev, static_cast<float*>(y), (int)(d.xcols ? d.xcols : d.H * d.P),
                          DxArgs{d.dxm_x, d.dxm_dy, d.dxm_dt, d.dxm_D, d.dxm_dx, d.dxm_xy, d.dxm_dyx}, err);
     }
