@@ -498,13 +498,53 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
         const int64_t go = (((int64_t)b * a.nc + c) * a.H + h) * PN;
         const float* Gn = a.Gn + go;
         const TI* G16 = static_cast<const TI*>(a.GnIO) + go;   // when only the I/O-type Gn exists
-        auto gn = [&](int64_t k) { return a.gn16 ? to_f32(G16[k]) : Gn[k]; };
-        if (c + 1 < a.nc) {
-            const TI* Sa = static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN;
-            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), to_f32(Sa[k]), gs);
-        } else {
-            const float* Sa = a.fin + ((int64_t)b * a.H + h) * PN;
-            for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), Sa[k], gs);
+        bool done = false;
+        if constexpr (sizeof(TI) == 2) {
+            if (a.gn16) {   // 16-byte loads: eight bf16 of Gn (and of Sprev) at a time (PN % 8 == 0)
+                const uint4* g4 = reinterpret_cast<const uint4*>(G16);
+                auto dot8 = [](uint4 g, const float (&s)[8], float acc) {
+                    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc = fmaf(__uint_as_float(gw[e] << 16), s[2 * e], acc);
+                        acc = fmaf(__uint_as_float(gw[e] & 0xffff0000u), s[2 * e + 1], acc);
+                    }
+                    return acc;
+                };
+                if (c + 1 < a.nc) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(
+                        static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN);
+                    for (int64_t k8 = tid; k8 < PN / 8; k8 += kThreads) {
+                        const uint4 sv = s4[k8];
+                        const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+                        float sf[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sf[2 * e] = __uint_as_float(sw[e] << 16);
+                            sf[2 * e + 1] = __uint_as_float(sw[e] & 0xffff0000u);
+                        }
+                        gs = dot8(g4[k8], sf, gs);
+                    }
+                } else {
+                    const float4* f4 = reinterpret_cast<const float4*>(a.fin + ((int64_t)b * a.H + h) * PN);
+                    for (int64_t k8 = tid; k8 < PN / 8; k8 += kThreads) {
+                        const float4 f0 = f4[2 * k8], f1 = f4[2 * k8 + 1];
+                        const float sf[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+                        gs = dot8(g4[k8], sf, gs);
+                    }
+                }
+                done = true;
+            }
+        }
+        if (!done) {
+            auto gn = [&](int64_t k) { return a.gn16 ? to_f32(G16[k]) : Gn[k]; };
+            if (c + 1 < a.nc) {
+                const TI* Sa = static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN;
+                for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), to_f32(Sa[k]), gs);
+            } else {
+                const float* Sa = a.fin + ((int64_t)b * a.H + h) * PN;
+                for (int64_t k = tid; k < PN; k += kThreads) gs = fmaf(gn(k), Sa[k], gs);
+            }
         }
     }
     const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
