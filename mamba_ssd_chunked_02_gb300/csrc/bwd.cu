@@ -355,10 +355,19 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     const int ts = c * a.L + (Lc - 1 - k);   // the source token of reversed position t
     const int hpg = a.H / a.G;
     // Rows are 16-byte multiples (P, N >= 16 elements) at 16-byte aligned starts.
+    // Four of a thread's 16-byte loads are in flight before their stores.
     auto copy = [&](const void* src, int64_t srow, void* dst, int64_t drow, int64_t n16) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(static_cast<const TI*>(src) + srow);
-        uint4* d4 = reinterpret_cast<uint4*>(static_cast<TI*>(dst) + drow);
-        for (int64_t i = threadIdx.x; i < n16; i += kThreads) d4[i] = s4[i];
+        const uint4* __restrict__ s4 = reinterpret_cast<const uint4*>(static_cast<const TI*>(src) + srow);
+        uint4* __restrict__ d4 = reinterpret_cast<uint4*>(static_cast<TI*>(dst) + drow);
+        for (int64_t i0 = threadIdx.x; i0 < n16; i0 += 4 * kThreads) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * kThreads < n16) v[u] = s4[i0 + u * kThreads];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * kThreads < n16) d4[i0 + u * kThreads] = v[u];
+        }
     };
     const int64_t rowx = (int64_t)a.H * a.P, rowbc = (int64_t)a.G * a.N, rowhn = (int64_t)a.H * a.N;
     const int64_t E = sizeof(TI);
