@@ -531,10 +531,10 @@ def run_backward(args, w):
                      "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": "whole backward",
                      "model": "backward I/O + chunk states at fp32 twice (bench.bwd_bytes)",
                      "algorithmic_bytes": nbytes, "peak_source": src},
-        # 12 of the library's kernels per call on the tensor-core path: stages 1-3
-        # (recompute), the y run, the chunk adjoints, bwd_state_pass_rev, bwd_prep,
-        # bwd_rev_cum, the y' run, dC, dB, bwd_token (plus two memsets)
-        "gpu_launches": 12 * K, "clocks": clk}), flush=True)
+        # 10 of the library's kernels per call on the tensor-core path: stages 1-3
+        # (recompute), the y run, the chunk adjoints, bwd_state_pass_rev, the y' run,
+        # dC, dB, bwd_token (plus two memsets)
+        "gpu_launches": 10 * K, "clocks": clk}), flush=True)
 
 
 def main():

@@ -189,10 +189,11 @@ BwdCarve bwd_carve(const Dims& d, bool copies, bool dot, bool half, bool xr) {
     take(c.GnIO, stE);
     take(c.yno, dot ? 0 : xy32);   // dot mode: the y run writes only dy . y (ydot2)
     take(c.yr, dot ? 0 : xy32);   // dot mode: the y' run writes dx and two dots per token
-    take(c.dyr, xyE);
-    take(c.Br, bcE);
-    take(c.Cr, bcE);
-    take(c.cum2r, cum);
+    // the reversed inputs of the y' run (dot mode: the run is anti-causal on the inputs)
+    take(c.dyr, dot ? 0 : xyE);
+    take(c.Br, dot ? 0 : bcE);
+    take(c.Cr, dot ? 0 : bcE);
+    take(c.cum2r, dot ? 0 : cum);
     take(c.ones, dot ? 0 : cum);   // dot mode: the y' run takes dt' = 1 without rows
     take(c.xB, copies ? hnE : 0);
     take(c.xCr, copies ? hnE : 0);

@@ -21,10 +21,11 @@
 //             dSprev_c = sum_i e_i dy_i C_i^T + E_c dSprev_{c+1},  dSprev_nc = dfinal
 //             Gn_c = dSprev_{c+1},  dinitial_state = dSprev_0
 //   dx and the decay terms come from the forward's own output kernel run
-//   backwards in time: with the tokens of each chunk reversed, B and C swapped,
-//   dt' = 1, cum2' = c2_last - c2 and Gn as the carried state, stage 4 computes
+//   backwards in time, with B and C swapped, dt' = 1 and Gn as the carried state:
 //             y'_j = sum_{i>=j} (B_j.C_i) exp2(c2_i - c2_j) dy_i + exp2(c2_last - c2_j) Gn B_j
-//   and then
+//   On the tensor cores (dx mode) stage 4 runs this anti-causal form directly,
+//   in token order; elsewhere it runs causally on each chunk's tokens reversed
+//   (cum2' = c2_last - c2).  Then
 //     dx_j   = dt_j y'_j + D dy_j
 //     ddt_j  = x_j.y'_j + A sum_{i>=j} dcum_i
 //     dcum_i = dy_i.(y_i - D x_i) - dt_i x_i.y'_i + [i = last] <Gn, S_after>
@@ -52,11 +53,12 @@
 //                       tensor-core kernel in its adjoint weight mode, or
 //                       bwd_chunk_adjoint where the shape does not allow it
 //   bwd_state_pass_rev  reverse pass over chunks, in place            -> Gn, dinit
-//   bwd_prep            the runs' reordered inputs (reversed chunks, per-head
-//                       copies of B and C, cum2' and dt' rows)
+//   bwd_prep            the reordered inputs of the runs that need them (reversed
+//                       chunks, per-head copies of B and C, cum2' and dt' rows;
+//                       none in dx mode with dC / dB from bwd_bc_tc)
 //   bwd_transpose       Sprev^T and Gn^T
-//   (stage 4)           y' (fp32), or on the tensor cores (dx mode) dx itself
-//                       and the per-token dots x . y' and dy . x
+//   (stage 4)           y' (fp32), or on the tensor cores (dx mode, anti-causal in
+//                       token order) dx itself and the per-token dots x . y', dy . x
 //   bwd_bc_tc (2 runs)  dC and dB, summed over the heads in the kernel (tensor
 //                       cores: bf16, P = 64, L in {128, 256}, N in {64, 128, 256})
 //   (stage 4, 2 runs)   otherwise the dC run and the dB run (per-head outputs in
@@ -329,23 +331,9 @@ struct PrepArgs {
     int T, H, G, P, N, L, Q;
     int copies;   // write xB, xCr and the per-(Q*H)-head rows (the CUDA-core dC / dB runs)
     int with_xr;  // write xr (not needed when dC and dB come from bwd_bc_tc)
-    int with_cr;  // write cum2r and ones (else bwd_rev_cum writes cum2r and the y' run takes dt' = 1)
+    int with_cr;  // write cum2r and ones, and dyr, Br, Cr (the reversed y' run; not in dx mode,
+                  // whose y' run is anti-causal on dy, B and C as they are)
 };
-
-// --- cum2' of the reversed run, one CTA per (b, h, chunk): the token of reversed
-// position k of chunk c (Lc tokens) is Lc - 1 - k, and cum2'_k = cum2[Lc - 1] -
-// cum2[Lc - 1 - k] (coalesced in both directions; bwd_prep would write it with
-// one scattered 4-byte store per head and token).
-__global__ void __launch_bounds__(256) bwd_rev_cum(const float* __restrict__ cum2,
-                                                   float* __restrict__ cum2r, int T, int L, int nc) {
-    const int64_t row = blockIdx.x / nc;   // (b, h)
-    const int c = (int)(blockIdx.x % nc);
-    const int Lc = min(L, T - c * L);
-    const float* src = cum2 + row * T + (int64_t)c * L;
-    float* dst = cum2r + row * T + (int64_t)c * L;
-    const float last = __ldg(src + Lc - 1);
-    for (int k = threadIdx.x; k < Lc; k += blockDim.x) dst[k] = last - __ldg(src + (Lc - 1 - k));
-}
 
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
@@ -372,7 +360,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
     const int64_t rowx = (int64_t)a.H * a.P, rowbc = (int64_t)a.G * a.N, rowhn = (int64_t)a.H * a.N;
     const int64_t E = sizeof(TI);
     const int64_t bt = (int64_t)b * a.T;
-    copy(a.dy, (bt + ts) * rowx, a.dyr, (bt + t) * rowx, rowx * E / 16);
+    if (a.with_cr) copy(a.dy, (bt + ts) * rowx, a.dyr, (bt + t) * rowx, rowx * E / 16);
     if (a.copies) {
         copy(a.x, (bt + ts) * rowx, a.xr, (bt + t) * rowx, rowx * E / 16);
     } else if (a.with_xr) {
@@ -392,8 +380,10 @@ __global__ void __launch_bounds__(kThreads) bwd_prep(PrepArgs a) {
             d4[i] = q;
         }
     }
-    copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
-    copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
+    if (a.with_cr) {
+        copy(a.C, (bt + ts) * rowbc, a.Br, (bt + t) * rowbc, rowbc * E / 16);
+        copy(a.B, (bt + ts) * rowbc, a.Cr, (bt + t) * rowbc, rowbc * E / 16);
+    }
     for (int h = threadIdx.x; a.with_cr && h < a.H; h += kThreads) {
         const float* c2 = a.cum2 + ((int64_t)b * a.H + h) * a.T;
         const int64_t o = ((int64_t)b * a.H + h) * a.T + t;
@@ -706,7 +696,8 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
                 w.cum2r, w.ones, w.cum2d, w.dtTd, w.cum2rd, w.onesd,
                 (int)d.T, (int)d.H, (int)d.G, (int)d.P, (int)d.N, (int)d.L, Q, tc2 ? 0 : 1,
                 bc ? 0 : 1, a.xyd ? 0 : 1};
-    bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
+    if (pa.with_cr || pa.with_xr || pa.copies)   // dx mode with dC / dB from bwd_bc_tc needs none
+        bwd_prep<TI><<<dim3((unsigned)d.T, (unsigned)d.b), kThreads, 0, st>>>(pa);
     if (!tc2) {   // the tensor-core runs read Sprev and Gn untransposed
         bwd_transpose<TI, TI><<<(unsigned)gt, kThreads, 0, st>>>(static_cast<const TI*>(a.Sprev),
                                                                  static_cast<TI*>(w.SprevT),
@@ -726,11 +717,11 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
         dd.dxm_dx = a.dx;
         dd.dxm_xy = a.xyd;
         dd.dxm_dyx = a.dyxd;
-        dd.dt1 = 1;   // dt' = 1: no rows of ones
-        bwd_rev_cum<<<(unsigned)(d.b * d.H * d.nc), 256, 0, st>>>(a.cum2, w.cum2r, (int)d.T, (int)d.L,
-                                                                 (int)d.nc);
-        // dy reversed within each chunk: the adjoint run's max |dy| per chunk holds
-        e = launch_chunk_out_tc(dd, w.dyr, w.Br, w.Cr, w.cum2r, a.dtT, gio, nullptr, a.dx, err, st,
+        // Anti-causal in token order: y'_j = sum_{i >= j} (B_j . C_i) exp2(c2_i - c2_j)
+        // dy_i + exp2(c2_last - c2_j) Gn B_j, i.e. x'' = dy, B'' = C, C'' = B, dt' = 1.
+        dd.dt1 = 1;
+        dd.antic = 1;
+        e = launch_chunk_out_tc(dd, a.dy, a.C, a.B, a.cum2, a.dtT, gio, nullptr, a.dx, err, st,
                                 w.xabs_dy, false, true);
     } else {
         e = out4(d, w.dyr, w.Br, w.Cr, w.cum2r, w.ones, gio, a.yr, true);

@@ -50,6 +50,10 @@ struct Dims {
     // Tensor-core output stage with fp32 y only: dt is 1 everywhere (the
     // backward's y' run); dtT is not read.
     int dt1 = 0;
+    // Tensor-core output stage with fp32 y only (the backward's y' run in token
+    // order): anti-causal, y_t = sum_{s >= t} M[t, s] x_s + exp2(cum2_last - cum2_t)
+    // (C_t . Sprev^T), M[t, s] = (C_t . B_s) exp2(cum2_s - cum2_t) dt_s.
+    int antic = 0;
     const void* dxm_x = nullptr;
     const void* dxm_dy = nullptr;
     const float* dxm_dt = nullptr;

@@ -52,6 +52,13 @@
 // [2^-4, 2^15], max|C.B| in [2^-8, 2^15], max dt >= 2^-10 -- and otherwise
 // keep bf16 for that head (x stays untouched, M is packed as bf16).
 //
+// The fp32-output variants also carry the backward's options; one of them,
+// anti-causal (a template parameter, for the backward's y' run in token order),
+// takes for the rows [128 qt, 128 qt + 128) the keys [128 qt, L), builds M over
+// keys at or after each row (the decay split at the warp's last row, the
+// diagonal block's packed path referenced to its first key) and scales the
+// carried-state term by exp2(cum2_last - cum2_t).
+//
 // Warp roles: 0, 1 = converters, 2 = TMA producer, 3 = MMA issuer (+ TMEM
 // owner), 4 .. 4+4*EG-1 = epilogue (TMEM lane quadrant = warp % 4, column
 // group (warp-4)/4).  Loads stream through a ring
@@ -153,7 +160,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 
-template <int L, int NA, bool kY32, bool kDot = false>
+template <int L, int NA, bool kY32, bool kDot = false, bool kAnti = false>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_s,
@@ -194,11 +201,16 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         bc0 = n1 / (NQ * (H / v1));
     }
     const int n_hblk = H / hpc;
-    const int qt = NQ - 1 - rest % NQ; rest /= NQ;
+    // Anti-causal mode (fp32-output variant only: the backward's y' run in token
+    // order): the keys of a row are the tokens at or after it, so the tile of rows
+    // [128 qt, 128 qt + 128) takes keys [128 qt, L) of the chunk.
+    constexpr bool anti = kY32 && kAnti;
+    const int qt = anti ? rest % NQ : NQ - 1 - rest % NQ; rest /= NQ;   // heaviest first
     const int hblk = rest % n_hblk; rest /= n_hblk;
     const int c = (bc0 + rest) % nc;
     const int b = (bc0 + rest) / nc;
-    const int KS = 128 * (qt + 1);
+    const int KS = anti ? L - 128 * qt : 128 * (qt + 1);   // keys of the tile
+    const int kb = anti ? 128 * qt : 0;                    // its first key (chunk position)
     const int h0 = hblk * hpc;
     const int g = h0 / (H / G);
     const int nh = hpc;
@@ -255,11 +267,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (!mbar_wait_or_abort(&bars.xfree[st], (k & 1) ^ 1, abort, kWaitNs)) break;
                 uint8_t* sx = sStage + st * C::STAGE;
                 if (it < NA) {
-                    // B block `it`: keys [0, KS) x state dims [64 it, 64 it + 64), K-major.
+                    // B block `it`: keys [kb, kb + KS) x state dims [64 it, 64 it + 64), K-major.
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + (it == 0 ? C::C_BYTES : 0));
                     for (int r = 0; r < KS / 128; ++r)
                         tma_load_3d(sx + r * 16384, &tm_b, &bars.full[st], g * N + 64 * it,
-                                    c * L + 128 * r, b);
+                                    c * L + kb + 128 * r, b);
                     if (it == 0)
                         for (int a = 0; a < NA; ++a)
                             tma_load_3d(sC + a * 16384, &tm_c, &bars.full[st], g * N + 64 * a,
@@ -272,7 +284,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     const int xcol = kY32 ? (h / xdiv) * xmul + (h % xmod) * C::P : h * pst;
                     mbar_arrive_expect_tx(&bars.full[st], KS * 128 + C::S_BYTES);
                     for (int r = 0; r < KS / 128; ++r)
-                        tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + 128 * r, b);
+                        tma_load_3d(sx + r * 16384, &tm_x, &bars.full[st], xcol, c * L + kb + 128 * r, b);
                     // Sprev comes from stage 3: with programmatic dependent launch
                     // everything before this point ran while it was finishing.
                     if (it == NA) grid_dep_wait();
@@ -306,7 +318,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
                 uint8_t* ds = sY + sl * kSlot;
                 if (dxa.dx) {
-                    const int row = c * L + Lc - 128 * (qt + 1);
+                    const int row = anti ? c * L + 128 * qt : c * L + Lc - 128 * (qt + 1);
                     mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
                     tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
                     tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
@@ -424,9 +436,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         const int etid = threadIdx.x - 32 * kEpiWarp0; // 0 .. kEpiThreads-1
         const int tl = 32 * q + lane;                  // row within the tile
         const int tc_ = 128 * qt + tl;                 // row within the chunk
-        const int jd = 4 * qt + q;                     // this warp's diagonal key block
+        const int jd = (128 * qt + 32 * q - kb) >> 5;  // this warp's diagonal key block
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const int nblk = KS / 32, hblkn = KS / 64;    // key blocks, key blocks per K-half
+        // In-mask key blocks: those up to the diagonal (causal) or from it (anti).
+        const int jmin = anti ? jd : 0, jmax = anti ? nblk - 1 : jd;
+        const int jown = jmin + ((grp - jmin) % EG + EG) % EG;   // first own in-mask block
         uint32_t sync_phase = 0;
         // Barrier of all epilogue threads; gives up (false) on abort or timeout.
         auto group_sync = [&]() -> bool {
@@ -435,13 +450,13 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             sync_phase ^= 1u;
             return __all_sync(0xffffffffu, r);
         };
-        // Key blocks above the diagonal are zero for every head: write them once.
+        // Key blocks outside the mask are zero for every head: write them once.
         {
             uint32_t z[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) z[e] = 0u;
-            for (int j = jd + 1; j < nblk; ++j)
-                if (j % EG == grp) tmem_st16(tmem + lane_off + COL_MM + 16 * j, z);
+            for (int j = 0; j < nblk; ++j)
+                if ((j < jmin || j > jmax) && j % EG == grp) tmem_st16(tmem + lane_off + COL_MM + 16 * j, z);
             tmem_wait_st();
         }
         bool ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&bars.cb_full, 0, abort, kWaitNs));
@@ -449,7 +464,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // max |C.B| over the entries this tile uses (bounds |M| for the fp16 check).
         float cbmax = 0.f;
         if (ok) {
-            for (int j = grp; j <= jd; j += EG) {
+            for (int j = jown; j <= jmax; j += EG) {
                 uint32_t r[32];
                 tmem_ld32_sync(tmem + lane_off + COL_CB32 + 32 * j, r);
 #pragma unroll
@@ -470,7 +485,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // the fp16 path), else bf16 (no head takes the fp16 path).
         const bool cb16 = cb_fits_f16(cbmax);
         if (ok) {
-            for (int j = grp; j <= jd; j += EG) {
+            for (int j = jown; j <= jmax; j += EG) {
                 uint32_t r[32];
                 tmem_ld32_sync(tmem + lane_off + COL_CB32 + 32 * j, r);
                 uint32_t p[16];
@@ -492,7 +507,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         auto prefetch_dt = [&](int hp) {
             if (!(kY32 && dxa.dx) || hp >= nh) return;
             const int k = 128 * qt + 32 * q + lane;
-            if (k < Lc) pf_dt = __ldg(dxa.dt + ((int64_t)b * H + h0 + hp) * T + (int64_t)c * L + (Lc - 1 - k));
+            if (k < Lc)
+                pf_dt = __ldg(dxa.dt + ((int64_t)b * H + h0 + hp) * T + (int64_t)c * L + (anti ? k : Lc - 1 - k));
             pf_D = dxa.D ? __ldg(dxa.D + h0 + hp) : 0.f;
         };
         prefetch_dt(0);
@@ -520,9 +536,10 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
                     return false;
-                // This row's token sits at row 127 - tl of the staged tiles (128-byte
-                // swizzled rows: 16-byte chunk cc of row r at cc ^ (r & 7)).
-                const int sr = 127 - (32 * q + lane);
+                // This row's token sits at row 127 - tl of the staged tiles (tl in
+                // anti mode, whose rows are in token order; 128-byte swizzled rows:
+                // 16-byte chunk cc of row r at cc ^ (r & 7)).
+                const int sr = anti ? 32 * q + lane : 127 - (32 * q + lane);
                 const uint8_t* xs = sY + sl * kSlot + sr * 128;
                 uint4 xw4[PC / 8], dw4[PC / 8];
 #pragma unroll
@@ -533,7 +550,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 }
                 if (k < Lc) {
                     const int hh = h0 + hp;
-                    const int64_t t = (int64_t)c * L + (Lc - 1 - k);
+                    const int64_t t = (int64_t)c * L + (anti ? k : Lc - 1 - k);
                     const int64_t ro = ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC;
                     const float dtj = pf_dt, dh = pf_D;
                     float4* op = reinterpret_cast<float4*>(dxa.dx + ro);
@@ -679,28 +696,35 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             const bool use16 = bars.use16s[st] != 0;
             const float dh = bars.dvals[st];           // D of this head: added to M[t, t]
             // Every load of the row's vectors first, so that their latencies overlap.
-            const float ct = ck[tc_];
-            const float cr = ck[32 * jd];
-            const float cml = ck[32 * jd + 31];
+            // (ck, dk index keys from kb: the tile's rows are keys tc_ - kb.)
+            const float ct = ck[tc_ - kb];
+            const float cfirst = ck[32 * jd], clast = ck[32 * jd + 31];
+            // Off the diagonal block the decay splits at the warp's first row (causal:
+            // keys before it) or last row (anti: keys after it); the diagonal block's
+            // packed path takes its last key (causal) or first key (anti).
+            const float cr = anti ? clast : cfirst;
+            const float cml = anti ? cfirst : clast;
             const float ckd = ck[32 * jd + lane];
             const float dsd = dk[32 * jd + lane];
-            constexpr int kMaxOwn = (L / 32 + EG - 1) / EG;   // own blocks below the diagonal
+            constexpr int kMaxOwn = (L / 32 + EG - 1) / EG;   // own blocks off the diagonal
             float cj[kMaxOwn], dj[kMaxOwn];
 #pragma unroll
             for (int i = 0; i < kMaxOwn; ++i) {
                 const int j = grp + EG * i;
-                cj[i] = j < jd ? ck[32 * j + lane] : 0.f;
-                dj[i] = j < jd ? dk[32 * j + lane] : 0.f;
+                const bool off = anti ? (j > jd && j < nblk) : j < jd;
+                cj[i] = off ? ck[32 * j + lane] : 0.f;
+                dj[i] = off ? dk[32 * j + lane] : 0.f;
             }
-            const float e_t = ex2(ct);
-            const float u_t = ex2(ct - cr);
+            // State term's row factor: exp2(cum2_t) (anti: exp2(cum2_last - cum2_t)).
+            const float e_t = anti ? ex2(ck[KS - 1] - ct) : ex2(ct);
+            const float u_t = anti ? ex2(cr - ct) : ex2(ct - cr);
             float* vq = vdt + q * 256;
             __half* vh = reinterpret_cast<__half*>(vq);
 #pragma unroll
             for (int i = 0; i < kMaxOwn; ++i) {
                 const int j = grp + EG * i;
-                if (j < jd) {
-                    const float v = ex2(cr - cj[i]) * dj[i];
+                if (anti ? (j > jd && j < nblk) : j < jd) {
+                    const float v = (anti ? ex2(cj[i] - cr) : ex2(cr - cj[i])) * dj[i];
                     if (use16) vh[32 * j + lane] = __float2half_rn(v);
                     else vq[32 * j + lane] = v;
                 }
@@ -712,15 +736,20 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             // every dt_s of the block is >= 2^-14; otherwise the fp32 path below.
             // The causal mask is applied to the final product.
             const bool owner = jd % EG == grp;
-            const bool dpack = use16 && cr - cml <= 14.f &&
+            const bool dpack = use16 && cfirst - clast <= 14.f &&
                                !__any_sync(0xffffffffu, owner && dsd < 6.1035156e-5f);
+            // The block's dt goes to the slot of block jd + 1, outside the causal
+            // mask; in anti mode that block is inside it, so to halves 256.., which
+            // the packed key factors (halves 0 .. 32 nblk - 1) never use.
+            constexpr int kNoSlot = 256;
+            const int dslot = anti ? kNoSlot : 32 * jd + 32;
             if (dpack && owner) {
-                vh[32 * jd + lane] = __float2half_rn(ex2(cml - ckd));
-                vh[32 * jd + 32 + lane] = __float2half_rn(dsd);
+                vh[32 * jd + lane] = __float2half_rn(anti ? ex2(ckd - cml) : ex2(cml - ckd));
+                vh[dslot + lane] = __float2half_rn(dsd);
             }
             __syncwarp();
             const __half2 u2 = __float2half2_rn(u_t);
-            const __half2 ud2 = __float2half2_rn(ex2(ct - cml));
+            const __half2 ud2 = __float2half2_rn(anti ? ex2(cml - ct) : ex2(ct - cml));
             const __half2 dd2 = (lane & 1) ? __floats2half2_rn(0.f, dh) : __floats2half2_rn(dh, 0.f);
 
             // ---- M, in two K-halves.
@@ -732,14 +761,14 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const int jlo = half * hblkn, jhi = min(jd, jlo + hblkn - 1);
-                int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own block >= jlo
+                const int jlo = max(half * hblkn, jmin), jhi = min(jmax, half * hblkn + hblkn - 1);
+                int j = jlo + ((grp - jlo) % EG + EG) % EG;    // first own in-mask block >= jlo
                 uint32_t r[16];
                 if (j <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * j, r);
                 for (; j <= jhi; j += EG) {
                     tmem_wait_ld_regs(r);
                     uint32_t m[16];
-                    if (j < jd && use16) {
+                    if (j != jd && use16) {
                         const uint4* v4 = reinterpret_cast<const uint4*>(vh + 32 * j);
 #pragma unroll
                         for (int e8 = 0; e8 < 4; ++e8) {
@@ -756,7 +785,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                         if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
                     } else if (j == jd && dpack) {
                         const uint4* w4 = reinterpret_cast<const uint4*>(vh + 32 * j);
-                        const uint4* d4 = reinterpret_cast<const uint4*>(vh + 32 * j + 32);
+                        const uint4* d4 = reinterpret_cast<const uint4*>(vh + dslot);
 #pragma unroll
                         for (int e8 = 0; e8 < 4; ++e8) {
                             const uint4 ww = w4[e8], dd = d4[e8];
@@ -771,7 +800,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                                 __half2 mm2 = __hmul2(cd, uw);
                                 if (e == (lane >> 1)) mm2 = __hadd2(mm2, dd2);   // key t: + D
                                 const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mm2);
-                                m[e] = 2 * e + 1 <= lane ? mw : (2 * e <= lane ? (mw & 0xffffu) : 0u);
+                                // keys 2e (low half) and 2e + 1 against row lane
+                                m[e] = anti ? (2 * e >= lane ? mw : (2 * e + 1 >= lane ? (mw & 0xffff0000u) : 0u))
+                                            : (2 * e + 1 <= lane ? mw : (2 * e <= lane ? (mw & 0xffffu) : 0u));
                             }
                         }
                         if (j + EG <= jhi) tmem_ld16(tmem + lane_off + COL_CB + 16 * (j + EG), r);
@@ -789,7 +820,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                             }
                         }
                         float mv[32];
-                        if (j < jd) {
+                        if (j != jd) {
                             const float4* v4 = reinterpret_cast<const float4*>(vq + 32 * j);
 #pragma unroll
                             for (int e4 = 0; e4 < 8; ++e4) {
@@ -810,7 +841,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
 #pragma unroll
                                 for (int u = 0; u < 4; ++u) {
                                     const int e = 4 * e4 + u;   // key 32 j + e, row 32 j + lane
-                                    mv[e] = e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f;
+                                    mv[e] = anti ? (e >= lane ? cbv[e] * ex2(cs[u] - ct) * ds[u] : 0.f)
+                                                 : (e <= lane ? cbv[e] * ex2(ct - cs[u]) * ds[u] : 0.f);
                                     if (e == lane) mv[e] += dh;          // key t: + D
                                 }
                             }
@@ -865,10 +897,10 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             plast = __ldg(crow + Lc - 1);
 #pragma unroll
             for (int i = 0; i < KPT; ++i) {
-                const int s = ctid + kConvThreads * i;
-                if (s < KS && s < Lc) {
-                    pc[i] = __ldg(crow + s);
-                    pd[i] = (kY32 && dt1) ? 1.f : __ldg(drow + s);
+                const int s = ctid + kConvThreads * i;   // key kb + s of the chunk
+                if (s < KS && kb + s < Lc) {
+                    pc[i] = __ldg(crow + kb + s);
+                    pd[i] = (kY32 && dt1) ? 1.f : __ldg(drow + kb + s);
                 }
             }
             pD = Dvec ? __ldg(Dvec + ((h0 + hh) >> pts)) : 0.f;
@@ -894,7 +926,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             for (int i = 0; i < KPT; ++i) {
                 const int s = ctid + kConvThreads * i;
                 if (s < KS) {
-                    const bool in = s < Lc;
+                    const bool in = kb + s < Lc;
                     ck[s] = in ? pc[i] : plast;
                     dk[s] = in ? pd[i] : 0.f;
                     if (in) dloc = fmaxf(dloc, pd[i]);
@@ -1042,7 +1074,7 @@ Split4 pick_split4(const Dims& d, int NQ) {
     return best;
 }
 
-template <int L, int NA, bool kY32, bool kDot = false>
+template <int L, int NA, bool kY32, bool kDot = false, bool kAnti = false>
 cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* Cm,
                       const float* cum2, const float* dtT, const void* Sprev, const float* D,
                       void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
@@ -1088,7 +1120,7 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
     }
     const Split4 sp = k4_split(d);
     const int64_t grid = sp.ctas;
-    auto k = chunk_out_tc_kernel<L, NA, kY32, kDot>;
+    auto k = chunk_out_tc_kernel<L, NA, kY32, kDot, kAnti>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     return launch_kernel(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM, st, pdl, tm_x, tm_b, tm_c,
@@ -1106,16 +1138,22 @@ cudaError_t launch_k4_n(const Dims& d, const void* x, const void* B, const void*
                         void* y, int32_t* err, cudaStream_t st, const uint32_t* xabs, bool pdl) {
     switch (d.N) {
         case 64:
-            if constexpr (kY32)
+            if constexpr (kY32) {
                 if (d.ydot_dy) return launch_k4<L, 1, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+                if (d.antic) return launch_k4<L, 1, true, false, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            }
             return launch_k4<L, 1, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
         case 128:
-            if constexpr (kY32)
+            if constexpr (kY32) {
                 if (d.ydot_dy) return launch_k4<L, 2, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+                if (d.antic) return launch_k4<L, 2, true, false, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            }
             return launch_k4<L, 2, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
         case 256:
-            if constexpr (kY32)
+            if constexpr (kY32) {
                 if (d.ydot_dy) return launch_k4<L, 4, true, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+                if (d.antic) return launch_k4<L, 4, true, false, true>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
+            }
             return launch_k4<L, 4, kY32>(d, x, B, Cm, cum2, dtT, Sprev, D, y, err, st, xabs, pdl);
     }
     return cudaErrorInvalidValue;

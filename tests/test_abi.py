@@ -245,35 +245,35 @@ def test_fwd_strided_validates_strides_without_launching(lib):
 
 def test_bwd_workspace_size_formula(lib):
     """Backward workspace: cum2 and dtT, dS (then the chunk adjoints; bf16 on the
-    tensor-core path, fp32 on the CUDA cores), Sprev in the I/O type, the
-    final state, an I/O-type copy of Gn and the reordered inputs of the y' run (dy
-    reversed; B, C reversed; cum2'), each rounded up to 256 bytes.
-    On the tensor-core path the y and y' runs leave three per-token dots (two
-    partials per token and head each: dy . y, x . y', dy . x; the y' run writes
-    dx itself), stage 2 hands them max |x| and max |dy| per (b, chunk, head) for
-    their fp16 range check, and dC and dB come from their own kernel, which reads x, dy, B,
-    C and the states directly.  On the CUDA cores (here: forced) the runs
-    instead need dt' = 1 rows, fp32 y and y', x reversed, per-head copies of B and reversed C,
-    cum2 / dt rows per run head (Q = N/64 of them per head), the dC and dB runs'
-    per-head outputs and Sprev^T, Gn^T."""
+    tensor-core path, fp32 on the CUDA cores), Sprev in the I/O type, the final
+    state and an I/O-type copy of Gn, each rounded up to 256 bytes.  On the
+    tensor-core path the y and y' runs leave three per-token dots (two partials
+    per token and head each: dy . y, x . y', dy . x; the y' run writes dx itself
+    and runs anti-causal on dy, B, C as they are), stage 2 hands them max |x| and
+    max |dy| per (b, chunk, head) for their fp16 range check, and dC and dB come
+    from their own kernel, which reads x, dy, B, C and the states directly.  On
+    the CUDA cores (here: forced) the runs instead need the reversed inputs of
+    the y' run (dy, B, C reversed; cum2' and dt' = 1 rows), fp32 y and y', x
+    reversed, per-head copies of B and reversed C, cum2 / dt rows per run head
+    (Q = N/64 of them per head), the dC and dB runs' per-head outputs and
+    Sprev^T, Gn^T."""
     a256 = lambda v: (v + 255) // 256 * 256
     b, T, H, P, N, G, L, E = 2, 512, 8, 64, 128, 1, 256, 2
     nc, Q = T // L, N // 64
     st = b * nc * H * P * N
     cum = a256(4 * b * H * T)
-    base = (3 * cum + 3 * a256(E * st) + a256(4 * b * H * P * N) +
-            a256(E * b * T * H * P) + 2 * a256(E * b * T * G * N))
+    base = 2 * cum + 3 * a256(E * st) + a256(4 * b * H * P * N)
     dots = a256(4 * 2 * b * H * T)           # per-token dots of the tensor-core y and y' runs
     y_no_skip = a256(4 * b * T * H * P)      # the CUDA-core y run's fp32 y
     y_rev = a256(4 * b * T * H * P)          # the CUDA-core y' run's fp32 y'
     xr = a256(E * b * T * H * P)             # x reversed, read by the dB run
+    rev_in = a256(E * b * T * H * P) + 2 * a256(E * b * T * G * N) + 2 * cum   # dy, B, C; cum2', 1
     copies = 4 * a256(E * b * T * H * N) + 4 * a256(4 * Q * b * H * T) + 2 * a256(E * st)
     xabs = a256(32 * b * nc * H)             # max |x|, max |dy| per (b, chunk, head) from stage 2
     assert m2.bwd_workspace_size(shp()) == base + 3 * dots + 2 * xabs
     fp32_states = a256(4 * st) - a256(E * st)   # dS / chunk adjoints in fp32 on the CUDA cores
-    rev_rows = cum                           # dt' = 1 rows of the CUDA-core y' run
     assert m2.bwd_workspace_size(shp(flags=m2.FLAG_FORCE_SIMT)) == \
-        base + rev_rows + y_rev + xr + y_no_skip + copies + fp32_states
+        base + rev_in + y_rev + xr + y_no_skip + copies + fp32_states
     assert m2.bwd_workspace_size(shp(headdim=3)) == 0          # invalid shape
 
 
