@@ -316,6 +316,83 @@ bwd_state_pass_rev(float4* __restrict__ buf, TI* __restrict__ gio, const float* 
     }
 }
 
+// The same reverse pass for bf16 chunk adjoints and a bf16 Gn (the tensor-core
+// path), laid out like the forward's state pass: one thread owns 8 consecutive
+// state elements (16 bytes of bf16) of one (b, h) for the whole chain, and keeps
+// kDepth chunks of adjoint loads in flight (a rolling prefetch, issued for chunk
+// c - kDepth as chunk c is consumed), so the pass is one HBM stream of adjoints
+// in and Gn out.
+constexpr int kRevDepth = 4;
+
+__global__ void __launch_bounds__(kThreads)
+bwd_state_pass_rev16(const __nv_bfloat16* __restrict__ adj, __nv_bfloat16* __restrict__ gio,
+                     const float* __restrict__ cum2, const float* __restrict__ dfinal,
+                     float* __restrict__ dinit, int T, int H, int L, int nc, int64_t PN,
+                     int64_t blocks_per_bh) {
+    const int64_t bh = blockIdx.x / blocks_per_bh;
+    const int64_t e = ((blockIdx.x % blocks_per_bh) * kThreads + threadIdx.x) * 8;
+    if (e >= PN) return;
+    const int64_t b = bh / H, h = bh % H;
+    float S[8];
+    if (dfinal) {
+        const float4 f0 = *reinterpret_cast<const float4*>(dfinal + bh * PN + e);
+        const float4 f1 = *reinterpret_cast<const float4*>(dfinal + bh * PN + e + 4);
+        S[0] = f0.x; S[1] = f0.y; S[2] = f0.z; S[3] = f0.w;
+        S[4] = f1.x; S[5] = f1.y; S[6] = f1.z; S[7] = f1.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) S[k] = 0.f;
+    }
+    const float* crow = cum2 + bh * T;
+    const int64_t cstride = (int64_t)H * PN;                       // chunk stride
+    const int64_t base = ((b * nc + (nc - 1)) * H + h) * PN + e;   // [b, c = nc-1, h, e]
+    // Chunk c's decay is exp2 of its last token's cum2 (the sequence end for a ragged last chunk).
+    auto last_c2 = [&](int c) { return __ldg(crow + (min(T, (c + 1) * L) - 1)); };
+    uint4 buf[kRevDepth];
+    float cl[kRevDepth];
+#pragma unroll
+    for (int u = 0; u < kRevDepth; ++u) {
+        const int c = nc - 1 - u;
+        if (c >= 0) {
+            buf[u] = __ldcs(reinterpret_cast<const uint4*>(adj + base - u * cstride));
+            cl[u] = last_c2(c);
+        }
+    }
+    for (int c0 = nc - 1; c0 >= 0; c0 -= kRevDepth) {
+#pragma unroll
+        for (int u = 0; u < kRevDepth; ++u) {
+            const int c = c0 - u;
+            if (c >= 0) {
+                const uint4 q = buf[u];
+                const float dec = ex2(cl[u]);
+                const int64_t o = base - (int64_t)(nc - 1 - c) * cstride;
+                if (c - kRevDepth >= 0) {
+                    buf[u] = __ldcs(reinterpret_cast<const uint4*>(adj + o - kRevDepth * cstride));
+                    cl[u] = last_c2(c - kRevDepth);
+                }
+                // Gn of chunk c: the adjoint of the state leaving it, before chunk c's own term.
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    __nv_bfloat162 t = __floats2bfloat162_rn(S[2 * k], S[2 * k + 1]);
+                    w[k] = *reinterpret_cast<uint32_t*>(&t);
+                }
+                *reinterpret_cast<uint4*>(gio + o) = make_uint4(w[0], w[1], w[2], w[3]);
+                const uint32_t qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    S[2 * k] = fmaf(dec, S[2 * k], __uint_as_float(qv[k] << 16));
+                    S[2 * k + 1] = fmaf(dec, S[2 * k + 1], __uint_as_float(qv[k] & 0xffff0000u));
+                }
+            }
+        }
+    }
+    if (dinit) {
+        *reinterpret_cast<float4*>(dinit + bh * PN + e) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4*>(dinit + bh * PN + e + 4) = make_float4(S[4], S[5], S[6], S[7]);
+    }
+}
+
 // --- Inputs of the three stage-4 runs, one CTA per (token t, b).  Token k of
 // chunk c (Lc tokens) is reversed to position Lc-1-k of the same chunk.
 //   y' run (H heads):         dyr = dy reversed, Br = C reversed, Cr = B reversed,
@@ -679,13 +756,26 @@ cudaError_t launch_t(const Dims& d, const BwdArgs& a, const BwdWork& w, bool tc,
     } else {
         bwd_chunk_adjoint<TI><<<(unsigned)g1, kThreads, 0, st>>>(a);
     }
-    const int64_t total4 = d.b * d.H * d.P * d.N / 4;   // N is a multiple of 16
-    const int64_t blocks = std::min<int64_t>((total4 + kThreads - 1) / kThreads, 152 * 16);
-    bwd_state_pass_rev<TI><<<(unsigned)blocks, kThreads, 0, st>>>(
-        reinterpret_cast<float4*>(a.Gn), static_cast<TI*>(a.GnIO), a.cum2,
-        reinterpret_cast<const float4*>(dfinal), reinterpret_cast<float4*>(dinit), total4,
-        (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc,
-        a.gn16 ? reinterpret_cast<const uint2*>(a.Gn) : nullptr);
+    bool rev_done = false;
+    if constexpr (sizeof(TI) == 2) {
+        if (a.gn16) {   // bf16 adjoints in, bf16 Gn out: 8 state elements per thread
+            const int64_t PN = d.P * d.N;   // a multiple of 256
+            const int64_t bpb = (PN / 8 + kThreads - 1) / kThreads;
+            bwd_state_pass_rev16<<<(unsigned)(d.b * d.H * bpb), kThreads, 0, st>>>(
+                reinterpret_cast<const __nv_bfloat16*>(a.Gn), reinterpret_cast<__nv_bfloat16*>(a.GnIO), a.cum2,
+                dfinal, dinit, (int)d.T, (int)d.H, (int)d.L, (int)d.nc, PN, bpb);
+            rev_done = true;
+        }
+    }
+    if (!rev_done) {
+        const int64_t total4 = d.b * d.H * d.P * d.N / 4;   // N is a multiple of 16
+        const int64_t blocks = std::min<int64_t>((total4 + kThreads - 1) / kThreads, 152 * 16);
+        bwd_state_pass_rev<TI><<<(unsigned)blocks, kThreads, 0, st>>>(
+            reinterpret_cast<float4*>(a.Gn), static_cast<TI*>(a.GnIO), a.cum2,
+            reinterpret_cast<const float4*>(dfinal), reinterpret_cast<float4*>(dinit), total4,
+            (int)d.H, d.P * d.N / 4, (int)d.T, (int)d.L, (int)d.nc,
+            a.gn16 ? reinterpret_cast<const uint2*>(a.Gn) : nullptr);
+    }
     // The dC / dB runs: Q heads of N/Q columns per head (64 wide when N >= 64).
     const int Q = d.N >= 64 ? (int)(d.N / 64) : 1;
     const Dims d2 = bwd_run_dims(d);

@@ -402,6 +402,10 @@ MAGNITUDES = [
     ("B,C*0.01", dict(B=0.01, C=0.01), 0.0),      # |C.B| below the fp16 normal range
     ("B,C*100", dict(B=100.0, C=100.0), 0.0),     # |C.B| above the fp16 range
     ("D*1e4", dict(D=1e4), 0.0),            # skip term dominates
+    # fast decay: dt up to 1, so a token's state decays by up to e^-16 per step; the
+    # decay factors and the carried-state term underflow, and the diagonal blocks'
+    # cum2 ranges rule out their packed fp16 path
+    ("dt*10,init", dict(dt=10.0), 0.1),
 ]
 
 
@@ -414,7 +418,20 @@ def test_input_magnitudes(name, scale, init):
     y, f = run_fwd(inp, w)
     yr, fr = oracle.ssd_recurrent(**inp, ngroups=w.ngroups)
     assert_close(to_np(y), yr, w.dtype, name + ": y")
-    assert_close(to_np(f), fr, w.dtype, name + ": final state")
+    if "dt" in scale and scale["dt"] > 1:
+        # Under fast decay the final state is nearly one token's dt x B^T (the last
+        # token carries about half of its energy here, its largest entries ~13 rms):
+        # nothing averages the two bf16 roundings each entry takes on its way (stage
+        # 2's decay-weighted operand and the bf16 dS hand-off, 2^-9 relative each),
+        # so the bound is relative to the entry sizes: relL2 as everywhere, and
+        # max|err| <= 2^-7 max|ref|.
+        got = to_np(f)
+        rel, _ = metrics(got, fr)
+        mxe = np.abs(got - fr).max() / np.abs(fr).max()
+        assert np.isfinite(got).all() and rel <= 1e-2 and mxe <= 2.0 ** -7, \
+            f"{name}: final state relL2 {rel:.3e}, max|err|/max|ref| {mxe:.3e}"
+    else:
+        assert_close(to_np(f), fr, w.dtype, name + ": final state")
 
 
 def test_outputs_do_not_depend_on_workspace_contents():
