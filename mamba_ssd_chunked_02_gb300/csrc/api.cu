@@ -402,9 +402,11 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
     const bool fuse = tc && m2::tc_fused_supported(d) && d.nc >= 3 && (shape->flags & MAMBA2_FLAG_FUSED_STATE) &&
                       ring + sizeof(int32_t) * (nflag + 1) <= cv.Sprev - cv.dS;
     int32_t* flags = reinterpret_cast<int32_t*>(ws + cv.dS + ring);
-    // Programmatic dependent launch of stages 2-4 (not across recorded events).
-    // Stage 1 is an ordinary launch, so everything queued before this call has
-    // completed before any stage reads its inputs.
+    // Programmatic dependent launch of stages 1-4 (not across recorded events).
+    // Stage 1 waits for the stream's previous kernel before anything else and
+    // only then lets stage 2 start, so everything queued before this call has
+    // completed before any stage reads its inputs; its launch overlaps the tail
+    // of that kernel.
     const bool pdl = !(shape->flags & MAMBA2_FLAG_SERIAL) && !events;
 
     auto mark = [&](int k) -> cudaError_t {
@@ -414,7 +416,7 @@ mamba2_status fwd_impl(const mamba2_ssd_shape* shape, const void* x, const float
     cudaError_t e = mark(0);
     if (e == cudaSuccess)
         e = fuse ? m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s, flags, (int64_t)nflag + 1)
-                 : m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s);
+                 : m2::launch_chunk_cumsum(d, dt, A, cum2, dtT, err, s, nullptr, 0, pdl);
     if (e == cudaSuccess) e = mark(1);
     if (fuse) {
         if (e == cudaSuccess)

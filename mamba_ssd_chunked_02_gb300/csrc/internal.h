@@ -94,7 +94,7 @@ inline int64_t esize(const Dims& d) { return d.dtype == 1 ? 2 : 4; }
 // flag words of the fused stage 2+3 kernel that follows on the same stream).
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, float* cum2,
                                 float* dtT, int32_t* err, cudaStream_t st,
-                                int32_t* zero = nullptr, int64_t nzero = 0);
+                                int32_t* zero = nullptr, int64_t nzero = 0, bool pdl = false);
 
 // Stage 2: chunk states.  CUDA-core variant (any supported shape / dtype).
 cudaError_t launch_chunk_state_simt(const Dims& d, const void* x, const void* B,

@@ -45,8 +45,12 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
     constexpr int kPitch = kRow + ((2 - kRow) & 7);   // 2 mod 8
     __shared__ float tile[kHB * kPitch];
     const int64_t c = blockIdx.x, b = blockIdx.y, h0 = (int64_t)blockIdx.z * kHB;
-    // Stage 2, when launched as this kernel's programmatic dependent, may start
-    // its loads of x and B now; it waits for this grid before reading cum2/dtT.
+    // Launched as a programmatic dependent (the whole-path call), this grid may
+    // start while the stream's previous kernel drains: nothing here runs before
+    // that kernel has completed.  Then stage 2 may start its loads of x and B (the
+    // call's inputs, complete by now); it waits for this grid before reading
+    // cum2/dtT.
+    grid_dep_wait();
     if (threadIdx.x == 0) grid_dep_launch();
     // Clear the next kernel's synchronisation words (grid-stride).
     if (zero) {
@@ -141,25 +145,21 @@ chunk_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A,
 
 cudaError_t launch_chunk_cumsum(const Dims& d, const float* dt, const float* A, float* cum2,
                                 float* dtT, int32_t* /*err*/, cudaStream_t st, int32_t* zero,
-                                int64_t nzero) {
+                                int64_t nzero, bool pdl) {
     if (d.b == 0 || d.H == 0 || d.T == 0) return cudaSuccess;
     const dim3 grid((unsigned)d.nc, (unsigned)d.b, (unsigned)((d.H + kHB - 1) / kHB));
     switch (d.L) {
         case 64:
-            chunk_cumsum_kernel<64><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
-                                                                d.sdt[1], zero, nzero);
-            break;
+            return launch_kernel(chunk_cumsum_kernel<64>, grid, dim3(kThreads), 0, st, pdl, dt, A, cum2, dtT,
+                                 (int64_t)d.T, (int64_t)d.H, (int64_t)d.sdt[0], (int64_t)d.sdt[1], zero, nzero);
         case 128:
-            chunk_cumsum_kernel<128><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
-                                                                d.sdt[1], zero, nzero);
-            break;
+            return launch_kernel(chunk_cumsum_kernel<128>, grid, dim3(kThreads), 0, st, pdl, dt, A, cum2, dtT,
+                                 (int64_t)d.T, (int64_t)d.H, (int64_t)d.sdt[0], (int64_t)d.sdt[1], zero, nzero);
         case 256:
-            chunk_cumsum_kernel<256><<<grid, kThreads, 0, st>>>(dt, A, cum2, dtT, d.T, d.H, d.sdt[0],
-                                                                d.sdt[1], zero, nzero);
-            break;
+            return launch_kernel(chunk_cumsum_kernel<256>, grid, dim3(kThreads), 0, st, pdl, dt, A, cum2, dtT,
+                                 (int64_t)d.T, (int64_t)d.H, (int64_t)d.sdt[0], (int64_t)d.sdt[1], zero, nzero);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace m2
