@@ -568,6 +568,18 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const int Lc = (int)min((int64_t)L, a.T - t0);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t PN = (int64_t)P * N;
+    // This thread's token (L <= kThreads: one token per thread): its dt and, when
+    // the y' run wrote them, its three dot pairs, loaded before the chunk dot below
+    // so that their latency overlaps it.
+    const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
+    const float pre_dt = tid < Lc ? dth[tid] : 0.f;
+    float2 pre_xy = make_float2(0.f, 0.f), pre_dyx = pre_xy, pre_yd = pre_xy;
+    if (a.xyd && tid < Lc) {
+        const int64_t po = (((int64_t)b * a.H + h) * a.T + t0) * 2;
+        pre_xy = reinterpret_cast<const float2*>(a.xyd + po)[tid];
+        pre_dyx = reinterpret_cast<const float2*>(a.dyxd + po)[tid];
+        pre_yd = reinterpret_cast<const float2*>(a.ydot2 + po)[tid];
+    }
     // <Gn_c, S_after_c>: S_after is the next chunk's Sprev, or the final state.
     float gs = 0.f;
     {
@@ -590,6 +602,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
                 if (c + 1 < a.nc) {
                     const uint4* s4 = reinterpret_cast<const uint4*>(
                         static_cast<const TI*>(a.Sprev) + (((int64_t)b * a.nc + c + 1) * a.H + h) * PN);
+#pragma unroll 4
                     for (int64_t k8 = tid; k8 < PN / 8; k8 += kThreads) {
                         const uint4 sv = s4[k8];
                         const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
@@ -623,8 +636,7 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
             }
         }
     }
-    const float* dth = a.dtT + ((int64_t)b * a.H + h) * a.T + t0;
-    for (int i = tid; i < 256; i += kThreads) s_dt[i] = i < Lc ? dth[i] : 0.f;
+    s_dt[tid] = pre_dt;   // kThreads = 256 slots
     __syncthreads();
     const float Dh = a.D ? a.D[h] : 0.f;
     const int64_t sxy = (int64_t)a.H * P;
@@ -635,17 +647,13 @@ __global__ void __launch_bounds__(kThreads) bwd_token(BwdArgs a) {
     const float* __restrict__ yd = a.ydot2 ? a.ydot2 + (((int64_t)b * a.H + h) * a.T + t0) * 2 : nullptr;
     float yx = 0.f;
     if (a.xyd) {
-        // The y' run wrote dx and the per-token dots x . y' and dy . x.
-        const int64_t po = (((int64_t)b * a.H + h) * a.T + t0) * 2;
-        const float2* xy2 = reinterpret_cast<const float2*>(a.xyd + po);
-        const float2* dx2 = reinterpret_cast<const float2*>(a.dyxd + po);
-        const float2* yd2 = reinterpret_cast<const float2*>(yd);
-        for (int j = tid; j < Lc; j += kThreads) {
-            const float2 v = xy2[j], w = dx2[j], u = yd2[j];
-            const float xy = v.x + v.y;
-            s_ddt[j] = xy;
-            s_dcum[j] = (u.x + u.y) - s_dt[j] * xy;
-            yx += w.x + w.y;
+        // The y' run wrote dx and the per-token dots x . y' and dy . x (this
+        // thread's token's, loaded above).
+        if (tid < Lc) {
+            const float xy = pre_xy.x + pre_xy.y;
+            s_ddt[tid] = xy;
+            s_dcum[tid] = (pre_yd.x + pre_yd.y) - pre_dt * xy;
+            yx += pre_dyx.x + pre_dyx.y;
         }
     } else {
     const float* __restrict__ yr = a.yr + base;
