@@ -304,12 +304,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (*abort)
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
-        } else if (lane == 1 && kY32 && (dxa.dx || dyv)) {
-            // dx / dot mode: the staged tiles, from a thread of their own so that the
-            // ring's loads never wait for a slot.  dx mode: the head's x and dy rows of
-            // this tile's tokens (the run's rows reversed: tokens Lc - 128 (qt + 1) ..
-            // Lc - 128 qt - 1 of the chunk; a start before token 0 reads zeros) into
-            // slot hi & 1.  Dot mode: the head's dy rows of the tile (tokens in order).
+        } else if (lane == 1 && kY32 && dxa.dx) {
+            // dx mode: the staged tiles, from a thread of their own so that the ring's
+            // loads never wait for a slot: the head's x and dy rows of this tile's
+            // tokens (the run's rows reversed: tokens Lc - 128 (qt + 1) .. Lc - 128 qt - 1
+            // of the chunk; a start before token 0 reads zeros) into slot hi & 1.  (Dot
+            // mode's dy rows are copied by the epilogue threads themselves.)
             prefetch_tmap(&tm_dxx);
             prefetch_tmap(&tm_ddy);
             int dissued = 0;
@@ -317,15 +317,10 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 const int sl = hi & 1, h = h0 + hi;
                 if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
                 uint8_t* ds = sY + sl * kSlot;
-                if (dxa.dx) {
-                    const int row = anti ? c * L + 128 * qt : c * L + Lc - 128 * (qt + 1);
-                    mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
-                    tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
-                    tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
-                } else {
-                    mbar_arrive_expect_tx(&bars.dfull[sl], 16384);
-                    tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, c * L + 128 * qt, b);
-                }
+                const int row = anti ? c * L + 128 * qt : c * L + Lc - 128 * (qt + 1);
+                mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
+                tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
+                tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
                 dissued = hi + 1;
             }
             if (*abort)   // the staged tiles of the last two heads issued
@@ -592,12 +587,12 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 // partial per (b, h, t, column group); y itself is not written.
                 const int64_t t = (int64_t)c * L + 128 * qt + 32 * q + lane;
                 const int hh = h0 + hp;
-                // dy of this row from the slot the producer staged (row tl, 128-byte
-                // swizzled: 16-byte chunk cc of row r at cc ^ (r & 7)).
+                // dy of this row: this thread's own copies into slot hp & 1 (row tl,
+                // 128-byte swizzled: 16-byte chunk cc of row r at cc ^ (r & 7)), issued
+                // as head hp's iteration began; those of head hp + 1 may still be in flight.
+                if (hp + 1 < nh) cp_async_wait<1>();
+                else cp_async_wait<0>();
                 const int sl = hp & 1;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
-                    return false;
                 const int sr = 32 * q + lane;
                 const uint8_t* dsr = sY + sl * kSlot + kSlotDy + sr * 128;
                 uint4 dw4[PC / 8];
@@ -621,9 +616,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                     }
                     ydot2[(((int64_t)b * H + hh) * T + t) * 2 + grp] = part;
                 }
-                fence_proxy_async_smem();   // the slot's reads before the next TMA load into it
-                mbar_arrive(&bars.dfree[sl]);
-                return true;
+                return true;   // the slot is next written by this thread's own copies
             }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
             // Reversed rows (yrev, with yred): the run's row k of the chunk is token
@@ -686,6 +679,22 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         };
         for (int hi = 0; hi < nh && ok; ++hi) {
             const int it = NA + hi, st = it % NS;
+            if (kY32 && dyv) {
+                // Dot mode: this row's dy (this thread's 32 columns of the head, 64
+                // bytes) into slot hi & 1, one group per head.  finish(hi), about a
+                // head later, reads it; the slot's last reader was this thread's
+                // finish(hi - 2), in the previous iteration.
+                const int64_t t = (int64_t)c * L + 128 * qt + tl;
+                if (t < T) {
+                    const __nv_bfloat16* src =
+                        dyv + ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)(h0 + hi) * C::P + grp * PC;
+                    uint8_t* dst = sY + (hi & 1) * kSlot + kSlotDy + tl * 128;
+#pragma unroll
+                    for (int k4 = 0; k4 < PC / 8; ++k4)
+                        cp_async16(smem_u32(dst + (((grp * PC / 8 + k4) ^ (tl & 7)) << 4)), src + 8 * k4);
+                }
+                cp_async_commit();
+            }
             // ---- x tile, decay vectors and range decision come from the converters
             // (phase of xready[st]: one per head item of that stage).
             ok = __all_sync(0xffffffffu,
@@ -868,6 +877,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             e_prev = e_t;
         }
         if (ok && nh > 0) ok = finish(nh - 1);
+        if (kY32 && dyv) cp_async_wait<0>();   // none of this thread's copies outlive it
         if (lane == 0) bulk_wait<0>();
     }
     else {
