@@ -511,6 +511,54 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // is in G, through M's diagonal), bf16, TMA-stored per warp.
         auto finish = [&](int hp) -> bool {
             const int pb = hp & 1;
+            if constexpr (kDot) {
+                // Dot mode (the backward's y run): sum_p dy[t, h, p] y[t, p] over this
+                // warp's 32 columns, one fp32 partial per (b, h, t, column group); y
+                // itself is not written.  dy of this row first: this thread's own
+                // copies into slot hp & 1 (row tl, 128-byte swizzled: 16-byte chunk cc
+                // of row r at cc ^ (r & 7)), issued as head hp's iteration began (those
+                // of head hp + 1 may still be in flight).  Then S and G in two 16-column
+                // halves, each used before the next is loaded, so that fewer
+                // accumulator words are live at once.
+                if (hp + 1 < nh) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                const uint8_t* dsr = sY + (hp & 1) * kSlot + kSlotDy + tl * 128;
+                uint4 dw4[PC / 8];
+#pragma unroll
+                for (int k4 = 0; k4 < PC / 8; ++k4)
+                    dw4[k4] = *reinterpret_cast<const uint4*>(dsr + (((grp * PC / 8 + k4) ^ (tl & 7)) << 4));
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
+                    return false;
+                tc_fence_after();
+                float part = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t g16[16], s16[16];
+                    tmem_ld16(tmem + lane_off + COL_S + 64 * pb + grp * PC + 16 * hf, s16);
+                    tmem_ld16(tmem + lane_off + COL_G + 64 * pb + grp * PC + 16 * hf, g16);
+                    tmem_wait_ld_regs(s16);
+                    tmem_wait_ld_regs(g16);
+#pragma unroll
+                    for (int k4 = 0; k4 < 2; ++k4) {
+                        const uint4 w = dw4[2 * hf + k4];
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int e = 8 * k4 + 2 * e2;
+                            part = fmaf(__uint_as_float(wv[e2] << 16),
+                                        fmaf(e_prev, __uint_as_float(s16[e]), __uint_as_float(g16[e])), part);
+                            part = fmaf(__uint_as_float(wv[e2] & 0xffff0000u),
+                                        fmaf(e_prev, __uint_as_float(s16[e + 1]), __uint_as_float(g16[e + 1])), part);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty[pb]);
+                const int64_t t = (int64_t)c * L + 128 * qt + tl;
+                if (t < T) ydot2[(((int64_t)b * H + h0 + hp) * T + t) * 2 + grp] = part;
+                return true;   // the slot is next written by this thread's own copies
+            }
             if (!__all_sync(0xffffffffu,
                             mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
                 return false;
@@ -582,42 +630,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 prefetch_dt(hp + 1);
                 return true;
             }
-            if (kY32 && dyv) {
-                // Dot mode: sum_p dy[t, h, p] y[t, p] over this warp's 32 columns, one fp32
-                // partial per (b, h, t, column group); y itself is not written.
-                const int64_t t = (int64_t)c * L + 128 * qt + 32 * q + lane;
-                const int hh = h0 + hp;
-                // dy of this row: this thread's own copies into slot hp & 1 (row tl,
-                // 128-byte swizzled: 16-byte chunk cc of row r at cc ^ (r & 7)), issued
-                // as head hp's iteration began; those of head hp + 1 may still be in flight.
-                if (hp + 1 < nh) cp_async_wait<1>();
-                else cp_async_wait<0>();
-                const int sl = hp & 1;
-                const int sr = 32 * q + lane;
-                const uint8_t* dsr = sY + sl * kSlot + kSlotDy + sr * 128;
-                uint4 dw4[PC / 8];
-#pragma unroll
-                for (int k4 = 0; k4 < PC / 8; ++k4)
-                    dw4[k4] = *reinterpret_cast<const uint4*>(dsr + (((grp * PC / 8 + k4) ^ (sr & 7)) << 4));
-                if (t < T) {
-                    float part = 0.f;
-#pragma unroll
-                    for (int k4 = 0; k4 < PC / 8; ++k4) {
-                        const uint4 w = dw4[k4];
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int e = 8 * k4 + 2 * e2;
-                            part = fmaf(__uint_as_float(wv[e2] << 16),
-                                        fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e])), part);
-                            part = fmaf(__uint_as_float(wv[e2] & 0xffff0000u),
-                                        fmaf(e_prev, __uint_as_float(rs[e + 1]), __uint_as_float(r[e + 1])), part);
-                        }
-                    }
-                    ydot2[(((int64_t)b * H + hh) * T + t) * 2 + grp] = part;
-                }
-                return true;   // the slot is next written by this thread's own copies
-            }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
             // Reversed rows (yrev, with yred): the run's row k of the chunk is token
             // Lc - 1 - k, so this warp's 32 rows are 32 consecutive tokens in reverse
@@ -679,7 +691,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         };
         for (int hi = 0; hi < nh && ok; ++hi) {
             const int it = NA + hi, st = it % NS;
-            if (kY32 && dyv) {
+            if constexpr (kDot) {
                 // Dot mode: this row's dy (this thread's 32 columns of the head, 64
                 // bytes) into slot hi & 1, one group per head.  finish(hi), about a
                 // head later, reads it; the slot's last reader was this thread's
@@ -877,7 +889,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             e_prev = e_t;
         }
         if (ok && nh > 0) ok = finish(nh - 1);
-        if (kY32 && dyv) cp_async_wait<0>();   // none of this thread's copies outlive it
+        if constexpr (kDot) cp_async_wait<0>();   // none of this thread's copies outlive it
         if (lane == 0) bulk_wait<0>();
     }
     else {
