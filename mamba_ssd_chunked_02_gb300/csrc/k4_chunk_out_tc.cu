@@ -559,6 +559,79 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 if (t < T) ydot2[(((int64_t)b * H + h0 + hp) * T + t) * 2 + grp] = part;
                 return true;   // the slot is next written by this thread's own copies
             }
+            if constexpr (anti) {
+                // dx mode (the backward's y' run, rows in token order): write
+                // dx = dt y' + D dy for this row's token and the partial dots x . y' and
+                // dy . x over this warp's 32 columns, from the x and dy tiles the
+                // producer staged in slot hp & 1 (row tl, 128-byte swizzled: 16-byte
+                // chunk cc of row r at cc ^ (r & 7)).  S and G in two 16-column halves,
+                // each used before the next is loaded, so that fewer accumulator words
+                // are live at once.
+                const int sl = hp & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
+                    return false;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
+                    return false;
+                tc_fence_after();
+                const uint8_t* xs = sY + sl * kSlot + tl * 128;
+                const int k = 128 * qt + tl;
+                const bool live = k < Lc;
+                const int hh = h0 + hp;
+                const int64_t t = (int64_t)c * L + k;
+                float4* op = reinterpret_cast<float4*>(
+                    dxa.dx + ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC);
+                const float dtj = pf_dt, dh = pf_D;
+                float xy = 0.f, dyx = 0.f;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t g16[16], s16[16];
+                    tmem_ld16(tmem + lane_off + COL_S + 64 * pb + grp * PC + 16 * hf, s16);
+                    tmem_ld16(tmem + lane_off + COL_G + 64 * pb + grp * PC + 16 * hf, g16);
+                    tmem_wait_ld_regs(s16);
+                    tmem_wait_ld_regs(g16);
+#pragma unroll
+                    for (int k4 = 0; k4 < 2; ++k4) {
+                        const int kc = 2 * hf + k4;   // 16-byte chunk of the row's 32 columns
+                        const int cc = (grp * PC / 8 + kc) ^ (tl & 7);
+                        const uint4 xw = *reinterpret_cast<const uint4*>(xs + (cc << 4));
+                        const uint4 dw = *reinterpret_cast<const uint4*>(xs + kSlotDy + (cc << 4));
+                        const uint32_t xv[4] = {xw.x, xw.y, xw.z, xw.w};
+                        const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
+                        float o[8];
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            const int e = 8 * k4 + 2 * e2;
+                            const float y0 = fmaf(e_prev, __uint_as_float(s16[e]), __uint_as_float(g16[e]));
+                            const float y1 = fmaf(e_prev, __uint_as_float(s16[e + 1]), __uint_as_float(g16[e + 1]));
+                            const float x0 = __uint_as_float(xv[e2] << 16), x1 = __uint_as_float(xv[e2] & 0xffff0000u);
+                            const float d0 = __uint_as_float(dv[e2] << 16), d1 = __uint_as_float(dv[e2] & 0xffff0000u);
+                            o[2 * e2] = fmaf(dtj, y0, dh * d0);
+                            o[2 * e2 + 1] = fmaf(dtj, y1, dh * d1);
+                            xy = fmaf(x0, y0, fmaf(x1, y1, xy));
+                            dyx = fmaf(d0, x0, fmaf(d1, x1, dyx));
+                        }
+                        if (live) {
+                            op[2 * kc] = make_float4(o[0], o[1], o[2], o[3]);
+                            op[2 * kc + 1] = make_float4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.acc_empty[pb]);
+                // Release the slot to the next head's TMA loads: this thread's reads
+                // (generic proxy) are ordered before those writes (async proxy).
+                fence_proxy_async_smem();
+                mbar_arrive(&bars.dfree[sl]);
+                if (live) {
+                    const int64_t po = (((int64_t)b * H + hh) * T + t) * 2 + grp;
+                    dxa.xy[po] = xy;
+                    dxa.dyx[po] = dyx;
+                }
+                prefetch_dt(hp + 1);
+                return true;
+            }
             if (!__all_sync(0xffffffffu,
                             mbar_wait_or_abort(&bars.acc_full[pb], (hp >> 1) & 1, abort, kWaitNs)))
                 return false;
@@ -570,66 +643,6 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             tmem_wait_ld_regs(r);
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[pb]);
-            if (kY32 && dxa.dx) {
-                // dx mode (the backward's y' run): row k of the chunk is token
-                // j = Lc - 1 - k; write dx = dt y' + D dy there and the partial dots
-                // x . y' and dy . x over this warp's 32 columns.
-                const int k = 128 * qt + 32 * q + lane;
-                const int sl = hp & 1;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_or_abort(&bars.dfull[sl], (hp >> 1) & 1, abort, kWaitNs)))
-                    return false;
-                // This row's token sits at row 127 - tl of the staged tiles (tl in
-                // anti mode, whose rows are in token order; 128-byte swizzled rows:
-                // 16-byte chunk cc of row r at cc ^ (r & 7)).
-                const int sr = anti ? 32 * q + lane : 127 - (32 * q + lane);
-                const uint8_t* xs = sY + sl * kSlot + sr * 128;
-                uint4 xw4[PC / 8], dw4[PC / 8];
-#pragma unroll
-                for (int k4 = 0; k4 < PC / 8; ++k4) {
-                    const int cc = (grp * PC / 8 + k4) ^ (sr & 7);
-                    xw4[k4] = *reinterpret_cast<const uint4*>(xs + (cc << 4));
-                    dw4[k4] = *reinterpret_cast<const uint4*>(xs + 16384 + (cc << 4));
-                }
-                if (k < Lc) {
-                    const int hh = h0 + hp;
-                    const int64_t t = (int64_t)c * L + (anti ? k : Lc - 1 - k);
-                    const int64_t ro = ((int64_t)b * T + t) * ((int64_t)H * C::P) + (int64_t)hh * C::P + grp * PC;
-                    const float dtj = pf_dt, dh = pf_D;
-                    float4* op = reinterpret_cast<float4*>(dxa.dx + ro);
-                    float xy = 0.f, dyx = 0.f;
-#pragma unroll
-                    for (int k4 = 0; k4 < PC / 8; ++k4) {
-                        const uint4 xw = xw4[k4], dw = dw4[k4];
-                        const uint32_t xv[4] = {xw.x, xw.y, xw.z, xw.w};
-                        const uint32_t dv[4] = {dw.x, dw.y, dw.z, dw.w};
-                        float o[8];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int e = 8 * k4 + 2 * e2;
-                            const float y0 = fmaf(e_prev, __uint_as_float(rs[e]), __uint_as_float(r[e]));
-                            const float y1 = fmaf(e_prev, __uint_as_float(rs[e + 1]), __uint_as_float(r[e + 1]));
-                            const float x0 = __uint_as_float(xv[e2] << 16), x1 = __uint_as_float(xv[e2] & 0xffff0000u);
-                            const float d0 = __uint_as_float(dv[e2] << 16), d1 = __uint_as_float(dv[e2] & 0xffff0000u);
-                            o[2 * e2] = fmaf(dtj, y0, dh * d0);
-                            o[2 * e2 + 1] = fmaf(dtj, y1, dh * d1);
-                            xy = fmaf(x0, y0, fmaf(x1, y1, xy));
-                            dyx = fmaf(d0, x0, fmaf(d1, x1, dyx));
-                        }
-                        op[2 * k4] = make_float4(o[0], o[1], o[2], o[3]);
-                        op[2 * k4 + 1] = make_float4(o[4], o[5], o[6], o[7]);
-                    }
-                    const int64_t po = (((int64_t)b * H + hh) * T + t) * 2 + grp;
-                    dxa.xy[po] = xy;
-                    dxa.dyx[po] = dyx;
-                }
-                // Release the slot to the next head's TMA loads: this thread's reads
-                // (generic proxy) are ordered before those writes (async proxy).
-                fence_proxy_async_smem();
-                mbar_arrive(&bars.dfree[sl]);
-                prefetch_dt(hp + 1);
-                return true;
-            }
             uint8_t* yw = sY + (hp % YB) * C::Y_BYTES + ew * C::YW_BYTES;
             // Reversed rows (yrev, with yred): the run's row k of the chunk is token
             // Lc - 1 - k, so this warp's 32 rows are 32 consecutive tokens in reverse
@@ -1128,7 +1141,8 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
     if (d.dxm_dx || d.ydot_dy) {   // dx / dot mode: x and dy tiles staged in the two y buffers
-        if (!kY32 || (d.ydot_dy && !kDot) || C::YB * C::Y_BYTES < 2 * (kDot ? 16384 : 32768))
+        if (!kY32 || (d.ydot_dy && !kDot) || (d.dxm_dx && !kAnti) ||
+            C::YB * C::Y_BYTES < 2 * (kDot ? 16384 : 32768))
             return cudaErrorNotSupported;
         const uint64_t dd[3] = {(uint64_t)(d.H * 64), (uint64_t)d.T, (uint64_t)d.b};
         const uint64_t ds[2] = {(uint64_t)(d.H * 64 * 2), (uint64_t)(d.T * d.H * 64 * 2)};
