@@ -175,7 +175,8 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
     using C = K4Cfg<L, NA, kY32, kDot>;
     constexpr int NS = C::NS, YB = C::YB, NQ = L / 128, N = NA * 64;
     // Staging slots of dx / dot mode in the y buffers: x at +0 and dy at +16384 of
-    // a 32 KB slot (dx), or dy alone in a 16 KB slot (dot).
+    // a 32 KB slot (dx mode, TMA tiles from the producer), or dy alone in a 16 KB
+    // slot (dot mode, each epilogue thread's own copies of its row).
     constexpr int kSlot = kDot ? 16384 : 32768, kSlotDy = kDot ? 0 : 16384;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -304,12 +305,11 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
             if (*abort)
                 for (int it = issued - 1; it >= 0 && it >= issued - NS; --it)
                     mbar_wait(&bars.full[it % NS], (it / NS) & 1, kWaitNs);
-        } else if (lane == 1 && kY32 && dxa.dx) {
-            // dx mode: the staged tiles, from a thread of their own so that the ring's
-            // loads never wait for a slot: the head's x and dy rows of this tile's
-            // tokens (the run's rows reversed: tokens Lc - 128 (qt + 1) .. Lc - 128 qt - 1
-            // of the chunk; a start before token 0 reads zeros) into slot hi & 1.  (Dot
-            // mode's dy rows are copied by the epilogue threads themselves.)
+        } else if (lane == 1 && anti) {
+            // dx mode (the anti-causal variant's only use): the staged tiles, from a
+            // thread of their own so that the ring's loads never wait for a slot: the
+            // head's x and dy rows of this tile's tokens (rows in token order) into
+            // slot hi & 1.
             prefetch_tmap(&tm_dxx);
             prefetch_tmap(&tm_ddy);
             int dissued = 0;
@@ -317,7 +317,7 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
                 const int sl = hi & 1, h = h0 + hi;
                 if (!mbar_wait_or_abort(&bars.dfree[sl], ((hi >> 1) & 1) ^ 1, abort, kWaitNs)) break;
                 uint8_t* ds = sY + sl * kSlot;
-                const int row = anti ? c * L + 128 * qt : c * L + Lc - 128 * (qt + 1);
+                const int row = c * L + 128 * qt;
                 mbar_arrive_expect_tx(&bars.dfull[sl], 32768);
                 tma_load_3d(ds, &tm_dxx, &bars.dfull[sl], h * C::P, row, b);
                 tma_load_3d(ds + kSlotDy, &tm_ddy, &bars.dfull[sl], h * C::P, row, b);
@@ -500,10 +500,9 @@ chunk_out_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_const
         // next, loaded one head ahead so that finish() does not wait for them.
         float pf_dt = 0.f, pf_D = 0.f;
         auto prefetch_dt = [&](int hp) {
-            if (!(kY32 && dxa.dx) || hp >= nh) return;
-            const int k = 128 * qt + 32 * q + lane;
-            if (k < Lc)
-                pf_dt = __ldg(dxa.dt + ((int64_t)b * H + h0 + hp) * T + (int64_t)c * L + (anti ? k : Lc - 1 - k));
+            if (!anti || hp >= nh) return;
+            const int k = 128 * qt + tl;
+            if (k < Lc) pf_dt = __ldg(dxa.dt + ((int64_t)b * H + h0 + hp) * T + (int64_t)c * L + k);
             pf_D = dxa.D ? __ldg(dxa.D + h0 + hp) : 0.f;
         };
         prefetch_dt(0);
@@ -1140,15 +1139,17 @@ cudaError_t launch_k4(const Dims& d, const void* x, const void* B, const void* C
                            CU_TENSOR_MAP_SWIZZLE_128B)
                : make_tmap_bf16(&tm_y, y, 3, xd, ys, ybox, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
-    if (d.dxm_dx || d.ydot_dy) {   // dx / dot mode: x and dy tiles staged in the two y buffers
-        if (!kY32 || (d.ydot_dy && !kDot) || (d.dxm_dx && !kAnti) ||
-            C::YB * C::Y_BYTES < 2 * (kDot ? 16384 : 32768))
-            return cudaErrorNotSupported;
+    // dx / dot mode: x and dy rows (contiguous [b, T, H, 64] bf16) staged in the two
+    // y buffers; dx mode is the anti-causal variant's, dot mode the dot variant's.
+    if ((d.dxm_dx || d.ydot_dy) &&
+        (!kY32 || (d.ydot_dy && !kDot) || (d.dxm_dx && !kAnti) ||
+         C::YB * C::Y_BYTES < 2 * (kDot ? 16384 : 32768)))
+        return cudaErrorNotSupported;
+    if ((kAnti && !d.dxm_dx) || (kDot && !d.ydot_dy)) return cudaErrorNotSupported;
+    if (d.dxm_dx) {   // dx mode: the producer's TMA tiles (dot mode's rows are per-thread copies)
         const uint64_t dd[3] = {(uint64_t)(d.H * 64), (uint64_t)d.T, (uint64_t)d.b};
         const uint64_t ds[2] = {(uint64_t)(d.H * 64 * 2), (uint64_t)(d.T * d.H * 64 * 2)};
-        const void* xs = d.dxm_dx ? d.dxm_x : d.ydot_dy;   // dot mode: x unused
-        const void* dys = d.dxm_dx ? d.dxm_dy : d.ydot_dy;
-        if (!make_tmap_bf16(&tm_dxx, xs, 3, dd, ds, box) || !make_tmap_bf16(&tm_ddy, dys, 3, dd, ds, box))
+        if (!make_tmap_bf16(&tm_dxx, d.dxm_x, 3, dd, ds, box) || !make_tmap_bf16(&tm_ddy, d.dxm_dy, 3, dd, ds, box))
             return cudaErrorInvalidValue;
     } else {
         tm_dxx = tm_x;   // unused
